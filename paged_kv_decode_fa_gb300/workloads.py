@@ -1,0 +1,195 @@
+"""Seeded synthetic decode batches.
+
+This module only draws inputs - context lengths, page tables and values - and
+holds none of the attention arithmetic, so both the CUDA path and the
+float64 oracle can be fed from it.
+
+The five named configurations are the decode workloads this library is
+measured on:
+
+``tiny``         B=4, 8 qo / 8 kv heads, head_dim 64, fp32, lengths
+                 {17, 64, 100, 255}; the 29 pages are drawn without replacement
+                 from a 64-page pool in seeded random order.
+``gqa_uniform``  B=64, 32 qo / 8 kv heads (group 4), head_dim 128, bf16,
+                 every length 2048; page ids a seeded permutation of the pool.
+``ragged``       B=450, 32/8 heads, head_dim 128, bf16, lengths log-uniform in
+                 [256, 64000] - the heterogeneous mix (256 to 64,000 tokens)
+                 of the incident on the page "FlashInfer vs FlashAttention-3".
+``long_split``   B=1, 32/32 heads (MHA), head_dim 128, bf16, length 65536: one
+                 sequence that has to be split across the whole GPU.
+``fp8_kv``       B=128, 64/8 heads (group 8), head_dim 128, bf16 q, K and V
+                 stored as FP8 E4M3 with one fp32 scale each (amax / 448),
+                 lengths uniform in [1024, 8192].
+
+All use page_size 16 and the combined [num_pages, 2, 16, Hkv, D] layout.
+Lengths and page tables come from a CPU ``torch.Generator``; values from a
+generator on the target device, both seeded with the config's seed
+(1000 + its position).  last_page_len = len - 16 * (pages - 1), i.e.
+len mod 16, or 16 when that is 0.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+PAGE_SIZE = 16
+E4M3_MAX = 448.0
+
+
+@dataclass(frozen=True)
+class DecodeConfig:
+    name: str
+    batch: int
+    num_qo_heads: int
+    num_kv_heads: int
+    head_dim: int
+    q_dtype: torch.dtype
+    kv_dtype: torch.dtype
+    seed: int
+    page_size: int = PAGE_SIZE
+
+    @property
+    def group(self) -> int:
+        return self.num_qo_heads // self.num_kv_heads
+
+
+CONFIGS: dict[str, DecodeConfig] = {
+    "tiny": DecodeConfig("tiny", 4, 8, 8, 64, torch.float32, torch.float32, 1001),
+    "gqa_uniform": DecodeConfig("gqa_uniform", 64, 32, 8, 128, torch.bfloat16, torch.bfloat16, 1002),
+    "ragged": DecodeConfig("ragged", 450, 32, 8, 128, torch.bfloat16, torch.bfloat16, 1003),
+    "long_split": DecodeConfig("long_split", 1, 32, 32, 128, torch.bfloat16, torch.bfloat16, 1004),
+    "fp8_kv": DecodeConfig("fp8_kv", 128, 64, 8, 128, torch.bfloat16, torch.float8_e4m3fn, 1005),
+}
+
+
+def draw_lengths(cfg: DecodeConfig, gen: torch.Generator) -> np.ndarray:
+    """Context length of every request of a named configuration."""
+    if cfg.name == "tiny":
+        return np.array([17, 64, 100, 255], dtype=np.int64)
+    if cfg.name == "gqa_uniform":
+        return np.full(cfg.batch, 2048, dtype=np.int64)
+    if cfg.name == "ragged":
+        u = torch.rand(cfg.batch, generator=gen, dtype=torch.float64).numpy()
+        lo, hi = math.log(256.0), math.log(64000.0)
+        return np.rint(np.exp(lo + u * (hi - lo))).astype(np.int64)
+    if cfg.name == "long_split":
+        return np.full(cfg.batch, 65536, dtype=np.int64)
+    if cfg.name == "fp8_kv":
+        return torch.randint(1024, 8193, (cfg.batch,), generator=gen).numpy().astype(np.int64)
+    raise KeyError(cfg.name)
+
+
+@dataclass
+class DecodeBatch:
+    """One decode batch: device tensors plus host copies of the page table."""
+    q: torch.Tensor                 # [B, Hq, D]
+    paged_kv: torch.Tensor          # [num_pages, 2, P, Hkv, D]
+    indptr: torch.Tensor            # [B+1] int32, host
+    indices: torch.Tensor           # [nnz] int32, on the device of paged_kv
+    last_page_len: torch.Tensor     # [B] int32, host
+    lengths: np.ndarray             # [B] int64
+    num_qo_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+    name: str = "custom"
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def batch(self) -> int:
+        return int(self.indptr.shape[0] - 1)
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.paged_kv.shape[0])
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.lengths.sum())
+
+
+def page_table(lengths, page_size: int, pool_pages: int | None, gen: torch.Generator,
+               shuffle: bool = True):
+    """indptr, indices, last_page_len for the given lengths.
+
+    Page ids are the first sum(pages) entries of a seeded permutation of
+    range(pool_pages) (or range(sum(pages)) when pool_pages is None), in the
+    permutation's order; shuffle=False hands them out in order instead.
+    """
+    lengths = np.asarray(lengths, dtype=np.int64)
+    pages = (lengths + page_size - 1) // page_size
+    last = np.where(pages > 0, lengths - (pages - 1) * page_size, 0)
+    # requests with no pages: last_page_len is ignored, keep it valid
+    last = np.where(pages > 0, last, page_size)
+    indptr = np.zeros(len(lengths) + 1, dtype=np.int64)
+    indptr[1:] = np.cumsum(pages)
+    nnz = int(indptr[-1])
+    pool = nnz if pool_pages is None else int(pool_pages)
+    if pool < nnz:
+        raise ValueError("page pool smaller than the pages requested")
+    if shuffle:
+        ids = torch.randperm(pool, generator=gen)[:nnz].numpy()
+    else:
+        ids = np.arange(nnz)
+    return (torch.from_numpy(indptr.astype(np.int32)), torch.from_numpy(ids.astype(np.int32)),
+            torch.from_numpy(last.astype(np.int32)), pool)
+
+
+def _fp8_quantise(x: torch.Tensor) -> tuple[torch.Tensor, float]:
+    """Per-tensor E4M3 quantisation of the input recipe: scale = amax / 448,
+    codes = round-to-nearest-even cast of x / scale."""
+    amax = float(x.abs().max())
+    scale = amax / E4M3_MAX if amax > 0 else 1.0
+    return (x / scale).to(torch.float8_e4m3fn), scale
+
+
+def make_batch(*, batch_lengths, num_qo_heads: int, num_kv_heads: int, head_dim: int,
+               q_dtype: torch.dtype, kv_dtype: torch.dtype, seed: int, device="cuda",
+               page_size: int = PAGE_SIZE, pool_pages: int | None = None, shuffle: bool = True,
+               name: str = "custom") -> DecodeBatch:
+    """A seeded batch with explicit lengths (any shape the library supports)."""
+    gen = torch.Generator().manual_seed(seed)
+    return _fill(batch_lengths, gen, num_qo_heads, num_kv_heads, head_dim, q_dtype, kv_dtype,
+                 seed, device, page_size, pool_pages, shuffle, name)
+
+
+def make_config_batch(name: str, device="cuda") -> DecodeBatch:
+    """The named configuration, drawn from its seed."""
+    cfg = CONFIGS[name]
+    gen = torch.Generator().manual_seed(cfg.seed)
+    lengths = draw_lengths(cfg, gen)
+    pool = 64 if name == "tiny" else None
+    return _fill(lengths, gen, cfg.num_qo_heads, cfg.num_kv_heads, cfg.head_dim, cfg.q_dtype,
+                 cfg.kv_dtype, cfg.seed, device, cfg.page_size, pool, True, name)
+
+
+def _fill(lengths, gen, Hq, Hkv, D, q_dtype, kv_dtype, seed, device, P, pool_pages, shuffle,
+          name) -> DecodeBatch:
+    lengths = np.asarray(lengths, dtype=np.int64)
+    indptr, ids, last, pool = page_table(lengths, P, pool_pages, gen, shuffle)
+    B = len(lengths)
+    dev = torch.device(device)
+    vgen = torch.Generator(device=dev).manual_seed(seed)
+    q = torch.randn((B, Hq, D), generator=vgen, device=dev, dtype=torch.float32).to(q_dtype)
+    k_scale = v_scale = 1.0
+    if kv_dtype == torch.float8_e4m3fn:
+        kv = torch.empty((pool, 2, P, Hkv, D), dtype=kv_dtype, device=dev)
+        scales = []
+        for half in range(2):
+            x = torch.randn((pool, P, Hkv, D), generator=vgen, device=dev, dtype=torch.float32)
+            codes, s = _fp8_quantise(x)
+            kv[:, half] = codes
+            scales.append(s)
+            del x, codes
+        k_scale, v_scale = scales
+    else:
+        kv = torch.randn((pool, 2, P, Hkv, D), generator=vgen, device=dev, dtype=kv_dtype)
+    return DecodeBatch(q=q, paged_kv=kv, indptr=indptr, indices=ids.to(dev),
+                       last_page_len=last, lengths=lengths, num_qo_heads=Hq,
+                       num_kv_heads=Hkv, head_dim=D, page_size=P, k_scale=k_scale,
+                       v_scale=v_scale, name=name)

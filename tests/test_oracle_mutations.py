@@ -1,0 +1,48 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check
+that the pins of test_oracle.py catch every one.  This is what makes the
+pins worth trusting: each mistake below is the kind a careless restatement
+of the method would make."""
+import os
+
+import pytest
+
+import oracle
+from tests import test_oracle as T
+
+# (name, text in oracle.c, replacement, pins expected to fail on it)
+MUTATIONS = [
+    ("gqa head mapping", "const int kvh = h / g;", "const int kvh = h % Hkv;",
+     [T.pin_gqa_equals_repeated_mha, T.pin_torch_dense]),
+    ("dropped logit scale", "s[t] = sm_scale * acc;", "s[t] = acc;",
+     [T.pin_single_key, T.pin_torch_dense, T.pin_brute_force]),
+    ("lse without the max", "lse[u] = m + log(den);", "lse[u] = log(den);",
+     [T.pin_single_key, T.pin_identical_keys]),
+    ("K and V swapped", "kv_offset(page, 0, slot, kvh, d, P, Hkv, D));",
+     "kv_offset(page, 1, slot, kvh, d, P, Hkv, D));",
+     [T.pin_torch_dense, T.pin_brute_force, T.pin_golden_decode]),
+    ("last page read in full", "(int64_t)(np - 1) * P + last_page_len[i]", "(int64_t)np * P",
+     [T.pin_padding_never_read, T.pin_golden_decode]),
+    ("no max subtraction in the weights", "den += exp(s[t] - m);", "den += exp(s[t]);",
+     [T.pin_identical_keys, T.pin_brute_force]),
+    ("e4m3 exponent bias 8", "pow(2.0, e - 7)", "pow(2.0, e - 8)",
+     [T.pin_e4m3_all_codes, T.pin_e4m3_spec_points]),
+    ("e4m3 subnormal scale", "((double)m / 8.0) * pow(2.0, 1 - 7)", "((double)m / 8.0) * pow(2.0, -7)",
+     [T.pin_e4m3_all_codes, T.pin_e4m3_spec_points]),
+    ("k_scale ignored", "double kd = k_scale * load_elem", "double kd = load_elem",
+     [T.pin_torch_dense]),
+    ("merge weight of b uses a", "d_b * w_b;", "d_b * w_a;",
+     [T.pin_golden_merge, T.pin_merge_algebra, T.pin_split_merge]),
+    ("merge sign flipped", "exp(m_b - m_new);", "exp(m_new - m_b);",
+     [T.pin_golden_merge, T.pin_merge_algebra]),
+]
+
+
+@pytest.mark.parametrize("name,old,new,pins", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(tmp_path, name, old, new, pins):
+    src = oracle.source()
+    assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
+    so = oracle.compile_variant(src.replace(old, new), os.path.join(tmp_path, "mut.so"))
+    bad = oracle.Oracle(so)
+    for pin in pins:
+        with pytest.raises((AssertionError, ValueError)):
+            pin(bad)
