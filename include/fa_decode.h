@@ -1,0 +1,221 @@
+/*
+ * fa_decode.h - C ABI of libfadecode.so: batched decode attention over a
+ * paged KV cache for ragged batches, on one GB300 (sm_103a).
+ *
+ * The calls follow the plan/run statement of the problem on the page
+ * "FlashDecoding + FlashInfer - the decode-time attention story", section
+ * "The API you actually use (Python)": plan() is called once per batch shape
+ * and amortised, run() is the hot path.  The merge of partial softmax states
+ * is the rule of section "FlashDecoding - the split-KV trick" on that page.
+ *
+ * Conventions shared by every entry point
+ *  - Plain C types only.  Pointers are "host" or "device" as stated per
+ *    argument; device pointers must come from the CUDA device that is current
+ *    on the calling thread.  The caller owns every buffer, including the
+ *    workspace; the library owns only the opaque plan handle.
+ *  - A stream argument is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  All device work of a call is enqueued on it.
+ *  - Return value: FA_OK (0) or a negative fa_status.  On error nothing has
+ *    been launched and no output has been written.
+ *  - Supported shapes: page_size 16; head_dim 64 or 128;
+ *    num_qo_heads / num_kv_heads in {1, 2, 4, 8}; (q, kv) element types
+ *    (F32, F32), (BF16, BF16), (F16, F16), (BF16, E4M3), (F16, E4M3).
+ *    Anything else returns FA_ERR_UNSUPPORTED.
+ *  - Layouts (row-major, innermost last):
+ *      q          [batch, num_qo_heads, head_dim]                 q dtype
+ *      paged_kv   [num_pages, 2, page_size, num_kv_heads, head_dim] kv dtype
+ *                 (index 0 = K, 1 = V; "NHD": tokens, then heads, then dim)
+ *      o          [batch, num_qo_heads, head_dim]                 q dtype
+ *      lse        [batch, num_qo_heads]                           float32
+ *    Query head h reads kv head h / (num_qo_heads / num_kv_heads).
+ *    lse is the natural-log log-sum-exp of the scaled logits
+ *    sm_scale * q . k over the request's context.
+ */
+#ifndef FA_DECODE_H_
+#define FA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types.  E4M3 is the OCP FP8 E4M3 "FN" encoding (finite, max 448). */
+typedef enum {
+  FA_DTYPE_F32 = 0,
+  FA_DTYPE_BF16 = 1,
+  FA_DTYPE_F16 = 2,
+  FA_DTYPE_E4M3 = 3
+} fa_dtype;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = -1,         /* malformed arguments (shapes, indptr, NULL) */
+  FA_ERR_UNSUPPORTED = -2,         /* valid but not built (dtype, head_dim, group) */
+  FA_ERR_WORKSPACE_TOO_SMALL = -3, /* workspace_bytes below what the plan needs */
+  FA_ERR_CUDA = -4,                /* a CUDA runtime call failed */
+  FA_ERR_DEVICE_CHECK = -5         /* a kernel recorded a device-side check */
+} fa_status;
+
+/* Opaque plan handle, created by fa_decode_plan, freed by
+ * fa_decode_plan_destroy.  Not thread-safe: one thread uses a plan at a time. */
+typedef struct fa_decode_plan_s* fa_decode_plan_t;
+
+/* Human-readable name of a status code.  Static storage, never NULL. */
+const char* fa_status_string(int status);
+
+/* Upper bound, in bytes, of the device workspace that fa_decode_plan needs
+ * for a batch of `batch` requests with these head counts and head_dim on the
+ * current CUDA device (it depends on the device's SM count).  The bound is
+ * independent of the context lengths.  Returns 0 for invalid arguments. */
+size_t fa_decode_workspace_size(int batch, int num_qo_heads, int num_kv_heads,
+                                int head_dim);
+
+/* plan: build the work list of one decode batch (page "FlashDecoding +
+ * FlashInfer", sections "The API you actually use" and "What FlashInfer is",
+ * item 3: load-balance across CTAs so that the longest sequence does not stall
+ * the batch).
+ *
+ *  indptr_host         [batch+1] int32, host.  Request i owns page positions
+ *                      indptr[i] .. indptr[i+1]-1 of indices_dev.
+ *                      indptr[0] = 0, non-decreasing.
+ *  indices_dev         [indptr[batch]] int32, device.  Physical page ids.  Kept
+ *                      by pointer and read by every fa_decode_run of this plan:
+ *                      it must stay valid and unchanged while the plan is used.
+ *                      Ids may repeat across requests (shared prefixes).
+ *  last_page_len_host  [batch] int32, host.  Valid slots in each request's last
+ *                      page, in [1, page_size]; ignored for a request with no
+ *                      pages (its output is o = 0, lse = -inf).
+ *  workspace_dev,      device scratch owned by the caller, at least
+ *  workspace_bytes     fa_decode_workspace_size(...) bytes, 256-byte aligned.
+ *                      It holds the work list and the fp32 partial states; it
+ *                      must not be shared by two plans used concurrently.
+ *  cuda_stream         the work list is copied into the workspace on this stream.
+ *  out_plan            receives the new handle.
+ *
+ * Per request, len = (pages - 1) * page_size + last_page_len.  Every
+ * (request, kv head, page) is assigned to exactly one chunk of the work list;
+ * fa_decode_plan_get_work exposes that list for inspection.
+ * Errors: FA_ERR_INVALID_ARG for a malformed indptr or last_page_len, NULL
+ * pointers or non-positive sizes; FA_ERR_UNSUPPORTED for shapes or types that
+ * are not built; FA_ERR_WORKSPACE_TOO_SMALL; FA_ERR_CUDA. */
+int fa_decode_plan(const int32_t* indptr_host, const int32_t* indices_dev,
+                   const int32_t* last_page_len_host, int batch,
+                   int num_qo_heads, int num_kv_heads, int head_dim,
+                   int page_size, fa_dtype q_dtype, fa_dtype kv_dtype,
+                   void* workspace_dev, size_t workspace_bytes,
+                   void* cuda_stream, fa_decode_plan_t* out_plan);
+
+/* run: decode attention for one query token per request (page "FlashDecoding
+ * + FlashInfer", section "FlashDecoding - the split-KV trick": every chunk of
+ * the KV axis yields a partial (m, d, o), and a small reduction combines the
+ * partials with the merge rule).
+ *
+ *  q          [batch, num_qo_heads, head_dim], plan's q dtype, device.
+ *  paged_kv   [num_pages, 2, page_size, num_kv_heads, head_dim], plan's kv
+ *             dtype, device, 16-byte aligned.
+ *  num_pages  leading extent of paged_kv.  A page id outside [0, num_pages)
+ *             reads zeros and sets the device-check word (see
+ *             fa_decode_check); it never reads outside paged_kv.
+ *  sm_scale   logit scale; <= 0 selects 1/sqrt(head_dim).
+ *  k_scale,   per-tensor dequantisation scales of an E4M3 cache (stored code
+ *  v_scale    times scale = value); use 1 for other kv types.
+ *  o          [batch, num_qo_heads, head_dim], q dtype, device, caller-allocated.
+ *  lse        [batch, num_qo_heads] float32, device, or NULL to skip it.
+ *
+ * No allocation and no host synchronisation: the call only enqueues kernels
+ * on cuda_stream, so it can be issued repeatedly between plans.  Results are
+ * bitwise reproducible for a fixed plan.
+ * Errors: FA_ERR_INVALID_ARG (NULL plan/q/paged_kv/o, num_pages <= 0,
+ * misaligned paged_kv), FA_ERR_CUDA (encoding the TMA descriptor or a launch
+ * failed). */
+int fa_decode_run(fa_decode_plan_t plan, const void* q, const void* paged_kv,
+                  int64_t num_pages, float sm_scale, float k_scale,
+                  float v_scale, void* o, float* lse, void* cuda_stream);
+
+/* merge_states: combine two sets of partial attention states with the merge
+ * rule (page "FlashDecoding + FlashInfer", section "FlashDecoding - the
+ * split-KV trick").  A state is a normalised output o_x with its natural-log
+ * lse_x, i.e. (m = lse_x, d = 1, o = o_x) in the rule's notation; the result is
+ * normalised again.  Two states with lse = -inf merge to o = 0, lse = -inf.
+ *
+ *  o_a, o_b, o_out        [n, num_heads, head_dim], `dtype` (F32, BF16, F16), device
+ *  lse_a, lse_b, lse_out  [n, num_heads] float32, device
+ * o_out/lse_out may alias o_a/lse_a element for element.
+ * Errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (dtype E4M3 or head_dim not
+ * a multiple of 4 up to 1024), FA_ERR_CUDA. */
+int fa_merge_states(const void* o_a, const float* lse_a, const void* o_b,
+                    const float* lse_b, void* o_out, float* lse_out, int n,
+                    int num_heads, int head_dim, fa_dtype dtype,
+                    void* cuda_stream);
+
+/* Free a plan handle (host memory only; the workspace stays the caller's).
+ * NULL is accepted. */
+int fa_decode_plan_destroy(fa_decode_plan_t plan);
+
+/* Summary of a plan, for logging and tests. */
+typedef struct {
+  int batch, num_qo_heads, num_kv_heads, head_dim, page_size;
+  int num_ctas;          /* persistent decode grid */
+  int ctas_per_sm;       /* occupancy the grid was sized for */
+  int num_sms;
+  int num_segments;      /* work items (request, kv head, page range) */
+  int num_merge_units;   /* (request, kv head) pairs split over several CTAs */
+  int num_partial_slots; /* fp32 partial states written by split work items */
+  int threads_per_cta;
+  int smem_bytes_per_cta;
+  int stages;            /* depth of the shared-memory page ring */
+  int64_t total_pages;   /* sum of pages over requests */
+  int64_t total_tokens;  /* sum of len over requests */
+  size_t workspace_bytes_used;
+} fa_plan_info;
+
+int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info);
+
+/* Work list of a plan, host copy owned by the plan (valid until destroy).
+ *  cta_offsets  [num_ctas+1]: CTA c runs segments cta_offsets[c] .. [c+1]-1
+ *  segments     [num_segments * FA_SEGMENT_INTS] int32, each
+ *               {request, kv_head, page_begin, page_end, last_valid,
+ *                out_slot, 0, 0}; page_begin/page_end index the indices
+ *               array, last_valid = valid slots of the segment's final page,
+ *               out_slot = -1 when the segment covers its whole request,
+ *               else the partial-state slot it writes.
+ *  merge        [num_merge_units * FA_MERGE_INTS] int32, each
+ *               {request, kv_head, first_slot, num_slots}. */
+#define FA_SEGMENT_INTS 8
+#define FA_MERGE_INTS 4
+int fa_decode_plan_get_work(fa_decode_plan_t plan, const int32_t** cta_offsets,
+                            const int32_t** segments, const int32_t** merge);
+
+/* Host-only planning step, no CUDA call: the work-list builder that
+ * fa_decode_plan uses, exposed so it can be checked without a GPU.  Output
+ * buffers are caller-owned host arrays of the stated capacities; counts are
+ * written to *n_ctas, *n_segments, *n_merge, *n_slots.
+ * Capacities needed: cta_offsets max_ctas+1, segments
+ * (batch*num_kv_heads + max_ctas) * FA_SEGMENT_INTS, merge
+ * max_ctas * FA_MERGE_INTS.  Errors: FA_ERR_INVALID_ARG. */
+int fa_plan_work_host(const int32_t* indptr, const int32_t* last_page_len,
+                      int batch, int num_kv_heads, int page_size, int max_ctas,
+                      int min_pages_per_cta, int32_t* cta_offsets,
+                      int32_t* segments, int32_t* merge, int* n_ctas,
+                      int* n_segments, int* n_merge, int* n_slots);
+
+/* Wait for cuda_stream, then read and clear the plan's device-check word.
+ * Returns FA_OK, FA_ERR_DEVICE_CHECK with *flags set (bit 0: page id outside
+ * [0, num_pages); bit 1: a pipeline wait timed out), or FA_ERR_CUDA.
+ * This is the one call that synchronises; keep it off the hot path. */
+int fa_decode_check(fa_decode_plan_t plan, void* cuda_stream, int* flags);
+
+/* Optional timing hook: when both events are non-NULL, later fa_decode_run
+ * calls record ev_before on the stream just before the split-KV decode kernel
+ * and ev_after just after it (events are cudaEvent_t passed as void*, created
+ * by the caller).  Pass NULLs to turn the hook off. */
+int fa_decode_set_timing_events(fa_decode_plan_t plan, void* ev_before,
+                                void* ev_after);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_DECODE_H_ */

@@ -1,0 +1,326 @@
+"""Batched decode attention over a paged KV cache, for one GB300 (sm_103a).
+
+Thin Python binding of ``libfadecode.so`` (C ABI in ``include/fa_decode.h``):
+argument marshalling only.  Every step of the decode path runs in the
+library's CUDA kernels; PyTorch supplies device memory and streams.  If the
+library has not been built, the first call into it raises RuntimeError -
+there is no fallback implementation.
+
+The calls follow the plan/run split of the page "FlashDecoding + FlashInfer -
+the decode-time attention story" (section "The API you actually use"):
+``plan`` once per batch shape, ``run`` on the hot path, plus ``merge_states``
+for the merge rule of section "FlashDecoding - the split-KV trick".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+__all__ = [
+    "FA_OK", "FaError", "DecodePlan", "plan", "run", "merge_states",
+    "workspace_size", "plan_work_host", "BatchDecodeWithPagedKVCacheWrapper",
+    "LIB_PATH", "EXPORTED_SYMBOLS", "library",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfadecode.so")
+
+# Entry points declared in include/fa_decode.h.
+EXPORTED_SYMBOLS = (
+    "fa_status_string", "fa_decode_workspace_size", "fa_decode_plan",
+    "fa_decode_run", "fa_merge_states", "fa_decode_plan_destroy",
+    "fa_decode_plan_get_info", "fa_decode_plan_get_work", "fa_plan_work_host",
+    "fa_decode_check", "fa_decode_set_timing_events",
+)
+
+FA_OK = 0
+SEGMENT_INTS = 8
+MERGE_INTS = 4
+DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2,
+               torch.float8_e4m3fn: 3}
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_L().fa_status_string(status).decode()} ({status})")
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "batch", "num_qo_heads", "num_kv_heads", "head_dim", "page_size",
+        "num_ctas", "ctas_per_sm", "num_sms", "num_segments", "num_merge_units",
+        "num_partial_slots", "threads_per_cta", "smem_bytes_per_cta", "stages")] + [
+        ("total_pages", ctypes.c_int64), ("total_tokens", ctypes.c_int64),
+        ("workspace_bytes_used", ctypes.c_size_t)]
+
+    def as_dict(self) -> dict:
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+def _load() -> ctypes.CDLL:
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                            ctypes.c_float, ctypes.c_size_t)
+    lib.fa_status_string.argtypes = [i32]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.fa_decode_workspace_size.restype = sz
+    lib.fa_decode_plan.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                   P, sz, P, ctypes.POINTER(P)]
+    lib.fa_decode_plan.restype = i32
+    lib.fa_decode_run.argtypes = [P, P, P, i64, f32, f32, f32, P, P, P]
+    lib.fa_decode_run.restype = i32
+    lib.fa_merge_states.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, P]
+    lib.fa_merge_states.restype = i32
+    lib.fa_decode_plan_destroy.argtypes = [P]
+    lib.fa_decode_plan_destroy.restype = i32
+    lib.fa_decode_plan_get_info.argtypes = [P, ctypes.POINTER(PlanInfo)]
+    lib.fa_decode_plan_get_info.restype = i32
+    pp = ctypes.POINTER(ctypes.POINTER(ctypes.c_int32))
+    lib.fa_decode_plan_get_work.argtypes = [P, pp, pp, pp]
+    lib.fa_decode_plan_get_work.restype = i32
+    lib.fa_plan_work_host.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P,
+                                      ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                      ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.fa_plan_work_host.restype = i32
+    lib.fa_decode_check.argtypes = [P, P, ctypes.POINTER(i32)]
+    lib.fa_decode_check.restype = i32
+    lib.fa_decode_set_timing_events.argtypes = [P, P, P]
+    lib.fa_decode_set_timing_events.restype = i32
+    return lib
+
+
+_lib_handle: ctypes.CDLL | None = None
+
+
+def _L() -> ctypes.CDLL:
+    """The loaded library.  Raises if it was never built: there is no fallback."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it first with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` (nvcc, sm_103a)")
+        _lib_handle = _load()
+    return _lib_handle
+
+
+def library() -> ctypes.CDLL:
+    """Load (once) and return the ctypes handle of libfadecode.so."""
+    return _L()
+
+
+def _check(status: int, what: str) -> None:
+    if status != FA_OK:
+        raise FaError(status, what)
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _host_i32(t) -> np.ndarray:
+    if isinstance(t, torch.Tensor):
+        t = t.detach().to("cpu")
+        return np.ascontiguousarray(t.numpy(), dtype=np.int32)
+    return np.ascontiguousarray(np.asarray(t), dtype=np.int32)
+
+
+def _dtype_code(dt) -> int:
+    if dt not in DTYPE_CODES:
+        raise ValueError(f"unsupported dtype {dt}")
+    return DTYPE_CODES[dt]
+
+
+def workspace_size(batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int) -> int:
+    """Bytes of device workspace a plan of this batch may need (current device)."""
+    n = _L().fa_decode_workspace_size(batch, num_qo_heads, num_kv_heads, head_dim)
+    if n == 0:
+        raise ValueError("invalid shape or no CUDA device")
+    return int(n)
+
+
+class DecodePlan:
+    """A planned decode batch.  Holds the library's plan handle and keeps the
+    tensors it refers to (indices, workspace) alive."""
+
+    def __init__(self, handle, indices, workspace, q_dtype, kv_dtype, shape):
+        self._h = handle
+        self._indices = indices
+        self._workspace = workspace
+        self.q_dtype = q_dtype
+        self.kv_dtype = kv_dtype
+        self.batch, self.num_qo_heads, self.num_kv_heads, self.head_dim, self.page_size = shape
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            _L().fa_decode_plan_destroy(h)
+            self._h = None
+
+    @property
+    def info(self) -> dict:
+        i = PlanInfo()
+        _check(_L().fa_decode_plan_get_info(self._h, ctypes.byref(i)), "fa_decode_plan_get_info")
+        return i.as_dict()
+
+    def work(self):
+        """(cta_offsets [num_ctas+1], segments [n, 8], merge [m, 4]) as numpy int32."""
+        info = self.info
+        co = ctypes.POINTER(ctypes.c_int32)()
+        sg = ctypes.POINTER(ctypes.c_int32)()
+        mg = ctypes.POINTER(ctypes.c_int32)()
+        _check(_L().fa_decode_plan_get_work(self._h, ctypes.byref(co), ctypes.byref(sg),
+                                            ctypes.byref(mg)), "fa_decode_plan_get_work")
+        n_c, n_s, n_m = info["num_ctas"], info["num_segments"], info["num_merge_units"]
+        cta = np.ctypeslib.as_array(co, shape=(n_c + 1,)).copy()
+        seg = (np.ctypeslib.as_array(sg, shape=(n_s * SEGMENT_INTS,)).reshape(n_s, SEGMENT_INTS).copy()
+               if n_s else np.zeros((0, SEGMENT_INTS), np.int32))
+        mer = (np.ctypeslib.as_array(mg, shape=(n_m * MERGE_INTS,)).reshape(n_m, MERGE_INTS).copy()
+               if n_m else np.zeros((0, MERGE_INTS), np.int32))
+        return cta, seg, mer
+
+    def run(self, q: torch.Tensor, paged_kv: torch.Tensor, *, sm_scale: float | None = None,
+            k_scale: float = 1.0, v_scale: float = 1.0, out: torch.Tensor | None = None,
+            lse: torch.Tensor | None = None, return_lse: bool = True, stream=None):
+        """Decode attention; returns (o, lse) (lse None if return_lse is False)."""
+        B, Hq, D = self.batch, self.num_qo_heads, self.head_dim
+        if q.dtype != self.q_dtype or paged_kv.dtype != self.kv_dtype:
+            raise TypeError("q / paged_kv dtype differs from the plan")
+        if tuple(q.shape) != (B, Hq, D) or not q.is_contiguous() or not q.is_cuda:
+            raise ValueError(f"q must be a contiguous CUDA tensor [{B}, {Hq}, {D}]")
+        if (paged_kv.dim() != 5 or paged_kv.shape[1] != 2 or paged_kv.shape[2] != self.page_size
+                or paged_kv.shape[3] != self.num_kv_heads or paged_kv.shape[4] != D
+                or not paged_kv.is_contiguous() or not paged_kv.is_cuda):
+            raise ValueError("paged_kv must be a contiguous CUDA tensor "
+                             "[num_pages, 2, page_size, num_kv_heads, head_dim]")
+        if out is None:
+            out = torch.empty((B, Hq, D), dtype=q.dtype, device=q.device)
+        if return_lse and lse is None:
+            lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        _check(_L().fa_decode_run(
+            self._h, q.data_ptr(), paged_kv.data_ptr(), paged_kv.shape[0],
+            0.0 if sm_scale is None else float(sm_scale), float(k_scale), float(v_scale),
+            out.data_ptr(), lse.data_ptr() if lse is not None else None,
+            _stream_handle(stream)), "fa_decode_run")
+        return out, lse
+
+    def check(self, stream=None) -> int:
+        """Synchronise and return the device-check flags (0 = clean)."""
+        flags = ctypes.c_int(0)
+        st = _L().fa_decode_check(self._h, _stream_handle(stream), ctypes.byref(flags))
+        if st not in (FA_OK, -5):
+            _check(st, "fa_decode_check")
+        return int(flags.value)
+
+    def set_timing_events(self, before, after) -> None:
+        """Record torch.cuda.Events around the decode kernel of later runs (None = off)."""
+        b = ctypes.c_void_p(before.cuda_event) if before is not None else None
+        a = ctypes.c_void_p(after.cuda_event) if after is not None else None
+        _check(_L().fa_decode_set_timing_events(self._h, b, a), "fa_decode_set_timing_events")
+
+
+def plan(indptr, indices: torch.Tensor, last_page_len, num_qo_heads: int, num_kv_heads: int,
+         head_dim: int, page_size: int, *, q_data_type=torch.bfloat16,
+         kv_data_type=None, workspace: torch.Tensor | None = None, stream=None) -> DecodePlan:
+    """Plan a decode batch.  indptr/last_page_len may live on the host or the
+    device (they are read on the host); indices must be an int32 CUDA tensor."""
+    kv_data_type = q_data_type if kv_data_type is None else kv_data_type
+    indptr_h = _host_i32(indptr)
+    last_h = _host_i32(last_page_len)
+    B = indptr_h.shape[0] - 1
+    if last_h.shape[0] < B:
+        raise ValueError("last_page_len shorter than the batch")
+    if indices.dtype != torch.int32 or not indices.is_cuda or not indices.is_contiguous():
+        raise ValueError("indices must be a contiguous int32 CUDA tensor")
+    if workspace is None:
+        workspace = torch.empty(workspace_size(B, num_qo_heads, num_kv_heads, head_dim),
+                                dtype=torch.uint8, device=indices.device)
+    handle = ctypes.c_void_p()
+    _check(_L().fa_decode_plan(
+        indptr_h.ctypes.data, indices.data_ptr() if indices.numel() else None,
+        last_h.ctypes.data if B else None, B, num_qo_heads, num_kv_heads, head_dim, page_size,
+        _dtype_code(q_data_type), _dtype_code(kv_data_type), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream),
+        ctypes.byref(handle)), "fa_decode_plan")
+    return DecodePlan(handle.value, indices, workspace, q_data_type, kv_data_type,
+                      (B, num_qo_heads, num_kv_heads, head_dim, page_size))
+
+
+def run(p: DecodePlan, q, paged_kv, **kw):
+    return p.run(q, paged_kv, **kw)
+
+
+def merge_states(o_a: torch.Tensor, lse_a: torch.Tensor, o_b: torch.Tensor, lse_b: torch.Tensor,
+                 *, out: torch.Tensor | None = None, lse_out: torch.Tensor | None = None,
+                 stream=None):
+    """Merge two sets of states o [n, H, D] (f32/bf16/f16) with lse [n, H] fp32."""
+    if o_a.shape != o_b.shape or lse_a.shape != lse_b.shape or o_a.dtype != o_b.dtype:
+        raise ValueError("state shapes / dtypes differ")
+    if o_a.dim() != 3 or tuple(lse_a.shape) != tuple(o_a.shape[:2]):
+        raise ValueError("o must be [n, H, D] and lse [n, H]")
+    for t in (o_a, o_b, lse_a, lse_b):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    if lse_a.dtype != torch.float32 or lse_b.dtype != torch.float32:
+        raise TypeError("lse must be float32")
+    n, H, D = o_a.shape
+    out = torch.empty_like(o_a) if out is None else out
+    lse_out = torch.empty_like(lse_a) if lse_out is None else lse_out
+    _check(_L().fa_merge_states(o_a.data_ptr(), lse_a.data_ptr(), o_b.data_ptr(),
+                                lse_b.data_ptr(), out.data_ptr(), lse_out.data_ptr(), n, H, D,
+                                _dtype_code(o_a.dtype), _stream_handle(stream)),
+           "fa_merge_states")
+    return out, lse_out
+
+
+def plan_work_host(indptr, last_page_len, num_kv_heads: int, page_size: int, max_ctas: int,
+                   min_pages_per_cta: int = 8):
+    """Host-only work-list builder (no GPU).  Returns (cta_offsets, segments [n,8],
+    merge [m,4], n_slots)."""
+    indptr_h = _host_i32(indptr)
+    last_h = _host_i32(last_page_len)
+    B = indptr_h.shape[0] - 1
+    cta = np.zeros(max_ctas + 1, np.int32)
+    seg = np.zeros(((B * num_kv_heads + max_ctas) * SEGMENT_INTS,), np.int32)
+    mer = np.zeros((max(max_ctas, 1) * MERGE_INTS,), np.int32)
+    n_c, n_s, n_m, n_sl = (ctypes.c_int() for _ in range(4))
+    _check(_L().fa_plan_work_host(indptr_h.ctypes.data, last_h.ctypes.data if B else None, B,
+                                  num_kv_heads, page_size, max_ctas, min_pages_per_cta,
+                                  cta.ctypes.data, seg.ctypes.data, mer.ctypes.data,
+                                  ctypes.byref(n_c), ctypes.byref(n_s), ctypes.byref(n_m),
+                                  ctypes.byref(n_sl)), "fa_plan_work_host")
+    return (cta[: n_c.value + 1].copy(), seg[: n_s.value * SEGMENT_INTS].reshape(-1, SEGMENT_INTS).copy(),
+            mer[: n_m.value * MERGE_INTS].reshape(-1, MERGE_INTS).copy(), n_sl.value)
+
+
+class BatchDecodeWithPagedKVCacheWrapper:
+    """plan/run wrapper in the shape the pages show: built once over a caller
+    workspace with the "NHD" layout, planned per batch, run on the hot path."""
+
+    def __init__(self, workspace_buffer: torch.Tensor, kv_layout: str = "NHD"):
+        if kv_layout != "NHD":
+            raise ValueError("only the NHD layout is supported")
+        self._workspace = workspace_buffer
+        self._plan: DecodePlan | None = None
+
+    def plan(self, indptr, indices, last_page_len, num_qo_heads, num_kv_heads, head_dim,
+             page_size, q_data_type=torch.bfloat16, kv_data_type=None, stream=None):
+        self._plan = plan(indptr, indices, last_page_len, num_qo_heads, num_kv_heads, head_dim,
+                          page_size, q_data_type=q_data_type, kv_data_type=kv_data_type,
+                          workspace=self._workspace, stream=stream)
+        return self._plan
+
+    def run(self, q, paged_kv_cache, *, sm_scale=None, k_scale=1.0, v_scale=1.0,
+            return_lse=False, out=None, lse=None, stream=None):
+        if self._plan is None:
+            raise RuntimeError("call plan() before run()")
+        o, l = self._plan.run(q, paged_kv_cache, sm_scale=sm_scale, k_scale=k_scale,
+                              v_scale=v_scale, out=out, lse=lse, return_lse=return_lse,
+                              stream=stream)
+        return (o, l) if return_lse else o

@@ -1,0 +1,399 @@
+// C ABI of libfadecode.so (declared in include/fa_decode.h): plan handle,
+// workspace layout, TMA descriptor of the KV cache and kernel launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "fa_decode.h"
+#include "kernels.h"
+#include "planner.h"
+
+using fadecode::DecodeKernel;
+using fadecode::DecodeParams;
+using fadecode::MergeParams;
+using fadecode::WorkList;
+
+namespace {
+
+constexpr int kMinPagesPerCta = 8;     // smallest chunk worth a CTA of its own
+constexpr int kMaxCtasPerSmBound = 8;  // workspace bound; real occupancy is lower
+constexpr size_t kAlign = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t off_err, off_cta, off_seg, off_merge, meta_bytes, off_part_o, off_part_lse, total;
+};
+
+Layout make_layout(int64_t n_ctas, int64_t n_segments, int64_t n_merge, int64_t n_slots, int G,
+                   int D) {
+  Layout L;
+  L.off_err = 0;
+  L.off_cta = align_up(L.off_err + sizeof(int));
+  L.off_seg = align_up(L.off_cta + sizeof(int32_t) * (size_t)(n_ctas + 1));
+  L.off_merge = align_up(L.off_seg + sizeof(fadecode::Segment) * (size_t)n_segments);
+  L.meta_bytes = align_up(L.off_merge + sizeof(fadecode::MergeUnit) * (size_t)n_merge);
+  L.off_part_o = L.meta_bytes;
+  L.off_part_lse = align_up(L.off_part_o + sizeof(float) * (size_t)n_slots * G * D);
+  L.total = align_up(L.off_part_lse + sizeof(float) * (size_t)n_slots * G);
+  return L;
+}
+
+int dtype_size(fa_dtype t) {
+  switch (t) {
+    case FA_DTYPE_F32: return 4;
+    case FA_DTYPE_BF16:
+    case FA_DTYPE_F16: return 2;
+    case FA_DTYPE_E4M3: return 1;
+  }
+  return 0;
+}
+
+bool find_kernel(fa_dtype q, fa_dtype kv, int D, int G, DecodeKernel* k) {
+  if (q == FA_DTYPE_F32 && kv == FA_DTYPE_F32) return fadecode::find_kernel_f32(D, G, k);
+  if (q == FA_DTYPE_BF16 && kv == FA_DTYPE_BF16) return fadecode::find_kernel_bf16(D, G, k);
+  if (q == FA_DTYPE_F16 && kv == FA_DTYPE_F16) return fadecode::find_kernel_f16(D, G, k);
+  if (q == FA_DTYPE_BF16 && kv == FA_DTYPE_E4M3) return fadecode::find_kernel_bf16_e4m3(D, G, k);
+  if (q == FA_DTYPE_F16 && kv == FA_DTYPE_E4M3) return fadecode::find_kernel_f16_e4m3(D, G, k);
+  return false;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+struct fa_decode_plan_s {
+  int device = 0;
+  int batch = 0, hq = 0, hkv = 0, d = 0, page_size = 0, group = 0;
+  fa_dtype q_dtype = FA_DTYPE_F32, kv_dtype = FA_DTYPE_F32;
+  DecodeKernel kern;
+  int num_sms = 0, ctas_per_sm = 0;
+  WorkList wl;
+  std::vector<int32_t> merge_flat;
+  const int32_t* indices = nullptr;
+  uint8_t* ws = nullptr;
+  size_t ws_bytes = 0;
+  Layout layout{};
+  // cached TMA descriptor of the KV cache
+  CUtensorMap tmap;
+  const void* tmap_base = nullptr;
+  int64_t tmap_pages = -1;
+  cudaEvent_t ev_before = nullptr, ev_after = nullptr;
+};
+
+extern "C" {
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_WORKSPACE_TOO_SMALL: return "FA_ERR_WORKSPACE_TOO_SMALL";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_DEVICE_CHECK: return "FA_ERR_DEVICE_CHECK";
+  }
+  return "FA_UNKNOWN_STATUS";
+}
+
+size_t fa_decode_workspace_size(int batch, int num_qo_heads, int num_kv_heads, int head_dim) {
+  if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      num_qo_heads % num_kv_heads)
+    return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  const int64_t max_ctas = (int64_t)sms * kMaxCtasPerSmBound;
+  const int64_t segs = (int64_t)batch * num_kv_heads + max_ctas;
+  const int G = num_qo_heads / num_kv_heads;
+  return make_layout(max_ctas, segs, max_ctas, 2 * max_ctas, G, head_dim).total;
+}
+
+int fa_plan_work_host(const int32_t* indptr, const int32_t* last_page_len, int batch,
+                      int num_kv_heads, int page_size, int max_ctas, int min_pages_per_cta,
+                      int32_t* cta_offsets, int32_t* segments, int32_t* merge, int* n_ctas,
+                      int* n_segments, int* n_merge, int* n_slots) {
+  if (!cta_offsets || !segments || !merge || !n_ctas || !n_segments || !n_merge || !n_slots)
+    return FA_ERR_INVALID_ARG;
+  WorkList wl;
+  try {
+    if (fadecode::build_work_list(indptr, last_page_len, batch, num_kv_heads, page_size,
+                                  max_ctas, min_pages_per_cta, &wl) != 0)
+      return FA_ERR_INVALID_ARG;
+  } catch (const std::bad_alloc&) {
+    return FA_ERR_INVALID_ARG;
+  }
+  std::memcpy(cta_offsets, wl.cta_offsets.data(), sizeof(int32_t) * wl.cta_offsets.size());
+  std::memcpy(segments, wl.segments.data(), sizeof(fadecode::Segment) * wl.segments.size());
+  std::memcpy(merge, wl.merge.data(), sizeof(fadecode::MergeUnit) * wl.merge.size());
+  *n_ctas = wl.num_ctas;
+  *n_segments = (int)wl.segments.size();
+  *n_merge = (int)wl.merge.size();
+  *n_slots = wl.num_slots;
+  return FA_OK;
+}
+
+int fa_decode_plan(const int32_t* indptr_host, const int32_t* indices_dev,
+                   const int32_t* last_page_len_host, int batch, int num_qo_heads,
+                   int num_kv_heads, int head_dim, int page_size, fa_dtype q_dtype,
+                   fa_dtype kv_dtype, void* workspace_dev, size_t workspace_bytes,
+                   void* cuda_stream, fa_decode_plan_t* out_plan) {
+  if (!out_plan) return FA_ERR_INVALID_ARG;
+  *out_plan = nullptr;
+  if (!indptr_host || batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      page_size <= 0 || num_qo_heads % num_kv_heads || !workspace_dev)
+    return FA_ERR_INVALID_ARG;
+  if (batch > 0 && !last_page_len_host) return FA_ERR_INVALID_ARG;
+  if (indptr_host[batch] > 0 && !indices_dev) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace_dev) % kAlign) return FA_ERR_INVALID_ARG;
+  if (dtype_size(q_dtype) == 0 || dtype_size(kv_dtype) == 0) return FA_ERR_INVALID_ARG;
+  const int G = num_qo_heads / num_kv_heads;
+  if (page_size != fadecode::kPageSize) return FA_ERR_UNSUPPORTED;
+  DecodeKernel kern;
+  if (!find_kernel(q_dtype, kv_dtype, head_dim, G, &kern)) return FA_ERR_UNSUPPORTED;
+
+  int dev = 0, sms = 0, occ = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (cudaFuncSetAttribute(kern.func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kern.smem_bytes) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern.func, kern.threads,
+                                                    kern.smem_bytes) != cudaSuccess)
+    return FA_ERR_CUDA;
+  occ = std::max(1, std::min(occ, kMaxCtasPerSmBound));
+
+  fa_decode_plan_s* plan = new (std::nothrow) fa_decode_plan_s();
+  if (!plan) return FA_ERR_INVALID_ARG;
+  plan->device = dev;
+  plan->batch = batch;
+  plan->hq = num_qo_heads;
+  plan->hkv = num_kv_heads;
+  plan->d = head_dim;
+  plan->page_size = page_size;
+  plan->group = G;
+  plan->q_dtype = q_dtype;
+  plan->kv_dtype = kv_dtype;
+  plan->kern = kern;
+  plan->num_sms = sms;
+  plan->ctas_per_sm = occ;
+  plan->indices = indices_dev;
+  plan->ws = static_cast<uint8_t*>(workspace_dev);
+  plan->ws_bytes = workspace_bytes;
+
+  int rc = FA_OK;
+  try {
+    if (fadecode::build_work_list(indptr_host, last_page_len_host, batch, num_kv_heads,
+                                  page_size, sms * occ, kMinPagesPerCta, &plan->wl) != 0)
+      rc = FA_ERR_INVALID_ARG;
+  } catch (const std::bad_alloc&) {
+    rc = FA_ERR_INVALID_ARG;
+  }
+  if (rc != FA_OK) {
+    delete plan;
+    return rc;
+  }
+  const WorkList& wl = plan->wl;
+  plan->layout = make_layout(wl.num_ctas, (int64_t)wl.segments.size(), (int64_t)wl.merge.size(),
+                             wl.num_slots, G, head_dim);
+  if (plan->layout.total > workspace_bytes) {
+    delete plan;
+    return FA_ERR_WORKSPACE_TOO_SMALL;
+  }
+  plan->merge_flat.resize(wl.merge.size() * FA_MERGE_INTS);
+  if (!wl.merge.empty())
+    std::memcpy(plan->merge_flat.data(), wl.merge.data(), wl.merge.size() * sizeof(wl.merge[0]));
+
+  // One host image of the metadata region, one copy into the workspace.
+  std::vector<uint8_t> meta(plan->layout.meta_bytes, 0);
+  std::memcpy(meta.data() + plan->layout.off_cta, wl.cta_offsets.data(),
+              sizeof(int32_t) * wl.cta_offsets.size());
+  if (!wl.segments.empty())
+    std::memcpy(meta.data() + plan->layout.off_seg, wl.segments.data(),
+                sizeof(fadecode::Segment) * wl.segments.size());
+  if (!wl.merge.empty())
+    std::memcpy(meta.data() + plan->layout.off_merge, wl.merge.data(),
+                sizeof(fadecode::MergeUnit) * wl.merge.size());
+  if (cudaMemcpyAsync(plan->ws, meta.data(), meta.size(), cudaMemcpyHostToDevice,
+                      static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
+    delete plan;
+    return FA_ERR_CUDA;
+  }
+  *out_plan = plan;
+  return FA_OK;
+}
+
+int fa_decode_run(fa_decode_plan_t plan, const void* q, const void* paged_kv, int64_t num_pages,
+                  float sm_scale, float k_scale, float v_scale, void* o, float* lse,
+                  void* cuda_stream) {
+  if (!plan) return FA_ERR_INVALID_ARG;
+  if (plan->batch == 0) return FA_OK;
+  if (!q || !paged_kv || !o || num_pages <= 0) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(paged_kv) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
+    return FA_ERR_INVALID_ARG;
+  if (2 * num_pages > (int64_t)0xffffffffLL) return FA_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const int D = plan->d, P = plan->page_size, Hkv = plan->hkv;
+  const size_t es = (size_t)dtype_size(plan->kv_dtype);
+
+  if (paged_kv != plan->tmap_base || num_pages != plan->tmap_pages) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
+    if (!encode) return FA_ERR_CUDA;
+    CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    switch (plan->kv_dtype) {
+      case FA_DTYPE_F32: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; break;
+      case FA_DTYPE_BF16: dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; break;
+      case FA_DTYPE_F16: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; break;
+      case FA_DTYPE_E4M3: dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;
+    }
+    // [2*num_pages][P][Hkv][D], innermost first; one box = K and V rows of
+    // one kv head of one page.
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)P,
+                          (cuuint64_t)(2 * num_pages)};
+    cuuint64_t strides[3] = {(cuuint64_t)(D * es), (cuuint64_t)(Hkv * D * es),
+                             (cuuint64_t)(P * Hkv * D * es)};
+    cuuint32_t box[4] = {(cuuint32_t)D, 1u, (cuuint32_t)P, 2u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r = encode(&plan->tmap, dt, 4, const_cast<void*>(paged_kv), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      plan->tmap_base = nullptr;
+      return FA_ERR_CUDA;
+    }
+    plan->tmap_base = paged_kv;
+    plan->tmap_pages = num_pages;
+  }
+
+  if (!(sm_scale > 0.f)) sm_scale = 1.0f / std::sqrt((float)D);
+  DecodeParams prm;
+  prm.q = q;
+  prm.o = o;
+  prm.lse = lse;
+  prm.indices = plan->indices;
+  prm.cta_offsets = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_cta);
+  prm.segments = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_seg);
+  prm.part_o = reinterpret_cast<float*>(plan->ws + plan->layout.off_part_o);
+  prm.part_lse = reinterpret_cast<float*>(plan->ws + plan->layout.off_part_lse);
+  prm.err = reinterpret_cast<int*>(plan->ws + plan->layout.off_err);
+  prm.num_pages = num_pages;
+  prm.num_qo_heads = plan->hq;
+  prm.q_scale = sm_scale * k_scale * kLog2e;
+  prm.v_scale = v_scale;
+
+  const bool timed = plan->ev_before && plan->ev_after;
+  if (timed && cudaEventRecord(plan->ev_before, st) != cudaSuccess) return FA_ERR_CUDA;
+  void* args[2] = {&plan->tmap, &prm};
+  if (cudaLaunchKernel(plan->kern.func, dim3(plan->wl.num_ctas), dim3(plan->kern.threads), args,
+                       (size_t)plan->kern.smem_bytes, st) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (timed && cudaEventRecord(plan->ev_after, st) != cudaSuccess) return FA_ERR_CUDA;
+  if (!plan->wl.merge.empty()) {
+    MergeParams mp;
+    mp.merge = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_merge);
+    mp.part_o = prm.part_o;
+    mp.part_lse = prm.part_lse;
+    mp.o = o;
+    mp.lse = lse;
+    mp.num_qo_heads = plan->hq;
+    void* margs[1] = {&mp};
+    if (cudaLaunchKernel(plan->kern.merge_func, dim3((unsigned)plan->wl.merge.size()), dim3(128),
+                         margs, 0, st) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
+                    void* o_out, float* lse_out, int n, int num_heads, int head_dim,
+                    fa_dtype dtype, void* cuda_stream) {
+  if (n < 0 || num_heads <= 0 || head_dim <= 0) return FA_ERR_INVALID_ARG;
+  if (n == 0) return FA_OK;
+  if (!o_a || !lse_a || !o_b || !lse_b || !o_out || !lse_out) return FA_ERR_INVALID_ARG;
+  if (head_dim > 1024 || dtype == FA_DTYPE_E4M3 || dtype_size(dtype) == 0)
+    return FA_ERR_UNSUPPORTED;
+  return fadecode::launch_merge_states(o_a, lse_a, o_b, lse_b, o_out, lse_out,
+                                       (int64_t)n * num_heads, head_dim, dtype, cuda_stream);
+}
+
+int fa_decode_plan_destroy(fa_decode_plan_t plan) {
+  delete plan;
+  return FA_OK;
+}
+
+int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info) {
+  if (!plan || !info) return FA_ERR_INVALID_ARG;
+  fa_plan_info i;
+  std::memset(&i, 0, sizeof i);
+  i.batch = plan->batch;
+  i.num_qo_heads = plan->hq;
+  i.num_kv_heads = plan->hkv;
+  i.head_dim = plan->d;
+  i.page_size = plan->page_size;
+  i.num_ctas = plan->wl.num_ctas;
+  i.ctas_per_sm = plan->ctas_per_sm;
+  i.num_sms = plan->num_sms;
+  i.num_segments = (int)plan->wl.segments.size();
+  i.num_merge_units = (int)plan->wl.merge.size();
+  i.num_partial_slots = plan->wl.num_slots;
+  i.threads_per_cta = plan->kern.threads;
+  i.smem_bytes_per_cta = plan->kern.smem_bytes;
+  i.stages = plan->kern.stages;
+  i.total_pages = plan->wl.total_pages;
+  i.total_tokens = plan->wl.total_tokens;
+  i.workspace_bytes_used = plan->layout.total;
+  *info = i;
+  return FA_OK;
+}
+
+int fa_decode_plan_get_work(fa_decode_plan_t plan, const int32_t** cta_offsets,
+                            const int32_t** segments, const int32_t** merge) {
+  if (!plan || !cta_offsets || !segments || !merge) return FA_ERR_INVALID_ARG;
+  *cta_offsets = plan->wl.cta_offsets.data();
+  *segments = reinterpret_cast<const int32_t*>(plan->wl.segments.data());
+  *merge = plan->merge_flat.data();
+  return FA_OK;
+}
+
+int fa_decode_check(fa_decode_plan_t plan, void* cuda_stream, int* flags) {
+  if (!plan || !flags) return FA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  int word = 0;
+  int* dword = reinterpret_cast<int*>(plan->ws + plan->layout.off_err);
+  if (cudaStreamSynchronize(st) != cudaSuccess ||
+      cudaMemcpy(&word, dword, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(dword, 0, sizeof word) != cudaSuccess)
+    return FA_ERR_CUDA;
+  *flags = word;
+  return word ? FA_ERR_DEVICE_CHECK : FA_OK;
+}
+
+int fa_decode_set_timing_events(fa_decode_plan_t plan, void* ev_before, void* ev_after) {
+  if (!plan) return FA_ERR_INVALID_ARG;
+  plan->ev_before = static_cast<cudaEvent_t>(ev_before);
+  plan->ev_after = static_cast<cudaEvent_t>(ev_after);
+  return FA_OK;
+}
+
+}  // extern "C"

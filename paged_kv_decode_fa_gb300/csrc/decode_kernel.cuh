@@ -1,0 +1,584 @@
+// Split-KV paged decode attention for sm_103a.
+//
+// One persistent CTA per planner chunk list (see planner.cpp).  Inside a CTA:
+//  - warp NW (the producer) walks the CTA's segments page by page, reads each
+//    page id from the index table and issues one 4-D TMA tensor copy per page
+//    that brings the page's K and V rows of one kv head ([2][16][D]) into a
+//    ring of S shared-memory stages, signalled through mbarriers;
+//  - warps 0..NW-1 (consumers) take the pages round-robin.  For each page a
+//    warp computes the scores of all G query heads of the kv head's group
+//    from one read of each K row (the tile is reused across the group), folds
+//    them into its running softmax state with the online-softmax recurrence,
+//    and accumulates P.V from one read of each V row;
+//  - at the end of a segment the NW warp states are combined with the merge
+//    rule and written either as the final o/lse or as an fp32 partial state
+//    that the merge kernel combines later.
+// The online-softmax update, the warp combine and the split merge are all the
+// same recurrence applied at three levels, as section "FlashDecoding - the
+// split-KV trick" of the page "FlashDecoding + FlashInfer - the decode-time
+// attention story" describes (tile level in the main kernel, split level in
+// the reduction).  Scores are kept in the log2 domain: q is pre-multiplied by
+// sm_scale * k_scale * log2(e), so exp(s - m) becomes exp2(s' - m').
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <type_traits>
+
+#include "kernels.h"
+
+namespace fadecode {
+namespace dev {
+
+constexpr float kLn2 = 0.693147180559945309f;
+// Upper bound on any single pipeline wait; a wait that runs out sets bit 1 of
+// the device-check word and the CTA finishes without waiting again.
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait without the abort short-cut: true if the phase completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+  return true;
+}
+
+// Bounded wait.  Once `aborted` is set (an earlier wait ran out) it returns
+// at once so that the CTA drains instead of hanging.
+__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity,
+                                          bool& aborted, int* err) {
+  if (aborted || mbar_try_wait(bar, parity)) return;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      aborted = true;
+      atomicOr(err, 2);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map,
+                                            int c0, int c1, int c2, int c3,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---- element conversion -------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
+  __half2 h;
+  memcpy(&h, &w, sizeof(h));
+  return __half22float2(h);
+}
+
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t w) {
+  __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w), __NV_E4M3);
+  __half2 h(hr);
+  return __half22float2(h);
+}
+
+// VEC elements of type T starting at p (16 or 8 bytes), widened to float.
+template <typename T, int VEC>
+struct VecLoad;
+
+template <>
+struct VecLoad<float, 4> {
+  static constexpr int kBytes = 16;
+  __device__ __forceinline__ static void load(const void* p, float (&f)[4]) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+  }
+};
+
+template <>
+struct VecLoad<__nv_bfloat16, 8> {
+  static constexpr int kBytes = 16;
+  __device__ __forceinline__ static void load(const void* p, float (&f)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+  }
+};
+
+template <>
+struct VecLoad<__half, 8> {
+  static constexpr int kBytes = 16;
+  __device__ __forceinline__ static void load(const void* p, float (&f)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    float2 a = half2_bits_to_float2(v.x), b = half2_bits_to_float2(v.y);
+    float2 c = half2_bits_to_float2(v.z), d = half2_bits_to_float2(v.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+  }
+};
+
+template <>
+struct VecLoad<__nv_fp8_e4m3, 8> {
+  static constexpr int kBytes = 8;
+  __device__ __forceinline__ static void load(const void* p, float (&f)[8]) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    float2 a = e4m3x2_to_float2((uint16_t)(v.x & 0xffff));
+    float2 b = e4m3x2_to_float2((uint16_t)(v.x >> 16));
+    float2 c = e4m3x2_to_float2((uint16_t)(v.y & 0xffff));
+    float2 d = e4m3x2_to_float2((uint16_t)(v.y >> 16));
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+  }
+};
+
+// q is read straight from global memory (it is small and L2-resident).
+template <typename T, int VEC>
+__device__ __forceinline__ void load_q(const T* p, float (&f)[VEC]) {
+  static_assert(VEC * sizeof(T) == 16 || (VEC == 8 && sizeof(T) == 4),
+                "q vector must be 16 or 32 bytes");
+  if constexpr (sizeof(T) == 4 && VEC == 8) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  } else if constexpr (sizeof(T) == 4) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  } else {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        f[2 * i] = bf16_lo(w[i]);
+        f[2 * i + 1] = bf16_hi(w[i]);
+      } else {
+        float2 x = half2_bits_to_float2(w[i]);
+        f[2 * i] = x.x;
+        f[2 * i + 1] = x.y;
+      }
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ T from_float(float x);
+template <>
+__device__ __forceinline__ float from_float<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+template <>
+__device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
+
+// Sum v[0..G) over the LPR lanes of a row group and leave lane c holding the
+// total of head c / (LPR / G): each halving step exchanges half of the
+// remaining values with the partner lane instead of reducing all of them.
+template <int G, int LPR>
+__device__ __forceinline__ float reduce_scatter(float (&v)[G], int c) {
+  static_assert(G >= 1 && G <= LPR, "group larger than a row group");
+  int n = G;
+#pragma unroll
+  for (int off = LPR / 2; off >= LPR / G && off >= 1; off >>= 1) {
+    if (n == 1) break;
+    const bool upper = (c & off) != 0;
+#pragma unroll
+    for (int i = 0; i < G / 2; ++i) {
+      if (i < n / 2) {
+        const float send = upper ? v[i] : v[i + n / 2];
+        const float keep = upper ? v[i + n / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+    }
+    n >>= 1;
+  }
+#pragma unroll
+  for (int off = LPR / (2 * G); off >= 1; off >>= 1)
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+  return v[0];
+}
+
+}  // namespace dev
+
+template <typename QT, typename KVT, int D, int G, int NW>
+struct DecodeCfg {
+  static constexpr int P = kPageSize;
+  static constexpr int KV_ES = sizeof(KVT);
+  static constexpr int VEC_BYTES = KV_ES == 1 ? 8 : 16;
+  static constexpr int VEC = VEC_BYTES / KV_ES;
+  static constexpr int LPR = D / VEC;  // lanes that share one K/V row
+  static constexpr int RPS = 32 / LPR;  // rows a warp covers per step
+  static constexpr int STEPS = P / RPS;
+  static constexpr int HPL = LPR / G;   // lanes holding the same head's score
+  static constexpr int ROW_BYTES = D * KV_ES;
+  static constexpr int STAGE_BYTES = 2 * P * ROW_BYTES;
+  static constexpr int S0 = 49152 / STAGE_BYTES;
+  static constexpr int S = S0 < 4 ? 4 : (S0 > 16 ? 16 : S0);
+  static constexpr int THREADS = (NW + 1) * 32;
+  static constexpr int OFF_FULL = S * STAGE_BYTES;
+  static constexpr int OFF_EMPTY = OFF_FULL + 8 * S;
+  static constexpr int OFF_P = OFF_EMPTY + 8 * S;
+  static constexpr int OFF_MO = OFF_P + 4 * NW * P * G;
+  static constexpr int OFF_MM = OFF_MO + 4 * NW * G * D;
+  static constexpr int OFF_MD = OFF_MM + 4 * NW * G;
+  static constexpr int SMEM = OFF_MD + 4 * NW * G;
+  static_assert(LPR <= 32 && 32 % LPR == 0 && P % RPS == 0, "row mapping");
+  static_assert(G <= LPR, "group size larger than lanes per row");
+  static_assert(STAGE_BYTES % 128 == 0, "stage alignment");
+};
+
+template <typename QT, typename KVT, int D, int G, int NW>
+__global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
+    fa_decode_split_kernel(const __grid_constant__ CUtensorMap kv_map,
+                           const DecodeParams p) {
+  using C = DecodeCfg<QT, KVT, D, G, NW>;
+  constexpr int P = C::P, VEC = C::VEC, LPR = C::LPR, RPS = C::RPS,
+                STEPS = C::STEPS, HPL = C::HPL, S = C::S;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_FULL);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + C::OFF_EMPTY);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int seg_begin = p.cta_offsets[blockIdx.x];
+  const int seg_end = p.cta_offsets[blockIdx.x + 1];
+  bool aborted = false;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      dev::mbar_init(dev::smem_addr(&full[s]), 1);
+      dev::mbar_init(dev::smem_addr(&empty[s]), 1);
+    }
+    dev::fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == NW) {
+    // ---------------- producer: page gather through the index table -------
+    const uint64_t policy = dev::evict_first_policy();
+    int k = 0;
+    for (int si = seg_begin; si < seg_end; ++si) {
+      const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * si);
+      const int kvh = sa.y, pb = sa.z, pe = sa.w;
+      for (int p0 = pb; p0 < pe; p0 += 32) {
+        const int cnt = min(32, pe - p0);
+        int id = lane < cnt ? __ldg(p.indices + p0 + lane) : 0;
+        const bool bad = lane < cnt && (id < 0 || (int64_t)id >= p.num_pages);
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, 1);
+        for (int i = 0; i < cnt; ++i, ++k) {
+          const int page = __shfl_sync(0xffffffffu, id, i);
+          if (lane == 0) {
+            const int stage = k % S;
+            const uint32_t round = (uint32_t)(k / S);
+            dev::mbar_wait(dev::smem_addr(&empty[stage]), (round & 1u) ^ 1u, aborted, p.err);
+            const uint32_t fb = dev::smem_addr(&full[stage]);
+            dev::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+            // Out-of-range ids (already flagged) land outside the tensor map
+            // and read zeros.
+            dev::tma_load_4d(dev::smem_addr(ring + stage * C::STAGE_BYTES), &kv_map, 0, kvh,
+                             0, 2 * page, fb, policy);
+          }
+        }
+      }
+    }
+    // Make sure no copy is still landing in shared memory when the CTA exits
+    // (only matters if a consumer gave up waiting).
+    if (lane == 0) {
+      const int first = k > S ? k - S : 0;
+      for (int kk = first; kk < k; ++kk)
+        if (!dev::mbar_wait_bounded(dev::smem_addr(&full[kk % S]), (uint32_t)((kk / S) & 1)))
+          atomicOr(p.err, 2);
+    }
+    return;
+  }
+
+  // ------------------ consumers ----------------------------------------
+  float* pw = reinterpret_cast<float*>(smem + C::OFF_P) + warp * P * G;
+  float* mo = reinterpret_cast<float*>(smem + C::OFF_MO);
+  float* mm = reinterpret_cast<float*>(smem + C::OFF_MM);
+  float* md = reinterpret_cast<float*>(smem + C::OFF_MD);
+  const int rs = lane / LPR;  // row within a step
+  const int c = lane % LPR;   // column chunk
+  const int hl = c / HPL;     // head whose score this lane ends up holding
+  const QT* __restrict__ qbase = static_cast<const QT*>(p.q);
+  QT* __restrict__ obase = static_cast<QT*>(p.o);
+  constexpr int CT = NW * 32;
+
+  int kbase = 0;
+  for (int si = seg_begin; si < seg_end; ++si) {
+    const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * si);
+    const int4 sb = *reinterpret_cast<const int4*>(p.segments + 8 * si + 4);
+    const int req = sa.x, kvh = sa.y, npg = sa.w - sa.z;
+    const int last_valid = sb.x, out_slot = sb.y;
+
+    float qf[G][VEC];
+    float acc[G][VEC];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const QT* qp = qbase + ((size_t)req * p.num_qo_heads + kvh * G + h) * D + c * VEC;
+      dev::load_q<QT, VEC>(qp, qf[h]);
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) {
+        qf[h][v] *= p.q_scale;
+        acc[h][v] = 0.f;
+      }
+    }
+    float m_l = -INFINITY, d_l = 0.f;
+
+    for (int lp = warp; lp < npg; lp += NW) {
+      const int k = kbase + lp;
+      const int stage = k % S;
+      dev::mbar_wait(dev::smem_addr(&full[stage]), (uint32_t)((k / S) & 1), aborted, p.err);
+      const uint8_t* kt = ring + stage * C::STAGE_BYTES;
+      const uint8_t* vt = kt + P * C::ROW_BYTES;
+      const int valid = (lp == npg - 1) ? last_valid : P;
+
+      float sc[STEPS];
+#pragma unroll
+      for (int st = 0; st < STEPS; ++st) {
+        const int j = st * RPS + rs;
+        float kf[VEC];
+        dev::VecLoad<KVT, VEC>::load(kt + j * C::ROW_BYTES + c * C::VEC_BYTES, kf);
+        float part[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float a = 0.f;
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) a = fmaf(qf[h][v], kf[v], a);
+          part[h] = a;
+        }
+        const float s = dev::reduce_scatter<G, LPR>(part, c);
+        sc[st] = j < valid ? s : -INFINITY;
+      }
+      float mx = sc[0];
+#pragma unroll
+      for (int st = 1; st < STEPS; ++st) mx = fmaxf(mx, sc[st]);
+#pragma unroll
+      for (int off = LPR; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float m_new = fmaxf(m_l, mx);
+      const float alpha = dev::fast_exp2(m_l - m_new);
+      float ps = 0.f;
+#pragma unroll
+      for (int st = 0; st < STEPS; ++st) {
+        sc[st] = dev::fast_exp2(sc[st] - m_new);
+        ps += sc[st];
+      }
+#pragma unroll
+      for (int off = LPR; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+      d_l = d_l * alpha + ps;
+      m_l = m_new;
+      if (c % HPL == 0) {
+#pragma unroll
+        for (int st = 0; st < STEPS; ++st) pw[(st * RPS + rs) * G + hl] = sc[st];
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float a = __shfl_sync(0xffffffffu, alpha, h * HPL);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) acc[h][v] *= a;
+      }
+      __syncwarp();
+#pragma unroll
+      for (int st = 0; st < STEPS; ++st) {
+        const int j = st * RPS + rs;
+        if (j < valid) {
+          float vf[VEC];
+          dev::VecLoad<KVT, VEC>::load(vt + j * C::ROW_BYTES + c * C::VEC_BYTES, vf);
+          float pj[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) pj[h] = pw[j * G + h];
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) acc[h][v] = fmaf(pj[h], vf[v], acc[h][v]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(dev::smem_addr(&empty[stage]));
+    }
+
+    // Sum the row groups of this warp (they share m and d).
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int v = 0; v < VEC; ++v)
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1)
+          acc[h][v] += __shfl_xor_sync(0xffffffffu, acc[h][v], off);
+    if (rs == 0) {
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) mo[(warp * G + h) * D + c * VEC + v] = acc[h][v];
+      if (c % HPL == 0) {
+        mm[warp * G + hl] = m_l;
+        md[warp * G + hl] = d_l;
+      }
+    }
+    dev::named_barrier(1, CT);
+
+    // Merge the NW warp states of this segment and emit.
+    for (int e = threadIdx.x; e < G * D; e += CT) {
+      const int h = e / D, dd = e % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * G + h]);
+      float out = 0.f, lse2 = -INFINITY;
+      if (M != -INFINITY) {
+        float den = 0.f, num = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float sw = dev::fast_exp2(mm[w * G + h] - M);
+          den = fmaf(md[w * G + h], sw, den);
+          num = fmaf(mo[(w * G + h) * D + dd], sw, num);
+        }
+        out = num / den * p.v_scale;
+        lse2 = M + dev::fast_log2(den);
+      }
+      if (out_slot < 0) {
+        const size_t row = (size_t)req * p.num_qo_heads + kvh * G + h;
+        obase[row * D + dd] = dev::from_float<QT>(out);
+        if (dd == 0 && p.lse) p.lse[row] = lse2 * dev::kLn2;
+      } else {
+        p.part_o[((size_t)out_slot * G + h) * D + dd] = out;
+        if (dd == 0) p.part_lse[(size_t)out_slot * G + h] = lse2;
+      }
+    }
+    dev::named_barrier(1, CT);
+    kbase += npg;
+  }
+}
+
+// Split-level merge: one CTA per (request, kv head) that the planner split;
+// folds its partial states with the merge rule (all in the log2 domain).
+template <typename QT, int D, int G>
+__global__ void __launch_bounds__(128) fa_merge_partials_kernel(const MergeParams p) {
+  const int4 u = reinterpret_cast<const int4*>(p.merge)[blockIdx.x];
+  const int req = u.x, kvh = u.y, s0 = u.z, ns = u.w;
+  QT* obase = static_cast<QT*>(p.o);
+  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+    const int h = e / D, dd = e % D;
+    float M = -INFINITY;
+    for (int k = 0; k < ns; ++k) M = fmaxf(M, p.part_lse[(size_t)(s0 + k) * G + h]);
+    float out = 0.f, lse2 = -INFINITY;
+    if (M != -INFINITY) {
+      float den = 0.f, num = 0.f;
+      for (int k = 0; k < ns; ++k) {
+        const float w = dev::fast_exp2(p.part_lse[(size_t)(s0 + k) * G + h] - M);
+        den += w;
+        num = fmaf(p.part_o[((size_t)(s0 + k) * G + h) * D + dd], w, num);
+      }
+      out = num / den;
+      lse2 = M + dev::fast_log2(den);
+    }
+    const size_t row = (size_t)req * p.num_qo_heads + kvh * G + h;
+    obase[row * D + dd] = dev::from_float<QT>(out);
+    if (dd == 0 && p.lse) p.lse[row] = lse2 * dev::kLn2;
+  }
+}
+
+template <typename QT, typename KVT, int D, int G, int NW = 4>
+inline void fill_kernel(DecodeKernel* k) {
+  using C = DecodeCfg<QT, KVT, D, G, NW>;
+  k->func = reinterpret_cast<const void*>(&fa_decode_split_kernel<QT, KVT, D, G, NW>);
+  k->merge_func = reinterpret_cast<const void*>(&fa_merge_partials_kernel<QT, D, G>);
+  k->threads = C::THREADS;
+  k->smem_bytes = C::SMEM;
+  k->stages = C::S;
+  k->stage_bytes = C::STAGE_BYTES;
+  k->group = G;
+  k->head_dim = D;
+}
+
+// Dispatch over the compiled head_dim x group grid for one dtype pair.
+template <typename QT, typename KVT>
+inline bool find_kernel_for(int head_dim, int group, DecodeKernel* k) {
+#define FA_CASE(DD, GG)                       \
+  if (head_dim == DD && group == GG) {        \
+    fill_kernel<QT, KVT, DD, GG>(k);          \
+    return true;                              \
+  }
+  FA_CASE(64, 1) FA_CASE(64, 2) FA_CASE(64, 4) FA_CASE(64, 8)
+  FA_CASE(128, 1) FA_CASE(128, 2) FA_CASE(128, 4) FA_CASE(128, 8)
+#undef FA_CASE
+  return false;
+}
+
+}  // namespace fadecode

@@ -1,0 +1,64 @@
+// Host-side view of the CUDA kernels: parameter blocks and the registry that
+// maps (q dtype, kv dtype, head_dim, group size) to a compiled instance.
+#pragma once
+#include <cstdint>
+
+#include "fa_decode.h"
+
+namespace fadecode {
+
+constexpr int kPageSize = 16;
+
+// Kernel parameters of the split-KV decode kernel (the TMA descriptor of the
+// KV cache travels beside it as a __grid_constant__ argument).
+struct DecodeParams {
+  const void* q;               // [B, Hq, D] q dtype
+  void* o;                     // [B, Hq, D] q dtype
+  float* lse;                  // [B, Hq] or nullptr
+  const int32_t* indices;      // page ids
+  const int32_t* cta_offsets;  // [num_ctas + 1]
+  const int32_t* segments;     // [num_segments * 8]
+  float* part_o;               // [slots, G, D] fp32, normalised partial outputs
+  float* part_lse;             // [slots, G] fp32, log2-domain log-sum-exp
+  int* err;                    // device-check word
+  int64_t num_pages;
+  int num_qo_heads;
+  float q_scale;  // sm_scale * k_scale * log2(e), folded into q
+  float v_scale;
+};
+
+struct MergeParams {
+  const int32_t* merge;  // [n_merge * 4]
+  const float* part_o;
+  const float* part_lse;
+  void* o;
+  float* lse;
+  int num_qo_heads;
+};
+
+// One compiled decode kernel instance and its launch shape.
+struct DecodeKernel {
+  const void* func = nullptr;      // __global__ (CUtensorMap, DecodeParams)
+  const void* merge_func = nullptr;  // __global__ (MergeParams)
+  int threads = 0;
+  int smem_bytes = 0;
+  int stages = 0;
+  int stage_bytes = 0;
+  int group = 0;
+  int head_dim = 0;
+};
+
+// Each returns false when the combination is not compiled.
+bool find_kernel_f32(int head_dim, int group, DecodeKernel* k);
+bool find_kernel_bf16(int head_dim, int group, DecodeKernel* k);
+bool find_kernel_f16(int head_dim, int group, DecodeKernel* k);
+bool find_kernel_bf16_e4m3(int head_dim, int group, DecodeKernel* k);
+bool find_kernel_f16_e4m3(int head_dim, int group, DecodeKernel* k);
+
+// fa_merge_states kernels (merge.cu).
+int launch_merge_states(const void* o_a, const float* lse_a, const void* o_b,
+                        const float* lse_b, void* o_out, float* lse_out,
+                        int64_t n_states, int head_dim, fa_dtype dtype,
+                        void* stream);
+
+}  // namespace fadecode

@@ -1,0 +1,44 @@
+// Host planner for split-KV paged decode: cuts the batch's KV work into
+// per-CTA chunks of equal page count.  Pure C++, no CUDA.
+#pragma once
+#include <cstdint>
+#include <vector>
+
+namespace fadecode {
+
+// One work item, eight int32 so the device can read it as two int4.
+struct Segment {
+  int32_t request;
+  int32_t kv_head;
+  int32_t page_begin;  // position in the indices array
+  int32_t page_end;    // exclusive
+  int32_t last_valid;  // valid slots in the segment's final page
+  int32_t out_slot;    // -1: writes o/lse directly; else partial-state slot
+  int32_t pad0, pad1;
+};
+static_assert(sizeof(Segment) == 32, "Segment must stay 32 bytes");
+
+struct MergeUnit {
+  int32_t request;
+  int32_t kv_head;
+  int32_t first_slot;
+  int32_t num_slots;
+};
+static_assert(sizeof(MergeUnit) == 16, "MergeUnit must stay 16 bytes");
+
+struct WorkList {
+  std::vector<int32_t> cta_offsets;  // num_ctas + 1
+  std::vector<Segment> segments;
+  std::vector<MergeUnit> merge;
+  int num_ctas = 0;
+  int num_slots = 0;
+  int64_t total_pages = 0;   // sum over requests (not times kv heads)
+  int64_t total_tokens = 0;  // sum of len over requests
+};
+
+// Returns 0 on success, -1 for malformed input (see fa_decode.h).
+int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
+                    int batch, int num_kv_heads, int page_size, int max_ctas,
+                    int min_pages_per_cta, WorkList* out);
+
+}  // namespace fadecode

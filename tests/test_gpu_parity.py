@@ -1,0 +1,223 @@
+"""CUDA path vs the float64 oracle, through the C ABI, on seeded inputs.
+
+Tolerances (absolute, on o and lse): fp32 1e-5, bf16 2e-2, E4M3 KV 3e-2
+against the dequantised oracle.  Small cases are compared element by
+element; the full-size workloads run in the launch configuration bench.py
+times and are checked on sampled requests that the oracle computes one by
+one (their pages copied out into a compact batch).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_fa_gb300 import workloads as W
+from tests.helpers import oracle_decode, sub_batch
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-2, torch.float16: 2e-2,
+       torch.float8_e4m3fn: 3e-2}
+
+
+def tol_for(b):
+    return TOL[b.paged_kv.dtype] if b.paged_kv.dtype == torch.float8_e4m3fn else TOL[b.q.dtype]
+
+
+def run_lib(fa, b, workspace=None, **kw):
+    p = fa.plan(b.indptr, b.indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                b.head_dim, b.page_size, q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype,
+                workspace=workspace)
+    o, lse = p.run(b.q, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale, **kw)
+    torch.cuda.synchronize()
+    return p, o, lse
+
+
+def compare(o, lse, ref_o, ref_lse, tol, rows=None):
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    if rows is not None:
+        o, lse = o[rows], lse[rows]
+    empty = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(lse), empty), "empty requests must give lse = -inf"
+    err_o = np.abs(o - ref_o).max() if o.size else 0.0
+    err_l = np.abs(lse[~empty] - ref_lse[~empty]).max() if (~empty).any() else 0.0
+    assert err_o <= tol, f"max |o - oracle| = {err_o:.3g} > {tol}"
+    assert err_l <= tol, f"max |lse - oracle| = {err_l:.3g} > {tol}"
+    return err_o, err_l
+
+
+def check_coverage(p, b):
+    _, seg, _ = p.work()
+    from tests.test_planner import expand
+    np.testing.assert_array_equal(expand(seg), oracle.expected_coverage(b.indptr.numpy(),
+                                                                        b.num_kv_heads))
+
+
+# ------------------------------------------------------------------ small, element by element
+
+def test_tiny_workload(lib, cuda):
+    b = W.make_config_batch("tiny", device=cuda)
+    p, o, lse = run_lib(lib, b)
+    check_coverage(p, b)
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, TOL[torch.float32])
+
+
+COMBOS = [(torch.float32, torch.float32), (torch.bfloat16, torch.bfloat16),
+          (torch.float16, torch.float16), (torch.bfloat16, torch.float8_e4m3fn),
+          (torch.float16, torch.float8_e4m3fn)]
+
+
+@pytest.mark.parametrize("q_dtype,kv_dtype", COMBOS, ids=lambda d: str(d).split(".")[-1])
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_small_shapes(lib, cuda, q_dtype, kv_dtype, head_dim, group):
+    """Ragged lengths over several pages with partial tails, a 1-token and an
+    empty request, spanning several CTAs and split units."""
+    Hkv = 2
+    lengths = [1, 0, 16, 17, 250, 1000, 33, 611]
+    b = W.make_batch(batch_lengths=lengths, num_qo_heads=Hkv * group, num_kv_heads=Hkv,
+                     head_dim=head_dim, q_dtype=q_dtype, kv_dtype=kv_dtype,
+                     seed=7 + head_dim + group, device=cuda, pool_pages=200)
+    p, o, lse = run_lib(lib, b)
+    check_coverage(p, b)
+    assert p.check() == 0
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, tol_for(b))
+
+
+def test_many_splits_and_merge(lib, cuda):
+    """One long request split over the whole grid plus short ones: exercises
+    the merge kernel across many partial slots."""
+    b = W.make_batch(batch_lengths=[9000, 3, 40], num_qo_heads=8, num_kv_heads=2, head_dim=128,
+                     q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, seed=3, device=cuda)
+    p, o, lse = run_lib(lib, b)
+    info = p.info
+    assert info["num_merge_units"] >= 2 and info["num_partial_slots"] > 10
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, TOL[torch.bfloat16])
+
+
+def test_shared_prefix_pages(lib, cuda):
+    """Requests that point at the same pages (prefix sharing) read them in place."""
+    b = W.make_batch(batch_lengths=[160, 160, 100], num_qo_heads=4, num_kv_heads=4, head_dim=64,
+                     q_dtype=torch.float32, kv_dtype=torch.float32, seed=5, device=cuda)
+    idx = b.indices.clone()
+    idx[10:16] = idx[0:6]          # request 1 reuses request 0's first 6 pages
+    b.indices = idx
+    p, o, lse = run_lib(lib, b)
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, TOL[torch.float32])
+
+
+def test_all_requests_empty(lib, cuda):
+    b = W.make_batch(batch_lengths=[0, 0, 0], num_qo_heads=4, num_kv_heads=2, head_dim=64,
+                     q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, seed=1, device=cuda,
+                     pool_pages=2)
+    p, o, lse = run_lib(lib, b)
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_deterministic_and_no_lse(lib, cuda):
+    b = W.make_batch(batch_lengths=[700, 5000, 64], num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                     q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, seed=11, device=cuda)
+    p, o1, l1 = run_lib(lib, b)
+    o2, l2 = p.run(b.q, b.paged_kv)
+    o3, l3 = p.run(b.q, b.paged_kv, return_lse=False)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3) and l3 is None
+
+
+def test_wrapper_api(lib, cuda):
+    """The plan/run wrapper in the shape the pages use it."""
+    b = W.make_batch(batch_lengths=[64] * 8, num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                     q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, seed=2, device=cuda)
+    ws = torch.zeros(128 * 1024 * 1024, dtype=torch.uint8, device=cuda)
+    w = lib.BatchDecodeWithPagedKVCacheWrapper(ws, "NHD")
+    w.plan(b.indptr.to(cuda), b.indices, b.last_page_len.to(cuda), 32, 8, 128, 16,
+           q_data_type=torch.bfloat16, kv_data_type=torch.bfloat16)
+    out = w.run(b.q, b.paged_kv)
+    torch.cuda.synchronize()
+    ref_o, _ = oracle_decode(b)
+    assert np.abs(out.float().cpu().numpy() - ref_o).max() <= TOL[torch.bfloat16]
+
+
+def test_workspace_too_small_rejected(lib, cuda):
+    b = W.make_batch(batch_lengths=[100] * 4, num_qo_heads=8, num_kv_heads=8, head_dim=64,
+                     q_dtype=torch.float32, kv_dtype=torch.float32, seed=1, device=cuda)
+    ws = torch.zeros(256, dtype=torch.uint8, device=cuda)
+    with pytest.raises(lib.FaError) as e:
+        run_lib(lib, b, workspace=ws)
+    assert e.value.status == -3
+
+
+def test_unsupported_rejected(lib, cuda):
+    idx = torch.zeros(1, dtype=torch.int32, device=cuda)
+    with pytest.raises(lib.FaError) as e:
+        lib.plan([0, 1], idx, [1], 12, 4, 128, 16)      # group 3
+    assert e.value.status == -2
+    with pytest.raises(lib.FaError) as e:
+        lib.plan([0, 1], idx, [1], 8, 8, 96, 16)        # head_dim 96
+    assert e.value.status == -2
+    with pytest.raises(lib.FaError) as e:
+        lib.plan([0, 1], idx, [1], 8, 8, 128, 32)       # page_size 32
+    assert e.value.status == -2
+
+
+# ------------------------------------------------------------------ merge_states
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_merge_states(lib, cuda, dtype):
+    g = torch.Generator(device=cuda).manual_seed(4)
+    n, H, D = 37, 8, 128
+    oa = torch.randn((n, H, D), generator=g, device=cuda).to(dtype)
+    ob = torch.randn((n, H, D), generator=g, device=cuda).to(dtype)
+    la = torch.randn((n, H), generator=g, device=cuda) * 4
+    lb = torch.randn((n, H), generator=g, device=cuda) * 4
+    la[0, :3] = -math.inf
+    lb[0, 1:4] = -math.inf
+    o, l = lib.merge_states(oa, la, ob, lb)
+    torch.cuda.synchronize()
+    ro, rl = oracle.merge_states(oa.double().cpu().numpy(), la.double().cpu().numpy(),
+                                 ob.double().cpu().numpy(), lb.double().cpu().numpy())
+    tol = TOL[dtype]
+    assert np.abs(o.double().cpu().numpy() - ro).max() <= tol
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isneginf(l.cpu().numpy()), ~fin)
+    assert np.abs(l.double().cpu().numpy()[fin] - rl[fin]).max() <= 1e-5
+    # in place (outputs alias the a inputs)
+    lib.merge_states(oa, la, ob, lb, out=oa, lse_out=la)
+    torch.cuda.synchronize()
+    assert torch.equal(oa, o) and torch.equal(la, l)
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+def _sample_requests(b, k=6):
+    lens = b.lengths
+    order = np.argsort(lens, kind="stable")
+    picks = {int(order[0]), int(order[-1])}
+    rng = np.random.default_rng(0)
+    picks |= set(int(x) for x in rng.choice(len(lens), size=min(k, len(lens)), replace=False))
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("name", ["gqa_uniform", "ragged", "long_split", "fp8_kv"])
+def test_full_size_workloads_sampled(lib, cuda, name):
+    b = W.make_config_batch(name, device=cuda)
+    p, o, lse = run_lib(lib, b)
+    assert p.check() == 0
+    check_coverage(p, b)
+    rows = _sample_requests(b)
+    sb = sub_batch(b, rows)
+    ref_o, ref_lse = oracle_decode(sb)
+    compare(o, lse, ref_o, ref_lse, tol_for(b), rows=rows)
+    # properties that hold at any size, on every row
+    lse_all = lse.cpu()
+    assert torch.isfinite(lse_all).all()
+    assert torch.isfinite(o.float()).all()
+    del b, o, lse
+    torch.cuda.empty_cache()

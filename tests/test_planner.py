@@ -1,0 +1,136 @@
+"""Host planner (no GPU): the work list covers every (request, kv head, page)
+exactly once - bit-exact against the oracle's coverage definition - and
+balances pages across the persistent grid."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_fa_gb300 import workloads as W
+
+
+def expand(seg):
+    """(request, kv head, page position) triples a work list covers, sorted."""
+    if len(seg) == 0:
+        return np.zeros((0, 3), np.int64)
+    cnt = (seg[:, 3] - seg[:, 2]).astype(np.int64)
+    r = np.repeat(seg[:, 0].astype(np.int64), cnt)
+    h = np.repeat(seg[:, 1].astype(np.int64), cnt)
+    starts = np.repeat(seg[:, 2].astype(np.int64), cnt)
+    offs = np.arange(cnt.sum()) - np.repeat(np.cumsum(cnt) - cnt, cnt)
+    out = np.stack([r, h, starts + offs], axis=1)
+    order = np.lexsort((out[:, 2], out[:, 1], out[:, 0]))
+    return out[order]
+
+
+def check_work(lib, indptr, last, Hkv, max_ctas, min_pages=8, P=16):
+    cta, seg, mer, n_slots = lib.plan_work_host(indptr, last, Hkv, P, max_ctas, min_pages)
+    indptr = np.asarray(indptr, np.int64)
+    B = len(indptr) - 1
+    # coverage, bit-exact
+    want = oracle.expected_coverage(indptr, Hkv)
+    np.testing.assert_array_equal(expand(seg), want)
+    # every empty (request, head) still has exactly one empty segment
+    for i in np.nonzero(np.diff(indptr) == 0)[0]:
+        e = seg[(seg[:, 0] == i)]
+        assert len(e) == Hkv and np.all(e[:, 2] == e[:, 3]) and np.all(e[:, 5] == -1)
+    # CTA ranges partition the segments, in order
+    n_ctas = len(cta) - 1
+    assert cta[0] == 0 and cta[-1] == len(seg) and np.all(np.diff(cta) >= 0)
+    assert 1 <= n_ctas <= max_ctas
+    T = int(indptr[-1]) * Hkv
+    pages = np.array([(seg[cta[c]:cta[c + 1], 3] - seg[cta[c]:cta[c + 1], 2]).sum()
+                      for c in range(n_ctas)])
+    assert pages.sum() == T
+    if T:
+        quota = -(-T // n_ctas)
+        assert pages.max() <= quota
+        assert np.all(pages[:-1] == quota)     # all but the last CTA are full
+        assert n_ctas <= -(-T // min_pages)
+    # last_valid: the page that ends a request carries its last_page_len
+    for s in seg:
+        r, pe = s[0], s[3]
+        if s[2] < pe:
+            want_last = last[r] if pe == indptr[r + 1] else P
+            assert s[4] == want_last
+    # split units: slots are contiguous, cover the pieces in page order
+    slots_seen = []
+    for r, h, s0, ns in mer:
+        pieces = seg[(seg[:, 0] == r) & (seg[:, 1] == h)]
+        assert len(pieces) == ns >= 2
+        assert list(pieces[:, 5]) == list(range(s0, s0 + ns))
+        assert np.all(pieces[1:, 2] == pieces[:-1, 3])
+        slots_seen += list(range(s0, s0 + ns))
+    assert sorted(slots_seen) == list(range(n_slots))
+    unsplit = seg[seg[:, 5] < 0]
+    for r, h in unsplit[:, :2]:
+        assert ((seg[:, 0] == r) & (seg[:, 1] == h)).sum() == 1
+    assert n_slots <= 2 * n_ctas
+    return cta, seg, mer, n_slots
+
+
+def _table(lengths, P=16):
+    lengths = np.asarray(lengths, np.int64)
+    indptr, _, last, _ = W.page_table(lengths, P, None, torch.Generator().manual_seed(0), False)
+    return indptr.numpy(), last.numpy()
+
+
+@pytest.mark.parametrize("name", list(W.CONFIGS))
+def test_named_workloads_coverage(lib, name):
+    cfg = W.CONFIGS[name]
+    lengths = W.draw_lengths(cfg, torch.Generator().manual_seed(cfg.seed))
+    indptr, last = _table(lengths)
+    for max_ctas in (152 * 3, 152 * 2, 7):
+        check_work(lib, indptr, last, cfg.num_kv_heads, max_ctas)
+
+
+def test_random_batches(lib):
+    rng = np.random.default_rng(0)
+    for _ in range(60):
+        B = int(rng.integers(1, 40))
+        lengths = rng.integers(0, 700, size=B)
+        lengths[rng.random(B) < 0.15] = 0       # some empty requests
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        indptr, last = _table(lengths)
+        check_work(lib, indptr, last, Hkv, int(rng.integers(1, 500)), int(rng.integers(1, 20)))
+
+
+def test_all_empty_and_single_page(lib):
+    check_work(lib, *_table([0, 0, 0]), 2, 100)
+    check_work(lib, *_table([1]), 1, 100)
+    check_work(lib, *_table([16]), 4, 1)
+
+
+def test_deterministic(lib):
+    indptr, last = _table(np.random.default_rng(1).integers(1, 5000, size=50))
+    a = lib.plan_work_host(indptr, last, 8, 16, 456)
+    b = lib.plan_work_host(indptr, last, 8, 16, 456)
+    for x, y in zip(a[:3], b[:3]):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_long_request_spread_over_grid(lib):
+    """One 65536-token request with 32 kv heads fills every CTA (split-KV)."""
+    indptr, last = _table([65536])
+    cta, seg, mer, _ = check_work(lib, indptr, last, 32, 456)
+    assert len(cta) - 1 == 456
+    assert len(mer) == 32   # every (request, head) split
+
+
+@pytest.mark.parametrize("indptr,last", [
+    ([0, 2, 1], [16, 16]),      # decreasing
+    ([1, 2], [16]),             # indptr[0] != 0
+    ([0, 2], [0]),              # last_page_len below 1
+    ([0, 2], [17]),             # last_page_len above page_size
+])
+def test_rejects_malformed(lib, indptr, last):
+    with pytest.raises(lib.FaError) as e:
+        lib.plan_work_host(np.array(indptr), np.array(last), 2, 16, 10)
+    assert e.value.status == -1
+
+
+def test_rejects_bad_sizes(lib):
+    with pytest.raises(lib.FaError):
+        lib.plan_work_host(np.array([0, 1]), np.array([3]), 0, 16, 10)
+    with pytest.raises(lib.FaError):
+        lib.plan_work_host(np.array([0, 1]), np.array([3]), 1, 16, 0)
