@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Decode-attention benchmark: tokens/s and achieved HBM GB/s on one GB300.
+
+A step is one fa_decode_run over one resident batch: the split-KV decode
+kernel plus the merge kernel of split requests.  The plan (host work list,
+one host-to-device copy) is amortised per batch, as the plan/run split
+intends; it is timed separately and it is inside the end-to-end number.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--no-cpu-baseline]
+
+Prints one JSON line (rank 0).  Workloads are the seeded synthetic batches of
+paged_kv_decode_fa_gb300.workloads; the default is the GQA uniform batch
+(B=64, 32 qo / 8 kv heads, head_dim 128, 2048 tokens each, bf16).  With
+--impl reference the float64 CPU oracle is timed instead, on the host cores,
+over bounded samples of the same workload.  Under torchrun (N > 1) each rank
+runs an independent replica of the workload on its own GPU (the path has no
+exchange step); value is the tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_decode_fa_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode attention tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+DTYPE_NAMES = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16",
+               torch.float8_e4m3fn: "e4m3"}
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ helpers
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(b: W.DecodeBatch) -> int:
+    """Bytes any decode implementation must move for this batch: K and V of
+    every valid token and kv head, the page ids, q, o and lse."""
+    kv_es = b.paged_kv.element_size()
+    q_es = b.q.element_size()
+    kv = b.total_tokens * b.num_kv_heads * 2 * b.head_dim * kv_es
+    idx = int(b.indptr[-1]) * 4
+    qo = 2 * b.batch * b.num_qo_heads * b.head_dim * q_es
+    lse = b.batch * b.num_qo_heads * 4
+    return int(kv + idx + qo + lse)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_fa_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary of this
+    workload, if the summary was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_t = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+    m_h = re.search(r"^kernel_source_hash:\s*([0-9a-f]+)", text, re.M)
+    if not m_t or not m_h or m_h.group(1) != kernel_source_hash():
+        return None
+    return float(m_t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 50 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.perf_counter(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for t, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((t, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        window = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        which = "timed"
+        if not window:
+            window, which = rows, "warmup+timed"
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in window for i, v in enumerate(r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in window),
+                "sm_max_mhz": max(r[2] for r in window), "reasons": reasons,
+                "samples": len(window), "window": which}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def oracle_timing(b: W.DecodeBatch, target_s: float, max_requests: int | None = None):
+    """Time the float64 oracle on a sample of whole requests of b sized to take
+    about target_s seconds on all host cores.  Returns (requests, seconds,
+    tokens, threads, description)."""
+    import oracle
+    from tests.helpers import oracle_decode, sub_batch  # test-side marshalling
+    order = list(np.random.default_rng(0).permutation(b.batch))
+    one = sub_batch(b, order[:1])
+    t = time.perf_counter()
+    oracle_decode(one)
+    t1 = max(time.perf_counter() - t, 1e-4)
+    n = int(max(1, min(b.batch if max_requests is None else max_requests, target_s / t1)))
+    sb = sub_batch(b, order[:n])
+    t = time.perf_counter()
+    oracle_decode(sb)
+    dt = time.perf_counter() - t
+    threads = oracle.max_threads()
+    desc = (f"{n} of {b.batch} requests ({int(sb.lengths.sum())} KV tokens), seeded random "
+            f"choice, float64 C oracle, OpenMP {threads} threads")
+    return n, dt, int(sb.lengths.sum()), threads, desc
+
+
+# ------------------------------------------------------------------ arms
+
+def bench_reference(args, world, rank):
+    """The oracle as the reference arm: K timed steps, each a bounded sample."""
+    if rank != 0:
+        return None
+    b = W.make_config_batch(args.workload, device="cpu")
+    import oracle
+    from tests.helpers import oracle_decode, sub_batch
+    budget = 150.0
+    order = list(np.random.default_rng(0).permutation(b.batch))
+    one = sub_batch(b, order[:1])
+    t = time.perf_counter()
+    oracle_decode(one)
+    t1 = max(time.perf_counter() - t, 1e-4)
+    per_step = budget / max(1, args.steps + args.warmup)
+    n = int(max(1, min(b.batch, per_step / t1)))
+    sb = sub_batch(b, order[:n])
+    for _ in range(args.warmup):
+        oracle_decode(sb)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_decode(sb)
+    dt = time.perf_counter() - t
+    value = n * args.steps / dt
+    threads = oracle.max_threads()
+    cfg = W.CONFIGS[args.workload]
+    desc = f"{n} of {b.batch} requests per step, float64 C oracle, OpenMP {threads} threads"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(cfg, b),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def config_dict(cfg: W.DecodeConfig, b: W.DecodeBatch) -> dict:
+    return {"workload": cfg.name, "batch": b.batch, "num_qo_heads": cfg.num_qo_heads,
+            "num_kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim,
+            "page_size": cfg.page_size, "q_dtype": DTYPE_NAMES[cfg.q_dtype],
+            "kv_dtype": DTYPE_NAMES[cfg.kv_dtype],
+            "kv_tokens": b.total_tokens, "mean_seq_len": round(b.total_tokens / max(1, b.batch), 1),
+            "kv_bytes": int(b.total_tokens * cfg.num_kv_heads * 2 * cfg.head_dim *
+                            b.paged_kv.element_size()),
+            "l2": "inputs larger than L2 (129 MB): the KV read each step exceeds it",
+            "parallelism": "replicas (one independent batch per GPU)"}
+
+
+def bench_ours(args, world, rank, local):
+    import paged_kv_decode_fa_gb300 as fa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = W.CONFIGS[args.workload]
+    b = W.make_config_batch(args.workload, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # plan (amortised), timed on the host including its upload
+    torch.cuda.synchronize(dev)
+    t = time.perf_counter()
+    p = fa.plan(b.indptr, b.indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                b.head_dim, b.page_size, q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype)
+    torch.cuda.synchronize(dev)
+    plan_ms = (time.perf_counter() - t) * 1e3
+    info = p.info
+    o = torch.empty_like(b.q)
+    lse = torch.empty((b.batch, b.num_qo_heads), dtype=torch.float32, device=dev)
+    kw = dict(k_scale=b.k_scale, v_scale=b.v_scale, out=o, lse=lse)
+
+    for _ in range(args.warmup):
+        p.run(b.q, b.paged_kv, **kw)
+    torch.cuda.synchronize(dev)
+    if p.check() != 0:
+        raise RuntimeError("device check flagged the benchmark batch")
+
+    launches_per_step = 1 + (1 if info["num_merge_units"] > 0 else 0)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local).start()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    start.record(stream)
+    for i in range(args.steps):
+        p.set_timing_events(*evs[i])
+        p.run(b.q, b.paged_kv, **kw)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.perf_counter()
+    barrier(world)
+    p.set_timing_events(None, None)
+    clocks.stop()
+    elapsed_s = start.elapsed_time(end) / 1e3
+    elapsed_s = max_over_ranks(elapsed_s, world, dev)
+    kern_ms = [a.elapsed_time(z) for a, z in evs]
+    kern_avg_s = statistics.mean(kern_ms) / 1e3
+    kern_med_s = statistics.median(kern_ms) / 1e3
+
+    # end to end through the public API with host buffers: upload q and the
+    # page table from pinned memory, plan, run, read o and lse back
+    q_h = b.q.cpu().pin_memory()
+    idx_h = b.indices.cpu().pin_memory()
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    q_d = torch.empty_like(b.q)
+    idx_d = torch.empty_like(b.indices)
+    ws = torch.empty(fa.workspace_size(b.batch, b.num_qo_heads, b.num_kv_heads, b.head_dim),
+                     dtype=torch.uint8, device=dev)
+    indptr_h, last_h = b.indptr.numpy(), b.last_page_len.numpy()
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        idx_d.copy_(idx_h, non_blocking=True)
+        pe = fa.plan(indptr_h, idx_d, last_h, b.num_qo_heads, b.num_kv_heads, b.head_dim,
+                     b.page_size, q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype,
+                     workspace=ws)
+        pe.run(q_d, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale, out=o, lse=lse)
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        return pe
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(1, min(args.steps, 200))
+    barrier(world)
+    te = time.perf_counter()
+    for _ in range(e2e_steps):
+        pe = e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(time.perf_counter() - te, world, dev)
+    upload = pe.info["plan_upload_bytes"]
+    h2d = q_h.numel() * q_h.element_size() + idx_h.numel() * 4 + upload
+    d2h = o_h.numel() * o_h.element_size() + lse_h.numel() * 4
+    assert torch.equal(o_h, o.cpu()), "end-to-end output differs from the device run"
+
+    alg = algorithmic_bytes(b)
+    peak, peak_kind = read_peaks()
+    step_s = elapsed_s / args.steps
+    value = world * b.batch * args.steps / elapsed_s
+    achieved = alg / kern_avg_s / 1e9
+    traffic = profiled_traffic(args.workload)
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": DTYPE_NAMES[cfg.kv_dtype] if cfg.kv_dtype != torch.float8_e4m3fn else "e4m3",
+        "data": "synthetic", "config": config_dict(cfg, b),
+        "kv_tokens_per_s": world * b.total_tokens * args.steps / elapsed_s,
+        "hbm_gbs": alg / step_s / 1e9,
+        "hbm_frac_of_peak": alg / step_s / 1e9 / peak,
+        "peak_kind": peak_kind,
+        "plan_ms": plan_ms,
+        "decode_kernel_us": {"mean": kern_avg_s * 1e6, "median": kern_med_s * 1e6},
+        "plan": {k: info[k] for k in ("num_ctas", "ctas_per_sm", "num_segments",
+                                      "num_merge_units", "num_partial_slots", "stages",
+                                      "threads_per_cta", "smem_bytes_per_cta")},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "fa_decode_split_kernel",
+                     "algorithmic_bytes_per_launch": alg},
+        "e2e": {"value": world * b.batch * e2e_steps / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "steps": e2e_steps, "includes": "H2D q + indices, plan, run, D2H o + lse"},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clocks.summary(t0, t1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n, dt, toks, threads, desc = oracle_timing(b, target_s=args.cpu_seconds)
+        out["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": threads,
+                               "kind": "oracle", "sample": desc,
+                               "kv_tokens_per_s": toks / dt}
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=15)
+    ap.add_argument("--workload", default="gqa_uniform", choices=list(W.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        res = bench_reference(args, world, rank)
+    else:
+        res = bench_ours(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

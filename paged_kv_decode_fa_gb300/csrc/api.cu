@@ -363,6 +363,7 @@ int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info) {
   i.total_pages = plan->wl.total_pages;
   i.total_tokens = plan->wl.total_tokens;
   i.workspace_bytes_used = plan->layout.total;
+  i.plan_upload_bytes = plan->layout.meta_bytes;
   *info = i;
   return FA_OK;
 }

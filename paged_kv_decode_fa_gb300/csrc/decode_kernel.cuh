@@ -5,7 +5,12 @@
 //    page id from the index table and issues one 4-D TMA tensor copy per page
 //    that brings the page's K and V rows of one kv head ([2][16][D]) into a
 //    ring of S shared-memory stages, signalled through mbarriers;
-//  - warps 0..NW-1 (consumers) take the pages round-robin.  For each page a
+//  - warps 0..NW-1 (consumers) take the pages round-robin by their position
+//    k in the CTA's page stream: page k lands in stage k % S and is consumed by
+//    warp k % NW.  S is a multiple of NW, so every stage belongs to one warp,
+//    which waits on that stage's phases strictly in order (a parity wait can
+//    only tell the current phase from the previous one, so two consumers of
+//    one stage could mistake an old phase for a new one).  For each page a
 //    warp computes the scores of all G query heads of the kv head's group
 //    from one read of each K row (the tile is reused across the group), folds
 //    them into its running softmax state with the online-softmax recurrence,
@@ -288,8 +293,10 @@ struct DecodeCfg {
   static constexpr int HPL = LPR / G;   // lanes holding the same head's score
   static constexpr int ROW_BYTES = D * KV_ES;
   static constexpr int STAGE_BYTES = 2 * P * ROW_BYTES;
-  static constexpr int S0 = 49152 / STAGE_BYTES;
-  static constexpr int S = S0 < 4 ? 4 : (S0 > 16 ? 16 : S0);
+  // ring of about 64 KB, a whole number of stages per consumer warp
+  static constexpr int SPW0 = 65536 / STAGE_BYTES / NW;
+  static constexpr int SPW = SPW0 < 1 ? 1 : (SPW0 > 4 ? 4 : SPW0);
+  static constexpr int S = SPW * NW;
   static constexpr int THREADS = (NW + 1) * 32;
   static constexpr int OFF_FULL = S * STAGE_BYTES;
   static constexpr int OFF_EMPTY = OFF_FULL + 8 * S;
@@ -301,6 +308,7 @@ struct DecodeCfg {
   static_assert(LPR <= 32 && 32 % LPR == 0 && P % RPS == 0, "row mapping");
   static_assert(G <= LPR, "group size larger than lanes per row");
   static_assert(STAGE_BYTES % 128 == 0, "stage alignment");
+  static_assert(S % NW == 0, "each ring stage must belong to exactly one consumer warp");
 };
 
 template <typename QT, typename KVT, int D, int G, int NW>
@@ -402,8 +410,9 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
     }
     float m_l = -INFINITY, d_l = 0.f;
 
-    for (int lp = warp; lp < npg; lp += NW) {
-      const int k = kbase + lp;
+    // this warp's pages of the segment: stream positions k with k % NW == warp
+    for (int k = kbase + (warp - kbase % NW + NW) % NW; k < kbase + npg; k += NW) {
+      const int lp = k - kbase;
       const int stage = k % S;
       dev::mbar_wait(dev::smem_addr(&full[stage]), (uint32_t)((k / S) & 1), aborted, p.err);
       const uint8_t* kt = ring + stage * C::STAGE_BYTES;
