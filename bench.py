@@ -287,6 +287,13 @@ def bench_ours(args, world, rank, local):
     launches_per_step = 1 + (1 if info["num_merge_units"] > 0 else 0)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
+    # torch creates an event at its first record and only then reports
+    # elapsed times; the library re-records the same events around the
+    # decode kernel of each timed step.
+    for a, z in evs:
+        a.record(stream)
+        z.record(stream)
+    torch.cuda.synchronize(dev)
     clocks = ClockSampler(local).start()
     time.sleep(0.3)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

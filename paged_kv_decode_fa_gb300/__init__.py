@@ -219,7 +219,13 @@ class DecodePlan:
         return int(flags.value)
 
     def set_timing_events(self, before, after) -> None:
-        """Record torch.cuda.Events around the decode kernel of later runs (None = off)."""
+        """Record torch.cuda.Events around the decode kernel of later runs (None = off).
+
+        torch creates an event lazily at its first record, so record each
+        event once from torch before handing it over."""
+        for ev in (before, after):
+            if ev is not None and not ev.cuda_event:
+                raise ValueError("record the torch.cuda.Event once before passing it")
         b = ctypes.c_void_p(before.cuda_event) if before is not None else None
         a = ctypes.c_void_p(after.cuda_event) if after is not None else None
         _check(_L().fa_decode_set_timing_events(self._h, b, a), "fa_decode_set_timing_events")
