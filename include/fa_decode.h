@@ -215,6 +215,45 @@ int fa_decode_check(fa_decode_plan_t plan, void* cuda_stream, int* flags);
 int fa_decode_set_timing_events(fa_decode_plan_t plan, void* ev_before,
                                 void* ev_after);
 
+/* Decode one batch without allocating any device memory.
+ *
+ * The paper has no counterpart to this call; it exists for callers that
+ * cannot allocate: code handed only input and output pointers by a host
+ * framework that owns every device buffer through its own pool, allocator or
+ * out-of-memory callbacks, and latency-critical loops where cudaMalloc (which
+ * may synchronise the whole device) is not acceptable.  It does what
+ * fa_decode_plan followed by fa_decode_run does, with the workspace replaced
+ * by a fixed array of FA_STATIC_SCRATCH_BYTES that the library keeps on every
+ * GPU that loads it, for the life of the process.
+ *
+ * Arguments are those of fa_decode_plan (page table, shapes, dtypes) and of
+ * fa_decode_run (q, paged_kv, num_pages, scales, o, lse, stream), with the
+ * same layouts and ownership; indices_dev must stay valid until the work
+ * enqueued on cuda_stream has finished.  No plan handle is returned: every
+ * call plans again on the host.
+ *
+ *  - The first call on a device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - Every call on a device shares the one array: calls whose GPU work
+ *    overlaps (different streams, or host threads without ordering) race on
+ *    it and give wrong results.  Calls in one stream are ordered and safe.
+ *  - The work list, including the device-check word, is rewritten by each
+ *    call, so nothing left by an earlier call is read.
+ *  - A batch whose plan needs more than FA_STATIC_SCRATCH_BYTES (about
+ *    (batch * num_kv_heads + CTAs) * 32 bytes of work list plus up to
+ *    2 * CTAs * (num_qo_heads / num_kv_heads) * (head_dim + 1) * 4 bytes of
+ *    partial states) is refused with FA_ERR_WORKSPACE_TOO_SMALL before
+ *    anything is launched; use fa_decode_plan with a larger workspace then.
+ * Errors: those of fa_decode_plan and fa_decode_run. */
+#define FA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int fa_decode_static(const int32_t* indptr_host, const int32_t* indices_dev,
+                     const int32_t* last_page_len_host, int batch,
+                     int num_qo_heads, int num_kv_heads, int head_dim,
+                     int page_size, fa_dtype q_dtype, fa_dtype kv_dtype,
+                     const void* q, const void* paged_kv, int64_t num_pages,
+                     float sm_scale, float k_scale, float v_scale, void* o,
+                     float* lse, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -33,7 +33,7 @@ EXPORTED_SYMBOLS = (
     "fa_status_string", "fa_decode_workspace_size", "fa_decode_plan",
     "fa_decode_run", "fa_merge_states", "fa_decode_plan_destroy",
     "fa_decode_plan_get_info", "fa_decode_plan_get_work", "fa_plan_work_host",
-    "fa_decode_check", "fa_decode_set_timing_events",
+    "fa_decode_check", "fa_decode_set_timing_events", "fa_decode_static",
 )
 
 FA_OK = 0
