@@ -374,10 +374,12 @@ def bench_ours(args, world, rank, local):
         "decode_kernel_us": {"mean": kern_avg_s * 1e6, "median": kern_med_s * 1e6},
         "plan": {k: info[k] for k in ("num_ctas", "ctas_per_sm", "num_segments",
                                       "num_merge_units", "num_partial_slots", "stages",
-                                      "threads_per_cta", "smem_bytes_per_cta")},
+                                      "threads_per_cta", "smem_bytes_per_cta",
+                                      "tensor_cores")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "fa_decode_split_kernel",
+                     "kernel": ("fa_decode_mma_kernel" if info["tensor_cores"]
+                                else "fa_decode_split_kernel"),
                      "algorithmic_bytes_per_launch": alg},
         "e2e": {"value": world * b.batch * e2e_steps / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),

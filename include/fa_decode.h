@@ -170,6 +170,7 @@ typedef struct {
   int64_t total_tokens;  /* sum of len over requests */
   size_t workspace_bytes_used;
   size_t plan_upload_bytes;   /* bytes fa_decode_plan copies host -> device */
+  int tensor_cores;           /* 1: per-page products on mma.sync, 0: CUDA cores */
 } fa_plan_info;
 
 int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info);

@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -57,12 +58,22 @@ int dtype_size(fa_dtype t) {
   return 0;
 }
 
+// FADECODE_KERNEL=simt keeps every plan on the CUDA-core consumer (for
+// comparisons); by default the tensor-core consumer is used where it applies.
+bool tensor_cores_allowed() {
+  const char* v = std::getenv("FADECODE_KERNEL");
+  return !(v && std::strcmp(v, "simt") == 0);
+}
+
 bool find_kernel(fa_dtype q, fa_dtype kv, int D, int G, DecodeKernel* k) {
-  if (q == FA_DTYPE_F32 && kv == FA_DTYPE_F32) return fadecode::find_kernel_f32(D, G, k);
-  if (q == FA_DTYPE_BF16 && kv == FA_DTYPE_BF16) return fadecode::find_kernel_bf16(D, G, k);
-  if (q == FA_DTYPE_F16 && kv == FA_DTYPE_F16) return fadecode::find_kernel_f16(D, G, k);
-  if (q == FA_DTYPE_BF16 && kv == FA_DTYPE_E4M3) return fadecode::find_kernel_bf16_e4m3(D, G, k);
-  if (q == FA_DTYPE_F16 && kv == FA_DTYPE_E4M3) return fadecode::find_kernel_f16_e4m3(D, G, k);
+  const bool mma = tensor_cores_allowed();
+  if (q == FA_DTYPE_F32 && kv == FA_DTYPE_F32) return fadecode::find_kernel_f32(D, G, mma, k);
+  if (q == FA_DTYPE_BF16 && kv == FA_DTYPE_BF16) return fadecode::find_kernel_bf16(D, G, mma, k);
+  if (q == FA_DTYPE_F16 && kv == FA_DTYPE_F16) return fadecode::find_kernel_f16(D, G, mma, k);
+  if (q == FA_DTYPE_BF16 && kv == FA_DTYPE_E4M3)
+    return fadecode::find_kernel_bf16_e4m3(D, G, mma, k);
+  if (q == FA_DTYPE_F16 && kv == FA_DTYPE_E4M3)
+    return fadecode::find_kernel_f16_e4m3(D, G, mma, k);
   return false;
 }
 
@@ -267,15 +278,18 @@ int fa_decode_run(fa_decode_plan_t plan, const void* q, const void* paged_kv, in
       case FA_DTYPE_E4M3: dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;
     }
     // [2*num_pages][P][Hkv][D], innermost first; one box = K and V rows of
-    // one kv head of one page.
+    // one kv head of one page (or of one 128-byte segment of those rows when
+    // the kernel stages them in 128-byte swizzle order).
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)P,
                           (cuuint64_t)(2 * num_pages)};
     cuuint64_t strides[3] = {(cuuint64_t)(D * es), (cuuint64_t)(Hkv * D * es),
                              (cuuint64_t)(P * Hkv * D * es)};
-    cuuint32_t box[4] = {(cuuint32_t)D, 1u, (cuuint32_t)P, 2u};
+    cuuint32_t box[4] = {(cuuint32_t)plan->kern.box_x, 1u, (cuuint32_t)P, 2u};
     cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     CUresult r = encode(&plan->tmap, dt, 4, const_cast<void*>(paged_kv), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        plan->kern.swizzle_128b ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -364,6 +378,7 @@ int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info) {
   i.total_tokens = plan->wl.total_tokens;
   i.workspace_bytes_used = plan->layout.total;
   i.plan_upload_bytes = plan->layout.meta_bytes;
+  i.tensor_cores = plan->kern.tensor_cores ? 1 : 0;
   *info = i;
   return FA_OK;
 }

@@ -1,9 +1,9 @@
 // Compiled instances of the split-KV decode kernel for q = __half, kv = __nv_fp8_e4m3
 // (one translation unit per dtype pair so the build runs in parallel).
-#include "decode_kernel.cuh"
+#include "decode_mma.cuh"
 
 namespace fadecode {
-bool find_kernel_f16_e4m3(int head_dim, int group, DecodeKernel* k) {
-  return find_kernel_for<__half, __nv_fp8_e4m3>(head_dim, group, k);
+bool find_kernel_f16_e4m3(int head_dim, int group, bool allow_mma, DecodeKernel* k) {
+  return find_kernel_for<__half, __nv_fp8_e4m3>(head_dim, group, allow_mma, k);
 }
 }  // namespace fadecode

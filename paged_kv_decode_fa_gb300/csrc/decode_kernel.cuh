@@ -281,6 +281,94 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[G], int c) {
 
 }  // namespace dev
 
+// Producer warp: walks the CTA's segments page by page, reads the page ids
+// through the index table (32 at a time) and issues, per page, BOXES 4-D TMA
+// tensor copies (box b starts at element b * BOX_X of a row and lands at
+// b * BOX_BYTES in the stage) completing on the stage's "full" barrier.  Page
+// k of the stream goes to stage k % S once the stage's previous page has been
+// released.  Ends by waiting (bounded) for its last copies to land.
+template <int S, int STAGE_BYTES, int BOXES, int BOX_X, int BOX_BYTES>
+__device__ __forceinline__ void produce_pages(const CUtensorMap* map, const DecodeParams& p,
+                                              int seg_begin, int seg_end, uint8_t* ring,
+                                              uint64_t* full, uint64_t* empty, int lane) {
+  bool aborted = false;
+  const uint64_t policy = dev::evict_first_policy();
+  int k = 0;
+  for (int si = seg_begin; si < seg_end; ++si) {
+    const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * si);
+    const int kvh = sa.y, pb = sa.z, pe = sa.w;
+    for (int p0 = pb; p0 < pe; p0 += 32) {
+      const int cnt = min(32, pe - p0);
+      int id = lane < cnt ? __ldg(p.indices + p0 + lane) : 0;
+      const bool bad = lane < cnt && (id < 0 || (int64_t)id >= p.num_pages);
+      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, 1);
+      for (int i = 0; i < cnt; ++i, ++k) {
+        const int page = __shfl_sync(0xffffffffu, id, i);
+        if (lane == 0) {
+          const int stage = k % S;
+          const uint32_t round = (uint32_t)(k / S);
+          dev::mbar_wait(dev::smem_addr(&empty[stage]), (round & 1u) ^ 1u, aborted, p.err);
+          const uint32_t fb = dev::smem_addr(&full[stage]);
+          dev::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          // Out-of-range ids (already flagged) land outside the tensor map
+          // and read zeros.
+#pragma unroll
+          for (int b = 0; b < BOXES; ++b)
+            dev::tma_load_4d(dev::smem_addr(ring + stage * STAGE_BYTES + b * BOX_BYTES), map,
+                             b * BOX_X, kvh, 0, 2 * page, fb, policy);
+        }
+      }
+    }
+  }
+  // No copy may still be landing in shared memory when the CTA exits (only
+  // possible if a consumer gave up waiting).
+  if (lane == 0) {
+    const int first = k > S ? k - S : 0;
+    for (int kk = first; kk < k; ++kk)
+      if (!dev::mbar_wait_bounded(dev::smem_addr(&full[kk % S]), (uint32_t)((kk / S) & 1)))
+        atomicOr(p.err, 2);
+  }
+}
+
+// Segment epilogue shared by the decode kernels: fold the NW warp states
+// (unnormalised o in mo[w][h][d] against the warp's max mm[w][h], sum
+// md[w][h], all log2 domain) with the merge rule and write either the final
+// o (q dtype) and lse, or an fp32 partial slot.  Runs on the NW*32 consumer
+// threads between two consumer barriers.
+template <typename QT, int D, int G, int NW>
+__device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const float* mo,
+                                                 const float* mm, const float* md, int req,
+                                                 int kvh, int out_slot) {
+  constexpr int CT = NW * 32;
+  QT* __restrict__ obase = static_cast<QT*>(p.o);
+  for (int e = threadIdx.x; e < G * D; e += CT) {
+    const int h = e / D, dd = e % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * G + h]);
+    float out = 0.f, lse2 = -INFINITY;
+    if (M != -INFINITY) {
+      float den = 0.f, num = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float sw = dev::fast_exp2(mm[w * G + h] - M);
+        den = fmaf(md[w * G + h], sw, den);
+        num = fmaf(mo[(w * G + h) * D + dd], sw, num);
+      }
+      out = num / den * p.v_scale;
+      lse2 = M + dev::fast_log2(den);
+    }
+    if (out_slot < 0) {
+      const size_t row = (size_t)req * p.num_qo_heads + kvh * G + h;
+      obase[row * D + dd] = dev::from_float<QT>(out);
+      if (dd == 0 && p.lse) p.lse[row] = lse2 * dev::kLn2;
+    } else {
+      p.part_o[((size_t)out_slot * G + h) * D + dd] = out;
+      if (dd == 0) p.part_lse[(size_t)out_slot * G + h] = lse2;
+    }
+  }
+}
+
 template <typename QT, typename KVT, int D, int G, int NW>
 struct DecodeCfg {
   static constexpr int P = kPageSize;
@@ -327,7 +415,6 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
   const int lane = threadIdx.x & 31;
   const int seg_begin = p.cta_offsets[blockIdx.x];
   const int seg_end = p.cta_offsets[blockIdx.x + 1];
-  bool aborted = false;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -339,41 +426,8 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
   __syncthreads();
 
   if (warp == NW) {
-    // ---------------- producer: page gather through the index table -------
-    const uint64_t policy = dev::evict_first_policy();
-    int k = 0;
-    for (int si = seg_begin; si < seg_end; ++si) {
-      const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * si);
-      const int kvh = sa.y, pb = sa.z, pe = sa.w;
-      for (int p0 = pb; p0 < pe; p0 += 32) {
-        const int cnt = min(32, pe - p0);
-        int id = lane < cnt ? __ldg(p.indices + p0 + lane) : 0;
-        const bool bad = lane < cnt && (id < 0 || (int64_t)id >= p.num_pages);
-        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, 1);
-        for (int i = 0; i < cnt; ++i, ++k) {
-          const int page = __shfl_sync(0xffffffffu, id, i);
-          if (lane == 0) {
-            const int stage = k % S;
-            const uint32_t round = (uint32_t)(k / S);
-            dev::mbar_wait(dev::smem_addr(&empty[stage]), (round & 1u) ^ 1u, aborted, p.err);
-            const uint32_t fb = dev::smem_addr(&full[stage]);
-            dev::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-            // Out-of-range ids (already flagged) land outside the tensor map
-            // and read zeros.
-            dev::tma_load_4d(dev::smem_addr(ring + stage * C::STAGE_BYTES), &kv_map, 0, kvh,
-                             0, 2 * page, fb, policy);
-          }
-        }
-      }
-    }
-    // Make sure no copy is still landing in shared memory when the CTA exits
-    // (only matters if a consumer gave up waiting).
-    if (lane == 0) {
-      const int first = k > S ? k - S : 0;
-      for (int kk = first; kk < k; ++kk)
-        if (!dev::mbar_wait_bounded(dev::smem_addr(&full[kk % S]), (uint32_t)((kk / S) & 1)))
-          atomicOr(p.err, 2);
-    }
+    produce_pages<S, C::STAGE_BYTES, 1, 0, C::STAGE_BYTES>(&kv_map, p, seg_begin, seg_end, ring,
+                                                          full, empty, lane);
     return;
   }
 
@@ -386,9 +440,9 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
   const int c = lane % LPR;   // column chunk
   const int hl = c / HPL;     // head whose score this lane ends up holding
   const QT* __restrict__ qbase = static_cast<const QT*>(p.q);
-  QT* __restrict__ obase = static_cast<QT*>(p.o);
   constexpr int CT = NW * 32;
 
+  bool aborted = false;  // a timed-out wait makes every later wait return at once
   int kbase = 0;
   for (int si = seg_begin; si < seg_end; ++si) {
     const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * si);
@@ -504,32 +558,7 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
     dev::named_barrier(1, CT);
 
     // Merge the NW warp states of this segment and emit.
-    for (int e = threadIdx.x; e < G * D; e += CT) {
-      const int h = e / D, dd = e % D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * G + h]);
-      float out = 0.f, lse2 = -INFINITY;
-      if (M != -INFINITY) {
-        float den = 0.f, num = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float sw = dev::fast_exp2(mm[w * G + h] - M);
-          den = fmaf(md[w * G + h], sw, den);
-          num = fmaf(mo[(w * G + h) * D + dd], sw, num);
-        }
-        out = num / den * p.v_scale;
-        lse2 = M + dev::fast_log2(den);
-      }
-      if (out_slot < 0) {
-        const size_t row = (size_t)req * p.num_qo_heads + kvh * G + h;
-        obase[row * D + dd] = dev::from_float<QT>(out);
-        if (dd == 0 && p.lse) p.lse[row] = lse2 * dev::kLn2;
-      } else {
-        p.part_o[((size_t)out_slot * G + h) * D + dd] = out;
-        if (dd == 0) p.part_lse[(size_t)out_slot * G + h] = lse2;
-      }
-    }
+    combine_and_emit<QT, D, G, NW>(p, mo, mm, md, req, kvh, out_slot);
     dev::named_barrier(1, CT);
     kbase += npg;
   }
@@ -574,20 +603,9 @@ inline void fill_kernel(DecodeKernel* k) {
   k->stage_bytes = C::STAGE_BYTES;
   k->group = G;
   k->head_dim = D;
-}
-
-// Dispatch over the compiled head_dim x group grid for one dtype pair.
-template <typename QT, typename KVT>
-inline bool find_kernel_for(int head_dim, int group, DecodeKernel* k) {
-#define FA_CASE(DD, GG)                       \
-  if (head_dim == DD && group == GG) {        \
-    fill_kernel<QT, KVT, DD, GG>(k);          \
-    return true;                              \
-  }
-  FA_CASE(64, 1) FA_CASE(64, 2) FA_CASE(64, 4) FA_CASE(64, 8)
-  FA_CASE(128, 1) FA_CASE(128, 2) FA_CASE(128, 4) FA_CASE(128, 8)
-#undef FA_CASE
-  return false;
+  k->box_x = D;
+  k->swizzle_128b = false;
+  k->tensor_cores = false;
 }
 
 }  // namespace fadecode

@@ -1,0 +1,478 @@
+// Split-KV paged decode with the per-page products on the tensor cores
+// (mma.sync m16n8k16, fp32 accumulate), for groups of 2..8 query heads per
+// kv head over 16-bit or E4M3 KV.
+//
+// Same pipeline, planner contract and epilogue as fa_decode_split_kernel
+// (decode_kernel.cuh); only the consumer arithmetic differs.  With a group
+// of G heads a page is a tiny contraction - scores S^T[16 tokens x G] =
+// K[16 x D] . q^T, then O^T[D x G] += V^T[D x 16] . P^T - and doing it as
+// per-lane FMAs with shuffle reductions costs about 1100 warp instructions
+// per (page, kv head) at G = 4, which keeps the issue slots busy enough to
+// cap the HBM rate.  Here each page costs D/16 MMAs for the scores and D/16
+// for P.V, with tokens on the M side (no padding whatever G is):
+//
+//  - the stage holds each 128-byte row segment of K/V in TMA "128B swizzle"
+//    order (16-byte granule c of row r stored at c ^ (r & 7)), one box per
+//    128 bytes of row, so that both fragment loads below are free of bank
+//    conflicts;
+//  - scores: lane (g, t) loads K rows g and g+8, granules 2t and 2t+1 of each
+//    row segment, with 128-bit loads; the reduction index of the MMA is
+//    permuted so that these are exactly the lane's A-fragment elements, and
+//    q's B fragment (held in registers for the whole segment) uses the same
+//    permutation; E4M3 K is widened to f16 in registers;
+//  - softmax on the C fragment (tokens g, g+8 x heads 2t, 2t+1): column max
+//    and sum over the 8 lanes of a column with three shuffles each;
+//  - P.V: P is rounded to the MMA type, transposed through a 256-byte
+//    per-warp buffer into B fragments, V^T fragments come straight from the
+//    stage with ldmatrix.trans (for E4M3, pairs of bytes are transposed as
+//    16-bit elements and split with one byte permute).
+#pragma once
+#include "decode_kernel.cuh"
+
+namespace fadecode {
+namespace mma {
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (kBf16)
+    mma_bf16(c, a0, a1, a2, a3, b0, b1);
+  else
+    mma_f16(c, a0, a1, a2, a3, b0, b1);
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// Two E4M3 codes (low byte first) -> f16x2 (low half first), exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  const __half2_raw h =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
+  if (bf16) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float2 unpack2(uint32_t w, bool bf16) {
+  if (bf16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  __half2 h;
+  memcpy(&h, &w, sizeof h);
+  return __half22float2(h);
+}
+
+}  // namespace mma
+
+template <typename QT, typename KVT, int D, int G, int NW>
+struct MmaCfg {
+  static constexpr int P = kPageSize;
+  static constexpr int KV_ES = sizeof(KVT);
+  static constexpr bool kFp8 = KV_ES == 1;
+  // MMA operand type: bf16 for bf16 KV, f16 for f16 and E4M3 KV.
+  static constexpr bool kBf16 = std::is_same<KVT, __nv_bfloat16>::value;
+  static constexpr int ROW_BYTES = D * KV_ES;
+  static constexpr int SEGS = ROW_BYTES / 128;    // 128-byte row segments = TMA boxes
+  static constexpr int BOX_X = 128 / KV_ES;       // elements per box row
+  static constexpr int BOX_BYTES = 2 * P * 128;   // K and V rows of one segment
+  static constexpr int STAGE_BYTES = SEGS * BOX_BYTES;
+  static constexpr int E = 16 / KV_ES;            // elements per 16-byte granule
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int MTILES = D / 16;
+  // ring of 64 KB (48 KB at G = 8, whose larger epilogue buffer would
+  // otherwise leave room for only two CTAs per SM), whole stages per warp
+  static constexpr int RING_BYTES = G >= 8 ? 49152 : 65536;
+  static constexpr int SPW0 = RING_BYTES / STAGE_BYTES / NW;
+  static constexpr int SPW = SPW0 < 1 ? 1 : (SPW0 > 4 ? 4 : SPW0);
+  static constexpr int S = SPW * NW;
+  static constexpr int THREADS = (NW + 1) * 32;
+  static constexpr int OFF_FULL = S * STAGE_BYTES;
+  static constexpr int OFF_EMPTY = OFF_FULL + 8 * S;
+  static constexpr int OFF_PT = OFF_EMPTY + 8 * S;          // [NW][8 heads][16 tokens] 16-bit
+  static constexpr int OFF_MO = OFF_PT + NW * 8 * P * 2;
+  static constexpr int OFF_MM = OFF_MO + 4 * NW * G * D;
+  static constexpr int OFF_MD = OFF_MM + 4 * NW * G;
+  static constexpr int SMEM = OFF_MD + 4 * NW * G;
+  static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte swizzle rows");
+  static_assert(G >= 1 && G <= 8, "group of at most 8 heads (the MMA N side)");
+  static_assert(STAGE_BYTES % 1024 == 0, "swizzled boxes need 1024-byte alignment");
+  static_assert(S % NW == 0, "each ring stage must belong to exactly one consumer warp");
+  static_assert(!kFp8 || D % 32 == 0, "E4M3 V is transposed two granules at a time");
+};
+
+template <typename QT, typename KVT, int D, int G, int NW>
+__global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW>::THREADS)
+    fa_decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
+  using C = MmaCfg<QT, KVT, D, G, NW>;
+  constexpr int P = C::P, S = C::S, SEGS = C::SEGS, KSTEPS = C::KSTEPS, MTILES = C::MTILES;
+  constexpr bool kBf16 = C::kBf16, kFp8 = C::kFp8;
+  static_assert(kBf16 ? std::is_same<QT, __nv_bfloat16>::value
+                      : (std::is_same<QT, __half>::value || kFp8),
+                "q type must match the MMA type (or be widened for E4M3 KV)");
+  // bf16 q with E4M3 KV runs the MMA in f16: q is scaled by a power of two
+  // per segment to sit well inside the f16 range.
+  constexpr bool kConvertQ = kFp8 && std::is_same<QT, __nv_bfloat16>::value;
+
+  // Swizzled TMA destinations must sit on 1024-byte boundaries: the launch
+  // reserves 1 KB more than the layout so the base can be rounded up.
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (dev::smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_FULL);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + C::OFF_EMPTY);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int seg_begin = p.cta_offsets[blockIdx.x];
+  const int seg_end = p.cta_offsets[blockIdx.x + 1];
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      dev::mbar_init(dev::smem_addr(&full[s]), 1);
+      dev::mbar_init(dev::smem_addr(&empty[s]), 1);
+    }
+    dev::fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == NW) {
+    produce_pages<S, C::STAGE_BYTES, SEGS, C::BOX_X, C::BOX_BYTES>(&kv_map, p, seg_begin, seg_end,
+                                                                   ring, full, empty, lane);
+    return;
+  }
+
+  uint16_t* pT = reinterpret_cast<uint16_t*>(smem + C::OFF_PT) + warp * 8 * P;
+  float* mo = reinterpret_cast<float*>(smem + C::OFF_MO);
+  float* mm = reinterpret_cast<float*>(smem + C::OFF_MM);
+  float* md = reinterpret_cast<float*>(smem + C::OFF_MD);
+  const int g = lane >> 2;  // MMA group id: token row g (and g+8), q/P head g
+  const int t = lane & 3;   // thread in group: heads 2t, 2t+1 of the C fragment
+  const QT* __restrict__ qbase = static_cast<const QT*>(p.q);
+  constexpr int CT = NW * 32;
+  const uint32_t ring_addr = dev::smem_addr(ring);
+
+  bool aborted = false;  // a timed-out wait makes every later wait return at once
+  int kbase = 0;
+  for (int si = seg_begin; si < seg_end; ++si) {
+    const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * si);
+    const int4 sb = *reinterpret_cast<const int4*>(p.segments + 8 * si + 4);
+    const int req = sa.x, kvh = sa.y, npg = sa.w - sa.z;
+    const int last_valid = sb.x, out_slot = sb.y;
+
+    // ---- q as the B fragment of the score MMA, for the whole segment.
+    // Reduction step j uses, in lane t, the four dims base(j) .. base(j)+3:
+    // b0 <- dims base, base+1 and b1 <- base+2, base+3, where base(j) walks
+    // granules 2t and 2t+1 of each 128-byte row segment (the same elements
+    // the lane loads from K).
+    uint32_t qb[KSTEPS][2];
+    float qscale = p.q_scale;
+    {
+      float qf[KSTEPS][4];
+#pragma unroll
+      for (int j = 0; j < KSTEPS; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qf[j][e] = 0.f;
+      uint32_t raw[KSTEPS][2];
+      if (g < G) {
+        const QT* qrow = qbase + ((size_t)req * p.num_qo_heads + kvh * G + g) * D;
+        // Load L (16 bytes, 8 consecutive elements) feeds reduction steps 2L
+        // and 2L+1.  16-bit KV: step j = 4*seg + 2*half + u covers dims
+        // seg*BOX_X + (2t + half)*8 + 4u .. +3.  E4M3 KV: step j = 4*half + w
+        // covers dims (2t + half)*16 + 4w .. +3.
+#pragma unroll
+        for (int L = 0; L < KSTEPS / 2; ++L) {
+          int d0;
+          if constexpr (kFp8)
+            d0 = (2 * t + (L >> 1)) * 16 + (L & 1) * 8;
+          else
+            d0 = (L >> 1) * C::BOX_X + (2 * t + (L & 1)) * 8;
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qrow + d0));
+          raw[2 * L][0] = v.x;
+          raw[2 * L][1] = v.y;
+          raw[2 * L + 1][0] = v.z;
+          raw[2 * L + 1][1] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < KSTEPS; ++j) raw[j][0] = raw[j][1] = 0u;
+      }
+      if constexpr (kConvertQ) {
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < KSTEPS; ++j) {
+          const float2 lo = mma::unpack2(raw[j][0], true), hi = mma::unpack2(raw[j][1], true);
+          qf[j][0] = lo.x; qf[j][1] = lo.y; qf[j][2] = hi.x; qf[j][3] = hi.y;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(qf[j][e]));
+        }
+        const unsigned bits = __reduce_max_sync(0xffffffffu, __float_as_uint(amax));
+        int shift = 0;
+        if (bits != 0u && bits < 0x7f800000u) {
+          const int ex = (int)((bits >> 23) & 0xff) - 127;  // amax in [2^ex, 2^(ex+1))
+          shift = min(max(14 - ex, -120), 120);
+        }
+        const float up = ldexpf(1.f, shift);
+        qscale = p.q_scale * ldexpf(1.f, -shift);
+#pragma unroll
+        for (int j = 0; j < KSTEPS; ++j) {
+          qb[j][0] = mma::pack2(qf[j][0] * up, qf[j][1] * up, false);
+          qb[j][1] = mma::pack2(qf[j][2] * up, qf[j][3] * up, false);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < KSTEPS; ++j) {
+          qb[j][0] = raw[j][0];
+          qb[j][1] = raw[j][1];
+        }
+      }
+    }
+
+    float o[MTILES][4];
+#pragma unroll
+    for (int mt = 0; mt < MTILES; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
+    float m_h[2] = {-INFINITY, -INFINITY}, d_h[2] = {0.f, 0.f};
+
+    for (int k = kbase + (warp - kbase % NW + NW) % NW; k < kbase + npg; k += NW) {
+      const int lp = k - kbase;
+      const int stage = k % S;
+      dev::mbar_wait(dev::smem_addr(&full[stage]), (uint32_t)((k / S) & 1), aborted, p.err);
+      const uint32_t st = ring_addr + stage * C::STAGE_BYTES;
+      const int valid = (lp == npg - 1) ? last_valid : P;
+
+      // ---- scores S^T[token][head] = K . q^T (two accumulators to halve the chain)
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const int sw = g & 7;  // swizzle of rows g and g+8
+#pragma unroll
+      for (int sgi = 0; sgi < SEGS; ++sgi) {
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          const uint32_t gran = (uint32_t)(((2 * t + qq) ^ sw) * 16);
+          const uint4 ka = mma::lds128(st + sgi * C::BOX_BYTES + g * 128 + gran);
+          const uint4 kb = mma::lds128(st + sgi * C::BOX_BYTES + (g + 8) * 128 + gran);
+          const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w};
+          const uint32_t wb[4] = {kb.x, kb.y, kb.z, kb.w};
+          if constexpr (kFp8) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const int j = qq * 4 + w;
+              mma::mma16816<false>(sc[j & 1], mma::e4m3x2_to_f16x2(wa[w]),
+                                   mma::e4m3x2_to_f16x2(wb[w]),
+                                   mma::e4m3x2_to_f16x2(wa[w] >> 16),
+                                   mma::e4m3x2_to_f16x2(wb[w] >> 16), qb[j][0], qb[j][1]);
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int j = sgi * 4 + qq * 2 + u;
+              mma::mma16816<kBf16>(sc[j & 1], wa[2 * u], wb[2 * u], wa[2 * u + 1],
+                                   wb[2 * u + 1], qb[j][0], qb[j][1]);
+            }
+          }
+        }
+      }
+      float s[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[e] = (sc[0][e] + sc[1][e]) * qscale;
+      if (g >= valid) s[0] = s[1] = -INFINITY;
+      if (g + 8 >= valid) s[2] = s[3] = -INFINITY;
+
+      // ---- online softmax for heads 2t (s[0], s[2]) and 2t+1 (s[1], s[3])
+      float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
+        mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
+      }
+      float alpha[2], pr[4];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float mn = fmaxf(m_h[e], mx[e]);
+        alpha[e] = dev::fast_exp2(m_h[e] - mn);
+        m_h[e] = mn;
+      }
+      const uint32_t p01 = mma::pack2(dev::fast_exp2(s[0] - m_h[0]),
+                                      dev::fast_exp2(s[1] - m_h[1]), kBf16);
+      const uint32_t p23 = mma::pack2(dev::fast_exp2(s[2] - m_h[0]),
+                                      dev::fast_exp2(s[3] - m_h[1]), kBf16);
+      {
+        // sums from the rounded weights, so numerator and denominator agree
+        const float2 a = mma::unpack2(p01, kBf16), b = mma::unpack2(p23, kBf16);
+        pr[0] = a.x; pr[1] = a.y; pr[2] = b.x; pr[3] = b.y;
+      }
+      float ps[2] = {pr[0] + pr[2], pr[1] + pr[3]};
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        ps[0] += __shfl_xor_sync(0xffffffffu, ps[0], off);
+        ps[1] += __shfl_xor_sync(0xffffffffu, ps[1], off);
+      }
+      d_h[0] = d_h[0] * alpha[0] + ps[0];
+      d_h[1] = d_h[1] * alpha[1] + ps[1];
+      // P^T B fragments: transpose [token][head] -> [head][token] through smem
+      pT[(2 * t) * P + g] = (uint16_t)(p01 & 0xffffu);
+      pT[(2 * t + 1) * P + g] = (uint16_t)(p01 >> 16);
+      pT[(2 * t) * P + g + 8] = (uint16_t)(p23 & 0xffffu);
+      pT[(2 * t + 1) * P + g + 8] = (uint16_t)(p23 >> 16);
+#pragma unroll
+      for (int mt = 0; mt < MTILES; ++mt) {
+        o[mt][0] *= alpha[0];
+        o[mt][1] *= alpha[1];
+        o[mt][2] *= alpha[0];
+        o[mt][3] *= alpha[1];
+      }
+      // slots past the last valid token may hold anything (NaN included): a
+      // zero weight would not cancel them in the MMA, so clear those V rows
+      if (valid < P) {
+        const int per_row = 128 / 16;  // 16-byte stores per 128-byte row
+        const int n = (P - valid) * SEGS * per_row;
+        for (int i = lane; i < n; i += 32) {
+          const int r = valid + i / (SEGS * per_row);
+          const int rem = i % (SEGS * per_row);
+          const uint32_t a = st + (rem / per_row) * C::BOX_BYTES + (P + r) * 128 + (rem % per_row) * 16;
+          asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(a), "r"(0u) : "memory");
+        }
+        // order these generic-proxy stores before the TMA that refills the stage
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      __syncwarp();
+      const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pT + g * P + 2 * t);
+      const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(pT + g * P + 2 * t + 8);
+
+      // ---- O^T[dim][head] += V^T . P^T
+      if constexpr (kFp8) {
+#pragma unroll
+        for (int c2 = 0; c2 < MTILES / 2; ++c2) {
+          const int mi = lane >> 3, r = lane & 7;
+          const int gran = 2 * c2 + (mi >> 1), tok = (mi & 1) * 8 + r;
+          uint32_t d0, d1, d2, d3;
+          mma::ldsm_x4_trans(st + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16), d0, d1, d2, d3);
+          const uint32_t x0 = __byte_perm(d0, 0u, 0x3120), x1 = __byte_perm(d1, 0u, 0x3120);
+          const uint32_t x2 = __byte_perm(d2, 0u, 0x3120), x3 = __byte_perm(d3, 0u, 0x3120);
+          mma::mma16816<false>(o[2 * c2], mma::e4m3x2_to_f16x2(x0), mma::e4m3x2_to_f16x2(x0 >> 16),
+                               mma::e4m3x2_to_f16x2(x1), mma::e4m3x2_to_f16x2(x1 >> 16), pb0, pb1);
+          mma::mma16816<false>(o[2 * c2 + 1], mma::e4m3x2_to_f16x2(x2),
+                               mma::e4m3x2_to_f16x2(x2 >> 16), mma::e4m3x2_to_f16x2(x3),
+                               mma::e4m3x2_to_f16x2(x3 >> 16), pb0, pb1);
+        }
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < MTILES; ++mt) {
+          const int mi = lane >> 3, r = lane & 7;
+          const int sgi = (mt * 16) / C::BOX_X;
+          const int gran = ((mt * 16) % C::BOX_X) / 8 + (mi & 1);
+          const int tok = (mi >> 1) * 8 + r;
+          uint32_t a0, a1, a2, a3;
+          mma::ldsm_x4_trans(st + sgi * C::BOX_BYTES + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16),
+                             a0, a1, a2, a3);
+          mma::mma16816<kBf16>(o[mt], a0, a1, a2, a3, pb0, pb1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(dev::smem_addr(&empty[stage]));
+    }
+
+    // ---- this warp's state: O^T rows -> dims, heads 2t and 2t+1
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int h = 2 * t + e;
+      if (h < G) {
+#pragma unroll
+        for (int mt = 0; mt < MTILES; ++mt) {
+          const int dlo = kFp8 ? mt * 16 + 2 * g : mt * 16 + g;
+          const int dhi = kFp8 ? mt * 16 + 2 * g + 1 : mt * 16 + g + 8;
+          mo[(warp * G + h) * D + dlo] = o[mt][e];
+          mo[(warp * G + h) * D + dhi] = o[mt][2 + e];
+        }
+        if (g == 0) {
+          mm[warp * G + h] = m_h[e];
+          md[warp * G + h] = d_h[e];
+        }
+      }
+    }
+    dev::named_barrier(1, CT);
+    combine_and_emit<QT, D, G, NW>(p, mo, mm, md, req, kvh, out_slot);
+    dev::named_barrier(1, CT);
+    kbase += npg;
+  }
+}
+
+template <typename QT, typename KVT, int D, int G, int NW = 4>
+inline void fill_mma_kernel(DecodeKernel* k) {
+  using C = MmaCfg<QT, KVT, D, G, NW>;
+  k->func = reinterpret_cast<const void*>(&fa_decode_mma_kernel<QT, KVT, D, G, NW>);
+  k->merge_func = reinterpret_cast<const void*>(&fa_merge_partials_kernel<QT, D, G>);
+  k->threads = C::THREADS;
+  k->smem_bytes = C::SMEM + 1024;  // room to align the ring to 1024 bytes
+  k->stages = C::S;
+  k->stage_bytes = C::STAGE_BYTES;
+  k->group = G;
+  k->head_dim = D;
+  k->box_x = C::BOX_X;
+  k->swizzle_128b = true;
+  k->tensor_cores = true;
+}
+
+}  // namespace fadecode
+
+namespace fadecode {
+
+// Dispatch over the compiled head_dim x group grid for one dtype pair: the
+// tensor-core consumer where it applies and is allowed, the CUDA-core one
+// otherwise.
+template <typename QT, typename KVT>
+inline bool find_kernel_for(int head_dim, int group, bool allow_mma, DecodeKernel* k) {
+  constexpr bool kMmaTypes = sizeof(KVT) <= 2;
+#define FA_CASE(DD, GG)                                                              \
+  if (head_dim == DD && group == GG) {                                               \
+    if constexpr (kMmaTypes && GG >= 2 && (DD * sizeof(KVT)) % 128 == 0) {           \
+      if (allow_mma) {                                                               \
+        fill_mma_kernel<QT, KVT, DD, GG>(k);                                         \
+        return true;                                                                 \
+      }                                                                              \
+    }                                                                                \
+    fill_kernel<QT, KVT, DD, GG>(k);                                                 \
+    return true;                                                                     \
+  }
+  FA_CASE(64, 1) FA_CASE(64, 2) FA_CASE(64, 4) FA_CASE(64, 8)
+  FA_CASE(128, 1) FA_CASE(128, 2) FA_CASE(128, 4) FA_CASE(128, 8)
+#undef FA_CASE
+  return false;
+}
+
+}  // namespace fadecode

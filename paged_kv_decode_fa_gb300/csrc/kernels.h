@@ -46,14 +46,19 @@ struct DecodeKernel {
   int stage_bytes = 0;
   int group = 0;
   int head_dim = 0;
+  int box_x = 0;              // elements per TMA box row (D, or 128 bytes' worth)
+  bool swizzle_128b = false;  // stage rows in TMA 128-byte swizzle order
+  bool tensor_cores = false;  // per-page products on mma.sync
 };
 
-// Each returns false when the combination is not compiled.
-bool find_kernel_f32(int head_dim, int group, DecodeKernel* k);
-bool find_kernel_bf16(int head_dim, int group, DecodeKernel* k);
-bool find_kernel_f16(int head_dim, int group, DecodeKernel* k);
-bool find_kernel_bf16_e4m3(int head_dim, int group, DecodeKernel* k);
-bool find_kernel_f16_e4m3(int head_dim, int group, DecodeKernel* k);
+// Each returns false when the combination is not compiled.  allow_mma
+// selects the tensor-core consumer where it applies (group >= 2, 16-bit or
+// E4M3 KV, rows a multiple of 128 bytes); otherwise the CUDA-core one.
+bool find_kernel_f32(int head_dim, int group, bool allow_mma, DecodeKernel* k);
+bool find_kernel_bf16(int head_dim, int group, bool allow_mma, DecodeKernel* k);
+bool find_kernel_f16(int head_dim, int group, bool allow_mma, DecodeKernel* k);
+bool find_kernel_bf16_e4m3(int head_dim, int group, bool allow_mma, DecodeKernel* k);
+bool find_kernel_f16_e4m3(int head_dim, int group, bool allow_mma, DecodeKernel* k);
 
 // fa_merge_states kernels (merge.cu).
 int launch_merge_states(const void* o_a, const float* lse_a, const void* o_b,

@@ -71,12 +71,18 @@ COMBOS = [(torch.float32, torch.float32), (torch.bfloat16, torch.bfloat16),
           (torch.float16, torch.float8_e4m3fn)]
 
 
+@pytest.mark.parametrize("kernel", ["default", "simt"])
 @pytest.mark.parametrize("q_dtype,kv_dtype", COMBOS, ids=lambda d: str(d).split(".")[-1])
 @pytest.mark.parametrize("head_dim", [64, 128])
 @pytest.mark.parametrize("group", [1, 2, 4, 8])
-def test_small_shapes(lib, cuda, q_dtype, kv_dtype, head_dim, group):
+def test_small_shapes(lib, cuda, monkeypatch, q_dtype, kv_dtype, head_dim, group, kernel):
     """Ragged lengths over several pages with partial tails, a 1-token and an
-    empty request, spanning several CTAs and split units."""
+    empty request, spanning several CTAs and split units; on the default
+    consumer (tensor cores where they apply) and on the CUDA-core one."""
+    if kernel == "simt":
+        monkeypatch.setenv("FADECODE_KERNEL", "simt")
+    else:
+        monkeypatch.delenv("FADECODE_KERNEL", raising=False)
     Hkv = 2
     lengths = [1, 0, 16, 17, 250, 1000, 33, 611]
     b = W.make_batch(batch_lengths=lengths, num_qo_heads=Hkv * group, num_kv_heads=Hkv,
@@ -85,6 +91,9 @@ def test_small_shapes(lib, cuda, q_dtype, kv_dtype, head_dim, group):
     p, o, lse = run_lib(lib, b)
     check_coverage(p, b)
     assert p.check() == 0
+    mma_applies = (kernel == "default" and group >= 2 and kv_dtype != torch.float32
+                   and head_dim * b.paged_kv.element_size() % 128 == 0)
+    assert p.info["tensor_cores"] == int(mma_applies)
     ref_o, ref_lse = oracle_decode(b)
     compare(o, lse, ref_o, ref_lse, tol_for(b))
 
