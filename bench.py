@@ -284,7 +284,7 @@ def bench_ours(args, world, rank, local):
     if p.check() != 0:
         raise RuntimeError("device check flagged the benchmark batch")
 
-    launches_per_step = 1 + (1 if info["num_merge_units"] > 0 else 0)
+    launches_per_step = 1 + (1 if info["num_merge_units"] > 0 and not info["fused_merge"] else 0)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     # torch creates an event at its first record and only then reports
@@ -375,7 +375,7 @@ def bench_ours(args, world, rank, local):
         "plan": {k: info[k] for k in ("num_ctas", "ctas_per_sm", "num_segments",
                                       "num_merge_units", "num_partial_slots", "stages",
                                       "threads_per_cta", "smem_bytes_per_cta",
-                                      "tensor_cores")},
+                                      "tensor_cores", "fused_merge")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": ("fa_decode_mma_kernel" if info["tensor_cores"]

@@ -171,6 +171,7 @@ typedef struct {
   size_t workspace_bytes_used;
   size_t plan_upload_bytes;   /* bytes fa_decode_plan copies host -> device */
   int tensor_cores;           /* 1: per-page products on mma.sync, 0: CUDA cores */
+  int fused_merge;            /* 1: split requests merged inside the decode kernel */
 } fa_plan_info;
 
 int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info);
@@ -179,10 +180,11 @@ int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info);
  *  cta_offsets  [num_ctas+1]: CTA c runs segments cta_offsets[c] .. [c+1]-1
  *  segments     [num_segments * FA_SEGMENT_INTS] int32, each
  *               {request, kv_head, page_begin, page_end, last_valid,
- *                out_slot, 0, 0}; page_begin/page_end index the indices
- *               array, last_valid = valid slots of the segment's final page,
- *               out_slot = -1 when the segment covers its whole request,
- *               else the partial-state slot it writes.
+ *                out_slot, merge_unit, 0}; page_begin/page_end index the
+ *               indices array, last_valid = valid slots of the segment's
+ *               final page, out_slot = -1 when the segment covers its whole
+ *               request, else the partial-state slot it writes, and
+ *               merge_unit = its row of the merge table (-1 when unsplit).
  *  merge        [num_merge_units * FA_MERGE_INTS] int32, each
  *               {request, kv_head, first_slot, num_slots}. */
 #define FA_SEGMENT_INTS 8

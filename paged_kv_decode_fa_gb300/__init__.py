@@ -55,7 +55,7 @@ class PlanInfo(ctypes.Structure):
         "num_partial_slots", "threads_per_cta", "smem_bytes_per_cta", "stages")] + [
         ("total_pages", ctypes.c_int64), ("total_tokens", ctypes.c_int64),
         ("workspace_bytes_used", ctypes.c_size_t), ("plan_upload_bytes", ctypes.c_size_t),
-        ("tensor_cores", ctypes.c_int)]
+        ("tensor_cores", ctypes.c_int), ("fused_merge", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -31,9 +31,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t off_err, off_cta, off_seg, off_merge, meta_bytes, off_part_o, off_part_lse, total;
+  size_t off_err, off_cta, off_seg, off_merge, off_count, meta_bytes, off_part_o, off_part_lse,
+      total;
 };
 
+// Metadata (uploaded by every plan, zeros included) then the partial states.
 Layout make_layout(int64_t n_ctas, int64_t n_segments, int64_t n_merge, int64_t n_slots, int G,
                    int D) {
   Layout L;
@@ -41,7 +43,8 @@ Layout make_layout(int64_t n_ctas, int64_t n_segments, int64_t n_merge, int64_t 
   L.off_cta = align_up(L.off_err + sizeof(int));
   L.off_seg = align_up(L.off_cta + sizeof(int32_t) * (size_t)(n_ctas + 1));
   L.off_merge = align_up(L.off_seg + sizeof(fadecode::Segment) * (size_t)n_segments);
-  L.meta_bytes = align_up(L.off_merge + sizeof(fadecode::MergeUnit) * (size_t)n_merge);
+  L.off_count = align_up(L.off_merge + sizeof(fadecode::MergeUnit) * (size_t)n_merge);
+  L.meta_bytes = align_up(L.off_count + sizeof(int32_t) * (size_t)n_merge);
   L.off_part_o = L.meta_bytes;
   L.off_part_lse = align_up(L.off_part_o + sizeof(float) * (size_t)n_slots * G * D);
   L.total = align_up(L.off_part_lse + sizeof(float) * (size_t)n_slots * G);
@@ -56,6 +59,14 @@ int dtype_size(fa_dtype t) {
     case FA_DTYPE_E4M3: return 1;
   }
   return 0;
+}
+
+// FADECODE_MERGE=kernel folds split requests in a separate merge kernel
+// after the decode kernel (for comparisons); by default the last CTA to
+// finish a piece of a split request folds it inside the decode kernel.
+bool fused_merge_enabled() {
+  const char* v = std::getenv("FADECODE_MERGE");
+  return !(v && std::strcmp(v, "kernel") == 0);
 }
 
 // FADECODE_KERNEL=simt keeps every plan on the CUDA-core consumer (for
@@ -105,6 +116,7 @@ struct fa_decode_plan_s {
   uint8_t* ws = nullptr;
   size_t ws_bytes = 0;
   Layout layout{};
+  bool fused_merge = true;
   // cached TMA descriptor of the KV cache
   CUtensorMap tmap;
   const void* tmap_base = nullptr;
@@ -211,6 +223,7 @@ int fa_decode_plan(const int32_t* indptr_host, const int32_t* indices_dev,
   plan->indices = indices_dev;
   plan->ws = static_cast<uint8_t*>(workspace_dev);
   plan->ws_bytes = workspace_bytes;
+  plan->fused_merge = fused_merge_enabled();
 
   int rc = FA_OK;
   try {
@@ -286,11 +299,17 @@ int fa_decode_run(fa_decode_plan_t plan, const void* q, const void* paged_kv, in
                              (cuuint64_t)(P * Hkv * D * es)};
     cuuint32_t box[4] = {(cuuint32_t)plan->kern.box_x, 1u, (cuuint32_t)P, 2u};
     cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    // Promote L2 fills to the box row length: a longer promotion would pull
+    // in the neighbouring kv heads' rows, which another CTA reads much later.
+    const size_t row_bytes = (size_t)plan->kern.box_x * es;
+    const CUtensorMapL2promotion promo = row_bytes >= 256   ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                         : row_bytes >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                                            : CU_TENSOR_MAP_L2_PROMOTION_L2_64B;
     CUresult r = encode(&plan->tmap, dt, 4, const_cast<void*>(paged_kv), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,
                         plan->kern.swizzle_128b ? CU_TENSOR_MAP_SWIZZLE_128B
                                                 : CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        promo,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
       plan->tmap_base = nullptr;
@@ -311,6 +330,9 @@ int fa_decode_run(fa_decode_plan_t plan, const void* q, const void* paged_kv, in
   prm.part_o = reinterpret_cast<float*>(plan->ws + plan->layout.off_part_o);
   prm.part_lse = reinterpret_cast<float*>(plan->ws + plan->layout.off_part_lse);
   prm.err = reinterpret_cast<int*>(plan->ws + plan->layout.off_err);
+  prm.merge = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_merge);
+  prm.merge_count = reinterpret_cast<int*>(plan->ws + plan->layout.off_count);
+  prm.fused_merge = plan->fused_merge ? 1 : 0;
   prm.num_pages = num_pages;
   prm.num_qo_heads = plan->hq;
   prm.q_scale = sm_scale * k_scale * kLog2e;
@@ -323,7 +345,7 @@ int fa_decode_run(fa_decode_plan_t plan, const void* q, const void* paged_kv, in
                        (size_t)plan->kern.smem_bytes, st) != cudaSuccess)
     return FA_ERR_CUDA;
   if (timed && cudaEventRecord(plan->ev_after, st) != cudaSuccess) return FA_ERR_CUDA;
-  if (!plan->wl.merge.empty()) {
+  if (!plan->fused_merge && !plan->wl.merge.empty()) {
     MergeParams mp;
     mp.merge = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_merge);
     mp.part_o = prm.part_o;
@@ -379,6 +401,7 @@ int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info) {
   i.workspace_bytes_used = plan->layout.total;
   i.plan_upload_bytes = plan->layout.meta_bytes;
   i.tensor_cores = plan->kern.tensor_cores ? 1 : 0;
+  i.fused_merge = plan->fused_merge ? 1 : 0;
   *info = i;
   return FA_OK;
 }

@@ -338,7 +338,8 @@ __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const Deco
 template <typename QT, int D, int G, int NW>
 __device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const float* mo,
                                                  const float* mm, const float* md, int req,
-                                                 int kvh, int out_slot) {
+                                                 int kvh, int out_slot, int merge_unit,
+                                                 int* flag) {
   constexpr int CT = NW * 32;
   QT* __restrict__ obase = static_cast<QT*>(p.o);
   for (int e = threadIdx.x; e < G * D; e += CT) {
@@ -367,6 +368,44 @@ __device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const fl
       if (dd == 0) p.part_lse[(size_t)out_slot * G + h] = lse2;
     }
   }
+  if (out_slot < 0 || !p.fused_merge) return;
+  // Split unit: the CTA whose piece arrives last folds all pieces, in slot
+  // order, so the result does not depend on which CTA finished last.
+  __threadfence();  // this thread's partial writes before the arrival count
+  dev::named_barrier(1, CT);
+  if (threadIdx.x == 0) {
+    const int4 u = reinterpret_cast<const int4*>(p.merge)[merge_unit];
+    const int prev = atomicAdd(&p.merge_count[merge_unit], 1);
+    const int last = (prev == u.w - 1);
+    if (last) {
+      __threadfence();
+      p.merge_count[merge_unit] = 0;  // re-armed for the next run of the plan
+    }
+    *flag = last;
+  }
+  dev::named_barrier(1, CT);
+  if (!*flag) return;
+  const int4 u = reinterpret_cast<const int4*>(p.merge)[merge_unit];
+  const int s0 = u.z, ns = u.w;
+  for (int e = threadIdx.x; e < G * D; e += CT) {
+    const int h = e / D, dd = e % D;
+    float M = -INFINITY;
+    for (int k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(p.part_lse + (size_t)(s0 + k) * G + h));
+    float out = 0.f, lse2 = -INFINITY;
+    if (M != -INFINITY) {
+      float den = 0.f, num = 0.f;
+      for (int k = 0; k < ns; ++k) {
+        const float w = dev::fast_exp2(__ldcg(p.part_lse + (size_t)(s0 + k) * G + h) - M);
+        den += w;
+        num = fmaf(__ldcg(p.part_o + ((size_t)(s0 + k) * G + h) * D + dd), w, num);
+      }
+      out = num / den;
+      lse2 = M + dev::fast_log2(den);
+    }
+    const size_t row = (size_t)req * p.num_qo_heads + kvh * G + h;
+    obase[row * D + dd] = dev::from_float<QT>(out);
+    if (dd == 0 && p.lse) p.lse[row] = lse2 * dev::kLn2;
+  }
 }
 
 template <typename QT, typename KVT, int D, int G, int NW>
@@ -392,7 +431,8 @@ struct DecodeCfg {
   static constexpr int OFF_MO = OFF_P + 4 * NW * P * G;
   static constexpr int OFF_MM = OFF_MO + 4 * NW * G * D;
   static constexpr int OFF_MD = OFF_MM + 4 * NW * G;
-  static constexpr int SMEM = OFF_MD + 4 * NW * G;
+  static constexpr int OFF_FLAG = OFF_MD + 4 * NW * G;
+  static constexpr int SMEM = OFF_FLAG + 16;
   static_assert(LPR <= 32 && 32 % LPR == 0 && P % RPS == 0, "row mapping");
   static_assert(G <= LPR, "group size larger than lanes per row");
   static_assert(STAGE_BYTES % 128 == 0, "stage alignment");
@@ -558,7 +598,8 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
     dev::named_barrier(1, CT);
 
     // Merge the NW warp states of this segment and emit.
-    combine_and_emit<QT, D, G, NW>(p, mo, mm, md, req, kvh, out_slot);
+    combine_and_emit<QT, D, G, NW>(p, mo, mm, md, req, kvh, out_slot, sb.z,
+                                   reinterpret_cast<int*>(smem + C::OFF_FLAG));
     dev::named_barrier(1, CT);
     kbase += npg;
   }

@@ -127,7 +127,8 @@ struct MmaCfg {
   static constexpr int OFF_MO = OFF_PT + NW * 8 * P * 2;
   static constexpr int OFF_MM = OFF_MO + 4 * NW * G * D;
   static constexpr int OFF_MD = OFF_MM + 4 * NW * G;
-  static constexpr int SMEM = OFF_MD + 4 * NW * G;
+  static constexpr int OFF_FLAG = OFF_MD + 4 * NW * G;
+  static constexpr int SMEM = OFF_FLAG + 16;
   static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte swizzle rows");
   static_assert(G >= 1 && G <= 8, "group of at most 8 heads (the MMA N side)");
   static_assert(STAGE_BYTES % 1024 == 0, "swizzled boxes need 1024-byte alignment");
@@ -426,7 +427,8 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW>::THREADS)
       }
     }
     dev::named_barrier(1, CT);
-    combine_and_emit<QT, D, G, NW>(p, mo, mm, md, req, kvh, out_slot);
+    combine_and_emit<QT, D, G, NW>(p, mo, mm, md, req, kvh, out_slot, sb.z,
+                                   reinterpret_cast<int*>(smem + C::OFF_FLAG));
     dev::named_barrier(1, CT);
     kbase += npg;
   }

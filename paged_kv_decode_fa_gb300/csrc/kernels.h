@@ -21,6 +21,9 @@ struct DecodeParams {
   float* part_o;               // [slots, G, D] fp32, normalised partial outputs
   float* part_lse;             // [slots, G] fp32, log2-domain log-sum-exp
   int* err;                    // device-check word
+  const int32_t* merge;        // [n_merge * 4] {request, kv_head, first_slot, num_slots}
+  int* merge_count;            // [n_merge] arrivals per split unit, zero between runs
+  int fused_merge;             // 1: the last CTA of a split unit merges it
   int64_t num_pages;
   int num_qo_heads;
   float q_scale;  // sm_scale * k_scale * log2(e), folded into q

@@ -67,7 +67,7 @@ int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
     for (int h = 0; h < num_kv_heads; ++h) {
       if (np == 0) {
         const int64_t cta = std::min<int64_t>(pos / quota, num_ctas - 1);
-        wl.segments.push_back(Segment{i, h, pb, pb, page_size, -1, 0, 0});
+        wl.segments.push_back(Segment{i, h, pb, pb, page_size, -1, -1, 0});
         seg_cta.push_back((int32_t)cta);
         continue;
       }
@@ -78,15 +78,19 @@ int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
         const int64_t b = std::min(end, (cta + 1) * quota);
         const int32_t last = (b == end) ? last_page_len[i] : page_size;
         wl.segments.push_back(Segment{i, h, (int32_t)(pb + (a - start)),
-                                      (int32_t)(pb + (b - start)), last, -1, 0,
+                                      (int32_t)(pb + (b - start)), last, -1, -1,
                                       0});
         seg_cta.push_back((int32_t)cta);
         a = b;
       }
       const int pieces = (int)(wl.segments.size() - first);
       if (pieces > 1) {
+        const int unit = (int)wl.merge.size();
         wl.merge.push_back(MergeUnit{i, h, slots, pieces});
-        for (int k = 0; k < pieces; ++k) wl.segments[first + k].out_slot = slots + k;
+        for (int k = 0; k < pieces; ++k) {
+          wl.segments[first + k].out_slot = slots + k;
+          wl.segments[first + k].merge_unit = unit;
+        }
         slots += pieces;
       }
       pos = end;

@@ -98,14 +98,25 @@ def test_small_shapes(lib, cuda, monkeypatch, q_dtype, kv_dtype, head_dim, group
     compare(o, lse, ref_o, ref_lse, tol_for(b))
 
 
-def test_many_splits_and_merge(lib, cuda):
+@pytest.mark.parametrize("merge", ["fused", "kernel"])
+def test_many_splits_and_merge(lib, cuda, monkeypatch, merge):
     """One long request split over the whole grid plus short ones: exercises
-    the merge kernel across many partial slots."""
+    the split merge across many partial slots, done by the last CTA of each
+    split request (default) or by the separate merge kernel."""
+    if merge == "kernel":
+        monkeypatch.setenv("FADECODE_MERGE", "kernel")
+    else:
+        monkeypatch.delenv("FADECODE_MERGE", raising=False)
     b = W.make_batch(batch_lengths=[9000, 3, 40], num_qo_heads=8, num_kv_heads=2, head_dim=128,
                      q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, seed=3, device=cuda)
     p, o, lse = run_lib(lib, b)
     info = p.info
     assert info["num_merge_units"] >= 2 and info["num_partial_slots"] > 10
+    assert info["fused_merge"] == int(merge == "fused")
+    # the same plan again: the arrival counters must have been re-armed
+    o2, lse2 = p.run(b.q, b.paged_kv)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
     ref_o, ref_lse = oracle_decode(b)
     compare(o, lse, ref_o, ref_lse, TOL[torch.bfloat16])
 
@@ -130,7 +141,12 @@ def test_all_requests_empty(lib, cuda):
     assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
 
 
-def test_deterministic_and_no_lse(lib, cuda):
+@pytest.mark.parametrize("merge", ["fused", "kernel"])
+def test_deterministic_and_no_lse(lib, cuda, monkeypatch, merge):
+    if merge == "kernel":
+        monkeypatch.setenv("FADECODE_MERGE", "kernel")
+    else:
+        monkeypatch.delenv("FADECODE_MERGE", raising=False)
     b = W.make_batch(batch_lengths=[700, 5000, 64], num_qo_heads=32, num_kv_heads=8, head_dim=128,
                      q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, seed=11, device=cuda)
     p, o1, l1 = run_lib(lib, b)

@@ -55,14 +55,16 @@ def check_work(lib, indptr, last, Hkv, max_ctas, min_pages=8, P=16):
             assert s[4] == want_last
     # split units: slots are contiguous, cover the pieces in page order
     slots_seen = []
-    for r, h, s0, ns in mer:
+    for u, (r, h, s0, ns) in enumerate(mer):
         pieces = seg[(seg[:, 0] == r) & (seg[:, 1] == h)]
         assert len(pieces) == ns >= 2
         assert list(pieces[:, 5]) == list(range(s0, s0 + ns))
+        assert np.all(pieces[:, 6] == u)
         assert np.all(pieces[1:, 2] == pieces[:-1, 3])
         slots_seen += list(range(s0, s0 + ns))
     assert sorted(slots_seen) == list(range(n_slots))
     unsplit = seg[seg[:, 5] < 0]
+    assert np.all(unsplit[:, 6] == -1)
     for r, h in unsplit[:, :2]:
         assert ((seg[:, 0] == r) & (seg[:, 1] == h)).sum() == 1
     assert n_slots <= 2 * n_ctas
