@@ -371,10 +371,12 @@ __device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const fl
   if (out_slot < 0 || !p.fused_merge) return;
   // Split unit: the CTA whose piece arrives last folds all pieces, in slot
   // order, so the result does not depend on which CTA finished last.
-  __threadfence();  // this thread's partial writes before the arrival count
-  dev::named_barrier(1, CT);
+  dev::named_barrier(1, CT);  // all partial writes of this CTA done
   if (threadIdx.x == 0) {
     const int4 u = reinterpret_cast<const int4*>(p.merge)[merge_unit];
+    // one fence after the barrier publishes the whole CTA's writes (fences
+    // are cumulative) before the arrival is counted
+    __threadfence();
     const int prev = atomicAdd(&p.merge_count[merge_unit], 1);
     const int last = (prev == u.w - 1);
     if (last) {

@@ -74,11 +74,27 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-// Two E4M3 codes (low byte first) -> f16x2 (low half first), exact.
+// The two E4M3 codes in the low 16 bits (low byte first) -> f16x2 (low
+// half first), exact; one hardware conversion.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  const __half2_raw h =
-      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+  uint32_t out;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+      : "=r"(out)
+      : "r"(two_codes));
+  return out;
+}
+
+// Both halves of a word of four E4M3 codes -> two f16x2.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_codes, uint32_t& lo,
+                                                  uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_codes));
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
@@ -293,10 +309,10 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW>::THREADS)
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
               const int j = qq * 4 + w;
-              mma::mma16816<false>(sc[j & 1], mma::e4m3x2_to_f16x2(wa[w]),
-                                   mma::e4m3x2_to_f16x2(wb[w]),
-                                   mma::e4m3x2_to_f16x2(wa[w] >> 16),
-                                   mma::e4m3x2_to_f16x2(wb[w] >> 16), qb[j][0], qb[j][1]);
+              uint32_t a0, a1, a2, a3;
+              mma::e4m3x4_to_f16x2x2(wa[w], a0, a2);
+              mma::e4m3x4_to_f16x2x2(wb[w], a1, a3);
+              mma::mma16816<false>(sc[j & 1], a0, a1, a2, a3, qb[j][0], qb[j][1]);
             }
           } else {
 #pragma unroll
@@ -350,12 +366,15 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW>::THREADS)
       pT[(2 * t + 1) * P + g] = (uint16_t)(p01 >> 16);
       pT[(2 * t) * P + g + 8] = (uint16_t)(p23 & 0xffffu);
       pT[(2 * t + 1) * P + g + 8] = (uint16_t)(p23 >> 16);
+      // once the running maxima settle, most pages leave them unchanged
+      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-      for (int mt = 0; mt < MTILES; ++mt) {
-        o[mt][0] *= alpha[0];
-        o[mt][1] *= alpha[1];
-        o[mt][2] *= alpha[0];
-        o[mt][3] *= alpha[1];
+        for (int mt = 0; mt < MTILES; ++mt) {
+          o[mt][0] *= alpha[0];
+          o[mt][1] *= alpha[1];
+          o[mt][2] *= alpha[0];
+          o[mt][3] *= alpha[1];
+        }
       }
       // slots past the last valid token may hold anything (NaN included): a
       // zero weight would not cancel them in the MMA, so clear those V rows
@@ -383,13 +402,13 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW>::THREADS)
           const int gran = 2 * c2 + (mi >> 1), tok = (mi & 1) * 8 + r;
           uint32_t d0, d1, d2, d3;
           mma::ldsm_x4_trans(st + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16), d0, d1, d2, d3);
-          const uint32_t x0 = __byte_perm(d0, 0u, 0x3120), x1 = __byte_perm(d1, 0u, 0x3120);
-          const uint32_t x2 = __byte_perm(d2, 0u, 0x3120), x3 = __byte_perm(d3, 0u, 0x3120);
-          mma::mma16816<false>(o[2 * c2], mma::e4m3x2_to_f16x2(x0), mma::e4m3x2_to_f16x2(x0 >> 16),
-                               mma::e4m3x2_to_f16x2(x1), mma::e4m3x2_to_f16x2(x1 >> 16), pb0, pb1);
-          mma::mma16816<false>(o[2 * c2 + 1], mma::e4m3x2_to_f16x2(x2),
-                               mma::e4m3x2_to_f16x2(x2 >> 16), mma::e4m3x2_to_f16x2(x3),
-                               mma::e4m3x2_to_f16x2(x3 >> 16), pb0, pb1);
+          uint32_t a[4][2];
+          mma::e4m3x4_to_f16x2x2(__byte_perm(d0, 0u, 0x3120), a[0][0], a[0][1]);
+          mma::e4m3x4_to_f16x2x2(__byte_perm(d1, 0u, 0x3120), a[1][0], a[1][1]);
+          mma::e4m3x4_to_f16x2x2(__byte_perm(d2, 0u, 0x3120), a[2][0], a[2][1]);
+          mma::e4m3x4_to_f16x2x2(__byte_perm(d3, 0u, 0x3120), a[3][0], a[3][1]);
+          mma::mma16816<false>(o[2 * c2], a[0][0], a[0][1], a[1][0], a[1][1], pb0, pb1);
+          mma::mma16816<false>(o[2 * c2 + 1], a[2][0], a[2][1], a[3][0], a[3][1], pb0, pb1);
         }
       } else {
 #pragma unroll
