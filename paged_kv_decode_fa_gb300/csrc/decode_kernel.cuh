@@ -330,6 +330,68 @@ __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const Deco
   }
 }
 
+// Fold the partial states of one split unit u = {request, kv_head,
+// first_slot, num_slots} with the merge rule (log2 domain) and write o and
+// lse.  The per-head weights are computed once, in `scratch` (at least
+// num_slots * G floats, else a slower path reads the lse values per
+// element); then every output element issues its num_slots loads at once.
+// Runs on `nthreads` threads numbered `tid`, which synchronise on named
+// barrier `bar` (0 = __syncthreads).
+template <typename QT, int D, int G>
+__device__ __forceinline__ void fold_split_unit(const float* part_o, const float* part_lse,
+                                                int4 u, QT* obase, float* lse_out, int num_qo_heads,
+                                                float* scratch, int scratch_floats, int tid,
+                                                int nthreads, int bar) {
+  const int req = u.x, kvh = u.y, s0 = u.z, ns = u.w;
+  if (ns * G <= scratch_floats) {
+    // weights w[k][h] = 2^(lse_k - M_h) / den_h, and lse
+    for (int h = tid; h < G; h += nthreads) {
+      float M = -INFINITY;
+      for (int k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(part_lse + (size_t)(s0 + k) * G + h));
+      float den = 0.f;
+      if (M != -INFINITY)
+        for (int k = 0; k < ns; ++k) {
+          const float w = dev::fast_exp2(__ldcg(part_lse + (size_t)(s0 + k) * G + h) - M);
+          scratch[k * G + h] = w;
+          den += w;
+        }
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      for (int k = 0; k < ns; ++k) scratch[k * G + h] = M != -INFINITY ? scratch[k * G + h] * inv : 0.f;
+      if (lse_out)
+        lse_out[(size_t)req * num_qo_heads + kvh * G + h] =
+            M != -INFINITY ? (M + dev::fast_log2(den)) * dev::kLn2 : -INFINITY;
+    }
+    if (bar == 0) __syncthreads(); else dev::named_barrier(bar, nthreads);
+    for (int e = tid; e < G * D; e += nthreads) {
+      const int h = e / D, dd = e % D;
+      float num = 0.f;
+      for (int k = 0; k < ns; ++k)
+        num = fmaf(__ldcg(part_o + ((size_t)(s0 + k) * G + h) * D + dd), scratch[k * G + h], num);
+      obase[((size_t)req * num_qo_heads + kvh * G + h) * D + dd] = dev::from_float<QT>(num);
+    }
+    return;
+  }
+  for (int e = tid; e < G * D; e += nthreads) {
+    const int h = e / D, dd = e % D;
+    float M = -INFINITY;
+    for (int k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(part_lse + (size_t)(s0 + k) * G + h));
+    float out = 0.f, lse2 = -INFINITY;
+    if (M != -INFINITY) {
+      float den = 0.f, num = 0.f;
+      for (int k = 0; k < ns; ++k) {
+        const float w = dev::fast_exp2(__ldcg(part_lse + (size_t)(s0 + k) * G + h) - M);
+        den += w;
+        num = fmaf(__ldcg(part_o + ((size_t)(s0 + k) * G + h) * D + dd), w, num);
+      }
+      out = num / den;
+      lse2 = M + dev::fast_log2(den);
+    }
+    const size_t row = (size_t)req * num_qo_heads + kvh * G + h;
+    obase[row * D + dd] = dev::from_float<QT>(out);
+    if (dd == 0 && lse_out) lse_out[row] = lse2 * dev::kLn2;
+  }
+}
+
 // Segment epilogue shared by the decode kernels: fold the NW warp states
 // (unnormalised o in mo[w][h][d] against the warp's max mm[w][h], sum
 // md[w][h], all log2 domain) with the merge rule and write either the final
@@ -388,26 +450,8 @@ __device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const fl
   dev::named_barrier(1, CT);
   if (!*flag) return;
   const int4 u = reinterpret_cast<const int4*>(p.merge)[merge_unit];
-  const int s0 = u.z, ns = u.w;
-  for (int e = threadIdx.x; e < G * D; e += CT) {
-    const int h = e / D, dd = e % D;
-    float M = -INFINITY;
-    for (int k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(p.part_lse + (size_t)(s0 + k) * G + h));
-    float out = 0.f, lse2 = -INFINITY;
-    if (M != -INFINITY) {
-      float den = 0.f, num = 0.f;
-      for (int k = 0; k < ns; ++k) {
-        const float w = dev::fast_exp2(__ldcg(p.part_lse + (size_t)(s0 + k) * G + h) - M);
-        den += w;
-        num = fmaf(__ldcg(p.part_o + ((size_t)(s0 + k) * G + h) * D + dd), w, num);
-      }
-      out = num / den;
-      lse2 = M + dev::fast_log2(den);
-    }
-    const size_t row = (size_t)req * p.num_qo_heads + kvh * G + h;
-    obase[row * D + dd] = dev::from_float<QT>(out);
-    if (dd == 0 && p.lse) p.lse[row] = lse2 * dev::kLn2;
-  }
+  fold_split_unit<QT, D, G>(p.part_o, p.part_lse, u, obase, p.lse, p.num_qo_heads,
+                            const_cast<float*>(mo), NW * G * D, threadIdx.x, CT, 1);
 }
 
 template <typename QT, typename KVT, int D, int G, int NW>
@@ -607,32 +651,14 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
   }
 }
 
-// Split-level merge: one CTA per (request, kv head) that the planner split;
-// folds its partial states with the merge rule (all in the log2 domain).
+// Split-level merge as a separate kernel: one CTA per (request, kv head)
+// that the planner split folds its partial states with the merge rule.
 template <typename QT, int D, int G>
 __global__ void __launch_bounds__(128) fa_merge_partials_kernel(const MergeParams p) {
+  __shared__ float weights[2048];
   const int4 u = reinterpret_cast<const int4*>(p.merge)[blockIdx.x];
-  const int req = u.x, kvh = u.y, s0 = u.z, ns = u.w;
-  QT* obase = static_cast<QT*>(p.o);
-  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-    const int h = e / D, dd = e % D;
-    float M = -INFINITY;
-    for (int k = 0; k < ns; ++k) M = fmaxf(M, p.part_lse[(size_t)(s0 + k) * G + h]);
-    float out = 0.f, lse2 = -INFINITY;
-    if (M != -INFINITY) {
-      float den = 0.f, num = 0.f;
-      for (int k = 0; k < ns; ++k) {
-        const float w = dev::fast_exp2(p.part_lse[(size_t)(s0 + k) * G + h] - M);
-        den += w;
-        num = fmaf(p.part_o[((size_t)(s0 + k) * G + h) * D + dd], w, num);
-      }
-      out = num / den;
-      lse2 = M + dev::fast_log2(den);
-    }
-    const size_t row = (size_t)req * p.num_qo_heads + kvh * G + h;
-    obase[row * D + dd] = dev::from_float<QT>(out);
-    if (dd == 0 && p.lse) p.lse[row] = lse2 * dev::kLn2;
-  }
+  fold_split_unit<QT, D, G>(p.part_o, p.part_lse, u, static_cast<QT*>(p.o), p.lse,
+                            p.num_qo_heads, weights, 2048, threadIdx.x, blockDim.x, 0);
 }
 
 template <typename QT, typename KVT, int D, int G, int NW = 4>
