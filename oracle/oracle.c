@@ -98,13 +98,20 @@ static int64_t kv_offset(int64_t page, int kv, int slot, int kvh, int d, int P,
   return (((page * 2 + kv) * (int64_t)P + slot) * Hkv + kvh) * (int64_t)D + d;
 }
 
-/* Returns 0 on success, 1 on invalid arguments (nothing written then). */
-int oracle_batch_decode(const void* q, int q_dtype, const void* paged_kv,
-                        int kv_dtype, int64_t num_pages, const int32_t* indptr,
-                        const int32_t* indices, const int32_t* last_page_len,
-                        int B, int Hq, int Hkv, int D, int P, double sm_scale,
-                        double k_scale, double v_scale, double* o, double* lse,
-                        int num_threads) {
+/* Decode attention with dequantisation scales either per tensor (k_scale,
+ * v_scale) or, when k_scales / v_scales are given, per token and kv head:
+ * the stored K (V) element of page p, slot t, kv head h is multiplied by
+ * k_scales[(p * Hkv + h) * P + t] (v_scales likewise) - the row-wise dynamic
+ * FP8 scaling of the page "FlashInfer vs FlashAttention-3" (section
+ * "Production War Story: The FP8 Precision Underflow Failure").
+ * Returns 0 on success, 1 on invalid arguments (nothing written then). */
+static int decode_impl(const void* q, int q_dtype, const void* paged_kv,
+                       int kv_dtype, int64_t num_pages, const int32_t* indptr,
+                       const int32_t* indices, const int32_t* last_page_len,
+                       int B, int Hq, int Hkv, int D, int P, double sm_scale,
+                       double k_scale, double v_scale, const float* k_scales,
+                       const float* v_scales, double* o, double* lse,
+                       int num_threads) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || P <= 0 || Hq % Hkv) return 1;
   if (indptr[0] != 0) return 1;
   for (int i = 0; i < B; ++i) {
@@ -137,11 +144,13 @@ int oracle_batch_decode(const void* q, int q_dtype, const void* paged_kv,
     for (int64_t t = 0; t < len; ++t) {
       const int64_t page = indices[indptr[i] + t / P];
       const int slot = (int)(t % P);
+      const double ks =
+          k_scales ? (double)k_scales[(page * Hkv + kvh) * P + slot] : k_scale;
       double acc = 0.0;
       for (int d = 0; d < D; ++d) {
         double qd = load_elem(q, q_dtype, u * D + d);
-        double kd = k_scale * load_elem(paged_kv, kv_dtype,
-                                        kv_offset(page, 0, slot, kvh, d, P, Hkv, D));
+        double kd = ks * load_elem(paged_kv, kv_dtype,
+                                   kv_offset(page, 0, slot, kvh, d, P, Hkv, D));
         acc += qd * kd;
       }
       s[t] = sm_scale * acc;
@@ -157,9 +166,11 @@ int oracle_batch_decode(const void* q, int q_dtype, const void* paged_kv,
     for (int64_t t = 0; t < len; ++t) {
       const int64_t page = indices[indptr[i] + t / P];
       const int slot = (int)(t % P);
+      const double vs =
+          v_scales ? (double)v_scales[(page * Hkv + kvh) * P + slot] : v_scale;
       const double w = exp(s[t] - m);
       for (int d = 0; d < D; ++d)
-        out[d] += w * v_scale *
+        out[d] += w * vs *
                   load_elem(paged_kv, kv_dtype,
                             kv_offset(page, 1, slot, kvh, d, P, Hkv, D));
     }
@@ -168,6 +179,30 @@ int oracle_batch_decode(const void* q, int q_dtype, const void* paged_kv,
     free(s);
   }
   return 0;
+}
+
+int oracle_batch_decode(const void* q, int q_dtype, const void* paged_kv,
+                        int kv_dtype, int64_t num_pages, const int32_t* indptr,
+                        const int32_t* indices, const int32_t* last_page_len,
+                        int B, int Hq, int Hkv, int D, int P, double sm_scale,
+                        double k_scale, double v_scale, double* o, double* lse,
+                        int num_threads) {
+  return decode_impl(q, q_dtype, paged_kv, kv_dtype, num_pages, indptr, indices,
+                     last_page_len, B, Hq, Hkv, D, P, sm_scale, k_scale, v_scale,
+                     NULL, NULL, o, lse, num_threads);
+}
+
+/* Same with per-token, per-kv-head scales [num_pages, Hkv, P] for K and V. */
+int oracle_batch_decode_token_scales(
+    const void* q, int q_dtype, const void* paged_kv, int kv_dtype,
+    int64_t num_pages, const int32_t* indptr, const int32_t* indices,
+    const int32_t* last_page_len, int B, int Hq, int Hkv, int D, int P,
+    double sm_scale, const float* k_scales, const float* v_scales, double* o,
+    double* lse, int num_threads) {
+  if (!k_scales || !v_scales) return 1;
+  return decode_impl(q, q_dtype, paged_kv, kv_dtype, num_pages, indptr, indices,
+                     last_page_len, B, Hq, Hkv, D, P, sm_scale, 1.0, 1.0,
+                     k_scales, v_scales, o, lse, num_threads);
 }
 
 /* ---- merge of partial states -------------------------------------------- */

@@ -278,6 +278,61 @@ def pin_torch_dense(orc):
             np.testing.assert_allclose(lse[i], ref_lse, rtol=0, atol=1e-12)
 
 
+def _fp8_batch(seed, lens=(1, 9, 14, 33), Hq=4, Hkv=2, D=16, P=4):
+    gen = torch.Generator().manual_seed(seed)
+    npg = [(n + P - 1) // P for n in lens]
+    num_pages = sum(npg) + 2
+    kv = (torch.randn((num_pages, 2, P, Hkv, D), generator=gen) * 40).to(torch.float8_e4m3fn)
+    q = torch.randn((len(lens), Hq, D), generator=gen).to(torch.bfloat16)
+    perm = torch.randperm(num_pages, generator=gen)[: sum(npg)].to(torch.int32)
+    indptr = np.concatenate([[0], np.cumsum(npg)]).astype(np.int32)
+    last = np.array([n - (p - 1) * P for n, p in zip(lens, npg)], np.int32)
+    ks = (torch.rand((num_pages, Hkv, P), generator=gen) * 0.05 + 0.001).to(torch.float32)
+    vs = (torch.rand((num_pages, Hkv, P), generator=gen) * 0.05 + 0.001).to(torch.float32)
+    return kv, q, perm, indptr, last, ks, vs, lens, (Hq, Hkv, D, P)
+
+
+def pin_token_scales_dense(orc):
+    """Per-token, per-kv-head scales against torch float64 on the tensors
+    dequantised element by element with their own scale."""
+    from tests.helpers import as_bits
+    kv, q, perm, indptr, last, ks, vs, lens, (Hq, Hkv, D, P) = _fp8_batch(13)
+    qb, qc = as_bits(q)
+    kb, kc = as_bits(kv)
+    o, lse = orc.batch_decode_token_scales(qb, qc, kb, kc, indptr, perm.numpy(), last, Hq, Hkv,
+                                           D, P, ks.numpy(), vs.numpy())
+    kvd = kv.to(torch.float64)
+    # [pages, Hkv, P] -> [pages, P, Hkv, 1] to match [pages, 2, P, Hkv, D]
+    ksd = ks.to(torch.float64).permute(0, 2, 1).unsqueeze(-1)
+    vsd = vs.to(torch.float64).permute(0, 2, 1).unsqueeze(-1)
+    g = Hq // Hkv
+    for i, n in enumerate(lens):
+        ids = perm[indptr[i]:indptr[i + 1]].long()
+        Kd = (kvd[ids, 0] * ksd[ids]).reshape(-1, Hkv, D)[:n]
+        Vd = (kvd[ids, 1] * vsd[ids]).reshape(-1, Hkv, D)[:n]
+        s = torch.einsum("hd,nhd->hn", q[i].to(torch.float64), Kd.repeat_interleave(g, 1))
+        s = s / math.sqrt(D)
+        ref_o = torch.einsum("hn,nhd->hd", torch.softmax(s, -1), Vd.repeat_interleave(g, 1))
+        np.testing.assert_allclose(o[i], ref_o.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[i], torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
+
+
+def pin_token_scales_uniform(orc):
+    """Every per-token scale equal to c is the per-tensor scale c."""
+    from tests.helpers import as_bits
+    kv, q, perm, indptr, last, ks, vs, lens, (Hq, Hkv, D, P) = _fp8_batch(14)
+    qb, qc = as_bits(q)
+    kb, kc = as_bits(kv)
+    ks[:] = 0.015625  # exactly representable in float32
+    vs[:] = 0.5
+    a = orc.batch_decode_token_scales(qb, qc, kb, kc, indptr, perm.numpy(), last, Hq, Hkv, D, P,
+                                      ks.numpy(), vs.numpy())
+    b = orc.batch_decode(qb, qc, kb, kc, indptr, perm.numpy(), last, Hq, Hkv, D, P,
+                         k_scale=0.015625, v_scale=0.5)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
 def pin_empty_request(orc):
     rng = np.random.default_rng(10)
     K = [rng.standard_normal((5, 1, 4)).astype(np.float32)]
@@ -339,7 +394,8 @@ def pin_rejects_bad_args(orc):
 @pytest.mark.parametrize("pin", [
     pin_single_key, pin_identical_keys, pin_zero_query, pin_convexity, pin_split_merge,
     pin_gqa_equals_repeated_mha, pin_page_permutation, pin_brute_force, pin_torch_dense,
-    pin_empty_request, pin_padding_never_read, pin_golden_decode, pin_rejects_bad_args])
+    pin_empty_request, pin_padding_never_read, pin_golden_decode, pin_rejects_bad_args,
+    pin_token_scales_dense, pin_token_scales_uniform])
 def test_decode_pins(orc, pin):
     pin(orc)
 

@@ -28,8 +28,15 @@ MUTATIONS = [
      [T.pin_e4m3_all_codes, T.pin_e4m3_spec_points]),
     ("e4m3 subnormal scale", "((double)m / 8.0) * pow(2.0, 1 - 7)", "((double)m / 8.0) * pow(2.0, -7)",
      [T.pin_e4m3_all_codes, T.pin_e4m3_spec_points]),
-    ("k_scale ignored", "double kd = k_scale * load_elem", "double kd = load_elem",
-     [T.pin_torch_dense]),
+    ("k_scale ignored", "double kd = ks * load_elem", "double kd = load_elem",
+     [T.pin_torch_dense, T.pin_token_scales_dense]),
+    ("per-token K scale ignored",
+     "k_scales ? (double)k_scales[(page * Hkv + kvh) * P + slot] : k_scale;",
+     "k_scale;", [T.pin_token_scales_dense]),
+    ("per-token scale index transposed",
+     "v_scales ? (double)v_scales[(page * Hkv + kvh) * P + slot] : v_scale;",
+     "v_scales ? (double)v_scales[(page * P + slot) * Hkv + kvh] : v_scale;",
+     [T.pin_token_scales_dense]),
     ("merge weight of b uses a", "d_b * w_b;", "d_b * w_a;",
      [T.pin_golden_merge, T.pin_merge_algebra, T.pin_split_merge]),
     ("merge sign flipped", "exp(m_b - m_new);", "exp(m_new - m_b);",
