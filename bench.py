@@ -61,6 +61,8 @@ def algorithmic_bytes(b: W.DecodeBatch) -> int:
     kv_es = b.paged_kv.element_size()
     q_es = b.q.element_size()
     kv = b.total_tokens * b.num_kv_heads * 2 * b.head_dim * kv_es
+    if "k_scales" in b.extra:          # one fp32 K and one V scale per token and kv head
+        kv += b.total_tokens * b.num_kv_heads * 2 * 4
     idx = int(b.indptr[-1]) * 4
     qo = 2 * b.batch * b.num_qo_heads * b.head_dim * q_es
     lse = b.batch * b.num_qo_heads * 4
@@ -276,10 +278,16 @@ def bench_ours(args, world, rank, local):
     info = p.info
     o = torch.empty_like(b.q)
     lse = torch.empty((b.batch, b.num_qo_heads), dtype=torch.float32, device=dev)
-    kw = dict(k_scale=b.k_scale, v_scale=b.v_scale, out=o, lse=lse)
+    token_scales = "k_scales" in b.extra
+
+    def run_step(plan, q):
+        if token_scales:
+            return plan.run_token_scales(q, b.paged_kv, b.extra["k_scales"], b.extra["v_scales"],
+                                         out=o, lse=lse)
+        return plan.run(q, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale, out=o, lse=lse)
 
     for _ in range(args.warmup):
-        p.run(b.q, b.paged_kv, **kw)
+        run_step(p, b.q)
     torch.cuda.synchronize(dev)
     if p.check() != 0:
         raise RuntimeError("device check flagged the benchmark batch")
@@ -303,7 +311,7 @@ def bench_ours(args, world, rank, local):
     start.record(stream)
     for i in range(args.steps):
         p.set_timing_events(*evs[i])
-        p.run(b.q, b.paged_kv, **kw)
+        run_step(p, b.q)
     end.record(stream)
     torch.cuda.synchronize(dev)
     t1 = time.perf_counter()
@@ -334,7 +342,7 @@ def bench_ours(args, world, rank, local):
         pe = fa.plan(indptr_h, idx_d, last_h, b.num_qo_heads, b.num_kv_heads, b.head_dim,
                      b.page_size, q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype,
                      workspace=ws)
-        pe.run(q_d, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale, out=o, lse=lse)
+        run_step(pe, q_d)
         o_h.copy_(o, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
         return pe

@@ -134,6 +134,25 @@ int fa_decode_run(fa_decode_plan_t plan, const void* q, const void* paged_kv,
                   int64_t num_pages, float sm_scale, float k_scale,
                   float v_scale, void* o, float* lse, void* cuda_stream);
 
+/* run with per-token FP8 scales: like fa_decode_run for a plan whose kv
+ * dtype is E4M3, but every stored K and V element is dequantised with the
+ * scale of its own token and kv head instead of one scale per tensor - the
+ * row-wise dynamic scaling that the page "FlashInfer vs FlashAttention-3"
+ * (section "Production War Story: The FP8 Precision Underflow Failure")
+ * names as the fix for static-scale underflow over long contexts.
+ *
+ *  k_scales, v_scales  [num_pages, num_kv_heads, page_size] float32, device,
+ *                      16-byte aligned: the K (V) element at page p, slot t,
+ *                      kv head h has the value code * scales[(p*Hkv + h)*P + t].
+ * Other arguments as fa_decode_run (sm_scale <= 0 selects 1/sqrt(head_dim)).
+ * Built for head_dim 128 and groups 2, 4, 8 (the tensor-core consumer); other
+ * plans return FA_ERR_UNSUPPORTED, as do plans whose kv dtype is not E4M3. */
+int fa_decode_run_token_scales(fa_decode_plan_t plan, const void* q,
+                               const void* paged_kv, int64_t num_pages,
+                               float sm_scale, const float* k_scales,
+                               const float* v_scales, void* o, float* lse,
+                               void* cuda_stream);
+
 /* merge_states: combine two sets of partial attention states with the merge
  * rule (page "FlashDecoding + FlashInfer", section "FlashDecoding - the
  * split-KV trick").  A state is a normalised output o_x with its natural-log

@@ -34,6 +34,7 @@ EXPORTED_SYMBOLS = (
     "fa_decode_run", "fa_merge_states", "fa_decode_plan_destroy",
     "fa_decode_plan_get_info", "fa_decode_plan_get_work", "fa_plan_work_host",
     "fa_decode_check", "fa_decode_set_timing_events", "fa_decode_static",
+    "fa_decode_run_token_scales",
 )
 
 FA_OK = 0
@@ -74,6 +75,8 @@ def _load() -> ctypes.CDLL:
     lib.fa_decode_plan.restype = i32
     lib.fa_decode_run.argtypes = [P, P, P, i64, f32, f32, f32, P, P, P]
     lib.fa_decode_run.restype = i32
+    lib.fa_decode_run_token_scales.argtypes = [P, P, P, i64, f32, P, P, P, P, P]
+    lib.fa_decode_run_token_scales.restype = i32
     lib.fa_merge_states.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, P]
     lib.fa_merge_states.restype = i32
     lib.fa_decode_plan_destroy.argtypes = [P]
@@ -209,6 +212,33 @@ class DecodePlan:
             0.0 if sm_scale is None else float(sm_scale), float(k_scale), float(v_scale),
             out.data_ptr(), lse.data_ptr() if lse is not None else None,
             _stream_handle(stream)), "fa_decode_run")
+        return out, lse
+
+    def run_token_scales(self, q: torch.Tensor, paged_kv: torch.Tensor, k_scales: torch.Tensor,
+                         v_scales: torch.Tensor, *, sm_scale: float | None = None,
+                         out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                         return_lse: bool = True, stream=None):
+        """Decode over an E4M3 cache with per-token, per-kv-head scales
+        k_scales / v_scales [num_pages, num_kv_heads, page_size] float32."""
+        B, Hq, D = self.batch, self.num_qo_heads, self.head_dim
+        if q.dtype != self.q_dtype or paged_kv.dtype != self.kv_dtype:
+            raise TypeError("q / paged_kv dtype differs from the plan")
+        want = (paged_kv.shape[0], self.num_kv_heads, self.page_size)
+        for t in (k_scales, v_scales):
+            if (t.dtype != torch.float32 or tuple(t.shape) != want or not t.is_contiguous()
+                    or not t.is_cuda):
+                raise ValueError(f"scales must be contiguous float32 CUDA tensors {want}")
+        if tuple(q.shape) != (B, Hq, D) or not q.is_contiguous():
+            raise ValueError(f"q must be a contiguous CUDA tensor [{B}, {Hq}, {D}]")
+        if out is None:
+            out = torch.empty((B, Hq, D), dtype=q.dtype, device=q.device)
+        if return_lse and lse is None:
+            lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        _check(_L().fa_decode_run_token_scales(
+            self._h, q.data_ptr(), paged_kv.data_ptr(), paged_kv.shape[0],
+            0.0 if sm_scale is None else float(sm_scale), k_scales.data_ptr(),
+            v_scales.data_ptr(), out.data_ptr(), lse.data_ptr() if lse is not None else None,
+            _stream_handle(stream)), "fa_decode_run_token_scales")
         return out, lse
 
     def check(self, stream=None) -> int:

@@ -102,7 +102,80 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
+struct MapCache {
+  CUtensorMap tmap;
+  const void* base = nullptr;
+  int64_t pages = -1;
+};
+
+// Encode (or reuse) the TMA descriptor of `paged_kv` for kernel `k`: the view
+// [2*num_pages][P][Hkv][D], innermost first; one box = K and V rows of one
+// kv head of one page (or of one 128-byte segment of those rows when the
+// kernel stages them in 128-byte swizzle order).
+int kv_tensor_map(MapCache* c, const DecodeKernel& k, fa_dtype kv_dtype, const void* paged_kv,
+                  int64_t num_pages, int D, int Hkv, int P) {
+  if (paged_kv == c->base && num_pages == c->pages) return FA_OK;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
+  if (!encode) return FA_ERR_CUDA;
+  const size_t es = (size_t)dtype_size(kv_dtype);
+  CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  switch (kv_dtype) {
+    case FA_DTYPE_F32: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; break;
+    case FA_DTYPE_BF16: dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; break;
+    case FA_DTYPE_F16: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; break;
+    case FA_DTYPE_E4M3: dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;
+  }
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)P,
+                        (cuuint64_t)(2 * num_pages)};
+  cuuint64_t strides[3] = {(cuuint64_t)(D * es), (cuuint64_t)(Hkv * D * es),
+                           (cuuint64_t)(P * Hkv * D * es)};
+  cuuint32_t box[4] = {(cuuint32_t)k.box_x, 1u, (cuuint32_t)P, 2u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  // Promote L2 fills to the box row length: a longer promotion would pull
+  // in the neighbouring kv heads' rows, which another CTA reads much later.
+  const size_t row_bytes = (size_t)k.box_x * es;
+  const CUtensorMapL2promotion promo = row_bytes >= 256   ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                       : row_bytes >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                                          : CU_TENSOR_MAP_L2_PROMOTION_L2_64B;
+  CUresult r = encode(&c->tmap, dt, 4, const_cast<void*>(paged_kv), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      k.swizzle_128b ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                      promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    c->base = nullptr;
+    return FA_ERR_CUDA;
+  }
+  c->base = paged_kv;
+  c->pages = num_pages;
+  return FA_OK;
+}
+
+bool find_token_scale_kernel(fa_dtype q, fa_dtype kv, int D, int G, DecodeKernel* k) {
+  if (kv != FA_DTYPE_E4M3) return false;
+  if (q == FA_DTYPE_BF16) return fadecode::find_token_scale_kernel_bf16_e4m3(D, G, k);
+  if (q == FA_DTYPE_F16) return fadecode::find_token_scale_kernel_f16_e4m3(D, G, k);
+  return false;
+}
+
+// Set a kernel's shared-memory limit and return how many of its CTAs fit on
+// one SM (0 on failure).
+int kernel_occupancy(const DecodeKernel& k) {
+  int occ = 0;
+  if (cudaFuncSetAttribute(k.func, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem_bytes) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.func, k.threads, k.smem_bytes) !=
+          cudaSuccess)
+    return 0;
+  return occ;
+}
+
 }  // namespace
+
+struct fa_decode_plan_s;
+static int run_impl(fa_decode_plan_s* plan, bool token_scales, const void* q,
+                    const void* paged_kv, int64_t num_pages, float sm_scale, float k_scale,
+                    float v_scale, const float* k_scales, const float* v_scales, void* o,
+                    float* lse, void* cuda_stream);
 
 struct fa_decode_plan_s {
   int device = 0;
@@ -117,10 +190,11 @@ struct fa_decode_plan_s {
   size_t ws_bytes = 0;
   Layout layout{};
   bool fused_merge = true;
-  // cached TMA descriptor of the KV cache
-  CUtensorMap tmap;
-  const void* tmap_base = nullptr;
-  int64_t tmap_pages = -1;
+  // E4M3 plans: the variant that reads per-token scales, if one is built
+  DecodeKernel kern_ts;
+  bool has_ts = false;
+  // cached TMA descriptors of the KV cache, one per kernel variant
+  MapCache map, map_ts;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
 };
 
@@ -199,11 +273,16 @@ int fa_decode_plan(const int32_t* indptr_host, const int32_t* indices_dev,
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return FA_ERR_CUDA;
-  if (cudaFuncSetAttribute(kern.func, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kern.smem_bytes) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern.func, kern.threads,
-                                                    kern.smem_bytes) != cudaSuccess)
-    return FA_ERR_CUDA;
+  occ = kernel_occupancy(kern);
+  if (occ == 0) return FA_ERR_CUDA;
+  // The persistent grid must fit for either variant a run may launch.
+  DecodeKernel kern_ts;
+  const bool has_ts = find_token_scale_kernel(q_dtype, kv_dtype, head_dim, G, &kern_ts);
+  if (has_ts) {
+    const int occ_ts = kernel_occupancy(kern_ts);
+    if (occ_ts == 0) return FA_ERR_CUDA;
+    occ = std::min(occ, occ_ts);
+  }
   occ = std::max(1, std::min(occ, kMaxCtasPerSmBound));
 
   fa_decode_plan_s* plan = new (std::nothrow) fa_decode_plan_s();
@@ -224,6 +303,8 @@ int fa_decode_plan(const int32_t* indptr_host, const int32_t* indices_dev,
   plan->ws = static_cast<uint8_t*>(workspace_dev);
   plan->ws_bytes = workspace_bytes;
   plan->fused_merge = fused_merge_enabled();
+  plan->kern_ts = kern_ts;
+  plan->has_ts = has_ts;
 
   int rc = FA_OK;
   try {
@@ -271,94 +352,20 @@ int fa_decode_run(fa_decode_plan_t plan, const void* q, const void* paged_kv, in
                   float sm_scale, float k_scale, float v_scale, void* o, float* lse,
                   void* cuda_stream) {
   if (!plan) return FA_ERR_INVALID_ARG;
-  if (plan->batch == 0) return FA_OK;
-  if (!q || !paged_kv || !o || num_pages <= 0) return FA_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(paged_kv) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
+  return run_impl(plan, false, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, nullptr,
+                  nullptr, o, lse, cuda_stream);
+}
+
+int fa_decode_run_token_scales(fa_decode_plan_t plan, const void* q, const void* paged_kv,
+                               int64_t num_pages, float sm_scale, const float* k_scales,
+                               const float* v_scales, void* o, float* lse, void* cuda_stream) {
+  if (!plan) return FA_ERR_INVALID_ARG;
+  if (plan->kv_dtype != FA_DTYPE_E4M3 || !plan->has_ts) return FA_ERR_UNSUPPORTED;
+  if (plan->batch > 0 && (!k_scales || !v_scales)) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(k_scales) % 16 || reinterpret_cast<uintptr_t>(v_scales) % 16)
     return FA_ERR_INVALID_ARG;
-  if (2 * num_pages > (int64_t)0xffffffffLL) return FA_ERR_UNSUPPORTED;
-  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  const int D = plan->d, P = plan->page_size, Hkv = plan->hkv;
-  const size_t es = (size_t)dtype_size(plan->kv_dtype);
-
-  if (paged_kv != plan->tmap_base || num_pages != plan->tmap_pages) {
-    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
-    if (!encode) return FA_ERR_CUDA;
-    CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    switch (plan->kv_dtype) {
-      case FA_DTYPE_F32: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; break;
-      case FA_DTYPE_BF16: dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; break;
-      case FA_DTYPE_F16: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; break;
-      case FA_DTYPE_E4M3: dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;
-    }
-    // [2*num_pages][P][Hkv][D], innermost first; one box = K and V rows of
-    // one kv head of one page (or of one 128-byte segment of those rows when
-    // the kernel stages them in 128-byte swizzle order).
-    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)P,
-                          (cuuint64_t)(2 * num_pages)};
-    cuuint64_t strides[3] = {(cuuint64_t)(D * es), (cuuint64_t)(Hkv * D * es),
-                             (cuuint64_t)(P * Hkv * D * es)};
-    cuuint32_t box[4] = {(cuuint32_t)plan->kern.box_x, 1u, (cuuint32_t)P, 2u};
-    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    // Promote L2 fills to the box row length: a longer promotion would pull
-    // in the neighbouring kv heads' rows, which another CTA reads much later.
-    const size_t row_bytes = (size_t)plan->kern.box_x * es;
-    const CUtensorMapL2promotion promo = row_bytes >= 256   ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
-                                         : row_bytes >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
-                                                            : CU_TENSOR_MAP_L2_PROMOTION_L2_64B;
-    CUresult r = encode(&plan->tmap, dt, 4, const_cast<void*>(paged_kv), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        plan->kern.swizzle_128b ? CU_TENSOR_MAP_SWIZZLE_128B
-                                                : CU_TENSOR_MAP_SWIZZLE_NONE,
-                        promo,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-      plan->tmap_base = nullptr;
-      return FA_ERR_CUDA;
-    }
-    plan->tmap_base = paged_kv;
-    plan->tmap_pages = num_pages;
-  }
-
-  if (!(sm_scale > 0.f)) sm_scale = 1.0f / std::sqrt((float)D);
-  DecodeParams prm;
-  prm.q = q;
-  prm.o = o;
-  prm.lse = lse;
-  prm.indices = plan->indices;
-  prm.cta_offsets = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_cta);
-  prm.segments = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_seg);
-  prm.part_o = reinterpret_cast<float*>(plan->ws + plan->layout.off_part_o);
-  prm.part_lse = reinterpret_cast<float*>(plan->ws + plan->layout.off_part_lse);
-  prm.err = reinterpret_cast<int*>(plan->ws + plan->layout.off_err);
-  prm.merge = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_merge);
-  prm.merge_count = reinterpret_cast<int*>(plan->ws + plan->layout.off_count);
-  prm.fused_merge = plan->fused_merge ? 1 : 0;
-  prm.num_pages = num_pages;
-  prm.num_qo_heads = plan->hq;
-  prm.q_scale = sm_scale * k_scale * kLog2e;
-  prm.v_scale = v_scale;
-
-  const bool timed = plan->ev_before && plan->ev_after;
-  if (timed && cudaEventRecord(plan->ev_before, st) != cudaSuccess) return FA_ERR_CUDA;
-  void* args[2] = {&plan->tmap, &prm};
-  if (cudaLaunchKernel(plan->kern.func, dim3(plan->wl.num_ctas), dim3(plan->kern.threads), args,
-                       (size_t)plan->kern.smem_bytes, st) != cudaSuccess)
-    return FA_ERR_CUDA;
-  if (timed && cudaEventRecord(plan->ev_after, st) != cudaSuccess) return FA_ERR_CUDA;
-  if (!plan->fused_merge && !plan->wl.merge.empty()) {
-    MergeParams mp;
-    mp.merge = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_merge);
-    mp.part_o = prm.part_o;
-    mp.part_lse = prm.part_lse;
-    mp.o = o;
-    mp.lse = lse;
-    mp.num_qo_heads = plan->hq;
-    void* margs[1] = {&mp};
-    if (cudaLaunchKernel(plan->kern.merge_func, dim3((unsigned)plan->wl.merge.size()), dim3(128),
-                         margs, 0, st) != cudaSuccess)
-      return FA_ERR_CUDA;
-  }
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return run_impl(plan, true, q, paged_kv, num_pages, sm_scale, 1.f, 1.f, k_scales, v_scales, o,
+                  lse, cuda_stream);
 }
 
 int fa_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
@@ -436,3 +443,65 @@ int fa_decode_set_timing_events(fa_decode_plan_t plan, void* ev_before, void* ev
 }
 
 }  // extern "C"
+
+static int run_impl(fa_decode_plan_s* plan, bool token_scales, const void* q,
+                    const void* paged_kv, int64_t num_pages, float sm_scale, float k_scale,
+                    float v_scale, const float* k_scales, const float* v_scales, void* o,
+                    float* lse, void* cuda_stream) {
+  if (plan->batch == 0) return FA_OK;
+  if (!q || !paged_kv || !o || num_pages <= 0) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(paged_kv) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
+    return FA_ERR_INVALID_ARG;
+  if (2 * num_pages > (int64_t)0xffffffffLL) return FA_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const DecodeKernel& kern = token_scales ? plan->kern_ts : plan->kern;
+  MapCache& mc = token_scales ? plan->map_ts : plan->map;
+  const int D = plan->d;
+  int rc = kv_tensor_map(&mc, kern, plan->kv_dtype, paged_kv, num_pages, D, plan->hkv,
+                         plan->page_size);
+  if (rc != FA_OK) return rc;
+
+  if (!(sm_scale > 0.f)) sm_scale = 1.0f / std::sqrt((float)D);
+  DecodeParams prm;
+  prm.q = q;
+  prm.o = o;
+  prm.lse = lse;
+  prm.indices = plan->indices;
+  prm.cta_offsets = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_cta);
+  prm.segments = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_seg);
+  prm.part_o = reinterpret_cast<float*>(plan->ws + plan->layout.off_part_o);
+  prm.part_lse = reinterpret_cast<float*>(plan->ws + plan->layout.off_part_lse);
+  prm.err = reinterpret_cast<int*>(plan->ws + plan->layout.off_err);
+  prm.merge = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_merge);
+  prm.merge_count = reinterpret_cast<int*>(plan->ws + plan->layout.off_count);
+  prm.fused_merge = plan->fused_merge ? 1 : 0;
+  prm.k_scales = k_scales;
+  prm.v_scales = v_scales;
+  prm.num_pages = num_pages;
+  prm.num_qo_heads = plan->hq;
+  prm.num_kv_heads = plan->hkv;
+  prm.q_scale = sm_scale * k_scale * kLog2e;
+  prm.v_scale = v_scale;
+
+  const bool timed = plan->ev_before && plan->ev_after;
+  if (timed && cudaEventRecord(plan->ev_before, st) != cudaSuccess) return FA_ERR_CUDA;
+  void* args[2] = {&mc.tmap, &prm};
+  if (cudaLaunchKernel(kern.func, dim3(plan->wl.num_ctas), dim3(kern.threads), args,
+                       (size_t)kern.smem_bytes, st) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (timed && cudaEventRecord(plan->ev_after, st) != cudaSuccess) return FA_ERR_CUDA;
+  if (!plan->fused_merge && !plan->wl.merge.empty()) {
+    MergeParams mp;
+    mp.merge = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_merge);
+    mp.part_o = prm.part_o;
+    mp.part_lse = prm.part_lse;
+    mp.o = o;
+    mp.lse = lse;
+    mp.num_qo_heads = plan->hq;
+    void* margs[1] = {&mp};
+    if (cudaLaunchKernel(kern.merge_func, dim3((unsigned)plan->wl.merge.size()), dim3(128), margs,
+                         0, st) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}

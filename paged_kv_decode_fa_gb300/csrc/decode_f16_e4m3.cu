@@ -6,4 +6,7 @@ namespace fadecode {
 bool find_kernel_f16_e4m3(int head_dim, int group, bool allow_mma, DecodeKernel* k) {
   return find_kernel_for<__half, __nv_fp8_e4m3>(head_dim, group, allow_mma, k);
 }
+bool find_token_scale_kernel_f16_e4m3(int head_dim, int group, DecodeKernel* k) {
+  return find_token_scale_kernel_for<__half>(head_dim, group, k);
+}
 }  // namespace fadecode

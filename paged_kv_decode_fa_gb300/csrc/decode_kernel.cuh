@@ -121,6 +121,17 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Contiguous global -> shared copy of `bytes` (multiple of 16, both
+// addresses 16-byte aligned) completing on mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -287,10 +298,13 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[G], int c) {
 // b * BOX_BYTES in the stage) completing on the stage's "full" barrier.  Page
 // k of the stream goes to stage k % S once the stage's previous page has been
 // released.  Ends by waiting (bounded) for its last copies to land.
-template <int S, int STAGE_BYTES, int BOXES, int BOX_X, int BOX_BYTES>
+// With SCALES, each page also brings the 16 per-token K scales and the 16 V
+// scales of its kv head (64 contiguous bytes each) into scales[stage][0..31].
+template <int S, int STAGE_BYTES, int BOXES, int BOX_X, int BOX_BYTES, bool SCALES = false>
 __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const DecodeParams& p,
                                               int seg_begin, int seg_end, uint8_t* ring,
-                                              uint64_t* full, uint64_t* empty, int lane) {
+                                              uint64_t* full, uint64_t* empty, int lane,
+                                              float* scales = nullptr) {
   bool aborted = false;
   const uint64_t policy = dev::evict_first_policy();
   int k = 0;
@@ -309,13 +323,23 @@ __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const Deco
           const uint32_t round = (uint32_t)(k / S);
           dev::mbar_wait(dev::smem_addr(&empty[stage]), (round & 1u) ^ 1u, aborted, p.err);
           const uint32_t fb = dev::smem_addr(&full[stage]);
-          dev::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          dev::mbar_arrive_expect_tx(fb, STAGE_BYTES + (SCALES ? 2 * kPageSize * 4 : 0));
           // Out-of-range ids (already flagged) land outside the tensor map
           // and read zeros.
 #pragma unroll
           for (int b = 0; b < BOXES; ++b)
             dev::tma_load_4d(dev::smem_addr(ring + stage * STAGE_BYTES + b * BOX_BYTES), map,
                              b * BOX_X, kvh, 0, 2 * page, fb, policy);
+          if constexpr (SCALES) {
+            // the scale rows have no bounds check of their own: a flagged
+            // out-of-range page reads page 0's scales
+            const int64_t pg = (page < 0 || (int64_t)page >= p.num_pages) ? 0 : page;
+            const size_t row = ((size_t)pg * p.num_kv_heads + kvh) * kPageSize;
+            dev::bulk_load(dev::smem_addr(scales + stage * 2 * kPageSize), p.k_scales + row,
+                           kPageSize * 4, fb);
+            dev::bulk_load(dev::smem_addr(scales + stage * 2 * kPageSize + kPageSize),
+                           p.v_scales + row, kPageSize * 4, fb);
+          }
         }
       }
     }

@@ -115,7 +115,7 @@ __device__ __forceinline__ float2 unpack2(uint32_t w, bool bf16) {
 
 }  // namespace mma
 
-template <typename QT, typename KVT, int D, int G, int NW>
+template <typename QT, typename KVT, int D, int G, int NW, bool TS = false>
 struct MmaCfg {
   static constexpr int P = kPageSize;
   static constexpr int KV_ES = sizeof(KVT);
@@ -144,7 +144,9 @@ struct MmaCfg {
   static constexpr int OFF_MM = OFF_MO + 4 * NW * G * D;
   static constexpr int OFF_MD = OFF_MM + 4 * NW * G;
   static constexpr int OFF_FLAG = OFF_MD + 4 * NW * G;
-  static constexpr int SMEM = OFF_FLAG + 16;
+  static constexpr int OFF_SCALES = OFF_FLAG + 16;                 // [S][32] fp32 if TS
+  static constexpr int SMEM = OFF_SCALES + (TS ? S * 2 * P * 4 : 0);
+  static_assert(!TS || kFp8, "per-token scales are for E4M3 KV");
   static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte swizzle rows");
   static_assert(G >= 1 && G <= 8, "group of at most 8 heads (the MMA N side)");
   static_assert(STAGE_BYTES % 1024 == 0, "swizzled boxes need 1024-byte alignment");
@@ -152,10 +154,10 @@ struct MmaCfg {
   static_assert(!kFp8 || D % 32 == 0, "E4M3 V is transposed two granules at a time");
 };
 
-template <typename QT, typename KVT, int D, int G, int NW>
-__global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW>::THREADS)
+template <typename QT, typename KVT, int D, int G, int NW, bool TS>
+__global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS>::THREADS)
     fa_decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
-  using C = MmaCfg<QT, KVT, D, G, NW>;
+  using C = MmaCfg<QT, KVT, D, G, NW, TS>;
   constexpr int P = C::P, S = C::S, SEGS = C::SEGS, KSTEPS = C::KSTEPS, MTILES = C::MTILES;
   constexpr bool kBf16 = C::kBf16, kFp8 = C::kFp8;
   static_assert(kBf16 ? std::is_same<QT, __nv_bfloat16>::value
@@ -188,8 +190,9 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW>::THREADS)
   __syncthreads();
 
   if (warp == NW) {
-    produce_pages<S, C::STAGE_BYTES, SEGS, C::BOX_X, C::BOX_BYTES>(&kv_map, p, seg_begin, seg_end,
-                                                                   ring, full, empty, lane);
+    produce_pages<S, C::STAGE_BYTES, SEGS, C::BOX_X, C::BOX_BYTES, TS>(
+        &kv_map, p, seg_begin, seg_end, ring, full, empty, lane,
+        reinterpret_cast<float*>(smem + C::OFF_SCALES));
     return;
   }
 
@@ -327,6 +330,17 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW>::THREADS)
       float s[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) s[e] = (sc[0][e] + sc[1][e]) * qscale;
+      float vs_lo = 1.f, vs_hi = 1.f;  // per-token V scales of tokens g, g+8
+      if constexpr (TS) {
+        const float* scl = reinterpret_cast<const float*>(smem + C::OFF_SCALES) + stage * 2 * P;
+        const float ks_lo = scl[g], ks_hi = scl[g + 8];
+        vs_lo = scl[P + g];
+        vs_hi = scl[P + g + 8];
+        s[0] *= ks_lo;
+        s[1] *= ks_lo;
+        s[2] *= ks_hi;
+        s[3] *= ks_hi;
+      }
       if (g >= valid) s[0] = s[1] = -INFINITY;
       if (g + 8 >= valid) s[2] = s[3] = -INFINITY;
 
@@ -354,6 +368,11 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW>::THREADS)
         pr[0] = a.x; pr[1] = a.y; pr[2] = b.x; pr[3] = b.y;
       }
       float ps[2] = {pr[0] + pr[2], pr[1] + pr[3]};
+      uint32_t pv01 = p01, pv23 = p23;  // weights times the per-token V scale
+      if constexpr (TS) {
+        pv01 = mma::pack2(pr[0] * vs_lo, pr[1] * vs_lo, kBf16);
+        pv23 = mma::pack2(pr[2] * vs_hi, pr[3] * vs_hi, kBf16);
+      }
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
         ps[0] += __shfl_xor_sync(0xffffffffu, ps[0], off);
@@ -362,10 +381,10 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW>::THREADS)
       d_h[0] = d_h[0] * alpha[0] + ps[0];
       d_h[1] = d_h[1] * alpha[1] + ps[1];
       // P^T B fragments: transpose [token][head] -> [head][token] through smem
-      pT[(2 * t) * P + g] = (uint16_t)(p01 & 0xffffu);
-      pT[(2 * t + 1) * P + g] = (uint16_t)(p01 >> 16);
-      pT[(2 * t) * P + g + 8] = (uint16_t)(p23 & 0xffffu);
-      pT[(2 * t + 1) * P + g + 8] = (uint16_t)(p23 >> 16);
+      pT[(2 * t) * P + g] = (uint16_t)(pv01 & 0xffffu);
+      pT[(2 * t + 1) * P + g] = (uint16_t)(pv01 >> 16);
+      pT[(2 * t) * P + g + 8] = (uint16_t)(pv23 & 0xffffu);
+      pT[(2 * t + 1) * P + g + 8] = (uint16_t)(pv23 >> 16);
       // once the running maxima settle, most pages leave them unchanged
       if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
@@ -453,10 +472,10 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW>::THREADS)
   }
 }
 
-template <typename QT, typename KVT, int D, int G, int NW = 4>
+template <typename QT, typename KVT, int D, int G, int NW = 4, bool TS = false>
 inline void fill_mma_kernel(DecodeKernel* k) {
-  using C = MmaCfg<QT, KVT, D, G, NW>;
-  k->func = reinterpret_cast<const void*>(&fa_decode_mma_kernel<QT, KVT, D, G, NW>);
+  using C = MmaCfg<QT, KVT, D, G, NW, TS>;
+  k->func = reinterpret_cast<const void*>(&fa_decode_mma_kernel<QT, KVT, D, G, NW, TS>);
   k->merge_func = reinterpret_cast<const void*>(&fa_merge_partials_kernel<QT, D, G>);
   k->threads = C::THREADS;
   k->smem_bytes = C::SMEM + 1024;  // room to align the ring to 1024 bytes
@@ -467,6 +486,7 @@ inline void fill_mma_kernel(DecodeKernel* k) {
   k->box_x = C::BOX_X;
   k->swizzle_128b = true;
   k->tensor_cores = true;
+  k->token_scales = TS;
 }
 
 }  // namespace fadecode
@@ -493,6 +513,16 @@ inline bool find_kernel_for(int head_dim, int group, bool allow_mma, DecodeKerne
   FA_CASE(64, 1) FA_CASE(64, 2) FA_CASE(64, 4) FA_CASE(64, 8)
   FA_CASE(128, 1) FA_CASE(128, 2) FA_CASE(128, 4) FA_CASE(128, 8)
 #undef FA_CASE
+  return false;
+}
+
+// E4M3 KV with per-token scales: tensor-core consumer, head_dim 128, group 2..8.
+template <typename QT>
+inline bool find_token_scale_kernel_for(int head_dim, int group, DecodeKernel* k) {
+  if (head_dim != 128) return false;
+  if (group == 2) { fill_mma_kernel<QT, __nv_fp8_e4m3, 128, 2, 4, true>(k); return true; }
+  if (group == 4) { fill_mma_kernel<QT, __nv_fp8_e4m3, 128, 4, 4, true>(k); return true; }
+  if (group == 8) { fill_mma_kernel<QT, __nv_fp8_e4m3, 128, 8, 4, true>(k); return true; }
   return false;
 }
 

@@ -24,8 +24,11 @@ struct DecodeParams {
   const int32_t* merge;        // [n_merge * 4] {request, kv_head, first_slot, num_slots}
   int* merge_count;            // [n_merge] arrivals per split unit, zero between runs
   int fused_merge;             // 1: the last CTA of a split unit merges it
+  const float* k_scales;       // [num_pages, Hkv, page_size] per-token scales, or nullptr
+  const float* v_scales;       // same for V
   int64_t num_pages;
   int num_qo_heads;
+  int num_kv_heads;
   float q_scale;  // sm_scale * k_scale * log2(e), folded into q
   float v_scale;
 };
@@ -52,6 +55,7 @@ struct DecodeKernel {
   int box_x = 0;              // elements per TMA box row (D, or 128 bytes' worth)
   bool swizzle_128b = false;  // stage rows in TMA 128-byte swizzle order
   bool tensor_cores = false;  // per-page products on mma.sync
+  bool token_scales = false;  // reads per-token K/V scales (E4M3 only)
 };
 
 // Each returns false when the combination is not compiled.  allow_mma
@@ -62,6 +66,9 @@ bool find_kernel_bf16(int head_dim, int group, bool allow_mma, DecodeKernel* k);
 bool find_kernel_f16(int head_dim, int group, bool allow_mma, DecodeKernel* k);
 bool find_kernel_bf16_e4m3(int head_dim, int group, bool allow_mma, DecodeKernel* k);
 bool find_kernel_f16_e4m3(int head_dim, int group, bool allow_mma, DecodeKernel* k);
+// E4M3 KV with per-token, per-kv-head scales (tensor-core consumer only).
+bool find_token_scale_kernel_bf16_e4m3(int head_dim, int group, DecodeKernel* k);
+bool find_token_scale_kernel_f16_e4m3(int head_dim, int group, DecodeKernel* k);
 
 // fa_merge_states kernels (merge.cu).
 int launch_merge_states(const void* o_a, const float* lse_a, const void* o_b,

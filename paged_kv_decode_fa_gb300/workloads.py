@@ -21,6 +21,12 @@ measured on:
                  stored as FP8 E4M3 with one fp32 scale each (amax / 448),
                  lengths uniform in [1024, 8192].
 
+``fp8_kv_token_scales``  the fp8_kv shapes and lengths, with K and V
+                 magnitudes that vary per token and kv head (N(0,1) times
+                 2^u, u uniform in [-3, 3]) stored as E4M3 with one fp32
+                 scale per (page, kv head, slot) = amax over head_dim / 448
+                 - the spread that underflows under a single static scale.
+
 All use page_size 16 and the combined [num_pages, 2, 16, Hkv, D] layout.
 Lengths and page tables come from a CPU ``torch.Generator``; values from a
 generator on the target device, both seeded with the config's seed
@@ -62,6 +68,8 @@ CONFIGS: dict[str, DecodeConfig] = {
     "ragged": DecodeConfig("ragged", 450, 32, 8, 128, torch.bfloat16, torch.bfloat16, 1003),
     "long_split": DecodeConfig("long_split", 1, 32, 32, 128, torch.bfloat16, torch.bfloat16, 1004),
     "fp8_kv": DecodeConfig("fp8_kv", 128, 64, 8, 128, torch.bfloat16, torch.float8_e4m3fn, 1005),
+    "fp8_kv_token_scales": DecodeConfig("fp8_kv_token_scales", 128, 64, 8, 128, torch.bfloat16,
+                                        torch.float8_e4m3fn, 1006),
 }
 
 
@@ -77,7 +85,7 @@ def draw_lengths(cfg: DecodeConfig, gen: torch.Generator) -> np.ndarray:
         return np.rint(np.exp(lo + u * (hi - lo))).astype(np.int64)
     if cfg.name == "long_split":
         return np.full(cfg.batch, 65536, dtype=np.int64)
-    if cfg.name == "fp8_kv":
+    if cfg.name in ("fp8_kv", "fp8_kv_token_scales"):
         return torch.randint(1024, 8193, (cfg.batch,), generator=gen).numpy().astype(np.int64)
     raise KeyError(cfg.name)
 
@@ -151,11 +159,13 @@ def _fp8_quantise(x: torch.Tensor) -> tuple[torch.Tensor, float]:
 def make_batch(*, batch_lengths, num_qo_heads: int, num_kv_heads: int, head_dim: int,
                q_dtype: torch.dtype, kv_dtype: torch.dtype, seed: int, device="cuda",
                page_size: int = PAGE_SIZE, pool_pages: int | None = None, shuffle: bool = True,
-               name: str = "custom") -> DecodeBatch:
-    """A seeded batch with explicit lengths (any shape the library supports)."""
+               name: str = "custom", token_scales: bool = False) -> DecodeBatch:
+    """A seeded batch with explicit lengths (any shape the library supports).
+    token_scales=True (E4M3 only) draws per-token magnitudes and stores one
+    scale per (page, kv head, slot) in extra["k_scales"] / extra["v_scales"]."""
     gen = torch.Generator().manual_seed(seed)
     return _fill(batch_lengths, gen, num_qo_heads, num_kv_heads, head_dim, q_dtype, kv_dtype,
-                 seed, device, page_size, pool_pages, shuffle, name)
+                 seed, device, page_size, pool_pages, shuffle, name, token_scales)
 
 
 def make_config_batch(name: str, device="cuda") -> DecodeBatch:
@@ -165,11 +175,22 @@ def make_config_batch(name: str, device="cuda") -> DecodeBatch:
     lengths = draw_lengths(cfg, gen)
     pool = 64 if name == "tiny" else None
     return _fill(lengths, gen, cfg.num_qo_heads, cfg.num_kv_heads, cfg.head_dim, cfg.q_dtype,
-                 cfg.kv_dtype, cfg.seed, device, cfg.page_size, pool, True, name)
+                 cfg.kv_dtype, cfg.seed, device, cfg.page_size, pool, True, name,
+                 name == "fp8_kv_token_scales")
+
+
+def _fp8_token_quantise(x: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
+    """Per-token E4M3 quantisation of x [pages, P, Hkv, D]: one scale per
+    (page, slot, kv head) = amax over D / 448.  Returns the codes and the
+    scales laid out [pages, Hkv, P]."""
+    amax = x.abs().amax(dim=-1, keepdim=True)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    codes = (x / scale).to(torch.float8_e4m3fn)
+    return codes, scale.squeeze(-1).permute(0, 2, 1).contiguous()
 
 
 def _fill(lengths, gen, Hq, Hkv, D, q_dtype, kv_dtype, seed, device, P, pool_pages, shuffle,
-          name) -> DecodeBatch:
+          name, token_scales=False) -> DecodeBatch:
     lengths = np.asarray(lengths, dtype=np.int64)
     indptr, ids, last, pool = page_table(lengths, P, pool_pages, gen, shuffle)
     B = len(lengths)
@@ -177,7 +198,19 @@ def _fill(lengths, gen, Hq, Hkv, D, q_dtype, kv_dtype, seed, device, P, pool_pag
     vgen = torch.Generator(device=dev).manual_seed(seed)
     q = torch.randn((B, Hq, D), generator=vgen, device=dev, dtype=torch.float32).to(q_dtype)
     k_scale = v_scale = 1.0
-    if kv_dtype == torch.float8_e4m3fn:
+    extra = {}
+    if token_scales:
+        if kv_dtype != torch.float8_e4m3fn:
+            raise ValueError("per-token scales are for E4M3 KV")
+        kv = torch.empty((pool, 2, P, Hkv, D), dtype=kv_dtype, device=dev)
+        for half, key in ((0, "k_scales"), (1, "v_scales")):
+            mag = torch.exp2(torch.rand((pool, P, Hkv, 1), generator=vgen, device=dev) * 6 - 3)
+            x = torch.randn((pool, P, Hkv, D), generator=vgen, device=dev) * mag
+            codes, scales = _fp8_token_quantise(x)
+            kv[:, half] = codes
+            extra[key] = scales
+            del x, codes, mag
+    elif kv_dtype == torch.float8_e4m3fn:
         kv = torch.empty((pool, 2, P, Hkv, D), dtype=kv_dtype, device=dev)
         scales = []
         for half in range(2):
@@ -192,4 +225,4 @@ def _fill(lengths, gen, Hq, Hkv, D, q_dtype, kv_dtype, seed, device, P, pool_pag
     return DecodeBatch(q=q, paged_kv=kv, indptr=indptr, indices=ids.to(dev),
                        last_page_len=last, lengths=lengths, num_qo_heads=Hq,
                        num_kv_heads=Hkv, head_dim=D, page_size=P, k_scale=k_scale,
-                       v_scale=v_scale, name=name)
+                       v_scale=v_scale, name=name, extra=extra)

@@ -28,10 +28,17 @@ def as_bits(t: torch.Tensor):
 
 
 def oracle_decode(b: DecodeBatch, orc=None, sm_scale=None, num_threads=0):
-    """Run the oracle on a whole batch; returns float64 (o, lse)."""
+    """Run the oracle on a whole batch; returns float64 (o, lse).  A batch
+    with per-token scales (extra["k_scales"]) uses the per-token oracle."""
     orc = orc or oracle._default()
     q, qc = as_bits(b.q)
     kv, kc = as_bits(b.paged_kv)
+    if "k_scales" in b.extra:
+        return orc.batch_decode_token_scales(
+            q, qc, kv, kc, b.indptr.numpy(), b.indices.cpu().numpy(), b.last_page_len.numpy(),
+            b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size,
+            b.extra["k_scales"].cpu().numpy(), b.extra["v_scales"].cpu().numpy(),
+            sm_scale=sm_scale, num_threads=num_threads)
     return orc.batch_decode(q, qc, kv, kc, b.indptr.numpy(), b.indices.cpu().numpy(),
                             b.last_page_len.numpy(), b.num_qo_heads, b.num_kv_heads,
                             b.head_dim, b.page_size, sm_scale=sm_scale, k_scale=b.k_scale,
@@ -53,6 +60,11 @@ def sub_batch(b: DecodeBatch, requests) -> DecodeBatch:
     new_indptr = np.zeros(len(requests) + 1, np.int64)
     new_indptr[1:] = np.cumsum(counts)
     rq = torch.tensor(requests, dtype=torch.int64, device=b.q.device)
+    extra = {}
+    for key in ("k_scales", "v_scales"):
+        if key in b.extra:
+            t = b.extra[key]
+            extra[key] = (t.index_select(0, sel).to("cpu") if len(page_ids) else t[:1].to("cpu"))
     return DecodeBatch(
         q=b.q.index_select(0, rq).to("cpu"), paged_kv=kv,
         indptr=torch.from_numpy(new_indptr.astype(np.int32)),
@@ -60,7 +72,7 @@ def sub_batch(b: DecodeBatch, requests) -> DecodeBatch:
         last_page_len=b.last_page_len[requests].clone(),
         lengths=b.lengths[requests], num_qo_heads=b.num_qo_heads,
         num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, page_size=b.page_size,
-        k_scale=b.k_scale, v_scale=b.v_scale, name=b.name + "-sub")
+        k_scale=b.k_scale, v_scale=b.v_scale, name=b.name + "-sub", extra=extra)
 
 
 def dense_pages(K, V, page_size, perm_seed=0, pool_extra=0, pad_value=np.nan):

@@ -192,6 +192,64 @@ def test_unsupported_rejected(lib, cuda):
     assert e.value.status == -2
 
 
+# ------------------------------------------------------------------ per-token FP8 scales
+
+def run_token_scales(lib, b):
+    p = lib.plan(b.indptr, b.indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                 b.head_dim, b.page_size, q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype)
+    o, lse = p.run_token_scales(b.q, b.paged_kv, b.extra["k_scales"], b.extra["v_scales"])
+    torch.cuda.synchronize()
+    return p, o, lse
+
+
+@pytest.mark.parametrize("q_dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+@pytest.mark.parametrize("group", [2, 4, 8])
+def test_token_scales_small(lib, cuda, q_dtype, group):
+    b = W.make_batch(batch_lengths=[1, 0, 16, 17, 250, 1000, 33, 611], num_qo_heads=2 * group,
+                     num_kv_heads=2, head_dim=128, q_dtype=q_dtype,
+                     kv_dtype=torch.float8_e4m3fn, seed=40 + group, device=cuda, pool_pages=200,
+                     token_scales=True)
+    p, o, lse = run_token_scales(lib, b)
+    assert p.check() == 0
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, TOL[torch.float8_e4m3fn])
+
+
+def test_token_scales_uniform_match_per_tensor(lib, cuda):
+    """All per-token scales equal to c give the per-tensor result with scale c."""
+    b = W.make_batch(batch_lengths=[300, 2000, 7], num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                     q_dtype=torch.bfloat16, kv_dtype=torch.float8_e4m3fn, seed=44, device=cuda,
+                     token_scales=True)
+    ks = torch.full_like(b.extra["k_scales"], 0.0078125)
+    vs = torch.full_like(b.extra["v_scales"], 0.25)
+    p = lib.plan(b.indptr, b.indices, b.last_page_len, 32, 8, 128, 16,
+                 q_data_type=torch.bfloat16, kv_data_type=torch.float8_e4m3fn)
+    o1, l1 = p.run_token_scales(b.q, b.paged_kv, ks, vs)
+    o2, l2 = p.run(b.q, b.paged_kv, k_scale=0.0078125, v_scale=0.25)
+    torch.cuda.synchronize()
+    assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+    assert (l1 - l2).abs().max().item() <= 1e-4
+
+
+def test_token_scales_unsupported(lib, cuda):
+    idx = torch.zeros(1, dtype=torch.int32, device=cuda)
+    kv = torch.zeros((1, 2, 16, 8, 128), dtype=torch.float8_e4m3fn, device=cuda)
+    sc = torch.ones((1, 8, 16), dtype=torch.float32, device=cuda)
+    q = torch.zeros((1, 8, 128), dtype=torch.bfloat16, device=cuda)
+    p = lib.plan([0, 1], idx, [1], 8, 8, 128, 16, q_data_type=torch.bfloat16,
+                 kv_data_type=torch.float8_e4m3fn)          # group 1: CUDA-core consumer only
+    with pytest.raises(lib.FaError) as e:
+        p.run_token_scales(q, kv, sc, sc)
+    assert e.value.status == -2
+    kvb = torch.zeros((1, 2, 16, 8, 128), dtype=torch.bfloat16, device=cuda)
+    pb = lib.plan([0, 1], idx, [1], 8, 8, 128, 16, q_data_type=torch.bfloat16)
+    rc = lib.library().fa_decode_run_token_scales(pb._h, q.data_ptr(), kvb.data_ptr(), 1, 0.0,
+                                                  sc.data_ptr(), sc.data_ptr(),
+                                                  torch.empty_like(q).data_ptr(), None,
+                                                  torch.cuda.current_stream().cuda_stream)
+    assert rc == -2   # bf16 KV has no per-token scales
+
+
 # ------------------------------------------------------------------ merge_states
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
@@ -230,10 +288,14 @@ def _sample_requests(b, k=6):
     return sorted(picks)
 
 
-@pytest.mark.parametrize("name", ["gqa_uniform", "ragged", "long_split", "fp8_kv"])
+@pytest.mark.parametrize("name", ["gqa_uniform", "ragged", "long_split", "fp8_kv",
+                                  "fp8_kv_token_scales"])
 def test_full_size_workloads_sampled(lib, cuda, name):
     b = W.make_config_batch(name, device=cuda)
-    p, o, lse = run_lib(lib, b)
+    if "k_scales" in b.extra:
+        p, o, lse = run_token_scales(lib, b)
+    else:
+        p, o, lse = run_lib(lib, b)
     assert p.check() == 0
     check_coverage(p, b)
     rows = _sample_requests(b)
