@@ -35,13 +35,20 @@ def run_lib(fa, b, workspace=None, **kw):
     return p, o, lse
 
 
-def compare(o, lse, ref_o, ref_lse, tol, rows=None):
+def compare(o, lse, ref_o, ref_lse, tol, rows=None, rel=0.0):
+    """Max-abs check of o and lse; rel adds rel * |oracle o| to the o bound
+    (for outputs whose magnitude makes the output dtype's own rounding
+    exceed tol)."""
     o = o.float().cpu().numpy().astype(np.float64)
     lse = lse.cpu().numpy().astype(np.float64)
     if rows is not None:
         o, lse = o[rows], lse[rows]
     empty = np.isneginf(ref_lse)
     assert np.array_equal(np.isneginf(lse), empty), "empty requests must give lse = -inf"
+    if rel and o.size:
+        excess = (np.abs(o - ref_o) - rel * np.abs(ref_o)).max()
+        assert excess <= tol, f"max |o - oracle| - {rel}|oracle| = {excess:.3g} > {tol}"
+        o = ref_o  # checked
     err_o = np.abs(o - ref_o).max() if o.size else 0.0
     err_l = np.abs(lse[~empty] - ref_lse[~empty]).max() if (~empty).any() else 0.0
     assert err_o <= tol, f"max |o - oracle| = {err_o:.3g} > {tol}"
@@ -194,6 +201,12 @@ def test_unsupported_rejected(lib, cuda):
 
 # ------------------------------------------------------------------ per-token FP8 scales
 
+# Per-token magnitudes up to 2^3 make |o| reach tens, where a bf16 output's
+# own rounding (half an ulp: 2^-9 relative) exceeds the absolute bound, so
+# this workload is checked against abs 3e-2 + 2^-8 * |oracle o|.
+TOKEN_SCALE_REL = 2.0 ** -8
+
+
 def run_token_scales(lib, b):
     p = lib.plan(b.indptr, b.indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                  b.head_dim, b.page_size, q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype)
@@ -212,7 +225,7 @@ def test_token_scales_small(lib, cuda, q_dtype, group):
     p, o, lse = run_token_scales(lib, b)
     assert p.check() == 0
     ref_o, ref_lse = oracle_decode(b)
-    compare(o, lse, ref_o, ref_lse, TOL[torch.float8_e4m3fn])
+    compare(o, lse, ref_o, ref_lse, TOL[torch.float8_e4m3fn], rel=TOKEN_SCALE_REL)
 
 
 def test_token_scales_uniform_match_per_tensor(lib, cuda):
@@ -301,7 +314,8 @@ def test_full_size_workloads_sampled(lib, cuda, name):
     rows = _sample_requests(b)
     sb = sub_batch(b, rows)
     ref_o, ref_lse = oracle_decode(sb)
-    compare(o, lse, ref_o, ref_lse, tol_for(b), rows=rows)
+    compare(o, lse, ref_o, ref_lse, tol_for(b), rows=rows,
+            rel=TOKEN_SCALE_REL if "k_scales" in b.extra else 0.0)
     # properties that hold at any size, on every row
     lse_all = lse.cpu()
     assert torch.isfinite(lse_all).all()
