@@ -130,9 +130,12 @@ struct MmaCfg {
   static constexpr int E = 16 / KV_ES;            // elements per 16-byte granule
   static constexpr int KSTEPS = D / 16;
   static constexpr int MTILES = D / 16;
-  // ring of 64 KB (48 KB at G = 8, whose larger epilogue buffer would
-  // otherwise leave room for only two CTAs per SM), whole stages per warp
-  static constexpr int RING_BYTES = G >= 8 ? 49152 : 65536;
+  // Ring size, whole stages per consumer warp.  16-bit KV: 64 KB (48 KB at
+  // G = 8, whose larger epilogue buffer would otherwise leave room for only
+  // two CTAs per SM), three CTAs per SM.  E4M3 KV: 32 KB (two 4 KB pages per
+  // warp) so that four CTAs fit per SM - its denser per-byte arithmetic needs
+  // the extra warps to hide each page's dependent chain.
+  static constexpr int RING_BYTES = KV_ES == 1 ? 32768 : (G >= 8 ? 49152 : 65536);
   static constexpr int SPW0 = RING_BYTES / STAGE_BYTES / NW;
   static constexpr int SPW = SPW0 < 1 ? 1 : (SPW0 > 4 ? 4 : SPW0);
   static constexpr int S = SPW * NW;
