@@ -205,6 +205,76 @@ int oracle_batch_decode_token_scales(
                      k_scales, v_scales, o, lse, num_threads);
 }
 
+/* Multi-token decode (speculative verification): every request carries
+ * q_len query tokens, q [B, q_len, Hq, D], whose own K/V are the last q_len
+ * positions of its context.  Query token i (0-based) attends to positions
+ * 0 .. len - q_len + i: the context before the draft and the draft tokens up
+ * to itself (the causal rule among the draft tokens).  Outputs
+ * o [B, q_len, Hq, D] and lse [B, q_len, Hq].  Each query row is computed
+ * exactly as decode_impl does for one token, over its own prefix. */
+int oracle_batch_decode_multi(const void* q, int q_dtype, const void* paged_kv,
+                              int kv_dtype, int64_t num_pages,
+                              const int32_t* indptr, const int32_t* indices,
+                              const int32_t* last_page_len, int B, int q_len,
+                              int Hq, int Hkv, int D, int P, double sm_scale,
+                              double k_scale, double v_scale, double* o,
+                              double* lse, int num_threads) {
+  if (q_len < 1 || B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || P <= 0 || Hq % Hkv) return 1;
+  if (indptr[0] != 0) return 1;
+  for (int i = 0; i < B; ++i) {
+    const int np = indptr[i + 1] - indptr[i];
+    if (np < 0) return 1;
+    if (np == 0 || last_page_len[i] < 1 || last_page_len[i] > P) return 1;
+    if ((int64_t)(np - 1) * P + last_page_len[i] < q_len) return 1;
+    for (int p = indptr[i]; p < indptr[i + 1]; ++p)
+      if (indices[p] < 0 || indices[p] >= num_pages) return 1;
+  }
+  const int g = Hq / Hkv;
+  const int64_t units = (int64_t)B * q_len * Hq;
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int64_t u = 0; u < units; ++u) {
+    const int i = (int)(u / ((int64_t)q_len * Hq));
+    const int qi = (int)((u / Hq) % q_len);
+    const int h = (int)(u % Hq);
+    const int kvh = h / g;
+    const int np = indptr[i + 1] - indptr[i];
+    const int64_t len = (int64_t)(np - 1) * P + last_page_len[i];
+    const int64_t visible = len - q_len + qi + 1; /* positions 0 .. len - q_len + qi */
+    double* out = o + u * D;
+    double* s = (double*)malloc(sizeof(double) * visible);
+    for (int64_t t = 0; t < visible; ++t) {
+      const int64_t page = indices[indptr[i] + t / P];
+      const int slot = (int)(t % P);
+      double acc = 0.0;
+      for (int d = 0; d < D; ++d)
+        acc += load_elem(q, q_dtype, u * D + d) * k_scale *
+               load_elem(paged_kv, kv_dtype, kv_offset(page, 0, slot, kvh, d, P, Hkv, D));
+      s[t] = sm_scale * acc;
+    }
+    double m = -INFINITY;
+    for (int64_t t = 0; t < visible; ++t)
+      if (s[t] > m) m = s[t];
+    double den = 0.0;
+    for (int64_t t = 0; t < visible; ++t) den += exp(s[t] - m);
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (int64_t t = 0; t < visible; ++t) {
+      const int64_t page = indices[indptr[i] + t / P];
+      const int slot = (int)(t % P);
+      const double w = exp(s[t] - m);
+      for (int d = 0; d < D; ++d)
+        out[d] += w * v_scale *
+                  load_elem(paged_kv, kv_dtype, kv_offset(page, 1, slot, kvh, d, P, Hkv, D));
+    }
+    for (int d = 0; d < D; ++d) out[d] /= den;
+    lse[u] = m + log(den);
+    free(s);
+  }
+  return 0;
+}
+
 /* ---- merge of partial states -------------------------------------------- */
 
 /* Each state is stored as a normalised output o_x (length D) with its

@@ -333,6 +333,66 @@ def pin_token_scales_uniform(orc):
     np.testing.assert_array_equal(a[1], b[1])
 
 
+def _multi_batch(seed, lens=(5, 16, 17, 40), q_len=3, Hq=4, Hkv=2, D=8, P=4):
+    rng = np.random.default_rng(seed)
+    K = [rng.standard_normal((n, Hkv, D)).astype(np.float32) for n in lens]
+    V = [rng.standard_normal((n, Hkv, D)).astype(np.float32) for n in lens]
+    kv, indptr, indices, last = dense_pages(K, V, P, perm_seed=seed, pool_extra=2)
+    q = rng.standard_normal((len(lens), q_len, Hq, D)).astype(np.float32)
+    return q, K, V, kv, indptr, indices, last, lens, (q_len, Hq, Hkv, D, P)
+
+
+def pin_multi_token_truncation(orc):
+    """Query token i of a request equals single-token decode over the request
+    cut after position len - q_len + i (same pages, shorter last page)."""
+    q, K, V, kv, indptr, indices, last, lens, (ql, Hq, Hkv, D, P) = _multi_batch(15)
+    o, lse = orc.batch_decode_multi(q, oracle.F32, kv, oracle.F32, indptr, indices, last, ql, Hq,
+                                    Hkv, D, P)
+    for r, n in enumerate(lens):
+        for i in range(ql):
+            vis = n - ql + i + 1
+            npg = (vis + P - 1) // P
+            ip = np.array([0, npg], np.int32)
+            ids = indices[indptr[r]:indptr[r] + npg]
+            lp = np.array([vis - (npg - 1) * P], np.int32)
+            o1, l1 = orc.batch_decode(np.ascontiguousarray(q[r, i][None]), oracle.F32, kv,
+                                      oracle.F32, ip, ids, lp, Hq, Hkv, D, P)
+            np.testing.assert_array_equal(o[r, i], o1[0])
+            np.testing.assert_array_equal(lse[r, i], l1[0])
+
+
+def pin_multi_token_causal_dense(orc):
+    """Against torch float64 attention with an explicit causal mask over the
+    draft tokens."""
+    q, K, V, kv, indptr, indices, last, lens, (ql, Hq, Hkv, D, P) = _multi_batch(16, q_len=4)
+    o, lse = orc.batch_decode_multi(q, oracle.F32, kv, oracle.F32, indptr, indices, last, ql, Hq,
+                                    Hkv, D, P)
+    g = Hq // Hkv
+    for r, n in enumerate(lens):
+        Kr = torch.from_numpy(K[r]).double().repeat_interleave(g, 1)   # [n, Hq, D]
+        Vr = torch.from_numpy(V[r]).double().repeat_interleave(g, 1)
+        qd = torch.from_numpy(q[r]).double()                             # [ql, Hq, D]
+        s = torch.einsum("ihd,nhd->ihn", qd, Kr) / math.sqrt(D)
+        pos = torch.arange(n)
+        limit = n - ql + torch.arange(ql)
+        s = s.masked_fill(pos[None, None, :] > limit[:, None, None], -math.inf)
+        np.testing.assert_allclose(o[r], torch.einsum("ihn,nhd->ihd", torch.softmax(s, -1), Vr).numpy(),
+                                   rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[r], torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
+
+
+def pin_multi_token_one_is_decode(orc):
+    q, K, V, kv, indptr, indices, last, lens, (ql, Hq, Hkv, D, P) = _multi_batch(17, q_len=1)
+    a = orc.batch_decode_multi(q, oracle.F32, kv, oracle.F32, indptr, indices, last, 1, Hq, Hkv,
+                               D, P)
+    b = orc.batch_decode(q[:, 0], oracle.F32, kv, oracle.F32, indptr, indices, last, Hq, Hkv, D, P)
+    np.testing.assert_array_equal(a[0][:, 0], b[0])
+    np.testing.assert_array_equal(a[1][:, 0], b[1])
+    with pytest.raises(ValueError):   # a request shorter than q_len
+        orc.batch_decode_multi(np.zeros((4, 6, Hq, D), np.float32), oracle.F32, kv, oracle.F32,
+                               indptr, indices, last, 6, Hq, Hkv, D, P)
+
+
 def pin_empty_request(orc):
     rng = np.random.default_rng(10)
     K = [rng.standard_normal((5, 1, 4)).astype(np.float32)]
@@ -395,7 +455,8 @@ def pin_rejects_bad_args(orc):
     pin_single_key, pin_identical_keys, pin_zero_query, pin_convexity, pin_split_merge,
     pin_gqa_equals_repeated_mha, pin_page_permutation, pin_brute_force, pin_torch_dense,
     pin_empty_request, pin_padding_never_read, pin_golden_decode, pin_rejects_bad_args,
-    pin_token_scales_dense, pin_token_scales_uniform])
+    pin_token_scales_dense, pin_token_scales_uniform, pin_multi_token_truncation,
+    pin_multi_token_causal_dense, pin_multi_token_one_is_decode])
 def test_decode_pins(orc, pin):
     pin(orc)
 
