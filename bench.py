@@ -64,8 +64,8 @@ def algorithmic_bytes(b: W.DecodeBatch) -> int:
     if "k_scales" in b.extra:          # one fp32 K and one V scale per token and kv head
         kv += b.total_tokens * b.num_kv_heads * 2 * 4
     idx = int(b.indptr[-1]) * 4
-    qo = 2 * b.batch * b.num_qo_heads * b.head_dim * q_es
-    lse = b.batch * b.num_qo_heads * 4
+    qo = 2 * b.batch * b.q_len * b.num_qo_heads * b.head_dim * q_es
+    lse = b.batch * b.q_len * b.num_qo_heads * 4
     return int(kv + idx + qo + lse)
 
 
@@ -231,7 +231,7 @@ def bench_reference(args, world, rank):
     for _ in range(args.steps):
         oracle_decode(sb)
     dt = time.perf_counter() - t
-    value = n * args.steps / dt
+    value = n * b.q_len * args.steps / dt
     threads = oracle.max_threads()
     cfg = W.CONFIGS[args.workload]
     desc = f"{n} of {b.batch} requests per step, float64 C oracle, OpenMP {threads} threads"
@@ -251,7 +251,7 @@ def bench_reference(args, world, rank):
 def config_dict(cfg: W.DecodeConfig, b: W.DecodeBatch) -> dict:
     return {"workload": cfg.name, "batch": b.batch, "num_qo_heads": cfg.num_qo_heads,
             "num_kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim,
-            "page_size": cfg.page_size, "q_dtype": DTYPE_NAMES[cfg.q_dtype],
+            "page_size": cfg.page_size, "q_len": cfg.q_len, "q_dtype": DTYPE_NAMES[cfg.q_dtype],
             "kv_dtype": DTYPE_NAMES[cfg.kv_dtype],
             "kv_tokens": b.total_tokens, "mean_seq_len": round(b.total_tokens / max(1, b.batch), 1),
             "kv_bytes": int(b.total_tokens * cfg.num_kv_heads * 2 * cfg.head_dim *
@@ -271,13 +271,22 @@ def bench_ours(args, world, rank, local):
     # plan (amortised), timed on the host including its upload
     torch.cuda.synchronize(dev)
     t = time.perf_counter()
-    p = fa.plan(b.indptr, b.indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
-                b.head_dim, b.page_size, q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype)
+    def make_plan(idx, ws=None):
+        if b.q_len > 1:
+            return fa.plan_multi_token(b.indptr.numpy(), idx, b.last_page_len.numpy(), b.q_len,
+                                       b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size,
+                                       q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype,
+                                       workspace=ws)
+        return fa.plan(b.indptr.numpy(), idx, b.last_page_len.numpy(), b.num_qo_heads,
+                       b.num_kv_heads, b.head_dim, b.page_size, q_data_type=b.q.dtype,
+                       kv_data_type=b.paged_kv.dtype, workspace=ws)
+
+    p = make_plan(b.indices)
     torch.cuda.synchronize(dev)
     plan_ms = (time.perf_counter() - t) * 1e3
     info = p.info
     o = torch.empty_like(b.q)
-    lse = torch.empty((b.batch, b.num_qo_heads), dtype=torch.float32, device=dev)
+    lse = torch.empty(tuple(b.q.shape[:-1]), dtype=torch.float32, device=dev)
     token_scales = "k_scales" in b.extra
 
     def run_step(plan, q):
@@ -332,16 +341,13 @@ def bench_ours(args, world, rank, local):
     lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     q_d = torch.empty_like(b.q)
     idx_d = torch.empty_like(b.indices)
-    ws = torch.empty(fa.workspace_size(b.batch, b.num_qo_heads, b.num_kv_heads, b.head_dim),
-                     dtype=torch.uint8, device=dev)
-    indptr_h, last_h = b.indptr.numpy(), b.last_page_len.numpy()
+    ws = torch.empty(fa.workspace_size(b.batch, b.num_qo_heads * b.q_len, b.num_kv_heads,
+                                       b.head_dim), dtype=torch.uint8, device=dev)
 
     def e2e_step():
         q_d.copy_(q_h, non_blocking=True)
         idx_d.copy_(idx_h, non_blocking=True)
-        pe = fa.plan(indptr_h, idx_d, last_h, b.num_qo_heads, b.num_kv_heads, b.head_dim,
-                     b.page_size, q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype,
-                     workspace=ws)
+        pe = make_plan(idx_d, ws)
         run_step(pe, q_d)
         o_h.copy_(o, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
@@ -365,7 +371,7 @@ def bench_ours(args, world, rank, local):
     alg = algorithmic_bytes(b)
     peak, peak_kind = read_peaks()
     step_s = elapsed_s / args.steps
-    value = world * b.batch * args.steps / elapsed_s
+    value = world * b.batch * b.q_len * args.steps / elapsed_s
     achieved = alg / kern_avg_s / 1e9
     traffic = profiled_traffic(args.workload)
     out = {
@@ -389,7 +395,7 @@ def bench_ours(args, world, rank, local):
                      "kernel": ("fa_decode_mma_kernel" if info["tensor_cores"]
                                 else "fa_decode_split_kernel"),
                      "algorithmic_bytes_per_launch": alg},
-        "e2e": {"value": world * b.batch * e2e_steps / e2e_s, "unit": "tokens/s",
+        "e2e": {"value": world * b.batch * b.q_len * e2e_steps / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "steps": e2e_steps, "includes": "H2D q + indices, plan, run, D2H o + lse"},
         "gpu_launches": args.steps * launches_per_step,
@@ -397,7 +403,7 @@ def bench_ours(args, world, rank, local):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n, dt, toks, threads, desc = oracle_timing(b, target_s=args.cpu_seconds)
-        out["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": threads,
+        out["cpu_baseline"] = {"value": n * b.q_len / dt, "unit": "tokens/s", "cores": threads,
                                "kind": "oracle", "sample": desc,
                                "kv_tokens_per_s": toks / dt}
     return out

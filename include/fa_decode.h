@@ -107,6 +107,33 @@ int fa_decode_plan(const int32_t* indptr_host, const int32_t* indices_dev,
                    void* workspace_dev, size_t workspace_bytes,
                    void* cuda_stream, fa_decode_plan_t* out_plan);
 
+/* plan for multi-token decode (speculative verification): every request
+ * carries q_len query tokens - the draft tokens of speculative decoding, "a
+ * handful with speculative decoding" in the page "FlashDecoding + FlashInfer"
+ * (section "FlashDecoding + FlashInfer") - whose own K and V are already the
+ * last q_len positions of its cache.  Query token i (0-based) attends to
+ * positions 0 .. len - q_len + i: the context and the draft tokens up to
+ * itself.  A later fa_decode_run of this plan takes
+ *      q    [batch, q_len, num_qo_heads, head_dim]
+ *      o    [batch, q_len, num_qo_heads, head_dim]
+ *      lse  [batch, q_len, num_qo_heads]
+ * Arguments otherwise as fa_decode_plan; every request needs len >= q_len
+ * (FA_ERR_INVALID_ARG otherwise).  The workspace bound is
+ * fa_decode_workspace_size(batch, num_qo_heads * q_len, num_kv_heads,
+ * head_dim).  Built for head_dim 128, (q, kv) = (BF16, BF16) or
+ * (BF16, E4M3), and (num_qo_heads / num_kv_heads) * q_len <= 8 with q_len
+ * in {2, 4, 8}: group 1 with q_len 2, 4, 8; group 2 with 2, 4; group 4
+ * with 2.  Other combinations return FA_ERR_UNSUPPORTED.  q_len = 1 is
+ * fa_decode_plan. */
+int fa_decode_plan_multi_token(const int32_t* indptr_host,
+                               const int32_t* indices_dev,
+                               const int32_t* last_page_len_host, int batch,
+                               int q_len, int num_qo_heads, int num_kv_heads,
+                               int head_dim, int page_size, fa_dtype q_dtype,
+                               fa_dtype kv_dtype, void* workspace_dev,
+                               size_t workspace_bytes, void* cuda_stream,
+                               fa_decode_plan_t* out_plan);
+
 /* run: decode attention for one query token per request (page "FlashDecoding
  * + FlashInfer", section "FlashDecoding - the split-KV trick": every chunk of
  * the KV axis yields a partial (m, d, o), and a small reduction combines the
@@ -191,6 +218,7 @@ typedef struct {
   size_t plan_upload_bytes;   /* bytes fa_decode_plan copies host -> device */
   int tensor_cores;           /* 1: per-page products on mma.sync, 0: CUDA cores */
   int fused_merge;            /* 1: split requests merged inside the decode kernel */
+  int q_len;                  /* query tokens per request */
 } fa_plan_info;
 
 int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info);
@@ -199,11 +227,13 @@ int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info);
  *  cta_offsets  [num_ctas+1]: CTA c runs segments cta_offsets[c] .. [c+1]-1
  *  segments     [num_segments * FA_SEGMENT_INTS] int32, each
  *               {request, kv_head, page_begin, page_end, last_valid,
- *                out_slot, merge_unit, 0}; page_begin/page_end index the
- *               indices array, last_valid = valid slots of the segment's
- *               final page, out_slot = -1 when the segment covers its whole
- *               request, else the partial-state slot it writes, and
- *               merge_unit = its row of the merge table (-1 when unsplit).
+ *                out_slot, merge_unit, to_end}; page_begin/page_end index
+ *               the indices array, last_valid = valid slots of the
+ *               segment's final page, out_slot = -1 when the segment covers
+ *               its whole request, else the partial-state slot it writes,
+ *               merge_unit = its row of the merge table (-1 when unsplit),
+ *               to_end = tokens from the segment's first token to the end
+ *               of its request.
  *  merge        [num_merge_units * FA_MERGE_INTS] int32, each
  *               {request, kv_head, first_slot, num_slots}. */
 #define FA_SEGMENT_INTS 8

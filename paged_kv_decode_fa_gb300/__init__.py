@@ -20,7 +20,7 @@ import numpy as np
 import torch
 
 __all__ = [
-    "FA_OK", "FaError", "DecodePlan", "plan", "run", "merge_states",
+    "FA_OK", "FaError", "DecodePlan", "plan", "plan_multi_token", "run", "merge_states",
     "workspace_size", "plan_work_host", "BatchDecodeWithPagedKVCacheWrapper",
     "LIB_PATH", "EXPORTED_SYMBOLS", "library",
 ]
@@ -34,7 +34,7 @@ EXPORTED_SYMBOLS = (
     "fa_decode_run", "fa_merge_states", "fa_decode_plan_destroy",
     "fa_decode_plan_get_info", "fa_decode_plan_get_work", "fa_plan_work_host",
     "fa_decode_check", "fa_decode_set_timing_events", "fa_decode_static",
-    "fa_decode_run_token_scales",
+    "fa_decode_run_token_scales", "fa_decode_plan_multi_token",
 )
 
 FA_OK = 0
@@ -56,7 +56,7 @@ class PlanInfo(ctypes.Structure):
         "num_partial_slots", "threads_per_cta", "smem_bytes_per_cta", "stages")] + [
         ("total_pages", ctypes.c_int64), ("total_tokens", ctypes.c_int64),
         ("workspace_bytes_used", ctypes.c_size_t), ("plan_upload_bytes", ctypes.c_size_t),
-        ("tensor_cores", ctypes.c_int), ("fused_merge", ctypes.c_int)]
+        ("tensor_cores", ctypes.c_int), ("fused_merge", ctypes.c_int), ("q_len", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -73,6 +73,9 @@ def _load() -> ctypes.CDLL:
     lib.fa_decode_plan.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                    P, sz, P, ctypes.POINTER(P)]
     lib.fa_decode_plan.restype = i32
+    lib.fa_decode_plan_multi_token.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                                               P, sz, P, ctypes.POINTER(P)]
+    lib.fa_decode_plan_multi_token.restype = i32
     lib.fa_decode_run.argtypes = [P, P, P, i64, f32, f32, f32, P, P, P]
     lib.fa_decode_run.restype = i32
     lib.fa_decode_run_token_scales.argtypes = [P, P, P, i64, f32, P, P, P, P, P]
@@ -153,13 +156,18 @@ class DecodePlan:
     """A planned decode batch.  Holds the library's plan handle and keeps the
     tensors it refers to (indices, workspace) alive."""
 
-    def __init__(self, handle, indices, workspace, q_dtype, kv_dtype, shape):
+    def __init__(self, handle, indices, workspace, q_dtype, kv_dtype, shape, q_len=1):
         self._h = handle
         self._indices = indices
         self._workspace = workspace
         self.q_dtype = q_dtype
         self.kv_dtype = kv_dtype
+        self.q_len = q_len
         self.batch, self.num_qo_heads, self.num_kv_heads, self.head_dim, self.page_size = shape
+
+    def _q_shape(self):
+        B, Hq, D = self.batch, self.num_qo_heads, self.head_dim
+        return (B, Hq, D) if self.q_len == 1 else (B, self.q_len, Hq, D)
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -193,20 +201,20 @@ class DecodePlan:
             k_scale: float = 1.0, v_scale: float = 1.0, out: torch.Tensor | None = None,
             lse: torch.Tensor | None = None, return_lse: bool = True, stream=None):
         """Decode attention; returns (o, lse) (lse None if return_lse is False)."""
-        B, Hq, D = self.batch, self.num_qo_heads, self.head_dim
+        D = self.head_dim
         if q.dtype != self.q_dtype or paged_kv.dtype != self.kv_dtype:
             raise TypeError("q / paged_kv dtype differs from the plan")
-        if tuple(q.shape) != (B, Hq, D) or not q.is_contiguous() or not q.is_cuda:
-            raise ValueError(f"q must be a contiguous CUDA tensor [{B}, {Hq}, {D}]")
+        if tuple(q.shape) != self._q_shape() or not q.is_contiguous() or not q.is_cuda:
+            raise ValueError(f"q must be a contiguous CUDA tensor {list(self._q_shape())}")
         if (paged_kv.dim() != 5 or paged_kv.shape[1] != 2 or paged_kv.shape[2] != self.page_size
                 or paged_kv.shape[3] != self.num_kv_heads or paged_kv.shape[4] != D
                 or not paged_kv.is_contiguous() or not paged_kv.is_cuda):
             raise ValueError("paged_kv must be a contiguous CUDA tensor "
                              "[num_pages, 2, page_size, num_kv_heads, head_dim]")
         if out is None:
-            out = torch.empty((B, Hq, D), dtype=q.dtype, device=q.device)
+            out = torch.empty(self._q_shape(), dtype=q.dtype, device=q.device)
         if return_lse and lse is None:
-            lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+            lse = torch.empty(self._q_shape()[:-1], dtype=torch.float32, device=q.device)
         _check(_L().fa_decode_run(
             self._h, q.data_ptr(), paged_kv.data_ptr(), paged_kv.shape[0],
             0.0 if sm_scale is None else float(sm_scale), float(k_scale), float(v_scale),
@@ -287,6 +295,34 @@ def plan(indptr, indices: torch.Tensor, last_page_len, num_qo_heads: int, num_kv
         ctypes.byref(handle)), "fa_decode_plan")
     return DecodePlan(handle.value, indices, workspace, q_data_type, kv_data_type,
                       (B, num_qo_heads, num_kv_heads, head_dim, page_size))
+
+
+def plan_multi_token(indptr, indices: torch.Tensor, last_page_len, q_len: int, num_qo_heads: int,
+                     num_kv_heads: int, head_dim: int, page_size: int, *,
+                     q_data_type=torch.bfloat16, kv_data_type=None,
+                     workspace: torch.Tensor | None = None, stream=None) -> DecodePlan:
+    """Plan multi-token decode: q_len query tokens per request (the last q_len
+    cache positions), query token i attending to positions <= len - q_len + i.
+    run() then takes q [B, q_len, Hq, D] and returns o of that shape and lse
+    [B, q_len, Hq]."""
+    kv_data_type = q_data_type if kv_data_type is None else kv_data_type
+    indptr_h = _host_i32(indptr)
+    last_h = _host_i32(last_page_len)
+    B = indptr_h.shape[0] - 1
+    if indices.dtype != torch.int32 or not indices.is_cuda or not indices.is_contiguous():
+        raise ValueError("indices must be a contiguous int32 CUDA tensor")
+    if workspace is None:
+        workspace = torch.empty(workspace_size(B, num_qo_heads * q_len, num_kv_heads, head_dim),
+                                dtype=torch.uint8, device=indices.device)
+    handle = ctypes.c_void_p()
+    _check(_L().fa_decode_plan_multi_token(
+        indptr_h.ctypes.data, indices.data_ptr() if indices.numel() else None,
+        last_h.ctypes.data if B else None, B, q_len, num_qo_heads, num_kv_heads, head_dim,
+        page_size, _dtype_code(q_data_type), _dtype_code(kv_data_type), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream),
+        ctypes.byref(handle)), "fa_decode_plan_multi_token")
+    return DecodePlan(handle.value, indices, workspace, q_data_type, kv_data_type,
+                      (B, num_qo_heads, num_kv_heads, head_dim, page_size), q_len=q_len)
 
 
 def run(p: DecodePlan, q, paged_kv, **kw):

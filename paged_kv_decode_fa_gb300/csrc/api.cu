@@ -190,6 +190,7 @@ struct fa_decode_plan_s {
   size_t ws_bytes = 0;
   Layout layout{};
   bool fused_merge = true;
+  int q_len = 1;
   // E4M3 plans: the variant that reads per-token scales, if one is built
   DecodeKernel kern_ts;
   bool has_ts = false;
@@ -250,11 +251,41 @@ int fa_plan_work_host(const int32_t* indptr, const int32_t* last_page_len, int b
   return FA_OK;
 }
 
+static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
+                     const int32_t* last_page_len_host, int batch, int q_len, int num_qo_heads,
+                     int num_kv_heads, int head_dim, int page_size, fa_dtype q_dtype,
+                     fa_dtype kv_dtype, void* workspace_dev, size_t workspace_bytes,
+                     void* cuda_stream, fa_decode_plan_t* out_plan);
+
 int fa_decode_plan(const int32_t* indptr_host, const int32_t* indices_dev,
                    const int32_t* last_page_len_host, int batch, int num_qo_heads,
                    int num_kv_heads, int head_dim, int page_size, fa_dtype q_dtype,
                    fa_dtype kv_dtype, void* workspace_dev, size_t workspace_bytes,
                    void* cuda_stream, fa_decode_plan_t* out_plan) {
+  return plan_impl(indptr_host, indices_dev, last_page_len_host, batch, 1, num_qo_heads,
+                   num_kv_heads, head_dim, page_size, q_dtype, kv_dtype, workspace_dev,
+                   workspace_bytes, cuda_stream, out_plan);
+}
+
+int fa_decode_plan_multi_token(const int32_t* indptr_host, const int32_t* indices_dev,
+                               const int32_t* last_page_len_host, int batch, int q_len,
+                               int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                               fa_dtype q_dtype, fa_dtype kv_dtype, void* workspace_dev,
+                               size_t workspace_bytes, void* cuda_stream,
+                               fa_decode_plan_t* out_plan) {
+  if (q_len < 1) return FA_ERR_INVALID_ARG;
+  return plan_impl(indptr_host, indices_dev, last_page_len_host, batch, q_len, num_qo_heads,
+                   num_kv_heads, head_dim, page_size, q_dtype, kv_dtype, workspace_dev,
+                   workspace_bytes, cuda_stream, out_plan);
+}
+
+}  // extern "C"
+
+static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
+                     const int32_t* last_page_len_host, int batch, int q_len, int num_qo_heads,
+                     int num_kv_heads, int head_dim, int page_size, fa_dtype q_dtype,
+                     fa_dtype kv_dtype, void* workspace_dev, size_t workspace_bytes,
+                     void* cuda_stream, fa_decode_plan_t* out_plan) {
   if (!out_plan) return FA_ERR_INVALID_ARG;
   *out_plan = nullptr;
   if (!indptr_host || batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
@@ -266,8 +297,26 @@ int fa_decode_plan(const int32_t* indptr_host, const int32_t* indices_dev,
   if (dtype_size(q_dtype) == 0 || dtype_size(kv_dtype) == 0) return FA_ERR_INVALID_ARG;
   const int G = num_qo_heads / num_kv_heads;
   if (page_size != fadecode::kPageSize) return FA_ERR_UNSUPPORTED;
+  if (q_len > 1) {
+    // every request must hold its q_len draft tokens
+    for (int i = 0; i < batch; ++i) {
+      const int64_t np = (int64_t)indptr_host[i + 1] - indptr_host[i];
+      if (np <= 0 || last_page_len_host[i] < 1 || last_page_len_host[i] > page_size ||
+          (np - 1) * page_size + last_page_len_host[i] < q_len)
+        return FA_ERR_INVALID_ARG;
+    }
+  }
   DecodeKernel kern;
-  if (!find_kernel(q_dtype, kv_dtype, head_dim, G, &kern)) return FA_ERR_UNSUPPORTED;
+  if (q_len == 1) {
+    if (!find_kernel(q_dtype, kv_dtype, head_dim, G, &kern)) return FA_ERR_UNSUPPORTED;
+  } else {
+    bool ok = false;
+    if (q_dtype == FA_DTYPE_BF16 && kv_dtype == FA_DTYPE_BF16)
+      ok = fadecode::find_multi_token_kernel_bf16(head_dim, G, q_len, &kern);
+    else if (q_dtype == FA_DTYPE_BF16 && kv_dtype == FA_DTYPE_E4M3)
+      ok = fadecode::find_multi_token_kernel_bf16_e4m3(head_dim, G, q_len, &kern);
+    if (!ok) return FA_ERR_UNSUPPORTED;
+  }
 
   int dev = 0, sms = 0, occ = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -277,7 +326,8 @@ int fa_decode_plan(const int32_t* indptr_host, const int32_t* indices_dev,
   if (occ == 0) return FA_ERR_CUDA;
   // The persistent grid must fit for either variant a run may launch.
   DecodeKernel kern_ts;
-  const bool has_ts = find_token_scale_kernel(q_dtype, kv_dtype, head_dim, G, &kern_ts);
+  const bool has_ts =
+      q_len == 1 && find_token_scale_kernel(q_dtype, kv_dtype, head_dim, G, &kern_ts);
   if (has_ts) {
     const int occ_ts = kernel_occupancy(kern_ts);
     if (occ_ts == 0) return FA_ERR_CUDA;
@@ -305,6 +355,7 @@ int fa_decode_plan(const int32_t* indptr_host, const int32_t* indices_dev,
   plan->fused_merge = fused_merge_enabled();
   plan->kern_ts = kern_ts;
   plan->has_ts = has_ts;
+  plan->q_len = q_len;
 
   int rc = FA_OK;
   try {
@@ -320,7 +371,7 @@ int fa_decode_plan(const int32_t* indptr_host, const int32_t* indices_dev,
   }
   const WorkList& wl = plan->wl;
   plan->layout = make_layout(wl.num_ctas, (int64_t)wl.segments.size(), (int64_t)wl.merge.size(),
-                             wl.num_slots, G, head_dim);
+                             wl.num_slots, G * q_len, head_dim);
   if (plan->layout.total > workspace_bytes) {
     delete plan;
     return FA_ERR_WORKSPACE_TOO_SMALL;
@@ -347,6 +398,8 @@ int fa_decode_plan(const int32_t* indptr_host, const int32_t* indices_dev,
   *out_plan = plan;
   return FA_OK;
 }
+
+extern "C" {
 
 int fa_decode_run(fa_decode_plan_t plan, const void* q, const void* paged_kv, int64_t num_pages,
                   float sm_scale, float k_scale, float v_scale, void* o, float* lse,
@@ -409,6 +462,7 @@ int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info) {
   i.plan_upload_bytes = plan->layout.meta_bytes;
   i.tensor_cores = plan->kern.tensor_cores ? 1 : 0;
   i.fused_merge = plan->fused_merge ? 1 : 0;
+  i.q_len = plan->q_len;
   *info = i;
   return FA_OK;
 }
@@ -480,6 +534,7 @@ static int run_impl(fa_decode_plan_s* plan, bool token_scales, const void* q,
   prm.num_pages = num_pages;
   prm.num_qo_heads = plan->hq;
   prm.num_kv_heads = plan->hkv;
+  prm.q_len = plan->q_len;
   prm.q_scale = sm_scale * k_scale * kLog2e;
   prm.v_scale = v_scale;
 

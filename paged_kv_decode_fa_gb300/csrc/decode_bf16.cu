@@ -6,4 +6,7 @@ namespace fadecode {
 bool find_kernel_bf16(int head_dim, int group, bool allow_mma, DecodeKernel* k) {
   return find_kernel_for<__nv_bfloat16, __nv_bfloat16>(head_dim, group, allow_mma, k);
 }
+bool find_multi_token_kernel_bf16(int head_dim, int group, int q_len, DecodeKernel* k) {
+  return find_multi_token_kernel_for<__nv_bfloat16, __nv_bfloat16>(head_dim, group, q_len, k);
+}
 }  // namespace fadecode

@@ -361,56 +361,64 @@ __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const Deco
 // element); then every output element issues its num_slots loads at once.
 // Runs on `nthreads` threads numbered `tid`, which synchronise on named
 // barrier `bar` (0 = __syncthreads).
-template <typename QT, int D, int G>
+// Output row of column n of a (request, kv head) unit: the unit's columns
+// are the G heads of the group times the QL query tokens, token-major.
+template <int G, int QL>
+__device__ __forceinline__ size_t out_row(int req, int kvh, int n, int num_qo_heads) {
+  return ((size_t)req * QL + n / G) * num_qo_heads + kvh * G + n % G;
+}
+
+template <typename QT, int D, int NC, int G, int QL>
 __device__ __forceinline__ void fold_split_unit(const float* part_o, const float* part_lse,
                                                 int4 u, QT* obase, float* lse_out, int num_qo_heads,
                                                 float* scratch, int scratch_floats, int tid,
                                                 int nthreads, int bar) {
+  static_assert(NC == G * QL, "columns = heads of the group x query tokens");
   const int req = u.x, kvh = u.y, s0 = u.z, ns = u.w;
-  if (ns * G <= scratch_floats) {
+  if (ns * NC <= scratch_floats) {
     // weights w[k][h] = 2^(lse_k - M_h) / den_h, and lse
-    for (int h = tid; h < G; h += nthreads) {
+    for (int h = tid; h < NC; h += nthreads) {
       float M = -INFINITY;
-      for (int k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(part_lse + (size_t)(s0 + k) * G + h));
+      for (int k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(part_lse + (size_t)(s0 + k) * NC + h));
       float den = 0.f;
       if (M != -INFINITY)
         for (int k = 0; k < ns; ++k) {
-          const float w = dev::fast_exp2(__ldcg(part_lse + (size_t)(s0 + k) * G + h) - M);
-          scratch[k * G + h] = w;
+          const float w = dev::fast_exp2(__ldcg(part_lse + (size_t)(s0 + k) * NC + h) - M);
+          scratch[k * NC + h] = w;
           den += w;
         }
       const float inv = den > 0.f ? 1.f / den : 0.f;
-      for (int k = 0; k < ns; ++k) scratch[k * G + h] = M != -INFINITY ? scratch[k * G + h] * inv : 0.f;
+      for (int k = 0; k < ns; ++k) scratch[k * NC + h] = M != -INFINITY ? scratch[k * NC + h] * inv : 0.f;
       if (lse_out)
-        lse_out[(size_t)req * num_qo_heads + kvh * G + h] =
+        lse_out[out_row<G, QL>(req, kvh, h, num_qo_heads)] =
             M != -INFINITY ? (M + dev::fast_log2(den)) * dev::kLn2 : -INFINITY;
     }
     if (bar == 0) __syncthreads(); else dev::named_barrier(bar, nthreads);
-    for (int e = tid; e < G * D; e += nthreads) {
+    for (int e = tid; e < NC * D; e += nthreads) {
       const int h = e / D, dd = e % D;
       float num = 0.f;
       for (int k = 0; k < ns; ++k)
-        num = fmaf(__ldcg(part_o + ((size_t)(s0 + k) * G + h) * D + dd), scratch[k * G + h], num);
-      obase[((size_t)req * num_qo_heads + kvh * G + h) * D + dd] = dev::from_float<QT>(num);
+        num = fmaf(__ldcg(part_o + ((size_t)(s0 + k) * NC + h) * D + dd), scratch[k * NC + h], num);
+      obase[out_row<G, QL>(req, kvh, h, num_qo_heads) * D + dd] = dev::from_float<QT>(num);
     }
     return;
   }
-  for (int e = tid; e < G * D; e += nthreads) {
+  for (int e = tid; e < NC * D; e += nthreads) {
     const int h = e / D, dd = e % D;
     float M = -INFINITY;
-    for (int k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(part_lse + (size_t)(s0 + k) * G + h));
+    for (int k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(part_lse + (size_t)(s0 + k) * NC + h));
     float out = 0.f, lse2 = -INFINITY;
     if (M != -INFINITY) {
       float den = 0.f, num = 0.f;
       for (int k = 0; k < ns; ++k) {
-        const float w = dev::fast_exp2(__ldcg(part_lse + (size_t)(s0 + k) * G + h) - M);
+        const float w = dev::fast_exp2(__ldcg(part_lse + (size_t)(s0 + k) * NC + h) - M);
         den += w;
-        num = fmaf(__ldcg(part_o + ((size_t)(s0 + k) * G + h) * D + dd), w, num);
+        num = fmaf(__ldcg(part_o + ((size_t)(s0 + k) * NC + h) * D + dd), w, num);
       }
       out = num / den;
       lse2 = M + dev::fast_log2(den);
     }
-    const size_t row = (size_t)req * num_qo_heads + kvh * G + h;
+    const size_t row = out_row<G, QL>(req, kvh, h, num_qo_heads);
     obase[row * D + dd] = dev::from_float<QT>(out);
     if (dd == 0 && lse_out) lse_out[row] = lse2 * dev::kLn2;
   }
@@ -421,37 +429,38 @@ __device__ __forceinline__ void fold_split_unit(const float* part_o, const float
 // md[w][h], all log2 domain) with the merge rule and write either the final
 // o (q dtype) and lse, or an fp32 partial slot.  Runs on the NW*32 consumer
 // threads between two consumer barriers.
-template <typename QT, int D, int G, int NW>
+template <typename QT, int D, int G, int NW, int QL = 1>
 __device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const float* mo,
                                                  const float* mm, const float* md, int req,
                                                  int kvh, int out_slot, int merge_unit,
                                                  int* flag) {
   constexpr int CT = NW * 32;
+  constexpr int NC = G * QL;  // columns: heads of the group x query tokens
   QT* __restrict__ obase = static_cast<QT*>(p.o);
-  for (int e = threadIdx.x; e < G * D; e += CT) {
+  for (int e = threadIdx.x; e < NC * D; e += CT) {
     const int h = e / D, dd = e % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * G + h]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * NC + h]);
     float out = 0.f, lse2 = -INFINITY;
     if (M != -INFINITY) {
       float den = 0.f, num = 0.f;
 #pragma unroll
       for (int w = 0; w < NW; ++w) {
-        const float sw = dev::fast_exp2(mm[w * G + h] - M);
-        den = fmaf(md[w * G + h], sw, den);
-        num = fmaf(mo[(w * G + h) * D + dd], sw, num);
+        const float sw = dev::fast_exp2(mm[w * NC + h] - M);
+        den = fmaf(md[w * NC + h], sw, den);
+        num = fmaf(mo[(w * NC + h) * D + dd], sw, num);
       }
       out = num / den * p.v_scale;
       lse2 = M + dev::fast_log2(den);
     }
     if (out_slot < 0) {
-      const size_t row = (size_t)req * p.num_qo_heads + kvh * G + h;
+      const size_t row = out_row<G, QL>(req, kvh, h, p.num_qo_heads);
       obase[row * D + dd] = dev::from_float<QT>(out);
       if (dd == 0 && p.lse) p.lse[row] = lse2 * dev::kLn2;
     } else {
-      p.part_o[((size_t)out_slot * G + h) * D + dd] = out;
-      if (dd == 0) p.part_lse[(size_t)out_slot * G + h] = lse2;
+      p.part_o[((size_t)out_slot * NC + h) * D + dd] = out;
+      if (dd == 0) p.part_lse[(size_t)out_slot * NC + h] = lse2;
     }
   }
   if (out_slot < 0 || !p.fused_merge) return;
@@ -474,8 +483,8 @@ __device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const fl
   dev::named_barrier(1, CT);
   if (!*flag) return;
   const int4 u = reinterpret_cast<const int4*>(p.merge)[merge_unit];
-  fold_split_unit<QT, D, G>(p.part_o, p.part_lse, u, obase, p.lse, p.num_qo_heads,
-                            const_cast<float*>(mo), NW * G * D, threadIdx.x, CT, 1);
+  fold_split_unit<QT, D, NC, G, QL>(p.part_o, p.part_lse, u, obase, p.lse, p.num_qo_heads,
+                                    const_cast<float*>(mo), NW * NC * D, threadIdx.x, CT, 1);
 }
 
 template <typename QT, typename KVT, int D, int G, int NW>
@@ -677,12 +686,12 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
 
 // Split-level merge as a separate kernel: one CTA per (request, kv head)
 // that the planner split folds its partial states with the merge rule.
-template <typename QT, int D, int G>
+template <typename QT, int D, int G, int QL = 1>
 __global__ void __launch_bounds__(128) fa_merge_partials_kernel(const MergeParams p) {
   __shared__ float weights[2048];
   const int4 u = reinterpret_cast<const int4*>(p.merge)[blockIdx.x];
-  fold_split_unit<QT, D, G>(p.part_o, p.part_lse, u, static_cast<QT*>(p.o), p.lse,
-                            p.num_qo_heads, weights, 2048, threadIdx.x, blockDim.x, 0);
+  fold_split_unit<QT, D, G * QL, G, QL>(p.part_o, p.part_lse, u, static_cast<QT*>(p.o), p.lse,
+                                        p.num_qo_heads, weights, 2048, threadIdx.x, blockDim.x, 0);
 }
 
 template <typename QT, typename KVT, int D, int G, int NW = 4>

@@ -115,8 +115,9 @@ __device__ __forceinline__ float2 unpack2(uint32_t w, bool bf16) {
 
 }  // namespace mma
 
-template <typename QT, typename KVT, int D, int G, int NW, bool TS = false>
+template <typename QT, typename KVT, int D, int G, int NW, bool TS = false, int QL = 1>
 struct MmaCfg {
+  static constexpr int NC = G * QL;  // MMA columns: heads of the group x query tokens
   static constexpr int P = kPageSize;
   static constexpr int KV_ES = sizeof(KVT);
   static constexpr bool kFp8 = KV_ES == 1;
@@ -135,7 +136,7 @@ struct MmaCfg {
   // two CTAs per SM), three CTAs per SM.  E4M3 KV: 32 KB (two 4 KB pages per
   // warp) so that four CTAs fit per SM - its denser per-byte arithmetic needs
   // the extra warps to hide each page's dependent chain.
-  static constexpr int RING_BYTES = KV_ES == 1 ? 32768 : (G >= 8 ? 49152 : 65536);
+  static constexpr int RING_BYTES = KV_ES == 1 ? 32768 : (NC >= 8 ? 49152 : 65536);
   static constexpr int SPW0 = RING_BYTES / STAGE_BYTES / NW;
   static constexpr int SPW = SPW0 < 1 ? 1 : (SPW0 > 4 ? 4 : SPW0);
   static constexpr int S = SPW * NW;
@@ -144,23 +145,24 @@ struct MmaCfg {
   static constexpr int OFF_EMPTY = OFF_FULL + 8 * S;
   static constexpr int OFF_PT = OFF_EMPTY + 8 * S;          // [NW][8 heads][16 tokens] 16-bit
   static constexpr int OFF_MO = OFF_PT + NW * 8 * P * 2;
-  static constexpr int OFF_MM = OFF_MO + 4 * NW * G * D;
-  static constexpr int OFF_MD = OFF_MM + 4 * NW * G;
-  static constexpr int OFF_FLAG = OFF_MD + 4 * NW * G;
+  static constexpr int OFF_MM = OFF_MO + 4 * NW * NC * D;
+  static constexpr int OFF_MD = OFF_MM + 4 * NW * NC;
+  static constexpr int OFF_FLAG = OFF_MD + 4 * NW * NC;
   static constexpr int OFF_SCALES = OFF_FLAG + 16;                 // [S][32] fp32 if TS
   static constexpr int SMEM = OFF_SCALES + (TS ? S * 2 * P * 4 : 0);
   static_assert(!TS || kFp8, "per-token scales are for E4M3 KV");
   static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte swizzle rows");
-  static_assert(G >= 1 && G <= 8, "group of at most 8 heads (the MMA N side)");
+  static_assert(NC >= 1 && NC <= 8, "at most 8 columns (the MMA N side)");
   static_assert(STAGE_BYTES % 1024 == 0, "swizzled boxes need 1024-byte alignment");
   static_assert(S % NW == 0, "each ring stage must belong to exactly one consumer warp");
   static_assert(!kFp8 || D % 32 == 0, "E4M3 V is transposed two granules at a time");
 };
 
-template <typename QT, typename KVT, int D, int G, int NW, bool TS>
-__global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS>::THREADS)
+template <typename QT, typename KVT, int D, int G, int NW, bool TS, int QL>
+__global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
     fa_decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
-  using C = MmaCfg<QT, KVT, D, G, NW, TS>;
+  using C = MmaCfg<QT, KVT, D, G, NW, TS, QL>;
+  constexpr int NC = C::NC;
   constexpr int P = C::P, S = C::S, SEGS = C::SEGS, KSTEPS = C::KSTEPS, MTILES = C::MTILES;
   constexpr bool kBf16 = C::kBf16, kFp8 = C::kFp8;
   static_assert(kBf16 ? std::is_same<QT, __nv_bfloat16>::value
@@ -203,8 +205,9 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS>::THREADS)
   float* mo = reinterpret_cast<float*>(smem + C::OFF_MO);
   float* mm = reinterpret_cast<float*>(smem + C::OFF_MM);
   float* md = reinterpret_cast<float*>(smem + C::OFF_MD);
-  const int g = lane >> 2;  // MMA group id: token row g (and g+8), q/P head g
-  const int t = lane & 3;   // thread in group: heads 2t, 2t+1 of the C fragment
+  const int g = lane >> 2;  // MMA group id: token row g (and g+8), q/P column g
+  const int t = lane & 3;   // thread in group: columns 2t, 2t+1 of the C fragment
+  // column n <-> query token n / G, head n % G of the group
   const QT* __restrict__ qbase = static_cast<const QT*>(p.q);
   constexpr int CT = NW * 32;
   const uint32_t ring_addr = dev::smem_addr(ring);
@@ -215,7 +218,14 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS>::THREADS)
     const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * si);
     const int4 sb = *reinterpret_cast<const int4*>(p.segments + 8 * si + 4);
     const int req = sa.x, kvh = sa.y, npg = sa.w - sa.z;
-    const int last_valid = sb.x, out_slot = sb.y;
+    const int last_valid = sb.x, out_slot = sb.y, to_end = sb.w;
+    // causal limits of columns 2t, 2t+1: token position (from the segment
+    // start) after which query token n / G must not look
+    int lim[2] = {0x7fffffff, 0x7fffffff};
+    if constexpr (QL > 1) {
+      lim[0] = to_end - QL + (2 * t) / G;
+      lim[1] = to_end - QL + (2 * t + 1) / G;
+    }
 
     // ---- q as the B fragment of the score MMA, for the whole segment.
     // Reduction step j uses, in lane t, the four dims base(j) .. base(j)+3:
@@ -231,8 +241,9 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS>::THREADS)
 #pragma unroll
         for (int e = 0; e < 4; ++e) qf[j][e] = 0.f;
       uint32_t raw[KSTEPS][2];
-      if (g < G) {
-        const QT* qrow = qbase + ((size_t)req * p.num_qo_heads + kvh * G + g) * D;
+      if (g < NC) {
+        const QT* qrow =
+            qbase + (((size_t)req * QL + g / G) * p.num_qo_heads + kvh * G + g % G) * D;
         // Load L (16 bytes, 8 consecutive elements) feeds reduction steps 2L
         // and 2L+1.  16-bit KV: step j = 4*seg + 2*half + u covers dims
         // seg*BOX_X + (2t + half)*8 + 4u .. +3.  E4M3 KV: step j = 4*half + w
@@ -346,6 +357,13 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS>::THREADS)
       }
       if (g >= valid) s[0] = s[1] = -INFINITY;
       if (g + 8 >= valid) s[2] = s[3] = -INFINITY;
+      if constexpr (QL > 1) {
+        const int pos = lp * P + g;  // token position from the segment start
+        if (pos > lim[0]) s[0] = -INFINITY;
+        if (pos > lim[1]) s[1] = -INFINITY;
+        if (pos + 8 > lim[0]) s[2] = -INFINITY;
+        if (pos + 8 > lim[1]) s[3] = -INFINITY;
+      }
 
       // ---- online softmax for heads 2t (s[0], s[2]) and 2t+1 (s[1], s[3])
       float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
@@ -452,34 +470,34 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS>::THREADS)
     // ---- this warp's state: O^T rows -> dims, heads 2t and 2t+1
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int h = 2 * t + e;
-      if (h < G) {
+      const int h = 2 * t + e;  // column
+      if (h < NC) {
 #pragma unroll
         for (int mt = 0; mt < MTILES; ++mt) {
           const int dlo = kFp8 ? mt * 16 + 2 * g : mt * 16 + g;
           const int dhi = kFp8 ? mt * 16 + 2 * g + 1 : mt * 16 + g + 8;
-          mo[(warp * G + h) * D + dlo] = o[mt][e];
-          mo[(warp * G + h) * D + dhi] = o[mt][2 + e];
+          mo[(warp * NC + h) * D + dlo] = o[mt][e];
+          mo[(warp * NC + h) * D + dhi] = o[mt][2 + e];
         }
         if (g == 0) {
-          mm[warp * G + h] = m_h[e];
-          md[warp * G + h] = d_h[e];
+          mm[warp * NC + h] = m_h[e];
+          md[warp * NC + h] = d_h[e];
         }
       }
     }
     dev::named_barrier(1, CT);
-    combine_and_emit<QT, D, G, NW>(p, mo, mm, md, req, kvh, out_slot, sb.z,
-                                   reinterpret_cast<int*>(smem + C::OFF_FLAG));
+    combine_and_emit<QT, D, G, NW, QL>(p, mo, mm, md, req, kvh, out_slot, sb.z,
+                                       reinterpret_cast<int*>(smem + C::OFF_FLAG));
     dev::named_barrier(1, CT);
     kbase += npg;
   }
 }
 
-template <typename QT, typename KVT, int D, int G, int NW = 4, bool TS = false>
+template <typename QT, typename KVT, int D, int G, int NW = 4, bool TS = false, int QL = 1>
 inline void fill_mma_kernel(DecodeKernel* k) {
-  using C = MmaCfg<QT, KVT, D, G, NW, TS>;
-  k->func = reinterpret_cast<const void*>(&fa_decode_mma_kernel<QT, KVT, D, G, NW, TS>);
-  k->merge_func = reinterpret_cast<const void*>(&fa_merge_partials_kernel<QT, D, G>);
+  using C = MmaCfg<QT, KVT, D, G, NW, TS, QL>;
+  k->func = reinterpret_cast<const void*>(&fa_decode_mma_kernel<QT, KVT, D, G, NW, TS, QL>);
+  k->merge_func = reinterpret_cast<const void*>(&fa_merge_partials_kernel<QT, D, G, QL>);
   k->threads = C::THREADS;
   k->smem_bytes = C::SMEM + 1024;  // room to align the ring to 1024 bytes
   k->stages = C::S;
@@ -490,6 +508,7 @@ inline void fill_mma_kernel(DecodeKernel* k) {
   k->swizzle_128b = true;
   k->tensor_cores = true;
   k->token_scales = TS;
+  k->q_len = QL;
 }
 
 }  // namespace fadecode
@@ -516,6 +535,21 @@ inline bool find_kernel_for(int head_dim, int group, bool allow_mma, DecodeKerne
   FA_CASE(64, 1) FA_CASE(64, 2) FA_CASE(64, 4) FA_CASE(64, 8)
   FA_CASE(128, 1) FA_CASE(128, 2) FA_CASE(128, 4) FA_CASE(128, 8)
 #undef FA_CASE
+  return false;
+}
+
+// Multi-token decode: tensor-core consumer, head_dim 128, group * q_len <= 8.
+template <typename QT, typename KVT>
+inline bool find_multi_token_kernel_for(int head_dim, int group, int q_len, DecodeKernel* k) {
+  if (head_dim != 128) return false;
+#define FA_QL_CASE(GG, QQ)                                 \
+  if (group == GG && q_len == QQ) {                        \
+    fill_mma_kernel<QT, KVT, 128, GG, 4, false, QQ>(k);    \
+    return true;                                           \
+  }
+  FA_QL_CASE(1, 2) FA_QL_CASE(1, 4) FA_QL_CASE(1, 8)
+  FA_QL_CASE(2, 2) FA_QL_CASE(2, 4) FA_QL_CASE(4, 2)
+#undef FA_QL_CASE
   return false;
 }
 

@@ -29,6 +29,7 @@ struct DecodeParams {
   int64_t num_pages;
   int num_qo_heads;
   int num_kv_heads;
+  int q_len;                   // query tokens per request (1 for plain decode)
   float q_scale;  // sm_scale * k_scale * log2(e), folded into q
   float v_scale;
 };
@@ -56,6 +57,7 @@ struct DecodeKernel {
   bool swizzle_128b = false;  // stage rows in TMA 128-byte swizzle order
   bool tensor_cores = false;  // per-page products on mma.sync
   bool token_scales = false;  // reads per-token K/V scales (E4M3 only)
+  int q_len = 1;              // query tokens per request the kernel was built for
 };
 
 // Each returns false when the combination is not compiled.  allow_mma
@@ -66,6 +68,10 @@ bool find_kernel_bf16(int head_dim, int group, bool allow_mma, DecodeKernel* k);
 bool find_kernel_f16(int head_dim, int group, bool allow_mma, DecodeKernel* k);
 bool find_kernel_bf16_e4m3(int head_dim, int group, bool allow_mma, DecodeKernel* k);
 bool find_kernel_f16_e4m3(int head_dim, int group, bool allow_mma, DecodeKernel* k);
+// Multi-token decode (q_len query tokens per request, causal among them):
+// tensor-core consumer, head_dim 128, group * q_len <= 8.
+bool find_multi_token_kernel_bf16(int head_dim, int group, int q_len, DecodeKernel* k);
+bool find_multi_token_kernel_bf16_e4m3(int head_dim, int group, int q_len, DecodeKernel* k);
 // E4M3 KV with per-token, per-kv-head scales (tensor-core consumer only).
 bool find_token_scale_kernel_bf16_e4m3(int head_dim, int group, DecodeKernel* k);
 bool find_token_scale_kernel_f16_e4m3(int head_dim, int group, DecodeKernel* k);

@@ -73,13 +73,14 @@ int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
       }
       const int64_t start = pos, end = pos + np;
       const size_t first = wl.segments.size();
+      const int64_t len = (np - 1) * page_size + last_page_len[i];
       for (int64_t a = start; a < end;) {
         const int64_t cta = a / quota;
         const int64_t b = std::min(end, (cta + 1) * quota);
         const int32_t last = (b == end) ? last_page_len[i] : page_size;
         wl.segments.push_back(Segment{i, h, (int32_t)(pb + (a - start)),
                                       (int32_t)(pb + (b - start)), last, -1, -1,
-                                      0});
+                                      (int32_t)(len - (a - start) * page_size)});
         seg_cta.push_back((int32_t)cta);
         a = b;
       }

@@ -15,7 +15,7 @@ struct Segment {
   int32_t last_valid;  // valid slots in the segment's final page
   int32_t out_slot;    // -1: writes o/lse directly; else partial-state slot
   int32_t merge_unit;  // -1 when unsplit; else index into the merge table
-  int32_t pad;
+  int32_t to_end;      // tokens from the segment's first token to the request end
 };
 static_assert(sizeof(Segment) == 32, "Segment must stay 32 bytes");
 

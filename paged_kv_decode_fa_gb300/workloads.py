@@ -27,6 +27,11 @@ measured on:
                  scale per (page, kv head, slot) = amax over head_dim / 448
                  - the spread that underflows under a single static scale.
 
+``spec_decode``  the gqa_uniform batch with two query tokens per request
+                 (speculative verification of one draft token): q is
+                 [B, 2, Hq, D] and each request's last two cache positions are
+                 the two query tokens' own K/V.
+
 All use page_size 16 and the combined [num_pages, 2, 16, Hkv, D] layout.
 Lengths and page tables come from a CPU ``torch.Generator``; values from a
 generator on the target device, both seeded with the config's seed
@@ -56,6 +61,7 @@ class DecodeConfig:
     kv_dtype: torch.dtype
     seed: int
     page_size: int = PAGE_SIZE
+    q_len: int = 1
 
     @property
     def group(self) -> int:
@@ -70,6 +76,8 @@ CONFIGS: dict[str, DecodeConfig] = {
     "fp8_kv": DecodeConfig("fp8_kv", 128, 64, 8, 128, torch.bfloat16, torch.float8_e4m3fn, 1005),
     "fp8_kv_token_scales": DecodeConfig("fp8_kv_token_scales", 128, 64, 8, 128, torch.bfloat16,
                                         torch.float8_e4m3fn, 1006),
+    "spec_decode": DecodeConfig("spec_decode", 64, 32, 8, 128, torch.bfloat16, torch.bfloat16,
+                                1007, q_len=2),
 }
 
 
@@ -77,7 +85,7 @@ def draw_lengths(cfg: DecodeConfig, gen: torch.Generator) -> np.ndarray:
     """Context length of every request of a named configuration."""
     if cfg.name == "tiny":
         return np.array([17, 64, 100, 255], dtype=np.int64)
-    if cfg.name == "gqa_uniform":
+    if cfg.name in ("gqa_uniform", "spec_decode"):
         return np.full(cfg.batch, 2048, dtype=np.int64)
     if cfg.name == "ragged":
         u = torch.rand(cfg.batch, generator=gen, dtype=torch.float64).numpy()
@@ -93,7 +101,7 @@ def draw_lengths(cfg: DecodeConfig, gen: torch.Generator) -> np.ndarray:
 @dataclass
 class DecodeBatch:
     """One decode batch: device tensors plus host copies of the page table."""
-    q: torch.Tensor                 # [B, Hq, D]
+    q: torch.Tensor                 # [B, Hq, D], or [B, q_len, Hq, D]
     paged_kv: torch.Tensor          # [num_pages, 2, P, Hkv, D]
     indptr: torch.Tensor            # [B+1] int32, host
     indices: torch.Tensor           # [nnz] int32, on the device of paged_kv
@@ -107,6 +115,7 @@ class DecodeBatch:
     v_scale: float = 1.0
     name: str = "custom"
     extra: dict = field(default_factory=dict)
+    q_len: int = 1
 
     @property
     def batch(self) -> int:
@@ -159,13 +168,13 @@ def _fp8_quantise(x: torch.Tensor) -> tuple[torch.Tensor, float]:
 def make_batch(*, batch_lengths, num_qo_heads: int, num_kv_heads: int, head_dim: int,
                q_dtype: torch.dtype, kv_dtype: torch.dtype, seed: int, device="cuda",
                page_size: int = PAGE_SIZE, pool_pages: int | None = None, shuffle: bool = True,
-               name: str = "custom", token_scales: bool = False) -> DecodeBatch:
+               name: str = "custom", token_scales: bool = False, q_len: int = 1) -> DecodeBatch:
     """A seeded batch with explicit lengths (any shape the library supports).
     token_scales=True (E4M3 only) draws per-token magnitudes and stores one
     scale per (page, kv head, slot) in extra["k_scales"] / extra["v_scales"]."""
     gen = torch.Generator().manual_seed(seed)
     return _fill(batch_lengths, gen, num_qo_heads, num_kv_heads, head_dim, q_dtype, kv_dtype,
-                 seed, device, page_size, pool_pages, shuffle, name, token_scales)
+                 seed, device, page_size, pool_pages, shuffle, name, token_scales, q_len)
 
 
 def make_config_batch(name: str, device="cuda") -> DecodeBatch:
@@ -176,7 +185,7 @@ def make_config_batch(name: str, device="cuda") -> DecodeBatch:
     pool = 64 if name == "tiny" else None
     return _fill(lengths, gen, cfg.num_qo_heads, cfg.num_kv_heads, cfg.head_dim, cfg.q_dtype,
                  cfg.kv_dtype, cfg.seed, device, cfg.page_size, pool, True, name,
-                 name == "fp8_kv_token_scales")
+                 name == "fp8_kv_token_scales", cfg.q_len)
 
 
 def _fp8_token_quantise(x: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
@@ -190,13 +199,14 @@ def _fp8_token_quantise(x: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
 
 
 def _fill(lengths, gen, Hq, Hkv, D, q_dtype, kv_dtype, seed, device, P, pool_pages, shuffle,
-          name, token_scales=False) -> DecodeBatch:
+          name, token_scales=False, q_len=1) -> DecodeBatch:
     lengths = np.asarray(lengths, dtype=np.int64)
     indptr, ids, last, pool = page_table(lengths, P, pool_pages, gen, shuffle)
     B = len(lengths)
     dev = torch.device(device)
     vgen = torch.Generator(device=dev).manual_seed(seed)
-    q = torch.randn((B, Hq, D), generator=vgen, device=dev, dtype=torch.float32).to(q_dtype)
+    q_shape = (B, Hq, D) if q_len == 1 else (B, q_len, Hq, D)
+    q = torch.randn(q_shape, generator=vgen, device=dev, dtype=torch.float32).to(q_dtype)
     k_scale = v_scale = 1.0
     extra = {}
     if token_scales:
@@ -225,4 +235,4 @@ def _fill(lengths, gen, Hq, Hkv, D, q_dtype, kv_dtype, seed, device, P, pool_pag
     return DecodeBatch(q=q, paged_kv=kv, indptr=indptr, indices=ids.to(dev),
                        last_page_len=last, lengths=lengths, num_qo_heads=Hq,
                        num_kv_heads=Hkv, head_dim=D, page_size=P, k_scale=k_scale,
-                       v_scale=v_scale, name=name, extra=extra)
+                       v_scale=v_scale, name=name, extra=extra, q_len=q_len)

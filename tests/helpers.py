@@ -33,6 +33,11 @@ def oracle_decode(b: DecodeBatch, orc=None, sm_scale=None, num_threads=0):
     orc = orc or oracle._default()
     q, qc = as_bits(b.q)
     kv, kc = as_bits(b.paged_kv)
+    if b.q_len > 1:
+        return orc.batch_decode_multi(
+            q, qc, kv, kc, b.indptr.numpy(), b.indices.cpu().numpy(), b.last_page_len.numpy(),
+            b.q_len, b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, sm_scale=sm_scale,
+            k_scale=b.k_scale, v_scale=b.v_scale, num_threads=num_threads)
     if "k_scales" in b.extra:
         return orc.batch_decode_token_scales(
             q, qc, kv, kc, b.indptr.numpy(), b.indices.cpu().numpy(), b.last_page_len.numpy(),
@@ -72,7 +77,7 @@ def sub_batch(b: DecodeBatch, requests) -> DecodeBatch:
         last_page_len=b.last_page_len[requests].clone(),
         lengths=b.lengths[requests], num_qo_heads=b.num_qo_heads,
         num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, page_size=b.page_size,
-        k_scale=b.k_scale, v_scale=b.v_scale, name=b.name + "-sub", extra=extra)
+        k_scale=b.k_scale, v_scale=b.v_scale, name=b.name + "-sub", extra=extra, q_len=b.q_len)
 
 
 def dense_pages(K, V, page_size, perm_seed=0, pool_extra=0, pad_value=np.nan):

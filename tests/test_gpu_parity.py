@@ -263,6 +263,45 @@ def test_token_scales_unsupported(lib, cuda):
     assert rc == -2   # bf16 KV has no per-token scales
 
 
+# ------------------------------------------------------------------ multi-token decode
+
+def run_multi(lib, b, workspace=None):
+    p = lib.plan_multi_token(b.indptr, b.indices, b.last_page_len, b.q_len, b.num_qo_heads,
+                             b.num_kv_heads, b.head_dim, b.page_size, q_data_type=b.q.dtype,
+                             kv_data_type=b.paged_kv.dtype, workspace=workspace)
+    o, lse = p.run(b.q, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale)
+    torch.cuda.synchronize()
+    return p, o, lse
+
+
+@pytest.mark.parametrize("kv_dtype", [torch.bfloat16, torch.float8_e4m3fn], ids=["bf16", "e4m3"])
+@pytest.mark.parametrize("group,q_len", [(1, 2), (1, 4), (1, 8), (2, 2), (2, 4), (4, 2)])
+def test_multi_token_small(lib, cuda, kv_dtype, group, q_len):
+    """Draft tokens straddling page boundaries (lengths 8, 9, 17, 33, ...),
+    requests split over CTAs, causal mask among the draft tokens."""
+    b = W.make_batch(batch_lengths=[8, 9, 16, 17, 250, 1000, 33, 611], num_qo_heads=2 * group,
+                     num_kv_heads=2, head_dim=128, q_dtype=torch.bfloat16, kv_dtype=kv_dtype,
+                     seed=60 + group + q_len, device=cuda, pool_pages=200, q_len=q_len)
+    p, o, lse = run_multi(lib, b)
+    assert p.info["q_len"] == q_len and p.check() == 0
+    check_coverage(p, b)
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, tol_for(b))
+
+
+def test_multi_token_rejects(lib, cuda):
+    b = W.make_batch(batch_lengths=[40, 3], num_qo_heads=8, num_kv_heads=2, head_dim=128,
+                     q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, seed=1, device=cuda,
+                     q_len=4)
+    with pytest.raises(lib.FaError) as e:      # request of 3 tokens cannot hold 4 queries
+        run_multi(lib, b)
+    assert e.value.status == -1
+    idx = torch.zeros(1, dtype=torch.int32, device=cuda)
+    with pytest.raises(lib.FaError) as e:      # group 8 x q_len 2 > 8 columns
+        lib.plan_multi_token([0, 1], idx, [16], 2, 64, 8, 128, 16)
+    assert e.value.status == -2
+
+
 # ------------------------------------------------------------------ merge_states
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
@@ -302,11 +341,13 @@ def _sample_requests(b, k=6):
 
 
 @pytest.mark.parametrize("name", ["gqa_uniform", "ragged", "long_split", "fp8_kv",
-                                  "fp8_kv_token_scales"])
+                                  "fp8_kv_token_scales", "spec_decode"])
 def test_full_size_workloads_sampled(lib, cuda, name):
     b = W.make_config_batch(name, device=cuda)
     if "k_scales" in b.extra:
         p, o, lse = run_token_scales(lib, b)
+    elif b.q_len > 1:
+        p, o, lse = run_multi(lib, b)
     else:
         p, o, lse = run_lib(lib, b)
     assert p.check() == 0

@@ -47,12 +47,15 @@ def check_work(lib, indptr, last, Hkv, max_ctas, min_pages=8, P=16):
         assert pages.max() <= quota
         assert np.all(pages[:-1] == quota)     # all but the last CTA are full
         assert n_ctas <= -(-T // min_pages)
-    # last_valid: the page that ends a request carries its last_page_len
+    # last_valid: the page that ends a request carries its last_page_len;
+    # to_end: tokens from the segment's first token to the end of its request
     for s in seg:
         r, pe = s[0], s[3]
         if s[2] < pe:
             want_last = last[r] if pe == indptr[r + 1] else P
             assert s[4] == want_last
+            length = (indptr[r + 1] - indptr[r] - 1) * P + last[r]
+            assert s[7] == length - (s[2] - indptr[r]) * P
     # split units: slots are contiguous, cover the pieces in page order
     slots_seen = []
     for u, (r, h, s0, ns) in enumerate(mer):
