@@ -372,17 +372,20 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
         mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
         mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
       }
-      float alpha[2], pr[4];
+      float alpha[2], pr[4], mref[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const float mn = fmaxf(m_h[e], mx[e]);
-        alpha[e] = dev::fast_exp2(m_h[e] - mn);
+        // a column can have seen nothing yet (every token so far masked by
+        // the causal rule): keep its state empty instead of exp2(-inf + inf)
+        mref[e] = mn == -INFINITY ? 0.f : mn;
+        alpha[e] = dev::fast_exp2(m_h[e] - mref[e]);
         m_h[e] = mn;
       }
-      const uint32_t p01 = mma::pack2(dev::fast_exp2(s[0] - m_h[0]),
-                                      dev::fast_exp2(s[1] - m_h[1]), kBf16);
-      const uint32_t p23 = mma::pack2(dev::fast_exp2(s[2] - m_h[0]),
-                                      dev::fast_exp2(s[3] - m_h[1]), kBf16);
+      const uint32_t p01 = mma::pack2(dev::fast_exp2(s[0] - mref[0]),
+                                      dev::fast_exp2(s[1] - mref[1]), kBf16);
+      const uint32_t p23 = mma::pack2(dev::fast_exp2(s[2] - mref[0]),
+                                      dev::fast_exp2(s[3] - mref[1]), kBf16);
       {
         // sums from the rounded weights, so numerator and denominator agree
         const float2 a = mma::unpack2(p01, kBf16), b = mma::unpack2(p23, kBf16);
