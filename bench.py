@@ -260,12 +260,117 @@ def config_dict(cfg: W.DecodeConfig, b: W.DecodeBatch) -> dict:
             "parallelism": "replicas (one independent batch per GPU)"}
 
 
+def cascade_bytes(b: W.DecodeBatch) -> int:
+    """Algorithmic bytes of a cascade batch: the shared prefix once, every
+    request's own tokens, page ids, q, o and lse."""
+    es = b.paged_kv.element_size()
+    npre = b.extra["prefix_pages"]
+    own_tokens = int(b.lengths.sum()) - b.batch * npre * b.page_size
+    kv = (npre * b.page_size + own_tokens) * b.num_kv_heads * 2 * b.head_dim * es
+    idx = (int(b.indptr[-1]) - (b.batch - 1) * npre) * 4
+    qo = 2 * b.batch * b.num_qo_heads * b.head_dim * b.q.element_size()
+    return int(kv + idx + qo + b.batch * b.num_qo_heads * 4)
+
+
+def bench_cascade(args, world, rank, local, b, cfg, dev):
+    """Cascade decode of a shared-prefix batch, next to plain decode of the
+    same batch (which reads the prefix once per request)."""
+    import paged_kv_decode_fa_gb300 as fa
+    stream = torch.cuda.current_stream(dev)
+    pre, ip, idx, last = W.cascade_parts(b)
+    t = time.perf_counter()
+    p = fa.cascade_plan(pre, ip, idx, last, b.num_qo_heads, b.num_kv_heads, b.head_dim,
+                        b.page_size, q_data_type=b.q.dtype)
+    torch.cuda.synchronize(dev)
+    plan_ms = (time.perf_counter() - t) * 1e3
+    o = torch.empty_like(b.q)
+    lse = torch.empty((b.batch, b.num_qo_heads), dtype=torch.float32, device=dev)
+    plain = fa.plan(b.indptr, b.indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                    b.head_dim, b.page_size, q_data_type=b.q.dtype)
+
+    def timed(fn, steps):
+        for _ in range(args.warmup):
+            fn()
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        z.record(stream)
+        torch.cuda.synchronize(dev)
+        return max_over_ranks(a.elapsed_time(z) / 1e3, world, dev)
+
+    clocks = ClockSampler(local).start()
+    time.sleep(0.3)
+    t0 = time.perf_counter()
+    elapsed_s = timed(lambda: p.run(b.q, b.paged_kv, out=o, lse=lse), args.steps)
+    t1 = time.perf_counter()
+    clocks.stop()
+    if p.check() != 0:
+        raise RuntimeError("device check flagged the cascade batch")
+    plain_s = timed(lambda: plain.run(b.q, b.paged_kv, out=o, lse=lse), args.steps)
+    # end to end: upload q, plan, run, read o and lse back
+    q_h = b.q.cpu().pin_memory()
+    q_d = torch.empty_like(b.q)
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    ws = torch.empty(fa.library().fa_cascade_workspace_size(b.batch, b.num_qo_heads,
+                                                            b.num_kv_heads, b.head_dim),
+                     dtype=torch.uint8, device=dev)
+    e2e_steps = max(1, min(args.steps, 200))
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        pe = fa.cascade_plan(pre, ip, idx, last, b.num_qo_heads, b.num_kv_heads, b.head_dim,
+                             b.page_size, q_data_type=b.q.dtype, workspace=ws)
+        pe.run(q_d, b.paged_kv, out=o, lse=lse)
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        return pe
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    te = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(time.perf_counter() - te, world, dev)
+    alg = cascade_bytes(b)
+    peak, peak_kind = read_peaks()
+    step_s = elapsed_s / args.steps
+    return {
+        "metric": METRIC, "value": world * b.batch * args.steps / elapsed_s, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": DTYPE_NAMES[cfg.kv_dtype], "data": "synthetic",
+        "config": dict(config_dict(cfg, b), prefix_pages=b.extra["prefix_pages"]),
+        "hbm_gbs": alg / step_s / 1e9, "hbm_frac_of_peak": alg / step_s / 1e9 / peak,
+        "peak_kind": peak_kind, "plan_ms": plan_ms,
+        "plain_decode_ms_per_step": plain_s / args.steps * 1e3,
+        "speedup_vs_plain_decode": plain_s / elapsed_s,
+        "roofline": {"bound": "hbm", "achieved": alg / step_s / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": alg / step_s / 1e9 / peak, "traffic": None,
+                     "kernel": "cascade step (suffix decode + fa_prefix_kernel + combine)",
+                     "algorithmic_bytes_per_launch": alg},
+        "e2e": {"value": world * b.batch * e2e_steps / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(q_h.numel() * q_h.element_size()),
+                "d2h_bytes_per_step": int(o_h.numel() * o_h.element_size() + lse_h.numel() * 4),
+                "steps": e2e_steps, "includes": "H2D q, cascade plan, run, D2H o + lse"},
+        "gpu_launches": args.steps * 3,
+        "clocks": clocks.summary(t0, t1),
+    }
+
+
 def bench_ours(args, world, rank, local):
     import paged_kv_decode_fa_gb300 as fa
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     cfg = W.CONFIGS[args.workload]
     b = W.make_config_batch(args.workload, device=dev)
+    if "prefix_pages" in b.extra:
+        return bench_cascade(args, world, rank, local, b, cfg, dev)
     stream = torch.cuda.current_stream(dev)
 
     # plan (amortised), timed on the host including its upload

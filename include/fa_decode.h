@@ -306,6 +306,52 @@ int fa_decode_static(const int32_t* indptr_host, const int32_t* indices_dev,
                      float sm_scale, float k_scale, float v_scale, void* o,
                      float* lse, void* cuda_stream);
 
+/* ---- cascade decode (shared prefix) ------------------------------------
+ *
+ * A batch whose requests all begin with the same shared prefix (whole pages,
+ * e.g. a system prompt or a retrieved document) followed by pages of their
+ * own.  Page "GitHub Spotlight: FlashInfer" (sections "Core Superpowers" and
+ * "Scenario A") describes cascade attention: the shared prefix is attended
+ * once for all requests and combined with each request's own part; the
+ * combination is the merge rule of page "FlashDecoding + FlashInfer",
+ * section "FlashDecoding - the split-KV trick".  The result equals
+ * fa_decode_run over each request's full page list (prefix pages, then its
+ * own), but the prefix is read from HBM once per kv head and block of 128
+ * query rows instead of once per request. */
+typedef struct fa_cascade_plan_s* fa_cascade_plan_t;
+
+/* Upper bound of the workspace fa_cascade_plan needs (current device). */
+size_t fa_cascade_workspace_size(int batch, int num_qo_heads, int num_kv_heads,
+                                 int head_dim);
+
+/*  prefix_indices_dev  [num_prefix_pages] int32, device: the shared pages, in
+ *                      order, all full (num_prefix_pages * page_size tokens).
+ *  indptr_host, indices_dev, last_page_len_host: each request's own pages
+ *                      after the prefix, as in fa_decode_plan (a request may
+ *                      have none).
+ * Both index arrays are kept by pointer for the plan's lifetime.  Supported:
+ * head_dim 128, page_size 16, q and kv both BF16 or both F16; otherwise
+ * FA_ERR_UNSUPPORTED.  Errors as fa_decode_plan. */
+int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
+                    const int32_t* indptr_host, const int32_t* indices_dev,
+                    const int32_t* last_page_len_host, int batch,
+                    int num_qo_heads, int num_kv_heads, int head_dim,
+                    int page_size, fa_dtype q_dtype, fa_dtype kv_dtype,
+                    void* workspace_dev, size_t workspace_bytes,
+                    void* cuda_stream, fa_cascade_plan_t* out_plan);
+
+/* q [batch, num_qo_heads, head_dim], o likewise, lse [batch, num_qo_heads]
+ * (may be NULL); paged_kv and num_pages as fa_decode_run.  Enqueues the
+ * suffix decode, the prefix kernel and the combine kernel on cuda_stream. */
+int fa_cascade_run(fa_cascade_plan_t plan, const void* q, const void* paged_kv,
+                   int64_t num_pages, float sm_scale, void* o, float* lse,
+                   void* cuda_stream);
+
+int fa_cascade_plan_destroy(fa_cascade_plan_t plan);
+
+/* As fa_decode_check, for both passes of a cascade plan. */
+int fa_cascade_check(fa_cascade_plan_t plan, void* cuda_stream, int* flags);
+
 #ifdef __cplusplus
 }
 #endif

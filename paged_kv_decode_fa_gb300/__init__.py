@@ -21,6 +21,7 @@ import torch
 
 __all__ = [
     "FA_OK", "FaError", "DecodePlan", "plan", "plan_multi_token", "run", "merge_states",
+    "CascadePlan", "cascade_plan",
     "workspace_size", "plan_work_host", "BatchDecodeWithPagedKVCacheWrapper",
     "LIB_PATH", "EXPORTED_SYMBOLS", "library",
 ]
@@ -35,6 +36,8 @@ EXPORTED_SYMBOLS = (
     "fa_decode_plan_get_info", "fa_decode_plan_get_work", "fa_plan_work_host",
     "fa_decode_check", "fa_decode_set_timing_events", "fa_decode_static",
     "fa_decode_run_token_scales", "fa_decode_plan_multi_token",
+    "fa_cascade_workspace_size", "fa_cascade_plan", "fa_cascade_run", "fa_cascade_plan_destroy",
+    "fa_cascade_check",
 )
 
 FA_OK = 0
@@ -80,6 +83,17 @@ def _load() -> ctypes.CDLL:
     lib.fa_decode_run.restype = i32
     lib.fa_decode_run_token_scales.argtypes = [P, P, P, i64, f32, P, P, P, P, P]
     lib.fa_decode_run_token_scales.restype = i32
+    lib.fa_cascade_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.fa_cascade_workspace_size.restype = sz
+    lib.fa_cascade_plan.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, i32, i32, i32, P, sz, P,
+                                    ctypes.POINTER(P)]
+    lib.fa_cascade_plan.restype = i32
+    lib.fa_cascade_run.argtypes = [P, P, P, i64, f32, P, P, P]
+    lib.fa_cascade_run.restype = i32
+    lib.fa_cascade_plan_destroy.argtypes = [P]
+    lib.fa_cascade_plan_destroy.restype = i32
+    lib.fa_cascade_check.argtypes = [P, P, ctypes.POINTER(i32)]
+    lib.fa_cascade_check.restype = i32
     lib.fa_merge_states.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, P]
     lib.fa_merge_states.restype = i32
     lib.fa_decode_plan_destroy.argtypes = [P]
@@ -370,6 +384,78 @@ def plan_work_host(indptr, last_page_len, num_kv_heads: int, page_size: int, max
                                   ctypes.byref(n_sl)), "fa_plan_work_host")
     return (cta[: n_c.value + 1].copy(), seg[: n_s.value * SEGMENT_INTS].reshape(-1, SEGMENT_INTS).copy(),
             mer[: n_m.value * MERGE_INTS].reshape(-1, MERGE_INTS).copy(), n_sl.value)
+
+
+class CascadePlan:
+    """A planned cascade batch: one shared prefix of whole pages, then each
+    request's own pages.  Keeps the index tensors and the workspace alive."""
+
+    def __init__(self, handle, keep, q_dtype, shape):
+        self._h = handle
+        self._keep = keep
+        self.q_dtype = q_dtype
+        self.batch, self.num_qo_heads, self.num_kv_heads, self.head_dim = shape
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            _L().fa_cascade_plan_destroy(h)
+            self._h = None
+
+    def run(self, q: torch.Tensor, paged_kv: torch.Tensor, *, sm_scale: float | None = None,
+            out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+            return_lse: bool = True, stream=None):
+        B, Hq, D = self.batch, self.num_qo_heads, self.head_dim
+        if q.dtype != self.q_dtype or paged_kv.dtype != self.q_dtype:
+            raise TypeError("q / paged_kv dtype differs from the plan")
+        if tuple(q.shape) != (B, Hq, D) or not q.is_contiguous() or not paged_kv.is_contiguous():
+            raise ValueError(f"q must be a contiguous CUDA tensor [{B}, {Hq}, {D}]")
+        if out is None:
+            out = torch.empty_like(q)
+        if return_lse and lse is None:
+            lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        _check(_L().fa_cascade_run(self._h, q.data_ptr(), paged_kv.data_ptr(), paged_kv.shape[0],
+                                   0.0 if sm_scale is None else float(sm_scale), out.data_ptr(),
+                                   lse.data_ptr() if lse is not None else None,
+                                   _stream_handle(stream)), "fa_cascade_run")
+        return out, lse
+
+    def check(self, stream=None) -> int:
+        flags = ctypes.c_int(0)
+        st = _L().fa_cascade_check(self._h, _stream_handle(stream), ctypes.byref(flags))
+        if st not in (FA_OK, -5):
+            _check(st, "fa_cascade_check")
+        return int(flags.value)
+
+
+def cascade_plan(prefix_indices: torch.Tensor, indptr, indices: torch.Tensor, last_page_len,
+                 num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int, *,
+                 q_data_type=torch.bfloat16, workspace: torch.Tensor | None = None,
+                 stream=None) -> CascadePlan:
+    """Plan cascade decode: prefix_indices are the shared (full) pages every
+    request starts with; indptr/indices/last_page_len describe each request's
+    own pages after them."""
+    indptr_h = _host_i32(indptr)
+    last_h = _host_i32(last_page_len)
+    B = indptr_h.shape[0] - 1
+    for t in (prefix_indices, indices):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("index arrays must be contiguous int32 CUDA tensors")
+    if workspace is None:
+        n = _L().fa_cascade_workspace_size(B, num_qo_heads, num_kv_heads, head_dim)
+        if n == 0:
+            raise ValueError("invalid shape or no CUDA device")
+        workspace = torch.empty(int(n), dtype=torch.uint8, device=prefix_indices.device)
+    handle = ctypes.c_void_p()
+    code = _dtype_code(q_data_type)
+    _check(_L().fa_cascade_plan(
+        prefix_indices.data_ptr(), prefix_indices.numel(), indptr_h.ctypes.data,
+        indices.data_ptr() if indices.numel() else None, last_h.ctypes.data, B, num_qo_heads,
+        num_kv_heads, head_dim, page_size, code, code, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream),
+        ctypes.byref(handle)), "fa_cascade_plan")
+    return CascadePlan(handle.value, (prefix_indices, indices, workspace), q_data_type,
+                       (B, num_qo_heads, num_kv_heads, head_dim))
 
 
 class BatchDecodeWithPagedKVCacheWrapper:

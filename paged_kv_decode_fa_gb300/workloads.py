@@ -32,6 +32,12 @@ measured on:
                  [B, 2, Hq, D] and each request's last two cache positions are
                  the two query tokens' own K/V.
 
+``cascade``      B=64, 32/8 heads, head_dim 128, bf16: every request starts
+                 with the same 2048-token prefix (128 shared pages, e.g. a
+                 system prompt) followed by U{1..512} tokens of its own.  The
+                 batch's page table lists each request's full sequence (prefix
+                 pages first); extra["prefix_pages"] says how many are shared.
+
 All use page_size 16 and the combined [num_pages, 2, 16, Hkv, D] layout.
 Lengths and page tables come from a CPU ``torch.Generator``; values from a
 generator on the target device, both seeded with the config's seed
@@ -78,7 +84,9 @@ CONFIGS: dict[str, DecodeConfig] = {
                                         torch.float8_e4m3fn, 1006),
     "spec_decode": DecodeConfig("spec_decode", 64, 32, 8, 128, torch.bfloat16, torch.bfloat16,
                                 1007, q_len=2),
+    "cascade": DecodeConfig("cascade", 64, 32, 8, 128, torch.bfloat16, torch.bfloat16, 1008),
 }
+CASCADE_PREFIX_PAGES = 128
 
 
 def draw_lengths(cfg: DecodeConfig, gen: torch.Generator) -> np.ndarray:
@@ -93,6 +101,8 @@ def draw_lengths(cfg: DecodeConfig, gen: torch.Generator) -> np.ndarray:
         return np.rint(np.exp(lo + u * (hi - lo))).astype(np.int64)
     if cfg.name == "long_split":
         return np.full(cfg.batch, 65536, dtype=np.int64)
+    if cfg.name == "cascade":   # the request's own tokens after the shared prefix
+        return torch.randint(1, 513, (cfg.batch,), generator=gen).numpy().astype(np.int64)
     if cfg.name in ("fp8_kv", "fp8_kv_token_scales"):
         return torch.randint(1024, 8193, (cfg.batch,), generator=gen).numpy().astype(np.int64)
     raise KeyError(cfg.name)
@@ -177,9 +187,70 @@ def make_batch(*, batch_lengths, num_qo_heads: int, num_kv_heads: int, head_dim:
                  seed, device, page_size, pool_pages, shuffle, name, token_scales, q_len)
 
 
+def make_cascade_batch(*, prefix_pages: int, suffix_lengths, num_qo_heads: int,
+                       num_kv_heads: int, head_dim: int, dtype: torch.dtype, seed: int,
+                       device="cuda", page_size: int = PAGE_SIZE, name="cascade") -> DecodeBatch:
+    """Requests sharing `prefix_pages` full pages, each followed by its own
+    suffix of the given length.  The page table lists every full sequence
+    (shared page ids first); extra["prefix_pages"] is the shared count."""
+    gen = torch.Generator().manual_seed(seed)
+    suffix_lengths = np.asarray(suffix_lengths, dtype=np.int64)
+    sfx_pages = (suffix_lengths + page_size - 1) // page_size
+    pool = prefix_pages + int(sfx_pages.sum())
+    perm = torch.randperm(pool, generator=gen).numpy().astype(np.int32)
+    prefix_ids, own = perm[:prefix_pages], perm[prefix_pages:]
+    ids, indptr, last = [], [0], []
+    off = 0
+    for n, npg in zip(suffix_lengths, sfx_pages):
+        ids.append(prefix_ids)
+        ids.append(own[off:off + npg])
+        off += npg
+        indptr.append(indptr[-1] + prefix_pages + int(npg))
+        last.append(int(n - (npg - 1) * page_size) if npg else page_size)
+    lengths = prefix_pages * page_size + suffix_lengths
+    dev = torch.device(device)
+    vgen = torch.Generator(device=dev).manual_seed(seed)
+    B = len(suffix_lengths)
+    q = torch.randn((B, num_qo_heads, head_dim), generator=vgen, device=dev).to(dtype)
+    kv = torch.randn((pool, 2, page_size, num_kv_heads, head_dim), generator=vgen, device=dev,
+                     dtype=dtype)
+    return DecodeBatch(q=q, paged_kv=kv, indptr=torch.tensor(indptr, dtype=torch.int32),
+                       indices=torch.from_numpy(np.concatenate(ids).astype(np.int32)).to(dev),
+                       last_page_len=torch.tensor(last, dtype=torch.int32), lengths=lengths,
+                       num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                       page_size=page_size, name=name,
+                       extra={"prefix_pages": prefix_pages})
+
+
+def cascade_parts(b: DecodeBatch):
+    """(prefix page ids, suffix indptr, suffix indices, suffix last_page_len)
+    of a cascade batch - the shared pages and each request's own pages."""
+    npre = b.extra["prefix_pages"]
+    indptr = b.indptr.numpy().astype(np.int64)
+    ids = b.indices.cpu().numpy()
+    prefix = ids[:npre]
+    own, sfx_indptr = [], [0]
+    for i in range(b.batch):
+        seg = ids[indptr[i] + npre:indptr[i + 1]]
+        own.append(seg)
+        sfx_indptr.append(sfx_indptr[-1] + len(seg))
+    dev = b.indices.device
+    own_ids = np.concatenate(own) if own else np.zeros(0, np.int32)
+    return (torch.from_numpy(prefix.astype(np.int32)).to(dev),
+            torch.tensor(sfx_indptr, dtype=torch.int32),
+            torch.from_numpy(own_ids.astype(np.int32)).to(dev), b.last_page_len.clone())
+
+
 def make_config_batch(name: str, device="cuda") -> DecodeBatch:
     """The named configuration, drawn from its seed."""
     cfg = CONFIGS[name]
+    if name == "cascade":
+        gen = torch.Generator().manual_seed(cfg.seed)
+        return make_cascade_batch(prefix_pages=CASCADE_PREFIX_PAGES,
+                                  suffix_lengths=draw_lengths(cfg, gen),
+                                  num_qo_heads=cfg.num_qo_heads, num_kv_heads=cfg.num_kv_heads,
+                                  head_dim=cfg.head_dim, dtype=cfg.q_dtype, seed=cfg.seed,
+                                  device=device)
     gen = torch.Generator().manual_seed(cfg.seed)
     lengths = draw_lengths(cfg, gen)
     pool = 64 if name == "tiny" else None

@@ -302,6 +302,49 @@ def test_multi_token_rejects(lib, cuda):
     assert e.value.status == -2
 
 
+# ------------------------------------------------------------------ cascade (shared prefix)
+
+def run_cascade(lib, b):
+    pre, ip, idx, last = W.cascade_parts(b)
+    p = lib.cascade_plan(pre, ip, idx, last, b.num_qo_heads, b.num_kv_heads, b.head_dim,
+                         b.page_size, q_data_type=b.q.dtype)
+    o, lse = p.run(b.q, b.paged_kv)
+    torch.cuda.synchronize()
+    return p, o, lse
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+@pytest.mark.parametrize("batch,hq,hkv,prefix_pages", [
+    (6, 8, 2, 5),       # 24 rows: one partial row block
+    (40, 16, 4, 9),     # 160 rows per kv head: two row blocks
+    (3, 16, 2, 1),      # group 8, a one-page prefix
+])
+def test_cascade_small(lib, cuda, dtype, batch, hq, hkv, prefix_pages):
+    """Cascade output equals attention over each request's full page list
+    (shared prefix pages, then its own), checked against the oracle."""
+    rng = np.random.default_rng(batch + prefix_pages)
+    sfx = rng.integers(0, 200, size=batch)
+    sfx[0] = 0          # a request with no pages of its own
+    sfx[-1] = 16        # one full page of its own
+    b = W.make_cascade_batch(prefix_pages=prefix_pages, suffix_lengths=sfx, num_qo_heads=hq,
+                             num_kv_heads=hkv, head_dim=128, dtype=dtype,
+                             seed=70 + batch, device=cuda)
+    p, o, lse = run_cascade(lib, b)
+    assert p.check() == 0
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, TOL[dtype])
+
+
+def test_cascade_rejects(lib, cuda):
+    idx = torch.zeros(1, dtype=torch.int32, device=cuda)
+    with pytest.raises(lib.FaError) as e:
+        lib.cascade_plan(idx, [0, 0], idx, [16], 8, 8, 64, 16, q_data_type=torch.bfloat16)
+    assert e.value.status == -2          # head_dim 64 not built
+    with pytest.raises(lib.FaError) as e:
+        lib.cascade_plan(idx, [0, 0], idx, [16], 8, 8, 128, 16, q_data_type=torch.float32)
+    assert e.value.status == -2
+
+
 # ------------------------------------------------------------------ merge_states
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
@@ -341,17 +384,23 @@ def _sample_requests(b, k=6):
 
 
 @pytest.mark.parametrize("name", ["gqa_uniform", "ragged", "long_split", "fp8_kv",
-                                  "fp8_kv_token_scales", "spec_decode"])
+                                  "fp8_kv_token_scales", "spec_decode", "cascade"])
 def test_full_size_workloads_sampled(lib, cuda, name):
     b = W.make_config_batch(name, device=cuda)
     if "k_scales" in b.extra:
         p, o, lse = run_token_scales(lib, b)
     elif b.q_len > 1:
         p, o, lse = run_multi(lib, b)
+    elif "prefix_pages" in b.extra:
+        p, o, lse = run_cascade(lib, b)
+        # and the same batch through plain decode
+        _, o2, lse2 = run_lib(lib, b)
+        assert (o.float() - o2.float()).abs().max().item() <= 2 * TOL[torch.bfloat16]
     else:
         p, o, lse = run_lib(lib, b)
     assert p.check() == 0
-    check_coverage(p, b)
+    if "prefix_pages" not in b.extra:
+        check_coverage(p, b)
     rows = _sample_requests(b)
     sb = sub_batch(b, rows)
     ref_o, ref_lse = oracle_decode(sb)
