@@ -33,8 +33,9 @@ measured on:
                  the two query tokens' own K/V.
 
 ``cascade``      B=64, 32/8 heads, head_dim 128, bf16: every request starts
-                 with the same 2048-token prefix (128 shared pages, e.g. a
-                 system prompt) followed by U{1..512} tokens of its own.  The
+                 with the same 32768-token prefix (2048 shared pages, 134 MB
+                 of KV - more than the 129 MB L2, e.g. a shared retrieved
+                 document) followed by U{1..512} tokens of its own.  The
                  batch's page table lists each request's full sequence (prefix
                  pages first); extra["prefix_pages"] says how many are shared.
 
@@ -86,7 +87,7 @@ CONFIGS: dict[str, DecodeConfig] = {
                                 1007, q_len=2),
     "cascade": DecodeConfig("cascade", 64, 32, 8, 128, torch.bfloat16, torch.bfloat16, 1008),
 }
-CASCADE_PREFIX_PAGES = 128
+CASCADE_PREFIX_PAGES = 2048
 
 
 def draw_lengths(cfg: DecodeConfig, gen: torch.Generator) -> np.ndarray:
