@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -156,8 +157,10 @@ __global__ void __launch_bounds__(PrefixCfg<QT, D, NW>::THREADS)
     dev::mbar_wait(dev::smem_addr(&full[stage]), (uint32_t)((k / S) & 1), aborted, p.err);
     const uint32_t st = ring_addr + stage * C::STAGE_BYTES;
 
-    // ---- S[rows][tokens]: n-tile 0 = tokens 0..7 (K row g), 1 = tokens 8..15
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // ---- S[rows][tokens]: n-tile 0 = tokens 0..7 (K row g), 1 = tokens 8..15;
+    // two accumulators per n-tile (even / odd reduction steps) halve the
+    // dependent MMA chain
+    float acc[2][2][4] = {};
     const int sw = g & 7;
 #pragma unroll
     for (int sgi = 0; sgi < SEGS; ++sgi) {
@@ -171,13 +174,18 @@ __global__ void __launch_bounds__(PrefixCfg<QT, D, NW>::THREADS)
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int j = sgi * 4 + qq * 2 + u;
-          mma::mma16816<kBf16>(sc[0], qa[j][0], qa[j][1], qa[j][2], qa[j][3], w0[2 * u],
+          mma::mma16816<kBf16>(acc[0][u], qa[j][0], qa[j][1], qa[j][2], qa[j][3], w0[2 * u],
                                w0[2 * u + 1]);
-          mma::mma16816<kBf16>(sc[1], qa[j][0], qa[j][1], qa[j][2], qa[j][3], w1[2 * u],
+          mma::mma16816<kBf16>(acc[1][u], qa[j][0], qa[j][1], qa[j][2], qa[j][3], w1[2 * u],
                                w1[2 * u + 1]);
         }
       }
     }
+    float sc[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[n][e] = acc[n][0][e] + acc[n][1][e];
     // lane holds rows g (e = 0, 1) and g+8 (e = 2, 3) x tokens 2t, 2t+1 (+8)
 #pragma unroll
     for (int n = 0; n < 2; ++n)
@@ -460,8 +468,20 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
   const int64_t rows = (int64_t)batch * plan->group;
   plan->row_blocks = (int)((rows + fadecode::kPrefixRows - 1) / fadecode::kPrefixRows);
   const int64_t base = (int64_t)num_kv_heads * plan->row_blocks;
-  int chunks = (int)std::max<int64_t>(1, ((int64_t)sms * occ) / base);
-  chunks = std::min(chunks, std::max(1, num_prefix_pages / 4));  // at least 4 pages a chunk
+  // chunk count with the fewest waves x pages per chunk (at least 4 pages a
+  // chunk), so that every SM gets work and the last wave is not a straggler
+  const int64_t slots = (int64_t)sms * occ;
+  int chunks = 1;
+  int64_t best = INT64_MAX;
+  for (int c = 1; c <= std::max(1, num_prefix_pages / 4); ++c) {
+    const int64_t waves = (base * c + slots - 1) / slots;
+    const int64_t cost = waves * ((num_prefix_pages + c - 1) / c);
+    if (cost < best) {
+      best = cost;
+      chunks = c;
+    }
+    if (base * c > 8 * slots) break;
+  }
   plan->chunks = chunks;
   plan->items = (int)(base * chunks);
   plan->L = cascade_layout(sw, plan->items, batch, num_qo_heads, head_dim);
