@@ -257,7 +257,9 @@ def config_dict(cfg: W.DecodeConfig, b: W.DecodeBatch) -> dict:
             "kv_bytes": int(b.total_tokens * cfg.num_kv_heads * 2 * cfg.head_dim *
                             b.paged_kv.element_size()),
             "l2": "inputs larger than L2 (129 MB): the KV read each step exceeds it",
-            "parallelism": "replicas (one independent batch per GPU)"}
+            "parallelism": "replicas (one independent batch per GPU)",
+            "softmax": ("unified max against a static Cauchy-Schwarz logit bound"
+                        if cfg.name == "gqa_unified_max" else "online (running max)")}
 
 
 def cascade_bytes(b: W.DecodeBatch) -> int:
@@ -393,8 +395,13 @@ def bench_ours(args, world, rank, local):
     o = torch.empty_like(b.q)
     lse = torch.empty(tuple(b.q.shape[:-1]), dtype=torch.float32, device=dev)
     token_scales = "k_scales" in b.extra
+    # unified max: a static logit bound, fixed before the timed region the
+    # way an offline profile of the model would fix it
+    um_bound = W.cauchy_schwarz_bound(b) if args.workload == "gqa_unified_max" else None
 
     def run_step(plan, q):
+        if um_bound is not None:
+            return plan.run_unified_max(q, b.paged_kv, um_bound, out=o, lse=lse)
         if token_scales:
             return plan.run_token_scales(q, b.paged_kv, b.extra["k_scales"], b.extra["v_scales"],
                                          out=o, lse=lse)
@@ -405,6 +412,8 @@ def bench_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     if p.check() != 0:
         raise RuntimeError("device check flagged the benchmark batch")
+    if um_bound is not None:
+        p.unified_max_fallbacks()  # clear the warm-up count
 
     launches_per_step = 1 + (1 if info["num_merge_units"] > 0 and not info["fused_merge"] else 0)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -432,6 +441,7 @@ def bench_ours(args, world, rank, local):
     barrier(world)
     p.set_timing_events(None, None)
     clocks.stop()
+    um_fallbacks = p.unified_max_fallbacks() if um_bound is not None else None
     elapsed_s = start.elapsed_time(end) / 1e3
     elapsed_s = max_over_ranks(elapsed_s, world, dev)
     kern_ms = [a.elapsed_time(z) for a, z in evs]
@@ -506,6 +516,8 @@ def bench_ours(args, world, rank, local):
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(t0, t1),
     }
+    if um_bound is not None:
+        out["unified_max"] = {"bound": um_bound, "fallbacks_in_timed_steps": um_fallbacks}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n, dt, toks, threads, desc = oracle_timing(b, target_s=args.cpu_seconds)
         out["cpu_baseline"] = {"value": n * b.q_len / dt, "unit": "tokens/s", "cores": threads,

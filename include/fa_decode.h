@@ -180,6 +180,38 @@ int fa_decode_run_token_scales(fa_decode_plan_t plan, const void* q,
                                const float* v_scales, void* o, float* lse,
                                void* cuda_stream);
 
+/* run with a unified max (page "FlashDecoding + FlashInfer", section
+ * "FlashDecoding++", item 1 "Async-softmax with unified max"): instead of a
+ * running maximum per query head, every weight is exp(s - max_bound) for a
+ * bound on the logits s = sm_scale * k_scale * (q . k) known before the run,
+ * so no page of the KV stream has to wait on a reduction of the maximum.  The
+ * result is the same softmax (up to rounding); where a head's true maximum
+ * lies more than 16 / log2(e) above max_bound (weights could overflow) or
+ * more than 64 / log2(e) below it (weights could underflow), the kernel
+ * re-centres that head on its true maximum (an exact rescale) and counts a
+ * fallback (see fa_decode_unified_max_fallbacks).
+ *
+ *  max_bound  the static bound, natural-log units of the logits, finite.
+ *             Any finite value gives a correct result; a bound near the true
+ *             maxima avoids fallbacks.  One that needs no look at the scores
+ *             is sm_scale * k_scale * max|q| * max|k| (Cauchy-Schwarz).
+ * Other arguments as fa_decode_run.  Built for q and kv both BF16 (the
+ * weights keep fp32's exponent range), groups 2, 4 and 8, head_dim 64 and
+ * 128, one query token; other plans return FA_ERR_UNSUPPORTED.
+ * Errors: as fa_decode_run; FA_ERR_INVALID_ARG for a non-finite bound. */
+int fa_decode_run_unified_max(fa_decode_plan_t plan, const void* q,
+                              const void* paged_kv, int64_t num_pages,
+                              float sm_scale, float k_scale, float v_scale,
+                              float max_bound, void* o, float* lse,
+                              void* cuda_stream);
+
+/* Wait for cuda_stream, then read and clear the plan's count of unified-max
+ * fallbacks: (work item, consumer warp) pairs that re-centred at least one
+ * head since the last read.  Synchronises; keep it off the hot path.
+ * Errors: FA_ERR_INVALID_ARG (NULL plan or count), FA_ERR_CUDA. */
+int fa_decode_unified_max_fallbacks(fa_decode_plan_t plan, void* cuda_stream,
+                                    int* count);
+
 /* merge_states: combine two sets of partial attention states with the merge
  * rule (page "FlashDecoding + FlashInfer", section "FlashDecoding - the
  * split-KV trick").  A state is a normalised output o_x with its natural-log
@@ -219,6 +251,7 @@ typedef struct {
   int tensor_cores;           /* 1: per-page products on mma.sync, 0: CUDA cores */
   int fused_merge;            /* 1: split requests merged inside the decode kernel */
   int q_len;                  /* query tokens per request */
+  int unified_max;            /* 1: fa_decode_run_unified_max is built for this plan */
 } fa_plan_info;
 
 int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info);

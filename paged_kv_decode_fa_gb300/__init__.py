@@ -37,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "fa_decode_check", "fa_decode_set_timing_events", "fa_decode_static",
     "fa_decode_run_token_scales", "fa_decode_plan_multi_token",
     "fa_cascade_workspace_size", "fa_cascade_plan", "fa_cascade_run", "fa_cascade_plan_destroy",
-    "fa_cascade_check",
+    "fa_cascade_check", "fa_decode_run_unified_max", "fa_decode_unified_max_fallbacks",
 )
 
 FA_OK = 0
@@ -59,7 +59,8 @@ class PlanInfo(ctypes.Structure):
         "num_partial_slots", "threads_per_cta", "smem_bytes_per_cta", "stages")] + [
         ("total_pages", ctypes.c_int64), ("total_tokens", ctypes.c_int64),
         ("workspace_bytes_used", ctypes.c_size_t), ("plan_upload_bytes", ctypes.c_size_t),
-        ("tensor_cores", ctypes.c_int), ("fused_merge", ctypes.c_int), ("q_len", ctypes.c_int)]
+        ("tensor_cores", ctypes.c_int), ("fused_merge", ctypes.c_int), ("q_len", ctypes.c_int),
+        ("unified_max", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -83,6 +84,10 @@ def _load() -> ctypes.CDLL:
     lib.fa_decode_run.restype = i32
     lib.fa_decode_run_token_scales.argtypes = [P, P, P, i64, f32, P, P, P, P, P]
     lib.fa_decode_run_token_scales.restype = i32
+    lib.fa_decode_run_unified_max.argtypes = [P, P, P, i64, f32, f32, f32, f32, P, P, P]
+    lib.fa_decode_run_unified_max.restype = i32
+    lib.fa_decode_unified_max_fallbacks.argtypes = [P, P, ctypes.POINTER(i32)]
+    lib.fa_decode_unified_max_fallbacks.restype = i32
     lib.fa_cascade_workspace_size.argtypes = [i32, i32, i32, i32]
     lib.fa_cascade_workspace_size.restype = sz
     lib.fa_cascade_plan.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, i32, i32, i32, P, sz, P,
@@ -215,6 +220,39 @@ class DecodePlan:
             k_scale: float = 1.0, v_scale: float = 1.0, out: torch.Tensor | None = None,
             lse: torch.Tensor | None = None, return_lse: bool = True, stream=None):
         """Decode attention; returns (o, lse) (lse None if return_lse is False)."""
+        out, lse = self._outputs(q, paged_kv, out, lse, return_lse)
+        _check(_L().fa_decode_run(
+            self._h, q.data_ptr(), paged_kv.data_ptr(), paged_kv.shape[0],
+            0.0 if sm_scale is None else float(sm_scale), float(k_scale), float(v_scale),
+            out.data_ptr(), lse.data_ptr() if lse is not None else None,
+            _stream_handle(stream)), "fa_decode_run")
+        return out, lse
+
+    def run_unified_max(self, q: torch.Tensor, paged_kv: torch.Tensor, max_bound: float, *,
+                        sm_scale: float | None = None, k_scale: float = 1.0,
+                        v_scale: float = 1.0, out: torch.Tensor | None = None,
+                        lse: torch.Tensor | None = None, return_lse: bool = True, stream=None):
+        """Decode attention with the softmax referenced to a static bound
+        `max_bound` on the logits sm_scale * k_scale * (q . k) instead of a
+        running maximum (bf16 plans, groups 2/4/8); returns (o, lse)."""
+        out, lse = self._outputs(q, paged_kv, out, lse, return_lse)
+        _check(_L().fa_decode_run_unified_max(
+            self._h, q.data_ptr(), paged_kv.data_ptr(), paged_kv.shape[0],
+            0.0 if sm_scale is None else float(sm_scale), float(k_scale), float(v_scale),
+            float(max_bound), out.data_ptr(), lse.data_ptr() if lse is not None else None,
+            _stream_handle(stream)), "fa_decode_run_unified_max")
+        return out, lse
+
+    def unified_max_fallbacks(self, stream=None) -> int:
+        """Synchronise; return and clear the count of unified-max re-centrings."""
+        n = ctypes.c_int(0)
+        _check(_L().fa_decode_unified_max_fallbacks(self._h, _stream_handle(stream),
+                                                    ctypes.byref(n)),
+               "fa_decode_unified_max_fallbacks")
+        return int(n.value)
+
+    def _outputs(self, q, paged_kv, out, lse, return_lse):
+        """Check q / paged_kv against the plan; allocate missing outputs."""
         D = self.head_dim
         if q.dtype != self.q_dtype or paged_kv.dtype != self.kv_dtype:
             raise TypeError("q / paged_kv dtype differs from the plan")
@@ -229,11 +267,6 @@ class DecodePlan:
             out = torch.empty(self._q_shape(), dtype=q.dtype, device=q.device)
         if return_lse and lse is None:
             lse = torch.empty(self._q_shape()[:-1], dtype=torch.float32, device=q.device)
-        _check(_L().fa_decode_run(
-            self._h, q.data_ptr(), paged_kv.data_ptr(), paged_kv.shape[0],
-            0.0 if sm_scale is None else float(sm_scale), float(k_scale), float(v_scale),
-            out.data_ptr(), lse.data_ptr() if lse is not None else None,
-            _stream_handle(stream)), "fa_decode_run")
         return out, lse
 
     def run_token_scales(self, q: torch.Tensor, paged_kv: torch.Tensor, k_scales: torch.Tensor,

@@ -31,7 +31,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t off_err, off_cta, off_seg, off_merge, off_count, meta_bytes, off_part_o, off_part_lse,
+  size_t off_err, off_umc, off_cta, off_seg, off_merge, off_count, meta_bytes, off_part_o, off_part_lse,
       total;
 };
 
@@ -40,7 +40,8 @@ Layout make_layout(int64_t n_ctas, int64_t n_segments, int64_t n_merge, int64_t 
                    int D) {
   Layout L;
   L.off_err = 0;
-  L.off_cta = align_up(L.off_err + sizeof(int));
+  L.off_umc = sizeof(int);  // unified-max re-centring counter
+  L.off_cta = align_up(L.off_umc + sizeof(int));
   L.off_seg = align_up(L.off_cta + sizeof(int32_t) * (size_t)(n_ctas + 1));
   L.off_merge = align_up(L.off_seg + sizeof(fadecode::Segment) * (size_t)n_segments);
   L.off_count = align_up(L.off_merge + sizeof(fadecode::MergeUnit) * (size_t)n_merge);
@@ -150,6 +151,11 @@ int kv_tensor_map(MapCache* c, const DecodeKernel& k, fa_dtype kv_dtype, const v
   return FA_OK;
 }
 
+bool find_unified_max_kernel(fa_dtype q, fa_dtype kv, int D, int G, DecodeKernel* k) {
+  if (q != FA_DTYPE_BF16 || kv != FA_DTYPE_BF16 || !tensor_cores_allowed()) return false;
+  return fadecode::find_unified_max_kernel_bf16(D, G, k);
+}
+
 bool find_token_scale_kernel(fa_dtype q, fa_dtype kv, int D, int G, DecodeKernel* k) {
   if (kv != FA_DTYPE_E4M3) return false;
   if (q == FA_DTYPE_BF16) return fadecode::find_token_scale_kernel_bf16_e4m3(D, G, k);
@@ -171,17 +177,23 @@ int kernel_occupancy(const DecodeKernel& k) {
 
 }  // namespace
 
+// Kernel variants a plan can launch.
+enum Variant { kPlain = 0, kTokenScales = 1, kUnifiedMax = 2, kNumVariants = 3 };
+
 struct fa_decode_plan_s;
-static int run_impl(fa_decode_plan_s* plan, bool token_scales, const void* q,
+static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
                     const void* paged_kv, int64_t num_pages, float sm_scale, float k_scale,
-                    float v_scale, const float* k_scales, const float* v_scales, void* o,
-                    float* lse, void* cuda_stream);
+                    float v_scale, const float* k_scales, const float* v_scales,
+                    float max_bound, void* o, float* lse, void* cuda_stream);
 
 struct fa_decode_plan_s {
   int device = 0;
   int batch = 0, hq = 0, hkv = 0, d = 0, page_size = 0, group = 0;
   fa_dtype q_dtype = FA_DTYPE_F32, kv_dtype = FA_DTYPE_F32;
-  DecodeKernel kern;
+  // kern[kPlain] always; kern[kTokenScales] / kern[kUnifiedMax] where
+  // has[...] says the plan's dtypes and shape have that variant built
+  DecodeKernel kern[kNumVariants];
+  bool has[kNumVariants] = {true, false, false};
   int num_sms = 0, ctas_per_sm = 0;
   WorkList wl;
   std::vector<int32_t> merge_flat;
@@ -191,11 +203,8 @@ struct fa_decode_plan_s {
   Layout layout{};
   bool fused_merge = true;
   int q_len = 1;
-  // E4M3 plans: the variant that reads per-token scales, if one is built
-  DecodeKernel kern_ts;
-  bool has_ts = false;
   // cached TMA descriptors of the KV cache, one per kernel variant
-  MapCache map, map_ts;
+  MapCache map[kNumVariants];
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
 };
 
@@ -324,14 +333,19 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
     return FA_ERR_CUDA;
   occ = kernel_occupancy(kern);
   if (occ == 0) return FA_ERR_CUDA;
-  // The persistent grid must fit for either variant a run may launch.
-  DecodeKernel kern_ts;
-  const bool has_ts =
-      q_len == 1 && find_token_scale_kernel(q_dtype, kv_dtype, head_dim, G, &kern_ts);
-  if (has_ts) {
-    const int occ_ts = kernel_occupancy(kern_ts);
-    if (occ_ts == 0) return FA_ERR_CUDA;
-    occ = std::min(occ, occ_ts);
+  // The persistent grid must fit for every variant a run may launch.
+  DecodeKernel kv[kNumVariants];
+  bool has[kNumVariants] = {true, false, false};
+  kv[kPlain] = kern;
+  if (q_len == 1) {
+    has[kTokenScales] = find_token_scale_kernel(q_dtype, kv_dtype, head_dim, G, &kv[kTokenScales]);
+    has[kUnifiedMax] = find_unified_max_kernel(q_dtype, kv_dtype, head_dim, G, &kv[kUnifiedMax]);
+  }
+  for (int v = 1; v < kNumVariants; ++v) {
+    if (!has[v]) continue;
+    const int occ_v = kernel_occupancy(kv[v]);
+    if (occ_v == 0) return FA_ERR_CUDA;
+    occ = std::min(occ, occ_v);
   }
   occ = std::max(1, std::min(occ, kMaxCtasPerSmBound));
 
@@ -346,15 +360,16 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
   plan->group = G;
   plan->q_dtype = q_dtype;
   plan->kv_dtype = kv_dtype;
-  plan->kern = kern;
+  for (int v = 0; v < kNumVariants; ++v) {
+    plan->kern[v] = kv[v];
+    plan->has[v] = has[v];
+  }
   plan->num_sms = sms;
   plan->ctas_per_sm = occ;
   plan->indices = indices_dev;
   plan->ws = static_cast<uint8_t*>(workspace_dev);
   plan->ws_bytes = workspace_bytes;
   plan->fused_merge = fused_merge_enabled();
-  plan->kern_ts = kern_ts;
-  plan->has_ts = has_ts;
   plan->q_len = q_len;
 
   int rc = FA_OK;
@@ -405,20 +420,43 @@ int fa_decode_run(fa_decode_plan_t plan, const void* q, const void* paged_kv, in
                   float sm_scale, float k_scale, float v_scale, void* o, float* lse,
                   void* cuda_stream) {
   if (!plan) return FA_ERR_INVALID_ARG;
-  return run_impl(plan, false, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, nullptr,
-                  nullptr, o, lse, cuda_stream);
+  return run_impl(plan, kPlain, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, nullptr,
+                  nullptr, 0.f, o, lse, cuda_stream);
+}
+
+int fa_decode_run_unified_max(fa_decode_plan_t plan, const void* q, const void* paged_kv,
+                              int64_t num_pages, float sm_scale, float k_scale, float v_scale,
+                              float max_bound, void* o, float* lse, void* cuda_stream) {
+  if (!plan) return FA_ERR_INVALID_ARG;
+  if (!plan->has[kUnifiedMax]) return FA_ERR_UNSUPPORTED;
+  // the reference enters the kernel in log2 units and must stay finite there
+  if (!(std::fabs(max_bound) <= 1e30f)) return FA_ERR_INVALID_ARG;
+  return run_impl(plan, kUnifiedMax, q, paged_kv, num_pages, sm_scale, k_scale, v_scale,
+                  nullptr, nullptr, max_bound, o, lse, cuda_stream);
+}
+
+int fa_decode_unified_max_fallbacks(fa_decode_plan_t plan, void* cuda_stream, int* count) {
+  if (!plan || !count) return FA_ERR_INVALID_ARG;
+  int word = 0;
+  int* dword = reinterpret_cast<int*>(plan->ws + plan->layout.off_umc);
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess ||
+      cudaMemcpy(&word, dword, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(dword, 0, sizeof word) != cudaSuccess)
+    return FA_ERR_CUDA;
+  *count = word;
+  return FA_OK;
 }
 
 int fa_decode_run_token_scales(fa_decode_plan_t plan, const void* q, const void* paged_kv,
                                int64_t num_pages, float sm_scale, const float* k_scales,
                                const float* v_scales, void* o, float* lse, void* cuda_stream) {
   if (!plan) return FA_ERR_INVALID_ARG;
-  if (plan->kv_dtype != FA_DTYPE_E4M3 || !plan->has_ts) return FA_ERR_UNSUPPORTED;
+  if (plan->kv_dtype != FA_DTYPE_E4M3 || !plan->has[kTokenScales]) return FA_ERR_UNSUPPORTED;
   if (plan->batch > 0 && (!k_scales || !v_scales)) return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(k_scales) % 16 || reinterpret_cast<uintptr_t>(v_scales) % 16)
     return FA_ERR_INVALID_ARG;
-  return run_impl(plan, true, q, paged_kv, num_pages, sm_scale, 1.f, 1.f, k_scales, v_scales, o,
-                  lse, cuda_stream);
+  return run_impl(plan, kTokenScales, q, paged_kv, num_pages, sm_scale, 1.f, 1.f, k_scales,
+                  v_scales, 0.f, o, lse, cuda_stream);
 }
 
 int fa_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
@@ -453,16 +491,17 @@ int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info) {
   i.num_segments = (int)plan->wl.segments.size();
   i.num_merge_units = (int)plan->wl.merge.size();
   i.num_partial_slots = plan->wl.num_slots;
-  i.threads_per_cta = plan->kern.threads;
-  i.smem_bytes_per_cta = plan->kern.smem_bytes;
-  i.stages = plan->kern.stages;
+  i.threads_per_cta = plan->kern[kPlain].threads;
+  i.smem_bytes_per_cta = plan->kern[kPlain].smem_bytes;
+  i.stages = plan->kern[kPlain].stages;
   i.total_pages = plan->wl.total_pages;
   i.total_tokens = plan->wl.total_tokens;
   i.workspace_bytes_used = plan->layout.total;
   i.plan_upload_bytes = plan->layout.meta_bytes;
-  i.tensor_cores = plan->kern.tensor_cores ? 1 : 0;
+  i.tensor_cores = plan->kern[kPlain].tensor_cores ? 1 : 0;
   i.fused_merge = plan->fused_merge ? 1 : 0;
   i.q_len = plan->q_len;
+  i.unified_max = plan->has[kUnifiedMax] ? 1 : 0;
   *info = i;
   return FA_OK;
 }
@@ -498,18 +537,18 @@ int fa_decode_set_timing_events(fa_decode_plan_t plan, void* ev_before, void* ev
 
 }  // extern "C"
 
-static int run_impl(fa_decode_plan_s* plan, bool token_scales, const void* q,
+static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
                     const void* paged_kv, int64_t num_pages, float sm_scale, float k_scale,
-                    float v_scale, const float* k_scales, const float* v_scales, void* o,
-                    float* lse, void* cuda_stream) {
+                    float v_scale, const float* k_scales, const float* v_scales,
+                    float max_bound, void* o, float* lse, void* cuda_stream) {
   if (plan->batch == 0) return FA_OK;
   if (!q || !paged_kv || !o || num_pages <= 0) return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(paged_kv) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
     return FA_ERR_INVALID_ARG;
   if (2 * num_pages > (int64_t)0xffffffffLL) return FA_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  const DecodeKernel& kern = token_scales ? plan->kern_ts : plan->kern;
-  MapCache& mc = token_scales ? plan->map_ts : plan->map;
+  const DecodeKernel& kern = plan->kern[variant];
+  MapCache& mc = plan->map[variant];
   const int D = plan->d;
   int rc = kv_tensor_map(&mc, kern, plan->kv_dtype, paged_kv, num_pages, D, plan->hkv,
                          plan->page_size);
@@ -537,6 +576,8 @@ static int run_impl(fa_decode_plan_s* plan, bool token_scales, const void* q,
   prm.q_len = plan->q_len;
   prm.q_scale = sm_scale * k_scale * kLog2e;
   prm.v_scale = v_scale;
+  prm.max_bound = max_bound * kLog2e;
+  prm.um_fallbacks = reinterpret_cast<int*>(plan->ws + plan->layout.off_umc);
 
   const bool timed = plan->ev_before && plan->ev_after;
   if (timed && cudaEventRecord(plan->ev_before, st) != cudaSuccess) return FA_ERR_CUDA;

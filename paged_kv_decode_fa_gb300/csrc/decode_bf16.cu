@@ -9,4 +9,7 @@ bool find_kernel_bf16(int head_dim, int group, bool allow_mma, DecodeKernel* k) 
 bool find_multi_token_kernel_bf16(int head_dim, int group, int q_len, DecodeKernel* k) {
   return find_multi_token_kernel_for<__nv_bfloat16, __nv_bfloat16>(head_dim, group, q_len, k);
 }
+bool find_unified_max_kernel_bf16(int head_dim, int group, DecodeKernel* k) {
+  return find_unified_max_kernel_for<__nv_bfloat16, __nv_bfloat16>(head_dim, group, k);
+}
 }  // namespace fadecode

@@ -158,7 +158,16 @@ struct MmaCfg {
   static_assert(!kFp8 || D % 32 == 0, "E4M3 V is transposed two granules at a time");
 };
 
-template <typename QT, typename KVT, int D, int G, int NW, bool TS, int QL>
+// Unified-max softmax window (log2 units): while a column's running maximum
+// m stays within [ref - kUmBelow, ref + kUmAbove] of the static reference,
+// its weights are exp2(s - ref) with no running-max bookkeeping.  Above: a
+// weight stays below 2^16 and a sum over 2^31 tokens below 2^47 (fp32 and
+// bf16 hold both).  Below: ex2.approx flushes weights under 2^-126 to zero,
+// so a flushed token weighs under 2^(64-126) relative to the maximum one.
+constexpr float kUmAbove = 16.f;
+constexpr float kUmBelow = 64.f;
+
+template <typename QT, typename KVT, int D, int G, int NW, bool TS, int QL, bool UM>
 __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
     fa_decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
   using C = MmaCfg<QT, KVT, D, G, NW, TS, QL>;
@@ -171,6 +180,8 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
   // bf16 q with E4M3 KV runs the MMA in f16: q is scaled by a power of two
   // per segment to sit well inside the f16 range.
   constexpr bool kConvertQ = kFp8 && std::is_same<QT, __nv_bfloat16>::value;
+  // the unified-max window relies on the 8-bit exponent of bf16 weights
+  static_assert(!UM || (kBf16 && !TS && QL == 1), "unified max: bf16 weights, plain decode");
 
   // Swizzled TMA destinations must sit on 1024-byte boundaries: the launch
   // reserves 1 KB more than the layout so the base can be rounded up.
@@ -301,7 +312,13 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
     for (int mt = 0; mt < MTILES; ++mt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
+    // m_h: the column's reference (running max, or the static bound when
+    // UM); d_h: this lane's share of the column's denominator, summed over
+    // the column's 8 lanes once the segment is done
     float m_h[2] = {-INFINITY, -INFINITY}, d_h[2] = {0.f, 0.f};
+    float tmx[2] = {-INFINITY, -INFINITY};  // UM: this lane's running maxima
+    bool um_first = true, um_moved = false;
+    if constexpr (UM) m_h[0] = m_h[1] = p.max_bound;
 
     for (int k = kbase + (warp - kbase % NW + NW) % NW; k < kbase + npg; k += NW) {
       const int lp = k - kbase;
@@ -365,22 +382,60 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
         if (pos + 8 > lim[1]) s[3] = -INFINITY;
       }
 
-      // ---- online softmax for heads 2t (s[0], s[2]) and 2t+1 (s[1], s[3])
-      float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
+      // ---- softmax for heads 2t (s[0], s[2]) and 2t+1 (s[1], s[3])
+      float alpha[2] = {1.f, 1.f}, pr[4], mref[2];
+      bool rescale;
+      if constexpr (UM) {
+        // Unified max: the weights use the static reference, so a page needs
+        // no column reduction - only a vote on whether some lane's running
+        // maximum rose past the window.  The first page of a segment also
+        // checks the window's lower edge (the running maximum never falls,
+        // so once a column is inside it stays inside).  A column outside
+        // the window is re-centred on its true maximum (an exact rescale).
+        tmx[0] = fmaxf(tmx[0], fmaxf(s[0], s[2]));
+        tmx[1] = fmaxf(tmx[1], fmaxf(s[1], s[3]));
+        const bool first = um_first;
+        um_first = false;
+        rescale = first ||
+                  __any_sync(0xffffffffu, tmx[0] > m_h[0] + kUmAbove || tmx[1] > m_h[1] + kUmAbove);
+        if (rescale) {
+          float mx[2] = {tmx[0], tmx[1]};
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
-        mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
-      }
-      float alpha[2], pr[4], mref[2];
+          for (int off = 4; off < 32; off <<= 1) {
+            mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
+            mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
+          }
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float mn = fmaxf(m_h[e], mx[e]);
-        // a column can have seen nothing yet (every token so far masked by
-        // the causal rule): keep its state empty instead of exp2(-inf + inf)
-        mref[e] = mn == -INFINITY ? 0.f : mn;
-        alpha[e] = dev::fast_exp2(m_h[e] - mref[e]);
-        m_h[e] = mn;
+          for (int e = 0; e < 2; ++e) {
+            const bool outside = mx[e] > m_h[e] + kUmAbove || mx[e] < m_h[e] - kUmBelow;
+            if (outside && mx[e] != -INFINITY) {
+              // nothing accumulated before the first page (and a lowered
+              // reference could make this factor overflow)
+              alpha[e] = first ? 1.f : dev::fast_exp2(m_h[e] - mx[e]);
+              m_h[e] = mx[e];
+              um_moved = true;
+            }
+          }
+        }
+        mref[0] = m_h[0];
+        mref[1] = m_h[1];
+      } else {
+        float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
+          mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float mn = fmaxf(m_h[e], mx[e]);
+          // a column can have seen nothing yet (every token so far masked by
+          // the causal rule): keep its state empty instead of exp2(-inf + inf)
+          mref[e] = mn == -INFINITY ? 0.f : mn;
+          alpha[e] = dev::fast_exp2(m_h[e] - mref[e]);
+          m_h[e] = mn;
+        }
+        rescale = true;
       }
       const uint32_t p01 = mma::pack2(dev::fast_exp2(s[0] - mref[0]),
                                       dev::fast_exp2(s[1] - mref[1]), kBf16);
@@ -391,26 +446,20 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
         const float2 a = mma::unpack2(p01, kBf16), b = mma::unpack2(p23, kBf16);
         pr[0] = a.x; pr[1] = a.y; pr[2] = b.x; pr[3] = b.y;
       }
-      float ps[2] = {pr[0] + pr[2], pr[1] + pr[3]};
       uint32_t pv01 = p01, pv23 = p23;  // weights times the per-token V scale
       if constexpr (TS) {
         pv01 = mma::pack2(pr[0] * vs_lo, pr[1] * vs_lo, kBf16);
         pv23 = mma::pack2(pr[2] * vs_hi, pr[3] * vs_hi, kBf16);
       }
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        ps[0] += __shfl_xor_sync(0xffffffffu, ps[0], off);
-        ps[1] += __shfl_xor_sync(0xffffffffu, ps[1], off);
-      }
-      d_h[0] = d_h[0] * alpha[0] + ps[0];
-      d_h[1] = d_h[1] * alpha[1] + ps[1];
+      d_h[0] = d_h[0] * alpha[0] + (pr[0] + pr[2]);
+      d_h[1] = d_h[1] * alpha[1] + (pr[1] + pr[3]);
       // P^T B fragments: transpose [token][head] -> [head][token] through smem
       pT[(2 * t) * P + g] = (uint16_t)(pv01 & 0xffffu);
       pT[(2 * t + 1) * P + g] = (uint16_t)(pv01 >> 16);
       pT[(2 * t) * P + g + 8] = (uint16_t)(pv23 & 0xffffu);
       pT[(2 * t + 1) * P + g + 8] = (uint16_t)(pv23 >> 16);
       // once the running maxima settle, most pages leave them unchanged
-      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+      if (rescale && __any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
         for (int mt = 0; mt < MTILES; ++mt) {
           o[mt][0] *= alpha[0];
@@ -472,6 +521,18 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
 
     // ---- this warp's state: O^T rows -> dims, heads 2t and 2t+1
 #pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      d_h[0] += __shfl_xor_sync(0xffffffffu, d_h[0], off);
+      d_h[1] += __shfl_xor_sync(0xffffffffu, d_h[1], off);
+    }
+    if constexpr (UM) {
+      if (__any_sync(0xffffffffu, um_moved) && lane == 0 && p.um_fallbacks)
+        atomicAdd(p.um_fallbacks, 1);
+      // a warp that drew no page holds no state: its reference must not
+      // outweigh the others' in the combine
+      if (um_first) m_h[0] = m_h[1] = -INFINITY;
+    }
+#pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int h = 2 * t + e;  // column
       if (h < NC) {
@@ -496,10 +557,11 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
   }
 }
 
-template <typename QT, typename KVT, int D, int G, int NW = 4, bool TS = false, int QL = 1>
+template <typename QT, typename KVT, int D, int G, int NW = 4, bool TS = false, int QL = 1,
+          bool UM = false>
 inline void fill_mma_kernel(DecodeKernel* k) {
   using C = MmaCfg<QT, KVT, D, G, NW, TS, QL>;
-  k->func = reinterpret_cast<const void*>(&fa_decode_mma_kernel<QT, KVT, D, G, NW, TS, QL>);
+  k->func = reinterpret_cast<const void*>(&fa_decode_mma_kernel<QT, KVT, D, G, NW, TS, QL, UM>);
   k->merge_func = reinterpret_cast<const void*>(&fa_merge_partials_kernel<QT, D, G, QL>);
   k->threads = C::THREADS;
   k->smem_bytes = C::SMEM + 1024;  // room to align the ring to 1024 bytes
@@ -512,6 +574,7 @@ inline void fill_mma_kernel(DecodeKernel* k) {
   k->tensor_cores = true;
   k->token_scales = TS;
   k->q_len = QL;
+  k->unified_max = UM;
 }
 
 }  // namespace fadecode
@@ -553,6 +616,20 @@ inline bool find_multi_token_kernel_for(int head_dim, int group, int q_len, Deco
   FA_QL_CASE(1, 2) FA_QL_CASE(1, 4) FA_QL_CASE(1, 8)
   FA_QL_CASE(2, 2) FA_QL_CASE(2, 4) FA_QL_CASE(4, 2)
 #undef FA_QL_CASE
+  return false;
+}
+
+// Unified-max softmax (bf16 q and KV): tensor-core consumer, groups 2, 4, 8.
+template <typename QT, typename KVT>
+inline bool find_unified_max_kernel_for(int head_dim, int group, DecodeKernel* k) {
+#define FA_UM_CASE(DD, GG)                                   \
+  if (head_dim == DD && group == GG) {                       \
+    fill_mma_kernel<QT, KVT, DD, GG, 4, false, 1, true>(k);  \
+    return true;                                             \
+  }
+  FA_UM_CASE(64, 2) FA_UM_CASE(64, 4) FA_UM_CASE(64, 8)
+  FA_UM_CASE(128, 2) FA_UM_CASE(128, 4) FA_UM_CASE(128, 8)
+#undef FA_UM_CASE
   return false;
 }
 

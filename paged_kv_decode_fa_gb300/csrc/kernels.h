@@ -32,6 +32,8 @@ struct DecodeParams {
   int q_len;                   // query tokens per request (1 for plain decode)
   float q_scale;  // sm_scale * k_scale * log2(e), folded into q
   float v_scale;
+  float max_bound;    // unified-max kernels: static reference of the logits, log2 units
+  int* um_fallbacks;  // unified-max kernels: count of (segment, warp) re-centrings, or nullptr
 };
 
 struct MergeParams {
@@ -58,6 +60,7 @@ struct DecodeKernel {
   bool tensor_cores = false;  // per-page products on mma.sync
   bool token_scales = false;  // reads per-token K/V scales (E4M3 only)
   int q_len = 1;              // query tokens per request the kernel was built for
+  bool unified_max = false;   // softmax against a static bound (no running max)
 };
 
 // Each returns false when the combination is not compiled.  allow_mma
@@ -72,6 +75,8 @@ bool find_kernel_f16_e4m3(int head_dim, int group, bool allow_mma, DecodeKernel*
 // tensor-core consumer, head_dim 128, group * q_len <= 8.
 bool find_multi_token_kernel_bf16(int head_dim, int group, int q_len, DecodeKernel* k);
 bool find_multi_token_kernel_bf16_e4m3(int head_dim, int group, int q_len, DecodeKernel* k);
+// Unified-max softmax (bf16 q and KV, groups 2, 4, 8, head_dim 64 or 128).
+bool find_unified_max_kernel_bf16(int head_dim, int group, DecodeKernel* k);
 // E4M3 KV with per-token, per-kv-head scales (tensor-core consumer only).
 bool find_token_scale_kernel_bf16_e4m3(int head_dim, int group, DecodeKernel* k);
 bool find_token_scale_kernel_f16_e4m3(int head_dim, int group, DecodeKernel* k);

@@ -39,6 +39,12 @@ measured on:
                  batch's page table lists each request's full sequence (prefix
                  pages first); extra["prefix_pages"] says how many are shared.
 
+``gqa_unified_max``  the gqa_uniform batch (same seed, same values), decoded
+                 with the unified-max softmax against cauchy_schwarz_bound.
+
+``cauchy_schwarz_bound`` turns a batch's values into the static logit bound
+that the unified-max softmax takes as an input (norms only, no scores).
+
 All use page_size 16 and the combined [num_pages, 2, 16, Hkv, D] layout.
 Lengths and page tables come from a CPU ``torch.Generator``; values from a
 generator on the target device, both seeded with the config's seed
@@ -86,6 +92,9 @@ CONFIGS: dict[str, DecodeConfig] = {
     "spec_decode": DecodeConfig("spec_decode", 64, 32, 8, 128, torch.bfloat16, torch.bfloat16,
                                 1007, q_len=2),
     "cascade": DecodeConfig("cascade", 64, 32, 8, 128, torch.bfloat16, torch.bfloat16, 1008),
+    # the gqa_uniform batch itself (same seed), run with the unified-max softmax
+    "gqa_unified_max": DecodeConfig("gqa_unified_max", 64, 32, 8, 128, torch.bfloat16,
+                                    torch.bfloat16, 1002),
 }
 CASCADE_PREFIX_PAGES = 2048
 
@@ -94,7 +103,7 @@ def draw_lengths(cfg: DecodeConfig, gen: torch.Generator) -> np.ndarray:
     """Context length of every request of a named configuration."""
     if cfg.name == "tiny":
         return np.array([17, 64, 100, 255], dtype=np.int64)
-    if cfg.name in ("gqa_uniform", "spec_decode"):
+    if cfg.name in ("gqa_uniform", "spec_decode", "gqa_unified_max"):
         return np.full(cfg.batch, 2048, dtype=np.int64)
     if cfg.name == "ragged":
         u = torch.rand(cfg.batch, generator=gen, dtype=torch.float64).numpy()
@@ -308,3 +317,19 @@ def _fill(lengths, gen, Hq, Hkv, D, q_dtype, kv_dtype, seed, device, P, pool_pag
                        last_page_len=last, lengths=lengths, num_qo_heads=Hq,
                        num_kv_heads=Hkv, head_dim=D, page_size=P, k_scale=k_scale,
                        v_scale=v_scale, name=name, extra=extra, q_len=q_len)
+
+
+def cauchy_schwarz_bound(b: DecodeBatch, sm_scale: float | None = None) -> float:
+    """A bound on every logit sm_scale * k_scale * (q . k) of the batch that
+    looks at no score: |q . k| <= |q| |k| (Cauchy-Schwarz), with the largest
+    query norm of the batch and the largest key norm of the whole cache (a
+    statistic a cache can keep as it is written).  The static bound a
+    unified-max softmax starts from."""
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(b.head_dim)
+    qn = b.q.float().norm(dim=-1).max().item()
+    kn = 0.0
+    for lo in range(0, b.num_pages, 4096):   # chunked: fp32 copies of a large cache
+        k = b.paged_kv[lo:lo + 4096, 0].float()
+        kn = max(kn, k.norm(dim=-1).max().item())
+    return float(sm_scale * b.k_scale * qn * kn)

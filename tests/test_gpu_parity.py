@@ -345,6 +345,123 @@ def test_cascade_rejects(lib, cuda):
     assert e.value.status == -2
 
 
+# ------------------------------------------------------------------ unified max
+
+# The window of the unified-max reference, natural-log units: the kernel
+# re-centres a head whose maximum logit lies more than UM_ABOVE above the
+# bound or more than UM_BELOW below it (16 and 64 in log2 units).
+UM_ABOVE = 16 / math.log2(math.e)
+UM_BELOW = 64 / math.log2(math.e)
+
+
+def run_um(lib, b, bound):
+    p = lib.plan(b.indptr, b.indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                 b.head_dim, b.page_size, q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype)
+    p.unified_max_fallbacks()          # start the count from zero
+    o, lse = p.run_unified_max(b.q, b.paged_kv, bound)
+    torch.cuda.synchronize()
+    return p, o, lse, p.unified_max_fallbacks()
+
+
+def max_logits(b):
+    """Per (request, qo head) maximum of sm_scale * q . k, in float64 on the
+    host (for choosing bounds in the tests; empty requests give -inf)."""
+    q = b.q.double().cpu()
+    kv = b.paged_kv.double().cpu()
+    G = b.num_qo_heads // b.num_kv_heads
+    ip, idx = b.indptr.numpy(), b.indices.cpu().numpy()
+    out = np.full((b.batch, b.num_qo_heads), -np.inf)
+    for r in range(b.batch):
+        n = int(b.lengths[r])
+        if n == 0:
+            continue
+        k = kv[idx[ip[r]:ip[r + 1]], 0].reshape(-1, b.num_kv_heads, b.head_dim)[:n]
+        for h in range(b.num_qo_heads):
+            s = k[:, h // G] @ q[r, h] / math.sqrt(b.head_dim)
+            out[r, h] = s.max().item()
+    return out
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("group", [2, 4, 8])
+@pytest.mark.parametrize("where", ["cauchy_schwarz", "inside_above", "inside_below",
+                                   "far_above", "far_below"])
+def test_unified_max_small(lib, cuda, head_dim, group, where):
+    """Softmax referenced to a static bound: the same result as the oracle
+    for any bound.  Inside the window no head is re-centred (weights down to
+    2^-43 or up to 2^11 relative to the bound still give the oracle's
+    answer); far outside it the re-centring fallback runs and still does."""
+    Hkv = 2
+    lengths = [1, 0, 16, 17, 250, 1000, 33, 611]
+    b = W.make_batch(batch_lengths=lengths, num_qo_heads=Hkv * group, num_kv_heads=Hkv,
+                     head_dim=head_dim, q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16,
+                     seed=90 + head_dim + group, device=cuda, pool_pages=200)
+    top = np.max(max_logits(b))
+    bound = {"cauchy_schwarz": W.cauchy_schwarz_bound(b),
+             "inside_above": top + 30.0,
+             "inside_below": top - 8.0,
+             "far_above": top + UM_BELOW + 40.0,
+             "far_below": top - UM_ABOVE - 20.0}[where]
+    p, o, lse, n = run_um(lib, b, bound)
+    assert p.info["unified_max"] == 1 and p.check() == 0
+    if where.startswith("far"):
+        assert n > 0, "a bound outside the window must take the fallback"
+    else:
+        assert n == 0, f"{n} fallbacks for a bound inside the window"
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, TOL[torch.bfloat16])
+
+
+def test_unified_max_many_splits(lib, cuda):
+    """A long request split over the grid: partial states of one head carry
+    different references (some pieces re-centred, some not) and still merge
+    to the oracle's result."""
+    b = W.make_batch(batch_lengths=[60000, 5, 300], num_qo_heads=16, num_kv_heads=4,
+                     head_dim=128, q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, seed=97,
+                     device=cuda)
+    top = np.max(max_logits(b))
+    # the window's upper edge 1 below the top logit: pieces holding the top
+    # logits re-centre, the others keep the bound
+    p, o, lse, n = run_um(lib, b, top - UM_ABOVE - 1.0)
+    assert p.info["num_merge_units"] > 0 and p.check() == 0
+    assert 0 < n < p.info["num_segments"] * 4
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, TOL[torch.bfloat16])
+    # same plan, regular softmax: results agree to rounding
+    o2, lse2 = p.run(b.q, b.paged_kv)
+    torch.cuda.synchronize()
+    assert (o.float() - o2.float()).abs().max().item() <= TOL[torch.bfloat16]
+
+
+def test_unified_max_rejects(lib, cuda):
+    b = W.make_batch(batch_lengths=[40, 3], num_qo_heads=8, num_kv_heads=2, head_dim=128,
+                     q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, seed=1, device=cuda)
+    p = lib.plan(b.indptr, b.indices, b.last_page_len, 8, 2, 128, 16,
+                 q_data_type=torch.bfloat16, kv_data_type=torch.bfloat16)
+    for bad in (math.inf, -math.inf, math.nan):
+        with pytest.raises(lib.FaError) as e:
+            p.run_unified_max(b.q, b.paged_kv, bad)
+        assert e.value.status == -1
+    # f16 weights, E4M3 KV, group 1 and multi-token plans have no unified-max kernel
+    for q_dt, kv_dt, hq in [(torch.float16, torch.float16, 8),
+                            (torch.bfloat16, torch.float8_e4m3fn, 8),
+                            (torch.bfloat16, torch.bfloat16, 2),
+                            (torch.float32, torch.float32, 8)]:
+        bb = W.make_batch(batch_lengths=[40, 3], num_qo_heads=hq, num_kv_heads=2,
+                          head_dim=128, q_dtype=q_dt, kv_dtype=kv_dt, seed=2, device=cuda)
+        pp = lib.plan(bb.indptr, bb.indices, bb.last_page_len, hq, 2, 128, 16,
+                      q_data_type=q_dt, kv_data_type=kv_dt)
+        assert pp.info["unified_max"] == 0
+        with pytest.raises(lib.FaError) as e:
+            pp.run_unified_max(bb.q, bb.paged_kv, 10.0)
+        assert e.value.status == -2
+    bm = W.make_batch(batch_lengths=[40, 30], num_qo_heads=8, num_kv_heads=2, head_dim=128,
+                      q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, seed=3, device=cuda,
+                      q_len=2)
+    pm = lib.plan_multi_token(bm.indptr, bm.indices, bm.last_page_len, 2, 8, 2, 128, 16)
+    assert pm.info["unified_max"] == 0
+
+
 # ------------------------------------------------------------------ merge_states
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
@@ -384,13 +501,17 @@ def _sample_requests(b, k=6):
 
 
 @pytest.mark.parametrize("name", ["gqa_uniform", "ragged", "long_split", "fp8_kv",
-                                  "fp8_kv_token_scales", "spec_decode", "cascade"])
+                                  "fp8_kv_token_scales", "spec_decode", "cascade",
+                                  "gqa_unified_max"])
 def test_full_size_workloads_sampled(lib, cuda, name):
     b = W.make_config_batch(name, device=cuda)
     if "k_scales" in b.extra:
         p, o, lse = run_token_scales(lib, b)
     elif b.q_len > 1:
         p, o, lse = run_multi(lib, b)
+    elif name == "gqa_unified_max":
+        p, o, lse, n = run_um(lib, b, W.cauchy_schwarz_bound(b))
+        assert n == 0
     elif "prefix_pages" in b.extra:
         p, o, lse = run_cascade(lib, b)
         # and the same batch through plain decode
