@@ -252,12 +252,19 @@ typedef struct {
   int fused_merge;            /* 1: split requests merged inside the decode kernel */
   int q_len;                  /* query tokens per request */
   int unified_max;            /* 1: fa_decode_run_unified_max is built for this plan */
+  int num_pool_segments;      /* segments claimed at run time (0: static quotas only) */
+  int64_t pool_pages;         /* (page, kv head) pairs in those segments */
 } fa_plan_info;
 
 int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info);
 
 /* Work list of a plan, host copy owned by the plan (valid until destroy).
- *  cta_offsets  [num_ctas+1]: CTA c runs segments cta_offsets[c] .. [c+1]-1
+ *  cta_offsets  [num_ctas+1]: CTA c runs segments cta_offsets[c] .. [c+1]-1,
+ *               then claims pool segments cta_offsets[num_ctas] ..
+ *               num_segments-1 one at a time, in order, until none is left
+ *               (the pool is the last part of the page stream, cut into
+ *               chunks that shrink towards its end; it evens out CTAs that
+ *               stream pages at different rates)
  *  segments     [num_segments * FA_SEGMENT_INTS] int32, each
  *               {request, kv_head, page_begin, page_end, last_valid,
  *                out_slot, merge_unit, to_end}; page_begin/page_end index
@@ -278,12 +285,17 @@ int fa_decode_plan_get_work(fa_decode_plan_t plan, const int32_t** cta_offsets,
  * fa_decode_plan uses, exposed so it can be checked without a GPU.  Output
  * buffers are caller-owned host arrays of the stated capacities; counts are
  * written to *n_ctas, *n_segments, *n_merge, *n_slots.
- * Capacities needed: cta_offsets max_ctas+1, segments
- * (batch*num_kv_heads + max_ctas) * FA_SEGMENT_INTS, merge
- * max_ctas * FA_MERGE_INTS.  Errors: FA_ERR_INVALID_ARG. */
+ * pool_fraction in [0, 1): share of the page stream left to the run-time
+ * pool (fa_decode_plan uses none unless FADECODE_POOL in the environment
+ * sets a fraction up to 0.5; a pool smaller than 4 pages per CTA is not
+ * made).
+ * With C = max_ctas * 7 + 1 (the most cuts a plan makes), capacities needed:
+ * cta_offsets max_ctas+1, segments (batch*num_kv_heads + C) *
+ * FA_SEGMENT_INTS, merge C * FA_MERGE_INTS.  Errors: FA_ERR_INVALID_ARG. */
 int fa_plan_work_host(const int32_t* indptr, const int32_t* last_page_len,
                       int batch, int num_kv_heads, int page_size, int max_ctas,
-                      int min_pages_per_cta, int32_t* cta_offsets,
+                      int min_pages_per_cta, double pool_fraction,
+                      int32_t* cta_offsets,
                       int32_t* segments, int32_t* merge, int* n_ctas,
                       int* n_segments, int* n_merge, int* n_slots);
 

@@ -60,7 +60,8 @@ class PlanInfo(ctypes.Structure):
         ("total_pages", ctypes.c_int64), ("total_tokens", ctypes.c_int64),
         ("workspace_bytes_used", ctypes.c_size_t), ("plan_upload_bytes", ctypes.c_size_t),
         ("tensor_cores", ctypes.c_int), ("fused_merge", ctypes.c_int), ("q_len", ctypes.c_int),
-        ("unified_max", ctypes.c_int)]
+        ("unified_max", ctypes.c_int), ("num_pool_segments", ctypes.c_int),
+        ("pool_pages", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -108,7 +109,7 @@ def _load() -> ctypes.CDLL:
     pp = ctypes.POINTER(ctypes.POINTER(ctypes.c_int32))
     lib.fa_decode_plan_get_work.argtypes = [P, pp, pp, pp]
     lib.fa_decode_plan_get_work.restype = i32
-    lib.fa_plan_work_host.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P,
+    lib.fa_plan_work_host.argtypes = [P, P, i32, i32, i32, i32, i32, ctypes.c_double, P, P, P,
                                       ctypes.POINTER(i32), ctypes.POINTER(i32),
                                       ctypes.POINTER(i32), ctypes.POINTER(i32)]
     lib.fa_plan_work_host.restype = i32
@@ -400,19 +401,20 @@ def merge_states(o_a: torch.Tensor, lse_a: torch.Tensor, o_b: torch.Tensor, lse_
 
 
 def plan_work_host(indptr, last_page_len, num_kv_heads: int, page_size: int, max_ctas: int,
-                   min_pages_per_cta: int = 8):
+                   min_pages_per_cta: int = 8, pool_fraction: float = 0.0):
     """Host-only work-list builder (no GPU).  Returns (cta_offsets, segments [n,8],
-    merge [m,4], n_slots)."""
+    merge [m,4], n_slots); segments cta_offsets[-1]: are the run-time pool."""
     indptr_h = _host_i32(indptr)
     last_h = _host_i32(last_page_len)
     B = indptr_h.shape[0] - 1
+    cuts = max_ctas * 7 + 1
     cta = np.zeros(max_ctas + 1, np.int32)
-    seg = np.zeros(((B * num_kv_heads + max_ctas) * SEGMENT_INTS,), np.int32)
-    mer = np.zeros((max(max_ctas, 1) * MERGE_INTS,), np.int32)
+    seg = np.zeros(((B * num_kv_heads + cuts) * SEGMENT_INTS,), np.int32)
+    mer = np.zeros((cuts * MERGE_INTS,), np.int32)
     n_c, n_s, n_m, n_sl = (ctypes.c_int() for _ in range(4))
     _check(_L().fa_plan_work_host(indptr_h.ctypes.data, last_h.ctypes.data if B else None, B,
                                   num_kv_heads, page_size, max_ctas, min_pages_per_cta,
-                                  cta.ctypes.data, seg.ctypes.data, mer.ctypes.data,
+                                  float(pool_fraction), cta.ctypes.data, seg.ctypes.data, mer.ctypes.data,
                                   ctypes.byref(n_c), ctypes.byref(n_s), ctypes.byref(n_m),
                                   ctypes.byref(n_sl)), "fa_plan_work_host")
     return (cta[: n_c.value + 1].copy(), seg[: n_s.value * SEGMENT_INTS].reshape(-1, SEGMENT_INTS).copy(),

@@ -15,6 +15,7 @@
 #include "fa_decode.h"
 #include "kernels.h"
 #include "planner.h"
+#include "staging.h"
 
 using fadecode::DecodeKernel;
 using fadecode::DecodeParams;
@@ -24,14 +25,21 @@ using fadecode::WorkList;
 namespace {
 
 constexpr int kMinPagesPerCta = 8;     // smallest chunk worth a CTA of its own
-constexpr int kMaxCtasPerSmBound = 8;  // workspace bound; real occupancy is lower
+constexpr int kMaxCtasPerSmBound = 4;  // grid bound (every kernel fits 3 or 4 CTAs per SM)
+// Share of the page stream balanced at run time.  Off: on a GB300 the
+// static quotas already finish within a few percent of each other in
+// back-to-back launches, and the pool's extra pieces cost more than it saves
+// except on strongly mixed lengths (FADECODE_POOL=0.25: -2.7 % on the
+// 256..64000-token mix); a unit whose pages all fall in the pool also ends
+// up with hundreds of pieces to fold.
+constexpr double kPoolFraction = 0.0;
 constexpr size_t kAlign = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t off_err, off_umc, off_cta, off_seg, off_merge, off_count, meta_bytes, off_part_o, off_part_lse,
+  size_t off_err, off_umc, off_pool, off_cta, off_seg, off_merge, off_count, meta_bytes, off_part_o, off_part_lse,
       total;
 };
 
@@ -41,7 +49,8 @@ Layout make_layout(int64_t n_ctas, int64_t n_segments, int64_t n_merge, int64_t 
   Layout L;
   L.off_err = 0;
   L.off_umc = sizeof(int);  // unified-max re-centring counter
-  L.off_cta = align_up(L.off_umc + sizeof(int));
+  L.off_pool = 2 * sizeof(int);  // pool claim and done counters
+  L.off_cta = align_up(L.off_pool + 2 * sizeof(int));
   L.off_seg = align_up(L.off_cta + sizeof(int32_t) * (size_t)(n_ctas + 1));
   L.off_merge = align_up(L.off_seg + sizeof(fadecode::Segment) * (size_t)n_segments);
   L.off_count = align_up(L.off_merge + sizeof(fadecode::MergeUnit) * (size_t)n_merge);
@@ -68,6 +77,15 @@ int dtype_size(fa_dtype t) {
 bool fused_merge_enabled() {
   const char* v = std::getenv("FADECODE_MERGE");
   return !(v && std::strcmp(v, "kernel") == 0);
+}
+
+// FADECODE_POOL=<fraction> sets the share of the page stream left to the
+// run-time pool (0 turns it off, for comparisons); default kPoolFraction.
+double pool_fraction() {
+  const char* v = std::getenv("FADECODE_POOL");
+  if (!v) return kPoolFraction;
+  const double f = std::atof(v);
+  return f >= 0.0 && f <= 0.5 ? f : kPoolFraction;
 }
 
 // FADECODE_KERNEL=simt keeps every plan on the CUDA-core consumer (for
@@ -164,14 +182,27 @@ bool find_token_scale_kernel(fa_dtype q, fa_dtype kv, int D, int G, DecodeKernel
 }
 
 // Set a kernel's shared-memory limit and return how many of its CTAs fit on
-// one SM (0 on failure).
+// one SM (0 on failure).  Cached per (kernel, device): a plan per decode
+// step should not pay for these queries every time.
 int kernel_occupancy(const DecodeKernel& k) {
+  struct Entry {
+    const void* func;
+    int device, occ;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : cache)
+    if (e.func == k.func && e.device == dev) return e.occ;
   int occ = 0;
   if (cudaFuncSetAttribute(k.func, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem_bytes) !=
           cudaSuccess ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.func, k.threads, k.smem_bytes) !=
           cudaSuccess)
     return 0;
+  cache.push_back(Entry{k.func, dev, occ});
   return occ;
 }
 
@@ -231,21 +262,22 @@ size_t fa_decode_workspace_size(int batch, int num_qo_heads, int num_kv_heads, i
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return 0;
   const int64_t max_ctas = (int64_t)sms * kMaxCtasPerSmBound;
-  const int64_t segs = (int64_t)batch * num_kv_heads + max_ctas;
+  const int64_t cuts = fadecode::max_plan_cuts(max_ctas);
+  const int64_t segs = (int64_t)batch * num_kv_heads + cuts;
   const int G = num_qo_heads / num_kv_heads;
-  return make_layout(max_ctas, segs, max_ctas, 2 * max_ctas, G, head_dim).total;
+  return make_layout(max_ctas, segs, cuts, 2 * cuts, G, head_dim).total;
 }
 
 int fa_plan_work_host(const int32_t* indptr, const int32_t* last_page_len, int batch,
                       int num_kv_heads, int page_size, int max_ctas, int min_pages_per_cta,
-                      int32_t* cta_offsets, int32_t* segments, int32_t* merge, int* n_ctas,
+                      double pool_fraction, int32_t* cta_offsets, int32_t* segments, int32_t* merge, int* n_ctas,
                       int* n_segments, int* n_merge, int* n_slots) {
   if (!cta_offsets || !segments || !merge || !n_ctas || !n_segments || !n_merge || !n_slots)
     return FA_ERR_INVALID_ARG;
   WorkList wl;
   try {
     if (fadecode::build_work_list(indptr, last_page_len, batch, num_kv_heads, page_size,
-                                  max_ctas, min_pages_per_cta, &wl) != 0)
+                                  max_ctas, min_pages_per_cta, pool_fraction, &wl) != 0)
       return FA_ERR_INVALID_ARG;
   } catch (const std::bad_alloc&) {
     return FA_ERR_INVALID_ARG;
@@ -374,9 +406,25 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
 
   int rc = FA_OK;
   try {
-    if (fadecode::build_work_list(indptr_host, last_page_len_host, batch, num_kv_heads,
-                                  page_size, sms * occ, kMinPagesPerCta, &plan->wl) != 0)
-      rc = FA_ERR_INVALID_ARG;
+    // with the run-time pool if its partial states fit the workspace, else
+    // static quotas only
+    const double fractions[2] = {pool_fraction(), 0.0};
+    rc = FA_ERR_WORKSPACE_TOO_SMALL;
+    for (double f : fractions) {
+      if (fadecode::build_work_list(indptr_host, last_page_len_host, batch, num_kv_heads,
+                                    page_size, sms * occ, kMinPagesPerCta, f, &plan->wl) != 0) {
+        rc = FA_ERR_INVALID_ARG;
+        break;
+      }
+      const WorkList& w = plan->wl;
+      plan->layout = make_layout(w.num_ctas, (int64_t)w.segments.size(),
+                                 (int64_t)w.merge.size(), w.num_slots, G * q_len, head_dim);
+      if (plan->layout.total <= workspace_bytes) {
+        rc = FA_OK;
+        break;
+      }
+      if (f == 0.0 || w.pool_pages == 0) break;
+    }
   } catch (const std::bad_alloc&) {
     rc = FA_ERR_INVALID_ARG;
   }
@@ -385,12 +433,6 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
     return rc;
   }
   const WorkList& wl = plan->wl;
-  plan->layout = make_layout(wl.num_ctas, (int64_t)wl.segments.size(), (int64_t)wl.merge.size(),
-                             wl.num_slots, G * q_len, head_dim);
-  if (plan->layout.total > workspace_bytes) {
-    delete plan;
-    return FA_ERR_WORKSPACE_TOO_SMALL;
-  }
   plan->merge_flat.resize(wl.merge.size() * FA_MERGE_INTS);
   if (!wl.merge.empty())
     std::memcpy(plan->merge_flat.data(), wl.merge.data(), wl.merge.size() * sizeof(wl.merge[0]));
@@ -405,8 +447,8 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
   if (!wl.merge.empty())
     std::memcpy(meta.data() + plan->layout.off_merge, wl.merge.data(),
                 sizeof(fadecode::MergeUnit) * wl.merge.size());
-  if (cudaMemcpyAsync(plan->ws, meta.data(), meta.size(), cudaMemcpyHostToDevice,
-                      static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
+  if (fadecode::upload_async(plan->ws, meta.data(), meta.size(),
+                             static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
     delete plan;
     return FA_ERR_CUDA;
   }
@@ -502,6 +544,8 @@ int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info) {
   i.fused_merge = plan->fused_merge ? 1 : 0;
   i.q_len = plan->q_len;
   i.unified_max = plan->has[kUnifiedMax] ? 1 : 0;
+  i.num_pool_segments = plan->wl.pool_count();
+  i.pool_pages = plan->wl.pool_pages;
   *info = i;
   return FA_OK;
 }
@@ -523,6 +567,13 @@ int fa_decode_check(fa_decode_plan_t plan, void* cuda_stream, int* flags) {
   if (cudaStreamSynchronize(st) != cudaSuccess ||
       cudaMemcpy(&word, dword, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess ||
       cudaMemset(dword, 0, sizeof word) != cudaSuccess)
+    return FA_ERR_CUDA;
+  // A run that gave up waiting may leave the pool and merge counters short
+  // of their re-armed zeros: clear them for the next run.
+  if (word &&
+      (cudaMemset(plan->ws + plan->layout.off_pool, 0, 2 * sizeof(int)) != cudaSuccess ||
+       cudaMemset(plan->ws + plan->layout.off_count, 0,
+                  sizeof(int32_t) * plan->wl.merge.size()) != cudaSuccess))
     return FA_ERR_CUDA;
   *flags = word;
   return word ? FA_ERR_DEVICE_CHECK : FA_OK;
@@ -578,6 +629,10 @@ static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
   prm.v_scale = v_scale;
   prm.max_bound = max_bound * kLog2e;
   prm.um_fallbacks = reinterpret_cast<int*>(plan->ws + plan->layout.off_umc);
+  prm.pool_begin = plan->wl.pool_begin();
+  prm.pool_count = plan->wl.pool_count();
+  prm.pool_claim = reinterpret_cast<int*>(plan->ws + plan->layout.off_pool);
+  prm.pool_done = prm.pool_claim + 1;
 
   const bool timed = plan->ev_before && plan->ev_after;
   if (timed && cudaEventRecord(plan->ev_before, st) != cudaSuccess) return FA_ERR_CUDA;

@@ -34,6 +34,7 @@
 
 #include "decode_mma.cuh"
 #include "fa_decode.h"
+#include "staging.h"
 
 namespace fadecode {
 
@@ -515,8 +516,8 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
         s[0] = r0; s[1] = h; s[2] = pb; s[3] = pe; s[4] = nrows; s[5] = it; s[6] = 0; s[7] = 0;
       }
   for (int i = 0; i <= plan->items; ++i) cta[i] = i;
-  if (cudaMemcpyAsync(plan->ws + plan->L.off_err, meta.data(), meta.size(), cudaMemcpyHostToDevice,
-                      static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
+  if (fadecode::upload_async(plan->ws + plan->L.off_err, meta.data(), meta.size(),
+                             static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
     fa_decode_plan_destroy(plan->suffix);
     delete plan;
     return FA_ERR_CUDA;

@@ -296,23 +296,85 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[G], int c) {
 
 }  // namespace dev
 
+// Pool segments claimed at run time travel from the producer warp to the
+// consumer warps through this ring in shared memory.
+constexpr int kSegRing = 4;
+struct SegQueue {
+  uint64_t full[kSegRing];   // producer -> consumers, one arrival
+  uint64_t empty[kSegRing];  // consumers -> producer, one arrival per consumer warp
+  int seg[kSegRing];         // segment index, -1 once the pool is empty
+};
+constexpr int kSegQueueBytes = (int)((sizeof(SegQueue) + 15) / 16 * 16);
+
+__device__ __forceinline__ void seg_queue_init(SegQueue* q, int consumer_warps) {
+  for (int i = 0; i < kSegRing; ++i) {
+    dev::mbar_init(dev::smem_addr(&q->full[i]), 1);
+    dev::mbar_init(dev::smem_addr(&q->empty[i]), consumer_warps);
+  }
+}
+
 // Producer warp: walks the CTA's segments page by page, reads the page ids
 // through the index table (32 at a time) and issues, per page, BOXES 4-D TMA
 // tensor copies (box b starts at element b * BOX_X of a row and lands at
 // b * BOX_BYTES in the stage) completing on the stage's "full" barrier.  Page
 // k of the stream goes to stage k % S once the stage's previous page has been
 // released.  Ends by waiting (bounded) for its last copies to land.
+// With a queue, after its static segments the warp claims pool segments one
+// at a time and passes each (then -1) to the consumers through the queue; a
+// pool segment starts on a stream position that is a multiple of `align`
+// (empty stages fill the gap), so that the consumer warps split its pages the
+// same way whichever CTA claims it.
 // With SCALES, each page also brings the 16 per-token K scales and the 16 V
 // scales of its kv head (64 contiguous bytes each) into scales[stage][0..31].
 template <int S, int STAGE_BYTES, int BOXES, int BOX_X, int BOX_BYTES, bool SCALES = false>
 __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const DecodeParams& p,
                                               int seg_begin, int seg_end, uint8_t* ring,
                                               uint64_t* full, uint64_t* empty, int lane,
-                                              float* scales = nullptr) {
+                                              float* scales = nullptr, SegQueue* queue = nullptr,
+                                              int align = 1) {
   bool aborted = false;
   const uint64_t policy = dev::evict_first_policy();
-  int k = 0;
-  for (int si = seg_begin; si < seg_end; ++si) {
+  int k = 0, claimed = 0;
+  // lane 0 claims one pool segment ahead - the first while it issues the
+  // copies of its last static segment - so that a claim's round trip
+  // overlaps the copies of the segment before it
+  const bool pooled = queue && p.pool_count > 0;
+  int ahead = -1;
+  bool claiming = false;
+  for (int si = seg_begin;; ++si) {
+    if (pooled && !claiming && si >= seg_end - 1) {
+      claiming = true;
+      if (lane == 0) ahead = atomicAdd(p.pool_claim, 1);
+    }
+    if (si >= seg_end) {
+      if (!pooled) break;
+      int idx = p.pool_count;
+      if (lane == 0 && !aborted) {
+        idx = ahead;
+        if (idx < p.pool_count) ahead = atomicAdd(p.pool_claim, 1);
+      }
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      const int cur = idx < p.pool_count ? p.pool_begin + idx : -1;
+      if (lane == 0) {
+        const int slot = claimed % kSegRing;
+        dev::mbar_wait(dev::smem_addr(&queue->empty[slot]),
+                       (uint32_t)(((claimed / kSegRing) & 1) ^ 1), aborted, p.err);
+        *reinterpret_cast<volatile int*>(&queue->seg[slot]) = cur;
+        dev::mbar_arrive(dev::smem_addr(&queue->full[slot]));
+      }
+      ++claimed;
+      if (cur < 0) break;
+      si = cur;
+      const int pad = (align - k % align) % align;
+      if (lane == 0)
+        for (int i = 0; i < pad; ++i) {  // empty stages: released at once by their warp
+          const int kk = k + i;
+          dev::mbar_wait(dev::smem_addr(&empty[kk % S]), (uint32_t)(((kk / S) & 1) ^ 1), aborted,
+                         p.err);
+          dev::mbar_arrive(dev::smem_addr(&full[kk % S]));
+        }
+      k += pad;
+    }
     const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * si);
     const int kvh = sa.y, pb = sa.z, pe = sa.w;
     for (int p0 = pb; p0 < pe; p0 += 32) {
@@ -347,6 +409,7 @@ __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const Deco
         }
       }
     }
+    if (si >= seg_end) si = seg_end;  // a pool segment: the next one is claimed again
   }
   // No copy may still be landing in shared memory when the CTA exits (only
   // possible if a consumer gave up waiting).
@@ -355,6 +418,50 @@ __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const Deco
     for (int kk = first; kk < k; ++kk)
       if (!dev::mbar_wait_bounded(dev::smem_addr(&full[kk % S]), (uint32_t)((kk / S) & 1)))
         atomicOr(p.err, 2);
+  }
+}
+
+// Next segment for a consumer warp: the CTA's static segments in order, then
+// the pool segments its producer claimed, -1 when none is left.  A pool
+// segment first consumes the empty stages the producer inserted before it
+// (those of this warp) and moves kbase to the aligned start.  Warp-uniform.
+template <int S, int NW>
+__device__ __forceinline__ int next_segment(const DecodeParams& p, SegQueue* queue, int& si,
+                                            int seg_end, int& taken, int& kbase,
+                                            uint64_t* full, uint64_t* empty, int warp, int lane,
+                                            bool& aborted) {
+  if (si < seg_end) return si++;
+  if (p.pool_count == 0) return -1;
+  const int slot = taken % kSegRing;
+  dev::mbar_wait(dev::smem_addr(&queue->full[slot]), (uint32_t)((taken / kSegRing) & 1), aborted,
+                 p.err);
+  int cur = aborted ? -1 : *reinterpret_cast<volatile int*>(&queue->seg[slot]);
+  cur = __shfl_sync(0xffffffffu, cur, 0);
+  __syncwarp();
+  if (lane == 0) dev::mbar_arrive(dev::smem_addr(&queue->empty[slot]));
+  ++taken;
+  if (cur < 0) return -1;
+  const int ka = (kbase + NW - 1) / NW * NW;
+  for (int k = kbase; k < ka; ++k) {
+    if (k % NW != warp) continue;
+    dev::mbar_wait(dev::smem_addr(&full[k % S]), (uint32_t)((k / S) & 1), aborted, p.err);
+    __syncwarp();
+    if (lane == 0) dev::mbar_arrive(dev::smem_addr(&empty[k % S]));
+  }
+  kbase = ka;
+  return cur;
+}
+
+// End of a CTA's run (one thread): count it; the last CTA re-arms the pool
+// counters for the next run.  Every claim of this CTA's producer happened
+// before the end marker the consumers saw, so after the last count nobody
+// claims any more.
+__device__ __forceinline__ void pool_finish(const DecodeParams& p) {
+  if (p.pool_count == 0) return;
+  __threadfence();
+  if (atomicAdd(p.pool_done, 1) == (int)gridDim.x - 1) {
+    atomicExch(p.pool_claim, 0);
+    atomicExch(p.pool_done, 0);
   }
 }
 
@@ -380,14 +487,21 @@ __device__ __forceinline__ void fold_split_unit(const float* part_o, const float
   static_assert(NC == G * QL, "columns = heads of the group x query tokens");
   const int req = u.x, kvh = u.y, s0 = u.z, ns = u.w;
   if (ns * NC <= scratch_floats) {
-    // weights w[k][h] = 2^(lse_k - M_h) / den_h, and lse
+    auto sync = [&]() {
+      if (bar == 0) __syncthreads(); else dev::named_barrier(bar, nthreads);
+    };
+    // the unit's slots are consecutive: all ns * NC lse values in one pass
+    for (int i = tid; i < ns * NC; i += nthreads)
+      scratch[i] = __ldcg(part_lse + (size_t)s0 * NC + i);
+    sync();
+    // weights w[k][h] = 2^(lse_k - M_h) / den_h in place, and lse
     for (int h = tid; h < NC; h += nthreads) {
       float M = -INFINITY;
-      for (int k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(part_lse + (size_t)(s0 + k) * NC + h));
+      for (int k = 0; k < ns; ++k) M = fmaxf(M, scratch[k * NC + h]);
       float den = 0.f;
       if (M != -INFINITY)
         for (int k = 0; k < ns; ++k) {
-          const float w = dev::fast_exp2(__ldcg(part_lse + (size_t)(s0 + k) * NC + h) - M);
+          const float w = dev::fast_exp2(scratch[k * NC + h] - M);
           scratch[k * NC + h] = w;
           den += w;
         }
@@ -397,13 +511,42 @@ __device__ __forceinline__ void fold_split_unit(const float* part_o, const float
         lse_out[out_row<G, QL>(req, kvh, h, num_qo_heads)] =
             M != -INFINITY ? (M + dev::fast_log2(den)) * dev::kLn2 : -INFINITY;
     }
-    if (bar == 0) __syncthreads(); else dev::named_barrier(bar, nthreads);
-    for (int e = tid; e < NC * D; e += nthreads) {
-      const int h = e / D, dd = e % D;
-      float num = 0.f;
-      for (int k = 0; k < ns; ++k)
-        num = fmaf(__ldcg(part_o + ((size_t)(s0 + k) * NC + h) * D + dd), scratch[k * NC + h], num);
-      obase[out_row<G, QL>(req, kvh, h, num_qo_heads) * D + dd] = dev::from_float<QT>(num);
+    sync();
+    // four consecutive dims per thread (16-byte loads), eight pieces in
+    // flight: a unit of many pieces is bound by load latency otherwise
+    static_assert(D % 4 == 0, "float4 rows");
+    for (int e = tid; e < NC * D / 4; e += nthreads) {
+      const int h = e / (D / 4), d4 = (e % (D / 4)) * 4;
+      const float4* po = reinterpret_cast<const float4*>(part_o + ((size_t)s0 * NC + h) * D + d4);
+      const size_t stride = (size_t)NC * D / 4;  // float4s between pieces
+      float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+      int k = 0;
+      for (; k + 8 <= ns; k += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = __ldcg(po + (size_t)(k + j) * stride);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float w = scratch[(k + j) * NC + h];
+          num.x = fmaf(v[j].x, w, num.x);
+          num.y = fmaf(v[j].y, w, num.y);
+          num.z = fmaf(v[j].z, w, num.z);
+          num.w = fmaf(v[j].w, w, num.w);
+        }
+      }
+      for (; k < ns; ++k) {
+        const float4 v = __ldcg(po + (size_t)k * stride);
+        const float w = scratch[k * NC + h];
+        num.x = fmaf(v.x, w, num.x);
+        num.y = fmaf(v.y, w, num.y);
+        num.z = fmaf(v.z, w, num.z);
+        num.w = fmaf(v.w, w, num.w);
+      }
+      QT* orow = obase + out_row<G, QL>(req, kvh, h, num_qo_heads) * D + d4;
+      orow[0] = dev::from_float<QT>(num.x);
+      orow[1] = dev::from_float<QT>(num.y);
+      orow[2] = dev::from_float<QT>(num.z);
+      orow[3] = dev::from_float<QT>(num.w);
     }
     return;
   }
@@ -428,16 +571,29 @@ __device__ __forceinline__ void fold_split_unit(const float* part_o, const float
   }
 }
 
-// Segment epilogue shared by the decode kernels: fold the NW warp states
+// Split units whose last piece this CTA completed; it folds them after its
+// last segment.  Filled by consumer thread 0 only.
+constexpr int kMaxFolds = 60;
+struct FoldList {
+  int n;
+  int unit[kMaxFolds];
+  int pad[3];
+};
+constexpr int kFoldListBytes = (int)((sizeof(FoldList) + 15) / 16 * 16);
+
+// Combine the NW consumer warps' states of one segment for all NC columns
 // (unnormalised o in mo[w][h][d] against the warp's max mm[w][h], sum
 // md[w][h], all log2 domain) with the merge rule and write either the final
 // o (q dtype) and lse, or an fp32 partial slot.  Runs on the NW*32 consumer
-// threads between two consumer barriers.
+// threads after a consumer barrier and ends with one (mo is free again).
+// A split piece is then counted by thread 0 alone while the other warps go
+// on: the piece that completes its unit puts the unit on the CTA's fold list
+// (fold_pending), so no warp waits for the count's round trip.
 template <typename QT, int D, int G, int NW, int QL = 1>
 __device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const float* mo,
                                                  const float* mm, const float* md, int req,
                                                  int kvh, int out_slot, int merge_unit,
-                                                 int* flag) {
+                                                 FoldList* folds) {
   constexpr int CT = NW * 32;
   constexpr int NC = G * QL;  // columns: heads of the group x query tokens
   QT* __restrict__ obase = static_cast<QT*>(p.o);
@@ -467,28 +623,42 @@ __device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const fl
       if (dd == 0) p.part_lse[(size_t)out_slot * NC + h] = lse2;
     }
   }
-  if (out_slot < 0 || !p.fused_merge) return;
-  // Split unit: the CTA whose piece arrives last folds all pieces, in slot
-  // order, so the result does not depend on which CTA finished last.
-  dev::named_barrier(1, CT);  // all partial writes of this CTA done
-  if (threadIdx.x == 0) {
-    const int4 u = reinterpret_cast<const int4*>(p.merge)[merge_unit];
-    // one fence after the barrier publishes the whole CTA's writes (fences
-    // are cumulative) before the arrival is counted
-    __threadfence();
-    const int prev = atomicAdd(&p.merge_count[merge_unit], 1);
-    const int last = (prev == u.w - 1);
-    if (last) {
-      __threadfence();
-      p.merge_count[merge_unit] = 0;  // re-armed for the next run of the plan
-    }
-    *flag = last;
-  }
-  dev::named_barrier(1, CT);
-  if (!*flag) return;
+  dev::named_barrier(1, CT);  // all reads of mo and all writes of this CTA done
+  if (out_slot < 0 || !p.fused_merge || threadIdx.x != 0) return;
   const int4 u = reinterpret_cast<const int4*>(p.merge)[merge_unit];
+  // one fence after the barrier publishes the whole CTA's writes (fences
+  // are cumulative) before the arrival is counted
+  __threadfence();
+  const int prev = atomicAdd(&p.merge_count[merge_unit], 1);
+  if (prev != u.w - 1) return;
+  __threadfence();
+  p.merge_count[merge_unit] = 0;  // re-armed for the next run of the plan
+  if (folds->n < kMaxFolds) {
+    folds->unit[folds->n++] = merge_unit;
+    return;
+  }
+  // list full (a CTA that completed very many units): fold this one now,
+  // on this thread alone
   fold_split_unit<QT, D, NC, G, QL>(p.part_o, p.part_lse, u, obase, p.lse, p.num_qo_heads,
-                                    const_cast<float*>(mo), NW * NC * D, threadIdx.x, CT, 1);
+                                    nullptr, 0, 0, 1, 1);
+}
+
+// After a CTA's last segment: fold the split units it completed, in the
+// order it completed them; each fold combines the unit's pieces in slot
+// order, so the result does not depend on which CTA folds.  Consumer
+// threads only; mo serves as scratch.
+template <typename QT, int D, int G, int NW, int QL = 1>
+__device__ __forceinline__ void fold_pending(const DecodeParams& p, float* mo, FoldList* folds) {
+  constexpr int CT = NW * 32;
+  constexpr int NC = G * QL;
+  dev::named_barrier(1, CT);  // thread 0's list is complete
+  const int n = folds->n;
+  for (int i = 0; i < n; ++i) {
+    const int4 u = reinterpret_cast<const int4*>(p.merge)[folds->unit[i]];
+    fold_split_unit<QT, D, NC, G, QL>(p.part_o, p.part_lse, u, static_cast<QT*>(p.o), p.lse,
+                                      p.num_qo_heads, mo, NW * NC * D, threadIdx.x, CT, 1);
+    dev::named_barrier(1, CT);  // scratch free for the next unit
+  }
 }
 
 template <typename QT, typename KVT, int D, int G, int NW>
@@ -514,8 +684,9 @@ struct DecodeCfg {
   static constexpr int OFF_MO = OFF_P + 4 * NW * P * G;
   static constexpr int OFF_MM = OFF_MO + 4 * NW * G * D;
   static constexpr int OFF_MD = OFF_MM + 4 * NW * G;
-  static constexpr int OFF_FLAG = OFF_MD + 4 * NW * G;
-  static constexpr int SMEM = OFF_FLAG + 16;
+  static constexpr int OFF_FOLDS = OFF_MD + 4 * NW * G;
+  static constexpr int OFF_QUEUE = OFF_FOLDS + kFoldListBytes;
+  static constexpr int SMEM = OFF_QUEUE + kSegQueueBytes;
   static_assert(LPR <= 32 && 32 % LPR == 0 && P % RPS == 0, "row mapping");
   static_assert(G <= LPR, "group size larger than lanes per row");
   static_assert(STAGE_BYTES % 128 == 0, "stage alignment");
@@ -539,18 +710,22 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
   const int seg_begin = p.cta_offsets[blockIdx.x];
   const int seg_end = p.cta_offsets[blockIdx.x + 1];
 
+  SegQueue* queue = reinterpret_cast<SegQueue*>(smem + C::OFF_QUEUE);
+  FoldList* folds = reinterpret_cast<FoldList*>(smem + C::OFF_FOLDS);
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       dev::mbar_init(dev::smem_addr(&full[s]), 1);
       dev::mbar_init(dev::smem_addr(&empty[s]), 1);
     }
+    seg_queue_init(queue, NW);
+    folds->n = 0;
     dev::fence_barrier_init();
   }
   __syncthreads();
 
   if (warp == NW) {
     produce_pages<S, C::STAGE_BYTES, 1, 0, C::STAGE_BYTES>(&kv_map, p, seg_begin, seg_end, ring,
-                                                          full, empty, lane);
+                                                          full, empty, lane, nullptr, queue, NW);
     return;
   }
 
@@ -566,8 +741,11 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
   constexpr int CT = NW * 32;
 
   bool aborted = false;  // a timed-out wait makes every later wait return at once
-  int kbase = 0;
-  for (int si = seg_begin; si < seg_end; ++si) {
+  int kbase = 0, next_si = seg_begin, taken = 0;
+  for (;;) {
+    const int si = next_segment<S, NW>(p, queue, next_si, seg_end, taken, kbase, full, empty,
+                                       warp, lane, aborted);
+    if (si < 0) break;
     const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * si);
     const int4 sb = *reinterpret_cast<const int4*>(p.segments + 8 * si + 4);
     const int req = sa.x, kvh = sa.y, npg = sa.w - sa.z;
@@ -681,11 +859,11 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
     dev::named_barrier(1, CT);
 
     // Merge the NW warp states of this segment and emit.
-    combine_and_emit<QT, D, G, NW>(p, mo, mm, md, req, kvh, out_slot, sb.z,
-                                   reinterpret_cast<int*>(smem + C::OFF_FLAG));
-    dev::named_barrier(1, CT);
+    combine_and_emit<QT, D, G, NW>(p, mo, mm, md, req, kvh, out_slot, sb.z, folds);
     kbase += npg;
   }
+  fold_pending<QT, D, G, NW>(p, mo, folds);
+  if (threadIdx.x == 0) pool_finish(p);
 }
 
 // Split-level merge as a separate kernel: one CTA per (request, kv head)

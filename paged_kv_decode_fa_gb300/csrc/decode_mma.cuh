@@ -147,8 +147,9 @@ struct MmaCfg {
   static constexpr int OFF_MO = OFF_PT + NW * 8 * P * 2;
   static constexpr int OFF_MM = OFF_MO + 4 * NW * NC * D;
   static constexpr int OFF_MD = OFF_MM + 4 * NW * NC;
-  static constexpr int OFF_FLAG = OFF_MD + 4 * NW * NC;
-  static constexpr int OFF_SCALES = OFF_FLAG + 16;                 // [S][32] fp32 if TS
+  static constexpr int OFF_FOLDS = OFF_MD + 4 * NW * NC;
+  static constexpr int OFF_QUEUE = OFF_FOLDS + kFoldListBytes;
+  static constexpr int OFF_SCALES = OFF_QUEUE + kSegQueueBytes;    // [S][32] fp32 if TS
   static constexpr int SMEM = OFF_SCALES + (TS ? S * 2 * P * 4 : 0);
   static_assert(!TS || kFp8, "per-token scales are for E4M3 KV");
   static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte swizzle rows");
@@ -196,11 +197,15 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
   const int seg_begin = p.cta_offsets[blockIdx.x];
   const int seg_end = p.cta_offsets[blockIdx.x + 1];
 
+  SegQueue* queue = reinterpret_cast<SegQueue*>(smem + C::OFF_QUEUE);
+  FoldList* folds = reinterpret_cast<FoldList*>(smem + C::OFF_FOLDS);
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       dev::mbar_init(dev::smem_addr(&full[s]), 1);
       dev::mbar_init(dev::smem_addr(&empty[s]), 1);
     }
+    seg_queue_init(queue, NW);
+    folds->n = 0;
     dev::fence_barrier_init();
   }
   __syncthreads();
@@ -208,7 +213,7 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
   if (warp == NW) {
     produce_pages<S, C::STAGE_BYTES, SEGS, C::BOX_X, C::BOX_BYTES, TS>(
         &kv_map, p, seg_begin, seg_end, ring, full, empty, lane,
-        reinterpret_cast<float*>(smem + C::OFF_SCALES));
+        reinterpret_cast<float*>(smem + C::OFF_SCALES), queue, NW);
     return;
   }
 
@@ -224,8 +229,11 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
   const uint32_t ring_addr = dev::smem_addr(ring);
 
   bool aborted = false;  // a timed-out wait makes every later wait return at once
-  int kbase = 0;
-  for (int si = seg_begin; si < seg_end; ++si) {
+  int kbase = 0, next_si = seg_begin, taken = 0;
+  for (;;) {
+    const int si = next_segment<S, NW>(p, queue, next_si, seg_end, taken, kbase, full, empty,
+                                       warp, lane, aborted);
+    if (si < 0) break;
     const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * si);
     const int4 sb = *reinterpret_cast<const int4*>(p.segments + 8 * si + 4);
     const int req = sa.x, kvh = sa.y, npg = sa.w - sa.z;
@@ -550,11 +558,11 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
       }
     }
     dev::named_barrier(1, CT);
-    combine_and_emit<QT, D, G, NW, QL>(p, mo, mm, md, req, kvh, out_slot, sb.z,
-                                       reinterpret_cast<int*>(smem + C::OFF_FLAG));
-    dev::named_barrier(1, CT);
+    combine_and_emit<QT, D, G, NW, QL>(p, mo, mm, md, req, kvh, out_slot, sb.z, folds);
     kbase += npg;
   }
+  fold_pending<QT, D, G, NW, QL>(p, mo, folds);
+  if (threadIdx.x == 0) pool_finish(p);
 }
 
 template <typename QT, typename KVT, int D, int G, int NW = 4, bool TS = false, int QL = 1,

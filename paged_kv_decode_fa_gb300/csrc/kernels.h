@@ -34,6 +34,13 @@ struct DecodeParams {
   float v_scale;
   float max_bound;    // unified-max kernels: static reference of the logits, log2 units
   int* um_fallbacks;  // unified-max kernels: count of (segment, warp) re-centrings, or nullptr
+  // Pool of the plan: segments pool_begin .. pool_begin + pool_count - 1,
+  // claimed in order through *pool_claim; *pool_done counts finished CTAs
+  // and the last one re-arms both (zero between runs).
+  int pool_begin;
+  int pool_count;
+  int* pool_claim;
+  int* pool_done;
 };
 
 struct MergeParams {

@@ -15,6 +15,16 @@
 // is spread over as many CTAs as its length needs, which is the split-KV
 // idea of section "FlashDecoding - the split-KV trick".
 //
+// Equal quotas assume equal speed, but CTAs do not stream pages at exactly
+// the same rate, so the slowest CTA sets the end of the launch.  With
+// pool_fraction > 0 the planner hands only the first (1 - pool_fraction) of
+// the stream out as quotas and cuts the rest into a pool of chunks, long ones
+// first, that CTAs claim at run time (one atomic per chunk) once their quota
+// is done - the fast CTAs take more of them and all CTAs finish within about
+// one short chunk of each other.  The chunks are fixed here, so every chunk
+// is computed the same way whichever CTA claims it.  Each chunk is one more
+// piece to merge, which is why the library leaves the pool off by default.
+//
 // Requests with no pages still get one (empty) segment per kv head so that
 // their output (o = 0, lse = -inf) is written.
 #include "planner.h"
@@ -25,9 +35,9 @@ namespace fadecode {
 
 int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
                     int batch, int num_kv_heads, int page_size, int max_ctas,
-                    int min_pages_per_cta, WorkList* out) {
+                    int min_pages_per_cta, double pool_fraction, WorkList* out) {
   if (!indptr || !out || batch < 0 || num_kv_heads <= 0 || page_size <= 0 ||
-      max_ctas <= 0)
+      max_ctas <= 0 || !(pool_fraction >= 0.0 && pool_fraction < 1.0))
     return -1;
   if (batch > 0 && !last_page_len) return -1;
   if (indptr[0] != 0) return -1;
@@ -47,60 +57,120 @@ int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
   int64_t n = max_ctas;
   if (T > 0) n = std::min<int64_t>(n, (T + min_pages_per_cta - 1) / min_pages_per_cta);
   if (n < 1) n = 1;
-  const int64_t quota = T > 0 ? (T + n - 1) / n : 1;
-  if (T > 0) n = (T + quota - 1) / quota;  // no CTA left without pages
+  // The pool: the last pool_pages positions of the stream, if there are
+  // enough of them to give every CTA a few chunks.
+  int64_t pool = (int64_t)(pool_fraction * (double)T);
+  if (pool < n * kPoolMinPages * 2) pool = 0;
+  const int64_t S = T - pool;  // static positions [0, S)
+  const int64_t quota = S > 0 ? (S + n - 1) / n : 1;
+  if (pool == 0 && T > 0) n = (T + quota - 1) / quota;  // no CTA left without pages
   const int num_ctas = (int)n;
+
+  // Pool chunk ends (absolute stream positions): tier t cuts n chunks of
+  // ceil(pool / (n * 2^(t+1))) pages, so early claims take long chunks and
+  // the last ones short chunks that even out the CTAs' finishing times.
+  std::vector<int64_t> chunk_end;
+  if (pool > 0) {
+    int64_t a = S, size = kPoolMinPages;
+    for (int t = 0; t < kPoolTiers && a < T; ++t) {
+      const int64_t div = n << (t + 1);
+      size = std::max<int64_t>(kPoolMinPages, (pool + div - 1) / div);
+      for (int64_t c = 0; c < n && a < T; ++c) chunk_end.push_back(a = std::min(T, a + size));
+      if (size == kPoolMinPages) break;
+    }
+    while (a < T) chunk_end.push_back(a = std::min(T, a + size));
+  }
 
   WorkList wl;
   wl.num_ctas = num_ctas;
   wl.total_pages = total_pages;
   wl.total_tokens = total_tokens;
-  std::vector<int32_t> seg_cta;  // owning CTA of each segment (non-decreasing)
-  wl.segments.reserve((size_t)batch * num_kv_heads + num_ctas);
-  seg_cta.reserve(wl.segments.capacity());
+  wl.pool_pages = pool;
+  wl.cta_offsets.assign((size_t)num_ctas + 1, 0);
+  const size_t units = (size_t)batch * num_kv_heads;
+  std::vector<Segment> pooled;  // pool segments, in stream order
+  wl.segments.reserve(units + num_ctas + 1);
+  if (pool > 0) pooled.reserve(chunk_end.size() + 64);
 
+  // Positions only grow, so the owning CTA and the next cut are tracked
+  // incrementally (64-bit divisions per piece cost more than the rest).
+  size_t ci = 0;        // first chunk end beyond the current position
+  int64_t cta = 0;      // CTA of the current static position
+  int64_t cut = quota;  // end of that CTA's quota
   int64_t pos = 0;
   int slots = 0;
   for (int i = 0; i < batch; ++i) {
     const int32_t pb = indptr[i], pe = indptr[i + 1];
     const int64_t np = (int64_t)pe - pb;
+    const int64_t len = np > 0 ? (np - 1) * page_size + last_page_len[i] : 0;
     for (int h = 0; h < num_kv_heads; ++h) {
+      const int64_t start = pos, end = pos + np;
+      pos = end;
+      while (start >= cut && cta < num_ctas - 1) {
+        ++cta;
+        cut += quota;
+      }
       if (np == 0) {
-        const int64_t cta = std::min<int64_t>(pos / quota, num_ctas - 1);
-        wl.segments.push_back(Segment{i, h, pb, pb, page_size, -1, -1, 0});
-        seg_cta.push_back((int32_t)cta);
+        const Segment e{i, h, pb, pb, page_size, -1, -1, 0};
+        if (pool > 0 && start >= S) {
+          pooled.push_back(e);
+        } else {
+          wl.segments.push_back(e);
+          wl.cta_offsets[(size_t)cta + 1]++;
+        }
         continue;
       }
-      const int64_t start = pos, end = pos + np;
-      const size_t first = wl.segments.size();
-      const int64_t len = (np - 1) * page_size + last_page_len[i];
-      for (int64_t a = start; a < end;) {
-        const int64_t cta = a / quota;
-        const int64_t b = std::min(end, (cta + 1) * quota);
-        const int32_t last = (b == end) ? last_page_len[i] : page_size;
-        wl.segments.push_back(Segment{i, h, (int32_t)(pb + (a - start)),
-                                      (int32_t)(pb + (b - start)), last, -1, -1,
-                                      (int32_t)(len - (a - start) * page_size)});
-        seg_cta.push_back((int32_t)cta);
-        a = b;
+      // pieces: static ones cut at quota boundaries, pool ones at chunk ends
+      const int64_t se = std::min(end, S);
+      int pieces = 0;
+      if (start < se) {
+        pieces = 1;
+        for (int64_t c = cut; c < se; c += quota) ++pieces;
       }
-      const int pieces = (int)(wl.segments.size() - first);
+      if (end > S) {
+        const int64_t a = std::max(start, S);
+        while (chunk_end[ci] <= a) ++ci;
+        size_t cj = ci;
+        while (chunk_end[cj] < end) ++cj;
+        pieces += (int)(cj - ci) + 1;
+      }
+      int slot = -1, unit = -1;
       if (pieces > 1) {
-        const int unit = (int)wl.merge.size();
+        unit = (int)wl.merge.size();
         wl.merge.push_back(MergeUnit{i, h, slots, pieces});
-        for (int k = 0; k < pieces; ++k) {
-          wl.segments[first + k].out_slot = slots + k;
-          wl.segments[first + k].merge_unit = unit;
-        }
+        slot = slots;
         slots += pieces;
       }
-      pos = end;
+      for (int64_t a = start; a < end;) {
+        const bool in_pool = a >= S;
+        int64_t b;
+        if (!in_pool) {
+          while (a >= cut) {
+            ++cta;
+            cut += quota;
+          }
+          b = std::min(se, cut);
+        } else {
+          while (chunk_end[ci] <= a) ++ci;
+          b = std::min(end, chunk_end[ci]);
+        }
+        const Segment sg{i, h, (int32_t)(pb + (a - start)), (int32_t)(pb + (b - start)),
+                         (b == end) ? last_page_len[i] : page_size, slot, unit,
+                         (int32_t)(len - (a - start) * page_size)};
+        if (in_pool) {
+          pooled.push_back(sg);
+        } else {
+          wl.segments.push_back(sg);
+          wl.cta_offsets[(size_t)cta + 1]++;
+        }
+        if (slot >= 0) ++slot;
+        a = b;
+      }
     }
   }
   wl.num_slots = slots;
-  wl.cta_offsets.assign((size_t)num_ctas + 1, 0);
-  for (int32_t c : seg_cta) wl.cta_offsets[(size_t)c + 1]++;
   for (int c = 0; c < num_ctas; ++c) wl.cta_offsets[c + 1] += wl.cta_offsets[c];
+  wl.segments.insert(wl.segments.end(), pooled.begin(), pooled.end());
   *out = std::move(wl);
   return 0;
 }

@@ -27,7 +27,22 @@ struct MergeUnit {
 };
 static_assert(sizeof(MergeUnit) == 16, "MergeUnit must stay 16 bytes");
 
+// Pool of the balanced plan: its chunk sizes halve over kPoolTiers tiers of
+// one chunk per CTA each, then the rest goes in chunks of the last size; no
+// chunk is shorter than kPoolMinPages pages (unless a unit ends first).
+constexpr int kPoolTiers = 4;
+constexpr int kPoolMinPages = 2;
+
+// Upper bound of the cuts a plan makes into (request, kv head) units for a
+// grid of n CTAs: n - 1 quota boundaries, the pool's start and at most
+// (kPoolTiers + 2) * n chunk boundaries.  Segments <= units + cuts and
+// partial slots <= 2 * cuts.
+inline int64_t max_plan_cuts(int64_t n) { return n * (kPoolTiers + 3) + 1; }
+
 struct WorkList {
+  // Static part: CTA c runs segments cta_offsets[c] .. cta_offsets[c+1]-1.
+  // Pool: segments cta_offsets[num_ctas] .. segments.size()-1, claimed at
+  // run time, in order, by whichever CTA is free (none when pool_pages = 0).
   std::vector<int32_t> cta_offsets;  // num_ctas + 1
   std::vector<Segment> segments;
   std::vector<MergeUnit> merge;
@@ -35,11 +50,15 @@ struct WorkList {
   int num_slots = 0;
   int64_t total_pages = 0;   // sum over requests (not times kv heads)
   int64_t total_tokens = 0;  // sum of len over requests
+  int64_t pool_pages = 0;    // (page, kv head) pairs left to the pool
+  int pool_begin() const { return cta_offsets.empty() ? 0 : cta_offsets.back(); }
+  int pool_count() const { return (int)segments.size() - pool_begin(); }
 };
 
 // Returns 0 on success, -1 for malformed input (see fa_decode.h).
+// pool_fraction in [0, 1): share of the page stream left to the pool.
 int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
                     int batch, int num_kv_heads, int page_size, int max_ctas,
-                    int min_pages_per_cta, WorkList* out);
+                    int min_pages_per_cta, double pool_fraction, WorkList* out);
 
 }  // namespace fadecode

@@ -148,6 +148,58 @@ def test_all_requests_empty(lib, cuda):
     assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
 
 
+POOL_CASES = [  # (q dtype, kv dtype, qo heads, kv heads, q_len, path)
+    (torch.bfloat16, torch.bfloat16, 8, 2, 1, "run"),
+    (torch.bfloat16, torch.float8_e4m3fn, 16, 2, 1, "run"),
+    (torch.float32, torch.float32, 2, 2, 1, "run"),            # CUDA-core consumer
+    (torch.bfloat16, torch.bfloat16, 4, 2, 2, "multi"),
+    (torch.bfloat16, torch.float8_e4m3fn, 8, 2, 1, "token_scales"),
+    (torch.bfloat16, torch.bfloat16, 8, 2, 1, "unified_max"),
+]
+
+
+@pytest.mark.parametrize("case", POOL_CASES, ids=lambda c: f"{c[5]}-{str(c[1]).split('.')[-1]}-g{c[2] // c[3]}")
+def test_run_time_pool(lib, cuda, monkeypatch, case):
+    """A batch large enough for the run-time pool (40 % of the page stream
+    here): every output against the oracle, twice in a row (the claim
+    counters re-arm), bitwise equal between the runs (a pool segment is
+    computed the same way whichever CTA claims it)."""
+    q_dt, kv_dt, hq, hkv, q_len, path = case
+    monkeypatch.setenv("FADECODE_POOL", "0.4")
+    # 3715 pages x 2 kv heads: enough for a pool on 4 CTAs per SM
+    lengths = [9000, 7, 0, 5000, 16, 12000, 33, 8191, 640, 3000, 20000, 1500]
+    lengths = [max(n, q_len) if q_len > 1 else n for n in lengths]  # room for the drafts
+    b = W.make_batch(batch_lengths=lengths, num_qo_heads=hq, num_kv_heads=hkv, head_dim=128,
+                     q_dtype=q_dt, kv_dtype=kv_dt, seed=120 + hq + q_len, device=cuda,
+                     token_scales=(path == "token_scales"), q_len=q_len)
+    if path == "multi":
+        p = lib.plan_multi_token(b.indptr, b.indices, b.last_page_len, q_len, hq, hkv, 128, 16,
+                                 q_data_type=q_dt, kv_data_type=kv_dt)
+    else:
+        p = lib.plan(b.indptr, b.indices, b.last_page_len, hq, hkv, 128, 16, q_data_type=q_dt,
+                     kv_data_type=kv_dt)
+    assert p.info["num_pool_segments"] > 0 and p.info["pool_pages"] > 0
+    check_coverage(p, b)
+
+    def once():
+        if path == "token_scales":
+            r = p.run_token_scales(b.q, b.paged_kv, b.extra["k_scales"], b.extra["v_scales"])
+        elif path == "unified_max":
+            r = p.run_unified_max(b.q, b.paged_kv, W.cauchy_schwarz_bound(b))
+        else:
+            r = p.run(b.q, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale)
+        torch.cuda.synchronize()
+        return r
+
+    o1, lse1 = once()
+    o2, lse2 = once()
+    assert p.check() == 0
+    assert torch.equal(o1, o2) and torch.equal(lse1, lse2)
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o2, lse2, ref_o, ref_lse, tol_for(b),
+            rel=TOKEN_SCALE_REL if path == "token_scales" else 0.0)
+
+
 @pytest.mark.parametrize("merge", ["fused", "kernel"])
 def test_deterministic_and_no_lse(lib, cuda, monkeypatch, merge):
     if merge == "kernel":

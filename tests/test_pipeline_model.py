@@ -138,3 +138,160 @@ def test_shared_stage_round_robin_aliases():
             found = True
             break
     assert found
+
+
+def simulate_pool(static_pages, pool_pages, S, NW, R, seed, max_ticks=400000):
+    """The kernel's protocol with a run-time pool: after its static segments
+    the producer publishes each claimed pool segment (then an end marker)
+    through a ring of R queue slots (mbarriers "qfull", one arrival, and
+    "qempty", NW arrivals) and starts it on a stream position that is a
+    multiple of NW, filling the gap with empty stages (arrive on "full"
+    without a copy).  Each consumer warp reads the queue, releases the empty
+    stages it owns and then takes the segment's pages k with k % NW == w.
+    Checks every admitted page and queue entry, and that nothing deadlocks."""
+    rng = random.Random(seed)
+    full = [Barrier() for _ in range(S)]
+    empty = [Barrier() for _ in range(S)]
+    qfull = [Barrier() for _ in range(R)]
+    qempty = [Barrier() for _ in range(R)]
+    qempty_arrivals = [0] * R
+    qval = [None] * R
+    errors = []
+
+    # stream layout: static segments back to back, pool segments aligned
+    prod = []      # producer steps: ("page", k) | ("pad", k) | ("pub", j, value)
+    cons = [[] for _ in range(NW)]   # ("page", k) | ("pad", k) | ("take", j, value) | ("bar", i)
+    k = 0
+    seg_no = 0
+    for n in static_pages:
+        for kk in range(k, k + n):
+            prod.append(("page", kk))
+            cons[kk % NW].append(("page", kk))
+        for w in range(NW):
+            cons[w].append(("bar", seg_no))
+        k += n
+        seg_no += 1
+    for j, n in enumerate(list(pool_pages) + [None]):
+        prod.append(("pub", j, n))
+        for w in range(NW):
+            cons[w].append(("take", j, n))
+        if n is None:
+            break
+        ka = -(-k // NW) * NW
+        for kk in range(k, ka):
+            prod.append(("pad", kk))
+            cons[kk % NW].append(("pad", kk))
+        k = ka
+        for kk in range(k, k + n):
+            prod.append(("page", kk))
+            cons[kk % NW].append(("page", kk))
+        for w in range(NW):
+            cons[w].append(("bar", seg_no))
+        k += n
+        seg_no += 1
+    K = k
+    issued, landed, consumed = [False] * K, [False] * K, [False] * K
+    in_flight = []
+    ppc = 0
+    pc = [0] * NW
+    at_bar = [None] * NW
+    bar_pos = [{} for _ in range(NW)]
+    for w in range(NW):
+        for i, st in enumerate(cons[w]):
+            if st[0] == "bar":
+                bar_pos[w][st[1]] = i
+    busy_until = [0] * NW
+    tick = 0
+    while tick < max_ticks:
+        tick += 1
+        still = []
+        for t, kk in in_flight:
+            if t <= tick:
+                s = kk % S
+                if full[s].completed != kk // S:
+                    errors.append(f"copy of page {kk} completed the wrong phase of stage {s}")
+                full[s].completed += 1
+                landed[kk] = True
+            else:
+                still.append((t, kk))
+        in_flight = still
+        agents = list(range(NW + 1))
+        rng.shuffle(agents)
+        for a in agents:
+            if a == NW:
+                if ppc >= len(prod):
+                    continue
+                st = prod[ppc]
+                if st[0] in ("page", "pad"):
+                    kk = st[1]
+                    s = kk % S
+                    if empty[s].try_wait(((kk // S) & 1) ^ 1):
+                        if kk >= S and not consumed[kk - S]:
+                            errors.append(f"stage {s} reused before page {kk - S} was released")
+                        issued[kk] = True
+                        if st[0] == "page":
+                            in_flight.append((tick + rng.randint(1, 40), kk))
+                        else:
+                            full[s].completed += 1
+                            landed[kk] = True
+                        ppc += 1
+                else:
+                    _, j, n = st
+                    slot = j % R
+                    if qempty[slot].try_wait(((j // R) & 1) ^ 1):
+                        qval[slot] = (j, n)
+                        qfull[slot].completed += 1
+                        ppc += 1
+                continue
+            w = a
+            if pc[w] >= len(cons[w]) or busy_until[w] > tick:
+                continue
+            st = cons[w][pc[w]]
+            if st[0] in ("page", "pad"):
+                kk = st[1]
+                s = kk % S
+                if full[s].try_wait((kk // S) & 1):
+                    if not landed[kk]:
+                        errors.append(f"warp {w} admitted stream position {kk} before it landed")
+                    if kk + S < K and issued[kk + S]:
+                        errors.append(f"warp {w} admitted position {kk} after its stage was refilled")
+                    consumed[kk] = True
+                    empty[s].completed += 1
+                    busy_until[w] = tick + (rng.randint(0, 6) if st[0] == "page" else 0)
+                    pc[w] += 1
+            elif st[0] == "take":
+                _, j, n = st
+                slot = j % R
+                if qfull[slot].try_wait((j // R) & 1):
+                    if qval[slot] != (j, n):
+                        errors.append(f"warp {w} read queue entry {qval[slot]} instead of {(j, n)}")
+                    qempty_arrivals[slot] += 1
+                    if qempty_arrivals[slot] == NW:
+                        qempty_arrivals[slot] = 0
+                        qempty[slot].completed += 1
+                    pc[w] += 1
+            else:
+                x = st[1]
+                at_bar[w] = x
+                if all(at_bar[v] == x or pc[v] > bar_pos[v][x] for v in range(NW)):
+                    for v in range(NW):
+                        if at_bar[v] == x:
+                            at_bar[v] = None
+                            pc[v] += 1
+        if errors:
+            return errors
+        if ppc == len(prod) and not in_flight and all(pc[w] == len(cons[w]) for w in range(NW)):
+            return []
+    return [f"no progress after {max_ticks} ticks (deadlock)"]
+
+
+@pytest.mark.parametrize("NW,spw", [(4, 2), (4, 4), (2, 3), (8, 1)])
+def test_pool_queue_and_alignment_are_safe(NW, spw):
+    """Static segments, then pool segments of 0..9 pages (many shorter than
+    NW, so most need padding), passed through a 4-slot queue."""
+    rng = random.Random(100 + NW * 10 + spw)
+    for trial in range(40):
+        static = random_segments(rng, n_max=4, pages_max=30)
+        pool = [rng.randint(0, 9) for _ in range(rng.randint(0, 25))]
+        errs = simulate_pool(static, pool, S=NW * spw, NW=NW, R=4, seed=trial)
+        assert not errs, (static, pool, errs[:3])

@@ -23,8 +23,11 @@ def expand(seg):
     return out[order]
 
 
-def check_work(lib, indptr, last, Hkv, max_ctas, min_pages=8, P=16):
-    cta, seg, mer, n_slots = lib.plan_work_host(indptr, last, Hkv, P, max_ctas, min_pages)
+POOL_TIERS, POOL_MIN = 4, 2   # the planner's pool schedule
+
+
+def check_work(lib, indptr, last, Hkv, max_ctas, min_pages=8, P=16, pool=0.0):
+    cta, seg, mer, n_slots = lib.plan_work_host(indptr, last, Hkv, P, max_ctas, min_pages, pool)
     indptr = np.asarray(indptr, np.int64)
     B = len(indptr) - 1
     # coverage, bit-exact
@@ -34,19 +37,42 @@ def check_work(lib, indptr, last, Hkv, max_ctas, min_pages=8, P=16):
     for i in np.nonzero(np.diff(indptr) == 0)[0]:
         e = seg[(seg[:, 0] == i)]
         assert len(e) == Hkv and np.all(e[:, 2] == e[:, 3]) and np.all(e[:, 5] == -1)
-    # CTA ranges partition the segments, in order
+    # CTA ranges partition the static segments, in order; the rest is the pool
     n_ctas = len(cta) - 1
-    assert cta[0] == 0 and cta[-1] == len(seg) and np.all(np.diff(cta) >= 0)
+    assert cta[0] == 0 and cta[-1] <= len(seg) and np.all(np.diff(cta) >= 0)
     assert 1 <= n_ctas <= max_ctas
     T = int(indptr[-1]) * Hkv
+    pool_pages = int(pool * T)
+    if pool_pages < n_ctas * POOL_MIN * 2:
+        pool_pages = 0
+    S = T - pool_pages
     pages = np.array([(seg[cta[c]:cta[c + 1], 3] - seg[cta[c]:cta[c + 1], 2]).sum()
                       for c in range(n_ctas)])
-    assert pages.sum() == T
+    pooled = seg[cta[-1]:]
+    assert pages.sum() == S
+    assert (pooled[:, 3] - pooled[:, 2]).sum() == pool_pages
+    if pool_pages == 0:
+        assert len(pooled) == 0
     if T:
-        quota = -(-T // n_ctas)
-        assert pages.max() <= quota
-        assert np.all(pages[:-1] == quota)     # all but the last CTA are full
+        quota = -(-S // n_ctas)
         assert n_ctas <= -(-T // min_pages)
+        # every CTA holds a full quota until the static part runs out
+        want = np.minimum(quota, np.maximum(0, S - quota * np.arange(n_ctas)))
+        np.testing.assert_array_equal(pages, want)
+        if pool_pages == 0:
+            assert pages[-1] > 0               # no CTA left without pages
+    if pool_pages:
+        # the pool is the end of the stream (request-major, then kv head, then
+        # page) and its chunks are no longer than the first tier's
+        key = lambda x: (x[:, 0].astype(np.int64) * Hkv + x[:, 1]) * (1 << 31) + x[:, 2]
+        stat = seg[:cta[-1]]
+        stat = stat[stat[:, 3] > stat[:, 2]]
+        if len(stat):
+            assert key(stat).max() < key(pooled[pooled[:, 3] > pooled[:, 2]]).min()
+        first = -(-pool_pages // (2 * n_ctas))
+        assert (pooled[:, 3] - pooled[:, 2]).max() <= max(first, POOL_MIN)
+        units = len({(int(r), int(h)) for r, h in pooled[:, :2]})
+        assert len(pooled) <= (POOL_TIERS + 1) * n_ctas + 1 + units
     # last_valid: the page that ends a request carries its last_page_len;
     # to_end: tokens from the segment's first token to the end of its request
     for s in seg:
@@ -70,7 +96,9 @@ def check_work(lib, indptr, last, Hkv, max_ctas, min_pages=8, P=16):
     assert np.all(unsplit[:, 6] == -1)
     for r, h in unsplit[:, :2]:
         assert ((seg[:, 0] == r) & (seg[:, 1] == h)).sum() == 1
-    assert n_slots <= 2 * n_ctas
+    assert n_slots <= 2 * (n_ctas * (POOL_TIERS + 3) + 1)
+    if pool_pages == 0:
+        assert n_slots <= 2 * n_ctas
     return cta, seg, mer, n_slots
 
 
@@ -86,7 +114,8 @@ def test_named_workloads_coverage(lib, name):
     lengths = W.draw_lengths(cfg, torch.Generator().manual_seed(cfg.seed))
     indptr, last = _table(lengths)
     for max_ctas in (152 * 3, 152 * 2, 7):
-        check_work(lib, indptr, last, cfg.num_kv_heads, max_ctas)
+        for pool in (0.0, 0.125, 0.3):
+            check_work(lib, indptr, last, cfg.num_kv_heads, max_ctas, pool=pool)
 
 
 def test_random_batches(lib):
@@ -97,13 +126,28 @@ def test_random_batches(lib):
         lengths[rng.random(B) < 0.15] = 0       # some empty requests
         Hkv = int(rng.choice([1, 2, 4, 8]))
         indptr, last = _table(lengths)
-        check_work(lib, indptr, last, Hkv, int(rng.integers(1, 500)), int(rng.integers(1, 20)))
+        check_work(lib, indptr, last, Hkv, int(rng.integers(1, 500)), int(rng.integers(1, 20)),
+                   pool=float(rng.choice([0.0, 0.125, 0.4])))
 
 
 def test_all_empty_and_single_page(lib):
     check_work(lib, *_table([0, 0, 0]), 2, 100)
     check_work(lib, *_table([1]), 1, 100)
     check_work(lib, *_table([16]), 4, 1)
+
+
+def test_pool_chunks_shrink(lib):
+    """gqa_uniform on 456 CTAs with 1/8 of the stream pooled: the chunks are
+    claimed long ones first and end in short ones."""
+    cfg = W.CONFIGS["gqa_uniform"]
+    indptr, last = _table(W.draw_lengths(cfg, torch.Generator().manual_seed(cfg.seed)))
+    cta, seg, mer, n_slots = check_work(lib, indptr, last, 8, 456, pool=0.125)
+    pooled = seg[cta[-1]:]
+    sizes = pooled[:, 3] - pooled[:, 2]
+    assert sizes.sum() == 65536 // 8
+    assert sizes[:100].mean() > 2 * sizes[-100:].mean()
+    assert sizes[-100:].max() <= 3
+    assert len(pooled) <= 5 * 456 + 64
 
 
 def test_deterministic(lib):
