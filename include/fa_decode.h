@@ -83,7 +83,11 @@ size_t fa_decode_workspace_size(int batch, int num_qo_heads, int num_kv_heads,
  *  indices_dev         [indptr[batch]] int32, device.  Physical page ids.  Kept
  *                      by pointer and read by every fa_decode_run of this plan:
  *                      it must stay valid and unchanged while the plan is used.
- *                      Ids may repeat across requests (shared prefixes).
+ *                      Ids may repeat across requests (shared prefixes).  May
+ *                      also be page-locked host memory (cudaHostAlloc or
+ *                      cudaHostRegister), which the kernels then read over
+ *                      the CPU-GPU link (on a GB300 node, NVLink-C2C: about 2 %
+ *                      slower than device memory, and no upload).
  *  last_page_len_host  [batch] int32, host.  Valid slots in each request's last
  *                      page, in [1, page_size]; ignored for a request with no
  *                      pages (its output is o = 0, lse = -inf).
@@ -139,7 +143,10 @@ int fa_decode_plan_multi_token(const int32_t* indptr_host,
  * the KV axis yields a partial (m, d, o), and a small reduction combines the
  * partials with the merge rule).
  *
- *  q          [batch, num_qo_heads, head_dim], plan's q dtype, device.
+ *  q          [batch, num_qo_heads, head_dim], plan's q dtype, device or
+ *             page-locked host memory (read by the kernels over the CPU-GPU
+ *             link; on a GB300 node this costs the kernel no time, and no
+ *             host-to-device copy is needed), 16-byte aligned.
  *  paged_kv   [num_pages, 2, page_size, num_kv_heads, head_dim], plan's kv
  *             dtype, device, 16-byte aligned.
  *  num_pages  leading extent of paged_kv.  A page id outside [0, num_pages)
@@ -148,8 +155,10 @@ int fa_decode_plan_multi_token(const int32_t* indptr_host,
  *  sm_scale   logit scale; <= 0 selects 1/sqrt(head_dim).
  *  k_scale,   per-tensor dequantisation scales of an E4M3 cache (stored code
  *  v_scale    times scale = value); use 1 for other kv types.
- *  o          [batch, num_qo_heads, head_dim], q dtype, device, caller-allocated.
- *  lse        [batch, num_qo_heads] float32, device, or NULL to skip it.
+ *  o          [batch, num_qo_heads, head_dim], q dtype, device or page-locked
+ *             host memory (written by the kernels directly), caller-allocated.
+ *  lse        [batch, num_qo_heads] float32, device or page-locked host
+ *             memory, or NULL to skip it.
  *
  * No allocation and no host synchronisation: the call only enqueues kernels
  * on cuda_stream, so it can be issued repeatedly between plans.  Results are

@@ -158,6 +158,17 @@ def _host_i32(t) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(t), dtype=np.int32)
 
 
+def _reachable(t: torch.Tensor) -> bool:
+    """Device memory, or page-locked host memory that the kernels read and
+    write directly over the CPU-GPU link (on a GB300 node, NVLink-C2C)."""
+    return t.is_cuda or t.is_pinned()
+
+
+def _cuda_device(t: torch.Tensor) -> torch.device:
+    """The device a tensor lives on, or the current CUDA device for host memory."""
+    return t.device if t.is_cuda else torch.device("cuda", torch.cuda.current_device())
+
+
 def _dtype_code(dt) -> int:
     if dt not in DTYPE_CODES:
         raise ValueError(f"unsupported dtype {dt}")
@@ -257,17 +268,24 @@ class DecodePlan:
         D = self.head_dim
         if q.dtype != self.q_dtype or paged_kv.dtype != self.kv_dtype:
             raise TypeError("q / paged_kv dtype differs from the plan")
-        if tuple(q.shape) != self._q_shape() or not q.is_contiguous() or not q.is_cuda:
-            raise ValueError(f"q must be a contiguous CUDA tensor {list(self._q_shape())}")
+        if tuple(q.shape) != self._q_shape() or not q.is_contiguous() or not _reachable(q):
+            raise ValueError(f"q must be a contiguous CUDA or page-locked tensor "
+                             f"{list(self._q_shape())}")
         if (paged_kv.dim() != 5 or paged_kv.shape[1] != 2 or paged_kv.shape[2] != self.page_size
                 or paged_kv.shape[3] != self.num_kv_heads or paged_kv.shape[4] != D
                 or not paged_kv.is_contiguous() or not paged_kv.is_cuda):
             raise ValueError("paged_kv must be a contiguous CUDA tensor "
                              "[num_pages, 2, page_size, num_kv_heads, head_dim]")
+        pinned = not q.is_cuda  # outputs follow q: device, or page-locked host memory
         if out is None:
-            out = torch.empty(self._q_shape(), dtype=q.dtype, device=q.device)
+            out = torch.empty(self._q_shape(), dtype=q.dtype, device=q.device,
+                              pin_memory=pinned)
         if return_lse and lse is None:
-            lse = torch.empty(self._q_shape()[:-1], dtype=torch.float32, device=q.device)
+            lse = torch.empty(self._q_shape()[:-1], dtype=torch.float32, device=q.device,
+                              pin_memory=pinned)
+        for t in (out, lse):
+            if t is not None and (not _reachable(t) or not t.is_contiguous()):
+                raise ValueError("out / lse must be contiguous CUDA or page-locked tensors")
         return out, lse
 
     def run_token_scales(self, q: torch.Tensor, paged_kv: torch.Tensor, k_scales: torch.Tensor,
@@ -329,11 +347,11 @@ def plan(indptr, indices: torch.Tensor, last_page_len, num_qo_heads: int, num_kv
     B = indptr_h.shape[0] - 1
     if last_h.shape[0] < B:
         raise ValueError("last_page_len shorter than the batch")
-    if indices.dtype != torch.int32 or not indices.is_cuda or not indices.is_contiguous():
-        raise ValueError("indices must be a contiguous int32 CUDA tensor")
+    if indices.dtype != torch.int32 or not _reachable(indices) or not indices.is_contiguous():
+        raise ValueError("indices must be a contiguous int32 CUDA or page-locked tensor")
     if workspace is None:
         workspace = torch.empty(workspace_size(B, num_qo_heads, num_kv_heads, head_dim),
-                                dtype=torch.uint8, device=indices.device)
+                                dtype=torch.uint8, device=_cuda_device(indices))
     handle = ctypes.c_void_p()
     _check(_L().fa_decode_plan(
         indptr_h.ctypes.data, indices.data_ptr() if indices.numel() else None,
@@ -357,11 +375,11 @@ def plan_multi_token(indptr, indices: torch.Tensor, last_page_len, q_len: int, n
     indptr_h = _host_i32(indptr)
     last_h = _host_i32(last_page_len)
     B = indptr_h.shape[0] - 1
-    if indices.dtype != torch.int32 or not indices.is_cuda or not indices.is_contiguous():
-        raise ValueError("indices must be a contiguous int32 CUDA tensor")
+    if indices.dtype != torch.int32 or not _reachable(indices) or not indices.is_contiguous():
+        raise ValueError("indices must be a contiguous int32 CUDA or page-locked tensor")
     if workspace is None:
         workspace = torch.empty(workspace_size(B, num_qo_heads * q_len, num_kv_heads, head_dim),
-                                dtype=torch.uint8, device=indices.device)
+                                dtype=torch.uint8, device=_cuda_device(indices))
     handle = ctypes.c_void_p()
     _check(_L().fa_decode_plan_multi_token(
         indptr_h.ctypes.data, indices.data_ptr() if indices.numel() else None,

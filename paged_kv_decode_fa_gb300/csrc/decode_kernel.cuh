@@ -581,22 +581,66 @@ struct FoldList {
 };
 constexpr int kFoldListBytes = (int)((sizeof(FoldList) + 15) / 16 * 16);
 
+// Fold the units on the fold list now, with `scratch` (free while the CTA is
+// between segments) for the weights; a unit whose weights do not fit stays
+// on the list for fold_pending.  All consumer threads, between consumer
+// barriers.  Folding here, with the producer's copies of the next pages in
+// flight, keeps the folds out of the launch's tail.
+template <typename QT, int D, int G, int NW, int QL = 1>
+__device__ __forceinline__ void fold_listed(const DecodeParams& p, FoldList* folds,
+                                            float* scratch, int scratch_floats) {
+  constexpr int CT = NW * 32;
+  constexpr int NC = G * QL;
+  const int n = folds->n;
+  if (n == 0) return;
+  int kept = 0;
+  for (int i = 0; i < n; ++i) {
+    const int unit = folds->unit[i];
+    const int4 u = reinterpret_cast<const int4*>(p.merge)[unit];
+    if (u.w * NC > scratch_floats) {
+      kept += 1;  // same decision in every thread
+      continue;
+    }
+    fold_split_unit<QT, D, NC, G, QL>(p.part_o, p.part_lse, u, static_cast<QT*>(p.o), p.lse,
+                                      p.num_qo_heads, scratch, scratch_floats, threadIdx.x, CT, 1);
+    dev::named_barrier(1, CT);  // scratch free for the next unit
+  }
+  if (kept) {  // compact the list (thread 0; the others have read it above)
+    dev::named_barrier(1, CT);
+    if (threadIdx.x == 0) {
+      int w = 0;
+      for (int i = 0; i < n; ++i) {
+        const int4 u = reinterpret_cast<const int4*>(p.merge)[folds->unit[i]];
+        if (u.w * NC > scratch_floats) folds->unit[w++] = folds->unit[i];
+      }
+      folds->n = w;
+    }
+  } else if (threadIdx.x == 0) {
+    folds->n = 0;
+  }
+  dev::named_barrier(1, CT);
+}
+
 // Combine the NW consumer warps' states of one segment for all NC columns
 // (unnormalised o in mo[w][h][d] against the warp's max mm[w][h], sum
 // md[w][h], all log2 domain) with the merge rule and write either the final
 // o (q dtype) and lse, or an fp32 partial slot.  Runs on the NW*32 consumer
 // threads after a consumer barrier and ends with one (mo is free again).
 // A split piece is then counted by thread 0 alone while the other warps go
-// on: the piece that completes its unit puts the unit on the CTA's fold list
-// (fold_pending), so no warp waits for the count's round trip.
+// on: the piece that completes its unit puts the unit on the CTA's fold list,
+// folded at the next segment's combine (fold_listed, with `scratch`) or
+// after the CTA's last segment (fold_pending), so no warp waits for the
+// count's round trip.
 template <typename QT, int D, int G, int NW, int QL = 1>
 __device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const float* mo,
                                                  const float* mm, const float* md, int req,
                                                  int kvh, int out_slot, int merge_unit,
-                                                 FoldList* folds) {
+                                                 FoldList* folds, float* scratch,
+                                                 int scratch_floats) {
   constexpr int CT = NW * 32;
   constexpr int NC = G * QL;  // columns: heads of the group x query tokens
   QT* __restrict__ obase = static_cast<QT*>(p.o);
+  fold_listed<QT, D, G, NW, QL>(p, folds, scratch, scratch_floats);
   for (int e = threadIdx.x; e < NC * D; e += CT) {
     const int h = e / D, dd = e % D;
     float M = -INFINITY;
@@ -859,7 +903,8 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
     dev::named_barrier(1, CT);
 
     // Merge the NW warp states of this segment and emit.
-    combine_and_emit<QT, D, G, NW>(p, mo, mm, md, req, kvh, out_slot, sb.z, folds);
+    combine_and_emit<QT, D, G, NW>(p, mo, mm, md, req, kvh, out_slot, sb.z, folds,
+                                   reinterpret_cast<float*>(smem + C::OFF_P), NW * P * G);
     kbase += npg;
   }
   fold_pending<QT, D, G, NW>(p, mo, folds);

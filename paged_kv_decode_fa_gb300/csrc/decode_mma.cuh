@@ -558,7 +558,10 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
       }
     }
     dev::named_barrier(1, CT);
-    combine_and_emit<QT, D, G, NW, QL>(p, mo, mm, md, req, kvh, out_slot, sb.z, folds);
+    // the P^T buffers (NW x 256 bytes) are free between segments
+    combine_and_emit<QT, D, G, NW, QL>(p, mo, mm, md, req, kvh, out_slot, sb.z, folds,
+                                       reinterpret_cast<float*>(smem + C::OFF_PT),
+                                       NW * 8 * P / 2);
     kbase += npg;
   }
   fold_pending<QT, D, G, NW, QL>(p, mo, folds);

@@ -200,6 +200,61 @@ def test_run_time_pool(lib, cuda, monkeypatch, case):
             rel=TOKEN_SCALE_REL if path == "token_scales" else 0.0)
 
 
+def test_page_locked_host_buffers(lib, cuda):
+    """q, the page ids, o and lse in page-locked host memory, read and written
+    by the kernels directly: bitwise the same as with device buffers."""
+    b = W.make_batch(batch_lengths=[3000, 17, 0, 900, 16, 5000], num_qo_heads=16,
+                     num_kv_heads=4, head_dim=128, q_dtype=torch.bfloat16,
+                     kv_dtype=torch.bfloat16, seed=141, device=cuda)
+    p = lib.plan(b.indptr, b.indices, b.last_page_len, 16, 4, 128, 16,
+                 q_data_type=torch.bfloat16, kv_data_type=torch.bfloat16)
+    o_d, lse_d = p.run(b.q, b.paged_kv)
+    idx_h = b.indices.cpu().pin_memory()
+    ph = lib.plan(b.indptr, idx_h, b.last_page_len, 16, 4, 128, 16,
+                  q_data_type=torch.bfloat16, kv_data_type=torch.bfloat16)
+    q_h = b.q.cpu().pin_memory()
+    o_h, lse_h = ph.run(q_h, b.paged_kv)
+    torch.cuda.synchronize()
+    assert o_h.is_pinned() and lse_h.is_pinned()
+    assert ph.check() == 0
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
+    with pytest.raises(ValueError):       # pageable host memory is refused
+        ph.run(b.q.cpu(), b.paged_kv)
+
+
+def test_cuda_graph_capture(lib, cuda):
+    """fa_decode_run only enqueues kernels (no allocation, no host sync), so a
+    run can be captured into a CUDA graph and replayed; every replay equals
+    the eager run bit for bit (split units re-arm their counters inside the
+    kernel, so replays need no reset)."""
+    b = W.make_batch(batch_lengths=[3000, 17, 0, 900, 16, 5000], num_qo_heads=16,
+                     num_kv_heads=4, head_dim=128, q_dtype=torch.bfloat16,
+                     kv_dtype=torch.bfloat16, seed=131, device=cuda)
+    p = lib.plan(b.indptr, b.indices, b.last_page_len, 16, 4, 128, 16,
+                 q_data_type=torch.bfloat16, kv_data_type=torch.bfloat16)
+    assert p.info["num_merge_units"] > 0
+    o = torch.empty_like(b.q)
+    lse = torch.empty((b.batch, 16), dtype=torch.float32, device=cuda)
+    p.run(b.q, b.paged_kv, out=o, lse=lse)
+    torch.cuda.synchronize()
+    ref_o, ref_lse = o.clone(), lse.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        p.run(b.q, b.paged_kv, out=o, lse=lse)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        p.run(b.q, b.paged_kv, out=o, lse=lse)
+    for _ in range(3):
+        o.zero_()
+        lse.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+    assert p.check() == 0
+
+
 @pytest.mark.parametrize("merge", ["fused", "kernel"])
 def test_deterministic_and_no_lse(lib, cuda, monkeypatch, merge):
     if merge == "kernel":
