@@ -177,6 +177,12 @@ def max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
+def whole_job_rate(world: int, units_per_rank_step: int, steps: int, elapsed_s: float) -> float:
+    """Units per second of the whole job: every rank processes the same units
+    per step (weak scaling), elapsed_s is the slowest rank's time."""
+    return world * units_per_rank_step * steps / elapsed_s
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -343,7 +349,7 @@ def bench_cascade(args, world, rank, local, b, cfg, dev):
     peak, peak_kind = read_peaks()
     step_s = elapsed_s / args.steps
     return {
-        "metric": METRIC, "value": world * b.batch * args.steps / elapsed_s, "unit": "tokens/s",
+        "metric": METRIC, "value": whole_job_rate(world, b.batch, args.steps, elapsed_s), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": DTYPE_NAMES[cfg.kv_dtype], "data": "synthetic",
@@ -356,7 +362,7 @@ def bench_cascade(args, world, rank, local, b, cfg, dev):
                      "frac": alg / step_s / 1e9 / peak, "traffic": None,
                      "kernel": "cascade step (suffix decode + fa_prefix_kernel + combine)",
                      "algorithmic_bytes_per_launch": alg},
-        "e2e": {"value": world * b.batch * e2e_steps / e2e_s, "unit": "tokens/s",
+        "e2e": {"value": whole_job_rate(world, b.batch, e2e_steps, e2e_s), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(q_h.numel() * q_h.element_size()),
                 "d2h_bytes_per_step": int(o_h.numel() * o_h.element_size() + lse_h.numel() * 4),
                 "steps": e2e_steps, "includes": "H2D q, cascade plan, run, D2H o + lse"},
@@ -504,7 +510,7 @@ def bench_ours(args, world, rank, local):
     alg = algorithmic_bytes(b)
     peak, peak_kind = read_peaks()
     step_s = elapsed_s / args.steps
-    value = world * b.batch * b.q_len * args.steps / elapsed_s
+    value = whole_job_rate(world, b.batch * b.q_len, args.steps, elapsed_s)
     achieved = alg / kern_avg_s / 1e9
     traffic = profiled_traffic(args.workload)
     out = {
@@ -529,13 +535,13 @@ def bench_ours(args, world, rank, local):
                      "kernel": ("fa_decode_mma_kernel" if info["tensor_cores"]
                                 else "fa_decode_split_kernel"),
                      "algorithmic_bytes_per_launch": alg},
-        "e2e": {"value": world * b.batch * b.q_len * e2e_steps / e2e_s, "unit": "tokens/s",
+        "e2e": {"value": whole_job_rate(world, b.batch * b.q_len, e2e_steps, e2e_s), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "steps": e2e_steps,
                 "includes": "plan (work-list upload) and run every step; q and page ids read, "
                             "o and lse written by the kernels in page-locked host memory",
                 "staged_copies": {
-                    "value": world * b.batch * b.q_len * e2e_steps / staged_s,
+                    "value": whole_job_rate(world, b.batch * b.q_len, e2e_steps, staged_s),
                     "includes": "pinned H2D q + page ids, plan, run, D2H o + lse on one stream"}},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(t0, t1),
