@@ -323,7 +323,7 @@ int fa_decode_set_timing_events(fa_decode_plan_t plan, void* ev_before,
 
 /* Decode one batch without allocating any device memory.
  *
- * The paper has no counterpart to this call; it exists for callers that
+ * The pages describe no counterpart to this call; it exists for callers that
  * cannot allocate: code handed only input and output pointers by a host
  * framework that owns every device buffer through its own pool, allocator or
  * out-of-memory callbacks, and latency-critical loops where cudaMalloc (which
