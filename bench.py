@@ -376,7 +376,7 @@ def bench_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     cfg = W.CONFIGS[args.workload]
-    b = W.make_config_batch(args.workload, device=dev)
+    b = W.make_config_batch(args.workload, device=dev, max_requests=args.max_requests)
     if "prefix_pages" in b.extra:
         return bench_cascade(args, world, rank, local, b, cfg, dev)
     stream = torch.cuda.current_stream(dev)
@@ -512,7 +512,7 @@ def bench_ours(args, world, rank, local):
     step_s = elapsed_s / args.steps
     value = whole_job_rate(world, b.batch * b.q_len, args.steps, elapsed_s)
     achieved = alg / kern_avg_s / 1e9
-    traffic = profiled_traffic(args.workload)
+    traffic = profiled_traffic(args.workload) if args.max_requests is None else None
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
@@ -565,6 +565,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--max-requests", type=int, default=None,
+                    help="keep only the first N requests of the workload (profiler captures "
+                         "that must fit a few GB; not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -54,6 +54,11 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
                : "memory");
 }
 
+// Fetch a TMA descriptor into the descriptor cache ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -333,6 +338,8 @@ __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const Deco
                                               float* scales = nullptr, SegQueue* queue = nullptr,
                                               int align = 1) {
   bool aborted = false;
+  // the descriptor loads while the first segment and its page ids are read
+  if (lane == 0) dev::prefetch_tensormap(map);
   const uint64_t policy = dev::evict_first_policy();
   int k = 0, claimed = 0;
   // lane 0 claims one pool segment ahead - the first while it issues the

@@ -251,8 +251,10 @@ def cascade_parts(b: DecodeBatch):
             torch.from_numpy(own_ids.astype(np.int32)).to(dev), b.last_page_len.clone())
 
 
-def make_config_batch(name: str, device="cuda") -> DecodeBatch:
-    """The named configuration, drawn from its seed."""
+def make_config_batch(name: str, device="cuda", max_requests: int | None = None) -> DecodeBatch:
+    """The named configuration, drawn from its seed.  max_requests keeps only
+    the first requests of its length draw (a smaller batch of the same length
+    distribution, e.g. for a profiler capture that must fit a few GB)."""
     cfg = CONFIGS[name]
     if name == "cascade":
         gen = torch.Generator().manual_seed(cfg.seed)
@@ -263,6 +265,8 @@ def make_config_batch(name: str, device="cuda") -> DecodeBatch:
                                   device=device)
     gen = torch.Generator().manual_seed(cfg.seed)
     lengths = draw_lengths(cfg, gen)
+    if max_requests is not None:
+        lengths = lengths[:max_requests]
     pool = 64 if name == "tiny" else None
     return _fill(lengths, gen, cfg.num_qo_heads, cfg.num_kv_heads, cfg.head_dim, cfg.q_dtype,
                  cfg.kv_dtype, cfg.seed, device, cfg.page_size, pool, True, name,
