@@ -1,7 +1,8 @@
 // Split-KV paged decode attention for sm_103a.
 //
 // One persistent CTA per planner chunk list (see planner.cpp).  Inside a CTA:
-//  - warp NW (the producer) walks the CTA's segments page by page, reads each
+//  - warp NW (the producer) walks the CTA's segments (then, with a run-time
+//    pool, the pool segments it claims) page by page, reads each
 //    page id from the index table and issues one 4-D TMA tensor copy per page
 //    that brings the page's K and V rows of one kv head ([2][16][D]) into a
 //    ring of S shared-memory stages, signalled through mbarriers;
@@ -16,8 +17,9 @@
 //    them into its running softmax state with the online-softmax recurrence,
 //    and accumulates P.V from one read of each V row;
 //  - at the end of a segment the NW warp states are combined with the merge
-//    rule and written either as the final o/lse or as an fp32 partial state
-//    that the merge kernel combines later.
+//    rule and written either as the final o/lse or as an fp32 partial state;
+//    the CTA that completes a split unit folds its partial states (or, on
+//    request, a separate merge kernel does).
 // The online-softmax update, the warp combine and the split merge are all the
 // same recurrence applied at three levels, as section "FlashDecoding - the
 // split-KV trick" of the page "FlashDecoding + FlashInfer - the decode-time

@@ -21,7 +21,9 @@
 //    q's B fragment (held in registers for the whole segment) uses the same
 //    permutation; E4M3 K is widened to f16 in registers;
 //  - softmax on the C fragment (tokens g, g+8 x heads 2t, 2t+1): column max
-//    and sum over the 8 lanes of a column with three shuffles each;
+//    over the 8 lanes of a column with three shuffles per page (none with the
+//    unified max, which only votes); each lane keeps its own share of the
+//    denominator, summed over the column once per segment;
 //  - P.V: P is rounded to the MMA type, transposed through a 256-byte
 //    per-warp buffer into B fragments, V^T fragments come straight from the
 //    stage with ldmatrix.trans (for E4M3, pairs of bytes are transposed as
