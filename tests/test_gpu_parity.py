@@ -640,3 +640,28 @@ def test_full_size_workloads_sampled(lib, cuda, name):
     assert torch.isfinite(o.float()).all()
     del b, o, lse
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ randomised sweep
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_batches_against_oracle(lib, cuda, seed):
+    """Random shapes, dtypes and length mixes (empty requests, one-token
+    requests, partial last pages, requests long enough to be split),
+    element by element against the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    q_dt, kv_dt = COMBOS[seed % len(COMBOS)]
+    D = int(rng.choice([64, 128]))
+    G = int(rng.choice([1, 2, 4, 8]))
+    Hkv = int(rng.choice([1, 2, 4]))
+    B = int(rng.integers(1, 24))
+    lengths = rng.integers(1, 2500, size=B)
+    lengths[rng.random(B) < 0.15] = 0
+    lengths[rng.random(B) < 0.1] = 1
+    b = W.make_batch(batch_lengths=lengths.tolist(), num_qo_heads=Hkv * G, num_kv_heads=Hkv,
+                     head_dim=D, q_dtype=q_dt, kv_dtype=kv_dt, seed=2000 + seed, device=cuda)
+    p, o, lse = run_lib(lib, b)
+    check_coverage(p, b)
+    assert p.check() == 0
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, tol_for(b))
