@@ -607,6 +607,7 @@ static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
 
   if (!(sm_scale > 0.f)) sm_scale = 1.0f / std::sqrt((float)D);
   DecodeParams prm;
+  std::memset(&prm, 0, sizeof prm);
   prm.q = q;
   prm.o = o;
   prm.lse = lse;
@@ -625,6 +626,7 @@ static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
   prm.num_qo_heads = plan->hq;
   prm.num_kv_heads = plan->hkv;
   prm.q_len = plan->q_len;
+  prm.q_row_bytes = D * dtype_size(plan->q_dtype);
   prm.q_scale = sm_scale * k_scale * kLog2e;
   prm.v_scale = v_scale;
   prm.max_bound = max_bound * kLog2e;

@@ -56,6 +56,10 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
                : "memory");
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* addr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+}
+
 // Fetch a TMA descriptor into the descriptor cache ahead of its first use.
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -386,6 +390,18 @@ __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const Deco
     }
     const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * si);
     const int kvh = sa.y, pb = sa.z, pe = sa.w;
+    // The consumers read this segment's q rows when they reach it, several
+    // pages from now: bring them into L2 while the pages are in flight.
+    if (p.q_row_bytes > 0) {
+      const int G = p.num_qo_heads / p.num_kv_heads;
+      const int lines = (G * p.q_row_bytes + 127) / 128;  // one query token's rows
+      for (int i = 0; i < p.q_len; ++i) {
+        const char* rows = static_cast<const char*>(p.q) +
+                           (((size_t)sa.x * p.q_len + i) * p.num_qo_heads + (size_t)kvh * G) *
+                               p.q_row_bytes;
+        for (int l = lane; l < lines; l += 32) dev::prefetch_l2(rows + (size_t)l * 128);
+      }
+    }
     for (int p0 = pb; p0 < pe; p0 += 32) {
       const int cnt = min(32, pe - p0);
       int id = lane < cnt ? __ldg(p.indices + p0 + lane) : 0;

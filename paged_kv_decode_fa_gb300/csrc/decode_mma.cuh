@@ -143,6 +143,8 @@ struct MmaCfg {
   static constexpr int SPW = SPW0 < 1 ? 1 : (SPW0 > 4 ? 4 : SPW0);
   static constexpr int S = SPW * NW;
   static constexpr int THREADS = (NW + 1) * 32;
+  // CTAs per SM the ring size is chosen for; the register budget must allow it
+  static constexpr int MIN_CTAS = KV_ES == 1 ? 4 : 3;
   static constexpr int OFF_FULL = S * STAGE_BYTES;
   static constexpr int OFF_EMPTY = OFF_FULL + 8 * S;
   static constexpr int OFF_PT = OFF_EMPTY + 8 * S;          // [NW][8 heads][16 tokens] 16-bit
@@ -171,7 +173,8 @@ constexpr float kUmAbove = 16.f;
 constexpr float kUmBelow = 64.f;
 
 template <typename QT, typename KVT, int D, int G, int NW, bool TS, int QL, bool UM>
-__global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS)
+__global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
+                                  MmaCfg<QT, KVT, D, G, NW, TS, QL>::MIN_CTAS)
     fa_decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
   using C = MmaCfg<QT, KVT, D, G, NW, TS, QL>;
   constexpr int NC = C::NC;

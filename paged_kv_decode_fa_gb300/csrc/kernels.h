@@ -30,6 +30,7 @@ struct DecodeParams {
   int num_qo_heads;
   int num_kv_heads;
   int q_len;                   // query tokens per request (1 for plain decode)
+  int q_row_bytes;             // head_dim * q element size (0: no q prefetch)
   float q_scale;  // sm_scale * k_scale * log2(e), folded into q
   float v_scale;
   float max_bound;    // unified-max kernels: static reference of the logits, log2 units
