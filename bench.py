@@ -69,13 +69,36 @@ def algorithmic_bytes(b: W.DecodeBatch) -> int:
     return int(kv + idx + qo + lse)
 
 
-def kernel_source_hash() -> str:
+def read_bf16_peak():
+    """Dense bf16 tensor TFLOP/s of this GPU: the measured burst figure (the
+    prefix kernel is timed alone, within a short step), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            v = json.load(f).get("bf16_tflops")
+        if v:
+            return float(v), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except (OSError, ValueError):
+        pass
+    return 1900.0, "fallback (1.9 PFLOP/s bf16 burst, one earlier GB300 measurement)"
+
+
+# Sources that are not part of the decode kernels or their launch: the
+# cascade's own kernels, the no-allocation entry point, fa_merge_states.
+NOT_DECODE_SOURCES = ("cascade.cu", "static_scratch.cu", "merge.cu")
+
+
+def kernel_source_hash(workload: str = "gqa_uniform") -> str:
+    """Hash of the sources a workload's kernels are built and launched from
+    (a profile summary is current while this hash matches)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_fa_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + f.read())
+        if not fn.endswith((".cu", ".cuh", ".h", ".cpp")):
+            continue
+        if workload != "cascade" and fn in NOT_DECODE_SOURCES:
+            continue
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -88,7 +111,7 @@ def profiled_traffic(workload: str):
     text = open(path).read()
     m_t = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
     m_h = re.search(r"^kernel_source_hash:\s*([0-9a-f]+)", text, re.M)
-    if not m_t or not m_h or m_h.group(1) != kernel_source_hash():
+    if not m_t or not m_h or m_h.group(1) != kernel_source_hash(workload):
         return None
     return float(m_t.group(1))
 
@@ -309,12 +332,30 @@ def bench_cascade(args, world, rank, local, b, cfg, dev):
         torch.cuda.synchronize(dev)
         return max_over_ranks(a.elapsed_time(z) / 1e3, world, dev)
 
+    # events around the prefix kernel of every timed step (recorded once by
+    # torch first so that they exist)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, z in evs:
+        a.record(stream)
+        z.record(stream)
+    step_no = [0]
+
+    def cascade_step():
+        i = step_no[0]
+        step_no[0] += 1
+        if i >= args.warmup:
+            p.set_timing_events(*evs[i - args.warmup])
+        p.run(b.q, b.paged_kv, out=o, lse=lse)
+
     clocks = ClockSampler(local).start()
     time.sleep(0.3)
     t0 = time.perf_counter()
-    elapsed_s = timed(lambda: p.run(b.q, b.paged_kv, out=o, lse=lse), args.steps)
+    elapsed_s = timed(cascade_step, args.steps)
     t1 = time.perf_counter()
     clocks.stop()
+    p.set_timing_events(None, None)
+    prefix_s = statistics.mean(a.elapsed_time(z) for a, z in evs) / 1e3
     if p.check() != 0:
         raise RuntimeError("device check flagged the cascade batch")
     plain_s = timed(lambda: plain.run(b.q, b.paged_kv, out=o, lse=lse), args.steps)
@@ -348,6 +389,12 @@ def bench_cascade(args, world, rank, local, b, cfg, dev):
     alg = cascade_bytes(b)
     peak, peak_kind = read_peaks()
     step_s = elapsed_s / args.steps
+    # the prefix kernel is a dense contraction: QK^T and P.V over the shared
+    # tokens for every query head of the batch, 2 flops per multiply-add
+    prefix_tokens = b.extra["prefix_pages"] * b.page_size
+    prefix_flops = 2 * 2 * b.batch * b.num_qo_heads * prefix_tokens * b.head_dim
+    prefix_bytes = prefix_tokens * b.num_kv_heads * 2 * b.head_dim * b.paged_kv.element_size()
+    tflops_peak, tflops_kind = read_bf16_peak()
     return {
         "metric": METRIC, "value": whole_job_rate(world, b.batch, args.steps, elapsed_s), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -358,10 +405,14 @@ def bench_cascade(args, world, rank, local, b, cfg, dev):
         "peak_kind": peak_kind, "plan_ms": plan_ms,
         "plain_decode_ms_per_step": plain_s / args.steps * 1e3,
         "speedup_vs_plain_decode": plain_s / elapsed_s,
-        "roofline": {"bound": "hbm", "achieved": alg / step_s / 1e9, "peak": peak, "unit": "GB/s",
-                     "frac": alg / step_s / 1e9 / peak, "traffic": None,
-                     "kernel": "cascade step (suffix decode + fa_prefix_kernel + combine)",
-                     "algorithmic_bytes_per_launch": alg},
+        "roofline": {"bound": "tensor", "achieved": prefix_flops / prefix_s / 1e12,
+                     "peak": tflops_peak, "unit": "TFLOP/s",
+                     "frac": prefix_flops / prefix_s / 1e12 / tflops_peak,
+                     "traffic": profiled_traffic("cascade"),
+                     "kernel": "fa_prefix_kernel (mma.sync bf16)", "peak_kind": tflops_kind,
+                     "flops_per_launch": prefix_flops,
+                     "prefix_kernel_us": prefix_s * 1e6,
+                     "prefix_hbm_gbs": prefix_bytes / prefix_s / 1e9},
         "e2e": {"value": whole_job_rate(world, b.batch, e2e_steps, e2e_s), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(q_h.numel() * q_h.element_size()),
                 "d2h_bytes_per_step": int(o_h.numel() * o_h.element_size() + lse_h.numel() * 4),

@@ -406,6 +406,11 @@ int fa_cascade_plan_destroy(fa_cascade_plan_t plan);
 /* As fa_decode_check, for both passes of a cascade plan. */
 int fa_cascade_check(fa_cascade_plan_t plan, void* cuda_stream, int* flags);
 
+/* As fa_decode_set_timing_events, around the prefix kernel of later
+ * fa_cascade_run calls (the events are recorded on their stream). */
+int fa_cascade_set_timing_events(fa_cascade_plan_t plan, void* ev_before,
+                                 void* ev_after);
+
 #ifdef __cplusplus
 }
 #endif

@@ -38,6 +38,7 @@ EXPORTED_SYMBOLS = (
     "fa_decode_run_token_scales", "fa_decode_plan_multi_token",
     "fa_cascade_workspace_size", "fa_cascade_plan", "fa_cascade_run", "fa_cascade_plan_destroy",
     "fa_cascade_check", "fa_decode_run_unified_max", "fa_decode_unified_max_fallbacks",
+    "fa_cascade_set_timing_events",
 )
 
 FA_OK = 0
@@ -117,6 +118,8 @@ def _load() -> ctypes.CDLL:
     lib.fa_decode_check.restype = i32
     lib.fa_decode_set_timing_events.argtypes = [P, P, P]
     lib.fa_decode_set_timing_events.restype = i32
+    lib.fa_cascade_set_timing_events.argtypes = [P, P, P]
+    lib.fa_cascade_set_timing_events.restype = i32
     return lib
 
 
@@ -328,12 +331,19 @@ class DecodePlan:
 
         torch creates an event lazily at its first record, so record each
         event once from torch before handing it over."""
-        for ev in (before, after):
-            if ev is not None and not ev.cuda_event:
-                raise ValueError("record the torch.cuda.Event once before passing it")
-        b = ctypes.c_void_p(before.cuda_event) if before is not None else None
-        a = ctypes.c_void_p(after.cuda_event) if after is not None else None
-        _check(_L().fa_decode_set_timing_events(self._h, b, a), "fa_decode_set_timing_events")
+        _check(_L().fa_decode_set_timing_events(self._h, *_event_handles(before, after)),
+               "fa_decode_set_timing_events")
+
+
+def _event_handles(before, after):
+    """CUDA event handles of two recorded torch.cuda.Events (None = off).
+    torch creates an event lazily at its first record, so record each event
+    once from torch before handing it over."""
+    for ev in (before, after):
+        if ev is not None and not ev.cuda_event:
+            raise ValueError("record the torch.cuda.Event once before passing it")
+    return (ctypes.c_void_p(before.cuda_event) if before is not None else None,
+            ctypes.c_void_p(after.cuda_event) if after is not None else None)
 
 
 def plan(indptr, indices: torch.Tensor, last_page_len, num_qo_heads: int, num_kv_heads: int,
@@ -472,6 +482,11 @@ class CascadePlan:
                                    lse.data_ptr() if lse is not None else None,
                                    _stream_handle(stream)), "fa_cascade_run")
         return out, lse
+
+    def set_timing_events(self, before, after) -> None:
+        """Record torch.cuda.Events around the prefix kernel of later runs (None = off)."""
+        _check(_L().fa_cascade_set_timing_events(self._h, *_event_handles(before, after)),
+               "fa_cascade_set_timing_events")
 
     def check(self, stream=None) -> int:
         flags = ctypes.c_int(0)

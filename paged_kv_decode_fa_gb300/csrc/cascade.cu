@@ -406,6 +406,7 @@ struct fa_cascade_plan_s {
   CUtensorMap map;
   const void* map_base = nullptr;
   int64_t map_pages = -1;
+  cudaEvent_t ev_before = nullptr, ev_after = nullptr;  // around the prefix kernel
 };
 
 extern "C" {
@@ -567,9 +568,12 @@ int fa_cascade_run(fa_cascade_plan_t plan, const void* q, const void* paged_kv,
   pp.group = plan->group;
   pp.q_scale = sm_scale * 1.4426950408889634f;
   void* args[3] = {&plan->map, &prm, &pp};
+  const bool timed = plan->ev_before && plan->ev_after;
+  if (timed && cudaEventRecord(plan->ev_before, st) != cudaSuccess) return FA_ERR_CUDA;
   if (cudaLaunchKernel(plan->k.prefix, dim3(plan->items), dim3(plan->k.threads), args,
                        (size_t)plan->k.smem, st) != cudaSuccess)
     return FA_ERR_CUDA;
+  if (timed && cudaEventRecord(plan->ev_after, st) != cudaSuccess) return FA_ERR_CUDA;
   // 3. fold prefix chunks and suffix
   fadecode::CombineParams c;
   c.part_o = pp.part_o;
@@ -596,6 +600,13 @@ int fa_cascade_plan_destroy(fa_cascade_plan_t plan) {
     fa_decode_plan_destroy(plan->suffix);
     delete plan;
   }
+  return FA_OK;
+}
+
+int fa_cascade_set_timing_events(fa_cascade_plan_t plan, void* ev_before, void* ev_after) {
+  if (!plan) return FA_ERR_INVALID_ARG;
+  plan->ev_before = static_cast<cudaEvent_t>(ev_before);
+  plan->ev_after = static_cast<cudaEvent_t>(ev_after);
   return FA_OK;
 }
 
