@@ -28,6 +28,7 @@
 #include <algorithm>
 #include <climits>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -275,6 +276,12 @@ __global__ void __launch_bounds__(PrefixCfg<QT, D, NW>::THREADS)
   }
 }
 
+}  // namespace fadecode
+
+#include "cascade_tc.cuh"
+
+namespace fadecode {
+
 // One warp per (request, qo head): fold the prefix chunks' states and the
 // suffix state with the merge rule.
 template <typename QT, int D>
@@ -331,21 +338,39 @@ struct CascadeKernels {
   const void* prefix = nullptr;
   const void* combine = nullptr;
   int threads = 0, smem = 0;
+  bool tcgen05 = false;  // prefix on the tcgen05 tensor cores (K and V boxes apart)
 };
+
+// FADECODE_CASCADE=mma keeps the prefix pass on the warp-level mma.sync
+// kernel (for comparisons); by default it runs on tcgen05.
+bool cascade_tcgen05() {
+  const char* v = std::getenv("FADECODE_CASCADE");
+  return !(v && std::strcmp(v, "mma") == 0);
+}
 
 template <typename QT>
 CascadeKernels cascade_kernels() {
-  using C = fadecode::PrefixCfg<QT, 128, 8>;
   CascadeKernels k;
-  k.prefix = reinterpret_cast<const void*>(&fadecode::fa_prefix_kernel<QT, 128, 8>);
   k.combine = reinterpret_cast<const void*>(&fadecode::fa_cascade_combine_kernel<QT, 128>);
+  if (cascade_tcgen05()) {
+    k.prefix = reinterpret_cast<const void*>(&fadecode::fa_prefix_tc_kernel<QT>);
+    k.threads = fadecode::tc::kThreads;
+    k.smem = fadecode::tc::kSmem + 1024;
+    k.tcgen05 = true;
+    return k;
+  }
+  using C = fadecode::PrefixCfg<QT, 128, 8>;
+  k.prefix = reinterpret_cast<const void*>(&fadecode::fa_prefix_kernel<QT, 128, 8>);
   k.threads = C::THREADS;
   k.smem = C::SMEM + 1024;
   return k;
 }
 
+// kv_rows = 2: one box brings a page's K and V rows together (mma.sync
+// kernel); 1: K and V in separate boxes (tcgen05 kernel, whose operands are
+// [tokens][dims] blocks of K or of V).
 int encode_prefix_map(CUtensorMap* map, fa_dtype dt, const void* paged_kv, int64_t num_pages,
-                      int D, int Hkv, int P) {
+                      int D, int Hkv, int P, int kv_rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
     void* f = nullptr;
@@ -361,7 +386,7 @@ int encode_prefix_map(CUtensorMap* map, fa_dtype dt, const void* paged_kv, int64
                         (cuuint64_t)(2 * num_pages)};
   cuuint64_t strides[3] = {(cuuint64_t)(D * es), (cuuint64_t)(Hkv * D * es),
                            (cuuint64_t)(P * Hkv * D * es)};
-  cuuint32_t box[4] = {64u, 1u, (cuuint32_t)P, 2u};
+  cuuint32_t box[4] = {64u, 1u, (cuuint32_t)P, (cuuint32_t)kv_rows};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   const CUresult r = fn(map,
                         dt == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -545,7 +570,7 @@ int fa_cascade_run(fa_cascade_plan_t plan, const void* q, const void* paged_kv,
   // 2. the shared prefix, once per kv head and row block
   if (paged_kv != plan->map_base || num_pages != plan->map_pages) {
     rc = encode_prefix_map(&plan->map, plan->dtype, paged_kv, num_pages, D, plan->hkv,
-                           fadecode::kPageSize);
+                           fadecode::kPageSize, plan->k.tcgen05 ? 1 : 2);
     if (rc != FA_OK) return rc;
     plan->map_base = paged_kv;
     plan->map_pages = num_pages;

@@ -420,15 +420,22 @@ def run_cascade(lib, b):
     return p, o, lse
 
 
+@pytest.mark.parametrize("kernel", ["tcgen05", "mma"])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
 @pytest.mark.parametrize("batch,hq,hkv,prefix_pages", [
-    (6, 8, 2, 5),       # 24 rows: one partial row block
+    (6, 8, 2, 5),       # 24 rows: one partial row block, a partial last tile
     (40, 16, 4, 9),     # 160 rows per kv head: two row blocks
     (3, 16, 2, 1),      # group 8, a one-page prefix
+    (20, 32, 4, 70),    # many tiles per chunk: TMEM score buffers and ring reused
 ])
-def test_cascade_small(lib, cuda, dtype, batch, hq, hkv, prefix_pages):
+def test_cascade_small(lib, cuda, monkeypatch, kernel, dtype, batch, hq, hkv, prefix_pages):
     """Cascade output equals attention over each request's full page list
-    (shared prefix pages, then its own), checked against the oracle."""
+    (shared prefix pages, then its own), checked against the oracle, with the
+    prefix pass on tcgen05 (default) and on mma.sync."""
+    if kernel == "mma":
+        monkeypatch.setenv("FADECODE_CASCADE", "mma")
+    else:
+        monkeypatch.delenv("FADECODE_CASCADE", raising=False)
     rng = np.random.default_rng(batch + prefix_pages)
     sfx = rng.integers(0, 200, size=batch)
     sfx[0] = 0          # a request with no pages of its own
