@@ -8,7 +8,7 @@
 // block, prefix chunk) item, 64 tokens (4 pages) at a time:
 //
 //  - warp 4 (TMA): per tile, 16 tensor copies of 2 KB (4 pages x {K, V} x two
-//    64-dim halves) into a 3-stage ring, each half-block a [64 tokens][64
+//    64-dim halves) into a 4-stage ring, each half-block a [64 tokens][64
 //    dims] 128-byte-swizzled matrix.  Pages past the chunk are fetched from
 //    an out-of-range page index, so the copy fills them with zeros;
 //  - warp 5 (MMA, one lane): S[b] = Q K^T (M 128, N 64, K 128: 8 MMAs, Q and
@@ -36,7 +36,7 @@ namespace tc {
 constexpr int kD = 128;
 constexpr int kTok = 64;                   // tokens per tile
 constexpr int kPages = kTok / kPageSize;   // 4
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kBlock = kTok * 128;         // [64 rows][128 bytes]
 constexpr int kStageBytes = 4 * kBlock;    // K lo, K hi, V lo, V hi
 constexpr int kQBytes = 2 * kPrefixRows * 128;
@@ -45,7 +45,7 @@ constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kQBytes;
 constexpr int kOffP = kOffKV + kStages * kStageBytes;
 constexpr int kOffBar = kOffP + 2 * kPBytes;
-// kv_full[3], kv_empty[3], s_full[2], s_free[2], p_full[2], p_free[2], o_done, q_ready
+// kv_full[4], kv_empty[4], s_full[2], s_free[2], p_full[2], p_free[2], o_done, q_ready
 constexpr int kNumBars = 2 * kStages + 10;
 constexpr int kOffTmem = kOffBar + 8 * kNumBars;
 constexpr int kSmem = kOffTmem + 16;
@@ -53,6 +53,7 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 256;
 constexpr float kRescaleAbove = 8.f;       // log2 units
 
+static_assert(32 % kPages == 0, "a warp's page-id load covers whole tiles");
 static_assert(kOffKV % 1024 == 0 && kStageBytes % 1024 == 0 && kOffP % 1024 == 0,
               "swizzled operands need 1024-byte alignment");
 
@@ -190,11 +191,33 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 
   if (warp == 4) {
     // ---------------------------------------------------------------- TMA
-    if (lane == 0) {
-      dev::prefetch_tensormap(&kv_map);
-      const uint64_t policy = dev::evict_first_policy();
-      const int oob = (int)(2 * p.num_pages);  // beyond the last page: zero fill
-      for (int j = 0; j < tiles; ++j) {
+    // The warp reads the page ids 32 at a time (eight tiles' worth, one per
+    // lane); lane 0 waits for ring stages and issues the copies.
+    if (lane == 0) dev::prefetch_tensormap(&kv_map);
+    const uint64_t policy = dev::evict_first_policy();
+    const int oob = (int)(2 * p.num_pages);  // beyond the last page: zero fill
+    int ids = 0;
+    for (int j = 0; j < tiles; ++j) {
+      const int first = j * kPages;  // page position within the chunk
+      if (first % 32 == 0) {
+        const int pos = first + lane;
+        int id = -1;
+        if (pos < npg) {
+          id = __ldg(p.indices + pb + pos);
+          if (id < 0 || (int64_t)id >= p.num_pages) {
+            atomicOr(p.err, 1);
+            id = -1;
+          }
+        }
+        ids = id;
+      }
+      int c3[kPages];
+#pragma unroll
+      for (int i = 0; i < kPages; ++i) {
+        const int id = __shfl_sync(0xffffffffu, ids, (first + i) % 32);
+        c3[i] = id < 0 ? oob : 2 * id;
+      }
+      if (lane == 0) {
         const int s = j % kStages;
         dev::mbar_wait(dev::smem_addr(&kv_empty[s]), (uint32_t)(((j / kStages) & 1) ^ 1),
                        aborted, p.err);
@@ -203,27 +226,21 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         const uint32_t st = sbase + kOffKV + s * kStageBytes;
 #pragma unroll
         for (int i = 0; i < kPages; ++i) {
-          int c3 = oob;
-          if (j * kPages + i < npg) {
-            const int id = __ldg(p.indices + pb + j * kPages + i);
-            if (id < 0 || (int64_t)id >= p.num_pages)
-              atomicOr(p.err, 1);
-            else
-              c3 = 2 * id;
-          }
           const uint32_t row = (uint32_t)i * (kPageSize * 128);
-          dev::tma_load_4d(st + 0 * kBlock + row, &kv_map, 0, kvh, 0, c3, fb, policy);
-          dev::tma_load_4d(st + 1 * kBlock + row, &kv_map, 64, kvh, 0, c3, fb, policy);
-          dev::tma_load_4d(st + 2 * kBlock + row, &kv_map, 0, kvh, 0, c3 + 1, fb, policy);
-          dev::tma_load_4d(st + 3 * kBlock + row, &kv_map, 64, kvh, 0, c3 + 1, fb, policy);
+          dev::tma_load_4d(st + 0 * kBlock + row, &kv_map, 0, kvh, 0, c3[i], fb, policy);
+          dev::tma_load_4d(st + 1 * kBlock + row, &kv_map, 64, kvh, 0, c3[i], fb, policy);
+          dev::tma_load_4d(st + 2 * kBlock + row, &kv_map, 0, kvh, 0, c3[i] + 1, fb, policy);
+          dev::tma_load_4d(st + 3 * kBlock + row, &kv_map, 64, kvh, 0, c3[i] + 1, fb, policy);
         }
       }
-      // no copy may still be landing when the CTA exits
+      __syncwarp();
+    }
+    // no copy may still be landing when the CTA exits
+    if (lane == 0)
       for (int j = tiles > kStages ? tiles - kStages : 0; j < tiles; ++j)
         if (!dev::mbar_wait_bounded(dev::smem_addr(&kv_full[j % kStages]),
                                     (uint32_t)((j / kStages) & 1)))
           atomicOr(p.err, 2);
-    }
   } else if (warp == 5) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
