@@ -84,7 +84,7 @@ def read_bf16_peak():
 
 # Sources that are not part of the decode kernels or their launch: the
 # cascade's own kernels, the no-allocation entry point, fa_merge_states.
-NOT_DECODE_SOURCES = ("cascade.cu", "static_scratch.cu", "merge.cu")
+NOT_DECODE_SOURCES = ("cascade.cu", "cascade_tc.cuh", "static_scratch.cu", "merge.cu")
 
 
 def kernel_source_hash(workload: str = "gqa_uniform") -> str:
@@ -409,7 +409,9 @@ def bench_cascade(args, world, rank, local, b, cfg, dev):
                      "peak": tflops_peak, "unit": "TFLOP/s",
                      "frac": prefix_flops / prefix_s / 1e12 / tflops_peak,
                      "traffic": profiled_traffic("cascade"),
-                     "kernel": "fa_prefix_kernel (mma.sync bf16)", "peak_kind": tflops_kind,
+                     "kernel": ("fa_prefix_kernel (mma.sync bf16)"
+                                if os.environ.get("FADECODE_CASCADE") == "mma"
+                                else "fa_prefix_tc_kernel (tcgen05 bf16, TMEM accumulators)"), "peak_kind": tflops_kind,
                      "flops_per_launch": prefix_flops,
                      "prefix_kernel_us": prefix_s * 1e6,
                      "prefix_hbm_gbs": prefix_bytes / prefix_s / 1e9},

@@ -45,6 +45,9 @@ struct PrefixParams {
   float* part_lse;      // [items][128 rows], log2 domain
   int group;            // query heads per kv head
   float q_scale;        // sm_scale * log2(e)
+  int row_blocks;       // 128-row blocks per kv head
+  int pair_blocks;      // pairs of row blocks per kv head (tcgen05 kernel)
+  int chunks;           // prefix chunks
 };
 
 struct CombineParams {
@@ -397,6 +400,12 @@ int encode_prefix_map(CUtensorMap* map, fa_dtype dt, const void* paged_kv, int64
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// Most prefix work items a plan makes (its partial states are sized by it):
+// at least one chunk per (kv head, row block), else up to 4 per SM.
+int64_t prefix_items_cap(int num_kv_heads, int64_t row_blocks, int sms) {
+  return std::max<int64_t>((int64_t)num_kv_heads * row_blocks, 4 * (int64_t)sms);
+}
+
 struct CascadeLayout {
   size_t off_suffix_ws, suffix_ws_bytes, off_err, off_items, off_cta, meta_bytes, off_part_o,
       off_part_lse, off_so, off_slse, total;
@@ -423,6 +432,7 @@ CascadeLayout cascade_layout(size_t suffix_ws, int64_t items, int batch, int Hq,
 struct fa_cascade_plan_s {
   fa_decode_plan_t suffix = nullptr;
   int batch = 0, hq = 0, hkv = 0, d = 0, group = 0, row_blocks = 0, chunks = 0, items = 0;
+  int grid = 0;  // prefix CTAs: one per item, or per item pair on tcgen05
   fa_dtype dtype = FA_DTYPE_BF16;
   const int32_t* prefix_indices = nullptr;
   uint8_t* ws = nullptr;
@@ -446,8 +456,8 @@ size_t fa_cascade_workspace_size(int batch, int num_qo_heads, int num_kv_heads, 
   const int G = num_qo_heads / num_kv_heads;
   const int64_t rows = (int64_t)batch * G;
   const int64_t rb = (rows + fadecode::kPrefixRows - 1) / fadecode::kPrefixRows;
-  const int64_t items = std::max<int64_t>((int64_t)num_kv_heads * rb, 2 * (int64_t)sms);
-  return cascade_layout(sw, items, batch, num_qo_heads, head_dim).total;
+  return cascade_layout(sw, prefix_items_cap(num_kv_heads, rb, sms), batch, num_qo_heads,
+                        head_dim).total;
 }
 
 int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
@@ -494,13 +504,17 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
   // prefix work: (kv head, row block, page chunk), about one wave of CTAs
   const int64_t rows = (int64_t)batch * plan->group;
   plan->row_blocks = (int)((rows + fadecode::kPrefixRows - 1) / fadecode::kPrefixRows);
-  const int64_t base = (int64_t)num_kv_heads * plan->row_blocks;
+  // the tcgen05 kernel takes two row blocks of a kv head per CTA
+  const int64_t base = (int64_t)num_kv_heads *
+                       (k.tcgen05 ? (plan->row_blocks + 1) / 2 : plan->row_blocks);
   // chunk count with the fewest waves x pages per chunk (at least 4 pages a
   // chunk), so that every SM gets work and the last wave is not a straggler
   const int64_t slots = (int64_t)sms * occ;
   int chunks = 1;
   int64_t best = INT64_MAX;
+  const int64_t cap = prefix_items_cap(num_kv_heads, plan->row_blocks, sms);
   for (int c = 1; c <= std::max(1, num_prefix_pages / 4); ++c) {
+    if (c > 1 && (int64_t)num_kv_heads * plan->row_blocks * c > cap) break;
     const int64_t waves = (base * c + slots - 1) / slots;
     const int64_t cost = waves * ((num_prefix_pages + c - 1) / c);
     if (cost < best) {
@@ -510,7 +524,8 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
     if (base * c > 8 * slots) break;
   }
   plan->chunks = chunks;
-  plan->items = (int)(base * chunks);
+  plan->items = (int)((int64_t)num_kv_heads * plan->row_blocks * chunks);
+  plan->grid = (int)(base * chunks);
   plan->L = cascade_layout(sw, plan->items, batch, num_qo_heads, head_dim);
   if (plan->L.total > workspace_bytes) {
     delete plan;
@@ -592,10 +607,13 @@ int fa_cascade_run(fa_cascade_plan_t plan, const void* q, const void* paged_kv,
   pp.part_lse = reinterpret_cast<float*>(ws + plan->L.off_part_lse);
   pp.group = plan->group;
   pp.q_scale = sm_scale * 1.4426950408889634f;
+  pp.row_blocks = plan->row_blocks;
+  pp.pair_blocks = (plan->row_blocks + 1) / 2;
+  pp.chunks = plan->chunks;
   void* args[3] = {&plan->map, &prm, &pp};
   const bool timed = plan->ev_before && plan->ev_after;
   if (timed && cudaEventRecord(plan->ev_before, st) != cudaSuccess) return FA_ERR_CUDA;
-  if (cudaLaunchKernel(plan->k.prefix, dim3(plan->items), dim3(plan->k.threads), args,
+  if (cudaLaunchKernel(plan->k.prefix, dim3(plan->grid), dim3(plan->k.threads), args,
                        (size_t)plan->k.smem, st) != cudaSuccess)
     return FA_ERR_CUDA;
   if (timed && cudaEventRecord(plan->ev_after, st) != cudaSuccess) return FA_ERR_CUDA;

@@ -4,19 +4,25 @@
 // every request that reads one kv head) against every token of the shared
 // prefix.  fa_prefix_kernel (cascade.cu) runs it on warp-level mma.sync,
 // where the legacy tensor pipe and nine warps per SM bound it far below the
-// GB300's tensor rate.  Here one CTA per SM works on one (kv head, 128-row
-// block, prefix chunk) item, 64 tokens (4 pages) at a time:
+// GB300's tensor rate.  Here one CTA per SM works on one (kv head, prefix
+// chunk) and on two 128-row blocks of that kv head's query rows at once (A
+// and B, 256 rows; B is absent when the kv head has a single block), 64
+// tokens (4 pages) at a time.  The two blocks share every K/V tile and give
+// the tensor cores independent work: while the softmax of block A runs, the
+// MMAs of block B proceed, and the other way round.
 //
-//  - warp 4 (TMA): per tile, 16 tensor copies of 2 KB (4 pages x {K, V} x two
+//  - warp 8 (TMA): per tile, 16 tensor copies of 2 KB (4 pages x {K, V} x two
 //    64-dim halves) into a 4-stage ring, each half-block a [64 tokens][64
 //    dims] 128-byte-swizzled matrix.  Pages past the chunk are fetched from
 //    an out-of-range page index, so the copy fills them with zeros;
-//  - warp 5 (MMA, one lane): S[b] = Q K^T (M 128, N 64, K 128: 8 MMAs, Q and
-//    K K-major) into one of two TMEM score buffers, then, once the softmax
-//    has written P for the previous tile, O += P V (M 128, N 128, K 64: 4
-//    MMAs, V read MN-major straight from the ring) into the TMEM output
-//    accumulator; tcgen05.commit signals each step's mbarrier;
-//  - warps 0-3 (softmax): thread r owns query row r = TMEM lane r.  It loads
+//  - warp 9 (MMA, one lane): per block, S[b] = Q K^T (M 128, N 64, K 128: 8
+//    MMAs, Q and K K-major) into one of its two TMEM score buffers, then,
+//    once the block's softmax has written P for the previous tile, O += P V
+//    (M 128, N 128, K 64: 4 MMAs, V read MN-major straight from the ring)
+//    into its TMEM output accumulator; tcgen05.commit signals each step's
+//    mbarrier;
+//  - warps 0-3 (block A) and 4-7 (block B), the softmax: thread r of a
+//    warpgroup owns query row r of its block = TMEM lane r.  It loads
 //    its 64 scores with tcgen05.ld, keeps the row maximum and sum in
 //    registers (no shuffles), writes its row of P as bf16/f16 into a
 //    swizzled shared-memory tile for the next MMA, and rescales its row of
@@ -25,7 +31,9 @@
 //    bf16/f16 and fp32 ranges.  At the end it normalises O and writes the
 //    row's partial state (o, log2-sum-exp) for fa_cascade_combine_kernel.
 //
-// TMEM: 256 columns - S0 [0, 64), S1 [64, 128), O [128, 256).  Every wait is
+// TMEM: all 512 columns - per block two score buffers of 64 columns and an
+// output accumulator of 128 (A: S [0, 128), O [256, 384); B: S [128, 256),
+// O [384, 512)).  Every wait is
 // bounded (2 s); a wait that runs out sets bit 1 of the device-check word and
 // the CTA drains, still freeing its TMEM.
 #pragma once
@@ -36,26 +44,29 @@ namespace tc {
 constexpr int kD = 128;
 constexpr int kTok = 64;                   // tokens per tile
 constexpr int kPages = kTok / kPageSize;   // 4
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kBlock = kTok * 128;         // [64 rows][128 bytes]
 constexpr int kStageBytes = 4 * kBlock;    // K lo, K hi, V lo, V hi
-constexpr int kQBytes = 2 * kPrefixRows * 128;
-constexpr int kPBytes = kPrefixRows * 128;
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffP = kOffKV + kStages * kStageBytes;
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-// kv_full[4], kv_empty[4], s_full[2], s_free[2], p_full[2], p_free[2], o_done, q_ready
-constexpr int kNumBars = 2 * kStages + 10;
+constexpr int kQBytes = 2 * kPrefixRows * 128;  // one block's Q: two [128][64] halves
+constexpr int kPBytes = kPrefixRows * 128;      // one P buffer: [128 rows][64 tokens]
+constexpr int kOffQ = 0;                        // Q of block A, then of block B
+constexpr int kOffKV = kOffQ + 2 * kQBytes;
+constexpr int kOffP = kOffKV + kStages * kStageBytes;  // P[block][buffer]
+constexpr int kOffBar = kOffP + 4 * kPBytes;
+// kv_full[S], kv_empty[S]; per block s_full[2], s_free[2], p_full[2],
+// p_free[2]; o_done, q_ready
+constexpr int kBlockBars = 8;
+constexpr int kNumBars = 2 * kStages + 2 * kBlockBars + 3;  // + o_done[2], q_ready
 constexpr int kOffTmem = kOffBar + 8 * kNumBars;
 constexpr int kSmem = kOffTmem + 16;
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kThreads = 352;  // 8 softmax warps, the TMA warp, an MMA warp per block
+constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleAbove = 8.f;       // log2 units
 
 static_assert(32 % kPages == 0, "a warp's page-id load covers whole tiles");
 static_assert(kOffKV % 1024 == 0 && kStageBytes % 1024 == 0 && kOffP % 1024 == 0,
               "swizzled operands need 1024-byte alignment");
+static_assert(kSmem + 1024 <= 227 * 1024, "shared memory per CTA");
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   // tcgen05 shared-memory matrix descriptor: start, leading and stride byte
@@ -71,19 +82,37 @@ __host__ __device__ constexpr uint32_t instr_desc(bool bf16, int m, int n, int b
          ((uint32_t)b_mn << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// Executed by a whole converged warp (warp-uniform operands); one elected
+// lane issues.
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                      bool accumulate) {
   asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "{\n.reg .pred e, p;\nelect.sync _|e, 0xffffffff;\nsetp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate));
 }
 
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+      "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
           dev::smem_addr(bar))
       : "memory");
+}
+
+// Non-blocking probe of an mbarrier phase (try_wait may suspend the thread
+// for a while, which would stall a scheduler polling several barriers).
+// Called by a whole warp: lane 0's answer is everyone's.
+__device__ __forceinline__ bool ready(const uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(dev::smem_addr(bar)), "r"(parity)
+      : "memory");
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 __device__ __forceinline__ void fence_before() {
@@ -131,6 +160,9 @@ __device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
 
 }  // namespace tc
 
+// Prefix work of one CTA: the chunk of kv head h and row-block pair q:
+// item_a = (h * row_blocks + 2q) * chunks + c and item_b = item_a + chunks
+// (the next row block) when that block exists.
 template <typename QT>
 __global__ void __launch_bounds__(tc::kThreads, 1)
     fa_prefix_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p,
@@ -144,38 +176,43 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + kStages;
-  uint64_t* s_full = bars + 2 * kStages;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* p_free = p_full + 2;
-  uint64_t* o_done = p_free + 2;
-  uint64_t* q_ready = o_done + 1;
+  // per block X: s_full[2], s_free[2], p_full[2], p_free[2]
+  auto blk_bar = [&](int X, int which, int b) -> uint64_t* {
+    return bars + 2 * kStages + X * kBlockBars + 2 * which + b;
+  };
+  uint64_t* o_done = bars + 2 * kStages + 2 * kBlockBars;  // [2], one per block
+  uint64_t* q_ready = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = blockIdx.x;
-  const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * item);
-  const int4 sb = *reinterpret_cast<const int4*>(p.segments + 8 * item + 4);
-  const int row0 = sa.x, kvh = sa.y, pb = sa.z, npg = sa.w - sa.z, row_count = sb.x;
-  const int out_item = sb.y;
+
+  const int c = blockIdx.x % pp.chunks;
+  const int pair = blockIdx.x / pp.chunks;
+  const int h_kv = pair / pp.pair_blocks, rbp = pair % pp.pair_blocks;
+  const int item_a = (h_kv * pp.row_blocks + 2 * rbp) * pp.chunks + c;
+  const int nblk = (2 * rbp + 1 < pp.row_blocks) ? 2 : 1;
+  const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * item_a);
+  const int kvh = sa.y, pb = sa.z, npg = sa.w - sa.z;
   const int tiles = (npg + kPages - 1) / kPages;
   const uint32_t sbase = dev::smem_addr(smem);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       dev::mbar_init(dev::smem_addr(&kv_full[s]), 1);
-      dev::mbar_init(dev::smem_addr(&kv_empty[s]), 1);
+      dev::mbar_init(dev::smem_addr(&kv_empty[s]), nblk);  // every block's P.V of the tile
     }
-    for (int b = 0; b < 2; ++b) {
-      dev::mbar_init(dev::smem_addr(&s_full[b]), 1);
-      dev::mbar_init(dev::smem_addr(&s_free[b]), 4);
-      dev::mbar_init(dev::smem_addr(&p_full[b]), 4);
-      dev::mbar_init(dev::smem_addr(&p_free[b]), 1);
-    }
-    dev::mbar_init(dev::smem_addr(o_done), 1);
-    dev::mbar_init(dev::smem_addr(q_ready), 4);
+    for (int X = 0; X < 2; ++X)
+      for (int b = 0; b < 2; ++b) {
+        dev::mbar_init(dev::smem_addr(blk_bar(X, 0, b)), 1);  // s_full
+        dev::mbar_init(dev::smem_addr(blk_bar(X, 1, b)), 4);  // s_free
+        dev::mbar_init(dev::smem_addr(blk_bar(X, 2, b)), 4);  // p_full
+        dev::mbar_init(dev::smem_addr(blk_bar(X, 3, b)), 1);  // p_free
+      }
+    dev::mbar_init(dev::smem_addr(&o_done[0]), 1);
+    dev::mbar_init(dev::smem_addr(&o_done[1]), 1);
+    dev::mbar_init(dev::smem_addr(q_ready), 4 * nblk);
     dev::fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      dev::smem_addr(tmem_slot)),
                  "r"(kTmemCols)
@@ -186,10 +223,10 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 2 * kTok;
+  // block X: scores at columns X*128 + b*64, output at 256 + X*128
   bool aborted = false;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------------------------------------------------------- TMA
     // The warp reads the page ids 32 at a time (eight tiles' worth, one per
     // lane); lane 0 waits for ring stages and issues the copies.
@@ -241,51 +278,89 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         if (!dev::mbar_wait_bounded(dev::smem_addr(&kv_full[j % kStages]),
                                     (uint32_t)((j / kStages) & 1)))
           atomicOr(p.err, 2);
-  } else if (warp == 5) {
+  } else if (warp == 9 || warp == 10) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
-      const uint32_t q_addr = sbase + kOffQ, p_addr = sbase + kOffP;
-      auto pv = [&](int i) {
-        const int b = i & 1, s = i % kStages;
-        dev::mbar_wait(dev::smem_addr(&p_full[b]), (uint32_t)((i >> 1) & 1), aborted, p.err);
-        fence_after();
-        const uint32_t v_addr = sbase + kOffKV + s * kStageBytes + 2 * kBlock;
-#pragma unroll
-        for (int k = 0; k < kTok / 16; ++k)  // 16 tokens per MMA
-          umma(tO, smem_desc(p_addr + b * kPBytes + k * 32, 16, 1024),
-              smem_desc(v_addr + k * 16 * 128, kBlock, 1024), kIdescPV, i > 0 || k > 0);
-        commit(&p_free[b]);
-        commit(&kv_empty[s]);
-      };
+    // Warp 9 issues block A's MMAs, warp 10 block B's, each a converged warp
+    // with one elected lane issuing (operands stay warp-uniform, and the two
+    // blocks' instruction streams proceed side by side).  Within a block, a
+    // ready P.V goes first (it frees a P buffer and the block's share of a
+    // K/V stage), then a ready Q K^T.
+    const int X = warp - 9;
+    if (X < nblk) {
+      int next_qk = 0, next_pv = 0;
       dev::mbar_wait(dev::smem_addr(q_ready), 0u, aborted, p.err);
+      aborted = __any_sync(0xffffffffu, aborted);
       fence_after();
-      for (int j = 0; j < tiles; ++j) {
-        const int s = j % kStages, b = j & 1;
-        dev::mbar_wait(dev::smem_addr(&kv_full[s]), (uint32_t)((j / kStages) & 1), aborted,
-                       p.err);
-        if (j >= 2)
-          dev::mbar_wait(dev::smem_addr(&s_free[b]), (uint32_t)(((j - 2) >> 1) & 1), aborted,
-                         p.err);
-        fence_after();
-        const uint32_t k_addr = sbase + kOffKV + s * kStageBytes;
+      const uint32_t q_addr = sbase + kOffQ + X * kQBytes;
+      const uint32_t tO = tmem + 256 + X * 128;
+      unsigned long long idle_since = 0;
+      while (!aborted && next_pv < tiles) {
+        bool progress = false;
+        if (next_pv < next_qk) {
+          const int i = next_pv, b = i & 1;
+          if (ready(blk_bar(X, 2, b), (uint32_t)((i >> 1) & 1))) {
+            fence_after();
+            const int s = i % kStages;
+            const uint32_t v_addr = sbase + kOffKV + s * kStageBytes + 2 * kBlock;
+            const uint32_t p_addr = sbase + kOffP + (2 * X + b) * kPBytes;
 #pragma unroll
-        for (int k = 0; k < kD / 16; ++k) {  // 16 dims per MMA, 64 per 128-byte block
-          const uint32_t off = (uint32_t)(k % 4) * 32;  // 32 bytes = 16 dims into the row
-          umma(tS + b * kTok, smem_desc(q_addr + (k / 4) * (kPrefixRows * 128) + off, 16, 1024),
-              smem_desc(k_addr + (k / 4) * kBlock + off, 16, 1024), kIdescQK, k > 0);
+            for (int k = 0; k < kTok / 16; ++k)  // 16 tokens per MMA
+              umma(tO, smem_desc(p_addr + k * 32, 16, 1024),
+                   smem_desc(v_addr + k * 16 * 128, kBlock, 1024), kIdescPV, i > 0 || k > 0);
+            commit(blk_bar(X, 3, b));  // p_free
+            commit(&kv_empty[s]);
+            next_pv = i + 1;
+            progress = true;
+          }
         }
-        commit(&s_full[b]);
-        if (j >= 1) pv(j - 1);
+        if (next_qk < tiles) {
+          const int j = next_qk, s = j % kStages, b = j & 1;
+          if ((j < 2 || ready(blk_bar(X, 1, b), (uint32_t)(((j - 2) >> 1) & 1))) &&
+              ready(&kv_full[s], (uint32_t)((j / kStages) & 1))) {
+            fence_after();
+            const uint32_t k_addr = sbase + kOffKV + s * kStageBytes;
+            const uint32_t tS = tmem + X * 128 + b * kTok;
+#pragma unroll
+            for (int k = 0; k < kD / 16; ++k) {  // 16 dims per MMA, 64 per 128-byte block
+              const uint32_t off = (uint32_t)(k % 4) * 32;  // 32 bytes = 16 dims into the row
+              umma(tS, smem_desc(q_addr + (k / 4) * (kPrefixRows * 128) + off, 16, 1024),
+                   smem_desc(k_addr + (k / 4) * kBlock + off, 16, 1024), kIdescQK, k > 0);
+            }
+            commit(blk_bar(X, 0, b));  // s_full
+            next_qk = j + 1;
+            progress = true;
+          }
+        }
+        if (progress) {
+          idle_since = 0;
+        } else {  // nothing ready: give up after the same bound as every other wait
+          const unsigned long long now =
+              __shfl_sync(0xffffffffu, dev::global_timer_ns(), 0);
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (now - idle_since > dev::kWaitTimeoutNs) {
+            aborted = true;
+            if (lane == 0) atomicOr(p.err, 2);
+          }
+        }
       }
-      if (tiles > 0) pv(tiles - 1);
-      commit(o_done);
+      commit(&o_done[X]);
     }
-  } else {
+  } else if (warp / 4 < nblk) {
     // ---------------------------------------------------------------- softmax
-    const int r = threadIdx.x;  // query row of the block = TMEM lane
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const int X = warp / 4;                 // block of this warpgroup
+    const int r = threadIdx.x % 128;        // query row of the block = TMEM lane
+    const int4 sx = *reinterpret_cast<const int4*>(p.segments + 8 * (item_a + X * pp.chunks));
+    const int4 sy = *reinterpret_cast<const int4*>(p.segments + 8 * (item_a + X * pp.chunks) + 4);
+    const int row0 = sx.x, row_count = sy.x, out_item = sy.y;
+    const uint32_t lane_off = (uint32_t)(32 * (warp % 4)) << 16;
+    const uint32_t tS0 = tmem + X * 128, tO = tmem + 256 + X * 128;
+    uint64_t* s_full = blk_bar(X, 0, 0);
+    uint64_t* s_free = blk_bar(X, 1, 0);
+    uint64_t* p_full = blk_bar(X, 2, 0);
+    uint64_t* p_free = blk_bar(X, 3, 0);
     // Q row into the swizzled A tile: granule c8 (8 elements) of row r lands
-    // in block c8 / 8 at granule (c8 % 8) ^ (r % 8)
+    // in half c8 / 8 at granule (c8 % 8) ^ (r % 8)
     {
       const int G = pp.group;
       const int rho = row0 + r;
@@ -296,8 +371,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       for (int c8 = 0; c8 < kD / 8; ++c8) {
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (live) v = __ldg(reinterpret_cast<const uint4*>(qrow + c8 * 8));
-        const uint32_t a = sbase + kOffQ + (c8 / 8) * (kPrefixRows * 128) + r * 128 +
-                           (uint32_t)(((c8 % 8) ^ (r & 7)) * 16);
+        const uint32_t a = sbase + kOffQ + X * kQBytes + (c8 / 8) * (kPrefixRows * 128) +
+                           r * 128 + (uint32_t)(((c8 % 8) ^ (r & 7)) * 16);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
                      "r"(v.z), "r"(v.w)
                      : "memory");
@@ -314,8 +389,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       float s[kTok];
       {
         float lo[32], hi[32];
-        ld32(tS + lane_off + b * kTok, lo);
-        ld32(tS + lane_off + b * kTok + 32, hi);
+        ld32(tS0 + lane_off + b * kTok, lo);
+        ld32(tS0 + lane_off + b * kTok + 32, hi);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           s[i] = lo[i];
@@ -343,12 +418,12 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         fence_after();
         const float f = rebase ? alpha : 1.f;
 #pragma unroll
-        for (int c = 0; c < kD / 32; ++c) {
+        for (int cc = 0; cc < kD / 32; ++cc) {
           float v[32];
-          ld32(tO + lane_off + c * 32, v);
+          ld32(tO + lane_off + cc * 32, v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= f;
-          st32(tO + lane_off + c * 32, v);
+          st32(tO + lane_off + cc * 32, v);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
@@ -368,7 +443,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       if (j >= 2)  // P buffer b was read by P.V of tile j-2
         dev::mbar_wait(dev::smem_addr(&p_free[b]), (uint32_t)(((j - 2) >> 1) & 1), aborted,
                        p.err);
-      const uint32_t prow = sbase + kOffP + b * kPBytes + r * 128;
+      const uint32_t prow = sbase + kOffP + (2 * X + b) * kPBytes + r * 128;
 #pragma unroll
       for (int g8 = 0; g8 < kTok / 8; ++g8) {
         const uint32_t a = prow + (uint32_t)((g8 ^ (r & 7)) * 16);
@@ -382,15 +457,15 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       if (lane == 0) dev::mbar_arrive(dev::smem_addr(&p_full[b]));
     }
     // ---- this row's partial state: o / d and log2-sum-exp
-    dev::mbar_wait(dev::smem_addr(o_done), 0u, aborted, p.err);
+    dev::mbar_wait(dev::smem_addr(&o_done[X]), 0u, aborted, p.err);
     fence_after();
     const float inv = d > 0.f ? 1.f / d : 0.f;
     float* dst = pp.part_o + ((size_t)out_item * kPrefixRows + r) * kD;
 #pragma unroll
-    for (int c = 0; c < kD / 32; ++c) {
+    for (int cc = 0; cc < kD / 32; ++cc) {
       float v[32];
       if (tiles > 0) {
-        ld32(tO + lane_off + c * 32, v);  // every lane of the warp takes part
+        ld32(tO + lane_off + cc * 32, v);  // every lane of the warp takes part
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.f;  // no tile: O was never written
@@ -398,7 +473,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       if (r < row_count) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(dst + c * 32 + i) =
+          *reinterpret_cast<float4*>(dst + cc * 32 + i) =
               make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
       }
     }
@@ -408,7 +483,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   }
   fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
