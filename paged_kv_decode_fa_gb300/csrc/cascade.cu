@@ -286,9 +286,12 @@ __global__ void __launch_bounds__(PrefixCfg<QT, D, NW>::THREADS)
 namespace fadecode {
 
 // One warp per (request, qo head): fold the prefix chunks' states and the
-// suffix state with the merge rule.
+// suffix state with the merge rule.  Lane k holds chunk k's log2-sum-exp
+// (32 chunks at a time) and lane l the dims [4l, 4l + 4) of the output;
+// the chunk loop keeps several 16-byte loads of partial outputs in flight.
 template <typename QT, int D>
 __global__ void __launch_bounds__(256) fa_cascade_combine_kernel(const CombineParams c) {
+  static_assert(D == 128, "four dims per lane");
   const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= (int64_t)c.batch * c.num_qo_heads) return;
@@ -297,32 +300,52 @@ __global__ void __launch_bounds__(256) fa_cascade_combine_kernel(const CombinePa
   const int rb = rho / kPrefixRows, row = rho % kPrefixRows;
   const int item0 = (kvh * c.row_blocks + rb) * c.chunks;
   constexpr float kLog2e = 1.4426950408889634f;
-  float M = -INFINITY;
-  for (int k = 0; k < c.chunks; ++k)
-    M = fmaxf(M, c.part_lse[(size_t)(item0 + k) * kPrefixRows + row]);
+  auto chunk_lse = [&](int k) -> float {
+    return k < c.chunks ? __ldg(c.part_lse + (size_t)(item0 + k) * kPrefixRows + row) : -INFINITY;
+  };
   const float ls = c.suffix_lse[wid] * kLog2e;
-  M = fmaxf(M, ls);
+  float M = ls;
+  for (int k0 = 0; k0 < c.chunks; k0 += 32) M = fmaxf(M, chunk_lse(k0 + lane));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float num[4] = {0.f, 0.f, 0.f, 0.f};
   float den = 0.f, lse2 = -INFINITY;
   if (M != -INFINITY) {
-    for (int k = 0; k < c.chunks; ++k)
-      den += dev::fast_exp2(c.part_lse[(size_t)(item0 + k) * kPrefixRows + row] - M);
-    den += dev::fast_exp2(ls - M);
+    for (int k0 = 0; k0 < c.chunks; k0 += 32) {
+      const float wl = dev::fast_exp2(chunk_lse(k0 + lane) - M);  // 0 past the last chunk
+      den += wl;
+      const int n = min(32, c.chunks - k0);
+      const float* src = c.part_o + ((size_t)(item0 + k0) * kPrefixRows + row) * D + 4 * lane;
+#pragma unroll 4
+      for (int i = 0; i < n; ++i) {
+        const float w = __shfl_sync(0xffffffffu, wl, i);
+        const float4 x = __ldg(reinterpret_cast<const float4*>(src + (size_t)i * kPrefixRows * D));
+        num[0] = fmaf(x.x, w, num[0]);
+        num[1] = fmaf(x.y, w, num[1]);
+        num[2] = fmaf(x.z, w, num[2]);
+        num[3] = fmaf(x.w, w, num[3]);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    const float ws = dev::fast_exp2(ls - M);
+    den += ws;
+    const uint2 sv =
+        *reinterpret_cast<const uint2*>(static_cast<const QT*>(c.suffix_o) + wid * D + 4 * lane);
+    const bool bf = std::is_same<QT, __nv_bfloat16>::value;
+    const float2 s01 = mma::unpack2(sv.x, bf), s23 = mma::unpack2(sv.y, bf);
+    num[0] = fmaf(s01.x, ws, num[0]);
+    num[1] = fmaf(s01.y, ws, num[1]);
+    num[2] = fmaf(s23.x, ws, num[2]);
+    num[3] = fmaf(s23.y, ws, num[3]);
     lse2 = M + dev::fast_log2(den);
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
-  const QT* so = static_cast<const QT*>(c.suffix_o) + wid * D;
-  QT* out = static_cast<QT*>(c.o) + wid * D;
-  for (int d = lane; d < D; d += 32) {
-    float num = 0.f;
-    if (M != -INFINITY) {
-      for (int k = 0; k < c.chunks; ++k) {
-        const float w = dev::fast_exp2(c.part_lse[(size_t)(item0 + k) * kPrefixRows + row] - M);
-        num = fmaf(c.part_o[((size_t)(item0 + k) * kPrefixRows + row) * D + d], w, num);
-      }
-      num = fmaf(dev::to_float(so[d]), dev::fast_exp2(ls - M), num);
-    }
-    out[d] = dev::from_float<QT>(num * inv);
-  }
+  const bool bf = std::is_same<QT, __nv_bfloat16>::value;
+  uint2 ov;
+  ov.x = mma::pack2(num[0] * inv, num[1] * inv, bf);
+  ov.y = mma::pack2(num[2] * inv, num[3] * inv, bf);
+  *reinterpret_cast<uint2*>(static_cast<QT*>(c.o) + wid * D + 4 * lane) = ov;
   if (lane == 0 && c.lse) c.lse[wid] = lse2 * 0.693147180559945309f;
 }
 

@@ -11,31 +11,36 @@
 // the tensor cores independent work: while the softmax of block A runs, the
 // MMAs of block B proceed, and the other way round.
 //
-//  - warp 8 (TMA): per tile, 16 tensor copies of 2 KB (4 pages x {K, V} x two
-//    64-dim halves) into a 4-stage ring, each half-block a [64 tokens][64
-//    dims] 128-byte-swizzled matrix.  Pages past the chunk are fetched from
-//    an out-of-range page index, so the copy fills them with zeros;
-//  - warp 9 (MMA, one lane): per block, S[b] = Q K^T (M 128, N 64, K 128: 8
-//    MMAs, Q and K K-major) into one of its two TMEM score buffers, then,
-//    once the block's softmax has written P for the previous tile, O += P V
-//    (M 128, N 128, K 64: 4 MMAs, V read MN-major straight from the ring)
-//    into its TMEM output accumulator; tcgen05.commit signals each step's
-//    mbarrier;
+//  - warps 8 and 11 (TMA): K and V of a tile go into separate 5-slot rings,
+//    filled by one warp each, each slot 8 tensor copies of 2 KB (4 pages x
+//    two 64-dim halves), each half a [64 tokens][64 dims] 128-byte-swizzled
+//    matrix.  A K slot comes free as soon as both blocks' Q K^T of it
+//    completed, a V slot once both blocks' P V did.  Two issuing threads
+//    keep twice the copies in flight that one does (a thread's copy
+//    instructions stall while the memory system is busy).  Pages past the
+//    chunk are fetched from an out-of-range page index, so the copy fills
+//    them with zeros;
+//  - warps 9 and 10 (MMA, one per block, one elected lane issuing): S = Q K^T
+//    (M 128, N 64, K 128: 8 MMAs, Q and K K-major) into one of the block's
+//    two TMEM score buffers, and O += P V (M 128, N 128, K 64: 4 MMAs, P read
+//    from TMEM, V MN-major straight from its ring slot) into the block's
+//    TMEM output accumulator.  The order is fixed: S(0), S(1), then per tile
+//    j: P V(j) once P(j) is written, then S(j + 2) into the buffer P(j) just
+//    left (MMAs of one thread run in issue order);
 //  - warps 0-3 (block A) and 4-7 (block B), the softmax: thread r of a
-//    warpgroup owns query row r of its block = TMEM lane r.  It loads
-//    its 64 scores with tcgen05.ld, keeps the row maximum and sum in
-//    registers (no shuffles), writes its row of P as bf16/f16 into a
-//    swizzled shared-memory tile for the next MMA, and rescales its row of
-//    O in TMEM (tcgen05.ld / st) only when the maximum has grown by more than
-//    2^8 - between rescales the weights stay below 256, far inside the
-//    bf16/f16 and fp32 ranges.  At the end it normalises O and writes the
-//    row's partial state (o, log2-sum-exp) for fa_cascade_combine_kernel.
+//    warpgroup owns query row r of its block = TMEM lane r.  It loads its 64
+//    scores with tcgen05.ld, keeps the row maximum and sum in registers (no
+//    shuffles), writes its row of P as bf16/f16 over the first 32 columns of
+//    the same score buffer (tcgen05.st), and rescales its row of O in TMEM
+//    only when the maximum has grown by more than 2^8 - between rescales the
+//    weights stay below 256, far inside the bf16/f16 and fp32 ranges.  At the
+//    end it normalises O and writes the row's partial state (o,
+//    log2-sum-exp) for fa_cascade_combine_kernel.
 //
-// TMEM: all 512 columns - per block two score buffers of 64 columns and an
+// TMEM: all 512 columns - per block two score/P buffers of 64 columns and an
 // output accumulator of 128 (A: S [0, 128), O [256, 384); B: S [128, 256),
-// O [384, 512)).  Every wait is
-// bounded (2 s); a wait that runs out sets bit 1 of the device-check word and
-// the CTA drains, still freeing its TMEM.
+// O [384, 512)).  Every wait is bounded (2 s); a wait that runs out sets bit
+// 1 of the device-check word and the CTA drains, still freeing its TMEM.
 #pragma once
 
 namespace fadecode {
@@ -44,27 +49,26 @@ namespace tc {
 constexpr int kD = 128;
 constexpr int kTok = 64;                   // tokens per tile
 constexpr int kPages = kTok / kPageSize;   // 4
-constexpr int kStages = 3;
-constexpr int kBlock = kTok * 128;         // [64 rows][128 bytes]
-constexpr int kStageBytes = 4 * kBlock;    // K lo, K hi, V lo, V hi
+constexpr int kSlots = 5;                  // depth of the K ring and of the V ring
+constexpr int kHalf = kTok * 128;          // [64 tokens][64 dims], 128-byte rows
+constexpr int kSlotBytes = 2 * kHalf;      // one tile of K (or V): both halves
 constexpr int kQBytes = 2 * kPrefixRows * 128;  // one block's Q: two [128][64] halves
-constexpr int kPBytes = kPrefixRows * 128;      // one P buffer: [128 rows][64 tokens]
 constexpr int kOffQ = 0;                        // Q of block A, then of block B
-constexpr int kOffKV = kOffQ + 2 * kQBytes;
-constexpr int kOffP = kOffKV + kStages * kStageBytes;  // P[block][buffer]
-constexpr int kOffBar = kOffP + 4 * kPBytes;
-// kv_full[S], kv_empty[S]; per block s_full[2], s_free[2], p_full[2],
-// p_free[2]; o_done, q_ready
-constexpr int kBlockBars = 8;
-constexpr int kNumBars = 2 * kStages + 2 * kBlockBars + 3;  // + o_done[2], q_ready
+constexpr int kOffK = kOffQ + 2 * kQBytes;
+constexpr int kOffV = kOffK + kSlots * kSlotBytes;
+constexpr int kOffBar = kOffV + kSlots * kSlotBytes;
+// k_full[n], k_empty[n], v_full[n], v_empty[n]; per block s_full[2],
+// p_full[2], pv_done[2]; o_done[2], q_ready
+constexpr int kBlockBars = 6;
+constexpr int kNumBars = 4 * kSlots + 2 * kBlockBars + 3;
 constexpr int kOffTmem = kOffBar + 8 * kNumBars;
 constexpr int kSmem = kOffTmem + 16;
-constexpr int kThreads = 352;  // 8 softmax warps, the TMA warp, an MMA warp per block
+constexpr int kThreads = 384;  // 8 softmax warps, K and V TMA warps, an MMA warp per block
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleAbove = 8.f;       // log2 units
 
 static_assert(32 % kPages == 0, "a warp's page-id load covers whole tiles");
-static_assert(kOffKV % 1024 == 0 && kStageBytes % 1024 == 0 && kOffP % 1024 == 0,
+static_assert(kOffK % 1024 == 0 && kSlotBytes % 1024 == 0 && kOffV % 1024 == 0,
               "swizzled operands need 1024-byte alignment");
 static_assert(kSmem + 1024 <= 227 * 1024, "shared memory per CTA");
 
@@ -158,6 +162,29 @@ __device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
       : "memory");
 }
 
+// O += P V with P (M x K, K-major, packed pairs per 32-bit column) in TMEM
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                        uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n.reg .pred e, p;\nelect.sync _|e, 0xffffffff;\nsetp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"((uint32_t)accumulate));
+}
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane from packed words
+__device__ __forceinline__ void st32u(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
 }  // namespace tc
 
 // Prefix work of one CTA: the chunk of kv head h and row-block pair q:
@@ -174,13 +201,15 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (dev::smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* kv_full = bars;
-  uint64_t* kv_empty = bars + kStages;
-  // per block X: s_full[2], s_free[2], p_full[2], p_free[2]
+  uint64_t* k_full = bars;
+  uint64_t* k_empty = bars + kSlots;
+  uint64_t* v_full = bars + 2 * kSlots;
+  uint64_t* v_empty = bars + 3 * kSlots;
+  // per block X: s_full[2], p_full[2], pv_done[2]
   auto blk_bar = [&](int X, int which, int b) -> uint64_t* {
-    return bars + 2 * kStages + X * kBlockBars + 2 * which + b;
+    return bars + 4 * kSlots + X * kBlockBars + 2 * which + b;
   };
-  uint64_t* o_done = bars + 2 * kStages + 2 * kBlockBars;  // [2], one per block
+  uint64_t* o_done = bars + 4 * kSlots + 2 * kBlockBars;  // [2], one per block
   uint64_t* q_ready = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -196,16 +225,17 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   const uint32_t sbase = dev::smem_addr(smem);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      dev::mbar_init(dev::smem_addr(&kv_full[s]), 1);
-      dev::mbar_init(dev::smem_addr(&kv_empty[s]), nblk);  // every block's P.V of the tile
+    for (int s = 0; s < kSlots; ++s) {
+      dev::mbar_init(dev::smem_addr(&k_full[s]), 1);
+      dev::mbar_init(dev::smem_addr(&k_empty[s]), nblk);  // every block's Q K^T of the tile
+      dev::mbar_init(dev::smem_addr(&v_full[s]), 1);
+      dev::mbar_init(dev::smem_addr(&v_empty[s]), nblk);  // every block's P V of the tile
     }
     for (int X = 0; X < 2; ++X)
       for (int b = 0; b < 2; ++b) {
         dev::mbar_init(dev::smem_addr(blk_bar(X, 0, b)), 1);  // s_full
-        dev::mbar_init(dev::smem_addr(blk_bar(X, 1, b)), 4);  // s_free
-        dev::mbar_init(dev::smem_addr(blk_bar(X, 2, b)), 4);  // p_full
-        dev::mbar_init(dev::smem_addr(blk_bar(X, 3, b)), 1);  // p_free
+        dev::mbar_init(dev::smem_addr(blk_bar(X, 1, b)), 4);  // p_full
+        dev::mbar_init(dev::smem_addr(blk_bar(X, 2, b)), 1);  // pv_done
       }
     dev::mbar_init(dev::smem_addr(&o_done[0]), 1);
     dev::mbar_init(dev::smem_addr(&o_done[1]), 1);
@@ -223,128 +253,115 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  // block X: scores at columns X*128 + b*64, output at 256 + X*128
+  // block X: score/P buffers at columns X*128 + b*64, output at 256 + X*128
   bool aborted = false;
 
-  if (warp == 8) {
+  if (warp == 8 || warp == 11) {
     // ---------------------------------------------------------------- TMA
-    // The warp reads the page ids 32 at a time (eight tiles' worth, one per
-    // lane); lane 0 waits for ring stages and issues the copies.
+    // Warp 8 fills the K ring, warp 11 the V ring.  Each lane holds one page
+    // id of a 32-page window (eight tiles); lane 0 waits for ring slots and
+    // issues the copies.
+    const int kv = warp == 8 ? 0 : 1;
     if (lane == 0) dev::prefetch_tensormap(&kv_map);
     const uint64_t policy = dev::evict_first_policy();
     const int oob = (int)(2 * p.num_pages);  // beyond the last page: zero fill
-    int ids = 0;
-    for (int j = 0; j < tiles; ++j) {
-      const int first = j * kPages;  // page position within the chunk
-      if (first % 32 == 0) {
-        const int pos = first + lane;
-        int id = -1;
-        if (pos < npg) {
-          id = __ldg(p.indices + pb + pos);
-          if (id < 0 || (int64_t)id >= p.num_pages) {
-            atomicOr(p.err, 1);
-            id = -1;
-          }
+    auto load_ids = [&](int first) -> int {
+      const int pos = first + lane;
+      int id = -1;
+      if (pos < npg) {
+        id = __ldg(p.indices + pb + pos);
+        if (id < 0 || (int64_t)id >= p.num_pages) {
+          if (kv == 0) atomicOr(p.err, 1);
+          id = -1;
         }
-        ids = id;
       }
+      return id;
+    };
+    auto issue = [&](int t, int ids, uint64_t* full, uint64_t* empty, uint32_t ring, int kv) {
       int c3[kPages];
 #pragma unroll
       for (int i = 0; i < kPages; ++i) {
-        const int id = __shfl_sync(0xffffffffu, ids, (first + i) % 32);
-        c3[i] = id < 0 ? oob : 2 * id;
+        const int id = __shfl_sync(0xffffffffu, ids, (t * kPages + i) % 32);
+        c3[i] = id < 0 ? oob : 2 * id + kv;
       }
       if (lane == 0) {
-        const int s = j % kStages;
-        dev::mbar_wait(dev::smem_addr(&kv_empty[s]), (uint32_t)(((j / kStages) & 1) ^ 1),
-                       aborted, p.err);
-        const uint32_t fb = dev::smem_addr(&kv_full[s]);
-        dev::mbar_arrive_expect_tx(fb, kStageBytes);
-        const uint32_t st = sbase + kOffKV + s * kStageBytes;
+        const int s = t % kSlots;
+        dev::mbar_wait(dev::smem_addr(&empty[s]), (uint32_t)(((t / kSlots) & 1) ^ 1), aborted,
+                       p.err);
+        const uint32_t fb = dev::smem_addr(&full[s]);
+        dev::mbar_arrive_expect_tx(fb, kSlotBytes);
+        const uint32_t st = ring + s * kSlotBytes;
 #pragma unroll
         for (int i = 0; i < kPages; ++i) {
           const uint32_t row = (uint32_t)i * (kPageSize * 128);
-          dev::tma_load_4d(st + 0 * kBlock + row, &kv_map, 0, kvh, 0, c3[i], fb, policy);
-          dev::tma_load_4d(st + 1 * kBlock + row, &kv_map, 64, kvh, 0, c3[i], fb, policy);
-          dev::tma_load_4d(st + 2 * kBlock + row, &kv_map, 0, kvh, 0, c3[i] + 1, fb, policy);
-          dev::tma_load_4d(st + 3 * kBlock + row, &kv_map, 64, kvh, 0, c3[i] + 1, fb, policy);
+          dev::tma_load_4d(st + row, &kv_map, 0, kvh, 0, c3[i], fb, policy);
+          dev::tma_load_4d(st + kHalf + row, &kv_map, 64, kvh, 0, c3[i], fb, policy);
         }
       }
       __syncwarp();
+    };
+    uint64_t* full = kv ? v_full : k_full;
+    uint64_t* empty = kv ? v_empty : k_empty;
+    const uint32_t ring = sbase + (kv ? kOffV : kOffK);
+    int ids = 0;
+    for (int t = 0; t < tiles; ++t) {
+      if ((t * kPages) % 32 == 0) ids = load_ids(t * kPages);
+      issue(t, ids, full, empty, ring, kv);
     }
     // no copy may still be landing when the CTA exits
     if (lane == 0)
-      for (int j = tiles > kStages ? tiles - kStages : 0; j < tiles; ++j)
-        if (!dev::mbar_wait_bounded(dev::smem_addr(&kv_full[j % kStages]),
-                                    (uint32_t)((j / kStages) & 1)))
+      for (int t = tiles > kSlots ? tiles - kSlots : 0; t < tiles; ++t)
+        if (!dev::mbar_wait_bounded(dev::smem_addr(&full[t % kSlots]),
+                                    (uint32_t)((t / kSlots) & 1)))
           atomicOr(p.err, 2);
   } else if (warp == 9 || warp == 10) {
     // ---------------------------------------------------------------- MMA
-    // Warp 9 issues block A's MMAs, warp 10 block B's, each a converged warp
-    // with one elected lane issuing (operands stay warp-uniform, and the two
-    // blocks' instruction streams proceed side by side).  Within a block, a
-    // ready P.V goes first (it frees a P buffer and the block's share of a
-    // K/V stage), then a ready Q K^T.
+    // Warp 9 issues block A's MMAs, warp 10 block B's: a converged warp, one
+    // elected lane issuing, blocking waits.
     const int X = warp - 9;
     if (X < nblk) {
-      int next_qk = 0, next_pv = 0;
       dev::mbar_wait(dev::smem_addr(q_ready), 0u, aborted, p.err);
       aborted = __any_sync(0xffffffffu, aborted);
       fence_after();
       const uint32_t q_addr = sbase + kOffQ + X * kQBytes;
       const uint32_t tO = tmem + 256 + X * 128;
-      unsigned long long idle_since = 0;
-      while (!aborted && next_pv < tiles) {
-        bool progress = false;
-        if (next_pv < next_qk) {
-          const int i = next_pv, b = i & 1;
-          if (ready(blk_bar(X, 2, b), (uint32_t)((i >> 1) & 1))) {
-            fence_after();
-            const int s = i % kStages;
-            const uint32_t v_addr = sbase + kOffKV + s * kStageBytes + 2 * kBlock;
-            const uint32_t p_addr = sbase + kOffP + (2 * X + b) * kPBytes;
+      auto qk = [&](int j) {
+        const int s = j % kSlots, b = j & 1;
+        dev::mbar_wait(dev::smem_addr(&k_full[s]), (uint32_t)((j / kSlots) & 1), aborted, p.err);
+        fence_after();
+        const uint32_t k_addr = sbase + kOffK + s * kSlotBytes;
+        const uint32_t tS = tmem + X * 128 + b * kTok;
 #pragma unroll
-            for (int k = 0; k < kTok / 16; ++k)  // 16 tokens per MMA
-              umma(tO, smem_desc(p_addr + k * 32, 16, 1024),
-                   smem_desc(v_addr + k * 16 * 128, kBlock, 1024), kIdescPV, i > 0 || k > 0);
-            commit(blk_bar(X, 3, b));  // p_free
-            commit(&kv_empty[s]);
-            next_pv = i + 1;
-            progress = true;
-          }
+        for (int k = 0; k < kD / 16; ++k) {  // 16 dims per MMA, 64 per 128-byte half
+          const uint32_t off = (uint32_t)(k % 4) * 32;  // 32 bytes = 16 dims into the row
+          umma(tS, smem_desc(q_addr + (k / 4) * (kPrefixRows * 128) + off, 16, 1024),
+               smem_desc(k_addr + (k / 4) * kHalf + off, 16, 1024), kIdescQK, k > 0);
         }
-        if (next_qk < tiles) {
-          const int j = next_qk, s = j % kStages, b = j & 1;
-          if ((j < 2 || ready(blk_bar(X, 1, b), (uint32_t)(((j - 2) >> 1) & 1))) &&
-              ready(&kv_full[s], (uint32_t)((j / kStages) & 1))) {
-            fence_after();
-            const uint32_t k_addr = sbase + kOffKV + s * kStageBytes;
-            const uint32_t tS = tmem + X * 128 + b * kTok;
+        commit(blk_bar(X, 0, b));  // s_full
+        commit(&k_empty[s]);
+      };
+      if (tiles > 0) qk(0);
+      if (tiles > 1) qk(1);
+      for (int j = 0; j < tiles; ++j) {
+        const int s = j % kSlots, b = j & 1;
+        dev::mbar_wait(dev::smem_addr(blk_bar(X, 1, b)), (uint32_t)((j >> 1) & 1), aborted,
+                       p.err);
+        dev::mbar_wait(dev::smem_addr(&v_full[s]), (uint32_t)((j / kSlots) & 1), aborted, p.err);
+        fence_after();
+        const uint32_t v_addr = sbase + kOffV + s * kSlotBytes;
+        const uint32_t tP = tmem + X * 128 + b * kTok;  // P(j): 32 columns of packed pairs
 #pragma unroll
-            for (int k = 0; k < kD / 16; ++k) {  // 16 dims per MMA, 64 per 128-byte block
-              const uint32_t off = (uint32_t)(k % 4) * 32;  // 32 bytes = 16 dims into the row
-              umma(tS, smem_desc(q_addr + (k / 4) * (kPrefixRows * 128) + off, 16, 1024),
-                   smem_desc(k_addr + (k / 4) * kBlock + off, 16, 1024), kIdescQK, k > 0);
-            }
-            commit(blk_bar(X, 0, b));  // s_full
-            next_qk = j + 1;
-            progress = true;
-          }
-        }
-        if (progress) {
-          idle_since = 0;
-        } else {  // nothing ready: give up after the same bound as every other wait
-          const unsigned long long now =
-              __shfl_sync(0xffffffffu, dev::global_timer_ns(), 0);
-          if (idle_since == 0) {
-            idle_since = now;
-          } else if (now - idle_since > dev::kWaitTimeoutNs) {
-            aborted = true;
-            if (lane == 0) atomicOr(p.err, 2);
-          }
-        }
+        for (int k = 0; k < kTok / 16; ++k)  // 16 tokens (8 columns of P) per MMA
+          umma_ts(tO, tP + k * 8, smem_desc(v_addr + k * 16 * 128, kHalf, 1024), kIdescPV,
+                  j > 0 || k > 0);
+        commit(blk_bar(X, 2, b));  // pv_done
+        commit(&v_empty[s]);
+        if (j + 2 < tiles) qk(j + 2);
+        aborted = __any_sync(0xffffffffu, aborted);
       }
       commit(&o_done[X]);
+      // TMEM is freed only after this block's last MMA completed
+      if (!dev::mbar_wait_bounded(dev::smem_addr(&o_done[X]), 0u) && lane == 0) atomicOr(p.err, 2);
     }
   } else if (warp / 4 < nblk) {
     // ---------------------------------------------------------------- softmax
@@ -354,11 +371,10 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     const int4 sy = *reinterpret_cast<const int4*>(p.segments + 8 * (item_a + X * pp.chunks) + 4);
     const int row0 = sx.x, row_count = sy.x, out_item = sy.y;
     const uint32_t lane_off = (uint32_t)(32 * (warp % 4)) << 16;
-    const uint32_t tS0 = tmem + X * 128, tO = tmem + 256 + X * 128;
+    const uint32_t tS0 = tmem + X * 128 + lane_off, tO = tmem + 256 + X * 128 + lane_off;
     uint64_t* s_full = blk_bar(X, 0, 0);
-    uint64_t* s_free = blk_bar(X, 1, 0);
-    uint64_t* p_full = blk_bar(X, 2, 0);
-    uint64_t* p_free = blk_bar(X, 3, 0);
+    uint64_t* p_full = blk_bar(X, 1, 0);
+    uint64_t* pv_done = blk_bar(X, 2, 0);
     // Q row into the swizzled A tile: granule c8 (8 elements) of row r lands
     // in half c8 / 8 at granule (c8 % 8) ^ (r % 8)
     {
@@ -381,6 +397,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       __syncwarp();
       if (lane == 0) dev::mbar_arrive(dev::smem_addr(q_ready));
     }
+    const float scale = pp.q_scale;  // log2-domain score scale (> 0)
     float m_ref = -INFINITY, d = 0.f;
     for (int j = 0; j < tiles; ++j) {
       const int b = j & 1;
@@ -389,69 +406,68 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       float s[kTok];
       {
         float lo[32], hi[32];
-        ld32(tS0 + lane_off + b * kTok, lo);
-        ld32(tS0 + lane_off + b * kTok + 32, hi);
+        ld32(tS0 + b * kTok, lo);
+        ld32(tS0 + b * kTok + 32, hi);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           s[i] = lo[i];
           s[32 + i] = hi[i];
         }
       }
-      fence_before();
-      __syncwarp();
-      if (lane == 0) dev::mbar_arrive(dev::smem_addr(&s_free[b]));
       const int valid = min(kTok, (npg - j * kPages) * kPageSize);
-      float mt = -INFINITY;
+      if (valid < kTok) {  // last tile of a ragged chunk
 #pragma unroll
-      for (int i = 0; i < kTok; ++i) {
-        s[i] = i < valid ? s[i] * pp.q_scale : -INFINITY;
-        mt = fmaxf(mt, s[i]);
+        for (int i = 0; i < kTok; ++i)
+          if (i >= valid) s[i] = -INFINITY;
       }
+      // row maximum of the raw scores, eight independent chains
+      float m8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m8[k] = s[k];
+#pragma unroll
+      for (int i = 8; i < kTok; ++i) m8[i % 8] = fmaxf(m8[i % 8], s[i]);
+      const float mt =
+          fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * scale;
       // re-reference the row only when its maximum rose by more than 2^8
       const bool rebase = mt > m_ref + kRescaleAbove;
       const float m_new = rebase ? mt : m_ref;
       const float alpha = m_ref == -INFINITY ? 0.f : dev::fast_exp2(m_ref - m_new);
       if (j >= 1 && __any_sync(0xffffffffu, rebase)) {
-        // O holds the tiles before j: wait for P.V of tile j-1, then scale
-        dev::mbar_wait(dev::smem_addr(&p_free[(j - 1) & 1]), (uint32_t)(((j - 1) >> 1) & 1),
+        // O holds the tiles before j: wait for P V of tile j-1, then scale
+        dev::mbar_wait(dev::smem_addr(&pv_done[(j - 1) & 1]), (uint32_t)(((j - 1) >> 1) & 1),
                        aborted, p.err);
         fence_after();
         const float f = rebase ? alpha : 1.f;
 #pragma unroll
         for (int cc = 0; cc < kD / 32; ++cc) {
           float v[32];
-          ld32(tO + lane_off + cc * 32, v);
+          ld32(tO + cc * 32, v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= f;
-          st32(tO + lane_off + cc * 32, v);
+          st32(tO + cc * 32, v);
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
       if (rebase) {
         d *= alpha;
         m_ref = m_new;
       }
       // P row: weights rounded to the MMA type, sums from the rounded values
+      const float neg_m = -m_ref;
       uint32_t pk[kTok / 2];
+      float d4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < kTok / 2; ++i) {
-        const float a0 = dev::fast_exp2(s[2 * i] - m_ref), a1 = dev::fast_exp2(s[2 * i + 1] - m_ref);
+        const float a0 = dev::fast_exp2(fmaf(s[2 * i], scale, neg_m));
+        const float a1 = dev::fast_exp2(fmaf(s[2 * i + 1], scale, neg_m));
         pk[i] = mma::pack2(a0, a1, kBf16);
         const float2 back = mma::unpack2(pk[i], kBf16);
-        d += back.x + back.y;
+        d4[i % 4] += back.x + back.y;
       }
-      if (j >= 2)  // P buffer b was read by P.V of tile j-2
-        dev::mbar_wait(dev::smem_addr(&p_free[b]), (uint32_t)(((j - 2) >> 1) & 1), aborted,
-                       p.err);
-      const uint32_t prow = sbase + kOffP + (2 * X + b) * kPBytes + r * 128;
-#pragma unroll
-      for (int g8 = 0; g8 < kTok / 8; ++g8) {
-        const uint32_t a = prow + (uint32_t)((g8 ^ (r & 7)) * 16);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[4 * g8]),
-                     "r"(pk[4 * g8 + 1]), "r"(pk[4 * g8 + 2]), "r"(pk[4 * g8 + 3])
-                     : "memory");
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      d += (d4[0] + d4[1]) + (d4[2] + d4[3]);
+      // P over the first 32 columns of the score buffer it came from
+      st32u(tS0 + b * kTok, pk);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       fence_before();
       __syncwarp();
       if (lane == 0) dev::mbar_arrive(dev::smem_addr(&p_full[b]));
@@ -465,7 +481,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     for (int cc = 0; cc < kD / 32; ++cc) {
       float v[32];
       if (tiles > 0) {
-        ld32(tO + lane_off + cc * 32, v);  // every lane of the warp takes part
+        ld32(tO + cc * 32, v);  // every lane of the warp takes part
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.f;  // no tile: O was never written

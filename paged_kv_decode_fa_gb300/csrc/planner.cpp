@@ -1,15 +1,18 @@
 // Host planner: balanced split of the KV axis over a persistent grid.
 //
 // The decode work of a batch is the sequence of units (request, kv head) in
-// request-major order, unit (i, h) costing the np_i pages of request i.
-// Laid end to end, the units form one stream of total T = num_kv_heads *
-// sum_i np_i pages.  The planner fixes the grid size N (at most the number of
-// CTAs resident at once, and no more than T / min_pages_per_cta) and gives CTA
-// c the stream positions [c*q, (c+1)*q) with q = ceil(T / N).  A unit that a
-// cut falls inside is split at that page boundary; each piece becomes a
-// segment that writes a partial (o, lse) state into its own slot, and a merge
-// unit records which slots to combine.  Every CTA therefore streams the same
-// number of pages (+-1) whatever the mix of context lengths, which is the
+// request-major order, unit (i, h) costing the np_i pages of request i plus
+// a fixed c0 = kSegmentCostPages for the segment's own overhead (0 for an
+// empty unit).  Laid end to end, the units form one stream of total
+// C = T + c0 * (non-empty units), T = num_kv_heads * sum_i np_i pages.  The
+// planner fixes the grid size N (at most the number of CTAs resident at once,
+// and no more than T / min_pages_per_cta) and gives CTA c the stream positions
+// [c*q, (c+1)*q) with q = ceil(C / N); a page belongs to the CTA whose range
+// holds its position.  A unit that a cut falls inside is split at that page
+// boundary; each piece becomes a segment that writes a partial (o, lse) state
+// into its own slot, and a merge unit records which slots to combine.  Every
+// CTA therefore carries the same cost (+-1) whatever the mix of context
+// lengths, which is the
 // load-balancing duty the page "FlashDecoding + FlashInfer" assigns to
 // FlashInfer's plan step ("What FlashInfer is", item 3), and a long request
 // is spread over as many CTAs as its length needs, which is the split-KV
@@ -61,9 +64,17 @@ int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
   // enough of them to give every CTA a few chunks.
   int64_t pool = (int64_t)(pool_fraction * (double)T);
   if (pool < n * kPoolMinPages * 2) pool = 0;
-  const int64_t S = T - pool;  // static positions [0, S)
+  // per-segment cost: without a pool, and only while a quota stays above
+  // twice the cost
+  int64_t busy_units = 0;
+  for (int i = 0; i < batch; ++i)
+    if (indptr[i + 1] > indptr[i]) busy_units += num_kv_heads;
+  int64_t c0 = pool == 0 ? kSegmentCostPages : 0;
+  if (c0 > 0 && (T + c0 * busy_units + n - 1) / n <= 2 * c0) c0 = 0;
+  const int64_t C = T + c0 * busy_units;  // stream length in cost positions
+  const int64_t S = C - pool;             // static positions [0, S)
   const int64_t quota = S > 0 ? (S + n - 1) / n : 1;
-  if (pool == 0 && T > 0) n = (T + quota - 1) / quota;  // no CTA left without pages
+  if (pool == 0 && T > 0) n = (C + quota - 1) / quota;  // no CTA left without pages
   const int num_ctas = (int)n;
 
   // Pool chunk ends (absolute stream positions): tier t cuts n chunks of
@@ -104,7 +115,8 @@ int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
     const int64_t np = (int64_t)pe - pb;
     const int64_t len = np > 0 ? (np - 1) * page_size + last_page_len[i] : 0;
     for (int h = 0; h < num_kv_heads; ++h) {
-      const int64_t start = pos, end = pos + np;
+      // the unit's pages sit at [start, end), after its fixed cost
+      const int64_t start = pos + (np > 0 ? c0 : 0), end = start + np;
       pos = end;
       while (start >= cut && cta < num_ctas - 1) {
         ++cta;

@@ -33,6 +33,13 @@ static_assert(sizeof(MergeUnit) == 16, "MergeUnit must stay 16 bytes");
 constexpr int kPoolTiers = 4;
 constexpr int kPoolMinPages = 2;
 
+// Fixed cost of a segment in the balanced plan, in pages: loading q, filling
+// the ring and writing the partial state cost a CTA about as long as
+// streaming two pages, so a CTA whose quota holds many short requests gets
+// fewer pages.  Applied only without a pool and when a quota exceeds twice
+// this cost (every CTA then still holds a page).
+constexpr int kSegmentCostPages = 2;
+
 // Upper bound of the cuts a plan makes into (request, kv head) units for a
 // grid of n CTAs: n - 1 quota boundaries, the pool's start and at most
 // (kPoolTiers + 2) * n chunk boundaries.  Segments <= units + cuts and

@@ -24,6 +24,30 @@ def expand(seg):
 
 
 POOL_TIERS, POOL_MIN = 4, 2   # the planner's pool schedule
+SEG_COST = 2                  # fixed cost of a segment, in pages (no pool)
+
+
+def expected_pages_per_cta(indptr, Hkv, max_ctas, min_pages, pool_pages, n_ctas):
+    """Pages of the static part each CTA should hold: the stream of units
+    (request-major, then kv head), each a fixed cost followed by its pages,
+    cut into equal quotas of cost positions."""
+    np_req = np.diff(np.asarray(indptr, np.int64))
+    T = int(np_req.sum()) * Hkv
+    n0 = max(1, min(max_ctas, -(-T // min_pages)))
+    busy = int((np_req > 0).sum()) * Hkv
+    c0 = SEG_COST if pool_pages == 0 else 0
+    if c0 and -(-(T + c0 * busy) // n0) <= 2 * c0:
+        c0 = 0
+    C = T + c0 * busy
+    S = C - pool_pages
+    quota = -(-S // n0)
+    units = np.repeat(np_req, Hkv)
+    length = units + c0 * (units > 0)
+    first = np.cumsum(length) - units          # position of each unit's first page
+    pos = np.repeat(first, units) + (np.arange(int(units.sum())) - np.repeat(np.cumsum(units) - units, units))
+    pos = pos[pos < S]
+    owner = np.minimum(pos // quota, n_ctas - 1)
+    return np.bincount(owner, minlength=n_ctas), C, quota
 
 
 def check_work(lib, indptr, last, Hkv, max_ctas, min_pages=8, P=16, pool=0.0):
@@ -54,13 +78,15 @@ def check_work(lib, indptr, last, Hkv, max_ctas, min_pages=8, P=16, pool=0.0):
     if pool_pages == 0:
         assert len(pooled) == 0
     if T:
-        quota = -(-S // n_ctas)
         assert n_ctas <= -(-T // min_pages)
-        # every CTA holds a full quota until the static part runs out
-        want = np.minimum(quota, np.maximum(0, S - quota * np.arange(n_ctas)))
+        # every CTA holds the pages of one quota of cost positions, the last
+        # CTA the rest
+        want, C, quota = expected_pages_per_cta(indptr, Hkv, max_ctas, min_pages, pool_pages,
+                                                n_ctas)
         np.testing.assert_array_equal(pages, want)
         if pool_pages == 0:
-            assert pages[-1] > 0               # no CTA left without pages
+            assert n_ctas == -(-C // quota)
+            assert np.all(pages > 0)           # no CTA left without pages
     if pool_pages:
         # the pool is the end of the stream (request-major, then kv head, then
         # page) and its chunks are no longer than the first tier's
