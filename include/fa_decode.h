@@ -396,7 +396,12 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
 
 /* q [batch, num_qo_heads, head_dim], o likewise, lse [batch, num_qo_heads]
  * (may be NULL); paged_kv and num_pages as fa_decode_run.  Enqueues the
- * suffix decode, the prefix kernel and the combine kernel on cuda_stream. */
+ * suffix decode, the prefix kernel and the combine kernel on cuda_stream;
+ * the prefix kernel goes on a stream of the plan's own, forked from
+ * cuda_stream before the suffix decode and joined before the combine, so
+ * that it runs alongside the decode (FADECODE_CASCADE_OVERLAP=0 at plan
+ * time, or timing events set, keep all three in order on cuda_stream).  The
+ * call is capturable into a CUDA graph either way. */
 int fa_cascade_run(fa_cascade_plan_t plan, const void* q, const void* paged_kv,
                    int64_t num_pages, float sm_scale, void* o, float* lse,
                    void* cuda_stream);
@@ -407,7 +412,8 @@ int fa_cascade_plan_destroy(fa_cascade_plan_t plan);
 int fa_cascade_check(fa_cascade_plan_t plan, void* cuda_stream, int* flags);
 
 /* As fa_decode_set_timing_events, around the prefix kernel of later
- * fa_cascade_run calls (the events are recorded on their stream). */
+ * fa_cascade_run calls (the events are recorded on their stream, and those
+ * calls run the prefix kernel alone, after the suffix decode). */
 int fa_cascade_set_timing_events(fa_cascade_plan_t plan, void* ev_before,
                                  void* ev_after);
 

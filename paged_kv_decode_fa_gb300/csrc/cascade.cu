@@ -30,6 +30,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -48,6 +49,8 @@ struct PrefixParams {
   int row_blocks;       // 128-row blocks per kv head
   int pair_blocks;      // pairs of row blocks per kv head (tcgen05 kernel)
   int chunks;           // prefix chunks
+  int rows;             // query rows per kv head (batch x group)
+  int prefix_pages;     // pages of the shared prefix
 };
 
 struct CombineParams {
@@ -455,6 +458,7 @@ CascadeLayout cascade_layout(size_t suffix_ws, int64_t items, int batch, int Hq,
 struct fa_cascade_plan_s {
   fa_decode_plan_t suffix = nullptr;
   int batch = 0, hq = 0, hkv = 0, d = 0, group = 0, row_blocks = 0, chunks = 0, items = 0;
+  int prefix_pages = 0;
   int grid = 0;  // prefix CTAs: one per item, or per item pair on tcgen05
   fa_dtype dtype = FA_DTYPE_BF16;
   const int32_t* prefix_indices = nullptr;
@@ -465,7 +469,39 @@ struct fa_cascade_plan_s {
   const void* map_base = nullptr;
   int64_t map_pages = -1;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;  // around the prefix kernel
+  // The prefix kernel runs on a side stream, forked before and joined after
+  // the suffix decode, so that its CTAs take each SM as the decode's CTAs
+  // leave it (null: both on the caller's stream).  The stream is the
+  // device's (shared by all plans, made once); the events are the plan's.
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  ~fa_cascade_plan_s() {
+    if (ev_fork) cudaEventDestroy(ev_fork);
+    if (ev_join) cudaEventDestroy(ev_join);
+  }
 };
+
+namespace {
+// FADECODE_CASCADE_OVERLAP=0 keeps the two passes in order on one stream.
+bool cascade_overlap() {
+  const char* v = std::getenv("FADECODE_CASCADE_OVERLAP");
+  return !(v && v[0] == '0');
+}
+
+// One non-blocking stream per device for the prefix pass, created on first
+// use and kept for the life of the process.
+cudaStream_t device_side_stream(int dev) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static cudaStream_t streams[kMaxDevices] = {};
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) !=
+                           cudaSuccess)
+    streams[dev] = nullptr;
+  return streams[dev];
+}
+}  // namespace
 
 extern "C" {
 
@@ -515,6 +551,13 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
 
   fa_cascade_plan_s* plan = new (std::nothrow) fa_cascade_plan_s();
   if (!plan) return FA_ERR_INVALID_ARG;
+  if (cascade_overlap() &&
+      (!(plan->side = device_side_stream(dev)) ||
+       cudaEventCreateWithFlags(&plan->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+       cudaEventCreateWithFlags(&plan->ev_join, cudaEventDisableTiming) != cudaSuccess)) {
+    delete plan;
+    return FA_ERR_CUDA;
+  }
   plan->batch = batch;
   plan->hq = num_qo_heads;
   plan->hkv = num_kv_heads;
@@ -547,6 +590,7 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
     if (base * c > 8 * slots) break;
   }
   plan->chunks = chunks;
+  plan->prefix_pages = num_prefix_pages;
   plan->items = (int)((int64_t)num_kv_heads * plan->row_blocks * chunks);
   plan->grid = (int)(base * chunks);
   plan->L = cascade_layout(sw, plan->items, batch, num_qo_heads, head_dim);
@@ -565,6 +609,7 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
   }
   // prefix work items in the decode segment format the producer reads:
   // {row_begin, kv_head, page_begin, page_end, row_count, item, 0, 0}
+  // (the tcgen05 kernel derives the same fields from its block index)
   std::vector<uint8_t> meta(plan->L.meta_bytes, 0);
   int32_t* items = reinterpret_cast<int32_t*>(meta.data() + (plan->L.off_items - plan->L.off_err));
   int32_t* cta = reinterpret_cast<int32_t*>(meta.data() + (plan->L.off_cta - plan->L.off_err));
@@ -601,6 +646,13 @@ int fa_cascade_run(fa_cascade_plan_t plan, const void* q, const void* paged_kv,
   uint8_t* ws = plan->ws;
   void* so = ws + plan->L.off_so;
   float* slse = reinterpret_cast<float*>(ws + plan->L.off_slse);
+  const bool timed = plan->ev_before && plan->ev_after;
+  // a timed run keeps the prefix kernel alone on the GPU
+  const bool fork = plan->side && !timed;
+  cudaStream_t pst = fork ? plan->side : st;
+  if (fork && (cudaEventRecord(plan->ev_fork, st) != cudaSuccess ||
+               cudaStreamWaitEvent(plan->side, plan->ev_fork, 0) != cudaSuccess))
+    return FA_ERR_CUDA;
   // 1. each request's own pages
   int rc = fa_decode_run(plan->suffix, q, paged_kv, num_pages, sm_scale, 1.f, 1.f, so, slse,
                          cuda_stream);
@@ -633,13 +685,17 @@ int fa_cascade_run(fa_cascade_plan_t plan, const void* q, const void* paged_kv,
   pp.row_blocks = plan->row_blocks;
   pp.pair_blocks = (plan->row_blocks + 1) / 2;
   pp.chunks = plan->chunks;
+  pp.rows = plan->batch * plan->group;
+  pp.prefix_pages = plan->prefix_pages;
   void* args[3] = {&plan->map, &prm, &pp};
-  const bool timed = plan->ev_before && plan->ev_after;
   if (timed && cudaEventRecord(plan->ev_before, st) != cudaSuccess) return FA_ERR_CUDA;
   if (cudaLaunchKernel(plan->k.prefix, dim3(plan->grid), dim3(plan->k.threads), args,
-                       (size_t)plan->k.smem, st) != cudaSuccess)
+                       (size_t)plan->k.smem, pst) != cudaSuccess)
     return FA_ERR_CUDA;
   if (timed && cudaEventRecord(plan->ev_after, st) != cudaSuccess) return FA_ERR_CUDA;
+  if (fork && (cudaEventRecord(plan->ev_join, plan->side) != cudaSuccess ||
+               cudaStreamWaitEvent(st, plan->ev_join, 0) != cudaSuccess))
+    return FA_ERR_CUDA;
   // 3. fold prefix chunks and suffix
   fadecode::CombineParams c;
   c.part_o = pp.part_o;

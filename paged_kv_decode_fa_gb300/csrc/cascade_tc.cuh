@@ -71,6 +71,8 @@ static_assert(32 % kPages == 0, "a warp's page-id load covers whole tiles");
 static_assert(kOffK % 1024 == 0 && kSlotBytes % 1024 == 0 && kOffV % 1024 == 0,
               "swizzled operands need 1024-byte alignment");
 static_assert(kSmem + 1024 <= 227 * 1024, "shared memory per CTA");
+static_assert(256 * (kD * 4 + 16) <= 2 * kSlots * kSlotBytes,
+              "the K/V ring holds the output rows of both blocks");
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   // tcgen05 shared-memory matrix descriptor: start, leading and stride byte
@@ -162,6 +164,33 @@ __device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
       : "memory");
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+
+// Two fp32 lanes in one 64-bit register, for the paired add / fma
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+  return v;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // O += P V with P (M x K, K-major, packed pairs per 32-bit column) in TMEM
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
                                         uint32_t idesc, bool accumulate) {
@@ -219,10 +248,49 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   const int h_kv = pair / pp.pair_blocks, rbp = pair % pp.pair_blocks;
   const int item_a = (h_kv * pp.row_blocks + 2 * rbp) * pp.chunks + c;
   const int nblk = (2 * rbp + 1 < pp.row_blocks) ? 2 : 1;
-  const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * item_a);
-  const int kvh = sa.y, pb = sa.z, npg = sa.w - sa.z;
+  // the plan's work items, derived here instead of read: chunk c holds
+  // prefix pages [pb, pb + npg)
+  const int kvh = h_kv;
+  const int pb = (int)((int64_t)pp.prefix_pages * c / pp.chunks);
+  const int npg = (int)((int64_t)pp.prefix_pages * (c + 1) / pp.chunks) - pb;
   const int tiles = (npg + kPages - 1) / kPages;
   const uint32_t sbase = dev::smem_addr(smem);
+
+  // Loads that need no shared memory go out before the CTA-wide barrier
+  // (they overlap the barrier set-up and the TMEM allocation): the TMA
+  // warps' first window of page ids, the softmax threads' query rows.
+  const int kv = warp == 11 ? 1 : 0;  // TMA warps: 8 loads K, 11 loads V
+  auto load_ids = [&](int first) -> int {
+    const int pos = first + lane;
+    int id = -1;
+    if (pos < npg) {
+      id = __ldg(p.indices + pb + pos);
+      if (id < 0 || (int64_t)id >= p.num_pages) {
+        if (kv == 0) atomicOr(p.err, 1);
+        id = -1;
+      }
+    }
+    return id;
+  };
+  int ids = 0;
+  if (warp == 8 || warp == 11) ids = load_ids(0);
+  const int X = (warp / 4) & 1;       // softmax: block of this warpgroup
+  const int r = threadIdx.x % 128;    // softmax: query row of the block = TMEM lane
+  int row0 = 0, row_count = 0, out_item = 0;
+  uint4 qv[kD / 8];
+  if (warp < 8 && X < nblk) {
+    row0 = (2 * rbp + X) * kPrefixRows;
+    row_count = min(kPrefixRows, pp.rows - row0);
+    out_item = item_a + X * pp.chunks;
+    const int G = pp.group;
+    const int rho = row0 + r;
+    const QT* qrow = static_cast<const QT*>(pp.q) +
+                     ((size_t)(rho / G) * p.num_qo_heads + (size_t)kvh * G + rho % G) * kD;
+#pragma unroll
+    for (int c8 = 0; c8 < kD / 8; ++c8)
+      qv[c8] = r < row_count ? __ldg(reinterpret_cast<const uint4*>(qrow + c8 * 8))
+                             : make_uint4(0u, 0u, 0u, 0u);
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
@@ -261,22 +329,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     // Warp 8 fills the K ring, warp 11 the V ring.  Each lane holds one page
     // id of a 32-page window (eight tiles); lane 0 waits for ring slots and
     // issues the copies.
-    const int kv = warp == 8 ? 0 : 1;
     if (lane == 0) dev::prefetch_tensormap(&kv_map);
     const uint64_t policy = dev::evict_first_policy();
     const int oob = (int)(2 * p.num_pages);  // beyond the last page: zero fill
-    auto load_ids = [&](int first) -> int {
-      const int pos = first + lane;
-      int id = -1;
-      if (pos < npg) {
-        id = __ldg(p.indices + pb + pos);
-        if (id < 0 || (int64_t)id >= p.num_pages) {
-          if (kv == 0) atomicOr(p.err, 1);
-          id = -1;
-        }
-      }
-      return id;
-    };
     auto issue = [&](int t, int ids, uint64_t* full, uint64_t* empty, uint32_t ring, int kv) {
       int c3[kPages];
 #pragma unroll
@@ -303,9 +358,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     uint64_t* full = kv ? v_full : k_full;
     uint64_t* empty = kv ? v_empty : k_empty;
     const uint32_t ring = sbase + (kv ? kOffV : kOffK);
-    int ids = 0;
     for (int t = 0; t < tiles; ++t) {
-      if ((t * kPages) % 32 == 0) ids = load_ids(t * kPages);
+      if (t > 0 && (t * kPages) % 32 == 0) ids = load_ids(t * kPages);
       issue(t, ids, full, empty, ring, kv);
     }
     // no copy may still be landing when the CTA exits
@@ -365,11 +419,6 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     }
   } else if (warp / 4 < nblk) {
     // ---------------------------------------------------------------- softmax
-    const int X = warp / 4;                 // block of this warpgroup
-    const int r = threadIdx.x % 128;        // query row of the block = TMEM lane
-    const int4 sx = *reinterpret_cast<const int4*>(p.segments + 8 * (item_a + X * pp.chunks));
-    const int4 sy = *reinterpret_cast<const int4*>(p.segments + 8 * (item_a + X * pp.chunks) + 4);
-    const int row0 = sx.x, row_count = sy.x, out_item = sy.y;
     const uint32_t lane_off = (uint32_t)(32 * (warp % 4)) << 16;
     const uint32_t tS0 = tmem + X * 128 + lane_off, tO = tmem + 256 + X * 128 + lane_off;
     uint64_t* s_full = blk_bar(X, 0, 0);
@@ -378,15 +427,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     // Q row into the swizzled A tile: granule c8 (8 elements) of row r lands
     // in half c8 / 8 at granule (c8 % 8) ^ (r % 8)
     {
-      const int G = pp.group;
-      const int rho = row0 + r;
-      const bool live = r < row_count;
-      const QT* qrow = static_cast<const QT*>(pp.q) +
-                       ((size_t)(rho / G) * p.num_qo_heads + (size_t)kvh * G + rho % G) * kD;
 #pragma unroll
       for (int c8 = 0; c8 < kD / 8; ++c8) {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (live) v = __ldg(reinterpret_cast<const uint4*>(qrow + c8 * 8));
+        const uint4 v = qv[c8];
         const uint32_t a = sbase + kOffQ + X * kQBytes + (c8 / 8) * (kPrefixRows * 128) +
                            r * 128 + (uint32_t)(((c8 % 8) ^ (r & 7)) * 16);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
@@ -420,15 +463,16 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         for (int i = 0; i < kTok; ++i)
           if (i >= valid) s[i] = -INFINITY;
       }
-      // row maximum of the raw scores, eight independent chains
-      float m8[8];
+      // row maximum of the raw scores: four chains of three-input maxima
+      float m4[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) m8[k] = s[k];
+      for (int k = 0; k < 4; ++k) {
+        float m = s[16 * k];
 #pragma unroll
-      for (int i = 8; i < kTok; ++i) m8[i % 8] = fmaxf(m8[i % 8], s[i]);
-      const float mt =
-          fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * scale;
+        for (int i = 1; i < 15; i += 2) m = max3(m, s[16 * k + i], s[16 * k + i + 1]);
+        m4[k] = fmaxf(m, s[16 * k + 15]);
+      }
+      const float mt = fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]) * scale;
       // re-reference the row only when its maximum rose by more than 2^8
       const bool rebase = mt > m_ref + kRescaleAbove;
       const float m_new = rebase ? mt : m_ref;
@@ -452,19 +496,25 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         d *= alpha;
         m_ref = m_new;
       }
-      // P row: weights rounded to the MMA type, sums from the rounded values
-      const float neg_m = -m_ref;
+      // P row: weights 2^(s * scale - m) for pairs of scores (paired fma),
+      // rounded to the MMA type for P V; the row sum takes the fp32 weights
+      // (paired adds, four accumulators)
+      const uint64_t scale2 = f2(scale, scale), neg_m2 = f2(-m_ref, -m_ref);
       uint32_t pk[kTok / 2];
-      float d4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // +0.0f in both lanes
 #pragma unroll
       for (int i = 0; i < kTok / 2; ++i) {
-        const float a0 = dev::fast_exp2(fmaf(s[2 * i], scale, neg_m));
-        const float a1 = dev::fast_exp2(fmaf(s[2 * i + 1], scale, neg_m));
+        float x0, x1;
+        f2_split(fma2(f2(s[2 * i], s[2 * i + 1]), scale2, neg_m2), x0, x1);
+        const float a0 = dev::fast_exp2(x0), a1 = dev::fast_exp2(x1);
         pk[i] = mma::pack2(a0, a1, kBf16);
-        const float2 back = mma::unpack2(pk[i], kBf16);
-        d4[i % 4] += back.x + back.y;
+        acc[i % 4] = add2(acc[i % 4], f2(a0, a1));
       }
-      d += (d4[0] + d4[1]) + (d4[2] + d4[3]);
+      {
+        float lo, hi;
+        f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), lo, hi);
+        d += lo + hi;
+      }
       // P over the first 32 columns of the score buffer it came from
       st32u(tS0 + b * kTok, pk);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -473,10 +523,16 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       if (lane == 0) dev::mbar_arrive(dev::smem_addr(&p_full[b]));
     }
     // ---- this row's partial state: o / d and log2-sum-exp
-    dev::mbar_wait(dev::smem_addr(&o_done[X]), 0u, aborted, p.err);
+    // Both blocks' MMAs are done once both o_done fired; from then on the
+    // K/V ring is idle and stages the rows: each thread writes its row of o
+    // (rows 528 bytes apart, so that a warp's 16-byte stores fall in distinct
+    // banks) and copies it out with one 512-byte bulk copy.
+    dev::mbar_wait(dev::smem_addr(&o_done[0]), 0u, aborted, p.err);
+    if (nblk > 1) dev::mbar_wait(dev::smem_addr(&o_done[1]), 0u, aborted, p.err);
     fence_after();
     const float inv = d > 0.f ? 1.f / d : 0.f;
-    float* dst = pp.part_o + ((size_t)out_item * kPrefixRows + r) * kD;
+    constexpr uint32_t kRowPitch = kD * 4 + 16;
+    const uint32_t srow = sbase + kOffK + (uint32_t)threadIdx.x * kRowPitch;
 #pragma unroll
     for (int cc = 0; cc < kD / 32; ++cc) {
       float v[32];
@@ -486,16 +542,25 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.f;  // no tile: O was never written
       }
-      if (r < row_count) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(dst + cc * 32 + i) =
-              make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
-      }
+      for (int i = 0; i < 32; i += 4)
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(srow + (cc * 32 + i) * 4),
+                     "f"(v[i] * inv), "f"(v[i + 1] * inv), "f"(v[i + 2] * inv),
+                     "f"(v[i + 3] * inv)
+                     : "memory");
     }
-    if (r < row_count)
+    if (r < row_count) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      float* dst = pp.part_o + ((size_t)out_item * kPrefixRows + r) * kD;
+      asm volatile(
+          "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\t"
+          "cp.async.bulk.commit_group;\n\t"
+          "cp.async.bulk.wait_group.read 0;" ::"l"(dst),
+          "r"(srow), "n"(kD * 4)
+          : "memory");
       pp.part_lse[(size_t)out_item * kPrefixRows + r] =
           d > 0.f ? m_ref + dev::fast_log2(d) : -INFINITY;
+    }
   }
   fence_before();
   __syncthreads();

@@ -449,6 +449,55 @@ def test_cascade_small(lib, cuda, monkeypatch, kernel, dtype, batch, hq, hkv, pr
     compare(o, lse, ref_o, ref_lse, TOL[dtype])
 
 
+def test_cascade_overlap_graph_and_timing(lib, cuda, monkeypatch):
+    """The prefix kernel on the plan's side stream (default), on the caller's
+    stream (FADECODE_CASCADE_OVERLAP=0), with timing events set (the kernel
+    alone) and replayed from a captured CUDA graph: the same kernels in every
+    arrangement, so the outputs agree bit for bit."""
+    rng = np.random.default_rng(5)
+    b = W.make_cascade_batch(prefix_pages=40, suffix_lengths=rng.integers(0, 300, size=24),
+                             num_qo_heads=16, num_kv_heads=4, head_dim=128,
+                             dtype=torch.bfloat16, seed=171, device=cuda)
+    pre, ip, idx, last = W.cascade_parts(b)
+    def make():
+        return lib.cascade_plan(pre, ip, idx, last, 16, 4, 128, 16, q_data_type=torch.bfloat16)
+    monkeypatch.setenv("FADECODE_CASCADE_OVERLAP", "0")
+    ref_o, ref_lse = make().run(b.q, b.paged_kv)
+    monkeypatch.delenv("FADECODE_CASCADE_OVERLAP")
+    p = make()
+    o = torch.empty_like(b.q)
+    lse = torch.empty((b.batch, 16), dtype=torch.float32, device=cuda)
+    p.run(b.q, b.paged_kv, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    ev1.record()
+    p.set_timing_events(ev0, ev1)
+    o.zero_()
+    p.run(b.q, b.paged_kv, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref_o) and ev0.elapsed_time(ev1) > 0
+    p.set_timing_events(None, None)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        p.run(b.q, b.paged_kv, out=o, lse=lse)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        p.run(b.q, b.paged_kv, out=o, lse=lse)
+    for _ in range(3):
+        o.zero_()
+        lse.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+    assert p.check() == 0
+    ref = oracle_decode(b)
+    compare(o, lse, ref[0], ref[1], TOL[torch.bfloat16])
+
+
 def test_cascade_rejects(lib, cuda):
     idx = torch.zeros(1, dtype=torch.int32, device=cuda)
     with pytest.raises(lib.FaError) as e:
