@@ -370,8 +370,10 @@ int fa_decode_static(const int32_t* indptr_host, const int32_t* indices_dev,
  * combination is the merge rule of page "FlashDecoding + FlashInfer",
  * section "FlashDecoding - the split-KV trick".  The result equals
  * fa_decode_run over each request's full page list (prefix pages, then its
- * own), but the prefix is read from HBM once per kv head and block of 128
- * query rows instead of once per request. */
+ * own), but the prefix is read from HBM once per kv head (per two blocks of
+ * 128 query rows) instead of once per request: the prefix pass is a dense
+ * contraction on the tcgen05 tensor cores (FADECODE_CASCADE=mma at plan time
+ * selects the earlier warp-level mma.sync kernel). */
 typedef struct fa_cascade_plan_s* fa_cascade_plan_t;
 
 /* Upper bound of the workspace fa_cascade_plan needs (current device). */
@@ -397,9 +399,9 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
 /* q [batch, num_qo_heads, head_dim], o likewise, lse [batch, num_qo_heads]
  * (may be NULL); paged_kv and num_pages as fa_decode_run.  Enqueues the
  * suffix decode, the prefix kernel and the combine kernel on cuda_stream;
- * the prefix kernel goes on a stream of the plan's own, forked from
- * cuda_stream before the suffix decode and joined before the combine, so
- * that it runs alongside the decode (FADECODE_CASCADE_OVERLAP=0 at plan
+ * the prefix kernel goes on a stream of the library's (one per device,
+ * shared by all plans), forked from cuda_stream before the suffix decode
+ * and joined before the combine, so that it runs alongside the decode (FADECODE_CASCADE_OVERLAP=0 at plan
  * time, or timing events set, keep all three in order on cuda_stream).  The
  * call is capturable into a CUDA graph either way. */
 int fa_cascade_run(fa_cascade_plan_t plan, const void* q, const void* paged_kv,

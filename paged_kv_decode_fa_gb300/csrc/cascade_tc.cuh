@@ -1,8 +1,8 @@
 // Cascade prefix attention on the fifth-generation tensor cores (tcgen05).
 //
-// The prefix pass is a real contraction: 128 query rows (the query heads of
-// every request that reads one kv head) against every token of the shared
-// prefix.  fa_prefix_kernel (cascade.cu) runs it on warp-level mma.sync,
+// The prefix pass is a real contraction: the query rows of one kv head (its
+// query heads in every request, 128 rows a block) against every token of the
+// shared prefix.  fa_prefix_kernel (cascade.cu) runs it on warp-level mma.sync,
 // where the legacy tensor pipe and nine warps per SM bound it far below the
 // GB300's tensor rate.  Here one CTA per SM works on one (kv head, prefix
 // chunk) and on two 128-row blocks of that kv head's query rows at once (A
@@ -35,7 +35,12 @@
 //    only when the maximum has grown by more than 2^8 - between rescales the
 //    weights stay below 256, far inside the bf16/f16 and fp32 ranges.  At the
 //    end it normalises O and writes the row's partial state (o,
-//    log2-sum-exp) for fa_cascade_combine_kernel.
+//    log2-sum-exp) for fa_cascade_combine_kernel: o staged in the then idle
+//    K/V ring and copied out with one bulk copy per row.
+//
+// The CTA's work item (kv head, chunk pages, rows) follows from its block
+// index and the plan's sizes, so the first global loads - the TMA warps' page
+// ids, the softmax threads' q rows - go out before the CTA-wide barrier.
 //
 // TMEM: all 512 columns - per block two score/P buffers of 64 columns and an
 // output accumulator of 128 (A: S [0, 128), O [256, 384); B: S [128, 256),

@@ -427,6 +427,7 @@ def run_cascade(lib, b):
     (40, 16, 4, 9),     # 160 rows per kv head: two row blocks
     (3, 16, 2, 1),      # group 8, a one-page prefix
     (20, 32, 4, 70),    # many tiles per chunk: TMEM score buffers and ring reused
+    (80, 16, 4, 9),     # 320 rows per kv head: a block pair and a lone third block
 ])
 def test_cascade_small(lib, cuda, monkeypatch, kernel, dtype, batch, hq, hkv, prefix_pages):
     """Cascade output equals attention over each request's full page list
