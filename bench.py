@@ -481,15 +481,10 @@ def bench_ours(args, world, rank, local):
         p.unified_max_fallbacks()  # clear the warm-up count
 
     launches_per_step = 1 + (1 if info["num_merge_units"] > 0 and not info["fused_merge"] else 0)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    # torch creates an event at its first record and only then reports
-    # elapsed times; the library re-records the same events around the
-    # decode kernel of each timed step.
-    for a, z in evs:
-        a.record(stream)
-        z.record(stream)
-    torch.cuda.synchronize(dev)
+    # The timed region: the production step back to back, nothing recorded
+    # between launches (an event pair around every launch adds its own
+    # records and keeps the next launch from being prepared while the
+    # kernel drains: about 4 us per step).
     clocks = ClockSampler(local).start()
     time.sleep(0.3)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -497,21 +492,40 @@ def bench_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     start.record(stream)
-    for i in range(args.steps):
-        p.set_timing_events(*evs[i])
+    for _ in range(args.steps):
         run_step(p, b.q)
     end.record(stream)
     torch.cuda.synchronize(dev)
     t1 = time.perf_counter()
     barrier(world)
-    p.set_timing_events(None, None)
     clocks.stop()
     um_fallbacks = p.unified_max_fallbacks() if um_bound is not None else None
     elapsed_s = start.elapsed_time(end) / 1e3
     elapsed_s = max_over_ranks(elapsed_s, world, dev)
+    # The decode kernel alone: a second loop of the same length with the
+    # library recording events around the kernel of every step (torch
+    # creates an event at its first record, so each is recorded once first).
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, z in evs:
+        a.record(stream)
+        z.record(stream)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        p.set_timing_events(*evs[i])
+        run_step(p, b.q)
+    torch.cuda.synchronize(dev)
+    p.set_timing_events(None, None)
     kern_ms = [a.elapsed_time(z) for a, z in evs]
     kern_avg_s = statistics.mean(kern_ms) / 1e3
     kern_med_s = statistics.median(kern_ms) / 1e3
+    # the dominant kernel's average duration inside the timed region: the
+    # region's events over its launches when a step is that one launch, else
+    # the per-launch events of the second loop
+    if launches_per_step == 1:
+        kern_region_s, duration_from = elapsed_s / args.steps, "timed-region events / launches"
+    else:
+        kern_region_s, duration_from = kern_avg_s, "events around each decode launch"
 
     # End to end through the public API with host buffers.  Every step plans
     # the batch and decodes it with q, the page ids, o and lse in page-locked
@@ -569,7 +583,7 @@ def bench_ours(args, world, rank, local):
     peak, peak_kind = read_peaks()
     step_s = elapsed_s / args.steps
     value = whole_job_rate(world, b.batch * b.q_len, args.steps, elapsed_s)
-    achieved = alg / kern_avg_s / 1e9
+    achieved = alg / kern_region_s / 1e9
     traffic = profiled_traffic(args.workload) if args.max_requests is None else None
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -583,7 +597,8 @@ def bench_ours(args, world, rank, local):
         "hbm_frac_of_nominal_7900": alg / step_s / 1e9 / 7900.0,
         "peak_kind": peak_kind,
         "plan_ms": plan_ms,
-        "decode_kernel_us": {"mean": kern_avg_s * 1e6, "median": kern_med_s * 1e6},
+        "decode_kernel_us": {"mean": kern_avg_s * 1e6, "median": kern_med_s * 1e6,
+                             "measured": "events around each launch, second loop"},
         "plan": {k: info[k] for k in ("num_ctas", "ctas_per_sm", "num_segments",
                                       "num_merge_units", "num_partial_slots", "stages",
                                       "threads_per_cta", "smem_bytes_per_cta",
@@ -592,7 +607,8 @@ def bench_ours(args, world, rank, local):
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": ("fa_decode_mma_kernel" if info["tensor_cores"]
                                 else "fa_decode_split_kernel"),
-                     "algorithmic_bytes_per_launch": alg},
+                     "algorithmic_bytes_per_launch": alg,
+                     "duration_us": kern_region_s * 1e6, "duration_from": duration_from},
         "e2e": {"value": whole_job_rate(world, b.batch * b.q_len, e2e_steps, e2e_s), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "steps": e2e_steps,
