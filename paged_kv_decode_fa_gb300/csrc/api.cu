@@ -639,9 +639,20 @@ static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
   const bool timed = plan->ev_before && plan->ev_after;
   if (timed && cudaEventRecord(plan->ev_before, st) != cudaSuccess) return FA_ERR_CUDA;
   void* args[2] = {&mc.tmap, &prm};
-  if (cudaLaunchKernel(kern.func, dim3(plan->wl.num_ctas), dim3(kern.threads), args,
-                       (size_t)kern.smem_bytes, st) != cudaSuccess)
-    return FA_ERR_CUDA;
+  // A programmatic dependent launch: the kernel's CTAs may be placed while
+  // the previous kernel in the stream drains; they read nothing global
+  // before it has completed (griddepcontrol.wait).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan->wl.num_ctas);
+  cfg.blockDim = dim3(kern.threads);
+  cfg.dynamicSmemBytes = (size_t)kern.smem_bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelExC(&cfg, kern.func, args) != cudaSuccess) return FA_ERR_CUDA;
   if (timed && cudaEventRecord(plan->ev_after, st) != cudaSuccess) return FA_ERR_CUDA;
   if (!plan->fused_merge && !plan->wl.merge.empty()) {
     MergeParams mp;

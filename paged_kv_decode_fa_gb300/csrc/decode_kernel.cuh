@@ -91,6 +91,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Programmatic dependent launch: let the next grid in the stream begin
+// launching / wait until the grid this one depends on has completed and its
+// memory is visible (both no-ops for an ordinary launch).
+__device__ __forceinline__ void grid_dependency_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ unsigned long long global_timer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -776,8 +786,6 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int seg_begin = p.cta_offsets[blockIdx.x];
-  const int seg_end = p.cta_offsets[blockIdx.x + 1];
 
   SegQueue* queue = reinterpret_cast<SegQueue*>(smem + C::OFF_QUEUE);
   FoldList* folds = reinterpret_cast<FoldList*>(smem + C::OFF_FOLDS);
@@ -791,6 +799,13 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
     dev::fence_barrier_init();
   }
   __syncthreads();
+  // Launched as a programmatic dependent (fa_decode_run): the next launch
+  // may start placing its CTAs now, and nothing global is read before the
+  // grid this one depends on has completed.
+  dev::grid_dependency_launch();
+  dev::grid_dependency_wait();
+  const int seg_begin = p.cta_offsets[blockIdx.x];
+  const int seg_end = p.cta_offsets[blockIdx.x + 1];
 
   if (warp == NW) {
     produce_pages<S, C::STAGE_BYTES, 1, 0, C::STAGE_BYTES>(&kv_map, p, seg_begin, seg_end, ring,

@@ -199,8 +199,6 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int seg_begin = p.cta_offsets[blockIdx.x];
-  const int seg_end = p.cta_offsets[blockIdx.x + 1];
 
   SegQueue* queue = reinterpret_cast<SegQueue*>(smem + C::OFF_QUEUE);
   FoldList* folds = reinterpret_cast<FoldList*>(smem + C::OFF_FOLDS);
@@ -214,6 +212,13 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
     dev::fence_barrier_init();
   }
   __syncthreads();
+  // Launched as a programmatic dependent (fa_decode_run): the next launch
+  // may start placing its CTAs now, and nothing global is read before the
+  // grid this one depends on has completed.
+  dev::grid_dependency_launch();
+  dev::grid_dependency_wait();
+  const int seg_begin = p.cta_offsets[blockIdx.x];
+  const int seg_end = p.cta_offsets[blockIdx.x + 1];
 
   if (warp == NW) {
     produce_pages<S, C::STAGE_BYTES, SEGS, C::BOX_X, C::BOX_BYTES, TS>(
