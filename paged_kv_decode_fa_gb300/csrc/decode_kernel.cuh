@@ -334,6 +334,27 @@ __device__ __forceinline__ void seg_queue_init(SegQueue* q, int consumer_warps) 
   }
 }
 
+// Before a programmatic dependent launch's wait: the CTA's first segment
+// record (plan data) and, into L2, the page ids of its first 64 pages and
+// its q rows (data a preceding kernel may still be writing: a prefetch only
+// warms L2, where that kernel's writes land, so what is read after the wait
+// is current).  Run by the producer warp.
+__device__ __forceinline__ void prefetch_first_segment(const DecodeParams& p, int si, int lane) {
+  const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * si);
+  const int kvh = sa.y, pb = sa.z, pe = sa.w;
+  if (lane < 2 && pb + 32 * lane < pe) dev::prefetch_l2(p.indices + pb + 32 * lane);
+  if (p.q_row_bytes > 0) {
+    const int G = p.num_qo_heads / p.num_kv_heads;
+    const int lines = (G * p.q_row_bytes + 127) / 128;  // one query token's rows
+    for (int i = 0; i < p.q_len; ++i) {
+      const char* rows = static_cast<const char*>(p.q) +
+                         (((size_t)sa.x * p.q_len + i) * p.num_qo_heads + (size_t)kvh * G) *
+                             p.q_row_bytes;
+      for (int l = lane; l < lines; l += 32) dev::prefetch_l2(rows + (size_t)l * 128);
+    }
+  }
+}
+
 // Producer warp: walks the CTA's segments page by page, reads the page ids
 // through the index table (32 at a time) and issues, per page, BOXES 4-D TMA
 // tensor copies (box b starts at element b * BOX_X of a row and lands at
@@ -800,12 +821,15 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
   }
   __syncthreads();
   // Launched as a programmatic dependent (fa_decode_run): the next launch
-  // may start placing its CTAs now, and nothing global is read before the
-  // grid this one depends on has completed.
+  // may start placing its CTAs now.  Until the grid this one depends on has
+  // completed, the CTA reads only plan data (written by the plan's upload,
+  // a copy the launch is fully ordered after) and brings its first page ids
+  // and q rows into L2, the GPU's point of coherence; everything else waits.
   dev::grid_dependency_launch();
-  dev::grid_dependency_wait();
   const int seg_begin = p.cta_offsets[blockIdx.x];
   const int seg_end = p.cta_offsets[blockIdx.x + 1];
+  if (warp == NW && seg_begin < seg_end) prefetch_first_segment(p, seg_begin, lane);
+  dev::grid_dependency_wait();
 
   if (warp == NW) {
     produce_pages<S, C::STAGE_BYTES, 1, 0, C::STAGE_BYTES>(&kv_map, p, seg_begin, seg_end, ring,

@@ -213,12 +213,15 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
   }
   __syncthreads();
   // Launched as a programmatic dependent (fa_decode_run): the next launch
-  // may start placing its CTAs now, and nothing global is read before the
-  // grid this one depends on has completed.
+  // may start placing its CTAs now.  Until the grid this one depends on has
+  // completed, the CTA reads only plan data (written by the plan's upload,
+  // a copy the launch is fully ordered after) and brings its first page ids
+  // and q rows into L2, the GPU's point of coherence; everything else waits.
   dev::grid_dependency_launch();
-  dev::grid_dependency_wait();
   const int seg_begin = p.cta_offsets[blockIdx.x];
   const int seg_end = p.cta_offsets[blockIdx.x + 1];
+  if (warp == NW && seg_begin < seg_end) prefetch_first_segment(p, seg_begin, lane);
+  dev::grid_dependency_wait();
 
   if (warp == NW) {
     produce_pages<S, C::STAGE_BYTES, SEGS, C::BOX_X, C::BOX_BYTES, TS>(
