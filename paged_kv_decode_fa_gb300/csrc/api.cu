@@ -627,6 +627,8 @@ static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
   prm.num_kv_heads = plan->hkv;
   prm.q_len = plan->q_len;
   prm.q_row_bytes = D * dtype_size(plan->q_dtype);
+  prm.kv = paged_kv;
+  prm.kv_row_bytes = D * dtype_size(plan->kv_dtype);
   prm.q_scale = sm_scale * k_scale * kLog2e;
   prm.v_scale = v_scale;
   prm.max_bound = max_bound * kLog2e;

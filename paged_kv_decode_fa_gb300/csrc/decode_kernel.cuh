@@ -335,14 +335,28 @@ __device__ __forceinline__ void seg_queue_init(SegQueue* q, int consumer_warps) 
 }
 
 // Before a programmatic dependent launch's wait: the CTA's first segment
-// record (plan data) and, into L2, the page ids of its first 64 pages and
-// its q rows (data a preceding kernel may still be writing: a prefetch only
-// warms L2, where that kernel's writes land, so what is read after the wait
-// is current).  Run by the producer warp.
+// record (plan data) and, into L2, the page ids of its first 64 pages, the
+// K and V rows of its first two pages and its q rows - data a preceding
+// kernel may still be writing.  A prefetch only warms L2, where that
+// kernel's writes land, so what is read after the wait is current; the two
+// page ids are read past L1 (a stale id only wastes its prefetch).  Run by
+// the producer warp.
 __device__ __forceinline__ void prefetch_first_segment(const DecodeParams& p, int si, int lane) {
   const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * si);
   const int kvh = sa.y, pb = sa.z, pe = sa.w;
   if (lane < 2 && pb + 32 * lane < pe) dev::prefetch_l2(p.indices + pb + 32 * lane);
+  if (p.kv != nullptr) {
+    const int lines = (p.kv_row_bytes + 127) / 128;
+    const int kv = lane >> 4, t = lane & 15;  // one row of K or V per lane
+    for (int i = 0; i < 2 && pb + i < pe; ++i) {
+      const int id = __ldcg(p.indices + pb + i);
+      if (id < 0 || (int64_t)id >= p.num_pages) continue;
+      const char* row = static_cast<const char*>(p.kv) +
+                        ((((size_t)id * 2 + kv) * kPageSize + t) * p.num_kv_heads + kvh) *
+                            (size_t)p.kv_row_bytes;
+      for (int l = 0; l < lines; ++l) dev::prefetch_l2(row + (size_t)l * 128);
+    }
+  }
   if (p.q_row_bytes > 0) {
     const int G = p.num_qo_heads / p.num_kv_heads;
     const int lines = (G * p.q_row_bytes + 127) / 128;  // one query token's rows

@@ -31,6 +31,8 @@ struct DecodeParams {
   int num_kv_heads;
   int q_len;                   // query tokens per request (1 for plain decode)
   int q_row_bytes;             // head_dim * q element size (0: no q prefetch)
+  const void* kv;              // paged KV base (for L2 prefetches), or nullptr
+  int kv_row_bytes;            // head_dim * KV element size
   float q_scale;  // sm_scale * k_scale * log2(e), folded into q
   float v_scale;
   float max_bound;    // unified-max kernels: static reference of the logits, log2 units
