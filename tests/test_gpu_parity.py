@@ -255,6 +255,40 @@ def test_cuda_graph_capture(lib, cuda):
     assert p.check() == 0
 
 
+def test_dependent_launch_chain(lib, cuda):
+    """Decode launches are programmatic dependents of the kernel before them
+    in the stream.  Here each second launch decodes with q = the output of
+    the launch just before it (nothing in between, fresh q for the first
+    launch every round): it must read that q only once the first launch
+    has completed, so its result equals the oracle on the first launch's
+    actual output, round after round."""
+    import dataclasses
+    b = W.make_batch(batch_lengths=[3000, 17, 900, 5000, 64, 2048], num_qo_heads=16,
+                     num_kv_heads=4, head_dim=128, q_dtype=torch.bfloat16,
+                     kv_dtype=torch.bfloat16, seed=181, device=cuda)
+    p = lib.plan(b.indptr, b.indices, b.last_page_len, 16, 4, 128, 16,
+                 q_data_type=torch.bfloat16, kv_data_type=torch.bfloat16)
+    gen = torch.Generator(device=cuda).manual_seed(182)
+    rounds = 3
+    qs = [torch.randn(b.q.shape, generator=gen, device=cuda).to(torch.bfloat16) * 4
+          for _ in range(rounds)]
+    o1s = [torch.zeros_like(b.q) for _ in range(rounds)]
+    o2s = [torch.zeros_like(b.q) for _ in range(rounds)]
+    l1s = [torch.zeros(b.q.shape[:-1], device=cuda) for _ in range(rounds)]
+    l2s = [torch.zeros(b.q.shape[:-1], device=cuda) for _ in range(rounds)]
+    torch.cuda.synchronize()
+    for k in range(rounds):
+        p.run(qs[k], b.paged_kv, out=o1s[k], lse=l1s[k])
+        p.run(o1s[k], b.paged_kv, out=o2s[k], lse=l2s[k])
+    torch.cuda.synchronize()
+    assert p.check() == 0
+    for k in range(rounds):
+        ref1 = oracle_decode(dataclasses.replace(b, q=qs[k]))
+        ref2 = oracle_decode(dataclasses.replace(b, q=o1s[k]))
+        compare(o1s[k], l1s[k], ref1[0], ref1[1], TOL[torch.bfloat16])
+        compare(o2s[k], l2s[k], ref2[0], ref2[1], TOL[torch.bfloat16])
+
+
 @pytest.mark.parametrize("merge", ["fused", "kernel"])
 def test_deterministic_and_no_lse(lib, cuda, monkeypatch, merge):
     if merge == "kernel":
