@@ -117,18 +117,64 @@ def profiled_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 50 ms while running."""
+    """SM clock and clock-event-reason samples while running: read through
+    NVML (ctypes, read-only queries) every 2 ms, else from an nvidia-smi
+    stream every 50 ms."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits: sw power cap, hw slowdown, sw thermal, hw thermal
+    _BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+             "hw_thermal_slowdown": 0x40}
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.samples = []
         self.proc = None
         self.thread = None
+        self.stop_flag = threading.Event()
+        self.source = None
+
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+            return None
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mhz, mx, mask = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+
+        def read():
+            if (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) != 0 or
+                    lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) != 0 or
+                    reasons(h, ctypes.byref(mask)) != 0):
+                return None
+            flags = ["Active" if mask.value & b else "Not Active" for b in
+                     (self._BITS["hw_slowdown"], self._BITS["hw_thermal_slowdown"],
+                      self._BITS["sw_thermal_slowdown"], self._BITS["sw_power_cap"])]
+            return ", ".join([str(self.gpu), str(mhz.value), str(mx.value), "", ""] + flags)
+        return read if read() is not None else None
 
     def start(self):
+        try:
+            read = self._nvml()
+        except (OSError, AttributeError):
+            read = None
+        if read is not None:
+            self.source = "nvml, 2 ms"
+
+            def loop():
+                while not self.stop_flag.is_set():
+                    line = read()
+                    if line is not None:
+                        self.samples.append((time.perf_counter(), line))
+                    time.sleep(0.002)
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
@@ -137,6 +183,7 @@ class ClockSampler:
         except OSError:
             self.proc = None
             return self
+        self.source = "nvidia-smi, 50 ms"
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
         return self
@@ -146,12 +193,14 @@ class ClockSampler:
             self.samples.append((time.perf_counter(), line.strip()))
 
     def stop(self):
+        self.stop_flag.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread is not None:
             self.thread.join(timeout=2)
 
     def summary(self, t0: float, t1: float):
@@ -164,7 +213,10 @@ class ClockSampler:
                 rows.append((t, float(parts[1]), float(parts[2]), parts[5:9]))
             except ValueError:
                 continue
-        window = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        # samples inside the region (nvidia-smi's 50 ms stream: within one
+        # interval of it)
+        margin = 0.005 if self.source and self.source.startswith("nvml") else 0.05
+        window = [r for r in rows if t0 - margin <= r[0] <= t1 + margin]
         which = "timed"
         if not window:
             window, which = rows, "warmup+timed"
@@ -175,7 +227,7 @@ class ClockSampler:
                           if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[1] for r in window),
                 "sm_max_mhz": max(r[2] for r in window), "reasons": reasons,
-                "samples": len(window), "window": which}
+                "samples": len(window), "window": which, "source": self.source}
 
 
 def dist_setup(n_gpus: int):
