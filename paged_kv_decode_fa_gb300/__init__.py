@@ -156,8 +156,12 @@ def _stream_handle(stream) -> int | None:
 
 def _host_i32(t) -> np.ndarray:
     if isinstance(t, torch.Tensor):
+        if t.device.type == "cpu" and t.dtype == torch.int32 and t.is_contiguous():
+            return t.detach().numpy()  # no copy
         t = t.detach().to("cpu")
         return np.ascontiguousarray(t.numpy(), dtype=np.int32)
+    if isinstance(t, np.ndarray) and t.dtype == np.int32 and t.flags.c_contiguous:
+        return t
     return np.ascontiguousarray(np.asarray(t), dtype=np.int32)
 
 

@@ -475,10 +475,8 @@ struct fa_cascade_plan_s {
   // device's (shared by all plans, made once); the events are the plan's.
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
-  ~fa_cascade_plan_s() {
-    if (ev_fork) cudaEventDestroy(ev_fork);
-    if (ev_join) cudaEventDestroy(ev_join);
-  }
+  int device = 0;
+  ~fa_cascade_plan_s();
 };
 
 namespace {
@@ -486,6 +484,57 @@ namespace {
 bool cascade_overlap() {
   const char* v = std::getenv("FADECODE_CASCADE_OVERLAP");
   return !(v && v[0] == '0');
+}
+
+// Shared-memory attribute and occupancy of a prefix kernel, set and queried
+// once per kernel and device.
+int prefix_occupancy(const CascadeKernels& k, int dev) {
+  struct Entry {
+    const void* func;
+    int device, occ;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : cache)
+    if (e.func == k.prefix && e.device == dev) return e.occ;
+  int occ = 0;
+  if (cudaFuncSetAttribute(k.prefix, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.prefix, k.threads, k.smem) !=
+          cudaSuccess)
+    return 0;
+  cache.push_back(Entry{k.prefix, dev, occ});
+  return occ;
+}
+
+// Fork / join events of cascade plans: a free list per device, so that
+// planning every step creates none once warm.
+constexpr int kMaxEventDevices = 64;
+std::mutex g_event_mu;
+std::vector<cudaEvent_t> g_free_events[kMaxEventDevices];
+
+bool take_event(int dev, cudaEvent_t* ev) {
+  if (dev < 0 || dev >= kMaxEventDevices) return false;
+  {
+    std::lock_guard<std::mutex> lock(g_event_mu);
+    if (!g_free_events[dev].empty()) {
+      *ev = g_free_events[dev].back();
+      g_free_events[dev].pop_back();
+      return true;
+    }
+  }
+  return cudaEventCreateWithFlags(ev, cudaEventDisableTiming) == cudaSuccess;
+}
+
+void give_event(int dev, cudaEvent_t ev) {
+  if (!ev) return;
+  if (dev < 0 || dev >= kMaxEventDevices) {
+    cudaEventDestroy(ev);
+    return;
+  }
+  std::lock_guard<std::mutex> lock(g_event_mu);
+  g_free_events[dev].push_back(ev);
 }
 
 // One non-blocking stream per device for the prefix pass, created on first
@@ -542,19 +591,15 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
     return FA_ERR_CUDA;
   CascadeKernels k = q_dtype == FA_DTYPE_BF16 ? cascade_kernels<__nv_bfloat16>()
                                               : cascade_kernels<__half>();
-  int occ = 0;
-  if (cudaFuncSetAttribute(k.prefix, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem) !=
-          cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.prefix, k.threads, k.smem) !=
-          cudaSuccess || occ < 1)
-    return FA_ERR_CUDA;
+  const int occ = prefix_occupancy(k, dev);
+  if (occ < 1) return FA_ERR_CUDA;
 
   fa_cascade_plan_s* plan = new (std::nothrow) fa_cascade_plan_s();
   if (!plan) return FA_ERR_INVALID_ARG;
+  plan->device = dev;
   if (cascade_overlap() &&
-      (!(plan->side = device_side_stream(dev)) ||
-       cudaEventCreateWithFlags(&plan->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-       cudaEventCreateWithFlags(&plan->ev_join, cudaEventDisableTiming) != cudaSuccess)) {
+      (!(plan->side = device_side_stream(dev)) || !take_event(dev, &plan->ev_fork) ||
+       !take_event(dev, &plan->ev_join))) {
     delete plan;
     return FA_ERR_CUDA;
   }
@@ -716,6 +761,15 @@ int fa_cascade_run(fa_cascade_plan_t plan, const void* q, const void* paged_kv,
     return FA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+
+}  // extern "C"
+
+fa_cascade_plan_s::~fa_cascade_plan_s() {
+  give_event(device, ev_fork);
+  give_event(device, ev_join);
+}
+
+extern "C" {
 
 int fa_cascade_plan_destroy(fa_cascade_plan_t plan) {
   if (plan) {
