@@ -533,6 +533,34 @@ def test_cascade_overlap_graph_and_timing(lib, cuda, monkeypatch):
     compare(o, lse, ref[0], ref[1], TOL[torch.bfloat16])
 
 
+def test_cascade_many_plans(lib, cuda):
+    """Cascade plans take their fork/join events from a per-device free list
+    and give them back when destroyed: several plans alive at once, run
+    interleaved, then destroyed and planned again, all give the same
+    results bit for bit."""
+    import gc
+    rng = np.random.default_rng(9)
+    b = W.make_cascade_batch(prefix_pages=24, suffix_lengths=rng.integers(0, 120, size=12),
+                             num_qo_heads=16, num_kv_heads=4, head_dim=128,
+                             dtype=torch.bfloat16, seed=191, device=cuda)
+    pre, ip, idx, last = W.cascade_parts(b)
+    def make():
+        return lib.cascade_plan(pre, ip, idx, last, 16, 4, 128, 16, q_data_type=torch.bfloat16)
+    ref_o, ref_lse = make().run(b.q, b.paged_kv)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        plans = [make() for _ in range(4)]
+        outs = [p.run(b.q, b.paged_kv) for p in plans for _ in range(2)]
+        torch.cuda.synchronize()
+        for o, lse in outs:
+            assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+        assert all(p.check() == 0 for p in plans)
+        del plans, outs
+        gc.collect()
+    ref = oracle_decode(b)
+    compare(ref_o, ref_lse, ref[0], ref[1], TOL[torch.bfloat16])
+
+
 def test_cascade_rejects(lib, cuda):
     idx = torch.zeros(1, dtype=torch.int32, device=cuda)
     with pytest.raises(lib.FaError) as e:
