@@ -148,8 +148,15 @@ def _check(status: int, what: str) -> None:
         raise FaError(status, what)
 
 
+# torch's current stream of a device as a raw handle, without building a
+# Stream object (a few microseconds a call on the plan and run paths)
+_current_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_handle(stream) -> int | None:
     if stream is None:
+        if _current_raw_stream is not None:
+            return _current_raw_stream(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
 
@@ -163,6 +170,16 @@ def _host_i32(t) -> np.ndarray:
     if isinstance(t, np.ndarray) and t.dtype == np.int32 and t.flags.c_contiguous:
         return t
     return np.ascontiguousarray(np.asarray(t), dtype=np.int32)
+
+
+def _host_i32_ptr(t):
+    """(owner, address, length) of a host int32 array: a contiguous CPU int32
+    tensor is passed as it is, anything else goes through _host_i32."""
+    if (isinstance(t, torch.Tensor) and t.device.type == "cpu" and t.dtype == torch.int32
+            and t.dim() == 1 and t.is_contiguous()):
+        return t, t.data_ptr(), t.shape[0]
+    a = _host_i32(t)
+    return a, a.ctypes.data, a.shape[0]
 
 
 def _reachable(t: torch.Tensor) -> bool:
@@ -356,10 +373,10 @@ def plan(indptr, indices: torch.Tensor, last_page_len, num_qo_heads: int, num_kv
     """Plan a decode batch.  indptr/last_page_len may live on the host or the
     device (they are read on the host); indices must be an int32 CUDA tensor."""
     kv_data_type = q_data_type if kv_data_type is None else kv_data_type
-    indptr_h = _host_i32(indptr)
-    last_h = _host_i32(last_page_len)
-    B = indptr_h.shape[0] - 1
-    if last_h.shape[0] < B:
+    indptr_h, indptr_p, n_indptr = _host_i32_ptr(indptr)
+    last_h, last_p, n_last = _host_i32_ptr(last_page_len)
+    B = n_indptr - 1
+    if n_last < B:
         raise ValueError("last_page_len shorter than the batch")
     if indices.dtype != torch.int32 or not _reachable(indices) or not indices.is_contiguous():
         raise ValueError("indices must be a contiguous int32 CUDA or page-locked tensor")
@@ -368,8 +385,8 @@ def plan(indptr, indices: torch.Tensor, last_page_len, num_qo_heads: int, num_kv
                                 dtype=torch.uint8, device=_cuda_device(indices))
     handle = ctypes.c_void_p()
     _check(_L().fa_decode_plan(
-        indptr_h.ctypes.data, indices.data_ptr() if indices.numel() else None,
-        last_h.ctypes.data if B else None, B, num_qo_heads, num_kv_heads, head_dim, page_size,
+        indptr_p, indices.data_ptr() if indices.numel() else None,
+        last_p if B else None, B, num_qo_heads, num_kv_heads, head_dim, page_size,
         _dtype_code(q_data_type), _dtype_code(kv_data_type), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream_handle(stream),
         ctypes.byref(handle)), "fa_decode_plan")
@@ -386,9 +403,11 @@ def plan_multi_token(indptr, indices: torch.Tensor, last_page_len, q_len: int, n
     run() then takes q [B, q_len, Hq, D] and returns o of that shape and lse
     [B, q_len, Hq]."""
     kv_data_type = q_data_type if kv_data_type is None else kv_data_type
-    indptr_h = _host_i32(indptr)
-    last_h = _host_i32(last_page_len)
-    B = indptr_h.shape[0] - 1
+    indptr_h, indptr_p, n_indptr = _host_i32_ptr(indptr)
+    last_h, last_p, n_last = _host_i32_ptr(last_page_len)
+    B = n_indptr - 1
+    if n_last < B:
+        raise ValueError("last_page_len shorter than the batch")
     if indices.dtype != torch.int32 or not _reachable(indices) or not indices.is_contiguous():
         raise ValueError("indices must be a contiguous int32 CUDA or page-locked tensor")
     if workspace is None:
@@ -396,8 +415,8 @@ def plan_multi_token(indptr, indices: torch.Tensor, last_page_len, q_len: int, n
                                 dtype=torch.uint8, device=_cuda_device(indices))
     handle = ctypes.c_void_p()
     _check(_L().fa_decode_plan_multi_token(
-        indptr_h.ctypes.data, indices.data_ptr() if indices.numel() else None,
-        last_h.ctypes.data if B else None, B, q_len, num_qo_heads, num_kv_heads, head_dim,
+        indptr_p, indices.data_ptr() if indices.numel() else None,
+        last_p if B else None, B, q_len, num_qo_heads, num_kv_heads, head_dim,
         page_size, _dtype_code(q_data_type), _dtype_code(kv_data_type), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream_handle(stream),
         ctypes.byref(handle)), "fa_decode_plan_multi_token")
@@ -436,15 +455,17 @@ def plan_work_host(indptr, last_page_len, num_kv_heads: int, page_size: int, max
                    min_pages_per_cta: int = 8, pool_fraction: float = 0.0):
     """Host-only work-list builder (no GPU).  Returns (cta_offsets, segments [n,8],
     merge [m,4], n_slots); segments cta_offsets[-1]: are the run-time pool."""
-    indptr_h = _host_i32(indptr)
-    last_h = _host_i32(last_page_len)
-    B = indptr_h.shape[0] - 1
+    indptr_h, indptr_p, n_indptr = _host_i32_ptr(indptr)
+    last_h, last_p, n_last = _host_i32_ptr(last_page_len)
+    B = n_indptr - 1
+    if n_last < B:
+        raise ValueError("last_page_len shorter than the batch")
     cuts = max_ctas * 7 + 1
     cta = np.zeros(max_ctas + 1, np.int32)
     seg = np.zeros(((B * num_kv_heads + cuts) * SEGMENT_INTS,), np.int32)
     mer = np.zeros((cuts * MERGE_INTS,), np.int32)
     n_c, n_s, n_m, n_sl = (ctypes.c_int() for _ in range(4))
-    _check(_L().fa_plan_work_host(indptr_h.ctypes.data, last_h.ctypes.data if B else None, B,
+    _check(_L().fa_plan_work_host(indptr_p, last_p if B else None, B,
                                   num_kv_heads, page_size, max_ctas, min_pages_per_cta,
                                   float(pool_fraction), cta.ctypes.data, seg.ctypes.data, mer.ctypes.data,
                                   ctypes.byref(n_c), ctypes.byref(n_s), ctypes.byref(n_m),
@@ -507,9 +528,11 @@ def cascade_plan(prefix_indices: torch.Tensor, indptr, indices: torch.Tensor, la
     """Plan cascade decode: prefix_indices are the shared (full) pages every
     request starts with; indptr/indices/last_page_len describe each request's
     own pages after them."""
-    indptr_h = _host_i32(indptr)
-    last_h = _host_i32(last_page_len)
-    B = indptr_h.shape[0] - 1
+    indptr_h, indptr_p, n_indptr = _host_i32_ptr(indptr)
+    last_h, last_p, n_last = _host_i32_ptr(last_page_len)
+    B = n_indptr - 1
+    if n_last < B:
+        raise ValueError("last_page_len shorter than the batch")
     for t in (prefix_indices, indices):
         if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
             raise ValueError("index arrays must be contiguous int32 CUDA tensors")
@@ -521,8 +544,8 @@ def cascade_plan(prefix_indices: torch.Tensor, indptr, indices: torch.Tensor, la
     handle = ctypes.c_void_p()
     code = _dtype_code(q_data_type)
     _check(_L().fa_cascade_plan(
-        prefix_indices.data_ptr(), prefix_indices.numel(), indptr_h.ctypes.data,
-        indices.data_ptr() if indices.numel() else None, last_h.ctypes.data, B, num_qo_heads,
+        prefix_indices.data_ptr(), prefix_indices.numel(), indptr_p,
+        indices.data_ptr() if indices.numel() else None, last_p if B else None, B, num_qo_heads,
         num_kv_heads, head_dim, page_size, code, code, workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream_handle(stream),
         ctypes.byref(handle)), "fa_cascade_plan")

@@ -652,9 +652,20 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
     delete plan;
     return rc;
   }
+  // The tcgen05 kernel derives its work from its block index: only the
+  // error word is reset, in stream order, with no host image to build.
+  if (k.tcgen05) {
+    if (cudaMemsetAsync(plan->ws + plan->L.off_err, 0, sizeof(int),
+                        static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
+      fa_decode_plan_destroy(plan->suffix);
+      delete plan;
+      return FA_ERR_CUDA;
+    }
+    *out_plan = plan;
+    return FA_OK;
+  }
   // prefix work items in the decode segment format the producer reads:
   // {row_begin, kv_head, page_begin, page_end, row_count, item, 0, 0}
-  // (the tcgen05 kernel derives the same fields from its block index)
   std::vector<uint8_t> meta(plan->L.meta_bytes, 0);
   int32_t* items = reinterpret_cast<int32_t*>(meta.data() + (plan->L.off_items - plan->L.off_err));
   int32_t* cta = reinterpret_cast<int32_t*>(meta.data() + (plan->L.off_cta - plan->L.off_err));

@@ -255,6 +255,19 @@ def test_cuda_graph_capture(lib, cuda):
     assert p.check() == 0
 
 
+def test_stream_handle_is_current_stream(lib, cuda):
+    """Without an explicit stream, calls go to torch's current stream of the
+    current device, inside a stream context too; an explicit stream or raw
+    handle is passed through."""
+    assert lib._stream_handle(None) == torch.cuda.current_stream().cuda_stream
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        assert lib._stream_handle(None) == side.cuda_stream
+        assert lib._stream_handle(None) == torch.cuda.current_stream().cuda_stream
+    assert lib._stream_handle(side) == side.cuda_stream
+    assert lib._stream_handle(side.cuda_stream) == side.cuda_stream
+
+
 def test_dependent_launch_chain(lib, cuda):
     """Decode launches are programmatic dependents of the kernel before them
     in the stream.  Here each second launch decodes with q = the output of

@@ -184,6 +184,31 @@ def test_deterministic(lib):
         np.testing.assert_array_equal(x, y)
 
 
+def test_host_array_forms(lib):
+    """indptr and last_page_len taken as a list, numpy or torch CPU array of
+    any integer type, contiguous or not, give the same work list (int32 CPU
+    tensors are read in place, everything else is converted first)."""
+    indptr, last = _table(np.random.default_rng(5).integers(1, 3000, size=37))
+    ref = lib.plan_work_host(indptr, last, 4, 16, 120)
+    ip32 = torch.tensor(indptr, dtype=torch.int32)
+    strided = torch.stack([ip32, torch.zeros_like(ip32)], 1)[:, 0]   # stride 2
+    assert not strided.is_contiguous()
+    forms = [
+        (list(map(int, indptr)), list(map(int, last))),
+        (np.asarray(indptr, np.int64), np.asarray(last, np.int64)),
+        (ip32, torch.tensor(last, dtype=torch.int32)),
+        (ip32.to(torch.int64), torch.tensor(last, dtype=torch.int64)),
+        (strided, torch.tensor(last, dtype=torch.int32)),
+    ]
+    for ip, ln in forms:
+        got = lib.plan_work_host(ip, ln, 4, 16, 120)
+        for x, y in zip(ref[:3], got[:3]):
+            np.testing.assert_array_equal(x, y)
+        assert ref[3] == got[3]
+    with pytest.raises(ValueError):
+        lib.plan_work_host(ip32, torch.tensor(last[:-1], dtype=torch.int32), 4, 16, 120)
+
+
 def test_long_request_spread_over_grid(lib):
     """One 65536-token request with 32 kv heads fills every CTA (split-KV)."""
     indptr, last = _table([65536])
