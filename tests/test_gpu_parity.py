@@ -200,6 +200,30 @@ def test_run_time_pool(lib, cuda, monkeypatch, case):
             rel=TOKEN_SCALE_REL if path == "token_scales" else 0.0)
 
 
+@pytest.mark.parametrize("q_dtype,kv_dtype,hq,hkv,token_scales", [
+    (torch.bfloat16, torch.bfloat16, 32, 8, False),
+    (torch.bfloat16, torch.float8_e4m3fn, 64, 8, False),
+    (torch.bfloat16, torch.float8_e4m3fn, 64, 8, True),
+], ids=["bf16", "e4m3", "e4m3-token-scales"])
+def test_many_short_requests(lib, cuda, q_dtype, kv_dtype, hq, hkv, token_scales):
+    """Thousands of short requests (a third empty, many of one token or one
+    page): tens of thousands of units over one grid, so every CTA runs dozens
+    of segments back to back; every output against the oracle."""
+    rng = np.random.default_rng(77)
+    lengths = rng.integers(0, 49, size=2500)
+    lengths[rng.random(lengths.size) < 0.3] = 0
+    lengths[rng.random(lengths.size) < 0.1] = 1
+    b = W.make_batch(batch_lengths=lengths.tolist(), num_qo_heads=hq, num_kv_heads=hkv,
+                     head_dim=128, q_dtype=q_dtype, kv_dtype=kv_dtype, seed=78, device=cuda,
+                     token_scales=token_scales)
+    p, o, lse = run_token_scales(lib, b) if token_scales else run_lib(lib, b)
+    assert p.info["num_segments"] > 10 * p.info["num_ctas"]
+    check_coverage(p, b)
+    assert p.check() == 0
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, tol_for(b))
+
+
 def test_page_locked_host_buffers(lib, cuda):
     """q, the page ids, o and lse in page-locked host memory, read and written
     by the kernels directly: bitwise the same as with device buffers."""
