@@ -153,6 +153,28 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// 16 bytes global -> shared through the load path (cp.async, L1 bypassed);
+// both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+
+// One of the mbarrier's expected arrivals, made once this thread's earlier
+// cp.async copies have landed.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -381,7 +403,12 @@ __device__ __forceinline__ void prefetch_first_segment(const DecodeParams& p, in
 // (empty stages fill the gap), so that the consumer warps split its pages the
 // same way whichever CTA claims it.
 // With SCALES, each page also brings the 16 per-token K scales and the 16 V
-// scales of its kv head (64 contiguous bytes each) into scales[stage][0..31].
+// scales of its kv head (64 contiguous bytes each) into scales[stage][0..31]:
+// lanes 0-7 copy 16 bytes each with cp.async (the load path, which keeps
+// these small rows off the copy engine the page itself goes through), and
+// the stage's "full" barrier counts their arrivals as well (kScaleLanes + 1).
+constexpr int kScaleLanes = 8;  // producer lanes that copy a page's scales
+
 template <int S, int STAGE_BYTES, int BOXES, int BOX_X, int BOX_BYTES, bool SCALES = false>
 __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const DecodeParams& p,
                                               int seg_begin, int seg_end, uint8_t* ring,
@@ -429,7 +456,7 @@ __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const Deco
           const int kk = k + i;
           dev::mbar_wait(dev::smem_addr(&empty[kk % S]), (uint32_t)(((kk / S) & 1) ^ 1), aborted,
                          p.err);
-          dev::mbar_arrive(dev::smem_addr(&full[kk % S]));
+          dev::mbar_arrive_n(dev::smem_addr(&full[kk % S]), SCALES ? kScaleLanes + 1 : 1);
         }
       k += pad;
     }
@@ -459,22 +486,25 @@ __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const Deco
           const uint32_t round = (uint32_t)(k / S);
           dev::mbar_wait(dev::smem_addr(&empty[stage]), (round & 1u) ^ 1u, aborted, p.err);
           const uint32_t fb = dev::smem_addr(&full[stage]);
-          dev::mbar_arrive_expect_tx(fb, STAGE_BYTES + (SCALES ? 2 * kPageSize * 4 : 0));
+          dev::mbar_arrive_expect_tx(fb, STAGE_BYTES);
           // Out-of-range ids (already flagged) land outside the tensor map
           // and read zeros.
 #pragma unroll
           for (int b = 0; b < BOXES; ++b)
             dev::tma_load_4d(dev::smem_addr(ring + stage * STAGE_BYTES + b * BOX_BYTES), map,
                              b * BOX_X, kvh, 0, 2 * page, fb, policy);
-          if constexpr (SCALES) {
-            // the scale rows have no bounds check of their own: a flagged
-            // out-of-range page reads page 0's scales
+        }
+        if constexpr (SCALES) {
+          // lane 0 found the stage free; the scale rows have no bounds check
+          // of their own: a flagged out-of-range page reads page 0's scales
+          __syncwarp();
+          if (lane < kScaleLanes) {
+            const int stage = k % S;
             const int64_t pg = (page < 0 || (int64_t)page >= p.num_pages) ? 0 : page;
             const size_t row = ((size_t)pg * p.num_kv_heads + kvh) * kPageSize;
-            dev::bulk_load(dev::smem_addr(scales + stage * 2 * kPageSize), p.k_scales + row,
-                           kPageSize * 4, fb);
-            dev::bulk_load(dev::smem_addr(scales + stage * 2 * kPageSize + kPageSize),
-                           p.v_scales + row, kPageSize * 4, fb);
+            const float* src = (lane < 4 ? p.k_scales : p.v_scales) + row + 4 * (lane & 3);
+            dev::cp_async16(dev::smem_addr(scales + stage * 2 * kPageSize + 4 * lane), src);
+            dev::cp_async_arrive(dev::smem_addr(&full[stage]));
           }
         }
       }
@@ -483,6 +513,7 @@ __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const Deco
   }
   // No copy may still be landing in shared memory when the CTA exits (only
   // possible if a consumer gave up waiting).
+  if constexpr (SCALES) dev::cp_async_wait_all();
   if (lane == 0) {
     const int first = k > S ? k - S : 0;
     for (int kk = first; kk < k; ++kk)

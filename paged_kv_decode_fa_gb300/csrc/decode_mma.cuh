@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
   FoldList* folds = reinterpret_cast<FoldList*>(smem + C::OFF_FOLDS);
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      dev::mbar_init(dev::smem_addr(&full[s]), 1);
+      dev::mbar_init(dev::smem_addr(&full[s]), TS ? kScaleLanes + 1 : 1);
       dev::mbar_init(dev::smem_addr(&empty[s]), 1);
     }
     seg_queue_init(queue, NW);
