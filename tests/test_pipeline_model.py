@@ -126,6 +126,17 @@ def test_kernel_assignment_is_safe(NW, spw):
         assert not errs, (segs, errs[:3])
 
 
+def test_kernel_assignment_is_safe_with_tiny_segments():
+    """Dozens of zero- to three-page segments per CTA (thousands of short
+    requests): the stage hand-off stays safe with E4M3's ring (8 stages, 4
+    consumer warps)."""
+    rng = random.Random(11)
+    for trial in range(100):
+        segs = [rng.choice([0, 0, 1, 1, 1, 2, 3]) for _ in range(rng.randint(30, 50))]
+        errs = simulate(segs, S=8, NW=4, assign="global", seed=trial)
+        assert not errs, (segs, errs[:3])
+
+
 def test_shared_stage_round_robin_aliases():
     """The assignment the kernel no longer uses - pages dealt round-robin per
     segment over a ring whose stages several warps share - admits pages that
