@@ -7,7 +7,8 @@ and it shares no code with that library.
 The arithmetic lives in ``oracle.c`` (plain float64 loops, compiled with gcc);
 this module compiles it on first use, loads it with ctypes and marshals numpy
 arrays in and out.  ``expected_coverage`` states, as a plain set, which
-(request, kv head, page) triples a decode plan has to cover.
+(request, kv head, page) triples a decode plan has to cover, and
+``expected_token_coverage`` which (request, kv head, token) triples.
 
 Every function here is pinned by ``tests/test_oracle.py`` against closed forms,
 brute force and library routines; nothing is marked "parity unpinned".
@@ -309,3 +310,42 @@ def expected_coverage(indptr, num_kv_heads):
     if not blocks:
         return np.zeros((0, 3), dtype=np.int64)
     return np.concatenate(blocks, axis=0)
+
+
+def request_lengths(indptr, last_page_len, page_size):
+    """Context length of every request: (pages - 1) * page_size + last_page_len,
+    0 for a request with no pages (its last_page_len is ignored).
+
+    Follows plan()'s arguments in section "The API you actually use" of the
+    page "FlashDecoding + FlashInfer - the decode-time attention story":
+    request i owns pages indptr[i] .. indptr[i+1]-1, the last one holding
+    last_page_len[i] valid slots."""
+    indptr = np.asarray(indptr, dtype=np.int64)
+    last = np.asarray(last_page_len, dtype=np.int64)
+    pages = np.diff(indptr)
+    return np.where(pages > 0, (pages - 1) * int(page_size) + last[:len(pages)], 0)
+
+
+def expected_token_coverage(indptr, last_page_len, num_kv_heads, page_size):
+    """Every (request, kv head, token) a decode plan must cover once: token t
+    of request i for t in [0, len_i), for each kv head.  int64 [n, 3] sorted
+    by (request, kv head, token)."""
+    lens = request_lengths(indptr, last_page_len, page_size)
+    blocks = []
+    for i, n in enumerate(lens):
+        t = np.arange(int(n), dtype=np.int64)
+        for h in range(num_kv_heads):
+            blocks.append(np.stack([np.full_like(t, i), np.full_like(t, h), t], axis=1))
+    if not blocks:
+        return np.zeros((0, 3), dtype=np.int64)
+    return np.concatenate(blocks, axis=0)
+
+
+def expected_token_intervals(indptr, last_page_len, num_kv_heads, page_size):
+    """The same set as expected_token_coverage, as one half-open token range
+    per non-empty (request, kv head): int64 [n, 4] rows (request, kv head,
+    0, len), sorted.  For batches whose triples would not fit in memory."""
+    lens = request_lengths(indptr, last_page_len, page_size)
+    rows = [(i, h, 0, int(n)) for i, n in enumerate(lens) if n > 0
+            for h in range(num_kv_heads)]
+    return np.array(rows, dtype=np.int64).reshape(-1, 4)

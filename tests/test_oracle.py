@@ -512,5 +512,39 @@ def test_golden_coverage():
     np.testing.assert_array_equal(got, np.array(spec["expected"]))
 
 
+def test_golden_token_coverage():
+    """Token-level coverage on the hand-worked example: lengths from the
+    page counts and last_page_len, each kv head covering tokens 0 .. len-1."""
+    with open(os.path.join(GOLDEN, "token_coverage_worked_example.json")) as f:
+        spec = json.load(f)
+    args = (spec["indptr"], spec["last_page_len"], spec["num_kv_heads"], spec["page_size"])
+    np.testing.assert_array_equal(
+        oracle.request_lengths(spec["indptr"], spec["last_page_len"], spec["page_size"]),
+        spec["lengths"])
+    runs = np.array(spec["expected_runs"])
+    np.testing.assert_array_equal(oracle.expected_token_intervals(*args), runs)
+    want = np.array([(r, h, t) for r, h, a, b in runs for t in range(a, b)])
+    np.testing.assert_array_equal(oracle.expected_token_coverage(*args), want)
+
+
+def test_token_coverage_refines_page_coverage():
+    """Independent route on random batches: every covered page position p of
+    request i contributes slots 0..15 (last page: 0..last-1) as tokens
+    (p - indptr[i]) * 16 + slot; the union equals the token coverage."""
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        B = int(rng.integers(1, 12))
+        pages = rng.integers(0, 6, size=B)
+        indptr = np.concatenate([[0], np.cumsum(pages)])
+        last = rng.integers(1, 17, size=B)
+        Hkv = int(rng.integers(1, 4))
+        got = set(map(tuple, oracle.expected_token_coverage(indptr, last, Hkv, 16).tolist()))
+        want = set()
+        for r, h, p in oracle.expected_coverage(indptr, Hkv).tolist():
+            n = last[r] if p == indptr[r + 1] - 1 else 16
+            want |= {(r, h, (p - indptr[r]) * 16 + s) for s in range(n)}
+        assert got == want
+
+
 def test_threads_reported(orc):
     assert orc.max_threads() >= 1

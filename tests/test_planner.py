@@ -1,6 +1,7 @@
 """Host planner (no GPU): the work list covers every (request, kv head, page)
-exactly once - bit-exact against the oracle's coverage definition - and
-balances pages across the persistent grid."""
+and every (request, kv head, token) exactly once - bit-exact against the
+oracle's coverage definitions - and balances pages across the persistent
+grid."""
 import numpy as np
 import pytest
 import torch
@@ -21,6 +22,57 @@ def expand(seg):
     out = np.stack([r, h, starts + offs], axis=1)
     order = np.lexsort((out[:, 2], out[:, 1], out[:, 0]))
     return out[order]
+
+
+def segment_token_ranges(seg, indptr, P):
+    """(request, kv head, first token, end token) of every non-empty segment,
+    read the way the kernels read a segment: its pages are full except the
+    last, which holds last_valid tokens."""
+    seg = np.asarray(seg, np.int64).reshape(-1, 8)
+    indptr = np.asarray(indptr, np.int64)
+    s = seg[seg[:, 3] > seg[:, 2]]
+    base = indptr[s[:, 0]]
+    t0 = (s[:, 2] - base) * P
+    t1 = (s[:, 3] - 1 - base) * P + s[:, 4]
+    return np.stack([s[:, 0], s[:, 1], t0, t1], axis=1)
+
+
+def expand_tokens(seg, indptr, P):
+    """(request, kv head, token) triples a work list covers, sorted."""
+    r = segment_token_ranges(seg, indptr, P)
+    cnt = r[:, 3] - r[:, 2]
+    assert np.all(cnt > 0), "a segment covers no token or a negative count"
+    rep = lambda c: np.repeat(r[:, c], cnt)
+    offs = np.arange(cnt.sum()) - np.repeat(np.cumsum(cnt) - cnt, cnt)
+    out = np.stack([rep(0), rep(1), rep(2) + offs], axis=1)
+    return out[np.lexsort((out[:, 2], out[:, 1], out[:, 0]))]
+
+
+def token_runs(seg, indptr, P):
+    """The same set as expand_tokens, as maximal runs (request, kv head,
+    first, end) of consecutive tokens: pieces of a unit that abut merge into
+    one run, a gap leaves two and an overlap or repeat leaves a run that
+    starts inside the previous one - neither matches the oracle's one run
+    [0, len) per unit."""
+    r = segment_token_ranges(seg, indptr, P)
+    r = r[np.lexsort((r[:, 2], r[:, 1], r[:, 0]))]
+    runs = []
+    for req, h, a, b in r.tolist():
+        if runs and runs[-1][0] == req and runs[-1][1] == h and runs[-1][3] == a:
+            runs[-1][3] = b
+        else:
+            runs.append([req, h, a, b])
+    return np.array(runs, dtype=np.int64).reshape(-1, 4)
+
+
+def assert_token_coverage(seg, indptr, last, Hkv, P=16, triples_limit=4_000_000):
+    """Bit-exact token coverage against the oracle: as runs always, and as
+    explicit triples when the batch is small enough to list them."""
+    np.testing.assert_array_equal(token_runs(seg, indptr, P),
+                                  oracle.expected_token_intervals(indptr, last, Hkv, P))
+    if int(oracle.request_lengths(indptr, last, P).sum()) * Hkv <= triples_limit:
+        np.testing.assert_array_equal(expand_tokens(seg, indptr, P),
+                                      oracle.expected_token_coverage(indptr, last, Hkv, P))
 
 
 POOL_TIERS, POOL_MIN = 4, 2   # the planner's pool schedule
@@ -54,9 +106,10 @@ def check_work(lib, indptr, last, Hkv, max_ctas, min_pages=8, P=16, pool=0.0):
     cta, seg, mer, n_slots = lib.plan_work_host(indptr, last, Hkv, P, max_ctas, min_pages, pool)
     indptr = np.asarray(indptr, np.int64)
     B = len(indptr) - 1
-    # coverage, bit-exact
+    # coverage, bit-exact: pages, and tokens (last_valid of every segment)
     want = oracle.expected_coverage(indptr, Hkv)
     np.testing.assert_array_equal(expand(seg), want)
+    assert_token_coverage(seg, indptr, last, Hkv, P)
     # every empty (request, head) still has exactly one empty segment
     for i in np.nonzero(np.diff(indptr) == 0)[0]:
         e = seg[(seg[:, 0] == i)]
@@ -234,3 +287,31 @@ def test_rejects_bad_sizes(lib):
         lib.plan_work_host(np.array([0, 1]), np.array([3]), 0, 16, 10)
     with pytest.raises(lib.FaError):
         lib.plan_work_host(np.array([0, 1]), np.array([3]), 1, 16, 0)
+
+
+def test_token_coverage_catches_planted_mistakes(lib):
+    """The token-level check fails on the plausible planner mistakes that a
+    page-level check cannot see: a full last page, a split piece that ends
+    early, a piece that repeats a token, a dropped empty-request segment
+    does not matter (no tokens) but a dropped page does."""
+    indptr, last = _table([37, 0, 16, 250, 1, 1000])
+    cta, seg, mer, n_slots = lib.plan_work_host(indptr, last, 2, 16, 9, 8, 0.0)
+    assert_token_coverage(seg, indptr, last, 2)
+    ends = np.nonzero((seg[:, 3] > seg[:, 2]) & (seg[:, 4] < 16))[0]
+    assert len(ends)
+    bad = seg.copy(); bad[ends[0], 4] = 16                       # last page taken as full
+    with pytest.raises(AssertionError):
+        assert_token_coverage(bad, indptr, last, 2)
+    pieces = np.nonzero(seg[:, 5] >= 0)[0]
+    assert len(pieces) >= 2
+    first_piece = pieces[0]
+    bad = seg.copy(); bad[first_piece, 4] = 15                   # a piece stops one token early
+    with pytest.raises(AssertionError):
+        assert_token_coverage(bad, indptr, last, 2)
+    bad = seg.copy(); bad[first_piece, 3] += 1; bad[first_piece, 4] = 16   # overlaps the next piece
+    with pytest.raises(AssertionError):
+        assert_token_coverage(bad, indptr, last, 2)
+    long_ = int(np.argmax(seg[:, 3] - seg[:, 2]))
+    bad = seg.copy(); bad[long_, 2] += 1                         # a page dropped
+    with pytest.raises(AssertionError):
+        assert_token_coverage(bad, indptr, last, 2)
