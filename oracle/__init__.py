@@ -58,6 +58,9 @@ def _bind(lib):
     lib.oracle_batch_decode_multi.argtypes = [
         P, i32, P, i32, i64, P, P, P, i32, i32, i32, i32, i32, i32, dbl, dbl, dbl, P, P, i32]
     lib.oracle_batch_decode_multi.restype = i32
+    lib.oracle_batch_decode_ragged_q.argtypes = [
+        P, i32, P, i32, i64, P, P, P, P, i32, i32, i32, i32, i32, dbl, dbl, dbl, P, P, i32]
+    lib.oracle_batch_decode_ragged_q.restype = i32
     lib.oracle_merge_states.argtypes = [P, P, P, P, P, P, i64, i32]
     lib.oracle_merge_states.restype = None
     lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
@@ -198,6 +201,47 @@ class Oracle:
             raise ValueError("oracle_batch_decode_multi rejected its arguments")
         return o, lse
 
+    def batch_decode_ragged_q(self, q, q_dtype, paged_kv, kv_dtype, indptr, indices,
+                              last_page_len, qo_indptr, num_qo_heads, num_kv_heads, head_dim,
+                              page_size, sm_scale=None, k_scale=1.0, v_scale=1.0,
+                              num_threads=0):
+        """Decode with n_i = qo_indptr[i+1] - qo_indptr[i] query tokens for
+        request i, q ragged [total_q, Hq, D]; query token j of request i
+        attends to its positions 0 .. len_i - n_i + j.  Returns float64
+        o [total_q, Hq, D] and lse [total_q, Hq]."""
+        q = np.ascontiguousarray(q)
+        paged_kv = np.ascontiguousarray(paged_kv)
+        indptr = np.ascontiguousarray(indptr, dtype=np.int32)
+        indices = np.ascontiguousarray(indices, dtype=np.int32)
+        last_page_len = np.ascontiguousarray(last_page_len, dtype=np.int32)
+        qo_indptr = np.ascontiguousarray(qo_indptr, dtype=np.int32)
+        B = indptr.shape[0] - 1
+        if qo_indptr.shape[0] != B + 1:
+            raise ValueError("qo_indptr must have batch + 1 entries")
+        if sm_scale is None:
+            sm_scale = 1.0 / float(np.sqrt(head_dim))
+        total_q = int(qo_indptr[-1])
+        per_page = 2 * page_size * num_kv_heads * head_dim
+        num_pages = paged_kv.size // per_page
+        if paged_kv.size % per_page or q.size != total_q * num_qo_heads * head_dim:
+            raise ValueError("bad q / paged_kv size")
+        o = np.zeros((total_q, num_qo_heads, head_dim), dtype=np.float64)
+        lse = np.zeros((total_q, num_qo_heads), dtype=np.float64)
+        if indices.size == 0:
+            indices = np.zeros(1, dtype=np.int32)
+        if last_page_len.size == 0:
+            last_page_len = np.zeros(1, dtype=np.int32)
+        if total_q == 0:
+            return o, lse
+        rc = self.lib.oracle_batch_decode_ragged_q(
+            _ptr(q), int(q_dtype), _ptr(paged_kv), int(kv_dtype), int(num_pages), _ptr(indptr),
+            _ptr(indices), _ptr(last_page_len), _ptr(qo_indptr), B, num_qo_heads,
+            num_kv_heads, head_dim, page_size, float(sm_scale), float(k_scale), float(v_scale),
+            _ptr(o), _ptr(lse), int(num_threads))
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments")
+        return o, lse
+
     def merge_states(self, o_a, lse_a, o_b, lse_b):
         """Merge two arrays of normalised states (o [..., D], lse [...]) in float64."""
         o_a = np.ascontiguousarray(o_a, dtype=np.float64)
@@ -271,6 +315,10 @@ def batch_decode_token_scales(*args, **kw):
 
 def batch_decode_multi(*args, **kw):
     return _default().batch_decode_multi(*args, **kw)
+
+
+def batch_decode_ragged_q(*args, **kw):
+    return _default().batch_decode_ragged_q(*args, **kw)
 
 
 def merge_states(*args, **kw):

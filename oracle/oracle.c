@@ -275,6 +275,84 @@ int oracle_batch_decode_multi(const void* q, int q_dtype, const void* paged_kv,
   return 0;
 }
 
+/* Decode with a different number of query tokens per request, laid out
+ * ragged: request i owns query rows qo_indptr[i] .. qo_indptr[i+1] of q and o
+ * ([total_q, Hq, D]) and of lse ([total_q, Hq]) - the indptr layout of
+ * section "Ragged attention - variable-length batching" of the page
+ * "FlashDecoding + FlashInfer", applied to the queries.  With n_i query
+ * tokens (the draft tokens a speculative verifier checks), they are the last
+ * n_i positions of the request's cache, and query token j (0-based) attends
+ * to positions 0 .. len_i - n_i + j: the context and the drafts up to itself.
+ * n_i may be 0 (the request contributes no rows); n_i <= len_i otherwise. */
+int oracle_batch_decode_ragged_q(const void* q, int q_dtype, const void* paged_kv,
+                                 int kv_dtype, int64_t num_pages,
+                                 const int32_t* indptr, const int32_t* indices,
+                                 const int32_t* last_page_len,
+                                 const int32_t* qo_indptr, int B, int Hq, int Hkv,
+                                 int D, int P, double sm_scale, double k_scale,
+                                 double v_scale, double* o, double* lse,
+                                 int num_threads) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || P <= 0 || Hq % Hkv) return 1;
+  if (indptr[0] != 0 || qo_indptr[0] != 0) return 1;
+  for (int i = 0; i < B; ++i) {
+    const int np = indptr[i + 1] - indptr[i];
+    const int nq = qo_indptr[i + 1] - qo_indptr[i];
+    if (np < 0 || nq < 0) return 1;
+    if (nq == 0) continue;
+    if (np == 0 || last_page_len[i] < 1 || last_page_len[i] > P) return 1;
+    if ((int64_t)(np - 1) * P + last_page_len[i] < nq) return 1;
+    for (int p = indptr[i]; p < indptr[i + 1]; ++p)
+      if (indices[p] < 0 || indices[p] >= num_pages) return 1;
+  }
+  const int g = Hq / Hkv;
+  const int64_t rows = (int64_t)qo_indptr[B] * Hq;
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int64_t u = 0; u < rows; ++u) {
+    const int64_t row = u / Hq; /* query token row */
+    const int h = (int)(u % Hq);
+    int i = 0; /* the request owning this row */
+    while (qo_indptr[i + 1] <= row) ++i;
+    const int nq = qo_indptr[i + 1] - qo_indptr[i];
+    const int j = (int)(row - qo_indptr[i]);
+    const int kvh = h / g;
+    const int np = indptr[i + 1] - indptr[i];
+    const int64_t len = (int64_t)(np - 1) * P + last_page_len[i];
+    const int64_t visible = len - nq + j + 1;
+    double* out = o + u * D;
+    double* s = (double*)malloc(sizeof(double) * visible);
+    for (int64_t t = 0; t < visible; ++t) {
+      const int64_t page = indices[indptr[i] + t / P];
+      const int slot = (int)(t % P);
+      double acc = 0.0;
+      for (int d = 0; d < D; ++d)
+        acc += load_elem(q, q_dtype, u * D + d) * k_scale *
+               load_elem(paged_kv, kv_dtype, kv_offset(page, 0, slot, kvh, d, P, Hkv, D));
+      s[t] = sm_scale * acc;
+    }
+    double m = -INFINITY;
+    for (int64_t t = 0; t < visible; ++t)
+      if (s[t] > m) m = s[t];
+    double den = 0.0;
+    for (int64_t t = 0; t < visible; ++t) den += exp(s[t] - m);
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (int64_t t = 0; t < visible; ++t) {
+      const int64_t page = indices[indptr[i] + t / P];
+      const int slot = (int)(t % P);
+      const double w = exp(s[t] - m);
+      for (int d = 0; d < D; ++d)
+        out[d] += w * v_scale *
+                  load_elem(paged_kv, kv_dtype, kv_offset(page, 1, slot, kvh, d, P, Hkv, D));
+    }
+    for (int d = 0; d < D; ++d) out[d] /= den;
+    lse[u] = m + log(den);
+    free(s);
+  }
+  return 0;
+}
+
 /* ---- merge of partial states -------------------------------------------- */
 
 /* Each state is stored as a normalised output o_x (length D) with its

@@ -393,6 +393,81 @@ def pin_multi_token_one_is_decode(orc):
                                indptr, indices, last, 6, Hq, Hkv, D, P)
 
 
+def _ragged_q_batch(seed, lens=(5, 0, 16, 17, 40, 3), nq=(3, 0, 1, 4, 2, 3), Hq=4, Hkv=2, D=8,
+                    P=4):
+    rng = np.random.default_rng(seed)
+    K = [rng.standard_normal((n, Hkv, D)).astype(np.float32) for n in lens]
+    V = [rng.standard_normal((n, Hkv, D)).astype(np.float32) for n in lens]
+    kv, indptr, indices, last = dense_pages(K, V, P, perm_seed=seed, pool_extra=2)
+    qo_indptr = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    q = rng.standard_normal((int(qo_indptr[-1]), Hq, D)).astype(np.float32)
+    return q, K, V, kv, indptr, indices, last, qo_indptr, lens, nq, (Hq, Hkv, D, P)
+
+
+def pin_ragged_q_truncation(orc):
+    """Query token j of request i (n_i tokens) equals single-token decode over
+    the request cut after position len_i - n_i + j."""
+    q, K, V, kv, indptr, indices, last, qo, lens, nq, (Hq, Hkv, D, P) = _ragged_q_batch(18)
+    o, lse = orc.batch_decode_ragged_q(q, oracle.F32, kv, oracle.F32, indptr, indices, last, qo,
+                                       Hq, Hkv, D, P)
+    assert o.shape[0] == sum(nq)
+    for r, (n, k) in enumerate(zip(lens, nq)):
+        for j in range(k):
+            vis = n - k + j + 1
+            npg = (vis + P - 1) // P
+            ip = np.array([0, npg], np.int32)
+            ids = indices[indptr[r]:indptr[r] + npg]
+            lp = np.array([vis - (npg - 1) * P], np.int32)
+            row = qo[r] + j
+            o1, l1 = orc.batch_decode(np.ascontiguousarray(q[row][None]), oracle.F32, kv,
+                                      oracle.F32, ip, ids, lp, Hq, Hkv, D, P)
+            np.testing.assert_array_equal(o[row], o1[0])
+            np.testing.assert_array_equal(lse[row], l1[0])
+
+
+def pin_ragged_q_sdpa(orc):
+    """Against torch's float64 scaled_dot_product_attention (a library
+    routine) with a boolean mask of the positions each query token sees."""
+    import torch.nn.functional as F
+    q, K, V, kv, indptr, indices, last, qo, lens, nq, (Hq, Hkv, D, P) = _ragged_q_batch(19)
+    o, lse = orc.batch_decode_ragged_q(q, oracle.F32, kv, oracle.F32, indptr, indices, last, qo,
+                                       Hq, Hkv, D, P)
+    g = Hq // Hkv
+    for r, (n, k) in enumerate(zip(lens, nq)):
+        if k == 0:
+            continue
+        Kr = torch.from_numpy(K[r]).double().repeat_interleave(g, 1).transpose(0, 1)  # [Hq, n, D]
+        Vr = torch.from_numpy(V[r]).double().repeat_interleave(g, 1).transpose(0, 1)
+        qr = torch.from_numpy(q[qo[r]:qo[r + 1]]).double().transpose(0, 1)            # [Hq, k, D]
+        mask = torch.arange(n)[None, :] <= (n - k + torch.arange(k))[:, None]          # [k, n]
+        ref = F.scaled_dot_product_attention(qr, Kr, Vr, attn_mask=mask)              # [Hq, k, D]
+        np.testing.assert_allclose(o[qo[r]:qo[r + 1]], ref.transpose(0, 1).numpy(), rtol=0,
+                                   atol=1e-12)
+
+
+def pin_ragged_q_one_token_is_decode(orc):
+    """n_i = 1 for every request is plain decode; n_i = q_len for every
+    request is the uniform multi-token decode; a request shorter than its
+    draft count is refused."""
+    q, K, V, kv, indptr, indices, last, qo, lens, nq, (Hq, Hkv, D, P) = _ragged_q_batch(
+        20, lens=(5, 16, 17, 40), nq=(1, 1, 1, 1))
+    a = orc.batch_decode_ragged_q(q, oracle.F32, kv, oracle.F32, indptr, indices, last, qo, Hq,
+                                  Hkv, D, P)
+    b = orc.batch_decode(q, oracle.F32, kv, oracle.F32, indptr, indices, last, Hq, Hkv, D, P)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+    q, K, V, kv, indptr, indices, last, qo, lens, nq, (Hq, Hkv, D, P) = _ragged_q_batch(
+        21, lens=(5, 16, 17, 40), nq=(3, 3, 3, 3))
+    a = orc.batch_decode_ragged_q(q, oracle.F32, kv, oracle.F32, indptr, indices, last, qo, Hq,
+                                  Hkv, D, P)
+    m = orc.batch_decode_multi(q.reshape(4, 3, Hq, D), oracle.F32, kv, oracle.F32, indptr,
+                               indices, last, 3, Hq, Hkv, D, P)
+    np.testing.assert_array_equal(a[0], m[0].reshape(12, Hq, D))
+    with pytest.raises(ValueError):
+        orc.batch_decode_ragged_q(np.zeros((6, Hq, D), np.float32), oracle.F32, kv, oracle.F32,
+                                  indptr, indices, last, [0, 6, 6, 6, 6], Hq, Hkv, D, P)
+
+
 def pin_empty_request(orc):
     rng = np.random.default_rng(10)
     K = [rng.standard_normal((5, 1, 4)).astype(np.float32)]
@@ -456,7 +531,8 @@ def pin_rejects_bad_args(orc):
     pin_gqa_equals_repeated_mha, pin_page_permutation, pin_brute_force, pin_torch_dense,
     pin_empty_request, pin_padding_never_read, pin_golden_decode, pin_rejects_bad_args,
     pin_token_scales_dense, pin_token_scales_uniform, pin_multi_token_truncation,
-    pin_multi_token_causal_dense, pin_multi_token_one_is_decode])
+    pin_multi_token_causal_dense, pin_multi_token_one_is_decode, pin_ragged_q_truncation,
+    pin_ragged_q_sdpa, pin_ragged_q_one_token_is_decode])
 def test_decode_pins(orc, pin):
     pin(orc)
 

@@ -43,6 +43,12 @@ MUTATIONS = [
     ("draft mask off by one", "const int64_t visible = len - q_len + qi + 1;",
      "const int64_t visible = len - q_len + qi;",
      [T.pin_multi_token_truncation, T.pin_multi_token_causal_dense]),
+    ("ragged draft mask off by one", "const int64_t visible = len - nq + j + 1;",
+     "const int64_t visible = len - nq + j;",
+     [T.pin_ragged_q_truncation, T.pin_ragged_q_sdpa]),
+    ("ragged drafts all stop at the first", "const int64_t visible = len - nq + j + 1;",
+     "const int64_t visible = len - nq + 1;",
+     [T.pin_ragged_q_truncation, T.pin_ragged_q_sdpa]),
     ("merge weight of b uses a", "d_b * w_b;", "d_b * w_a;",
      [T.pin_golden_merge, T.pin_merge_algebra, T.pin_split_merge]),
     ("merge sign flipped", "exp(m_b - m_new);", "exp(m_new - m_b);",
