@@ -10,8 +10,11 @@ intends; it is timed separately and it is inside the end-to-end number.
                   [--impl ours|reference] [--no-cpu-baseline]
 
 Prints one JSON line (rank 0).  Workloads are the seeded synthetic batches of
-paged_kv_decode_fa_gb300.workloads; the default is the GQA uniform batch
-(B=64, 32 qo / 8 kv heads, head_dim 128, 2048 tokens each, bf16).  With
+paged_kv_decode_fa_gb300.workloads; the default is the largest one, the
+heterogeneous ragged batch (B=450, 32 qo / 8 kv heads, head_dim 128, bf16,
+lengths log-uniform in [256, 64000], 21.5 GB of KV).  The other decode
+workloads are measured in the same run and reported under "other_workloads",
+each with its own algorithmic bytes, kernel time and roofline fraction.  With
 --impl reference the float64 CPU oracle is timed instead, on the host cores,
 over bounded samples of the same workload.  Under torchrun (N > 1) each rank
 runs an independent replica of the workload on its own GPU (the path has no
@@ -23,7 +26,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -64,9 +66,16 @@ def algorithmic_bytes(b: W.DecodeBatch) -> int:
     if "k_scales" in b.extra:          # one fp32 K and one V scale per token and kv head
         kv += b.total_tokens * b.num_kv_heads * 2 * 4
     idx = int(b.indptr[-1]) * 4
-    qo = 2 * b.batch * b.q_len * b.num_qo_heads * b.head_dim * q_es
-    lse = b.batch * b.q_len * b.num_qo_heads * 4
+    qo = 2 * b.q.numel() * q_es                     # q read, o written (any q layout)
+    lse = b.q.numel() // b.head_dim * 4
+    if "qo_indptr" in b.extra:                       # a ragged plan's row boundaries
+        idx += (b.batch + 1) * 4
     return int(kv + idx + qo + lse)
+
+
+def query_rows(b: W.DecodeBatch) -> int:
+    """Query tokens of one step: B, B * q_len, or the ragged rows."""
+    return b.q.numel() // (b.num_qo_heads * b.head_dim)
 
 
 def read_bf16_peak():
@@ -103,17 +112,17 @@ def kernel_source_hash(workload: str = "gqa_uniform") -> str:
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary of this
-    workload, if the summary was taken on the current kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}.md")
+    """DRAM bytes per launch of the workload's dominant kernel from the
+    committed ncu figures (profiles/traffic.json), if they were taken on the
+    current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
-    text = open(path).read()
-    m_t = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
-    m_h = re.search(r"^kernel_source_hash:\s*([0-9a-f]+)", text, re.M)
-    if not m_t or not m_h or m_h.group(1) != kernel_source_hash(workload):
+    with open(path) as f:
+        entry = json.load(f).get("workloads", {}).get(workload)
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash(workload):
         return None
-    return float(m_t.group(1))
+    return float(entry["traffic_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -285,7 +294,7 @@ def oracle_timing(b: W.DecodeBatch, target_s: float, max_requests: int | None = 
     threads = oracle.max_threads()
     desc = (f"{n} of {b.batch} requests ({int(sb.lengths.sum())} KV tokens), seeded random "
             f"choice, float64 C oracle, OpenMP {threads} threads")
-    return n, dt, int(sb.lengths.sum()), threads, desc, algorithmic_bytes(sb)
+    return query_rows(sb), dt, int(sb.lengths.sum()), threads, desc, algorithmic_bytes(sb)
 
 
 # ------------------------------------------------------------------ arms
@@ -294,7 +303,10 @@ def bench_reference(args, world, rank):
     """The oracle as the reference arm: K timed steps, each a bounded sample."""
     if rank != 0:
         return None
-    b = W.make_config_batch(args.workload, device="cpu")
+    # inputs drawn where the timed arm draws them (the same values); only
+    # the sampled requests are copied to the host for the oracle
+    b = W.make_config_batch(args.workload,
+                            device="cuda" if torch.cuda.is_available() else "cpu")
     import oracle
     from tests.helpers import oracle_decode, sub_batch
     budget = 150.0
@@ -312,7 +324,7 @@ def bench_reference(args, world, rank):
     for _ in range(args.steps):
         oracle_decode(sb)
     dt = time.perf_counter() - t
-    value = n * b.q_len * args.steps / dt
+    value = query_rows(sb) * args.steps / dt
     threads = oracle.max_threads()
     cfg = W.CONFIGS[args.workload]
     desc = f"{n} of {b.batch} requests per step, float64 C oracle, OpenMP {threads} threads"
@@ -330,14 +342,19 @@ def bench_reference(args, world, rank):
 
 
 def config_dict(cfg: W.DecodeConfig, b: W.DecodeBatch) -> dict:
+    kv_bytes = int(b.total_tokens * cfg.num_kv_heads * 2 * cfg.head_dim *
+                   b.paged_kv.element_size())
     return {"workload": cfg.name, "batch": b.batch, "num_qo_heads": cfg.num_qo_heads,
             "num_kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim,
             "page_size": cfg.page_size, "q_len": cfg.q_len, "q_dtype": DTYPE_NAMES[cfg.q_dtype],
             "kv_dtype": DTYPE_NAMES[cfg.kv_dtype],
             "kv_tokens": b.total_tokens, "mean_seq_len": round(b.total_tokens / max(1, b.batch), 1),
-            "kv_bytes": int(b.total_tokens * cfg.num_kv_heads * 2 * cfg.head_dim *
-                            b.paged_kv.element_size()),
-            "l2": "inputs larger than L2 (129 MB): the KV read each step exceeds it",
+            "query_tokens": query_rows(b),
+            "kv_bytes": kv_bytes,
+            "l2": ("inputs larger than L2 (129 MB): the KV read each step exceeds it"
+                   if kv_bytes > 129e6 else
+                   f"L2-resident ({kv_bytes / 1e6:.1f} MB of KV): a launch-bound correctness "
+                   "case; its HBM fraction is not a bandwidth figure"),
             "parallelism": "replicas (one independent batch per GPU)",
             "softmax": ("unified max against a static Cauchy-Schwarz logit bound"
                         if cfg.name == "gqa_unified_max" else "online (running max)")}
@@ -481,6 +498,110 @@ def bench_cascade(args, world, rank, local, b, cfg, dev):
     }
 
 
+def plan_batch(fa, b: W.DecodeBatch, idx=None, ws=None):
+    """Plan a decode batch (multi-token plans for q_len > 1, ragged-q plans
+    for a per-request number of query tokens)."""
+    idx = b.indices if idx is None else idx
+    if "qo_indptr" in b.extra:
+        return fa.plan_ragged_q(b.indptr.numpy(), idx, b.last_page_len.numpy(),
+                                b.extra["qo_indptr"], b.num_qo_heads, b.num_kv_heads, b.head_dim,
+                                b.page_size, q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype,
+                                workspace=ws)
+    if b.q_len > 1:
+        return fa.plan_multi_token(b.indptr.numpy(), idx, b.last_page_len.numpy(), b.q_len,
+                                   b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size,
+                                   q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype,
+                                   workspace=ws)
+    return fa.plan(b.indptr.numpy(), idx, b.last_page_len.numpy(), b.num_qo_heads,
+                   b.num_kv_heads, b.head_dim, b.page_size, q_data_type=b.q.dtype,
+                   kv_data_type=b.paged_kv.dtype, workspace=ws)
+
+
+def workspace_bytes(fa, b: W.DecodeBatch) -> int:
+    """Workspace bound of the batch's plan kind."""
+    G = b.num_qo_heads // b.num_kv_heads
+    if "qo_indptr" in b.extra or G * b.q_len > 8:
+        return int(fa.library().fa_decode_workspace_size_ragged_q(
+            b.batch, b.num_qo_heads, b.num_kv_heads, b.head_dim))
+    return fa.workspace_size(b.batch, b.num_qo_heads * b.q_len, b.num_kv_heads, b.head_dim)
+
+
+def step_fn(name: str, b: W.DecodeBatch, um_bound):
+    """The production run call of a workload: plan.run, the per-token-scale
+    run, or the unified-max run against a static bound."""
+    token_scales = "k_scales" in b.extra
+
+    def run_step(plan, q, out, lse_out):
+        if um_bound is not None:
+            return plan.run_unified_max(q, b.paged_kv, um_bound, out=out, lse=lse_out)
+        if token_scales:
+            return plan.run_token_scales(q, b.paged_kv, b.extra["k_scales"], b.extra["v_scales"],
+                                         out=out, lse=lse_out)
+        return plan.run(q, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale, out=out,
+                        lse=lse_out)
+    return run_step
+
+
+# Decode workloads measured beside the headline one, in the same run.
+OTHER_WORKLOADS = ("tiny", "gqa_uniform", "long_split", "fp8_kv", "fp8_kv_token_scales",
+                   "spec_decode", "spec_decode_ragged", "gqa_unified_max")
+
+
+def measure_other(args, world, dev, name: str) -> dict:
+    """One more decode workload: K timed steps after W warm-ups, the region's
+    events over its launches as the kernel time, the workload's own
+    algorithmic bytes, roofline fraction and (current) ncu traffic."""
+    import paged_kv_decode_fa_gb300 as fa
+    cfg = W.CONFIGS[name]
+    b = W.make_config_batch(name, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    p = plan_batch(fa, b)
+    info = p.info
+    o = torch.empty_like(b.q)
+    lse = torch.empty(tuple(b.q.shape[:-1]), dtype=torch.float32, device=dev)
+    um_bound = W.cauchy_schwarz_bound(b) if name == "gqa_unified_max" else None
+    run_step = step_fn(name, b, um_bound)
+    for _ in range(args.warmup):
+        run_step(p, b.q, o, lse)
+    torch.cuda.synchronize(dev)
+    if p.check() != 0:
+        raise RuntimeError(f"device check flagged the {name} batch")
+    launches = 1 + (1 if info["num_merge_units"] > 0 and not info["fused_merge"] else 0)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for _ in range(args.steps):
+        run_step(p, b.q, o, lse)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, world, dev)
+    step_s = elapsed_s / args.steps
+    alg = algorithmic_bytes(b)
+    peak, _ = read_peaks()
+    res = {
+        "config": config_dict(cfg, b),
+        "value": whole_job_rate(world, query_rows(b), args.steps, elapsed_s),
+        "unit": "tokens/s", "ms_per_step": step_s * 1e3,
+        "kv_tokens_per_s": world * b.total_tokens * args.steps / elapsed_s,
+        "hbm_gbs": alg / step_s / 1e9,
+        "roofline": {"bound": "hbm", "achieved": alg / step_s / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": alg / step_s / 1e9 / peak,
+                     "traffic": profiled_traffic(name),
+                     "kernel": ("fa_decode_mma_kernel" if info["tensor_cores"]
+                                else "fa_decode_split_kernel"),
+                     "algorithmic_bytes_per_launch": alg, "duration_us": step_s * 1e6,
+                     "duration_from": ("timed-region events / launches" if launches == 1 else
+                                       "timed-region events / steps (decode + merge kernel)")},
+        "gpu_launches": args.steps * launches,
+    }
+    if um_bound is not None:
+        res["unified_max"] = {"bound": um_bound, "fallbacks": p.unified_max_fallbacks()}
+    del p, b, o, lse
+    torch.cuda.empty_cache()
+    return res
+
+
 def bench_ours(args, world, rank, local):
     import paged_kv_decode_fa_gb300 as fa
     dev = torch.device("cuda", local)
@@ -491,38 +612,37 @@ def bench_ours(args, world, rank, local):
         return bench_cascade(args, world, rank, local, b, cfg, dev)
     stream = torch.cuda.current_stream(dev)
 
-    # plan (amortised), timed on the host including its upload
+    # plan (amortised), timed on the host including its upload: the first
+    # plan of the process (occupancy queries, staging buffers) and the
+    # median of later plans of the same batch
     torch.cuda.synchronize(dev)
     t = time.perf_counter()
-    def make_plan(idx, ws=None):
-        if b.q_len > 1:
-            return fa.plan_multi_token(b.indptr.numpy(), idx, b.last_page_len.numpy(), b.q_len,
-                                       b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size,
-                                       q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype,
-                                       workspace=ws)
-        return fa.plan(b.indptr.numpy(), idx, b.last_page_len.numpy(), b.num_qo_heads,
-                       b.num_kv_heads, b.head_dim, b.page_size, q_data_type=b.q.dtype,
-                       kv_data_type=b.paged_kv.dtype, workspace=ws)
-
-    p = make_plan(b.indices)
+    p = plan_batch(fa, b)
     torch.cuda.synchronize(dev)
     plan_ms = (time.perf_counter() - t) * 1e3
     info = p.info
+    ws_warm = torch.empty(workspace_bytes(fa, b), dtype=torch.uint8, device=dev)
+    warm = []
+    for _ in range(50):
+        t = time.perf_counter()
+        pw = plan_batch(fa, b, ws=ws_warm)
+        torch.cuda.synchronize(dev)
+        warm.append((time.perf_counter() - t) * 1e3)
+        del pw
+    plan_ms_warm = statistics.median(warm)
+    del ws_warm
     o = torch.empty_like(b.q)
     lse = torch.empty(tuple(b.q.shape[:-1]), dtype=torch.float32, device=dev)
-    token_scales = "k_scales" in b.extra
     # unified max: a static logit bound, fixed before the timed region the
     # way an offline profile of the model would fix it
     um_bound = W.cauchy_schwarz_bound(b) if args.workload == "gqa_unified_max" else None
+    run_step_fn = step_fn(args.workload, b, um_bound)
 
     def run_step(plan, q, out=o, lse_out=lse):
-        if um_bound is not None:
-            return plan.run_unified_max(q, b.paged_kv, um_bound, out=out, lse=lse_out)
-        if token_scales:
-            return plan.run_token_scales(q, b.paged_kv, b.extra["k_scales"], b.extra["v_scales"],
-                                         out=out, lse=lse_out)
-        return plan.run(q, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale, out=out,
-                        lse=lse_out)
+        return run_step_fn(plan, q, out, lse_out)
+
+    def make_plan(idx, ws=None):
+        return plan_batch(fa, b, idx, ws)
 
     for _ in range(args.warmup):
         run_step(p, b.q)
@@ -592,8 +712,7 @@ def bench_ours(args, world, rank, local):
     lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     q_d = torch.empty_like(b.q)
     idx_d = torch.empty_like(b.indices)
-    ws = torch.empty(fa.workspace_size(b.batch, b.num_qo_heads * b.q_len, b.num_kv_heads,
-                                       b.head_dim), dtype=torch.uint8, device=dev)
+    ws = torch.empty(workspace_bytes(fa, b), dtype=torch.uint8, device=dev)
 
     def e2e_step():
         pe = make_plan(idx_h, ws)
@@ -634,7 +753,7 @@ def bench_ours(args, world, rank, local):
     alg = algorithmic_bytes(b)
     peak, peak_kind = read_peaks()
     step_s = elapsed_s / args.steps
-    value = whole_job_rate(world, b.batch * b.q_len, args.steps, elapsed_s)
+    value = whole_job_rate(world, query_rows(b), args.steps, elapsed_s)
     achieved = alg / kern_region_s / 1e9
     traffic = profiled_traffic(args.workload) if args.max_requests is None else None
     out = {
@@ -649,6 +768,7 @@ def bench_ours(args, world, rank, local):
         "hbm_frac_of_nominal_7900": alg / step_s / 1e9 / 7900.0,
         "peak_kind": peak_kind,
         "plan_ms": plan_ms,
+        "plan_ms_warm": plan_ms_warm,
         "decode_kernel_us": {"mean": kern_avg_s * 1e6, "median": kern_med_s * 1e6,
                              "measured": "events around each launch, second loop"},
         "plan": {k: info[k] for k in ("num_ctas", "ctas_per_sm", "num_segments",
@@ -661,13 +781,13 @@ def bench_ours(args, world, rank, local):
                                 else "fa_decode_split_kernel"),
                      "algorithmic_bytes_per_launch": alg,
                      "duration_us": kern_region_s * 1e6, "duration_from": duration_from},
-        "e2e": {"value": whole_job_rate(world, b.batch * b.q_len, e2e_steps, e2e_s), "unit": "tokens/s",
+        "e2e": {"value": whole_job_rate(world, query_rows(b), e2e_steps, e2e_s), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "steps": e2e_steps,
                 "includes": "plan (work-list upload) and run every step; q and page ids read, "
                             "o and lse written by the kernels in page-locked host memory",
                 "staged_copies": {
-                    "value": whole_job_rate(world, b.batch * b.q_len, e2e_steps, staged_s),
+                    "value": whole_job_rate(world, query_rows(b), e2e_steps, staged_s),
                     "includes": "pinned H2D q + page ids, plan, run, D2H o + lse on one stream"}},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(t0, t1),
@@ -676,9 +796,17 @@ def bench_ours(args, world, rank, local):
         out["unified_max"] = {"bound": um_bound, "fallbacks_in_timed_steps": um_fallbacks}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n, dt, toks, threads, desc, nbytes = oracle_timing(b, target_s=args.cpu_seconds)
-        out["cpu_baseline"] = {"value": n * b.q_len / dt, "unit": "tokens/s", "cores": threads,
+        out["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": threads,
                                "kind": "oracle", "sample": desc,
                                "kv_tokens_per_s": toks / dt, "gbs": nbytes / dt / 1e9}
+    if not args.no_others and args.max_requests is None:
+        # the headline batch's memory is released first: every workload
+        # holds its own batch while it is measured (each in its own timed
+        # region; gpu_launches above counts the headline's region only)
+        del b, p, pe, o, lse, q_h, idx_h, o_h, lse_h, q_d, idx_d, ws
+        torch.cuda.empty_cache()
+        out["other_workloads"] = {name: measure_other(args, world, dev, name)
+                                  for name in OTHER_WORKLOADS if name != args.workload}
     return out
 
 
@@ -687,9 +815,11 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=15)
-    ap.add_argument("--workload", default="gqa_uniform", choices=list(W.CONFIGS))
+    ap.add_argument("--workload", default="ragged", choices=list(W.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-others", action="store_true",
+                    help="measure only --workload (not the other decode workloads)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--max-requests", type=int, default=None,
                     help="keep only the first N requests of the workload (profiler captures "

@@ -124,11 +124,13 @@ int fa_decode_plan(const int32_t* indptr_host, const int32_t* indices_dev,
  * Arguments otherwise as fa_decode_plan; every request needs len >= q_len
  * (FA_ERR_INVALID_ARG otherwise).  The workspace bound is
  * fa_decode_workspace_size(batch, num_qo_heads * q_len, num_kv_heads,
- * head_dim).  Built for head_dim 128, (q, kv) = (BF16, BF16) or
- * (BF16, E4M3), and (num_qo_heads / num_kv_heads) * q_len <= 8 with q_len
- * in {2, 4, 8}: group 1 with q_len 2, 4, 8; group 2 with 2, 4; group 4
- * with 2.  Other combinations return FA_ERR_UNSUPPORTED.  q_len = 1 is
- * fa_decode_plan. */
+ * head_dim) for (num_qo_heads / num_kv_heads) * q_len <= 8, else
+ * fa_decode_workspace_size_ragged_q.  Built for head_dim 128, (q, kv) =
+ * (BF16, BF16) or (BF16, E4M3): with group x q_len <= 8 for q_len 2, 4, 8 at
+ * group 1, 2, 4 at group 2 and 2 at group 4; with more columns, the kernels
+ * of fa_decode_plan_ragged_q (every request holding q_len rows), up to
+ * group x q_len = 32.  Other combinations return FA_ERR_UNSUPPORTED.
+ * q_len = 1 is fa_decode_plan. */
 int fa_decode_plan_multi_token(const int32_t* indptr_host,
                                const int32_t* indices_dev,
                                const int32_t* last_page_len_host, int batch,
@@ -137,6 +139,40 @@ int fa_decode_plan_multi_token(const int32_t* indptr_host,
                                fa_dtype kv_dtype, void* workspace_dev,
                                size_t workspace_bytes, void* cuda_stream,
                                fa_decode_plan_t* out_plan);
+
+/* plan for decode with a different number of query tokens per request:
+ * request i owns rows qo_indptr[i] .. qo_indptr[i+1] of q and o - the
+ * ragged (indptr) layout of section "Ragged attention - variable-length
+ * batching" of the page "FlashDecoding + FlashInfer", applied to the
+ * queries, e.g. speculative verification with a draft length of its own per
+ * request.  Its n_i query tokens are the last n_i positions of the request's
+ * cache and query token j (0-based) attends to positions 0 .. len_i - n_i + j.
+ * A later fa_decode_run of this plan takes
+ *      q    [qo_indptr[batch], num_qo_heads, head_dim]
+ *      o    [qo_indptr[batch], num_qo_heads, head_dim]
+ *      lse  [qo_indptr[batch], num_qo_heads]
+ *  qo_indptr_host  [batch + 1] int32, host, read during the call: 0 first,
+ *                  non-decreasing, n_i <= len_i (n_i = 0 allowed: the
+ *                  request contributes no rows; its pages are still read).
+ * Arguments otherwise as fa_decode_plan; the workspace bound is
+ * fa_decode_workspace_size_ragged_q.  Built for head_dim 128, (q, kv) =
+ * (BF16, BF16) or (BF16, E4M3), groups 1, 2, 4, 8 with
+ * group x max_i n_i <= 32 (group 8: up to 4 query tokens per request).
+ * Up to 8 columns (group x n) the consumer warps split a segment's pages; with
+ * more, each warp owns 8 columns and reads every page.  Errors as
+ * fa_decode_plan; FA_ERR_UNSUPPORTED for shapes beyond those. */
+int fa_decode_plan_ragged_q(const int32_t* indptr_host, const int32_t* indices_dev,
+                            const int32_t* last_page_len_host,
+                            const int32_t* qo_indptr_host, int batch,
+                            int num_qo_heads, int num_kv_heads, int head_dim,
+                            int page_size, fa_dtype q_dtype, fa_dtype kv_dtype,
+                            void* workspace_dev, size_t workspace_bytes,
+                            void* cuda_stream, fa_decode_plan_t* out_plan);
+
+/* Workspace bound of any ragged-q plan of this batch and shape (the widest
+ * kernel's partial states, 32 columns), current device. */
+size_t fa_decode_workspace_size_ragged_q(int batch, int num_qo_heads,
+                                         int num_kv_heads, int head_dim);
 
 /* run: decode attention for one query token per request (page "FlashDecoding
  * + FlashInfer", section "FlashDecoding - the split-KV trick": every chunk of
@@ -259,10 +295,13 @@ typedef struct {
   size_t plan_upload_bytes;   /* bytes fa_decode_plan copies host -> device */
   int tensor_cores;           /* 1: per-page products on mma.sync, 0: CUDA cores */
   int fused_merge;            /* 1: split requests merged inside the decode kernel */
-  int q_len;                  /* query tokens per request */
+  int q_len;                  /* query tokens per request (ragged plans: the most the
+                                 kernel chosen holds) */
   int unified_max;            /* 1: fa_decode_run_unified_max is built for this plan */
   int num_pool_segments;      /* segments claimed at run time (0: static quotas only) */
   int64_t pool_pages;         /* (page, kv head) pairs in those segments */
+  int ragged_q;               /* 1: query rows per request from qo_indptr */
+  int64_t total_q_rows;       /* query rows of q / o (batch * q_len unless ragged) */
 } fa_plan_info;
 
 int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info);
@@ -321,36 +360,51 @@ int fa_decode_check(fa_decode_plan_t plan, void* cuda_stream, int* flags);
 int fa_decode_set_timing_events(fa_decode_plan_t plan, void* ev_before,
                                 void* ev_after);
 
-/* Decode one batch without allocating any device memory.
+/* Decode one batch without allocating anything.
  *
  * The pages describe no counterpart to this call; it exists for callers that
  * cannot allocate: code handed only input and output pointers by a host
  * framework that owns every device buffer through its own pool, allocator or
  * out-of-memory callbacks, and latency-critical loops where cudaMalloc (which
- * may synchronise the whole device) is not acceptable.  It does what
- * fa_decode_plan followed by fa_decode_run does, with the workspace replaced
- * by a fixed array of FA_STATIC_SCRATCH_BYTES that the library keeps on every
- * GPU that loads it, for the life of the process.
+ * may synchronise the whole device) or a page-locked host allocation is not
+ * acceptable.  It does what fa_decode_plan followed by fa_decode_run does,
+ * with the workspace replaced by a fixed array of FA_STATIC_SCRATCH_BYTES
+ * that the library keeps on every GPU that loads it, for the life of the
+ * process, and gives bitwise the same o and lse (same kernels, same grid,
+ * same work list).
  *
  * Arguments are those of fa_decode_plan (page table, shapes, dtypes) and of
  * fa_decode_run (q, paged_kv, num_pages, scales, o, lse, stream), with the
  * same layouts and ownership; indices_dev must stay valid until the work
  * enqueued on cuda_stream has finished.  No plan handle is returned: every
- * call plans again on the host.
+ * call plans again on the host, into fixed host arrays (no run-time pool).
  *
+ *  - Nothing is allocated on any call: no device memory, no page-locked host
+ *    memory, no events, no heap objects.  The work list goes to the GPU with
+ *    one cudaMemcpyAsync from a library-owned pageable host buffer, which
+ *    the driver stages before the call returns (the call may wait for that
+ *    staging, never for the stream's other work).
  *  - The first call on a device looks up the array's device address with
- *    that device current; make that first call before any stream capture.
+ *    that device current (cudaGetSymbolAddress) and caches the kernels'
+ *    occupancy; make that first call outside any stream capture.
+ *  - It must not be called while cuda_stream is being captured into a CUDA
+ *    graph: a capture cannot record a copy from pageable memory.  Such a
+ *    call returns FA_ERR_UNSUPPORTED and enqueues nothing.
  *  - Every call on a device shares the one array: calls whose GPU work
  *    overlaps (different streams, or host threads without ordering) race on
  *    it and give wrong results.  Calls in one stream are ordered and safe.
+ *    The host side of calls is serialised by a lock.
  *  - The work list, including the device-check word, is rewritten by each
- *    call, so nothing left by an earlier call is read.
+ *    call, so nothing left by an earlier call is read.  To see whether a
+ *    call hit a bad page id or a timed-out wait, call fa_decode_static_check
+ *    after it and before the next call.
  *  - A batch whose plan needs more than FA_STATIC_SCRATCH_BYTES (about
  *    (batch * num_kv_heads + CTAs) * 32 bytes of work list plus up to
  *    2 * CTAs * (num_qo_heads / num_kv_heads) * (head_dim + 1) * 4 bytes of
  *    partial states) is refused with FA_ERR_WORKSPACE_TOO_SMALL before
- *    anything is launched; use fa_decode_plan with a larger workspace then.
- * Errors: those of fa_decode_plan and fa_decode_run. */
+ *    anything is enqueued; use fa_decode_plan with a larger workspace then.
+ * Errors: those of fa_decode_plan and fa_decode_run, and FA_ERR_UNSUPPORTED
+ * during a stream capture. */
 #define FA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
 int fa_decode_static(const int32_t* indptr_host, const int32_t* indices_dev,
                      const int32_t* last_page_len_host, int batch,
@@ -359,6 +413,26 @@ int fa_decode_static(const int32_t* indptr_host, const int32_t* indices_dev,
                      const void* q, const void* paged_kv, int64_t num_pages,
                      float sm_scale, float k_scale, float v_scale, void* o,
                      float* lse, void* cuda_stream);
+
+/* The device-check word of the last fa_decode_static call on the current
+ * device: waits for cuda_stream, reads the word from the library's array and
+ * clears it.  Returns FA_OK, FA_ERR_DEVICE_CHECK with *flags set (bit 0: a
+ * page id outside [0, num_pages); bit 1: a pipeline wait timed out), or
+ * FA_ERR_CUDA.  Allocates nothing.  Like fa_decode_check, it synchronises:
+ * keep it off the hot path. */
+int fa_decode_static_check(void* cuda_stream, int* flags);
+
+/* Counters of the library's own host-side resources since it was loaded:
+ * page-locked staging buffers allocated for plan uploads (count and bytes)
+ * and uploads made through them.  fa_decode_plan may allocate a staging
+ * buffer on its first calls or when a work list outgrows one;
+ * fa_decode_static never touches them. */
+typedef struct {
+  int64_t pinned_host_allocations;
+  int64_t pinned_host_bytes;
+  int64_t staged_uploads;
+} fa_library_stats;
+int fa_library_get_stats(fa_library_stats* stats);
 
 /* ---- cascade decode (shared prefix) ------------------------------------
  *

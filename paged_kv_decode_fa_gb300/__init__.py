@@ -20,10 +20,11 @@ import numpy as np
 import torch
 
 __all__ = [
-    "FA_OK", "FaError", "DecodePlan", "plan", "plan_multi_token", "run", "merge_states",
+    "FA_OK", "FaError", "DecodePlan", "plan", "plan_multi_token", "plan_ragged_q", "run",
+    "merge_states",
     "CascadePlan", "cascade_plan",
     "workspace_size", "plan_work_host", "BatchDecodeWithPagedKVCacheWrapper",
-    "LIB_PATH", "EXPORTED_SYMBOLS", "library",
+    "LIB_PATH", "EXPORTED_SYMBOLS", "library", "library_stats",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -38,7 +39,8 @@ EXPORTED_SYMBOLS = (
     "fa_decode_run_token_scales", "fa_decode_plan_multi_token",
     "fa_cascade_workspace_size", "fa_cascade_plan", "fa_cascade_run", "fa_cascade_plan_destroy",
     "fa_cascade_check", "fa_decode_run_unified_max", "fa_decode_unified_max_fallbacks",
-    "fa_cascade_set_timing_events",
+    "fa_cascade_set_timing_events", "fa_decode_static_check", "fa_library_get_stats",
+    "fa_decode_plan_ragged_q", "fa_decode_workspace_size_ragged_q",
 )
 
 FA_OK = 0
@@ -62,10 +64,23 @@ class PlanInfo(ctypes.Structure):
         ("workspace_bytes_used", ctypes.c_size_t), ("plan_upload_bytes", ctypes.c_size_t),
         ("tensor_cores", ctypes.c_int), ("fused_merge", ctypes.c_int), ("q_len", ctypes.c_int),
         ("unified_max", ctypes.c_int), ("num_pool_segments", ctypes.c_int),
-        ("pool_pages", ctypes.c_int64)]
+        ("pool_pages", ctypes.c_int64), ("ragged_q", ctypes.c_int),
+        ("total_q_rows", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class LibraryStats(ctypes.Structure):
+    _fields_ = [("pinned_host_allocations", ctypes.c_int64), ("pinned_host_bytes", ctypes.c_int64),
+                ("staged_uploads", ctypes.c_int64)]
+
+
+def library_stats() -> dict:
+    """The library's own host-side resource counters (fa_library_get_stats)."""
+    s = LibraryStats()
+    _check(_L().fa_library_get_stats(ctypes.byref(s)), "fa_library_get_stats")
+    return {n: int(getattr(s, n)) for n, _ in s._fields_}
 
 
 def _load() -> ctypes.CDLL:
@@ -82,6 +97,11 @@ def _load() -> ctypes.CDLL:
     lib.fa_decode_plan_multi_token.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
                                                P, sz, P, ctypes.POINTER(P)]
     lib.fa_decode_plan_multi_token.restype = i32
+    lib.fa_decode_plan_ragged_q.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                            P, sz, P, ctypes.POINTER(P)]
+    lib.fa_decode_plan_ragged_q.restype = i32
+    lib.fa_decode_workspace_size_ragged_q.argtypes = [i32, i32, i32, i32]
+    lib.fa_decode_workspace_size_ragged_q.restype = sz
     lib.fa_decode_run.argtypes = [P, P, P, i64, f32, f32, f32, P, P, P]
     lib.fa_decode_run.restype = i32
     lib.fa_decode_run_token_scales.argtypes = [P, P, P, i64, f32, P, P, P, P, P]
@@ -120,6 +140,13 @@ def _load() -> ctypes.CDLL:
     lib.fa_decode_set_timing_events.restype = i32
     lib.fa_cascade_set_timing_events.argtypes = [P, P, P]
     lib.fa_cascade_set_timing_events.restype = i32
+    lib.fa_decode_static.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, i64,
+                                     f32, f32, f32, P, P, P]
+    lib.fa_decode_static.restype = i32
+    lib.fa_decode_static_check.argtypes = [P, ctypes.POINTER(i32)]
+    lib.fa_decode_static_check.restype = i32
+    lib.fa_library_get_stats.argtypes = [ctypes.POINTER(LibraryStats)]
+    lib.fa_library_get_stats.restype = i32
     return lib
 
 
@@ -211,17 +238,21 @@ class DecodePlan:
     """A planned decode batch.  Holds the library's plan handle and keeps the
     tensors it refers to (indices, workspace) alive."""
 
-    def __init__(self, handle, indices, workspace, q_dtype, kv_dtype, shape, q_len=1):
+    def __init__(self, handle, indices, workspace, q_dtype, kv_dtype, shape, q_len=1,
+                 total_q_rows=None):
         self._h = handle
         self._indices = indices
         self._workspace = workspace
         self.q_dtype = q_dtype
         self.kv_dtype = kv_dtype
         self.q_len = q_len
+        self.total_q_rows = total_q_rows  # ragged plans: rows of q / o
         self.batch, self.num_qo_heads, self.num_kv_heads, self.head_dim, self.page_size = shape
 
     def _q_shape(self):
         B, Hq, D = self.batch, self.num_qo_heads, self.head_dim
+        if self.total_q_rows is not None:
+            return (self.total_q_rows, Hq, D)
         return (B, Hq, D) if self.q_len == 1 else (B, self.q_len, Hq, D)
 
     def __del__(self):
@@ -411,8 +442,13 @@ def plan_multi_token(indptr, indices: torch.Tensor, last_page_len, q_len: int, n
     if indices.dtype != torch.int32 or not _reachable(indices) or not indices.is_contiguous():
         raise ValueError("indices must be a contiguous int32 CUDA or page-locked tensor")
     if workspace is None:
-        workspace = torch.empty(workspace_size(B, num_qo_heads * q_len, num_kv_heads, head_dim),
-                                dtype=torch.uint8, device=_cuda_device(indices))
+        if (num_qo_heads // max(1, num_kv_heads)) * q_len > 8:   # the ragged-q kernels
+            n = _L().fa_decode_workspace_size_ragged_q(B, num_qo_heads, num_kv_heads, head_dim)
+        else:
+            n = workspace_size(B, num_qo_heads * q_len, num_kv_heads, head_dim)
+        if n == 0:
+            raise ValueError("invalid shape or no CUDA device")
+        workspace = torch.empty(int(n), dtype=torch.uint8, device=_cuda_device(indices))
     handle = ctypes.c_void_p()
     _check(_L().fa_decode_plan_multi_token(
         indptr_p, indices.data_ptr() if indices.numel() else None,
@@ -422,6 +458,41 @@ def plan_multi_token(indptr, indices: torch.Tensor, last_page_len, q_len: int, n
         ctypes.byref(handle)), "fa_decode_plan_multi_token")
     return DecodePlan(handle.value, indices, workspace, q_data_type, kv_data_type,
                       (B, num_qo_heads, num_kv_heads, head_dim, page_size), q_len=q_len)
+
+
+def plan_ragged_q(indptr, indices: torch.Tensor, last_page_len, qo_indptr, num_qo_heads: int,
+                  num_kv_heads: int, head_dim: int, page_size: int, *,
+                  q_data_type=torch.bfloat16, kv_data_type=None,
+                  workspace: torch.Tensor | None = None, stream=None) -> DecodePlan:
+    """Plan decode with qo_indptr[i+1] - qo_indptr[i] query tokens for request
+    i (the last positions of its cache, causal among themselves).  run() then
+    takes q [qo_indptr[-1], Hq, D] and returns o of that shape and lse
+    [qo_indptr[-1], Hq]."""
+    kv_data_type = q_data_type if kv_data_type is None else kv_data_type
+    indptr_h, indptr_p, n_indptr = _host_i32_ptr(indptr)
+    last_h, last_p, n_last = _host_i32_ptr(last_page_len)
+    qo_h, qo_p, n_qo = _host_i32_ptr(qo_indptr)
+    B = n_indptr - 1
+    if n_last < B or n_qo != B + 1:
+        raise ValueError("last_page_len shorter than the batch, or qo_indptr not batch + 1 long")
+    if indices.dtype != torch.int32 or not _reachable(indices) or not indices.is_contiguous():
+        raise ValueError("indices must be a contiguous int32 CUDA or page-locked tensor")
+    if workspace is None:
+        n = _L().fa_decode_workspace_size_ragged_q(B, num_qo_heads, num_kv_heads, head_dim)
+        if n == 0:
+            raise ValueError("invalid shape or no CUDA device")
+        workspace = torch.empty(int(n), dtype=torch.uint8, device=_cuda_device(indices))
+    handle = ctypes.c_void_p()
+    _check(_L().fa_decode_plan_ragged_q(
+        indptr_p, indices.data_ptr() if indices.numel() else None,
+        last_p if B else None, qo_p, B, num_qo_heads, num_kv_heads, head_dim,
+        page_size, _dtype_code(q_data_type), _dtype_code(kv_data_type), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream),
+        ctypes.byref(handle)), "fa_decode_plan_ragged_q")
+    total_q = int(np.asarray(qo_h)[B]) if B >= 0 else 0
+    return DecodePlan(handle.value, indices, workspace, q_data_type, kv_data_type,
+                      (B, num_qo_heads, num_kv_heads, head_dim, page_size),
+                      total_q_rows=total_q)
 
 
 def run(p: DecodePlan, q, paged_kv, **kw):

@@ -39,13 +39,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t off_err, off_umc, off_pool, off_cta, off_seg, off_merge, off_count, meta_bytes, off_part_o, off_part_lse,
-      total;
+  size_t off_err, off_umc, off_pool, off_cta, off_seg, off_merge, off_count, off_qo, meta_bytes,
+      off_part_o, off_part_lse, total;
 };
 
 // Metadata (uploaded by every plan, zeros included) then the partial states.
+// G is the columns of a partial state (group x query tokens); n_qo the
+// entries of a ragged plan's qo_indptr copy (0 otherwise).
 Layout make_layout(int64_t n_ctas, int64_t n_segments, int64_t n_merge, int64_t n_slots, int G,
-                   int D) {
+                   int D, int64_t n_qo = 0) {
   Layout L;
   L.off_err = 0;
   L.off_umc = sizeof(int);  // unified-max re-centring counter
@@ -54,7 +56,8 @@ Layout make_layout(int64_t n_ctas, int64_t n_segments, int64_t n_merge, int64_t 
   L.off_seg = align_up(L.off_cta + sizeof(int32_t) * (size_t)(n_ctas + 1));
   L.off_merge = align_up(L.off_seg + sizeof(fadecode::Segment) * (size_t)n_segments);
   L.off_count = align_up(L.off_merge + sizeof(fadecode::MergeUnit) * (size_t)n_merge);
-  L.meta_bytes = align_up(L.off_count + sizeof(int32_t) * (size_t)n_merge);
+  L.off_qo = align_up(L.off_count + sizeof(int32_t) * (size_t)n_merge);
+  L.meta_bytes = align_up(L.off_qo + sizeof(int32_t) * (size_t)n_qo);
   L.off_part_o = L.meta_bytes;
   L.off_part_lse = align_up(L.off_part_o + sizeof(float) * (size_t)n_slots * G * D);
   L.total = align_up(L.off_part_lse + sizeof(float) * (size_t)n_slots * G);
@@ -169,6 +172,13 @@ int kv_tensor_map(MapCache* c, const DecodeKernel& k, fa_dtype kv_dtype, const v
   return FA_OK;
 }
 
+bool find_ragged_q_kernel(fa_dtype q, fa_dtype kv, int D, int G, int max_q, DecodeKernel* k) {
+  if (!tensor_cores_allowed() || q != FA_DTYPE_BF16) return false;
+  if (kv == FA_DTYPE_BF16) return fadecode::find_ragged_q_kernel_bf16(D, G, max_q, k);
+  if (kv == FA_DTYPE_E4M3) return fadecode::find_ragged_q_kernel_bf16_e4m3(D, G, max_q, k);
+  return false;
+}
+
 bool find_unified_max_kernel(fa_dtype q, fa_dtype kv, int D, int G, DecodeKernel* k) {
   if (q != FA_DTYPE_BF16 || kv != FA_DTYPE_BF16 || !tensor_cores_allowed()) return false;
   return fadecode::find_unified_max_kernel_bf16(D, G, k);
@@ -189,20 +199,25 @@ int kernel_occupancy(const DecodeKernel& k) {
     const void* func;
     int device, occ;
   };
+  // a fixed table (no allocation on any call): the compiled kernels times
+  // the devices in use stay far below its size; past it, queries are simply
+  // not cached
+  constexpr int kEntries = 256;
   static std::mutex mu;
-  static std::vector<Entry> cache;
+  static Entry cache[kEntries];
+  static int used = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  for (const Entry& e : cache)
-    if (e.func == k.func && e.device == dev) return e.occ;
+  for (int i = 0; i < used; ++i)
+    if (cache[i].func == k.func && cache[i].device == dev) return cache[i].occ;
   int occ = 0;
   if (cudaFuncSetAttribute(k.func, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem_bytes) !=
           cudaSuccess ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.func, k.threads, k.smem_bytes) !=
           cudaSuccess)
     return 0;
-  cache.push_back(Entry{k.func, dev, occ});
+  if (used < kEntries) cache[used++] = Entry{k.func, dev, occ};
   return occ;
 }
 
@@ -210,6 +225,70 @@ int kernel_occupancy(const DecodeKernel& k) {
 
 // Kernel variants a plan can launch.
 enum Variant { kPlain = 0, kTokenScales = 1, kUnifiedMax = 2, kNumVariants = 3 };
+
+namespace {
+
+// The kernels a plan of these dtypes and shape may launch (kPlain always,
+// the others where built) and the persistent grid's CTAs per SM: the
+// smallest occupancy among them, so that every variant fits the grid.
+int select_kernels(fa_dtype q_dtype, fa_dtype kv_dtype, int head_dim, int G, int q_len,
+                   DecodeKernel (&kv)[kNumVariants], bool (&has)[kNumVariants],
+                   int* ctas_per_sm, bool ragged = false) {
+  DecodeKernel base;
+  if (ragged) {
+    if (!find_ragged_q_kernel(q_dtype, kv_dtype, head_dim, G, q_len, &base))
+      return FA_ERR_UNSUPPORTED;
+  } else if (q_len == 1) {
+    if (!find_kernel(q_dtype, kv_dtype, head_dim, G, &base)) return FA_ERR_UNSUPPORTED;
+  } else {
+    bool ok = false;
+    if (q_dtype == FA_DTYPE_BF16 && kv_dtype == FA_DTYPE_BF16)
+      ok = fadecode::find_multi_token_kernel_bf16(head_dim, G, q_len, &base);
+    else if (q_dtype == FA_DTYPE_BF16 && kv_dtype == FA_DTYPE_E4M3)
+      ok = fadecode::find_multi_token_kernel_bf16_e4m3(head_dim, G, q_len, &base);
+    if (!ok) return FA_ERR_UNSUPPORTED;
+  }
+  int occ = kernel_occupancy(base);
+  if (occ == 0) return FA_ERR_CUDA;
+  kv[kPlain] = base;
+  has[kPlain] = true;
+  has[kTokenScales] = has[kUnifiedMax] = false;
+  if (q_len == 1 && !ragged) {
+    has[kTokenScales] = find_token_scale_kernel(q_dtype, kv_dtype, head_dim, G, &kv[kTokenScales]);
+    has[kUnifiedMax] = find_unified_max_kernel(q_dtype, kv_dtype, head_dim, G, &kv[kUnifiedMax]);
+  }
+  for (int v = 1; v < kNumVariants; ++v) {
+    if (!has[v]) continue;
+    const int occ_v = kernel_occupancy(kv[v]);
+    if (occ_v == 0) return FA_ERR_CUDA;
+    occ = std::min(occ, occ_v);
+  }
+  *ctas_per_sm = std::max(1, std::min(occ, kMaxCtasPerSmBound));
+  return FA_OK;
+}
+
+// Everything one decode launch needs, owned elsewhere: by a plan object, or
+// by the stack of the allocation-free entry point.
+struct LaunchView {
+  int batch = 0, hq = 0, hkv = 0, d = 0, page_size = 0, q_len = 1;
+  fa_dtype q_dtype = FA_DTYPE_F32, kv_dtype = FA_DTYPE_F32;
+  const DecodeKernel* kern = nullptr;
+  MapCache* map = nullptr;
+  const int32_t* indices = nullptr;
+  uint8_t* ws = nullptr;
+  Layout layout{};
+  int num_ctas = 0, num_merge = 0, pool_begin = 0, pool_count = 0;
+  bool fused_merge = true;
+  bool ragged_q = false;  // query rows per request from the plan's qo_indptr copy
+  cudaEvent_t ev_before = nullptr, ev_after = nullptr;
+};
+
+int launch_decode(const LaunchView& lv, const void* q, const void* paged_kv, int64_t num_pages,
+                  float sm_scale, float k_scale, float v_scale, const float* k_scales,
+                  const float* v_scales, float max_bound, void* o, float* lse,
+                  void* cuda_stream);
+
+}  // namespace
 
 struct fa_decode_plan_s;
 static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
@@ -233,7 +312,9 @@ struct fa_decode_plan_s {
   size_t ws_bytes = 0;
   Layout layout{};
   bool fused_merge = true;
-  int q_len = 1;
+  int q_len = 1;          // query tokens per request (ragged: the kernel's largest)
+  bool ragged_q = false;  // query rows from qo_indptr
+  int64_t total_q = 0;    // query rows of the batch
   // cached TMA descriptors of the KV cache, one per kernel variant
   MapCache map[kNumVariants];
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
@@ -265,7 +346,7 @@ size_t fa_decode_workspace_size(int batch, int num_qo_heads, int num_kv_heads, i
   const int64_t cuts = fadecode::max_plan_cuts(max_ctas);
   const int64_t segs = (int64_t)batch * num_kv_heads + cuts;
   const int G = num_qo_heads / num_kv_heads;
-  return make_layout(max_ctas, segs, cuts, 2 * cuts, G, head_dim).total;
+  return make_layout(max_ctas, segs, cuts, 2 * cuts, G, head_dim, (int64_t)batch + 1).total;
 }
 
 int fa_plan_work_host(const int32_t* indptr, const int32_t* last_page_len, int batch,
@@ -296,7 +377,8 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
                      const int32_t* last_page_len_host, int batch, int q_len, int num_qo_heads,
                      int num_kv_heads, int head_dim, int page_size, fa_dtype q_dtype,
                      fa_dtype kv_dtype, void* workspace_dev, size_t workspace_bytes,
-                     void* cuda_stream, fa_decode_plan_t* out_plan);
+                     void* cuda_stream, fa_decode_plan_t* out_plan,
+                     const int32_t* qo_indptr_host = nullptr);
 
 int fa_decode_plan(const int32_t* indptr_host, const int32_t* indices_dev,
                    const int32_t* last_page_len_host, int batch, int num_qo_heads,
@@ -315,9 +397,47 @@ int fa_decode_plan_multi_token(const int32_t* indptr_host, const int32_t* indice
                                size_t workspace_bytes, void* cuda_stream,
                                fa_decode_plan_t* out_plan) {
   if (q_len < 1) return FA_ERR_INVALID_ARG;
+  if (batch >= 0 && num_kv_heads > 0 && num_qo_heads % num_kv_heads == 0 &&
+      (num_qo_heads / num_kv_heads) * q_len > 8) {
+    // more columns than one MMA tile: the kernels with ragged query rows,
+    // every request holding q_len rows (the same q / o layout)
+    std::vector<int32_t> qo;
+    try {
+      qo.resize((size_t)batch + 1);
+    } catch (const std::bad_alloc&) {
+      return FA_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i <= batch; ++i) qo[i] = i * q_len;
+    return plan_impl(indptr_host, indices_dev, last_page_len_host, batch, q_len, num_qo_heads,
+                     num_kv_heads, head_dim, page_size, q_dtype, kv_dtype, workspace_dev,
+                     workspace_bytes, cuda_stream, out_plan, qo.data());
+  }
   return plan_impl(indptr_host, indices_dev, last_page_len_host, batch, q_len, num_qo_heads,
                    num_kv_heads, head_dim, page_size, q_dtype, kv_dtype, workspace_dev,
                    workspace_bytes, cuda_stream, out_plan);
+}
+
+int fa_decode_plan_ragged_q(const int32_t* indptr_host, const int32_t* indices_dev,
+                            const int32_t* last_page_len_host, const int32_t* qo_indptr_host,
+                            int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                            int page_size, fa_dtype q_dtype, fa_dtype kv_dtype,
+                            void* workspace_dev, size_t workspace_bytes, void* cuda_stream,
+                            fa_decode_plan_t* out_plan) {
+  if (!qo_indptr_host || batch < 0) return FA_ERR_INVALID_ARG;
+  int max_q = 1;
+  for (int i = 0; i < batch; ++i) max_q = std::max(max_q, qo_indptr_host[i + 1] - qo_indptr_host[i]);
+  return plan_impl(indptr_host, indices_dev, last_page_len_host, batch, max_q, num_qo_heads,
+                   num_kv_heads, head_dim, page_size, q_dtype, kv_dtype, workspace_dev,
+                   workspace_bytes, cuda_stream, out_plan, qo_indptr_host);
+}
+
+size_t fa_decode_workspace_size_ragged_q(int batch, int num_qo_heads, int num_kv_heads,
+                                         int head_dim) {
+  if (num_kv_heads <= 0 || num_qo_heads <= 0 || num_qo_heads % num_kv_heads) return 0;
+  // the widest ragged kernel holds 32 columns (group x query tokens)
+  const int G = num_qo_heads / num_kv_heads;
+  const int max_q = G <= 32 ? 32 / G : 1;
+  return fa_decode_workspace_size(batch, num_qo_heads * max_q, num_kv_heads, head_dim);
 }
 
 }  // extern "C"
@@ -326,7 +446,8 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
                      const int32_t* last_page_len_host, int batch, int q_len, int num_qo_heads,
                      int num_kv_heads, int head_dim, int page_size, fa_dtype q_dtype,
                      fa_dtype kv_dtype, void* workspace_dev, size_t workspace_bytes,
-                     void* cuda_stream, fa_decode_plan_t* out_plan) {
+                     void* cuda_stream, fa_decode_plan_t* out_plan,
+                     const int32_t* qo_indptr_host) {
   if (!out_plan) return FA_ERR_INVALID_ARG;
   *out_plan = nullptr;
   if (!indptr_host || batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
@@ -338,7 +459,23 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
   if (dtype_size(q_dtype) == 0 || dtype_size(kv_dtype) == 0) return FA_ERR_INVALID_ARG;
   const int G = num_qo_heads / num_kv_heads;
   if (page_size != fadecode::kPageSize) return FA_ERR_UNSUPPORTED;
-  if (q_len > 1) {
+  const bool ragged = qo_indptr_host != nullptr;
+  int64_t total_q = (int64_t)batch * q_len;
+  if (ragged) {
+    // request i has n_i = qo_indptr[i+1] - qo_indptr[i] query tokens, the
+    // last n_i positions of its cache (0 allowed: it contributes no rows)
+    if (qo_indptr_host[0] != 0) return FA_ERR_INVALID_ARG;
+    for (int i = 0; i < batch; ++i) {
+      const int64_t nq = (int64_t)qo_indptr_host[i + 1] - qo_indptr_host[i];
+      const int64_t np = (int64_t)indptr_host[i + 1] - indptr_host[i];
+      if (nq < 0 || nq > q_len) return FA_ERR_INVALID_ARG;
+      if (nq == 0) continue;
+      if (np <= 0 || last_page_len_host[i] < 1 || last_page_len_host[i] > page_size ||
+          (np - 1) * page_size + last_page_len_host[i] < nq)
+        return FA_ERR_INVALID_ARG;
+    }
+    total_q = qo_indptr_host[batch];
+  } else if (q_len > 1) {
     // every request must hold its q_len draft tokens
     for (int i = 0; i < batch; ++i) {
       const int64_t np = (int64_t)indptr_host[i + 1] - indptr_host[i];
@@ -347,39 +484,17 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
         return FA_ERR_INVALID_ARG;
     }
   }
-  DecodeKernel kern;
-  if (q_len == 1) {
-    if (!find_kernel(q_dtype, kv_dtype, head_dim, G, &kern)) return FA_ERR_UNSUPPORTED;
-  } else {
-    bool ok = false;
-    if (q_dtype == FA_DTYPE_BF16 && kv_dtype == FA_DTYPE_BF16)
-      ok = fadecode::find_multi_token_kernel_bf16(head_dim, G, q_len, &kern);
-    else if (q_dtype == FA_DTYPE_BF16 && kv_dtype == FA_DTYPE_E4M3)
-      ok = fadecode::find_multi_token_kernel_bf16_e4m3(head_dim, G, q_len, &kern);
-    if (!ok) return FA_ERR_UNSUPPORTED;
-  }
-
   int dev = 0, sms = 0, occ = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return FA_ERR_CUDA;
-  occ = kernel_occupancy(kern);
-  if (occ == 0) return FA_ERR_CUDA;
   // The persistent grid must fit for every variant a run may launch.
   DecodeKernel kv[kNumVariants];
   bool has[kNumVariants] = {true, false, false};
-  kv[kPlain] = kern;
-  if (q_len == 1) {
-    has[kTokenScales] = find_token_scale_kernel(q_dtype, kv_dtype, head_dim, G, &kv[kTokenScales]);
-    has[kUnifiedMax] = find_unified_max_kernel(q_dtype, kv_dtype, head_dim, G, &kv[kUnifiedMax]);
-  }
-  for (int v = 1; v < kNumVariants; ++v) {
-    if (!has[v]) continue;
-    const int occ_v = kernel_occupancy(kv[v]);
-    if (occ_v == 0) return FA_ERR_CUDA;
-    occ = std::min(occ, occ_v);
-  }
-  occ = std::max(1, std::min(occ, kMaxCtasPerSmBound));
+  const int sel = select_kernels(q_dtype, kv_dtype, head_dim, G, q_len, kv, has, &occ, ragged);
+  if (sel != FA_OK) return sel;
+  // query tokens a partial state holds columns for: the kernel's bucket
+  const int ql_kernel = kv[kPlain].q_len;
 
   fa_decode_plan_s* plan = new (std::nothrow) fa_decode_plan_s();
   if (!plan) return FA_ERR_INVALID_ARG;
@@ -402,7 +517,9 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
   plan->ws = static_cast<uint8_t*>(workspace_dev);
   plan->ws_bytes = workspace_bytes;
   plan->fused_merge = fused_merge_enabled();
-  plan->q_len = q_len;
+  plan->q_len = ragged ? ql_kernel : q_len;
+  plan->ragged_q = ragged;
+  plan->total_q = total_q;
 
   int rc = FA_OK;
   try {
@@ -418,7 +535,8 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
       }
       const WorkList& w = plan->wl;
       plan->layout = make_layout(w.num_ctas, (int64_t)w.segments.size(),
-                                 (int64_t)w.merge.size(), w.num_slots, G * q_len, head_dim);
+                                 (int64_t)w.merge.size(), w.num_slots, G * plan->q_len, head_dim,
+                                 ragged ? (int64_t)batch + 1 : 0);
       if (plan->layout.total <= workspace_bytes) {
         rc = FA_OK;
         break;
@@ -447,6 +565,9 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
   if (!wl.merge.empty())
     std::memcpy(meta.data() + plan->layout.off_merge, wl.merge.data(),
                 sizeof(fadecode::MergeUnit) * wl.merge.size());
+  if (ragged)
+    std::memcpy(meta.data() + plan->layout.off_qo, qo_indptr_host,
+                sizeof(int32_t) * ((size_t)batch + 1));
   if (fadecode::upload_async(plan->ws, meta.data(), meta.size(),
                              static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
     delete plan;
@@ -543,6 +664,8 @@ int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info) {
   i.tensor_cores = plan->kern[kPlain].tensor_cores ? 1 : 0;
   i.fused_merge = plan->fused_merge ? 1 : 0;
   i.q_len = plan->q_len;
+  i.ragged_q = plan->ragged_q ? 1 : 0;
+  i.total_q_rows = plan->total_q;
   i.unified_max = plan->has[kUnifiedMax] ? 1 : 0;
   i.num_pool_segments = plan->wl.pool_count();
   i.pool_pages = plan->wl.pool_pages;
@@ -586,66 +709,220 @@ int fa_decode_set_timing_events(fa_decode_plan_t plan, void* ev_before, void* ev
   return FA_OK;
 }
 
+int fa_library_get_stats(fa_library_stats* stats) {
+  if (!stats) return FA_ERR_INVALID_ARG;
+  fa_library_stats s;
+  std::memset(&s, 0, sizeof s);
+  fadecode::staging_stats(&s.pinned_host_allocations, &s.pinned_host_bytes, &s.staged_uploads);
+  *stats = s;
+  return FA_OK;
+}
+
 }  // extern "C"
+
+// ---- the allocation-free path behind fa_decode_static ---------------------
+//
+// The plan is built into fixed host arrays (no pool: a pool's chunk list is
+// sized at run time), laid out as the workspace's metadata image in a
+// file-scope host buffer, and copied into the caller-less scratch array with
+// one cudaMemcpyAsync from that pageable buffer: the driver stages a copy
+// from pageable memory before the call returns, so the buffer is free for
+// the next call at once and nothing is pinned or allocated.  The launch
+// state lives on the stack.  One mutex serialises the host side of calls.
+namespace {
+
+constexpr int kStaticMaxCtas = 8192;
+constexpr int kStaticMaxSegments = (int)(FA_STATIC_SCRATCH_BYTES / sizeof(fadecode::Segment));
+constexpr int kStaticMaxMerge = kStaticMaxCtas;
+
+std::mutex g_static_mu;
+int32_t g_static_cta[kStaticMaxCtas + 1];
+fadecode::Segment g_static_seg[kStaticMaxSegments];
+fadecode::MergeUnit g_static_merge[kStaticMaxMerge];
+alignas(256) uint8_t g_static_image[FA_STATIC_SCRATCH_BYTES];
+
+}  // namespace
+
+namespace fadecode {
+
+int static_decode(void* scratch, size_t scratch_bytes, const int32_t* indptr_host,
+                  const int32_t* indices_dev, const int32_t* last_page_len_host, int batch,
+                  int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                  fa_dtype q_dtype, fa_dtype kv_dtype, const void* q, const void* paged_kv,
+                  int64_t num_pages, float sm_scale, float k_scale, float v_scale, void* o,
+                  float* lse, void* cuda_stream) {
+  if (!scratch || !indptr_host || batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 ||
+      head_dim <= 0 || page_size <= 0 || num_qo_heads % num_kv_heads)
+    return FA_ERR_INVALID_ARG;
+  if (batch > 0 && !last_page_len_host) return FA_ERR_INVALID_ARG;
+  if (indptr_host[batch] > 0 && !indices_dev) return FA_ERR_INVALID_ARG;
+  if (dtype_size(q_dtype) == 0 || dtype_size(kv_dtype) == 0) return FA_ERR_INVALID_ARG;
+  if (page_size != fadecode::kPageSize) return FA_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  // the upload below is a copy from pageable memory, which a stream capture
+  // cannot record
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return FA_ERR_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) return FA_ERR_UNSUPPORTED;
+  const int G = num_qo_heads / num_kv_heads;
+
+  int dev = 0, sms = 0, occ = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FA_ERR_CUDA;
+  DecodeKernel kv[kNumVariants];
+  bool has[kNumVariants] = {true, false, false};
+  // the same kernels and grid as fa_decode_plan picks, so both paths give
+  // bitwise the same result
+  const int sel = select_kernels(q_dtype, kv_dtype, head_dim, G, 1, kv, has, &occ);
+  if (sel != FA_OK) return sel;
+
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  FixedWorkList fw;
+  fw.cta_offsets = g_static_cta;
+  fw.segments = g_static_seg;
+  fw.merge = g_static_merge;
+  fw.cta_capacity = kStaticMaxCtas;
+  fw.segment_capacity = kStaticMaxSegments;
+  fw.merge_capacity = kStaticMaxMerge;
+  const int prc = build_work_list_fixed(indptr_host, last_page_len_host, batch, num_kv_heads,
+                                        page_size, std::min(sms * occ, kStaticMaxCtas),
+                                        kMinPagesPerCta, &fw);
+  if (prc == -2) return FA_ERR_WORKSPACE_TOO_SMALL;
+  if (prc != 0) return FA_ERR_INVALID_ARG;
+  const Layout L = make_layout(fw.num_ctas, fw.num_segments, fw.num_merge, fw.num_slots, G,
+                               head_dim);
+  if (L.total > scratch_bytes || L.meta_bytes > sizeof(g_static_image))
+    return FA_ERR_WORKSPACE_TOO_SMALL;
+  if (batch == 0) return FA_OK;
+
+  std::memset(g_static_image, 0, L.meta_bytes);
+  std::memcpy(g_static_image + L.off_cta, g_static_cta,
+              sizeof(int32_t) * ((size_t)fw.num_ctas + 1));
+  std::memcpy(g_static_image + L.off_seg, g_static_seg,
+              sizeof(Segment) * (size_t)fw.num_segments);
+  std::memcpy(g_static_image + L.off_merge, g_static_merge,
+              sizeof(MergeUnit) * (size_t)fw.num_merge);
+  if (cudaMemcpyAsync(scratch, g_static_image, L.meta_bytes, cudaMemcpyHostToDevice, st) !=
+      cudaSuccess)
+    return FA_ERR_CUDA;
+
+  MapCache map;
+  LaunchView lv;
+  lv.batch = batch;
+  lv.hq = num_qo_heads;
+  lv.hkv = num_kv_heads;
+  lv.d = head_dim;
+  lv.page_size = page_size;
+  lv.q_len = 1;
+  lv.q_dtype = q_dtype;
+  lv.kv_dtype = kv_dtype;
+  lv.kern = &kv[kPlain];
+  lv.map = &map;
+  lv.indices = indices_dev;
+  lv.ws = static_cast<uint8_t*>(scratch);
+  lv.layout = L;
+  lv.num_ctas = fw.num_ctas;
+  lv.num_merge = fw.num_merge;
+  lv.fused_merge = fused_merge_enabled();
+  return launch_decode(lv, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, nullptr,
+                       nullptr, 0.f, o, lse, cuda_stream);
+}
+
+}  // namespace fadecode
 
 static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
                     const void* paged_kv, int64_t num_pages, float sm_scale, float k_scale,
                     float v_scale, const float* k_scales, const float* v_scales,
                     float max_bound, void* o, float* lse, void* cuda_stream) {
-  if (plan->batch == 0) return FA_OK;
+  LaunchView lv;
+  lv.batch = plan->batch;
+  lv.hq = plan->hq;
+  lv.hkv = plan->hkv;
+  lv.d = plan->d;
+  lv.page_size = plan->page_size;
+  lv.q_len = plan->q_len;
+  lv.q_dtype = plan->q_dtype;
+  lv.kv_dtype = plan->kv_dtype;
+  lv.kern = &plan->kern[variant];
+  lv.map = &plan->map[variant];
+  lv.indices = plan->indices;
+  lv.ws = plan->ws;
+  lv.layout = plan->layout;
+  lv.num_ctas = plan->wl.num_ctas;
+  lv.num_merge = (int)plan->wl.merge.size();
+  lv.pool_begin = plan->wl.pool_begin();
+  lv.pool_count = plan->wl.pool_count();
+  lv.fused_merge = plan->fused_merge;
+  lv.ragged_q = plan->ragged_q;
+  lv.ev_before = plan->ev_before;
+  lv.ev_after = plan->ev_after;
+  return launch_decode(lv, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, k_scales,
+                       v_scales, max_bound, o, lse, cuda_stream);
+}
+
+namespace {
+
+int launch_decode(const LaunchView& lv, const void* q, const void* paged_kv, int64_t num_pages,
+                  float sm_scale, float k_scale, float v_scale, const float* k_scales,
+                  const float* v_scales, float max_bound, void* o, float* lse,
+                  void* cuda_stream) {
+  if (lv.batch == 0) return FA_OK;
   if (!q || !paged_kv || !o || num_pages <= 0) return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(paged_kv) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
     return FA_ERR_INVALID_ARG;
   if (2 * num_pages > (int64_t)0xffffffffLL) return FA_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  const DecodeKernel& kern = plan->kern[variant];
-  MapCache& mc = plan->map[variant];
-  const int D = plan->d;
-  int rc = kv_tensor_map(&mc, kern, plan->kv_dtype, paged_kv, num_pages, D, plan->hkv,
-                         plan->page_size);
+  const DecodeKernel& kern = *lv.kern;
+  MapCache& mc = *lv.map;
+  const int D = lv.d;
+  int rc = kv_tensor_map(&mc, kern, lv.kv_dtype, paged_kv, num_pages, D, lv.hkv, lv.page_size);
   if (rc != FA_OK) return rc;
 
   if (!(sm_scale > 0.f)) sm_scale = 1.0f / std::sqrt((float)D);
+  uint8_t* ws = lv.ws;
+  const Layout& L = lv.layout;
   DecodeParams prm;
   std::memset(&prm, 0, sizeof prm);
   prm.q = q;
   prm.o = o;
   prm.lse = lse;
-  prm.indices = plan->indices;
-  prm.cta_offsets = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_cta);
-  prm.segments = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_seg);
-  prm.part_o = reinterpret_cast<float*>(plan->ws + plan->layout.off_part_o);
-  prm.part_lse = reinterpret_cast<float*>(plan->ws + plan->layout.off_part_lse);
-  prm.err = reinterpret_cast<int*>(plan->ws + plan->layout.off_err);
-  prm.merge = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_merge);
-  prm.merge_count = reinterpret_cast<int*>(plan->ws + plan->layout.off_count);
-  prm.fused_merge = plan->fused_merge ? 1 : 0;
+  prm.indices = lv.indices;
+  prm.cta_offsets = reinterpret_cast<const int32_t*>(ws + L.off_cta);
+  prm.segments = reinterpret_cast<const int32_t*>(ws + L.off_seg);
+  prm.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
+  prm.part_lse = reinterpret_cast<float*>(ws + L.off_part_lse);
+  prm.err = reinterpret_cast<int*>(ws + L.off_err);
+  prm.merge = reinterpret_cast<const int32_t*>(ws + L.off_merge);
+  prm.merge_count = reinterpret_cast<int*>(ws + L.off_count);
+  prm.fused_merge = lv.fused_merge ? 1 : 0;
   prm.k_scales = k_scales;
   prm.v_scales = v_scales;
   prm.num_pages = num_pages;
-  prm.num_qo_heads = plan->hq;
-  prm.num_kv_heads = plan->hkv;
-  prm.q_len = plan->q_len;
-  prm.q_row_bytes = D * dtype_size(plan->q_dtype);
+  prm.num_qo_heads = lv.hq;
+  prm.num_kv_heads = lv.hkv;
+  prm.q_len = lv.q_len;
+  prm.qo_indptr = lv.ragged_q ? reinterpret_cast<const int32_t*>(ws + L.off_qo) : nullptr;
+  prm.q_row_bytes = D * dtype_size(lv.q_dtype);
   prm.kv = paged_kv;
-  prm.kv_row_bytes = D * dtype_size(plan->kv_dtype);
+  prm.kv_row_bytes = D * dtype_size(lv.kv_dtype);
   prm.q_scale = sm_scale * k_scale * kLog2e;
   prm.v_scale = v_scale;
   prm.max_bound = max_bound * kLog2e;
-  prm.um_fallbacks = reinterpret_cast<int*>(plan->ws + plan->layout.off_umc);
-  prm.pool_begin = plan->wl.pool_begin();
-  prm.pool_count = plan->wl.pool_count();
-  prm.pool_claim = reinterpret_cast<int*>(plan->ws + plan->layout.off_pool);
+  prm.um_fallbacks = reinterpret_cast<int*>(ws + L.off_umc);
+  prm.pool_begin = lv.pool_begin;
+  prm.pool_count = lv.pool_count;
+  prm.pool_claim = reinterpret_cast<int*>(ws + L.off_pool);
   prm.pool_done = prm.pool_claim + 1;
 
-  const bool timed = plan->ev_before && plan->ev_after;
-  if (timed && cudaEventRecord(plan->ev_before, st) != cudaSuccess) return FA_ERR_CUDA;
+  const bool timed = lv.ev_before && lv.ev_after;
+  if (timed && cudaEventRecord(lv.ev_before, st) != cudaSuccess) return FA_ERR_CUDA;
   void* args[2] = {&mc.tmap, &prm};
   // A programmatic dependent launch: the kernel's CTAs may be placed while
   // the previous kernel in the stream drains; they read nothing global
   // before it has completed (griddepcontrol.wait).
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(plan->wl.num_ctas);
+  cfg.gridDim = dim3(lv.num_ctas);
   cfg.blockDim = dim3(kern.threads);
   cfg.dynamicSmemBytes = (size_t)kern.smem_bytes;
   cfg.stream = st;
@@ -655,19 +932,22 @@ static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelExC(&cfg, kern.func, args) != cudaSuccess) return FA_ERR_CUDA;
-  if (timed && cudaEventRecord(plan->ev_after, st) != cudaSuccess) return FA_ERR_CUDA;
-  if (!plan->fused_merge && !plan->wl.merge.empty()) {
+  if (timed && cudaEventRecord(lv.ev_after, st) != cudaSuccess) return FA_ERR_CUDA;
+  if (!lv.fused_merge && lv.num_merge > 0) {
     MergeParams mp;
-    mp.merge = reinterpret_cast<const int32_t*>(plan->ws + plan->layout.off_merge);
+    mp.merge = reinterpret_cast<const int32_t*>(ws + L.off_merge);
+    mp.qo_indptr = prm.qo_indptr;
     mp.part_o = prm.part_o;
     mp.part_lse = prm.part_lse;
     mp.o = o;
     mp.lse = lse;
-    mp.num_qo_heads = plan->hq;
+    mp.num_qo_heads = lv.hq;
     void* margs[1] = {&mp};
-    if (cudaLaunchKernel(kern.merge_func, dim3((unsigned)plan->wl.merge.size()), dim3(128), margs,
-                         0, st) != cudaSuccess)
+    if (cudaLaunchKernel(kern.merge_func, dim3((unsigned)lv.num_merge), dim3(128), margs, 0,
+                         st) != cudaSuccess)
       return FA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+
+}  // namespace

@@ -259,8 +259,7 @@ __global__ void __launch_bounds__(PrefixCfg<QT, D, NW>::THREADS)
       mma::mma16816<kBf16>(o[2 * n2], pa[0], pa[1], pa[2], pa[3], b0, b1);
       mma::mma16816<kBf16>(o[2 * n2 + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
     }
-    __syncwarp();
-    if (lane == 0) dev::mbar_arrive(dev::smem_addr(&empty[stage]));
+    dev::release_stage(dev::smem_addr(&empty[stage]), lane);
   }
 
   // ---- partial state of this chunk, per row: o / d and log2-sum-exp

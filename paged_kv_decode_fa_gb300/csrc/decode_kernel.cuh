@@ -131,6 +131,21 @@ __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// Hand a ring stage back to the producer once this warp has read it with
+// generic-proxy loads (ld.shared, ldmatrix).  The producer refills the stage
+// with a TMA copy, an async-proxy write; without a proxy fence between the
+// reads and the release, that write can land before the reads are
+// performed, and the warp then reads part of the next page (seen on GB300
+// as V bytes of the next page under correct K bytes, a few units per
+// hundred thousand on the E4M3 consumer with thousands of short segments;
+// none with the fence).
+// All lanes fence, then lane 0 arrives once the warp has converged.
+__device__ __forceinline__ void release_stage(uint32_t empty_bar, int lane) {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty_bar);
+}
+
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map,
                                             int c0, int c1, int c2, int c3,
                                             uint32_t bar, uint64_t policy) {
@@ -356,6 +371,29 @@ __device__ __forceinline__ void seg_queue_init(SegQueue* q, int consumer_warps) 
   }
 }
 
+// q rows of request `req` (first row and count): ragged from qo_indptr (plan
+// data, uploaded with the work list) or q_len per request.
+__device__ __forceinline__ int2 request_q_rows(const DecodeParams& p, int req) {
+  if (p.qo_indptr) {
+    const int a = p.qo_indptr[req];
+    return make_int2(a, p.qo_indptr[req + 1] - a);
+  }
+  return make_int2(req * p.q_len, p.q_len);
+}
+
+// Bring one segment's q rows (G heads of each of its request's query
+// tokens) into L2, 128-byte lines spread over the warp's lanes.
+__device__ __forceinline__ void prefetch_q_rows(const DecodeParams& p, int req, int kvh, int lane) {
+  const int G = p.num_qo_heads / p.num_kv_heads;
+  const int lines = (G * p.q_row_bytes + 127) / 128;  // one query token's rows
+  const int2 qr = request_q_rows(p, req);
+  for (int i = 0; i < qr.y; ++i) {
+    const char* rows = static_cast<const char*>(p.q) +
+                       (((size_t)qr.x + i) * p.num_qo_heads + (size_t)kvh * G) * p.q_row_bytes;
+    for (int l = lane; l < lines; l += 32) dev::prefetch_l2(rows + (size_t)l * 128);
+  }
+}
+
 // Before a programmatic dependent launch's wait: the CTA's first segment
 // record (plan data) and, into L2, the page ids of its first 64 pages, the
 // K and V rows of its first two pages and its q rows - data a preceding
@@ -379,16 +417,7 @@ __device__ __forceinline__ void prefetch_first_segment(const DecodeParams& p, in
       for (int l = 0; l < lines; ++l) dev::prefetch_l2(row + (size_t)l * 128);
     }
   }
-  if (p.q_row_bytes > 0) {
-    const int G = p.num_qo_heads / p.num_kv_heads;
-    const int lines = (G * p.q_row_bytes + 127) / 128;  // one query token's rows
-    for (int i = 0; i < p.q_len; ++i) {
-      const char* rows = static_cast<const char*>(p.q) +
-                         (((size_t)sa.x * p.q_len + i) * p.num_qo_heads + (size_t)kvh * G) *
-                             p.q_row_bytes;
-      for (int l = lane; l < lines; l += 32) dev::prefetch_l2(rows + (size_t)l * 128);
-    }
-  }
+  if (p.q_row_bytes > 0) prefetch_q_rows(p, sa.x, kvh, lane);
 }
 
 // Producer warp: walks the CTA's segments page by page, reads the page ids
@@ -464,16 +493,7 @@ __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const Deco
     const int kvh = sa.y, pb = sa.z, pe = sa.w;
     // The consumers read this segment's q rows when they reach it, several
     // pages from now: bring them into L2 while the pages are in flight.
-    if (p.q_row_bytes > 0) {
-      const int G = p.num_qo_heads / p.num_kv_heads;
-      const int lines = (G * p.q_row_bytes + 127) / 128;  // one query token's rows
-      for (int i = 0; i < p.q_len; ++i) {
-        const char* rows = static_cast<const char*>(p.q) +
-                           (((size_t)sa.x * p.q_len + i) * p.num_qo_heads + (size_t)kvh * G) *
-                               p.q_row_bytes;
-        for (int l = lane; l < lines; l += 32) dev::prefetch_l2(rows + (size_t)l * 128);
-      }
-    }
+    if (p.q_row_bytes > 0) prefetch_q_rows(p, sa.x, kvh, lane);
     for (int p0 = pb; p0 < pe; p0 += 32) {
       const int cnt = min(32, pe - p0);
       int id = lane < cnt ? __ldg(p.indices + p0 + lane) : 0;
@@ -525,8 +545,10 @@ __device__ __forceinline__ void produce_pages(const CUtensorMap* map, const Deco
 // Next segment for a consumer warp: the CTA's static segments in order, then
 // the pool segments its producer claimed, -1 when none is left.  A pool
 // segment first consumes the empty stages the producer inserted before it
-// (those of this warp) and moves kbase to the aligned start.  Warp-uniform.
-template <int S, int NW>
+// (those of this warp) and moves kbase to the aligned start.  With the
+// column split (CS) every warp consumes every page and pool segments need no
+// alignment.  Warp-uniform.
+template <int S, int NW, bool CS = false>
 __device__ __forceinline__ int next_segment(const DecodeParams& p, SegQueue* queue, int& si,
                                             int seg_end, int& taken, int& kbase,
                                             uint64_t* full, uint64_t* empty, int warp, int lane,
@@ -542,7 +564,7 @@ __device__ __forceinline__ int next_segment(const DecodeParams& p, SegQueue* que
   if (lane == 0) dev::mbar_arrive(dev::smem_addr(&queue->empty[slot]));
   ++taken;
   if (cur < 0) return -1;
-  const int ka = (kbase + NW - 1) / NW * NW;
+  const int ka = CS ? kbase : (kbase + NW - 1) / NW * NW;
   for (int k = kbase; k < ka; ++k) {
     if (k % NW != warp) continue;
     dev::mbar_wait(dev::smem_addr(&full[k % S]), (uint32_t)((k / S) & 1), aborted, p.err);
@@ -573,20 +595,40 @@ __device__ __forceinline__ void pool_finish(const DecodeParams& p) {
 // element); then every output element issues its num_slots loads at once.
 // Runs on `nthreads` threads numbered `tid`, which synchronise on named
 // barrier `bar` (0 = __syncthreads).
-// Output row of column n of a (request, kv head) unit: the unit's columns
-// are the G heads of the group times the QL query tokens, token-major.
-template <int G, int QL>
-__device__ __forceinline__ size_t out_row(int req, int kvh, int n, int num_qo_heads) {
-  return ((size_t)req * QL + n / G) * num_qo_heads + kvh * G + n % G;
+// Query rows of a request: the first row q0 of q / o / lse and the number
+// of columns in use, G heads x its query tokens.  Ragged (RQ): request i owns
+// rows qo_indptr[i] .. qo_indptr[i+1] (section "Ragged attention" of the page
+// "FlashDecoding + FlashInfer" applied to the queries); otherwise every
+// request has QL rows.
+struct QRows {
+  int q0, ncols;
+};
+template <int G, int QL, bool RQ>
+__device__ __forceinline__ QRows query_rows(const int32_t* qo_indptr, int req) {
+  if constexpr (RQ) {
+    const int a = __ldg(qo_indptr + req);
+    return QRows{a, G * (__ldg(qo_indptr + req + 1) - a)};
+  } else {
+    return QRows{req * QL, G * QL};
+  }
 }
 
-template <typename QT, int D, int NC, int G, int QL>
+// Output row of column n of a (request, kv head) unit: the unit's columns
+// are the G heads of the group times its query tokens, token-major.
+template <int G>
+__device__ __forceinline__ size_t out_row(int q0, int kvh, int n, int num_qo_heads) {
+  return ((size_t)q0 + n / G) * num_qo_heads + kvh * G + n % G;
+}
+
+template <typename QT, int D, int NC, int G, int QL, bool RQ = false>
 __device__ __forceinline__ void fold_split_unit(const float* part_o, const float* part_lse,
                                                 int4 u, QT* obase, float* lse_out, int num_qo_heads,
+                                                const int32_t* qo_indptr,
                                                 float* scratch, int scratch_floats, int tid,
                                                 int nthreads, int bar) {
   static_assert(NC == G * QL, "columns = heads of the group x query tokens");
-  const int req = u.x, kvh = u.y, s0 = u.z, ns = u.w;
+  const int kvh = u.y, s0 = u.z, ns = u.w;
+  const QRows qr = query_rows<G, QL, RQ>(qo_indptr, u.x);
   if (ns * NC <= scratch_floats) {
     auto sync = [&]() {
       if (bar == 0) __syncthreads(); else dev::named_barrier(bar, nthreads);
@@ -608,15 +650,15 @@ __device__ __forceinline__ void fold_split_unit(const float* part_o, const float
         }
       const float inv = den > 0.f ? 1.f / den : 0.f;
       for (int k = 0; k < ns; ++k) scratch[k * NC + h] = M != -INFINITY ? scratch[k * NC + h] * inv : 0.f;
-      if (lse_out)
-        lse_out[out_row<G, QL>(req, kvh, h, num_qo_heads)] =
+      if (lse_out && h < qr.ncols)
+        lse_out[out_row<G>(qr.q0, kvh, h, num_qo_heads)] =
             M != -INFINITY ? (M + dev::fast_log2(den)) * dev::kLn2 : -INFINITY;
     }
     sync();
     // four consecutive dims per thread (16-byte loads), eight pieces in
     // flight: a unit of many pieces is bound by load latency otherwise
     static_assert(D % 4 == 0, "float4 rows");
-    for (int e = tid; e < NC * D / 4; e += nthreads) {
+    for (int e = tid; e < qr.ncols * D / 4; e += nthreads) {
       const int h = e / (D / 4), d4 = (e % (D / 4)) * 4;
       const float4* po = reinterpret_cast<const float4*>(part_o + ((size_t)s0 * NC + h) * D + d4);
       const size_t stride = (size_t)NC * D / 4;  // float4s between pieces
@@ -643,7 +685,7 @@ __device__ __forceinline__ void fold_split_unit(const float* part_o, const float
         num.z = fmaf(v.z, w, num.z);
         num.w = fmaf(v.w, w, num.w);
       }
-      QT* orow = obase + out_row<G, QL>(req, kvh, h, num_qo_heads) * D + d4;
+      QT* orow = obase + out_row<G>(qr.q0, kvh, h, num_qo_heads) * D + d4;
       orow[0] = dev::from_float<QT>(num.x);
       orow[1] = dev::from_float<QT>(num.y);
       orow[2] = dev::from_float<QT>(num.z);
@@ -651,7 +693,7 @@ __device__ __forceinline__ void fold_split_unit(const float* part_o, const float
     }
     return;
   }
-  for (int e = tid; e < NC * D; e += nthreads) {
+  for (int e = tid; e < qr.ncols * D; e += nthreads) {
     const int h = e / D, dd = e % D;
     float M = -INFINITY;
     for (int k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(part_lse + (size_t)(s0 + k) * NC + h));
@@ -666,7 +708,7 @@ __device__ __forceinline__ void fold_split_unit(const float* part_o, const float
       out = num / den;
       lse2 = M + dev::fast_log2(den);
     }
-    const size_t row = out_row<G, QL>(req, kvh, h, num_qo_heads);
+    const size_t row = out_row<G>(qr.q0, kvh, h, num_qo_heads);
     obase[row * D + dd] = dev::from_float<QT>(out);
     if (dd == 0 && lse_out) lse_out[row] = lse2 * dev::kLn2;
   }
@@ -687,7 +729,7 @@ constexpr int kFoldListBytes = (int)((sizeof(FoldList) + 15) / 16 * 16);
 // on the list for fold_pending.  All consumer threads, between consumer
 // barriers.  Folding here, with the producer's copies of the next pages in
 // flight, keeps the folds out of the launch's tail.
-template <typename QT, int D, int G, int NW, int QL = 1>
+template <typename QT, int D, int G, int NW, int QL = 1, bool RQ = false>
 __device__ __forceinline__ void fold_listed(const DecodeParams& p, FoldList* folds,
                                             float* scratch, int scratch_floats) {
   constexpr int CT = NW * 32;
@@ -702,8 +744,9 @@ __device__ __forceinline__ void fold_listed(const DecodeParams& p, FoldList* fol
       kept += 1;  // same decision in every thread
       continue;
     }
-    fold_split_unit<QT, D, NC, G, QL>(p.part_o, p.part_lse, u, static_cast<QT*>(p.o), p.lse,
-                                      p.num_qo_heads, scratch, scratch_floats, threadIdx.x, CT, 1);
+    fold_split_unit<QT, D, NC, G, QL, RQ>(p.part_o, p.part_lse, u, static_cast<QT*>(p.o), p.lse,
+                                          p.num_qo_heads, p.qo_indptr, scratch, scratch_floats,
+                                          threadIdx.x, CT, 1);
     dev::named_barrier(1, CT);  // scratch free for the next unit
   }
   if (kept) {  // compact the list (thread 0; the others have read it above)
@@ -722,36 +765,40 @@ __device__ __forceinline__ void fold_listed(const DecodeParams& p, FoldList* fol
   dev::named_barrier(1, CT);
 }
 
-// Combine the NW consumer warps' states of one segment for all NC columns
-// (unnormalised o in mo[w][h][d] against the warp's max mm[w][h], sum
-// md[w][h], all log2 domain) with the merge rule and write either the final
-// o (q dtype) and lse, or an fp32 partial slot.  Runs on the NW*32 consumer
+// Combine the NS states of one segment for all NC columns (unnormalised o in
+// mo[w][h][d] against the state's max mm[w][h], sum md[w][h], all log2
+// domain; NS = NW when the warps split the pages, 1 when each warp owns its
+// columns) with the merge rule and write either the final o (q dtype) and
+// lse of the columns in use, or an fp32 partial slot.  Runs on the NW*32 consumer
 // threads after a consumer barrier and ends with one (mo is free again).
 // A split piece is then counted by thread 0 alone while the other warps go
 // on: the piece that completes its unit puts the unit on the CTA's fold list,
 // folded at the next segment's combine (fold_listed, with `scratch`) or
 // after the CTA's last segment (fold_pending), so no warp waits for the
 // count's round trip.
-template <typename QT, int D, int G, int NW, int QL = 1>
+template <typename QT, int D, int G, int NW, int QL = 1, bool RQ = false, int NS = NW>
 __device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const float* mo,
-                                                 const float* mm, const float* md, int req,
+                                                 const float* mm, const float* md, QRows qr,
                                                  int kvh, int out_slot, int merge_unit,
                                                  FoldList* folds, float* scratch,
                                                  int scratch_floats) {
   constexpr int CT = NW * 32;
   constexpr int NC = G * QL;  // columns: heads of the group x query tokens
   QT* __restrict__ obase = static_cast<QT*>(p.o);
-  fold_listed<QT, D, G, NW, QL>(p, folds, scratch, scratch_floats);
-  for (int e = threadIdx.x; e < NC * D; e += CT) {
+  fold_listed<QT, D, G, NW, QL, RQ>(p, folds, scratch, scratch_floats);
+  // a split piece stores every column of its slot; final rows only the
+  // columns in use
+  const int cols = out_slot < 0 ? qr.ncols : NC;
+  for (int e = threadIdx.x; e < cols * D; e += CT) {
     const int h = e / D, dd = e % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, mm[w * NC + h]);
+    for (int w = 0; w < NS; ++w) M = fmaxf(M, mm[w * NC + h]);
     float out = 0.f, lse2 = -INFINITY;
     if (M != -INFINITY) {
       float den = 0.f, num = 0.f;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) {
+      for (int w = 0; w < NS; ++w) {
         const float sw = dev::fast_exp2(mm[w * NC + h] - M);
         den = fmaf(md[w * NC + h], sw, den);
         num = fmaf(mo[(w * NC + h) * D + dd], sw, num);
@@ -760,7 +807,7 @@ __device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const fl
       lse2 = M + dev::fast_log2(den);
     }
     if (out_slot < 0) {
-      const size_t row = out_row<G, QL>(req, kvh, h, p.num_qo_heads);
+      const size_t row = out_row<G>(qr.q0, kvh, h, p.num_qo_heads);
       obase[row * D + dd] = dev::from_float<QT>(out);
       if (dd == 0 && p.lse) p.lse[row] = lse2 * dev::kLn2;
     } else {
@@ -784,24 +831,26 @@ __device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const fl
   }
   // list full (a CTA that completed very many units): fold this one now,
   // on this thread alone
-  fold_split_unit<QT, D, NC, G, QL>(p.part_o, p.part_lse, u, obase, p.lse, p.num_qo_heads,
-                                    nullptr, 0, 0, 1, 1);
+  fold_split_unit<QT, D, NC, G, QL, RQ>(p.part_o, p.part_lse, u, obase, p.lse, p.num_qo_heads,
+                                        p.qo_indptr, nullptr, 0, 0, 1, 1);
 }
 
 // After a CTA's last segment: fold the split units it completed, in the
 // order it completed them; each fold combines the unit's pieces in slot
 // order, so the result does not depend on which CTA folds.  Consumer
 // threads only; mo serves as scratch.
-template <typename QT, int D, int G, int NW, int QL = 1>
-__device__ __forceinline__ void fold_pending(const DecodeParams& p, float* mo, FoldList* folds) {
+template <typename QT, int D, int G, int NW, int QL = 1, bool RQ = false>
+__device__ __forceinline__ void fold_pending(const DecodeParams& p, float* mo, FoldList* folds,
+                                             int scratch_floats) {
   constexpr int CT = NW * 32;
   constexpr int NC = G * QL;
   dev::named_barrier(1, CT);  // thread 0's list is complete
   const int n = folds->n;
   for (int i = 0; i < n; ++i) {
     const int4 u = reinterpret_cast<const int4*>(p.merge)[folds->unit[i]];
-    fold_split_unit<QT, D, NC, G, QL>(p.part_o, p.part_lse, u, static_cast<QT*>(p.o), p.lse,
-                                      p.num_qo_heads, mo, NW * NC * D, threadIdx.x, CT, 1);
+    fold_split_unit<QT, D, NC, G, QL, RQ>(p.part_o, p.part_lse, u, static_cast<QT*>(p.o), p.lse,
+                                          p.num_qo_heads, p.qo_indptr, mo, scratch_floats,
+                                          threadIdx.x, CT, 1);
     dev::named_barrier(1, CT);  // scratch free for the next unit
   }
 }
@@ -987,8 +1036,7 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
             for (int v = 0; v < VEC; ++v) acc[h][v] = fmaf(pj[h], vf[v], acc[h][v]);
         }
       }
-      __syncwarp();
-      if (lane == 0) dev::mbar_arrive(dev::smem_addr(&empty[stage]));
+      dev::release_stage(dev::smem_addr(&empty[stage]), lane);
     }
 
     // Sum the row groups of this warp (they share m and d).
@@ -1012,22 +1060,23 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
     dev::named_barrier(1, CT);
 
     // Merge the NW warp states of this segment and emit.
-    combine_and_emit<QT, D, G, NW>(p, mo, mm, md, req, kvh, out_slot, sb.z, folds,
+    combine_and_emit<QT, D, G, NW>(p, mo, mm, md, QRows{req, G}, kvh, out_slot, sb.z, folds,
                                    reinterpret_cast<float*>(smem + C::OFF_P), NW * P * G);
     kbase += npg;
   }
-  fold_pending<QT, D, G, NW>(p, mo, folds);
+  fold_pending<QT, D, G, NW>(p, mo, folds, NW * G * D);
   if (threadIdx.x == 0) pool_finish(p);
 }
 
 // Split-level merge as a separate kernel: one CTA per (request, kv head)
 // that the planner split folds its partial states with the merge rule.
-template <typename QT, int D, int G, int QL = 1>
+template <typename QT, int D, int G, int QL = 1, bool RQ = false>
 __global__ void __launch_bounds__(128) fa_merge_partials_kernel(const MergeParams p) {
   __shared__ float weights[2048];
   const int4 u = reinterpret_cast<const int4*>(p.merge)[blockIdx.x];
-  fold_split_unit<QT, D, G * QL, G, QL>(p.part_o, p.part_lse, u, static_cast<QT*>(p.o), p.lse,
-                                        p.num_qo_heads, weights, 2048, threadIdx.x, blockDim.x, 0);
+  fold_split_unit<QT, D, G * QL, G, QL, RQ>(p.part_o, p.part_lse, u, static_cast<QT*>(p.o),
+                                            p.lse, p.num_qo_heads, p.qo_indptr, weights, 2048,
+                                            threadIdx.x, blockDim.x, 0);
 }
 
 template <typename QT, typename KVT, int D, int G, int NW = 4>

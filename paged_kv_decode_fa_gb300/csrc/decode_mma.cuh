@@ -52,6 +52,30 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// m16n8k32 with E4M3 A and B (fp32 accumulate): four 8-bit elements per
+// register, element i in byte i.
+__device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four floats -> four E4M3 codes (round to nearest even, saturating at
+// 448), element i in byte i.
+__device__ __forceinline__ uint32_t f32x4_to_e4m3x4(float e0, float e1, float e2, float e3) {
+  uint32_t out;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(out)
+      : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
+  return out;
+}
+
 template <bool kBf16>
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -120,6 +144,13 @@ __device__ __forceinline__ float2 unpack2(uint32_t w, bool bf16) {
 template <typename QT, typename KVT, int D, int G, int NW, bool TS = false, int QL = 1>
 struct MmaCfg {
   static constexpr int NC = G * QL;  // MMA columns: heads of the group x query tokens
+  // Column split: with more than 8 columns every consumer warp takes every
+  // page of a segment and owns 8 columns of its own (warp w: columns
+  // 8w .. 8w+7), so no warp holds more than one 8-column accumulator tile
+  // and a column's state never needs merging across warps.  With at most 8
+  // columns the warps split the pages instead (page k to warp k % NW).
+  static constexpr bool CS = NC > 8;
+  static constexpr int NS = CS ? 1 : NW;  // partial states per column at a segment's end
   static constexpr int P = kPageSize;
   static constexpr int KV_ES = sizeof(KVT);
   static constexpr bool kFp8 = KV_ES == 1;
@@ -141,7 +172,8 @@ struct MmaCfg {
   static constexpr int RING_BYTES = KV_ES == 1 ? 32768 : (NC >= 8 ? 49152 : 65536);
   static constexpr int SPW0 = RING_BYTES / STAGE_BYTES / NW;
   static constexpr int SPW = SPW0 < 1 ? 1 : (SPW0 > 4 ? 4 : SPW0);
-  static constexpr int S = SPW * NW;
+  // column split: every warp reads every stage, any number of stages works
+  static constexpr int S = CS ? RING_BYTES / STAGE_BYTES : SPW * NW;
   static constexpr int THREADS = (NW + 1) * 32;
   // CTAs per SM the ring size is chosen for; the register budget must allow it
   static constexpr int MIN_CTAS = KV_ES == 1 ? 4 : 3;
@@ -149,17 +181,17 @@ struct MmaCfg {
   static constexpr int OFF_EMPTY = OFF_FULL + 8 * S;
   static constexpr int OFF_PT = OFF_EMPTY + 8 * S;          // [NW][8 heads][16 tokens] 16-bit
   static constexpr int OFF_MO = OFF_PT + NW * 8 * P * 2;
-  static constexpr int OFF_MM = OFF_MO + 4 * NW * NC * D;
-  static constexpr int OFF_MD = OFF_MM + 4 * NW * NC;
-  static constexpr int OFF_FOLDS = OFF_MD + 4 * NW * NC;
+  static constexpr int OFF_MM = OFF_MO + 4 * NS * NC * D;
+  static constexpr int OFF_MD = OFF_MM + 4 * NS * NC;
+  static constexpr int OFF_FOLDS = OFF_MD + 4 * NS * NC;
   static constexpr int OFF_QUEUE = OFF_FOLDS + kFoldListBytes;
   static constexpr int OFF_SCALES = OFF_QUEUE + kSegQueueBytes;    // [S][32] fp32 if TS
   static constexpr int SMEM = OFF_SCALES + (TS ? S * 2 * P * 4 : 0);
   static_assert(!TS || kFp8, "per-token scales are for E4M3 KV");
   static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte swizzle rows");
-  static_assert(NC >= 1 && NC <= 8, "at most 8 columns (the MMA N side)");
+  static_assert(NC >= 1 && (NC <= 8 || NC <= 8 * NW), "8 columns (the MMA N side) per warp");
   static_assert(STAGE_BYTES % 1024 == 0, "swizzled boxes need 1024-byte alignment");
-  static_assert(S % NW == 0, "each ring stage must belong to exactly one consumer warp");
+  static_assert(CS || S % NW == 0, "each ring stage must belong to exactly one consumer warp");
   static_assert(!kFp8 || D % 32 == 0, "E4M3 V is transposed two granules at a time");
 };
 
@@ -172,12 +204,16 @@ struct MmaCfg {
 constexpr float kUmAbove = 16.f;
 constexpr float kUmBelow = 64.f;
 
-template <typename QT, typename KVT, int D, int G, int NW, bool TS, int QL, bool UM>
+template <typename QT, typename KVT, int D, int G, int NW, bool TS, int QL, bool UM,
+          bool RQ = false>
 __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
                                   MmaCfg<QT, KVT, D, G, NW, TS, QL>::MIN_CTAS)
     fa_decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
   using C = MmaCfg<QT, KVT, D, G, NW, TS, QL>;
   constexpr int NC = C::NC;
+  constexpr bool CS = C::CS;
+  // causal masking among the query tokens (multi-token and ragged plans)
+  constexpr bool kCausal = QL > 1 || RQ;
   constexpr int P = C::P, S = C::S, SEGS = C::SEGS, KSTEPS = C::KSTEPS, MTILES = C::MTILES;
   constexpr bool kBf16 = C::kBf16, kFp8 = C::kFp8;
   static_assert(kBf16 ? std::is_same<QT, __nv_bfloat16>::value
@@ -187,7 +223,8 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
   // per segment to sit well inside the f16 range.
   constexpr bool kConvertQ = kFp8 && std::is_same<QT, __nv_bfloat16>::value;
   // the unified-max window relies on the 8-bit exponent of bf16 weights
-  static_assert(!UM || (kBf16 && !TS && QL == 1), "unified max: bf16 weights, plain decode");
+  static_assert(!UM || (kBf16 && !TS && QL == 1 && !RQ), "unified max: bf16 weights, plain decode");
+  static_assert(!RQ || !TS, "ragged q: no per-token scales");
 
   // Swizzled TMA destinations must sit on 1024-byte boundaries: the launch
   // reserves 1 KB more than the layout so the base can be rounded up.
@@ -205,7 +242,7 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       dev::mbar_init(dev::smem_addr(&full[s]), TS ? kScaleLanes + 1 : 1);
-      dev::mbar_init(dev::smem_addr(&empty[s]), 1);
+      dev::mbar_init(dev::smem_addr(&empty[s]), CS ? NW : 1);  // its consumer warps
     }
     seg_queue_init(queue, NW);
     folds->n = 0;
@@ -226,7 +263,7 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
   if (warp == NW) {
     produce_pages<S, C::STAGE_BYTES, SEGS, C::BOX_X, C::BOX_BYTES, TS>(
         &kv_map, p, seg_begin, seg_end, ring, full, empty, lane,
-        reinterpret_cast<float*>(smem + C::OFF_SCALES), queue, NW);
+        reinterpret_cast<float*>(smem + C::OFF_SCALES), queue, CS ? 1 : NW);
     return;
   }
 
@@ -244,19 +281,30 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
   bool aborted = false;  // a timed-out wait makes every later wait return at once
   int kbase = 0, next_si = seg_begin, taken = 0;
   for (;;) {
-    const int si = next_segment<S, NW>(p, queue, next_si, seg_end, taken, kbase, full, empty,
-                                       warp, lane, aborted);
+    const int si = next_segment<S, NW, CS>(p, queue, next_si, seg_end, taken, kbase, full, empty,
+                                           warp, lane, aborted);
     if (si < 0) break;
     const int4 sa = *reinterpret_cast<const int4*>(p.segments + 8 * si);
     const int4 sb = *reinterpret_cast<const int4*>(p.segments + 8 * si + 4);
     const int req = sa.x, kvh = sa.y, npg = sa.w - sa.z;
     const int last_valid = sb.x, out_slot = sb.y, to_end = sb.w;
-    // causal limits of columns 2t, 2t+1: token position (from the segment
-    // start) after which query token n / G must not look
+    const QRows qr = query_rows<G, QL, RQ>(p.qo_indptr, req);
+    const int nq = qr.ncols / G;  // this request's query tokens
+    // this warp's columns: cb .. cb + 7 (the column split), else 0 .. 7
+    const int cb = CS ? 8 * warp : 0;
+    // a warp whose columns are all past the request's still takes its pages
+    // (every warp releases every stage) but computes nothing
+    const bool active = !CS || cb < qr.ncols;
+    // causal limits of columns cb+2t, cb+2t+1: token position (from the
+    // segment start) after which query token n / G must not look; columns
+    // past the request's see nothing
     int lim[2] = {0x7fffffff, 0x7fffffff};
-    if constexpr (QL > 1) {
-      lim[0] = to_end - QL + (2 * t) / G;
-      lim[1] = to_end - QL + (2 * t + 1) / G;
+    if constexpr (kCausal) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int n = cb + 2 * t + e;
+        lim[e] = n < qr.ncols ? to_end - nq + n / G : -1;
+      }
     }
 
     // ---- q as the B fragment of the score MMA, for the whole segment.
@@ -273,9 +321,9 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
 #pragma unroll
         for (int e = 0; e < 4; ++e) qf[j][e] = 0.f;
       uint32_t raw[KSTEPS][2];
-      if (g < NC) {
-        const QT* qrow =
-            qbase + (((size_t)req * QL + g / G) * p.num_qo_heads + kvh * G + g % G) * D;
+      if (cb + g < qr.ncols) {
+        const int n = cb + g;  // this lane's column of the B fragment
+        const QT* qrow = qbase + (((size_t)qr.q0 + n / G) * p.num_qo_heads + kvh * G + n % G) * D;
         // Load L (16 bytes, 8 consecutive elements) feeds reduction steps 2L
         // and 2L+1.  16-bit KV: step j = 4*seg + 2*half + u covers dims
         // seg*BOX_X + (2t + half)*8 + 4u .. +3.  E4M3 KV: step j = 4*half + w
@@ -341,10 +389,17 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
     bool um_first = true, um_moved = false;
     if constexpr (UM) m_h[0] = m_h[1] = p.max_bound;
 
-    for (int k = kbase + (warp - kbase % NW + NW) % NW; k < kbase + npg; k += NW) {
+    // page split: page k to warp k % NW; column split: every page to every warp
+    for (int k = CS ? kbase : kbase + (warp - kbase % NW + NW) % NW; k < kbase + npg;
+         k += CS ? 1 : NW) {
       const int lp = k - kbase;
       const int stage = k % S;
       dev::mbar_wait(dev::smem_addr(&full[stage]), (uint32_t)((k / S) & 1), aborted, p.err);
+      if (CS && !active) {  // nothing to compute: release the stage
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(dev::smem_addr(&empty[stage]));
+        continue;
+      }
       const uint32_t st = ring_addr + stage * C::STAGE_BYTES;
       const int valid = (lp == npg - 1) ? last_valid : P;
 
@@ -395,7 +450,7 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
       }
       if (g >= valid) s[0] = s[1] = -INFINITY;
       if (g + 8 >= valid) s[2] = s[3] = -INFINITY;
-      if constexpr (QL > 1) {
+      if constexpr (kCausal) {
         const int pos = lp * P + g;  // token position from the segment start
         if (pos > lim[0]) s[0] = -INFINITY;
         if (pos > lim[1]) s[1] = -INFINITY;
@@ -489,20 +544,17 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
           o[mt][3] *= alpha[1];
         }
       }
-      // slots past the last valid token may hold anything (NaN included): a
-      // zero weight would not cancel them in the MMA, so clear those V rows
-      if (valid < P) {
-        const int per_row = 128 / 16;  // 16-byte stores per 128-byte row
-        const int n = (P - valid) * SEGS * per_row;
-        for (int i = lane; i < n; i += 32) {
-          const int r = valid + i / (SEGS * per_row);
-          const int rem = i % (SEGS * per_row);
-          const uint32_t a = st + (rem / per_row) * C::BOX_BYTES + (P + r) * 128 + (rem % per_row) * 16;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(a), "r"(0u) : "memory");
-        }
-        // order these generic-proxy stores before the TMA that refills the stage
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      }
+      // Slots past the last valid token may hold anything (NaN included): a
+      // zero weight would not cancel them in the MMA, so their V elements
+      // are cleared in the A fragments below, in registers.  The stage itself
+      // is never written by the consumers: it belongs to the copy engine,
+      // which refills it for a later page as soon as this warp releases it.
+      // Each fragment register holds two consecutive tokens (low half 2t,
+      // high half 2t+1; +8 for the upper token block).
+      const uint32_t vmask_lo = (2 * t < valid ? 0x0000ffffu : 0u) |
+                                (2 * t + 1 < valid ? 0xffff0000u : 0u);
+      const uint32_t vmask_hi = (2 * t + 8 < valid ? 0x0000ffffu : 0u) |
+                                (2 * t + 9 < valid ? 0xffff0000u : 0u);
       __syncwarp();
       const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pT + g * P + 2 * t);
       const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(pT + g * P + 2 * t + 8);
@@ -515,6 +567,11 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
           const int gran = 2 * c2 + (mi >> 1), tok = (mi & 1) * 8 + r;
           uint32_t d0, d1, d2, d3;
           mma::ldsm_x4_trans(st + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16), d0, d1, d2, d3);
+          // matrices 0 and 2 hold tokens 2t, 2t+1; 1 and 3 tokens 2t+8, 2t+9
+          d0 &= vmask_lo;
+          d2 &= vmask_lo;
+          d1 &= vmask_hi;
+          d3 &= vmask_hi;
           uint32_t a[4][2];
           mma::e4m3x4_to_f16x2x2(__byte_perm(d0, 0u, 0x3120), a[0][0], a[0][1]);
           mma::e4m3x4_to_f16x2x2(__byte_perm(d1, 0u, 0x3120), a[1][0], a[1][1]);
@@ -533,11 +590,15 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
           uint32_t a0, a1, a2, a3;
           mma::ldsm_x4_trans(st + sgi * C::BOX_BYTES + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16),
                              a0, a1, a2, a3);
+          // matrices 0 and 1 hold tokens 2t, 2t+1; 2 and 3 tokens 2t+8, 2t+9
+          a0 &= vmask_lo;
+          a1 &= vmask_lo;
+          a2 &= vmask_hi;
+          a3 &= vmask_hi;
           mma::mma16816<kBf16>(o[mt], a0, a1, a2, a3, pb0, pb1);
         }
       }
-      __syncwarp();
-      if (lane == 0) dev::mbar_arrive(dev::smem_addr(&empty[stage]));
+      dev::release_stage(dev::smem_addr(&empty[stage]), lane);
     }
 
     // ---- this warp's state: O^T rows -> dims, heads 2t and 2t+1
@@ -553,40 +614,44 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
       // outweigh the others' in the combine
       if (um_first) m_h[0] = m_h[1] = -INFINITY;
     }
+    // state slot of this warp's columns: its own row (page split) or the
+    // columns' only state (column split); an idle warp of the column split
+    // leaves its columns empty (m = -inf, d = 0, o = 0: what it holds)
+    const int srow = CS ? 0 : warp;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int h = 2 * t + e;  // column
+      const int h = cb + 2 * t + e;  // column
       if (h < NC) {
 #pragma unroll
         for (int mt = 0; mt < MTILES; ++mt) {
           const int dlo = kFp8 ? mt * 16 + 2 * g : mt * 16 + g;
           const int dhi = kFp8 ? mt * 16 + 2 * g + 1 : mt * 16 + g + 8;
-          mo[(warp * NC + h) * D + dlo] = o[mt][e];
-          mo[(warp * NC + h) * D + dhi] = o[mt][2 + e];
+          mo[(srow * NC + h) * D + dlo] = o[mt][e];
+          mo[(srow * NC + h) * D + dhi] = o[mt][2 + e];
         }
         if (g == 0) {
-          mm[warp * NC + h] = m_h[e];
-          md[warp * NC + h] = d_h[e];
+          mm[srow * NC + h] = m_h[e];
+          md[srow * NC + h] = d_h[e];
         }
       }
     }
     dev::named_barrier(1, CT);
     // the P^T buffers (NW x 256 bytes) are free between segments
-    combine_and_emit<QT, D, G, NW, QL>(p, mo, mm, md, req, kvh, out_slot, sb.z, folds,
-                                       reinterpret_cast<float*>(smem + C::OFF_PT),
-                                       NW * 8 * P / 2);
+    combine_and_emit<QT, D, G, NW, QL, RQ, C::NS>(p, mo, mm, md, qr, kvh, out_slot, sb.z, folds,
+                                                  reinterpret_cast<float*>(smem + C::OFF_PT),
+                                                  NW * 8 * P / 2);
     kbase += npg;
   }
-  fold_pending<QT, D, G, NW, QL>(p, mo, folds);
+  fold_pending<QT, D, G, NW, QL, RQ>(p, mo, folds, C::NS * NC * D);
   if (threadIdx.x == 0) pool_finish(p);
 }
 
 template <typename QT, typename KVT, int D, int G, int NW = 4, bool TS = false, int QL = 1,
-          bool UM = false>
+          bool UM = false, bool RQ = false>
 inline void fill_mma_kernel(DecodeKernel* k) {
   using C = MmaCfg<QT, KVT, D, G, NW, TS, QL>;
-  k->func = reinterpret_cast<const void*>(&fa_decode_mma_kernel<QT, KVT, D, G, NW, TS, QL, UM>);
-  k->merge_func = reinterpret_cast<const void*>(&fa_merge_partials_kernel<QT, D, G, QL>);
+  k->func = reinterpret_cast<const void*>(&fa_decode_mma_kernel<QT, KVT, D, G, NW, TS, QL, UM, RQ>);
+  k->merge_func = reinterpret_cast<const void*>(&fa_merge_partials_kernel<QT, D, G, QL, RQ>);
   k->threads = C::THREADS;
   k->smem_bytes = C::SMEM + 1024;  // room to align the ring to 1024 bytes
   k->stages = C::S;
@@ -599,6 +664,7 @@ inline void fill_mma_kernel(DecodeKernel* k) {
   k->token_scales = TS;
   k->q_len = QL;
   k->unified_max = UM;
+  k->ragged_q = RQ;
 }
 
 }  // namespace fadecode
@@ -640,6 +706,24 @@ inline bool find_multi_token_kernel_for(int head_dim, int group, int q_len, Deco
   FA_QL_CASE(1, 2) FA_QL_CASE(1, 4) FA_QL_CASE(1, 8)
   FA_QL_CASE(2, 2) FA_QL_CASE(2, 4) FA_QL_CASE(4, 2)
 #undef FA_QL_CASE
+  return false;
+}
+
+// Ragged query rows (qo_indptr): tensor-core consumer, head_dim 128, the
+// smallest built bucket of query tokens per request that holds max_q: at most
+// 8 columns (group x tokens) with the pages split over the warps, else up to
+// 32 columns split over the warps (8 each).
+template <typename QT, typename KVT>
+inline bool find_ragged_q_kernel_for(int head_dim, int group, int max_q, DecodeKernel* k) {
+  if (head_dim != 128 || max_q < 1) return false;
+#define FA_RQ_CASE(GG, QQ)                                          \
+  if (group == GG && max_q <= QQ) {                                 \
+    fill_mma_kernel<QT, KVT, 128, GG, 4, false, QQ, false, true>(k); \
+    return true;                                                    \
+  }
+  FA_RQ_CASE(1, 8) FA_RQ_CASE(1, 32) FA_RQ_CASE(2, 4) FA_RQ_CASE(2, 16)
+  FA_RQ_CASE(4, 2) FA_RQ_CASE(4, 8) FA_RQ_CASE(8, 1) FA_RQ_CASE(8, 4)
+#undef FA_RQ_CASE
   return false;
 }
 

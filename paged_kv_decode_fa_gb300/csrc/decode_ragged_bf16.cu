@@ -1,0 +1,10 @@
+// Compiled instances of the decode kernel with ragged query rows (qo_indptr)
+// for q = __nv_bfloat16, kv = __nv_bfloat16 (a translation unit of their own so the build
+// runs in parallel).
+#include "decode_mma.cuh"
+
+namespace fadecode {
+bool find_ragged_q_kernel_bf16(int head_dim, int group, int max_q, DecodeKernel* k) {
+  return find_ragged_q_kernel_for<__nv_bfloat16, __nv_bfloat16>(head_dim, group, max_q, k);
+}
+}  // namespace fadecode

@@ -1,6 +1,7 @@
 // Host-side view of the CUDA kernels: parameter blocks and the registry that
 // maps (q dtype, kv dtype, head_dim, group size) to a compiled instance.
 #pragma once
+#include <cstddef>
 #include <cstdint>
 
 #include "fa_decode.h"
@@ -29,7 +30,9 @@ struct DecodeParams {
   int64_t num_pages;
   int num_qo_heads;
   int num_kv_heads;
-  int q_len;                   // query tokens per request (1 for plain decode)
+  int q_len;                   // query tokens per request (1 for plain decode); with
+                               // qo_indptr, the most a request may have
+  const int32_t* qo_indptr;    // [B + 1] query rows per request (ragged q), or nullptr
   int q_row_bytes;             // head_dim * q element size (0: no q prefetch)
   const void* kv;              // paged KV base (for L2 prefetches), or nullptr
   int kv_row_bytes;            // head_dim * KV element size
@@ -48,6 +51,7 @@ struct DecodeParams {
 
 struct MergeParams {
   const int32_t* merge;  // [n_merge * 4]
+  const int32_t* qo_indptr;  // [B + 1] for ragged q, else nullptr
   const float* part_o;
   const float* part_lse;
   void* o;
@@ -69,8 +73,10 @@ struct DecodeKernel {
   bool swizzle_128b = false;  // stage rows in TMA 128-byte swizzle order
   bool tensor_cores = false;  // per-page products on mma.sync
   bool token_scales = false;  // reads per-token K/V scales (E4M3 only)
-  int q_len = 1;              // query tokens per request the kernel was built for
+  int q_len = 1;              // query tokens per request the kernel was built for (ragged:
+                              // the most a request may have)
   bool unified_max = false;   // softmax against a static bound (no running max)
+  bool ragged_q = false;      // query rows per request from qo_indptr
 };
 
 // Each returns false when the combination is not compiled.  allow_mma
@@ -85,11 +91,25 @@ bool find_kernel_f16_e4m3(int head_dim, int group, bool allow_mma, DecodeKernel*
 // tensor-core consumer, head_dim 128, group * q_len <= 8.
 bool find_multi_token_kernel_bf16(int head_dim, int group, int q_len, DecodeKernel* k);
 bool find_multi_token_kernel_bf16_e4m3(int head_dim, int group, int q_len, DecodeKernel* k);
+// Ragged query rows: request i has qo_indptr[i+1] - qo_indptr[i] <= max_q
+// query tokens (head_dim 128; group x max_q <= 32).
+bool find_ragged_q_kernel_bf16(int head_dim, int group, int max_q, DecodeKernel* k);
+bool find_ragged_q_kernel_bf16_e4m3(int head_dim, int group, int max_q, DecodeKernel* k);
 // Unified-max softmax (bf16 q and KV, groups 2, 4, 8, head_dim 64 or 128).
 bool find_unified_max_kernel_bf16(int head_dim, int group, DecodeKernel* k);
 // E4M3 KV with per-token, per-kv-head scales (tensor-core consumer only).
 bool find_token_scale_kernel_bf16_e4m3(int head_dim, int group, DecodeKernel* k);
 bool find_token_scale_kernel_f16_e4m3(int head_dim, int group, DecodeKernel* k);
+
+// Plan + run of one batch with the workspace replaced by `scratch` (the
+// library's own device array) and no allocation of any kind: the path
+// behind fa_decode_static (api.cu).  Returns an fa_status.
+int static_decode(void* scratch, size_t scratch_bytes, const int32_t* indptr_host,
+                  const int32_t* indices_dev, const int32_t* last_page_len_host, int batch,
+                  int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                  fa_dtype q_dtype, fa_dtype kv_dtype, const void* q, const void* paged_kv,
+                  int64_t num_pages, float sm_scale, float k_scale, float v_scale, void* o,
+                  float* lse, void* cuda_stream);
 
 // fa_merge_states kernels (merge.cu).
 int launch_merge_states(const void* o_a, const float* lse_a, const void* o_b,

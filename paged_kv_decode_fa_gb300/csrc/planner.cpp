@@ -35,12 +35,76 @@
 #include <algorithm>
 
 namespace fadecode {
+namespace {
 
-int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
-                    int batch, int num_kv_heads, int page_size, int max_ctas,
-                    int min_pages_per_cta, double pool_fraction, WorkList* out) {
-  if (!indptr || !out || batch < 0 || num_kv_heads <= 0 || page_size <= 0 ||
-      max_ctas <= 0 || !(pool_fraction >= 0.0 && pool_fraction < 1.0))
+// Where the planner's output goes: growable vectors (WorkList) or fixed
+// arrays (FixedWorkList).  Each push returns false when the output is full.
+struct VectorSink {
+  WorkList* wl;
+  std::vector<Segment> pooled;  // pool segments, in stream order
+  bool start(int num_ctas, size_t units, bool pool) {
+    wl->cta_offsets.assign((size_t)num_ctas + 1, 0);
+    wl->segments.reserve(units + num_ctas + 1);
+    if (pool) pooled.reserve(units / 4 + 64);
+    return true;
+  }
+  bool segment(int64_t cta, const Segment& s) {
+    wl->segments.push_back(s);
+    wl->cta_offsets[(size_t)cta + 1]++;
+    return true;
+  }
+  bool pool_segment(const Segment& s) {
+    pooled.push_back(s);
+    return true;
+  }
+  bool merge(const MergeUnit& m) {
+    wl->merge.push_back(m);
+    return true;
+  }
+  void finish(int num_ctas) {
+    for (int c = 0; c < num_ctas; ++c) wl->cta_offsets[c + 1] += wl->cta_offsets[c];
+    wl->segments.insert(wl->segments.end(), pooled.begin(), pooled.end());
+  }
+};
+
+struct FixedSink {
+  FixedWorkList* wl;
+  bool start(int num_ctas, size_t, bool pool) {
+    if (pool || num_ctas > wl->cta_capacity) return false;
+    for (int c = 0; c <= num_ctas; ++c) wl->cta_offsets[c] = 0;
+    wl->num_segments = wl->num_merge = 0;
+    return true;
+  }
+  bool segment(int64_t cta, const Segment& s) {
+    if (wl->num_segments >= wl->segment_capacity) return false;
+    wl->segments[wl->num_segments++] = s;
+    wl->cta_offsets[cta + 1]++;
+    return true;
+  }
+  bool pool_segment(const Segment&) { return false; }
+  bool merge(const MergeUnit& m) {
+    if (wl->num_merge >= wl->merge_capacity) return false;
+    wl->merge[wl->num_merge++] = m;
+    return true;
+  }
+  void finish(int num_ctas) {
+    for (int c = 0; c < num_ctas; ++c) wl->cta_offsets[c + 1] += wl->cta_offsets[c];
+  }
+};
+
+struct Totals {
+  int num_ctas = 0, num_slots = 0;
+  int64_t total_pages = 0, total_tokens = 0, pool_pages = 0;
+};
+
+// The planner proper, writing through `sink`.  Returns 0, -1 for malformed
+// input, or -2 when the sink is full.
+template <typename Sink>
+int plan_stream(const int32_t* indptr, const int32_t* last_page_len, int batch,
+                int num_kv_heads, int page_size, int max_ctas, int min_pages_per_cta,
+                double pool_fraction, Sink& sink, Totals* tot) {
+  if (!indptr || batch < 0 || num_kv_heads <= 0 || page_size <= 0 || max_ctas <= 0 ||
+      !(pool_fraction >= 0.0 && pool_fraction < 1.0))
     return -1;
   if (batch > 0 && !last_page_len) return -1;
   if (indptr[0] != 0) return -1;
@@ -80,6 +144,7 @@ int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
   // Pool chunk ends (absolute stream positions): tier t cuts n chunks of
   // ceil(pool / (n * 2^(t+1))) pages, so early claims take long chunks and
   // the last ones short chunks that even out the CTAs' finishing times.
+  // (Empty without a pool: a plan without one allocates nothing here.)
   std::vector<int64_t> chunk_end;
   if (pool > 0) {
     int64_t a = S, size = kPoolMinPages;
@@ -92,16 +157,7 @@ int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
     while (a < T) chunk_end.push_back(a = std::min(T, a + size));
   }
 
-  WorkList wl;
-  wl.num_ctas = num_ctas;
-  wl.total_pages = total_pages;
-  wl.total_tokens = total_tokens;
-  wl.pool_pages = pool;
-  wl.cta_offsets.assign((size_t)num_ctas + 1, 0);
-  const size_t units = (size_t)batch * num_kv_heads;
-  std::vector<Segment> pooled;  // pool segments, in stream order
-  wl.segments.reserve(units + num_ctas + 1);
-  if (pool > 0) pooled.reserve(chunk_end.size() + 64);
+  if (!sink.start(num_ctas, (size_t)batch * num_kv_heads, pool > 0)) return -2;
 
   // Positions only grow, so the owning CTA and the next cut are tracked
   // incrementally (64-bit divisions per piece cost more than the rest).
@@ -109,7 +165,7 @@ int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
   int64_t cta = 0;      // CTA of the current static position
   int64_t cut = quota;  // end of that CTA's quota
   int64_t pos = 0;
-  int slots = 0;
+  int slots = 0, n_merge = 0;
   for (int i = 0; i < batch; ++i) {
     const int32_t pb = indptr[i], pe = indptr[i + 1];
     const int64_t np = (int64_t)pe - pb;
@@ -124,12 +180,8 @@ int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
       }
       if (np == 0) {
         const Segment e{i, h, pb, pb, page_size, -1, -1, 0};
-        if (pool > 0 && start >= S) {
-          pooled.push_back(e);
-        } else {
-          wl.segments.push_back(e);
-          wl.cta_offsets[(size_t)cta + 1]++;
-        }
+        const bool ok = (pool > 0 && start >= S) ? sink.pool_segment(e) : sink.segment(cta, e);
+        if (!ok) return -2;
         continue;
       }
       // pieces: static ones cut at quota boundaries, pool ones at chunk ends
@@ -148,8 +200,8 @@ int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
       }
       int slot = -1, unit = -1;
       if (pieces > 1) {
-        unit = (int)wl.merge.size();
-        wl.merge.push_back(MergeUnit{i, h, slots, pieces});
+        unit = n_merge++;
+        if (!sink.merge(MergeUnit{i, h, slots, pieces})) return -2;
         slot = slots;
         slots += pieces;
       }
@@ -169,21 +221,55 @@ int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
         const Segment sg{i, h, (int32_t)(pb + (a - start)), (int32_t)(pb + (b - start)),
                          (b == end) ? last_page_len[i] : page_size, slot, unit,
                          (int32_t)(len - (a - start) * page_size)};
-        if (in_pool) {
-          pooled.push_back(sg);
-        } else {
-          wl.segments.push_back(sg);
-          wl.cta_offsets[(size_t)cta + 1]++;
-        }
+        if (!(in_pool ? sink.pool_segment(sg) : sink.segment(cta, sg))) return -2;
         if (slot >= 0) ++slot;
         a = b;
       }
     }
   }
-  wl.num_slots = slots;
-  for (int c = 0; c < num_ctas; ++c) wl.cta_offsets[c + 1] += wl.cta_offsets[c];
-  wl.segments.insert(wl.segments.end(), pooled.begin(), pooled.end());
+  sink.finish(num_ctas);
+  tot->num_ctas = num_ctas;
+  tot->num_slots = slots;
+  tot->total_pages = total_pages;
+  tot->total_tokens = total_tokens;
+  tot->pool_pages = pool;
+  return 0;
+}
+
+}  // namespace
+
+int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
+                    int batch, int num_kv_heads, int page_size, int max_ctas,
+                    int min_pages_per_cta, double pool_fraction, WorkList* out) {
+  if (!out) return -1;
+  WorkList wl;
+  VectorSink sink{&wl, {}};
+  Totals tot;
+  const int rc = plan_stream(indptr, last_page_len, batch, num_kv_heads, page_size, max_ctas,
+                             min_pages_per_cta, pool_fraction, sink, &tot);
+  if (rc != 0) return -1;
+  wl.num_ctas = tot.num_ctas;
+  wl.num_slots = tot.num_slots;
+  wl.total_pages = tot.total_pages;
+  wl.total_tokens = tot.total_tokens;
+  wl.pool_pages = tot.pool_pages;
   *out = std::move(wl);
+  return 0;
+}
+
+int build_work_list_fixed(const int32_t* indptr, const int32_t* last_page_len, int batch,
+                          int num_kv_heads, int page_size, int max_ctas, int min_pages_per_cta,
+                          FixedWorkList* out) {
+  if (!out || !out->cta_offsets || !out->segments || !out->merge) return -1;
+  FixedSink sink{out};
+  Totals tot;
+  const int rc = plan_stream(indptr, last_page_len, batch, num_kv_heads, page_size, max_ctas,
+                             min_pages_per_cta, 0.0, sink, &tot);
+  if (rc != 0) return rc;
+  out->num_ctas = tot.num_ctas;
+  out->num_slots = tot.num_slots;
+  out->total_pages = tot.total_pages;
+  out->total_tokens = tot.total_tokens;
   return 0;
 }
 

@@ -68,4 +68,21 @@ int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
                     int batch, int num_kv_heads, int page_size, int max_ctas,
                     int min_pages_per_cta, double pool_fraction, WorkList* out);
 
+// The same plan without a pool, written into arrays the caller owns (no
+// allocation): cta_offsets[cta_capacity + 1], segments[segment_capacity],
+// merge[merge_capacity].  The counts are filled in on success.
+struct FixedWorkList {
+  int32_t* cta_offsets = nullptr;
+  Segment* segments = nullptr;
+  MergeUnit* merge = nullptr;
+  int cta_capacity = 0, segment_capacity = 0, merge_capacity = 0;
+  int num_ctas = 0, num_segments = 0, num_merge = 0, num_slots = 0;
+  int64_t total_pages = 0, total_tokens = 0;
+};
+
+// Returns 0, -1 for malformed input, -2 when a plan does not fit the arrays.
+int build_work_list_fixed(const int32_t* indptr, const int32_t* last_page_len, int batch,
+                          int num_kv_heads, int page_size, int max_ctas, int min_pages_per_cta,
+                          FixedWorkList* out);
+
 }  // namespace fadecode

@@ -2,6 +2,7 @@
 #include "staging.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -22,6 +23,7 @@ struct Slot {
 std::mutex g_mu;
 Slot g_slots[kSlots];
 int g_next = 0;
+std::atomic<int64_t> g_allocs{0}, g_alloc_bytes{0}, g_uploads{0};
 
 }  // namespace
 
@@ -53,13 +55,22 @@ cudaError_t upload_async(void* dst, const void* src, size_t bytes, cudaStream_t 
     while (cap < bytes) cap *= 2;
     if ((e = cudaMallocHost(&s.buf, cap)) != cudaSuccess) return e;
     s.cap = cap;
+    g_allocs.fetch_add(1);
+    g_alloc_bytes.fetch_add((int64_t)cap);
   }
   std::memcpy(s.buf, src, bytes);
   if ((e = cudaMemcpyAsync(dst, s.buf, bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
     return e;
   if ((e = cudaEventRecord(s.done, stream)) != cudaSuccess) return e;
   s.pending = true;
+  g_uploads.fetch_add(1);
   return cudaSuccess;
+}
+
+void staging_stats(int64_t* allocations, int64_t* bytes, int64_t* uploads) {
+  *allocations = g_allocs.load();
+  *bytes = g_alloc_bytes.load();
+  *uploads = g_uploads.load();
 }
 
 }  // namespace fadecode

@@ -1,6 +1,7 @@
 // Asynchronous upload of small host buffers (plan metadata).
 #pragma once
 #include <cstddef>
+#include <cstdint>
 
 #include <cuda_runtime.h>
 
@@ -14,5 +15,9 @@ namespace fadecode {
 // library owns (reused round-robin, each once its previous copy is done).
 // Returns cudaSuccess or the failing call's error.
 cudaError_t upload_async(void* dst, const void* src, size_t bytes, cudaStream_t stream);
+
+// Page-locked staging buffers allocated so far (count and bytes) and
+// uploads made through the ring, since the library was loaded.
+void staging_stats(int64_t* allocations, int64_t* bytes, int64_t* uploads);
 
 }  // namespace fadecode

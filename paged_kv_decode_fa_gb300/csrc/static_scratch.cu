@@ -1,6 +1,7 @@
 // fa_decode_static: plan + run of one decode batch with the work list and the
 // partial softmax states kept in a fixed array that the library itself owns,
-// so that the call never allocates device memory.
+// so that the call allocates nothing: no device memory, no page-locked host
+// memory, no events, no heap objects.
 //
 // Who needs this: code that is handed only input and output pointers and is
 // not allowed to allocate - a custom operator inside a host framework that
@@ -18,6 +19,7 @@
 #include <mutex>
 
 #include "fa_decode.h"
+#include "kernels.h"
 
 static_assert(FA_STATIC_SCRATCH_BYTES % 256 == 0, "scratch size must keep 256-byte alignment");
 
@@ -57,16 +59,30 @@ extern "C" int fa_decode_static(const int32_t* indptr_host, const int32_t* indic
   void* scratch = nullptr;
   int rc = static_scratch_address(&scratch);
   if (rc != FA_OK) return rc;
-  // The plan writes the work list (and a zeroed device-check word) into the
-  // scratch on the stream; a batch whose plan does not fit is refused with
-  // FA_ERR_WORKSPACE_TOO_SMALL before anything is launched.
-  fa_decode_plan_t plan = nullptr;
-  rc = fa_decode_plan(indptr_host, indices_dev, last_page_len_host, batch, num_qo_heads,
-                      num_kv_heads, head_dim, page_size, q_dtype, kv_dtype, scratch,
-                      FA_STATIC_SCRATCH_BYTES, cuda_stream, &plan);
+  // Plans into fixed host arrays, copies the work list (and a zeroed
+  // device-check word) into the scratch on the stream and launches; a batch
+  // whose plan does not fit is refused with FA_ERR_WORKSPACE_TOO_SMALL
+  // before anything is enqueued.
+  return fadecode::static_decode(scratch, FA_STATIC_SCRATCH_BYTES, indptr_host, indices_dev,
+                                 last_page_len_host, batch, num_qo_heads, num_kv_heads,
+                                 head_dim, page_size, q_dtype, kv_dtype, q, paged_kv, num_pages,
+                                 sm_scale, k_scale, v_scale, o, lse, cuda_stream);
+}
+
+extern "C" int fa_decode_static_check(void* cuda_stream, int* flags) {
+  if (!flags) return FA_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  int rc = static_scratch_address(&scratch);
   if (rc != FA_OK) return rc;
-  rc = fa_decode_run(plan, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, o, lse,
-                     cuda_stream);
-  fa_decode_plan_destroy(plan);
-  return rc;
+  // the device-check word is the first int of the scratch (the work list's
+  // layout starts with it)
+  int word = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess ||
+      cudaMemcpy(&word, scratch, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemsetAsync(scratch, 0, sizeof word, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return FA_ERR_CUDA;
+  *flags = word;
+  return word ? FA_ERR_DEVICE_CHECK : FA_OK;
 }

@@ -39,6 +39,13 @@ measured on:
                  batch's page table lists each request's full sequence (prefix
                  pages first); extra["prefix_pages"] says how many are shared.
 
+``spec_decode_ragged``  the fp8_kv shapes (B=128, 64/8 heads, group 8,
+                 E4M3 KV, lengths U{1024..8192}) verifying U{1..4} draft
+                 tokens per request (speculative decoding with a draft length
+                 of its own per request): q is ragged [sum of drafts, 64, 128]
+                 with extra["qo_indptr"]; up to 32 columns per (request, kv
+                 head).
+
 ``gqa_unified_max``  the gqa_uniform batch (same seed, same values), decoded
                  with the unified-max softmax against cauchy_schwarz_bound.
 
@@ -92,6 +99,8 @@ CONFIGS: dict[str, DecodeConfig] = {
     "spec_decode": DecodeConfig("spec_decode", 64, 32, 8, 128, torch.bfloat16, torch.bfloat16,
                                 1007, q_len=2),
     "cascade": DecodeConfig("cascade", 64, 32, 8, 128, torch.bfloat16, torch.bfloat16, 1008),
+    "spec_decode_ragged": DecodeConfig("spec_decode_ragged", 128, 64, 8, 128, torch.bfloat16,
+                                       torch.float8_e4m3fn, 1009, q_len=4),
     # the gqa_uniform batch itself (same seed), run with the unified-max softmax
     "gqa_unified_max": DecodeConfig("gqa_unified_max", 64, 32, 8, 128, torch.bfloat16,
                                     torch.bfloat16, 1002),
@@ -113,7 +122,7 @@ def draw_lengths(cfg: DecodeConfig, gen: torch.Generator) -> np.ndarray:
         return np.full(cfg.batch, 65536, dtype=np.int64)
     if cfg.name == "cascade":   # the request's own tokens after the shared prefix
         return torch.randint(1, 513, (cfg.batch,), generator=gen).numpy().astype(np.int64)
-    if cfg.name in ("fp8_kv", "fp8_kv_token_scales"):
+    if cfg.name in ("fp8_kv", "fp8_kv_token_scales", "spec_decode_ragged"):
         return torch.randint(1024, 8193, (cfg.batch,), generator=gen).numpy().astype(np.int64)
     raise KeyError(cfg.name)
 
@@ -188,13 +197,16 @@ def _fp8_quantise(x: torch.Tensor) -> tuple[torch.Tensor, float]:
 def make_batch(*, batch_lengths, num_qo_heads: int, num_kv_heads: int, head_dim: int,
                q_dtype: torch.dtype, kv_dtype: torch.dtype, seed: int, device="cuda",
                page_size: int = PAGE_SIZE, pool_pages: int | None = None, shuffle: bool = True,
-               name: str = "custom", token_scales: bool = False, q_len: int = 1) -> DecodeBatch:
+               name: str = "custom", token_scales: bool = False, q_len: int = 1,
+               token_spread: float = 3.0) -> DecodeBatch:
     """A seeded batch with explicit lengths (any shape the library supports).
-    token_scales=True (E4M3 only) draws per-token magnitudes and stores one
+    token_scales=True (E4M3 only) draws per-token magnitudes 2^u, u uniform
+    in [-token_spread, token_spread] (0: plain N(0,1) values), and stores one
     scale per (page, kv head, slot) in extra["k_scales"] / extra["v_scales"]."""
     gen = torch.Generator().manual_seed(seed)
     return _fill(batch_lengths, gen, num_qo_heads, num_kv_heads, head_dim, q_dtype, kv_dtype,
-                 seed, device, page_size, pool_pages, shuffle, name, token_scales, q_len)
+                 seed, device, page_size, pool_pages, shuffle, name, token_scales, q_len,
+                 token_spread)
 
 
 def make_cascade_batch(*, prefix_pages: int, suffix_lengths, num_qo_heads: int,
@@ -268,9 +280,35 @@ def make_config_batch(name: str, device="cuda", max_requests: int | None = None)
     if max_requests is not None:
         lengths = lengths[:max_requests]
     pool = 64 if name == "tiny" else None
+    if name == "spec_decode_ragged":   # U{1..4} draft tokens per request
+        drafts = torch.randint(1, cfg.q_len + 1, (len(lengths),), generator=gen).numpy()
+        return make_ragged_q_batch(batch_lengths=lengths, q_counts=drafts,
+                                   num_qo_heads=cfg.num_qo_heads, num_kv_heads=cfg.num_kv_heads,
+                                   head_dim=cfg.head_dim, q_dtype=cfg.q_dtype,
+                                   kv_dtype=cfg.kv_dtype, seed=cfg.seed, device=device,
+                                   name=name, gen=gen)
     return _fill(lengths, gen, cfg.num_qo_heads, cfg.num_kv_heads, cfg.head_dim, cfg.q_dtype,
                  cfg.kv_dtype, cfg.seed, device, cfg.page_size, pool, True, name,
                  name == "fp8_kv_token_scales", cfg.q_len)
+
+
+def make_ragged_q_batch(*, batch_lengths, q_counts, num_qo_heads: int, num_kv_heads: int,
+                        head_dim: int, q_dtype: torch.dtype, kv_dtype: torch.dtype, seed: int,
+                        device="cuda", page_size: int = PAGE_SIZE, name: str = "custom",
+                        gen: torch.Generator | None = None) -> DecodeBatch:
+    """A seeded batch whose request i carries q_counts[i] query tokens (the
+    last positions of its cache): q is [sum(q_counts), Hq, D] and
+    extra["qo_indptr"] the request boundaries of its rows."""
+    gen = gen if gen is not None else torch.Generator().manual_seed(seed)
+    counts = np.asarray(q_counts, dtype=np.int64)
+    b = _fill(batch_lengths, gen, num_qo_heads, num_kv_heads, head_dim, q_dtype, kv_dtype, seed,
+              device, page_size, None, True, name, False, 1)
+    qo = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    vgen = torch.Generator(device=b.q.device).manual_seed(seed + 7919)
+    b.q = torch.randn((int(qo[-1]), num_qo_heads, head_dim), generator=vgen, device=b.q.device,
+                      dtype=torch.float32).to(q_dtype)
+    b.extra["qo_indptr"] = qo
+    return b
 
 
 def _fp8_token_quantise(x: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
@@ -284,7 +322,7 @@ def _fp8_token_quantise(x: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
 
 
 def _fill(lengths, gen, Hq, Hkv, D, q_dtype, kv_dtype, seed, device, P, pool_pages, shuffle,
-          name, token_scales=False, q_len=1) -> DecodeBatch:
+          name, token_scales=False, q_len=1, token_spread=3.0) -> DecodeBatch:
     lengths = np.asarray(lengths, dtype=np.int64)
     indptr, ids, last, pool = page_table(lengths, P, pool_pages, gen, shuffle)
     B = len(lengths)
@@ -299,7 +337,8 @@ def _fill(lengths, gen, Hq, Hkv, D, q_dtype, kv_dtype, seed, device, P, pool_pag
             raise ValueError("per-token scales are for E4M3 KV")
         kv = torch.empty((pool, 2, P, Hkv, D), dtype=kv_dtype, device=dev)
         for half, key in ((0, "k_scales"), (1, "v_scales")):
-            mag = torch.exp2(torch.rand((pool, P, Hkv, 1), generator=vgen, device=dev) * 6 - 3)
+            u = torch.rand((pool, P, Hkv, 1), generator=vgen, device=dev)
+            mag = torch.exp2((u * 2 - 1) * token_spread)
             x = torch.randn((pool, P, Hkv, D), generator=vgen, device=dev) * mag
             codes, scales = _fp8_token_quantise(x)
             kv[:, half] = codes

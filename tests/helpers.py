@@ -33,6 +33,12 @@ def oracle_decode(b: DecodeBatch, orc=None, sm_scale=None, num_threads=0):
     orc = orc or oracle._default()
     q, qc = as_bits(b.q)
     kv, kc = as_bits(b.paged_kv)
+    if "qo_indptr" in b.extra:
+        return orc.batch_decode_ragged_q(
+            q, qc, kv, kc, b.indptr.numpy(), b.indices.cpu().numpy(), b.last_page_len.numpy(),
+            np.asarray(b.extra["qo_indptr"]), b.num_qo_heads, b.num_kv_heads, b.head_dim,
+            b.page_size, sm_scale=sm_scale, k_scale=b.k_scale, v_scale=b.v_scale,
+            num_threads=num_threads)
     if b.q_len > 1:
         return orc.batch_decode_multi(
             q, qc, kv, kc, b.indptr.numpy(), b.indices.cpu().numpy(), b.last_page_len.numpy(),
@@ -66,12 +72,19 @@ def sub_batch(b: DecodeBatch, requests) -> DecodeBatch:
     new_indptr[1:] = np.cumsum(counts)
     rq = torch.tensor(requests, dtype=torch.int64, device=b.q.device)
     extra = {}
+    q_sel = b.q.index_select(0, rq).to("cpu") if "qo_indptr" not in b.extra else None
+    if "qo_indptr" in b.extra:   # ragged query rows: the requests' own rows, re-indexed
+        qo = np.asarray(b.extra["qo_indptr"], np.int64)
+        rows = np.concatenate([np.arange(qo[r], qo[r + 1]) for r in requests] + [np.zeros(0, np.int64)])
+        q_sel = b.q.index_select(0, torch.from_numpy(rows).to(b.q.device)).to("cpu")
+        counts = [int(qo[r + 1] - qo[r]) for r in requests]
+        extra["qo_indptr"] = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     for key in ("k_scales", "v_scales"):
         if key in b.extra:
             t = b.extra[key]
             extra[key] = (t.index_select(0, sel).to("cpu") if len(page_ids) else t[:1].to("cpu"))
     return DecodeBatch(
-        q=b.q.index_select(0, rq).to("cpu"), paged_kv=kv,
+        q=q_sel, paged_kv=kv,
         indptr=torch.from_numpy(new_indptr.astype(np.int32)),
         indices=torch.arange(len(page_ids), dtype=torch.int32),
         last_page_len=b.last_page_len[requests].clone(),
