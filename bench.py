@@ -548,9 +548,11 @@ OTHER_WORKLOADS = ("tiny", "gqa_uniform", "long_split", "fp8_kv", "fp8_kv_token_
 
 
 def measure_other(args, world, dev, name: str) -> dict:
-    """One more decode workload: K timed steps after W warm-ups, the region's
-    events over its launches as the kernel time, the workload's own
-    algorithmic bytes, roofline fraction and (current) ncu traffic."""
+    """One more decode workload: at least 100 timed steps after at least 10
+    warm-ups (a region of a few 0.1 ms launches is too short to time well),
+    the region's events over its launches as the kernel time, the workload's
+    own algorithmic bytes, roofline fraction and (current) ncu traffic."""
+    steps, warmup = max(args.steps, 100), max(args.warmup, 10)
     import paged_kv_decode_fa_gb300 as fa
     cfg = W.CONFIGS[name]
     b = W.make_config_batch(name, device=dev)
@@ -561,7 +563,7 @@ def measure_other(args, world, dev, name: str) -> dict:
     lse = torch.empty(tuple(b.q.shape[:-1]), dtype=torch.float32, device=dev)
     um_bound = W.cauchy_schwarz_bound(b) if name == "gqa_unified_max" else None
     run_step = step_fn(name, b, um_bound)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         run_step(p, b.q, o, lse)
     torch.cuda.synchronize(dev)
     if p.check() != 0:
@@ -571,19 +573,19 @@ def measure_other(args, world, dev, name: str) -> dict:
     barrier(world)
     torch.cuda.synchronize(dev)
     start.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         run_step(p, b.q, o, lse)
     end.record(stream)
     torch.cuda.synchronize(dev)
     elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, world, dev)
-    step_s = elapsed_s / args.steps
+    step_s = elapsed_s / steps
     alg = algorithmic_bytes(b)
     peak, _ = read_peaks()
     res = {
         "config": config_dict(cfg, b),
-        "value": whole_job_rate(world, query_rows(b), args.steps, elapsed_s),
+        "value": whole_job_rate(world, query_rows(b), steps, elapsed_s),
         "unit": "tokens/s", "ms_per_step": step_s * 1e3,
-        "kv_tokens_per_s": world * b.total_tokens * args.steps / elapsed_s,
+        "kv_tokens_per_s": world * b.total_tokens * steps / elapsed_s,
         "hbm_gbs": alg / step_s / 1e9,
         "roofline": {"bound": "hbm", "achieved": alg / step_s / 1e9, "peak": peak,
                      "unit": "GB/s", "frac": alg / step_s / 1e9 / peak,
@@ -593,7 +595,7 @@ def measure_other(args, world, dev, name: str) -> dict:
                      "algorithmic_bytes_per_launch": alg, "duration_us": step_s * 1e6,
                      "duration_from": ("timed-region events / launches" if launches == 1 else
                                        "timed-region events / steps (decode + merge kernel)")},
-        "gpu_launches": args.steps * launches,
+        "steps": steps, "warmup": warmup, "gpu_launches": steps * launches,
     }
     if um_bound is not None:
         res["unified_max"] = {"bound": um_bound, "fallbacks": p.unified_max_fallbacks()}

@@ -460,8 +460,11 @@ size_t fa_cascade_workspace_size(int batch, int num_qo_heads, int num_kv_heads,
  *                      after the prefix, as in fa_decode_plan (a request may
  *                      have none).
  * Both index arrays are kept by pointer for the plan's lifetime.  Supported:
- * head_dim 128, page_size 16, q and kv both BF16 or both F16; otherwise
- * FA_ERR_UNSUPPORTED.  Errors as fa_decode_plan. */
+ * page_size 16 and (q, kv, head_dim) in (BF16, BF16, 64 or 128),
+ * (F16, F16, 64 or 128), (BF16, E4M3, 128), (F16, E4M3, 128); otherwise
+ * FA_ERR_UNSUPPORTED.  The prefix pass runs on the tcgen05 tensor cores for
+ * 16-bit KV at head_dim 128, on warp-level MMAs otherwise (an E4M3 cache is
+ * widened to f16 in registers).  Errors as fa_decode_plan. */
 int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
                     const int32_t* indptr_host, const int32_t* indices_dev,
                     const int32_t* last_page_len_host, int batch,
@@ -481,6 +484,14 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
 int fa_cascade_run(fa_cascade_plan_t plan, const void* q, const void* paged_kv,
                    int64_t num_pages, float sm_scale, void* o, float* lse,
                    void* cuda_stream);
+
+/* fa_cascade_run over an E4M3 cache with its per-tensor scales (value =
+ * code x scale, as fa_decode_run): k_scale folds into the logit scale of
+ * both passes, v_scale into their outputs.  A 16-bit cache takes 1 and 1
+ * only (FA_ERR_INVALID_ARG otherwise). */
+int fa_cascade_run_scaled(fa_cascade_plan_t plan, const void* q, const void* paged_kv,
+                          int64_t num_pages, float sm_scale, float k_scale,
+                          float v_scale, void* o, float* lse, void* cuda_stream);
 
 int fa_cascade_plan_destroy(fa_cascade_plan_t plan);
 

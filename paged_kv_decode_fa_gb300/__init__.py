@@ -40,7 +40,7 @@ EXPORTED_SYMBOLS = (
     "fa_cascade_workspace_size", "fa_cascade_plan", "fa_cascade_run", "fa_cascade_plan_destroy",
     "fa_cascade_check", "fa_decode_run_unified_max", "fa_decode_unified_max_fallbacks",
     "fa_cascade_set_timing_events", "fa_decode_static_check", "fa_library_get_stats",
-    "fa_decode_plan_ragged_q", "fa_decode_workspace_size_ragged_q",
+    "fa_decode_plan_ragged_q", "fa_decode_workspace_size_ragged_q", "fa_cascade_run_scaled",
 )
 
 FA_OK = 0
@@ -117,6 +117,8 @@ def _load() -> ctypes.CDLL:
     lib.fa_cascade_plan.restype = i32
     lib.fa_cascade_run.argtypes = [P, P, P, i64, f32, P, P, P]
     lib.fa_cascade_run.restype = i32
+    lib.fa_cascade_run_scaled.argtypes = [P, P, P, i64, f32, f32, f32, P, P, P]
+    lib.fa_cascade_run_scaled.restype = i32
     lib.fa_cascade_plan_destroy.argtypes = [P]
     lib.fa_cascade_plan_destroy.restype = i32
     lib.fa_cascade_check.argtypes = [P, P, ctypes.POINTER(i32)]
@@ -549,10 +551,11 @@ class CascadePlan:
     """A planned cascade batch: one shared prefix of whole pages, then each
     request's own pages.  Keeps the index tensors and the workspace alive."""
 
-    def __init__(self, handle, keep, q_dtype, shape):
+    def __init__(self, handle, keep, q_dtype, shape, kv_dtype=None):
         self._h = handle
         self._keep = keep
         self.q_dtype = q_dtype
+        self.kv_dtype = q_dtype if kv_dtype is None else kv_dtype
         self.batch, self.num_qo_heads, self.num_kv_heads, self.head_dim = shape
 
     def __del__(self):
@@ -562,10 +565,12 @@ class CascadePlan:
             self._h = None
 
     def run(self, q: torch.Tensor, paged_kv: torch.Tensor, *, sm_scale: float | None = None,
-            out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-            return_lse: bool = True, stream=None):
+            k_scale: float = 1.0, v_scale: float = 1.0, out: torch.Tensor | None = None,
+            lse: torch.Tensor | None = None, return_lse: bool = True, stream=None):
+        """Cascade decode; k_scale / v_scale are an E4M3 cache's per-tensor
+        scales (1 for a 16-bit cache)."""
         B, Hq, D = self.batch, self.num_qo_heads, self.head_dim
-        if q.dtype != self.q_dtype or paged_kv.dtype != self.q_dtype:
+        if q.dtype != self.q_dtype or paged_kv.dtype != self.kv_dtype:
             raise TypeError("q / paged_kv dtype differs from the plan")
         if tuple(q.shape) != (B, Hq, D) or not q.is_contiguous() or not paged_kv.is_contiguous():
             raise ValueError(f"q must be a contiguous CUDA tensor [{B}, {Hq}, {D}]")
@@ -573,10 +578,11 @@ class CascadePlan:
             out = torch.empty_like(q)
         if return_lse and lse is None:
             lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
-        _check(_L().fa_cascade_run(self._h, q.data_ptr(), paged_kv.data_ptr(), paged_kv.shape[0],
-                                   0.0 if sm_scale is None else float(sm_scale), out.data_ptr(),
-                                   lse.data_ptr() if lse is not None else None,
-                                   _stream_handle(stream)), "fa_cascade_run")
+        _check(_L().fa_cascade_run_scaled(
+            self._h, q.data_ptr(), paged_kv.data_ptr(), paged_kv.shape[0],
+            0.0 if sm_scale is None else float(sm_scale), float(k_scale), float(v_scale),
+            out.data_ptr(), lse.data_ptr() if lse is not None else None,
+            _stream_handle(stream)), "fa_cascade_run_scaled")
         return out, lse
 
     def set_timing_events(self, before, after) -> None:
@@ -594,8 +600,8 @@ class CascadePlan:
 
 def cascade_plan(prefix_indices: torch.Tensor, indptr, indices: torch.Tensor, last_page_len,
                  num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int, *,
-                 q_data_type=torch.bfloat16, workspace: torch.Tensor | None = None,
-                 stream=None) -> CascadePlan:
+                 q_data_type=torch.bfloat16, kv_data_type=None,
+                 workspace: torch.Tensor | None = None, stream=None) -> CascadePlan:
     """Plan cascade decode: prefix_indices are the shared (full) pages every
     request starts with; indptr/indices/last_page_len describe each request's
     own pages after them."""
@@ -613,15 +619,15 @@ def cascade_plan(prefix_indices: torch.Tensor, indptr, indices: torch.Tensor, la
             raise ValueError("invalid shape or no CUDA device")
         workspace = torch.empty(int(n), dtype=torch.uint8, device=prefix_indices.device)
     handle = ctypes.c_void_p()
-    code = _dtype_code(q_data_type)
+    kv_data_type = q_data_type if kv_data_type is None else kv_data_type
     _check(_L().fa_cascade_plan(
         prefix_indices.data_ptr(), prefix_indices.numel(), indptr_p,
         indices.data_ptr() if indices.numel() else None, last_p if B else None, B, num_qo_heads,
-        num_kv_heads, head_dim, page_size, code, code, workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), _stream_handle(stream),
-        ctypes.byref(handle)), "fa_cascade_plan")
+        num_kv_heads, head_dim, page_size, _dtype_code(q_data_type), _dtype_code(kv_data_type),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream), ctypes.byref(handle)), "fa_cascade_plan")
     return CascadePlan(handle.value, (prefix_indices, indices, workspace), q_data_type,
-                       (B, num_qo_heads, num_kv_heads, head_dim))
+                       (B, num_qo_heads, num_kv_heads, head_dim), kv_dtype=kv_data_type)
 
 
 class BatchDecodeWithPagedKVCacheWrapper:

@@ -180,8 +180,14 @@ bool find_ragged_q_kernel(fa_dtype q, fa_dtype kv, int D, int G, int max_q, Deco
 }
 
 bool find_unified_max_kernel(fa_dtype q, fa_dtype kv, int D, int G, DecodeKernel* k) {
-  if (q != FA_DTYPE_BF16 || kv != FA_DTYPE_BF16 || !tensor_cores_allowed()) return false;
-  return fadecode::find_unified_max_kernel_bf16(D, G, k);
+  if (!tensor_cores_allowed()) return false;
+  if (q == FA_DTYPE_BF16 && kv == FA_DTYPE_BF16) return fadecode::find_unified_max_kernel_bf16(D, G, k);
+  if (q == FA_DTYPE_F16 && kv == FA_DTYPE_F16) return fadecode::find_unified_max_kernel_f16(D, G, k);
+  if (q == FA_DTYPE_BF16 && kv == FA_DTYPE_E4M3)
+    return fadecode::find_unified_max_kernel_bf16_e4m3(D, G, k);
+  if (q == FA_DTYPE_F16 && kv == FA_DTYPE_E4M3)
+    return fadecode::find_unified_max_kernel_f16_e4m3(D, G, k);
+  return false;
 }
 
 bool find_token_scale_kernel(fa_dtype q, fa_dtype kv, int D, int G, DecodeKernel* k) {

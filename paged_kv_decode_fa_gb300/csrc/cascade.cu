@@ -45,7 +45,8 @@ struct PrefixParams {
   float* part_o;        // [items][128 rows][D], normalised
   float* part_lse;      // [items][128 rows], log2 domain
   int group;            // query heads per kv head
-  float q_scale;        // sm_scale * log2(e)
+  float q_scale;        // sm_scale * k_scale * log2(e)
+  float v_scale;        // applied to the partial outputs (E4M3 KV; 1 otherwise)
   int row_blocks;       // 128-row blocks per kv head
   int pair_blocks;      // pairs of row blocks per kv head (tcgen05 kernel)
   int chunks;           // prefix chunks
@@ -65,11 +66,13 @@ struct CombineParams {
 
 constexpr int kPrefixRows = 128;  // rows per CTA: 8 consumer warps x 16
 
-template <typename QT, int D, int NW>
+template <typename KVT, int D, int NW>
 struct PrefixCfg {
   static constexpr int P = kPageSize;
-  static constexpr int SEGS = D * 2 / 128;        // 128-byte row segments (16-bit KV)
-  static constexpr int BOX_X = 64;
+  static constexpr int KV_ES = sizeof(KVT);
+  static constexpr bool kFp8 = KV_ES == 1;
+  static constexpr int SEGS = D * KV_ES / 128;    // 128-byte row segments
+  static constexpr int BOX_X = 128 / KV_ES;       // elements per box row
   static constexpr int BOX_BYTES = 2 * P * 128;
   static constexpr int STAGE_BYTES = SEGS * BOX_BYTES;
   static constexpr int KSTEPS = D / 16;
@@ -80,16 +83,26 @@ struct PrefixCfg {
   static constexpr int OFF_EMPTY = OFF_FULL + 8 * S;
   static constexpr int SMEM = OFF_EMPTY + 8 * S;
   static_assert(NW * 16 == kPrefixRows, "16 rows per consumer warp");
-  static_assert((D * 2) % 128 == 0, "rows must be whole 128-byte swizzle rows");
+  static_assert((D * KV_ES) % 128 == 0, "rows must be whole 128-byte swizzle rows");
+  static_assert(!kFp8 || D == 128, "E4M3 prefix rows are laid out for head_dim 128");
 };
 
-template <typename QT, int D, int NW>
-__global__ void __launch_bounds__(PrefixCfg<QT, D, NW>::THREADS)
+// The prefix pass on warp-level MMAs.  16-bit KV: the MMA type is the KV
+// type and q is its A fragment as stored.  E4M3 KV: the MMAs run in f16 -
+// K and V are widened in registers (exact), q is scaled by a power of two
+// per warp into f16 range (the scores are scaled back), k_scale is folded
+// into q_scale and v_scale into the partial outputs.
+template <typename QT, typename KVT, int D, int NW>
+__global__ void __launch_bounds__(PrefixCfg<KVT, D, NW>::THREADS)
     fa_prefix_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p,
                      const PrefixParams pp) {
-  using C = PrefixCfg<QT, D, NW>;
+  using C = PrefixCfg<KVT, D, NW>;
   constexpr int P = C::P, S = C::S, SEGS = C::SEGS, KSTEPS = C::KSTEPS, NT = C::NT;
-  constexpr bool kBf16 = std::is_same<QT, __nv_bfloat16>::value;
+  constexpr bool kFp8 = C::kFp8;
+  constexpr bool kQBf16 = std::is_same<QT, __nv_bfloat16>::value;
+  // MMA operand type: the KV type for 16-bit KV, f16 for E4M3
+  constexpr bool kBf16 = !kFp8 && kQBf16;
+  static_assert(kFp8 || std::is_same<QT, KVT>::value, "16-bit KV: q of the same type");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (dev::smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* ring = smem;
@@ -120,9 +133,12 @@ __global__ void __launch_bounds__(PrefixCfg<QT, D, NW>::THREADS)
   const int r_lo = warp * 16 + g, r_hi = r_lo + 8;  // rows within the block
 
   // Q as the A fragment for the whole chunk, reduction index permuted as in
-  // the decode kernels: step j = 4*seg + 2*half + u covers dims
+  // the decode kernels.  16-bit KV: step j = 4*seg + 2*half + u covers dims
   // seg*64 + (2t + half)*8 + 4u .. +3 (a0/a1 the first two, a2/a3 the last).
+  // E4M3 KV: step j covers dims 32t + 4j .. +3, the four bytes word j%4 of
+  // granule 2t + j/4 of a K row holds.
   uint32_t qa[KSTEPS][4];
+  float qscale = pp.q_scale;
   {
     const QT* qbase = static_cast<const QT*>(pp.q);
     const int rows[2] = {r_lo, r_hi};
@@ -134,13 +150,45 @@ __global__ void __launch_bounds__(PrefixCfg<QT, D, NW>::THREADS)
       const QT* qrow = qbase + ((size_t)(rho / G) * p.num_qo_heads + kvh * G + rho % G) * D;
 #pragma unroll
       for (int L = 0; L < KSTEPS / 2; ++L) {
+        const int d0 = kFp8 ? 32 * t + 8 * L : (L >> 1) * 64 + (2 * t + (L & 1)) * 8;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (live) v = __ldg(reinterpret_cast<const uint4*>(qrow + (L >> 1) * 64 + (2 * t + (L & 1)) * 8));
+        if (live) v = __ldg(reinterpret_cast<const uint4*>(qrow + d0));
         raw[rr][2 * L][0] = v.x;
         raw[rr][2 * L][1] = v.y;
         raw[rr][2 * L + 1][0] = v.z;
         raw[rr][2 * L + 1][1] = v.w;
       }
+    }
+    if constexpr (kFp8) {
+      // f16 MMAs: q times 2^shift (one shift per warp) with its largest
+      // magnitude in [2^14, 2^15); the scores are scaled back by qscale
+      float amax = 0.f;
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int j = 0; j < KSTEPS; ++j)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float2 f = mma::unpack2(raw[rr][j][h], kQBf16);
+            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+          }
+      const unsigned bits = __reduce_max_sync(0xffffffffu, __float_as_uint(amax));
+      int shift = 0;
+      if (bits != 0u && bits < 0x7f800000u) {
+        const int ex = (int)((bits >> 23) & 0xff) - 127;
+        shift = min(max(14 - ex, -120), 120);
+      }
+      const float up = ldexpf(1.f, shift);
+      qscale = pp.q_scale * ldexpf(1.f, -shift);
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int j = 0; j < KSTEPS; ++j)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float2 f = mma::unpack2(raw[rr][j][h], kQBf16);
+            raw[rr][j][h] = mma::pack2(f.x * up, f.y * up, false);
+          }
     }
 #pragma unroll
     for (int j = 0; j < KSTEPS; ++j) {
@@ -179,13 +227,27 @@ __global__ void __launch_bounds__(PrefixCfg<QT, D, NW>::THREADS)
         const uint4 k1 = mma::lds128(st + sgi * C::BOX_BYTES + (g + 8) * 128 + gran);
         const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
         const uint32_t w1[4] = {k1.x, k1.y, k1.z, k1.w};
+        if constexpr (kFp8) {
+          // word w: dims 32t + 16qq + 4w .. +3 of K rows g / g+8, widened to
+          // the B fragment (b0: the first two dims, b1: the last two)
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int j = sgi * 4 + qq * 2 + u;
-          mma::mma16816<kBf16>(acc[0][u], qa[j][0], qa[j][1], qa[j][2], qa[j][3], w0[2 * u],
-                               w0[2 * u + 1]);
-          mma::mma16816<kBf16>(acc[1][u], qa[j][0], qa[j][1], qa[j][2], qa[j][3], w1[2 * u],
-                               w1[2 * u + 1]);
+          for (int w = 0; w < 4; ++w) {
+            const int j = qq * 4 + w;
+            uint32_t b0, b1, c0, c1;
+            mma::e4m3x4_to_f16x2x2(w0[w], b0, b1);
+            mma::e4m3x4_to_f16x2x2(w1[w], c0, c1);
+            mma::mma16816<false>(acc[0][j & 1], qa[j][0], qa[j][1], qa[j][2], qa[j][3], b0, b1);
+            mma::mma16816<false>(acc[1][j & 1], qa[j][0], qa[j][1], qa[j][2], qa[j][3], c0, c1);
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int j = sgi * 4 + qq * 2 + u;
+            mma::mma16816<kBf16>(acc[0][u], qa[j][0], qa[j][1], qa[j][2], qa[j][3], w0[2 * u],
+                                 w0[2 * u + 1]);
+            mma::mma16816<kBf16>(acc[1][u], qa[j][0], qa[j][1], qa[j][2], qa[j][3], w1[2 * u],
+                                 w1[2 * u + 1]);
+          }
         }
       }
     }
@@ -198,7 +260,7 @@ __global__ void __launch_bounds__(PrefixCfg<QT, D, NW>::THREADS)
 #pragma unroll
     for (int n = 0; n < 2; ++n)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) sc[n][e] *= pp.q_scale;
+      for (int e = 0; e < 4; ++e) sc[n][e] *= qscale;
     float mx[2] = {fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])),
                    fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]))};
 #pragma unroll
@@ -246,18 +308,44 @@ __global__ void __launch_bounds__(PrefixCfg<QT, D, NW>::THREADS)
       }
     }
     // ---- O[rows][dims] += P V: B fragments of V from ldmatrix.trans
+    if constexpr (kFp8) {
+      // a granule holds 16 dims of 8 tokens as 8 byte pairs; transposed as
+      // 16-bit elements, a lane gets dim pair g of tokens 2t, 2t+1 (and of
+      // 8+2t, 9+2t), split with one byte permute into the f16 B fragments of
+      // dim 2g (n-tile 2*gran) and dim 2g+1 (n-tile 2*gran+1): n-tile
+      // 2*gran + e, column c holds dim 16*gran + 2c + e
 #pragma unroll
-    for (int n2 = 0; n2 < NT / 2; ++n2) {
-      const int mi = lane >> 3, r = lane & 7;
-      const int sgi = (n2 * 16) / C::BOX_X;
-      const int gran = ((n2 * 16) % C::BOX_X) / 8 + (mi >> 1);
-      const int tok = (mi & 1) * 8 + r;
-      uint32_t b0, b1, b2, b3;
-      mma::ldsm_x4_trans(st + sgi * C::BOX_BYTES + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16),
-                         b0, b1, b2, b3);
-      // b0/b1: dims 16*n2 + 0..7, tokens 0..7 / 8..15; b2/b3: dims + 8..15
-      mma::mma16816<kBf16>(o[2 * n2], pa[0], pa[1], pa[2], pa[3], b0, b1);
-      mma::mma16816<kBf16>(o[2 * n2 + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
+      for (int g2 = 0; g2 < NT / 4; ++g2) {
+        const int mi = lane >> 3, r = lane & 7;
+        const int gran = 2 * g2 + (mi >> 1);
+        const int tok = (mi & 1) * 8 + r;
+        uint32_t d0, d1, d2, d3;
+        mma::ldsm_x4_trans(st + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16), d0, d1, d2, d3);
+        uint32_t lo0, hi0, lo1, hi1, lo2, hi2, lo3, hi3;
+        mma::e4m3x4_to_f16x2x2(__byte_perm(d0, 0u, 0x3120), lo0, hi0);
+        mma::e4m3x4_to_f16x2x2(__byte_perm(d1, 0u, 0x3120), lo1, hi1);
+        mma::e4m3x4_to_f16x2x2(__byte_perm(d2, 0u, 0x3120), lo2, hi2);
+        mma::e4m3x4_to_f16x2x2(__byte_perm(d3, 0u, 0x3120), lo3, hi3);
+        // matrices 0/1: granule 2*g2, tokens 0..7 / 8..15; 2/3: granule 2*g2+1
+        mma::mma16816<false>(o[4 * g2], pa[0], pa[1], pa[2], pa[3], lo0, lo1);
+        mma::mma16816<false>(o[4 * g2 + 1], pa[0], pa[1], pa[2], pa[3], hi0, hi1);
+        mma::mma16816<false>(o[4 * g2 + 2], pa[0], pa[1], pa[2], pa[3], lo2, lo3);
+        mma::mma16816<false>(o[4 * g2 + 3], pa[0], pa[1], pa[2], pa[3], hi2, hi3);
+      }
+    } else {
+#pragma unroll
+      for (int n2 = 0; n2 < NT / 2; ++n2) {
+        const int mi = lane >> 3, r = lane & 7;
+        const int sgi = (n2 * 16) / C::BOX_X;
+        const int gran = ((n2 * 16) % C::BOX_X) / 8 + (mi >> 1);
+        const int tok = (mi & 1) * 8 + r;
+        uint32_t b0, b1, b2, b3;
+        mma::ldsm_x4_trans(st + sgi * C::BOX_BYTES + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16),
+                           b0, b1, b2, b3);
+        // b0/b1: dims 16*n2 + 0..7, tokens 0..7 / 8..15; b2/b3: dims + 8..15
+        mma::mma16816<kBf16>(o[2 * n2], pa[0], pa[1], pa[2], pa[3], b0, b1);
+        mma::mma16816<kBf16>(o[2 * n2 + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
+      }
     }
     dev::release_stage(dev::smem_addr(&empty[stage]), lane);
   }
@@ -268,12 +356,19 @@ __global__ void __launch_bounds__(PrefixCfg<QT, D, NW>::THREADS)
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
     if (rows[rr] >= row_count) continue;
-    const float inv = d_r[rr] > 0.f ? 1.f / d_r[rr] : 0.f;
+    const float inv = d_r[rr] > 0.f ? pp.v_scale / d_r[rr] : 0.f;
     float* dst = pp.part_o + ((size_t)out_item * kPrefixRows + rows[rr]) * D;
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-      const float2 v = make_float2(o[n][2 * rr] * inv, o[n][2 * rr + 1] * inv);
-      *reinterpret_cast<float2*>(dst + n * 8 + 2 * t) = v;
+      if constexpr (kFp8) {
+        // n-tile n = 2*gran + e, column c: dim 16*gran + 2c + e
+        const int base = 16 * (n >> 1) + (n & 1);
+        dst[base + 2 * (2 * t)] = o[n][2 * rr] * inv;
+        dst[base + 2 * (2 * t + 1)] = o[n][2 * rr + 1] * inv;
+      } else {
+        const float2 v = make_float2(o[n][2 * rr] * inv, o[n][2 * rr + 1] * inv);
+        *reinterpret_cast<float2*>(dst + n * 8 + 2 * t) = v;
+      }
     }
     if (t == 0)
       pp.part_lse[(size_t)out_item * kPrefixRows + rows[rr]] =
@@ -289,11 +384,13 @@ namespace fadecode {
 
 // One warp per (request, qo head): fold the prefix chunks' states and the
 // suffix state with the merge rule.  Lane k holds chunk k's log2-sum-exp
-// (32 chunks at a time) and lane l the dims [4l, 4l + 4) of the output;
-// the chunk loop keeps several 16-byte loads of partial outputs in flight.
+// (32 chunks at a time) and lane l the dims [V*l, V*l + V) of the output
+// (V = D / 32); the chunk loop keeps several loads of partial outputs in
+// flight.
 template <typename QT, int D>
 __global__ void __launch_bounds__(256) fa_cascade_combine_kernel(const CombineParams c) {
-  static_assert(D == 128, "four dims per lane");
+  static_assert(D == 128 || D == 64, "four or two dims per lane");
+  constexpr int V = D / 32;
   const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= (int64_t)c.batch * c.num_qo_heads) return;
@@ -310,44 +407,50 @@ __global__ void __launch_bounds__(256) fa_cascade_combine_kernel(const CombinePa
   for (int k0 = 0; k0 < c.chunks; k0 += 32) M = fmaxf(M, chunk_lse(k0 + lane));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float num[4] = {0.f, 0.f, 0.f, 0.f};
+  float num[V] = {};
   float den = 0.f, lse2 = -INFINITY;
+  const bool bf = std::is_same<QT, __nv_bfloat16>::value;
   if (M != -INFINITY) {
     for (int k0 = 0; k0 < c.chunks; k0 += 32) {
       const float wl = dev::fast_exp2(chunk_lse(k0 + lane) - M);  // 0 past the last chunk
       den += wl;
       const int n = min(32, c.chunks - k0);
-      const float* src = c.part_o + ((size_t)(item0 + k0) * kPrefixRows + row) * D + 4 * lane;
+      const float* src = c.part_o + ((size_t)(item0 + k0) * kPrefixRows + row) * D + V * lane;
 #pragma unroll 4
       for (int i = 0; i < n; ++i) {
         const float w = __shfl_sync(0xffffffffu, wl, i);
-        const float4 x = __ldg(reinterpret_cast<const float4*>(src + (size_t)i * kPrefixRows * D));
-        num[0] = fmaf(x.x, w, num[0]);
-        num[1] = fmaf(x.y, w, num[1]);
-        num[2] = fmaf(x.z, w, num[2]);
-        num[3] = fmaf(x.w, w, num[3]);
+        const float* s = src + (size_t)i * kPrefixRows * D;
+        if constexpr (V == 4) {
+          const float4 x = __ldg(reinterpret_cast<const float4*>(s));
+          num[0] = fmaf(x.x, w, num[0]);
+          num[1] = fmaf(x.y, w, num[1]);
+          num[2] = fmaf(x.z, w, num[2]);
+          num[3] = fmaf(x.w, w, num[3]);
+        } else {
+          const float2 x = __ldg(reinterpret_cast<const float2*>(s));
+          num[0] = fmaf(x.x, w, num[0]);
+          num[1] = fmaf(x.y, w, num[1]);
+        }
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     const float ws = dev::fast_exp2(ls - M);
     den += ws;
-    const uint2 sv =
-        *reinterpret_cast<const uint2*>(static_cast<const QT*>(c.suffix_o) + wid * D + 4 * lane);
-    const bool bf = std::is_same<QT, __nv_bfloat16>::value;
-    const float2 s01 = mma::unpack2(sv.x, bf), s23 = mma::unpack2(sv.y, bf);
-    num[0] = fmaf(s01.x, ws, num[0]);
-    num[1] = fmaf(s01.y, ws, num[1]);
-    num[2] = fmaf(s23.x, ws, num[2]);
-    num[3] = fmaf(s23.y, ws, num[3]);
+    const QT* sv = static_cast<const QT*>(c.suffix_o) + wid * D + V * lane;
+#pragma unroll
+    for (int v = 0; v < V; v += 2) {
+      const float2 s01 = mma::unpack2(*reinterpret_cast<const uint32_t*>(sv + v), bf);
+      num[v] = fmaf(s01.x, ws, num[v]);
+      num[v + 1] = fmaf(s01.y, ws, num[v + 1]);
+    }
     lse2 = M + dev::fast_log2(den);
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
-  const bool bf = std::is_same<QT, __nv_bfloat16>::value;
-  uint2 ov;
-  ov.x = mma::pack2(num[0] * inv, num[1] * inv, bf);
-  ov.y = mma::pack2(num[2] * inv, num[3] * inv, bf);
-  *reinterpret_cast<uint2*>(static_cast<QT*>(c.o) + wid * D + 4 * lane) = ov;
+  QT* ov = static_cast<QT*>(c.o) + wid * D + V * lane;
+#pragma unroll
+  for (int v = 0; v < V; v += 2)
+    *reinterpret_cast<uint32_t*>(ov + v) = mma::pack2(num[v] * inv, num[v + 1] * inv, bf);
   if (lane == 0 && c.lse) c.lse[wid] = lse2 * 0.693147180559945309f;
 }
 
@@ -376,22 +479,45 @@ bool cascade_tcgen05() {
   return !(v && std::strcmp(v, "mma") == 0);
 }
 
-template <typename QT>
+// The prefix pass on tcgen05 for 16-bit KV at head_dim 128 (unless
+// FADECODE_CASCADE=mma), on the mma.sync kernel otherwise (head_dim 64,
+// E4M3 KV).
+template <typename QT, typename KVT, int D>
 CascadeKernels cascade_kernels() {
   CascadeKernels k;
-  k.combine = reinterpret_cast<const void*>(&fadecode::fa_cascade_combine_kernel<QT, 128>);
-  if (cascade_tcgen05()) {
-    k.prefix = reinterpret_cast<const void*>(&fadecode::fa_prefix_tc_kernel<QT>);
-    k.threads = fadecode::tc::kThreads;
-    k.smem = fadecode::tc::kSmem + 1024;
-    k.tcgen05 = true;
-    return k;
+  k.combine = reinterpret_cast<const void*>(&fadecode::fa_cascade_combine_kernel<QT, D>);
+  if constexpr (std::is_same<QT, KVT>::value && D == 128) {
+    if (cascade_tcgen05()) {
+      k.prefix = reinterpret_cast<const void*>(&fadecode::fa_prefix_tc_kernel<QT>);
+      k.threads = fadecode::tc::kThreads;
+      k.smem = fadecode::tc::kSmem + 1024;
+      k.tcgen05 = true;
+      return k;
+    }
   }
-  using C = fadecode::PrefixCfg<QT, 128, 8>;
-  k.prefix = reinterpret_cast<const void*>(&fadecode::fa_prefix_kernel<QT, 128, 8>);
+  using C = fadecode::PrefixCfg<KVT, D, 8>;
+  k.prefix = reinterpret_cast<const void*>(&fadecode::fa_prefix_kernel<QT, KVT, D, 8>);
   k.threads = C::THREADS;
   k.smem = C::SMEM + 1024;
   return k;
+}
+
+// The kernels of a (q, kv, head_dim) combination; false if not built.
+bool find_cascade_kernels(fa_dtype q, fa_dtype kv, int D, CascadeKernels* k) {
+  const bool e4m3 = kv == FA_DTYPE_E4M3;
+  if (q == FA_DTYPE_BF16 && kv == FA_DTYPE_BF16) {
+    *k = D == 128 ? cascade_kernels<__nv_bfloat16, __nv_bfloat16, 128>()
+                  : cascade_kernels<__nv_bfloat16, __nv_bfloat16, 64>();
+  } else if (q == FA_DTYPE_F16 && kv == FA_DTYPE_F16) {
+    *k = D == 128 ? cascade_kernels<__half, __half, 128>() : cascade_kernels<__half, __half, 64>();
+  } else if (e4m3 && D == 128 && q == FA_DTYPE_BF16) {
+    *k = cascade_kernels<__nv_bfloat16, __nv_fp8_e4m3, 128>();
+  } else if (e4m3 && D == 128 && q == FA_DTYPE_F16) {
+    *k = cascade_kernels<__half, __nv_fp8_e4m3, 128>();
+  } else {
+    return false;
+  }
+  return true;
 }
 
 // kv_rows = 2: one box brings a page's K and V rows together (mma.sync
@@ -409,17 +535,18 @@ int encode_prefix_map(CUtensorMap* map, fa_dtype dt, const void* paged_kv, int64
       return FA_ERR_CUDA;
     fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
   }
-  const size_t es = 2;
+  const size_t es = dt == FA_DTYPE_E4M3 ? 1 : 2;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)P,
                         (cuuint64_t)(2 * num_pages)};
   cuuint64_t strides[3] = {(cuuint64_t)(D * es), (cuuint64_t)(Hkv * D * es),
                            (cuuint64_t)(P * Hkv * D * es)};
-  cuuint32_t box[4] = {64u, 1u, (cuuint32_t)P, (cuuint32_t)kv_rows};
+  // one box row is 128 bytes of a K or V row (the 128-byte swizzle span)
+  cuuint32_t box[4] = {(cuuint32_t)(128 / es), 1u, (cuuint32_t)P, (cuuint32_t)kv_rows};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  const CUresult r = fn(map,
-                        dt == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        4, const_cast<void*>(paged_kv), dims, strides, box, estr,
+  const CUtensorMapDataType type = dt == FA_DTYPE_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : dt == FA_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUresult r = fn(map, type, 4, const_cast<void*>(paged_kv), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
@@ -459,7 +586,8 @@ struct fa_cascade_plan_s {
   int batch = 0, hq = 0, hkv = 0, d = 0, group = 0, row_blocks = 0, chunks = 0, items = 0;
   int prefix_pages = 0;
   int grid = 0;  // prefix CTAs: one per item, or per item pair on tcgen05
-  fa_dtype dtype = FA_DTYPE_BF16;
+  fa_dtype dtype = FA_DTYPE_BF16;     // q
+  fa_dtype kv_dtype = FA_DTYPE_BF16;
   const int32_t* prefix_indices = nullptr;
   uint8_t* ws = nullptr;
   CascadeLayout L{};
@@ -579,8 +707,9 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
       num_qo_heads <= 0 || num_kv_heads <= 0 || num_qo_heads % num_kv_heads || !workspace_dev ||
       reinterpret_cast<uintptr_t>(workspace_dev) % kCAlign)
     return FA_ERR_INVALID_ARG;
-  if (page_size != fadecode::kPageSize || head_dim != 128 || q_dtype != kv_dtype ||
-      (q_dtype != FA_DTYPE_BF16 && q_dtype != FA_DTYPE_F16))
+  CascadeKernels k;
+  if (page_size != fadecode::kPageSize || (head_dim != 128 && head_dim != 64) ||
+      !find_cascade_kernels(q_dtype, kv_dtype, head_dim, &k))
     return FA_ERR_UNSUPPORTED;
   const size_t sw = fa_decode_workspace_size(batch, num_qo_heads, num_kv_heads, head_dim);
   if (sw == 0) return FA_ERR_CUDA;
@@ -588,8 +717,6 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return FA_ERR_CUDA;
-  CascadeKernels k = q_dtype == FA_DTYPE_BF16 ? cascade_kernels<__nv_bfloat16>()
-                                              : cascade_kernels<__half>();
   const int occ = prefix_occupancy(k, dev);
   if (occ < 1) return FA_ERR_CUDA;
 
@@ -608,6 +735,7 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
   plan->d = head_dim;
   plan->group = num_qo_heads / num_kv_heads;
   plan->dtype = q_dtype;
+  plan->kv_dtype = kv_dtype;
   plan->prefix_indices = prefix_indices_dev;
   plan->ws = static_cast<uint8_t*>(workspace_dev);
   plan->k = k;
@@ -692,7 +820,18 @@ int fa_cascade_plan(const int32_t* prefix_indices_dev, int num_prefix_pages,
 
 int fa_cascade_run(fa_cascade_plan_t plan, const void* q, const void* paged_kv,
                    int64_t num_pages, float sm_scale, void* o, float* lse, void* cuda_stream) {
+  return fa_cascade_run_scaled(plan, q, paged_kv, num_pages, sm_scale, 1.f, 1.f, o, lse,
+                               cuda_stream);
+}
+
+int fa_cascade_run_scaled(fa_cascade_plan_t plan, const void* q, const void* paged_kv,
+                          int64_t num_pages, float sm_scale, float k_scale, float v_scale,
+                          void* o, float* lse, void* cuda_stream) {
   if (!plan || !q || !paged_kv || !o || num_pages <= 0) return FA_ERR_INVALID_ARG;
+  // per-tensor scales belong to an E4M3 cache; a 16-bit one is used as stored
+  if (plan->kv_dtype != FA_DTYPE_E4M3 && (k_scale != 1.f || v_scale != 1.f))
+    return FA_ERR_INVALID_ARG;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(paged_kv) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
     return FA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
@@ -709,12 +848,12 @@ int fa_cascade_run(fa_cascade_plan_t plan, const void* q, const void* paged_kv,
                cudaStreamWaitEvent(plan->side, plan->ev_fork, 0) != cudaSuccess))
     return FA_ERR_CUDA;
   // 1. each request's own pages
-  int rc = fa_decode_run(plan->suffix, q, paged_kv, num_pages, sm_scale, 1.f, 1.f, so, slse,
-                         cuda_stream);
+  int rc = fa_decode_run(plan->suffix, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, so,
+                         slse, cuda_stream);
   if (rc != FA_OK) return rc;
   // 2. the shared prefix, once per kv head and row block
   if (paged_kv != plan->map_base || num_pages != plan->map_pages) {
-    rc = encode_prefix_map(&plan->map, plan->dtype, paged_kv, num_pages, D, plan->hkv,
+    rc = encode_prefix_map(&plan->map, plan->kv_dtype, paged_kv, num_pages, D, plan->hkv,
                            fadecode::kPageSize, plan->k.tcgen05 ? 1 : 2);
     if (rc != FA_OK) return rc;
     plan->map_base = paged_kv;
@@ -736,7 +875,8 @@ int fa_cascade_run(fa_cascade_plan_t plan, const void* q, const void* paged_kv,
   pp.part_o = reinterpret_cast<float*>(ws + plan->L.off_part_o);
   pp.part_lse = reinterpret_cast<float*>(ws + plan->L.off_part_lse);
   pp.group = plan->group;
-  pp.q_scale = sm_scale * 1.4426950408889634f;
+  pp.q_scale = sm_scale * k_scale * 1.4426950408889634f;
+  pp.v_scale = v_scale;
   pp.row_blocks = plan->row_blocks;
   pp.pair_blocks = (plan->row_blocks + 1) / 2;
   pp.chunks = plan->chunks;

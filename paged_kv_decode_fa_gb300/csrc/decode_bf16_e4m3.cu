@@ -12,4 +12,7 @@ bool find_token_scale_kernel_bf16_e4m3(int head_dim, int group, DecodeKernel* k)
 bool find_multi_token_kernel_bf16_e4m3(int head_dim, int group, int q_len, DecodeKernel* k) {
   return find_multi_token_kernel_for<__nv_bfloat16, __nv_fp8_e4m3>(head_dim, group, q_len, k);
 }
+bool find_unified_max_kernel_bf16_e4m3(int head_dim, int group, DecodeKernel* k) {
+  return find_unified_max_kernel_for<__nv_bfloat16, __nv_fp8_e4m3>(head_dim, group, k);
+}
 }  // namespace fadecode

@@ -9,4 +9,7 @@ bool find_kernel_f16_e4m3(int head_dim, int group, bool allow_mma, DecodeKernel*
 bool find_token_scale_kernel_f16_e4m3(int head_dim, int group, DecodeKernel* k) {
   return find_token_scale_kernel_for<__half>(head_dim, group, k);
 }
+bool find_unified_max_kernel_f16_e4m3(int head_dim, int group, DecodeKernel* k) {
+  return find_unified_max_kernel_for<__half, __nv_fp8_e4m3>(head_dim, group, k);
+}
 }  // namespace fadecode

@@ -52,30 +52,6 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// m16n8k32 with E4M3 A and B (fp32 accumulate): four 8-bit elements per
-// register, element i in byte i.
-__device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Four floats -> four E4M3 codes (round to nearest even, saturating at
-// 448), element i in byte i.
-__device__ __forceinline__ uint32_t f32x4_to_e4m3x4(float e0, float e1, float e2, float e3) {
-  uint32_t out;
-  asm("{\n\t.reg .b16 lo, hi;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
-      "mov.b32 %0, {lo, hi};\n\t}"
-      : "=r"(out)
-      : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
-  return out;
-}
-
 template <bool kBf16>
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -196,13 +172,24 @@ struct MmaCfg {
 };
 
 // Unified-max softmax window (log2 units): while a column's running maximum
-// m stays within [ref - kUmBelow, ref + kUmAbove] of the static reference,
-// its weights are exp2(s - ref) with no running-max bookkeeping.  Above: a
-// weight stays below 2^16 and a sum over 2^31 tokens below 2^47 (fp32 and
-// bf16 hold both).  Below: ex2.approx flushes weights under 2^-126 to zero,
-// so a flushed token weighs under 2^(64-126) relative to the maximum one.
-constexpr float kUmAbove = 16.f;
-constexpr float kUmBelow = 64.f;
+// m stays within [ref - below, ref + above] of the static reference, its
+// weights are exp2(s - ref) with no running-max bookkeeping.  bf16 weights:
+// above 16 - a weight stays below 2^16 and a sum over 2^31 tokens below 2^47
+// (fp32 and bf16 hold both); below 64 - ex2.approx flushes weights under
+// 2^-126 to zero, so a flushed token weighs under 2^(64-126) relative to the
+// maximum one.  f16 weights (f16 and E4M3 KV) have a 5-bit exponent: above
+// 15 keeps every weight under 2^15 (f16 tops out at 65504); below 8 keeps the
+// largest weight at 2^-8 or more, so the tokens that matter (weights down to
+// 2^-6 of it) stay normal f16 numbers (2^-14 and up) and the ones that go
+// subnormal or flush (under 2^-24) weigh under 2^-6 and 2^-16 of it.
+constexpr float kUmAboveBf16 = 16.f, kUmBelowBf16 = 64.f;
+constexpr float kUmAboveF16 = 15.f, kUmBelowF16 = 8.f;
+// Without a static bound the reference of a column is its first observed
+// maximum, re-centred (exactly) only when a later page's maximum exceeds it
+// by more than 2^8: weights stay below 256, inside bf16 and f16 alike, and
+// the largest weight of a column is at least 1, so the weights that the
+// f16 conversion flushes (below 2^-24) weigh nothing next to it.
+constexpr float kLazyAbove = 8.f;
 
 template <typename QT, typename KVT, int D, int G, int NW, bool TS, int QL, bool UM,
           bool RQ = false>
@@ -223,7 +210,9 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
   // per segment to sit well inside the f16 range.
   constexpr bool kConvertQ = kFp8 && std::is_same<QT, __nv_bfloat16>::value;
   // the unified-max window relies on the 8-bit exponent of bf16 weights
-  static_assert(!UM || (kBf16 && !TS && QL == 1 && !RQ), "unified max: bf16 weights, plain decode");
+  static_assert(!UM || (!TS && QL == 1 && !RQ), "unified max: plain decode");
+  constexpr float kUmAbove = kBf16 ? kUmAboveBf16 : kUmAboveF16;
+  constexpr float kUmBelow = kBf16 ? kUmBelowBf16 : kUmBelowF16;
   static_assert(!RQ || !TS, "ragged q: no per-token scales");
 
   // Swizzled TMA destinations must sit on 1024-byte boundaries: the launch
@@ -385,7 +374,7 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
     // UM); d_h: this lane's share of the column's denominator, summed over
     // the column's 8 lanes once the segment is done
     float m_h[2] = {-INFINITY, -INFINITY}, d_h[2] = {0.f, 0.f};
-    float tmx[2] = {-INFINITY, -INFINITY};  // UM: this lane's running maxima
+    float tmx[2] = {-INFINITY, -INFINITY};  // this lane's running maxima of the columns
     bool um_first = true, um_moved = false;
     if constexpr (UM) m_h[0] = m_h[1] = p.max_bound;
 
@@ -459,21 +448,25 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
       }
 
       // ---- softmax for heads 2t (s[0], s[2]) and 2t+1 (s[1], s[3])
+      // The weights use a reference per column that moves only rarely, so a
+      // page needs no column reduction - only a vote on whether some lane's
+      // running maximum rose past the window above the reference.  Unified
+      // max (UM): the reference starts at the caller's static bound, and the
+      // first page of a segment also checks the window's lower edge (the
+      // running maximum never falls, so once a column is inside it stays
+      // inside).  Otherwise it starts empty and takes the column's first
+      // observed maximum.  A column leaving its window is re-centred on its
+      // true maximum (an exact rescale of its state).
       float alpha[2] = {1.f, 1.f}, pr[4], mref[2];
       bool rescale;
-      if constexpr (UM) {
-        // Unified max: the weights use the static reference, so a page needs
-        // no column reduction - only a vote on whether some lane's running
-        // maximum rose past the window.  The first page of a segment also
-        // checks the window's lower edge (the running maximum never falls,
-        // so once a column is inside it stays inside).  A column outside
-        // the window is re-centred on its true maximum (an exact rescale).
+      {
+        constexpr float kAbove = UM ? kUmAbove : kLazyAbove;
         tmx[0] = fmaxf(tmx[0], fmaxf(s[0], s[2]));
         tmx[1] = fmaxf(tmx[1], fmaxf(s[1], s[3]));
         const bool first = um_first;
         um_first = false;
         rescale = first ||
-                  __any_sync(0xffffffffu, tmx[0] > m_h[0] + kUmAbove || tmx[1] > m_h[1] + kUmAbove);
+                  __any_sync(0xffffffffu, tmx[0] > m_h[0] + kAbove || tmx[1] > m_h[1] + kAbove);
         if (rescale) {
           float mx[2] = {tmx[0], tmx[1]};
 #pragma unroll
@@ -483,35 +476,22 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
           }
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const bool outside = mx[e] > m_h[e] + kUmAbove || mx[e] < m_h[e] - kUmBelow;
+            const bool outside =
+                mx[e] > m_h[e] + kAbove || (UM && mx[e] < m_h[e] - kUmBelow);
             if (outside && mx[e] != -INFINITY) {
               // nothing accumulated before the first page (and a lowered
-              // reference could make this factor overflow)
+              // reference could make this factor overflow); a column still
+              // empty gets 0, which keeps its empty state
               alpha[e] = first ? 1.f : dev::fast_exp2(m_h[e] - mx[e]);
               m_h[e] = mx[e];
               um_moved = true;
             }
           }
         }
-        mref[0] = m_h[0];
-        mref[1] = m_h[1];
-      } else {
-        float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
-          mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
-        }
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float mn = fmaxf(m_h[e], mx[e]);
-          // a column can have seen nothing yet (every token so far masked by
-          // the causal rule): keep its state empty instead of exp2(-inf + inf)
-          mref[e] = mn == -INFINITY ? 0.f : mn;
-          alpha[e] = dev::fast_exp2(m_h[e] - mref[e]);
-          m_h[e] = mn;
-        }
-        rescale = true;
+        // a column that has seen nothing yet (every token so far masked):
+        // weights exp2(-inf - 0) = 0 keep its state empty
+        mref[0] = m_h[0] == -INFINITY ? 0.f : m_h[0];
+        mref[1] = m_h[1] == -INFINITY ? 0.f : m_h[1];
       }
       const uint32_t p01 = mma::pack2(dev::fast_exp2(s[0] - mref[0]),
                                       dev::fast_exp2(s[1] - mref[1]), kBf16);
@@ -727,13 +707,17 @@ inline bool find_ragged_q_kernel_for(int head_dim, int group, int max_q, DecodeK
   return false;
 }
 
-// Unified-max softmax (bf16 q and KV): tensor-core consumer, groups 2, 4, 8.
+// Unified-max softmax: tensor-core consumer, groups 2, 4, 8, rows of a
+// whole number of 128 bytes (E4M3: head_dim 128).
 template <typename QT, typename KVT>
 inline bool find_unified_max_kernel_for(int head_dim, int group, DecodeKernel* k) {
-#define FA_UM_CASE(DD, GG)                                   \
-  if (head_dim == DD && group == GG) {                       \
-    fill_mma_kernel<QT, KVT, DD, GG, 4, false, 1, true>(k);  \
-    return true;                                             \
+#define FA_UM_CASE(DD, GG)                                       \
+  if (head_dim == DD && group == GG) {                           \
+    if constexpr ((DD * sizeof(KVT)) % 128 == 0) {               \
+      fill_mma_kernel<QT, KVT, DD, GG, 4, false, 1, true>(k);    \
+      return true;                                               \
+    }                                                            \
+    return false;                                                \
   }
   FA_UM_CASE(64, 2) FA_UM_CASE(64, 4) FA_UM_CASE(64, 8)
   FA_UM_CASE(128, 2) FA_UM_CASE(128, 4) FA_UM_CASE(128, 8)

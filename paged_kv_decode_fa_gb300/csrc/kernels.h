@@ -95,8 +95,12 @@ bool find_multi_token_kernel_bf16_e4m3(int head_dim, int group, int q_len, Decod
 // query tokens (head_dim 128; group x max_q <= 32).
 bool find_ragged_q_kernel_bf16(int head_dim, int group, int max_q, DecodeKernel* k);
 bool find_ragged_q_kernel_bf16_e4m3(int head_dim, int group, int max_q, DecodeKernel* k);
-// Unified-max softmax (bf16 q and KV, groups 2, 4, 8, head_dim 64 or 128).
+// Unified-max softmax (groups 2, 4, 8; bf16 q and KV at head_dim 64 or 128).
 bool find_unified_max_kernel_bf16(int head_dim, int group, DecodeKernel* k);
+// The same with f16 weights: f16 q and KV, or E4M3 KV (head_dim 128 for E4M3).
+bool find_unified_max_kernel_f16(int head_dim, int group, DecodeKernel* k);
+bool find_unified_max_kernel_bf16_e4m3(int head_dim, int group, DecodeKernel* k);
+bool find_unified_max_kernel_f16_e4m3(int head_dim, int group, DecodeKernel* k);
 // E4M3 KV with per-token, per-kv-head scales (tensor-core consumer only).
 bool find_token_scale_kernel_bf16_e4m3(int head_dim, int group, DecodeKernel* k);
 bool find_token_scale_kernel_f16_e4m3(int head_dim, int group, DecodeKernel* k);

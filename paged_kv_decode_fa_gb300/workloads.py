@@ -211,10 +211,13 @@ def make_batch(*, batch_lengths, num_qo_heads: int, num_kv_heads: int, head_dim:
 
 def make_cascade_batch(*, prefix_pages: int, suffix_lengths, num_qo_heads: int,
                        num_kv_heads: int, head_dim: int, dtype: torch.dtype, seed: int,
-                       device="cuda", page_size: int = PAGE_SIZE, name="cascade") -> DecodeBatch:
+                       device="cuda", page_size: int = PAGE_SIZE, name="cascade",
+                       kv_dtype: torch.dtype | None = None) -> DecodeBatch:
     """Requests sharing `prefix_pages` full pages, each followed by its own
     suffix of the given length.  The page table lists every full sequence
-    (shared page ids first); extra["prefix_pages"] is the shared count."""
+    (shared page ids first); extra["prefix_pages"] is the shared count.
+    kv_dtype (default: dtype) may be E4M3, quantised with one scale per half
+    as make_batch does."""
     gen = torch.Generator().manual_seed(seed)
     suffix_lengths = np.asarray(suffix_lengths, dtype=np.int64)
     sfx_pages = (suffix_lengths + page_size - 1) // page_size
@@ -234,13 +237,26 @@ def make_cascade_batch(*, prefix_pages: int, suffix_lengths, num_qo_heads: int,
     vgen = torch.Generator(device=dev).manual_seed(seed)
     B = len(suffix_lengths)
     q = torch.randn((B, num_qo_heads, head_dim), generator=vgen, device=dev).to(dtype)
-    kv = torch.randn((pool, 2, page_size, num_kv_heads, head_dim), generator=vgen, device=dev,
-                     dtype=dtype)
+    kv_dtype = dtype if kv_dtype is None else kv_dtype
+    k_scale = v_scale = 1.0
+    if kv_dtype == torch.float8_e4m3fn:
+        kv = torch.empty((pool, 2, page_size, num_kv_heads, head_dim), dtype=kv_dtype, device=dev)
+        scales = []
+        for half in range(2):
+            x = torch.randn((pool, page_size, num_kv_heads, head_dim), generator=vgen,
+                            device=dev, dtype=torch.float32)
+            codes, s = _fp8_quantise(x)
+            kv[:, half] = codes
+            scales.append(s)
+        k_scale, v_scale = scales
+    else:
+        kv = torch.randn((pool, 2, page_size, num_kv_heads, head_dim), generator=vgen,
+                         device=dev, dtype=kv_dtype)
     return DecodeBatch(q=q, paged_kv=kv, indptr=torch.tensor(indptr, dtype=torch.int32),
                        indices=torch.from_numpy(np.concatenate(ids).astype(np.int32)).to(dev),
                        last_page_len=torch.tensor(last, dtype=torch.int32), lengths=lengths,
                        num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
-                       page_size=page_size, name=name,
+                       page_size=page_size, k_scale=k_scale, v_scale=v_scale, name=name,
                        extra={"prefix_pages": prefix_pages})
 
 

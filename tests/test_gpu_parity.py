@@ -620,8 +620,8 @@ def test_multi_token_rejects(lib, cuda):
 def run_cascade(lib, b):
     pre, ip, idx, last = W.cascade_parts(b)
     p = lib.cascade_plan(pre, ip, idx, last, b.num_qo_heads, b.num_kv_heads, b.head_dim,
-                         b.page_size, q_data_type=b.q.dtype)
-    o, lse = p.run(b.q, b.paged_kv)
+                         b.page_size, q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype)
+    o, lse = p.run(b.q, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale)
     torch.cuda.synchronize()
     return p, o, lse
 
@@ -654,6 +654,45 @@ def test_cascade_small(lib, cuda, monkeypatch, kernel, dtype, batch, hq, hkv, pr
     assert p.check() == 0
     ref_o, ref_lse = oracle_decode(b)
     compare(o, lse, ref_o, ref_lse, TOL[dtype])
+
+
+@pytest.mark.parametrize("kernel", ["tcgen05", "mma"])
+@pytest.mark.parametrize("q_dtype,kv_dtype,head_dim", [
+    (torch.bfloat16, torch.float8_e4m3fn, 128),
+    (torch.float16, torch.float8_e4m3fn, 128),
+    (torch.bfloat16, torch.bfloat16, 64),
+    (torch.float16, torch.float16, 64),
+], ids=["bf16-e4m3-d128", "f16-e4m3-d128", "bf16-d64", "f16-d64"])
+@pytest.mark.parametrize("batch,hq,hkv,prefix_pages", [
+    (6, 8, 2, 5),
+    (40, 16, 4, 9),
+    (20, 32, 4, 70),
+])
+def test_cascade_kv_dtypes(lib, cuda, monkeypatch, kernel, q_dtype, kv_dtype, head_dim, batch,
+                           hq, hkv, prefix_pages):
+    """Cascade over an E4M3 cache (per-tensor k/v scales) and at head_dim 64.
+    The prefix pass of these runs on the mma.sync kernel whichever kernel is
+    asked for (the tcgen05 one takes 16-bit D=128 only), so both settings
+    must give the same bits; each is checked against the oracle's attention
+    over the full page lists."""
+    if kernel == "mma":
+        monkeypatch.setenv("FADECODE_CASCADE", "mma")
+    else:
+        monkeypatch.delenv("FADECODE_CASCADE", raising=False)
+    rng = np.random.default_rng(batch * 3 + prefix_pages)
+    sfx = rng.integers(0, 200, size=batch)
+    sfx[0] = 0
+    sfx[-1] = 16
+    b = W.make_cascade_batch(prefix_pages=prefix_pages, suffix_lengths=sfx, num_qo_heads=hq,
+                             num_kv_heads=hkv, head_dim=head_dim, dtype=q_dtype,
+                             kv_dtype=kv_dtype, seed=90 + batch, device=cuda)
+    p, o, lse = run_cascade(lib, b)
+    assert p.check() == 0
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, tol_for(b))
+    with pytest.raises(TypeError):      # the plan's KV dtype is checked on every run
+        other = torch.float16 if kv_dtype != torch.float16 else torch.bfloat16
+        p.run(b.q, b.paged_kv.view(torch.uint8).to(other))
 
 
 def test_cascade_overlap_graph_and_timing(lib, cuda, monkeypatch):
@@ -736,8 +775,12 @@ def test_cascade_many_plans(lib, cuda):
 def test_cascade_rejects(lib, cuda):
     idx = torch.zeros(1, dtype=torch.int32, device=cuda)
     with pytest.raises(lib.FaError) as e:
-        lib.cascade_plan(idx, [0, 0], idx, [16], 8, 8, 64, 16, q_data_type=torch.bfloat16)
-    assert e.value.status == -2          # head_dim 64 not built
+        lib.cascade_plan(idx, [0, 0], idx, [16], 8, 8, 256, 16, q_data_type=torch.bfloat16)
+    assert e.value.status == -2          # head_dim 256 not built
+    with pytest.raises(lib.FaError) as e:
+        lib.cascade_plan(idx, [0, 0], idx, [16], 8, 8, 64, 16, q_data_type=torch.bfloat16,
+                         kv_data_type=torch.float8_e4m3fn)
+    assert e.value.status == -2          # E4M3 at head_dim 64 not built
     with pytest.raises(lib.FaError) as e:
         lib.cascade_plan(idx, [0, 0], idx, [16], 8, 8, 128, 16, q_data_type=torch.float32)
     assert e.value.status == -2
@@ -756,7 +799,7 @@ def run_um(lib, b, bound):
     p = lib.plan(b.indptr, b.indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                  b.head_dim, b.page_size, q_data_type=b.q.dtype, kv_data_type=b.paged_kv.dtype)
     p.unified_max_fallbacks()          # start the count from zero
-    o, lse = p.run_unified_max(b.q, b.paged_kv, bound)
+    o, lse = p.run_unified_max(b.q, b.paged_kv, bound, k_scale=b.k_scale, v_scale=b.v_scale)
     torch.cuda.synchronize()
     return p, o, lse, p.unified_max_fallbacks()
 
@@ -810,6 +853,32 @@ def test_unified_max_small(lib, cuda, head_dim, group, where):
     compare(o, lse, ref_o, ref_lse, TOL[torch.bfloat16])
 
 
+@pytest.mark.parametrize("q_dtype,kv_dtype", [(torch.float16, torch.float16),
+                                              (torch.bfloat16, torch.float8_e4m3fn),
+                                              (torch.float16, torch.float8_e4m3fn)],
+                         ids=["f16", "bf16-e4m3", "f16-e4m3"])
+@pytest.mark.parametrize("group", [2, 4, 8])
+@pytest.mark.parametrize("where", ["cauchy_schwarz", "top", "far_above", "far_below"])
+def test_unified_max_f16_weights(lib, cuda, q_dtype, kv_dtype, group, where):
+    """Unified max with f16 weights (f16 or E4M3 KV): window [bound - 8,
+    bound + 15] in log2 units.  The oracle's result for any bound; far from
+    the logits the exact re-centring runs."""
+    Hkv = 2
+    lengths = [1, 0, 16, 17, 250, 1000, 33, 611]
+    b = W.make_batch(batch_lengths=lengths, num_qo_heads=Hkv * group, num_kv_heads=Hkv,
+                     head_dim=128, q_dtype=q_dtype, kv_dtype=kv_dtype, seed=110 + group,
+                     device=cuda, pool_pages=200)
+    top = np.max(max_logits(b)) * b.k_scale
+    bound = {"cauchy_schwarz": W.cauchy_schwarz_bound(b), "top": top,
+             "far_above": top + 30.0, "far_below": top - 30.0}[where]
+    p, o, lse, n = run_um(lib, b, bound)
+    assert p.info["unified_max"] == 1 and p.check() == 0
+    if where.startswith("far"):
+        assert n > 0, "a bound outside the window must take the fallback"
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, tol_for(b))
+
+
 def test_unified_max_many_splits(lib, cuda):
     """A long request split over the grid: partial states of one head carry
     different references (some pieces re-centred, some not) and still merge
@@ -840,10 +909,9 @@ def test_unified_max_rejects(lib, cuda):
         with pytest.raises(lib.FaError) as e:
             p.run_unified_max(b.q, b.paged_kv, bad)
         assert e.value.status == -1
-    # f16 weights, E4M3 KV, group 1 and multi-token plans have no unified-max kernel
-    for q_dt, kv_dt, hq in [(torch.float16, torch.float16, 8),
-                            (torch.bfloat16, torch.float8_e4m3fn, 8),
-                            (torch.bfloat16, torch.bfloat16, 2),
+    # group 1, fp32 and multi-token plans have no unified-max kernel
+    for q_dt, kv_dt, hq in [(torch.bfloat16, torch.bfloat16, 2),
+                            (torch.float16, torch.float8_e4m3fn, 2),
                             (torch.float32, torch.float32, 8)]:
         bb = W.make_batch(batch_lengths=[40, 3], num_qo_heads=hq, num_kv_heads=2,
                           head_dim=128, q_dtype=q_dt, kv_dtype=kv_dt, seed=2, device=cuda)
