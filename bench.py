@@ -154,17 +154,20 @@ class ClockSampler:
             return None
         reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
             getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
-        mhz, mx, mask = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        mhz, mx, mem, mask = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
 
         def read():
+            # clock types: 1 = SM, 2 = memory
             if (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) != 0 or
                     lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) != 0 or
                     reasons(h, ctypes.byref(mask)) != 0):
                 return None
+            mem_mhz = str(mem.value) if lib.nvmlDeviceGetClockInfo(h, 2, ctypes.byref(mem)) == 0 \
+                else ""
             flags = ["Active" if mask.value & b else "Not Active" for b in
                      (self._BITS["hw_slowdown"], self._BITS["hw_thermal_slowdown"],
                       self._BITS["sw_thermal_slowdown"], self._BITS["sw_power_cap"])]
-            return ", ".join([str(self.gpu), str(mhz.value), str(mx.value), "", ""] + flags)
+            return ", ".join([str(self.gpu), str(mhz.value), str(mx.value), "", mem_mhz] + flags)
         return read if read() is not None else None
 
     def start(self):
@@ -219,9 +222,14 @@ class ClockSampler:
             if len(parts) < 9:
                 continue
             try:
-                rows.append((t, float(parts[1]), float(parts[2]), parts[5:9]))
+                row = (t, float(parts[1]), float(parts[2]), parts[5:9])
             except ValueError:
                 continue
+            try:  # memory clock (NVML samples only)
+                row += (float(parts[4]),)
+            except ValueError:
+                pass
+            rows.append(row)
         # samples inside the region (nvidia-smi's 50 ms stream: within one
         # interval of it)
         margin = 0.005 if self.source and self.source.startswith("nvml") else 0.05
@@ -234,9 +242,13 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in window for i, v in enumerate(r[3])
                           if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[1] for r in window),
-                "sm_max_mhz": max(r[2] for r in window), "reasons": reasons,
-                "samples": len(window), "window": which, "source": self.source}
+        out = {"sm_mhz": statistics.median(r[1] for r in window),
+               "sm_max_mhz": max(r[2] for r in window), "reasons": reasons,
+               "samples": len(window), "window": which, "source": self.source}
+        mem = [r[4] for r in window if len(r) > 4]
+        if mem:
+            out["mem_mhz"] = statistics.median(mem)
+        return out
 
 
 def dist_setup(n_gpus: int):
@@ -544,7 +556,7 @@ def step_fn(name: str, b: W.DecodeBatch, um_bound):
 
 # Decode workloads measured beside the headline one, in the same run.
 OTHER_WORKLOADS = ("tiny", "gqa_uniform", "long_split", "fp8_kv", "fp8_kv_token_scales",
-                   "spec_decode", "spec_decode_ragged", "gqa_unified_max")
+                   "spec_decode", "spec_decode_ragged", "gqa_unified_max", "cascade")
 
 
 def measure_other(args, world, dev, name: str) -> dict:
@@ -556,6 +568,15 @@ def measure_other(args, world, dev, name: str) -> dict:
     import paged_kv_decode_fa_gb300 as fa
     cfg = W.CONFIGS[name]
     b = W.make_config_batch(name, device=dev)
+    if name == "cascade":
+        sub = argparse.Namespace(**dict(vars(args), steps=steps, warmup=warmup))
+        r = bench_cascade(sub, world, 0, dev.index, b, cfg, dev)
+        keep = ("config", "value", "unit", "ms_per_step", "hbm_gbs", "hbm_frac_of_peak",
+                "serial_ms_per_step", "plain_decode_ms_per_step", "speedup_vs_plain_decode",
+                "roofline", "e2e", "steps", "warmup", "gpu_launches", "clocks")
+        del b
+        torch.cuda.empty_cache()
+        return {k: r[k] for k in keep}
     stream = torch.cuda.current_stream(dev)
     p = plan_batch(fa, b)
     info = p.info
@@ -570,13 +591,18 @@ def measure_other(args, world, dev, name: str) -> dict:
         raise RuntimeError(f"device check flagged the {name} batch")
     launches = 1 + (1 if info["num_merge_units"] > 0 and not info["fused_merge"] else 0)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index).start()
+    time.sleep(0.05)
     barrier(world)
     torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
     start.record(stream)
     for _ in range(steps):
         run_step(p, b.q, o, lse)
     end.record(stream)
     torch.cuda.synchronize(dev)
+    t1 = time.perf_counter()
+    clocks.stop()
     elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, world, dev)
     step_s = elapsed_s / steps
     alg = algorithmic_bytes(b)
@@ -596,6 +622,7 @@ def measure_other(args, world, dev, name: str) -> dict:
                      "duration_from": ("timed-region events / launches" if launches == 1 else
                                        "timed-region events / steps (decode + merge kernel)")},
         "steps": steps, "warmup": warmup, "gpu_launches": steps * launches,
+        "clocks": clocks.summary(t0, t1),
     }
     if um_bound is not None:
         res["unified_max"] = {"bound": um_bound, "fallbacks": p.unified_max_fallbacks()}

@@ -29,6 +29,8 @@
 //    stage with ldmatrix.trans (for E4M3, pairs of bytes are transposed as
 //    16-bit elements and split with one byte permute).
 #pragma once
+#include <type_traits>
+
 #include "decode_kernel.cuh"
 
 namespace fadecode {
@@ -377,6 +379,10 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
     float tmx[2] = {-INFINITY, -INFINITY};  // this lane's running maxima of the columns
     bool um_first = true, um_moved = false;
     if constexpr (UM) m_h[0] = m_h[1] = p.max_bound;
+    // the reference the weights are taken against: m_h, or 0 for a column
+    // that has seen nothing yet (every token so far masked), whose weights
+    // exp2(-inf - 0) = 0 keep its state empty; it changes only on a rescale
+    float mref[2] = {0.f, 0.f};
 
     // page split: page k to warp k % NW; column split: every page to every warp
     for (int k = CS ? kbase : kbase + (warp - kbase % NW + NW) % NW; k < kbase + npg;
@@ -437,8 +443,10 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
         s[2] *= ks_hi;
         s[3] *= ks_hi;
       }
-      if (g >= valid) s[0] = s[1] = -INFINITY;
-      if (g + 8 >= valid) s[2] = s[3] = -INFINITY;
+      if (valid < P) {
+        if (g >= valid) s[0] = s[1] = -INFINITY;
+        if (g + 8 >= valid) s[2] = s[3] = -INFINITY;
+      }
       if constexpr (kCausal) {
         const int pos = lp * P + g;  // token position from the segment start
         if (pos > lim[0]) s[0] = -INFINITY;
@@ -457,7 +465,7 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
       // inside).  Otherwise it starts empty and takes the column's first
       // observed maximum.  A column leaving its window is re-centred on its
       // true maximum (an exact rescale of its state).
-      float alpha[2] = {1.f, 1.f}, pr[4], mref[2];
+      float alpha[2] = {1.f, 1.f}, pr[4];
       bool rescale;
       {
         constexpr float kAbove = UM ? kUmAbove : kLazyAbove;
@@ -486,12 +494,9 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
               m_h[e] = mx[e];
               um_moved = true;
             }
+            mref[e] = m_h[e] == -INFINITY ? 0.f : m_h[e];
           }
         }
-        // a column that has seen nothing yet (every token so far masked):
-        // weights exp2(-inf - 0) = 0 keep its state empty
-        mref[0] = m_h[0] == -INFINITY ? 0.f : m_h[0];
-        mref[1] = m_h[1] == -INFINITY ? 0.f : m_h[1];
       }
       const uint32_t p01 = mma::pack2(dev::fast_exp2(s[0] - mref[0]),
                                       dev::fast_exp2(s[1] - mref[1]), kBf16);
@@ -524,60 +529,74 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
           o[mt][3] *= alpha[1];
         }
       }
-      // Slots past the last valid token may hold anything (NaN included): a
-      // zero weight would not cancel them in the MMA, so their V elements
-      // are cleared in the A fragments below, in registers.  The stage itself
-      // is never written by the consumers: it belongs to the copy engine,
-      // which refills it for a later page as soon as this warp releases it.
-      // Each fragment register holds two consecutive tokens (low half 2t,
-      // high half 2t+1; +8 for the upper token block).
-      const uint32_t vmask_lo = (2 * t < valid ? 0x0000ffffu : 0u) |
-                                (2 * t + 1 < valid ? 0xffff0000u : 0u);
-      const uint32_t vmask_hi = (2 * t + 8 < valid ? 0x0000ffffu : 0u) |
-                                (2 * t + 9 < valid ? 0xffff0000u : 0u);
       __syncwarp();
       const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pT + g * P + 2 * t);
       const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(pT + g * P + 2 * t + 8);
 
       // ---- O^T[dim][head] += V^T . P^T
-      if constexpr (kFp8) {
-#pragma unroll
-        for (int c2 = 0; c2 < MTILES / 2; ++c2) {
-          const int mi = lane >> 3, r = lane & 7;
-          const int gran = 2 * c2 + (mi >> 1), tok = (mi & 1) * 8 + r;
-          uint32_t d0, d1, d2, d3;
-          mma::ldsm_x4_trans(st + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16), d0, d1, d2, d3);
-          // matrices 0 and 2 hold tokens 2t, 2t+1; 1 and 3 tokens 2t+8, 2t+9
-          d0 &= vmask_lo;
-          d2 &= vmask_lo;
-          d1 &= vmask_hi;
-          d3 &= vmask_hi;
-          uint32_t a[4][2];
-          mma::e4m3x4_to_f16x2x2(__byte_perm(d0, 0u, 0x3120), a[0][0], a[0][1]);
-          mma::e4m3x4_to_f16x2x2(__byte_perm(d1, 0u, 0x3120), a[1][0], a[1][1]);
-          mma::e4m3x4_to_f16x2x2(__byte_perm(d2, 0u, 0x3120), a[2][0], a[2][1]);
-          mma::e4m3x4_to_f16x2x2(__byte_perm(d3, 0u, 0x3120), a[3][0], a[3][1]);
-          mma::mma16816<false>(o[2 * c2], a[0][0], a[0][1], a[1][0], a[1][1], pb0, pb1);
-          mma::mma16816<false>(o[2 * c2 + 1], a[2][0], a[2][1], a[3][0], a[3][1], pb0, pb1);
+      // Slots past the last valid token may hold anything (NaN included): a
+      // zero weight would not cancel them in the MMA, so on a segment's
+      // partial last page their V elements are cleared in the A fragments,
+      // in registers (a full page takes the same step without the masks).
+      // The stage itself is never written by the consumers: it belongs to
+      // the copy engine, which refills it for a later page as soon as this
+      // warp releases it.  Each fragment register holds two consecutive
+      // tokens (low half 2t, high half 2t+1; +8 for the upper token block).
+      auto pv_step = [&](auto masked) {
+        constexpr bool kMask = decltype(masked)::value;
+        uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
+        if constexpr (kMask) {
+          vmask_lo = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
+          vmask_hi = (2 * t + 8 < valid ? 0x0000ffffu : 0u) | (2 * t + 9 < valid ? 0xffff0000u : 0u);
         }
-      } else {
+        if constexpr (kFp8) {
 #pragma unroll
-        for (int mt = 0; mt < MTILES; ++mt) {
-          const int mi = lane >> 3, r = lane & 7;
-          const int sgi = (mt * 16) / C::BOX_X;
-          const int gran = ((mt * 16) % C::BOX_X) / 8 + (mi & 1);
-          const int tok = (mi >> 1) * 8 + r;
-          uint32_t a0, a1, a2, a3;
-          mma::ldsm_x4_trans(st + sgi * C::BOX_BYTES + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16),
-                             a0, a1, a2, a3);
-          // matrices 0 and 1 hold tokens 2t, 2t+1; 2 and 3 tokens 2t+8, 2t+9
-          a0 &= vmask_lo;
-          a1 &= vmask_lo;
-          a2 &= vmask_hi;
-          a3 &= vmask_hi;
-          mma::mma16816<kBf16>(o[mt], a0, a1, a2, a3, pb0, pb1);
+          for (int c2 = 0; c2 < MTILES / 2; ++c2) {
+            const int mi = lane >> 3, r = lane & 7;
+            const int gran = 2 * c2 + (mi >> 1), tok = (mi & 1) * 8 + r;
+            uint32_t d0, d1, d2, d3;
+            mma::ldsm_x4_trans(st + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16), d0, d1, d2, d3);
+            // matrices 0 and 2 hold tokens 2t, 2t+1; 1 and 3 tokens 2t+8, 2t+9
+            if constexpr (kMask) {
+              d0 &= vmask_lo;
+              d2 &= vmask_lo;
+              d1 &= vmask_hi;
+              d3 &= vmask_hi;
+            }
+            uint32_t a[4][2];
+            mma::e4m3x4_to_f16x2x2(__byte_perm(d0, 0u, 0x3120), a[0][0], a[0][1]);
+            mma::e4m3x4_to_f16x2x2(__byte_perm(d1, 0u, 0x3120), a[1][0], a[1][1]);
+            mma::e4m3x4_to_f16x2x2(__byte_perm(d2, 0u, 0x3120), a[2][0], a[2][1]);
+            mma::e4m3x4_to_f16x2x2(__byte_perm(d3, 0u, 0x3120), a[3][0], a[3][1]);
+            mma::mma16816<false>(o[2 * c2], a[0][0], a[0][1], a[1][0], a[1][1], pb0, pb1);
+            mma::mma16816<false>(o[2 * c2 + 1], a[2][0], a[2][1], a[3][0], a[3][1], pb0, pb1);
+          }
+        } else {
+#pragma unroll
+          for (int mt = 0; mt < MTILES; ++mt) {
+            const int mi = lane >> 3, r = lane & 7;
+            const int sgi = (mt * 16) / C::BOX_X;
+            const int gran = ((mt * 16) % C::BOX_X) / 8 + (mi & 1);
+            const int tok = (mi >> 1) * 8 + r;
+            uint32_t a0, a1, a2, a3;
+            mma::ldsm_x4_trans(
+                st + sgi * C::BOX_BYTES + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16), a0, a1,
+                a2, a3);
+            // matrices 0 and 1 hold tokens 2t, 2t+1; 2 and 3 tokens 2t+8, 2t+9
+            if constexpr (kMask) {
+              a0 &= vmask_lo;
+              a1 &= vmask_lo;
+              a2 &= vmask_hi;
+              a3 &= vmask_hi;
+            }
+            mma::mma16816<kBf16>(o[mt], a0, a1, a2, a3, pb0, pb1);
+          }
         }
-      }
+      };
+      if (valid < P)
+        pv_step(std::true_type{});
+      else
+        pv_step(std::false_type{});
       dev::release_stage(dev::smem_addr(&empty[stage]), lane);
     }
 
