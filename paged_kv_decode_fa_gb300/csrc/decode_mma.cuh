@@ -129,6 +129,9 @@ struct MmaCfg {
   // columns the warps split the pages instead (page k to warp k % NW).
   static constexpr bool CS = NC > 8;
   static constexpr int NS = CS ? 1 : NW;  // partial states per column at a segment's end
+  // pages a consumer warp takes per step: two for the column split (every
+  // warp takes every page), one for the page split
+  static constexpr int NPP = CS ? 2 : 1;
   static constexpr int P = kPageSize;
   static constexpr int KV_ES = sizeof(KVT);
   static constexpr bool kFp8 = KV_ES == 1;
@@ -146,19 +149,20 @@ struct MmaCfg {
   // G = 8, whose larger epilogue buffer would otherwise leave room for only
   // two CTAs per SM), three CTAs per SM.  E4M3 KV: 32 KB (two 4 KB pages per
   // warp) so that four CTAs fit per SM - its denser per-byte arithmetic needs
-  // the extra warps to hide each page's dependent chain.
-  static constexpr int RING_BYTES = KV_ES == 1 ? 32768 : (NC >= 8 ? 49152 : 65536);
+  // the extra warps to hide each page's dependent chain; the E4M3 column
+  // split (two pages a warp step) 48 KB at three CTAs per SM.
+  static constexpr int RING_BYTES = KV_ES == 1 ? (CS ? 49152 : 32768) : (NC >= 8 ? 49152 : 65536);
   static constexpr int SPW0 = RING_BYTES / STAGE_BYTES / NW;
   static constexpr int SPW = SPW0 < 1 ? 1 : (SPW0 > 4 ? 4 : SPW0);
   // column split: every warp reads every stage, any number of stages works
   static constexpr int S = CS ? RING_BYTES / STAGE_BYTES : SPW * NW;
   static constexpr int THREADS = (NW + 1) * 32;
   // CTAs per SM the ring size is chosen for; the register budget must allow it
-  static constexpr int MIN_CTAS = KV_ES == 1 ? 4 : 3;
+  static constexpr int MIN_CTAS = KV_ES == 1 && !CS ? 4 : 3;
   static constexpr int OFF_FULL = S * STAGE_BYTES;
   static constexpr int OFF_EMPTY = OFF_FULL + 8 * S;
-  static constexpr int OFF_PT = OFF_EMPTY + 8 * S;          // [NW][8 heads][16 tokens] 16-bit
-  static constexpr int OFF_MO = OFF_PT + NW * 8 * P * 2;
+  static constexpr int OFF_PT = OFF_EMPTY + 8 * S;  // [NW][NPP][8 heads][16 tokens] 16-bit
+  static constexpr int OFF_MO = OFF_PT + NW * NPP * 8 * P * 2;
   static constexpr int OFF_MM = OFF_MO + 4 * NS * NC * D;
   static constexpr int OFF_MD = OFF_MM + 4 * NS * NC;
   static constexpr int OFF_FOLDS = OFF_MD + 4 * NS * NC;
@@ -258,7 +262,7 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
     return;
   }
 
-  uint16_t* pT = reinterpret_cast<uint16_t*>(smem + C::OFF_PT) + warp * 8 * P;
+  uint16_t* pT = reinterpret_cast<uint16_t*>(smem + C::OFF_PT) + warp * C::NPP * 8 * P;
   float* mo = reinterpret_cast<float*>(smem + C::OFF_MO);
   float* mm = reinterpret_cast<float*>(smem + C::OFF_MM);
   float* md = reinterpret_cast<float*>(smem + C::OFF_MD);
@@ -384,93 +388,173 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
     // exp2(-inf - 0) = 0 keep its state empty; it changes only on a rescale
     float mref[2] = {0.f, 0.f};
 
-    // page split: page k to warp k % NW; column split: every page to every warp
-    for (int k = CS ? kbase : kbase + (warp - kbase % NW + NW) % NW; k < kbase + npg;
-         k += CS ? 1 : NW) {
-      const int lp = k - kbase;
-      const int stage = k % S;
-      dev::mbar_wait(dev::smem_addr(&full[stage]), (uint32_t)((k / S) & 1), aborted, p.err);
-      if (CS && !active) {  // nothing to compute: release the stage
-        __syncwarp();
-        if (lane == 0) dev::mbar_arrive(dev::smem_addr(&empty[stage]));
-        continue;
+    // ---- O^T[dim][head] += V^T . P^T for one page (stage address st).
+    // Slots past the last valid token may hold anything (NaN included): a
+    // zero weight would not cancel them in the MMA, so on a segment's
+    // partial last page their V elements are cleared in the A fragments,
+    // in registers (a full page takes the same step without the masks).
+    // The stage itself is never written by the consumers: it belongs to
+    // the copy engine, which refills it for a later page as soon as this
+    // warp releases it.  Each fragment register holds two consecutive
+    // tokens (low half 2t, high half 2t+1; +8 for the upper token block).
+    auto pv_step = [&](auto masked, uint32_t st, uint32_t pb0, uint32_t pb1, int valid) {
+      constexpr bool kMask = decltype(masked)::value;
+      uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
+      if constexpr (kMask) {
+        vmask_lo = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
+        vmask_hi = (2 * t + 8 < valid ? 0x0000ffffu : 0u) | (2 * t + 9 < valid ? 0xffff0000u : 0u);
       }
-      const uint32_t st = ring_addr + stage * C::STAGE_BYTES;
-      const int valid = (lp == npg - 1) ? last_valid : P;
+      if constexpr (kFp8) {
+#pragma unroll
+        for (int c2 = 0; c2 < MTILES / 2; ++c2) {
+          const int mi = lane >> 3, r = lane & 7;
+          const int gran = 2 * c2 + (mi >> 1), tok = (mi & 1) * 8 + r;
+          uint32_t d0, d1, d2, d3;
+          mma::ldsm_x4_trans(st + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16), d0, d1, d2, d3);
+          // matrices 0 and 2 hold tokens 2t, 2t+1; 1 and 3 tokens 2t+8, 2t+9
+          if constexpr (kMask) {
+            d0 &= vmask_lo;
+            d2 &= vmask_lo;
+            d1 &= vmask_hi;
+            d3 &= vmask_hi;
+          }
+          uint32_t a[4][2];
+          mma::e4m3x4_to_f16x2x2(__byte_perm(d0, 0u, 0x3120), a[0][0], a[0][1]);
+          mma::e4m3x4_to_f16x2x2(__byte_perm(d1, 0u, 0x3120), a[1][0], a[1][1]);
+          mma::e4m3x4_to_f16x2x2(__byte_perm(d2, 0u, 0x3120), a[2][0], a[2][1]);
+          mma::e4m3x4_to_f16x2x2(__byte_perm(d3, 0u, 0x3120), a[3][0], a[3][1]);
+          mma::mma16816<false>(o[2 * c2], a[0][0], a[0][1], a[1][0], a[1][1], pb0, pb1);
+          mma::mma16816<false>(o[2 * c2 + 1], a[2][0], a[2][1], a[3][0], a[3][1], pb0, pb1);
+        }
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < MTILES; ++mt) {
+          const int mi = lane >> 3, r = lane & 7;
+          const int sgi = (mt * 16) / C::BOX_X;
+          const int gran = ((mt * 16) % C::BOX_X) / 8 + (mi & 1);
+          const int tok = (mi >> 1) * 8 + r;
+          uint32_t a0, a1, a2, a3;
+          mma::ldsm_x4_trans(
+              st + sgi * C::BOX_BYTES + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16), a0, a1,
+              a2, a3);
+          // matrices 0 and 1 hold tokens 2t, 2t+1; 2 and 3 tokens 2t+8, 2t+9
+          if constexpr (kMask) {
+            a0 &= vmask_lo;
+            a1 &= vmask_lo;
+            a2 &= vmask_hi;
+            a3 &= vmask_hi;
+          }
+          mma::mma16816<kBf16>(o[mt], a0, a1, a2, a3, pb0, pb1);
+        }
+      }
+    };
 
-      // ---- scores S^T[token][head] = K . q^T (two accumulators to halve the chain)
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // One step over NPP consecutive pages k .. k + NPP - 1 of the segment:
+    // scores, one softmax update over all of them, P.V.  Two pages a step
+    // (the column split) keep two pages' independent loads and MMA chains
+    // in flight in the warp at once.
+    auto step = [&](auto npp_tag, int k) {
+      constexpr int NPP = decltype(npp_tag)::value;
+      int stage[NPP], lp[NPP], valid[NPP];
+      uint32_t st[NPP];
+#pragma unroll
+      for (int u = 0; u < NPP; ++u) {
+        lp[u] = k + u - kbase;
+        stage[u] = (k + u) % S;
+        dev::mbar_wait(dev::smem_addr(&full[stage[u]]), (uint32_t)(((k + u) / S) & 1), aborted,
+                       p.err);
+        st[u] = ring_addr + stage[u] * C::STAGE_BYTES;
+        valid[u] = (lp[u] == npg - 1) ? last_valid : P;
+      }
+      if (CS && !active) {  // nothing to compute: release the stages
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int u = 0; u < NPP; ++u) dev::mbar_arrive(dev::smem_addr(&empty[stage[u]]));
+        }
+        return;
+      }
+
+      // ---- scores S^T[token][head] = K . q^T (two accumulators a page to halve the chain)
+      float s[NPP][4], vs_lo[NPP], vs_hi[NPP];  // vs: per-token V scales of tokens g, g+8
       const int sw = g & 7;  // swizzle of rows g and g+8
 #pragma unroll
-      for (int sgi = 0; sgi < SEGS; ++sgi) {
+      for (int u = 0; u < NPP; ++u) {
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          const uint32_t gran = (uint32_t)(((2 * t + qq) ^ sw) * 16);
-          const uint4 ka = mma::lds128(st + sgi * C::BOX_BYTES + g * 128 + gran);
-          const uint4 kb = mma::lds128(st + sgi * C::BOX_BYTES + (g + 8) * 128 + gran);
-          const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w};
-          const uint32_t wb[4] = {kb.x, kb.y, kb.z, kb.w};
-          if constexpr (kFp8) {
+        for (int sgi = 0; sgi < SEGS; ++sgi) {
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const int j = qq * 4 + w;
-              uint32_t a0, a1, a2, a3;
-              mma::e4m3x4_to_f16x2x2(wa[w], a0, a2);
-              mma::e4m3x4_to_f16x2x2(wb[w], a1, a3);
-              mma::mma16816<false>(sc[j & 1], a0, a1, a2, a3, qb[j][0], qb[j][1]);
-            }
-          } else {
+          for (int qq = 0; qq < 2; ++qq) {
+            const uint32_t gran = (uint32_t)(((2 * t + qq) ^ sw) * 16);
+            const uint4 ka = mma::lds128(st[u] + sgi * C::BOX_BYTES + g * 128 + gran);
+            const uint4 kb = mma::lds128(st[u] + sgi * C::BOX_BYTES + (g + 8) * 128 + gran);
+            const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w};
+            const uint32_t wb[4] = {kb.x, kb.y, kb.z, kb.w};
+            if constexpr (kFp8) {
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int j = sgi * 4 + qq * 2 + u;
-              mma::mma16816<kBf16>(sc[j & 1], wa[2 * u], wb[2 * u], wa[2 * u + 1],
-                                   wb[2 * u + 1], qb[j][0], qb[j][1]);
+              for (int w = 0; w < 4; ++w) {
+                const int j = qq * 4 + w;
+                uint32_t a0, a1, a2, a3;
+                mma::e4m3x4_to_f16x2x2(wa[w], a0, a2);
+                mma::e4m3x4_to_f16x2x2(wb[w], a1, a3);
+                mma::mma16816<false>(sc[j & 1], a0, a1, a2, a3, qb[j][0], qb[j][1]);
+              }
+            } else {
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const int j = sgi * 4 + qq * 2 + h2;
+                mma::mma16816<kBf16>(sc[j & 1], wa[2 * h2], wb[2 * h2], wa[2 * h2 + 1],
+                                     wb[2 * h2 + 1], qb[j][0], qb[j][1]);
+              }
             }
           }
         }
-      }
-      float s[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[e] = (sc[0][e] + sc[1][e]) * qscale;
-      float vs_lo = 1.f, vs_hi = 1.f;  // per-token V scales of tokens g, g+8
-      if constexpr (TS) {
-        const float* scl = reinterpret_cast<const float*>(smem + C::OFF_SCALES) + stage * 2 * P;
-        const float ks_lo = scl[g], ks_hi = scl[g + 8];
-        vs_lo = scl[P + g];
-        vs_hi = scl[P + g + 8];
-        s[0] *= ks_lo;
-        s[1] *= ks_lo;
-        s[2] *= ks_hi;
-        s[3] *= ks_hi;
-      }
-      if (valid < P) {
-        if (g >= valid) s[0] = s[1] = -INFINITY;
-        if (g + 8 >= valid) s[2] = s[3] = -INFINITY;
-      }
-      if constexpr (kCausal) {
-        const int pos = lp * P + g;  // token position from the segment start
-        if (pos > lim[0]) s[0] = -INFINITY;
-        if (pos > lim[1]) s[1] = -INFINITY;
-        if (pos + 8 > lim[0]) s[2] = -INFINITY;
-        if (pos + 8 > lim[1]) s[3] = -INFINITY;
+        for (int e = 0; e < 4; ++e) s[u][e] = (sc[0][e] + sc[1][e]) * qscale;
+        vs_lo[u] = vs_hi[u] = 1.f;
+        if constexpr (TS) {
+          const float* scl =
+              reinterpret_cast<const float*>(smem + C::OFF_SCALES) + stage[u] * 2 * P;
+          const float ks_lo = scl[g], ks_hi = scl[g + 8];
+          vs_lo[u] = scl[P + g];
+          vs_hi[u] = scl[P + g + 8];
+          s[u][0] *= ks_lo;
+          s[u][1] *= ks_lo;
+          s[u][2] *= ks_hi;
+          s[u][3] *= ks_hi;
+        }
+        if (valid[u] < P) {
+          if (g >= valid[u]) s[u][0] = s[u][1] = -INFINITY;
+          if (g + 8 >= valid[u]) s[u][2] = s[u][3] = -INFINITY;
+        }
+        if constexpr (kCausal) {
+          const int pos = lp[u] * P + g;  // token position from the segment start
+          if (pos > lim[0]) s[u][0] = -INFINITY;
+          if (pos > lim[1]) s[u][1] = -INFINITY;
+          if (pos + 8 > lim[0]) s[u][2] = -INFINITY;
+          if (pos + 8 > lim[1]) s[u][3] = -INFINITY;
+        }
       }
 
-      // ---- softmax for heads 2t (s[0], s[2]) and 2t+1 (s[1], s[3])
+      // ---- softmax for heads 2t (s[.][0], s[.][2]) and 2t+1 (s[.][1], s[.][3])
       // The weights use a reference per column that moves only rarely, so a
-      // page needs no column reduction - only a vote on whether some lane's
+      // step needs no column reduction - only a vote on whether some lane's
       // running maximum rose past the window above the reference.  Unified
       // max (UM): the reference starts at the caller's static bound, and the
-      // first page of a segment also checks the window's lower edge (the
+      // first step of a segment also checks the window's lower edge (the
       // running maximum never falls, so once a column is inside it stays
       // inside).  Otherwise it starts empty and takes the column's first
       // observed maximum.  A column leaving its window is re-centred on its
       // true maximum (an exact rescale of its state).
-      float alpha[2] = {1.f, 1.f}, pr[4];
+      float alpha[2] = {1.f, 1.f};
       bool rescale;
       {
         constexpr float kAbove = UM ? kUmAbove : kLazyAbove;
-        tmx[0] = fmaxf(tmx[0], fmaxf(s[0], s[2]));
-        tmx[1] = fmaxf(tmx[1], fmaxf(s[1], s[3]));
+#pragma unroll
+        for (int u = 0; u < NPP; ++u) {
+          tmx[0] = fmaxf(tmx[0], fmaxf(s[u][0], s[u][2]));
+          tmx[1] = fmaxf(tmx[1], fmaxf(s[u][1], s[u][3]));
+        }
         const bool first = um_first;
         um_first = false;
         rescale = first ||
@@ -487,7 +571,7 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
             const bool outside =
                 mx[e] > m_h[e] + kAbove || (UM && mx[e] < m_h[e] - kUmBelow);
             if (outside && mx[e] != -INFINITY) {
-              // nothing accumulated before the first page (and a lowered
+              // nothing accumulated before the first step (and a lowered
               // reference could make this factor overflow); a column still
               // empty gets 0, which keeps its empty state
               alpha[e] = first ? 1.f : dev::fast_exp2(m_h[e] - mx[e]);
@@ -498,28 +582,34 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
           }
         }
       }
-      const uint32_t p01 = mma::pack2(dev::fast_exp2(s[0] - mref[0]),
-                                      dev::fast_exp2(s[1] - mref[1]), kBf16);
-      const uint32_t p23 = mma::pack2(dev::fast_exp2(s[2] - mref[0]),
-                                      dev::fast_exp2(s[3] - mref[1]), kBf16);
-      {
+#pragma unroll
+      for (int u = 0; u < NPP; ++u) {
+        const uint32_t p01 = mma::pack2(dev::fast_exp2(s[u][0] - mref[0]),
+                                        dev::fast_exp2(s[u][1] - mref[1]), kBf16);
+        const uint32_t p23 = mma::pack2(dev::fast_exp2(s[u][2] - mref[0]),
+                                        dev::fast_exp2(s[u][3] - mref[1]), kBf16);
         // sums from the rounded weights, so numerator and denominator agree
         const float2 a = mma::unpack2(p01, kBf16), b = mma::unpack2(p23, kBf16);
-        pr[0] = a.x; pr[1] = a.y; pr[2] = b.x; pr[3] = b.y;
+        uint32_t pv01 = p01, pv23 = p23;  // weights times the per-token V scale
+        if constexpr (TS) {
+          pv01 = mma::pack2(a.x * vs_lo[u], a.y * vs_lo[u], kBf16);
+          pv23 = mma::pack2(b.x * vs_hi[u], b.y * vs_hi[u], kBf16);
+        }
+        if (u == 0) {
+          d_h[0] = fmaf(d_h[0], alpha[0], a.x + b.x);
+          d_h[1] = fmaf(d_h[1], alpha[1], a.y + b.y);
+        } else {
+          d_h[0] += a.x + b.x;
+          d_h[1] += a.y + b.y;
+        }
+        // P^T B fragments: transpose [token][head] -> [head][token] through smem
+        uint16_t* pu = pT + u * 8 * P;
+        pu[(2 * t) * P + g] = (uint16_t)(pv01 & 0xffffu);
+        pu[(2 * t + 1) * P + g] = (uint16_t)(pv01 >> 16);
+        pu[(2 * t) * P + g + 8] = (uint16_t)(pv23 & 0xffffu);
+        pu[(2 * t + 1) * P + g + 8] = (uint16_t)(pv23 >> 16);
       }
-      uint32_t pv01 = p01, pv23 = p23;  // weights times the per-token V scale
-      if constexpr (TS) {
-        pv01 = mma::pack2(pr[0] * vs_lo, pr[1] * vs_lo, kBf16);
-        pv23 = mma::pack2(pr[2] * vs_hi, pr[3] * vs_hi, kBf16);
-      }
-      d_h[0] = d_h[0] * alpha[0] + (pr[0] + pr[2]);
-      d_h[1] = d_h[1] * alpha[1] + (pr[1] + pr[3]);
-      // P^T B fragments: transpose [token][head] -> [head][token] through smem
-      pT[(2 * t) * P + g] = (uint16_t)(pv01 & 0xffffu);
-      pT[(2 * t + 1) * P + g] = (uint16_t)(pv01 >> 16);
-      pT[(2 * t) * P + g + 8] = (uint16_t)(pv23 & 0xffffu);
-      pT[(2 * t + 1) * P + g + 8] = (uint16_t)(pv23 >> 16);
-      // once the running maxima settle, most pages leave them unchanged
+      // once the running maxima settle, most steps leave them unchanged
       if (rescale && __any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
         for (int mt = 0; mt < MTILES; ++mt) {
@@ -530,74 +620,29 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
         }
       }
       __syncwarp();
-      const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pT + g * P + 2 * t);
-      const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(pT + g * P + 2 * t + 8);
+#pragma unroll
+      for (int u = 0; u < NPP; ++u) {
+        const uint16_t* pu = pT + u * 8 * P;
+        const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pu + g * P + 2 * t);
+        const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(pu + g * P + 2 * t + 8);
+        if (valid[u] < P)
+          pv_step(std::true_type{}, st[u], pb0, pb1, valid[u]);
+        else
+          pv_step(std::false_type{}, st[u], pb0, pb1, valid[u]);
+        dev::release_stage(dev::smem_addr(&empty[stage[u]]), lane);
+      }
+    };
 
-      // ---- O^T[dim][head] += V^T . P^T
-      // Slots past the last valid token may hold anything (NaN included): a
-      // zero weight would not cancel them in the MMA, so on a segment's
-      // partial last page their V elements are cleared in the A fragments,
-      // in registers (a full page takes the same step without the masks).
-      // The stage itself is never written by the consumers: it belongs to
-      // the copy engine, which refills it for a later page as soon as this
-      // warp releases it.  Each fragment register holds two consecutive
-      // tokens (low half 2t, high half 2t+1; +8 for the upper token block).
-      auto pv_step = [&](auto masked) {
-        constexpr bool kMask = decltype(masked)::value;
-        uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
-        if constexpr (kMask) {
-          vmask_lo = (2 * t < valid ? 0x0000ffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
-          vmask_hi = (2 * t + 8 < valid ? 0x0000ffffu : 0u) | (2 * t + 9 < valid ? 0xffff0000u : 0u);
-        }
-        if constexpr (kFp8) {
-#pragma unroll
-          for (int c2 = 0; c2 < MTILES / 2; ++c2) {
-            const int mi = lane >> 3, r = lane & 7;
-            const int gran = 2 * c2 + (mi >> 1), tok = (mi & 1) * 8 + r;
-            uint32_t d0, d1, d2, d3;
-            mma::ldsm_x4_trans(st + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16), d0, d1, d2, d3);
-            // matrices 0 and 2 hold tokens 2t, 2t+1; 1 and 3 tokens 2t+8, 2t+9
-            if constexpr (kMask) {
-              d0 &= vmask_lo;
-              d2 &= vmask_lo;
-              d1 &= vmask_hi;
-              d3 &= vmask_hi;
-            }
-            uint32_t a[4][2];
-            mma::e4m3x4_to_f16x2x2(__byte_perm(d0, 0u, 0x3120), a[0][0], a[0][1]);
-            mma::e4m3x4_to_f16x2x2(__byte_perm(d1, 0u, 0x3120), a[1][0], a[1][1]);
-            mma::e4m3x4_to_f16x2x2(__byte_perm(d2, 0u, 0x3120), a[2][0], a[2][1]);
-            mma::e4m3x4_to_f16x2x2(__byte_perm(d3, 0u, 0x3120), a[3][0], a[3][1]);
-            mma::mma16816<false>(o[2 * c2], a[0][0], a[0][1], a[1][0], a[1][1], pb0, pb1);
-            mma::mma16816<false>(o[2 * c2 + 1], a[2][0], a[2][1], a[3][0], a[3][1], pb0, pb1);
-          }
-        } else {
-#pragma unroll
-          for (int mt = 0; mt < MTILES; ++mt) {
-            const int mi = lane >> 3, r = lane & 7;
-            const int sgi = (mt * 16) / C::BOX_X;
-            const int gran = ((mt * 16) % C::BOX_X) / 8 + (mi & 1);
-            const int tok = (mi >> 1) * 8 + r;
-            uint32_t a0, a1, a2, a3;
-            mma::ldsm_x4_trans(
-                st + sgi * C::BOX_BYTES + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16), a0, a1,
-                a2, a3);
-            // matrices 0 and 1 hold tokens 2t, 2t+1; 2 and 3 tokens 2t+8, 2t+9
-            if constexpr (kMask) {
-              a0 &= vmask_lo;
-              a1 &= vmask_lo;
-              a2 &= vmask_hi;
-              a3 &= vmask_hi;
-            }
-            mma::mma16816<kBf16>(o[mt], a0, a1, a2, a3, pb0, pb1);
-          }
-        }
-      };
-      if (valid < P)
-        pv_step(std::true_type{});
-      else
-        pv_step(std::false_type{});
-      dev::release_stage(dev::smem_addr(&empty[stage]), lane);
+    // page split: page k to warp k % NW, one page a step; column split:
+    // every page to every warp, two pages a step (and a last single page)
+    if constexpr (CS) {
+      int k = kbase;
+      for (; k + C::NPP - 1 < kbase + npg; k += C::NPP)
+        step(std::integral_constant<int, C::NPP>{}, k);
+      for (; k < kbase + npg; ++k) step(std::integral_constant<int, 1>{}, k);
+    } else {
+      for (int k = kbase + (warp - kbase % NW + NW) % NW; k < kbase + npg; k += NW)
+        step(std::integral_constant<int, 1>{}, k);
     }
 
     // ---- this warp's state: O^T rows -> dims, heads 2t and 2t+1
