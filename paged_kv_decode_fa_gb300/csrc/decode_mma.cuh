@@ -129,9 +129,9 @@ struct MmaCfg {
   // columns the warps split the pages instead (page k to warp k % NW).
   static constexpr bool CS = NC > 8;
   static constexpr int NS = CS ? 1 : NW;  // partial states per column at a segment's end
-  // pages a consumer warp takes per step: two for the column split (every
-  // warp takes every page), one for the page split
-  static constexpr int NPP = CS ? 2 : 1;
+  // pages a consumer warp takes per step: two or three (E4M3) for the
+  // column split (every warp takes every page), one for the page split
+  static constexpr int NPP = CS ? (sizeof(KVT) == 1 ? 3 : 2) : 1;
   static constexpr int P = kPageSize;
   static constexpr int KV_ES = sizeof(KVT);
   static constexpr bool kFp8 = KV_ES == 1;
@@ -450,8 +450,8 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
     };
 
     // One step over NPP consecutive pages k .. k + NPP - 1 of the segment:
-    // scores, one softmax update over all of them, P.V.  Two pages a step
-    // (the column split) keep two pages' independent loads and MMA chains
+    // scores, one softmax update over all of them, P.V.  Several pages a
+    // step (the column split) keep their independent loads and MMA chains
     // in flight in the warp at once.
     auto step = [&](auto npp_tag, int k) {
       constexpr int NPP = decltype(npp_tag)::value;
@@ -634,7 +634,7 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
     };
 
     // page split: page k to warp k % NW, one page a step; column split:
-    // every page to every warp, two pages a step (and a last single page)
+    // every page to every warp, NPP pages a step (the rest one at a time)
     if constexpr (CS) {
       int k = kbase;
       for (; k + C::NPP - 1 < kbase + npg; k += C::NPP)
