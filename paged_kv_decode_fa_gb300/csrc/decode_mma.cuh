@@ -449,20 +449,22 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
       }
     };
 
-    // One step over NPP consecutive pages k .. k + NPP - 1 of the segment:
-    // scores, one softmax update over all of them, P.V.  Several pages a
-    // step (the column split) keep their independent loads and MMA chains
+    // One step over NPP of the warp's pages, k, k + PS, ..., of the segment
+    // (PS: the distance between the warp's pages, 1 for the column split,
+    // NW for the page split): scores, one softmax update over all of them,
+    // P.V.  Several pages a step keep their independent loads and MMA chains
     // in flight in the warp at once.
+    constexpr int PS = CS ? 1 : NW;
     auto step = [&](auto npp_tag, int k) {
       constexpr int NPP = decltype(npp_tag)::value;
       int stage[NPP], lp[NPP], valid[NPP];
       uint32_t st[NPP];
 #pragma unroll
       for (int u = 0; u < NPP; ++u) {
-        lp[u] = k + u - kbase;
-        stage[u] = (k + u) % S;
-        dev::mbar_wait(dev::smem_addr(&full[stage[u]]), (uint32_t)(((k + u) / S) & 1), aborted,
-                       p.err);
+        const int ku = k + u * PS;
+        lp[u] = ku - kbase;
+        stage[u] = ku % S;
+        dev::mbar_wait(dev::smem_addr(&full[stage[u]]), (uint32_t)((ku / S) & 1), aborted, p.err);
         st[u] = ring_addr + stage[u] * C::STAGE_BYTES;
         valid[u] = (lp[u] == npg - 1) ? last_valid : P;
       }
@@ -635,14 +637,13 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
 
     // page split: page k to warp k % NW, one page a step; column split:
     // every page to every warp, NPP pages a step (the rest one at a time)
-    if constexpr (CS) {
-      int k = kbase;
-      for (; k + C::NPP - 1 < kbase + npg; k += C::NPP)
-        step(std::integral_constant<int, C::NPP>{}, k);
-      for (; k < kbase + npg; ++k) step(std::integral_constant<int, 1>{}, k);
-    } else {
-      for (int k = kbase + (warp - kbase % NW + NW) % NW; k < kbase + npg; k += NW)
-        step(std::integral_constant<int, 1>{}, k);
+    {
+      int k = CS ? kbase : kbase + (warp - kbase % NW + NW) % NW;
+      if constexpr (C::NPP > 1) {
+        for (; k + (C::NPP - 1) * PS < kbase + npg; k += C::NPP * PS)
+          step(std::integral_constant<int, C::NPP>{}, k);
+      }
+      for (; k < kbase + npg; k += PS) step(std::integral_constant<int, 1>{}, k);
     }
 
     // ---- this warp's state: O^T rows -> dims, heads 2t and 2t+1
