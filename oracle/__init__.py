@@ -168,6 +168,30 @@ class Oracle:
             raise ValueError("oracle_batch_decode_token_scales rejected its arguments")
         return o, lse
 
+    def batch_decode_head_scales(self, q, q_dtype, paged_kv, kv_dtype, indptr, indices,
+                                 last_page_len, num_qo_heads, num_kv_heads, head_dim, page_size,
+                                 k_head_scales, v_head_scales, sm_scale=None, num_threads=0):
+        """Decode attention with one dequantisation scale per kv head
+        ("FlashInfer vs FlashAttention-3", "Production War Story: The FP8
+        Precision Underflow Failure": scales finer than one per tensor):
+        k_head_scales / v_head_scales are float32 [num_kv_heads] and multiply
+        every stored K / V element of that head.  By definition this is the
+        per-token form with every token of kv head h scaled by its head's
+        scale, which is how it is computed here."""
+        k_head_scales = np.asarray(k_head_scales, dtype=np.float32).reshape(-1)
+        v_head_scales = np.asarray(v_head_scales, dtype=np.float32).reshape(-1)
+        if k_head_scales.size != num_kv_heads or v_head_scales.size != num_kv_heads:
+            raise ValueError("head scales must be [num_kv_heads]")
+        per_page = 2 * page_size * num_kv_heads * head_dim
+        num_pages = np.asarray(paged_kv).size // per_page
+        shape = (num_pages, num_kv_heads, page_size)
+        ks = np.broadcast_to(k_head_scales[None, :, None], shape)
+        vs = np.broadcast_to(v_head_scales[None, :, None], shape)
+        return self.batch_decode_token_scales(q, q_dtype, paged_kv, kv_dtype, indptr, indices,
+                                              last_page_len, num_qo_heads, num_kv_heads,
+                                              head_dim, page_size, ks, vs, sm_scale=sm_scale,
+                                              num_threads=num_threads)
+
     def batch_decode_multi(self, q, q_dtype, paged_kv, kv_dtype, indptr, indices, last_page_len,
                            q_len, num_qo_heads, num_kv_heads, head_dim, page_size,
                            sm_scale=None, k_scale=1.0, v_scale=1.0, num_threads=0):
@@ -311,6 +335,10 @@ def batch_decode(*args, **kw):
 
 def batch_decode_token_scales(*args, **kw):
     return _default().batch_decode_token_scales(*args, **kw)
+
+
+def batch_decode_head_scales(*args, **kw):
+    return _default().batch_decode_head_scales(*args, **kw)
 
 
 def batch_decode_multi(*args, **kw):

@@ -333,6 +333,59 @@ def pin_token_scales_uniform(orc):
     np.testing.assert_array_equal(a[1], b[1])
 
 
+def _head_scale_case(seed=15):
+    from tests.helpers import as_bits
+    kv, q, perm, indptr, last, _, _, lens, (Hq, Hkv, D, P) = _fp8_batch(seed, Hq=6, Hkv=3)
+    rng = np.random.default_rng(seed)
+    kh = (rng.random(Hkv) * 0.05 + 0.002).astype(np.float32)
+    vh = (rng.random(Hkv) * 0.05 + 0.002).astype(np.float32)
+    qb, qc = as_bits(q)
+    kb, kc = as_bits(kv)
+    return (qb, qc, kb, kc, indptr, perm.numpy(), last, Hq, Hkv, D, P), kh, vh, kv, q, lens
+
+
+def head_scales_match_per_tensor_per_head(orc, o, lse, args, kh, vh):
+    """Rows of kv head h's query heads equal the per-tensor oracle run with
+    k_scale = kh[h], v_scale = vh[h] (the heads do not interact)."""
+    qb, qc, kb, kc, indptr, ids, last, Hq, Hkv, D, P = args
+    g = Hq // Hkv
+    for h in range(Hkv):
+        ro, rl = orc.batch_decode(qb, qc, kb, kc, indptr, ids, last, Hq, Hkv, D, P,
+                                  k_scale=float(kh[h]), v_scale=float(vh[h]))
+        rows = slice(h * g, (h + 1) * g)
+        np.testing.assert_allclose(o[:, rows], ro[:, rows], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[:, rows], rl[:, rows], rtol=0, atol=1e-12)
+
+
+def pin_head_scales_per_head(orc):
+    """One scale per kv head: each head's rows are the per-tensor result
+    with that head's two scales."""
+    args, kh, vh, *_ = _head_scale_case()
+    o, lse = orc.batch_decode_head_scales(*args, kh, vh)
+    head_scales_match_per_tensor_per_head(orc, o, lse, args, kh, vh)
+
+
+def pin_head_scales_dense(orc):
+    """One scale per kv head against torch float64 on K and V dequantised
+    with their head's scale."""
+    args, kh, vh, kv, q, lens = _head_scale_case(16)
+    qb, qc, kb, kc, indptr, ids, last, Hq, Hkv, D, P = args
+    o, lse = orc.batch_decode_head_scales(*args, kh, vh)
+    kvd = kv.to(torch.float64)
+    khd = torch.tensor(kh, dtype=torch.float64)[:, None]
+    vhd = torch.tensor(vh, dtype=torch.float64)[:, None]
+    g = Hq // Hkv
+    for i, n in enumerate(lens):
+        pid = torch.from_numpy(ids[indptr[i]:indptr[i + 1]]).long()
+        Kd = kvd[pid, 0].reshape(-1, Hkv, D)[:n] * khd
+        Vd = kvd[pid, 1].reshape(-1, Hkv, D)[:n] * vhd
+        s = torch.einsum("hd,nhd->hn", q[i].to(torch.float64), Kd.repeat_interleave(g, 1))
+        s = s / math.sqrt(D)
+        ref_o = torch.einsum("hn,nhd->hd", torch.softmax(s, -1), Vd.repeat_interleave(g, 1))
+        np.testing.assert_allclose(o[i], ref_o.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[i], torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
+
+
 def _multi_batch(seed, lens=(5, 16, 17, 40), q_len=3, Hq=4, Hkv=2, D=8, P=4):
     rng = np.random.default_rng(seed)
     K = [rng.standard_normal((n, Hkv, D)).astype(np.float32) for n in lens]
@@ -530,7 +583,8 @@ def pin_rejects_bad_args(orc):
     pin_single_key, pin_identical_keys, pin_zero_query, pin_convexity, pin_split_merge,
     pin_gqa_equals_repeated_mha, pin_page_permutation, pin_brute_force, pin_torch_dense,
     pin_empty_request, pin_padding_never_read, pin_golden_decode, pin_rejects_bad_args,
-    pin_token_scales_dense, pin_token_scales_uniform, pin_multi_token_truncation,
+    pin_token_scales_dense, pin_token_scales_uniform, pin_head_scales_per_head,
+    pin_head_scales_dense, pin_multi_token_truncation,
     pin_multi_token_causal_dense, pin_multi_token_one_is_decode, pin_ragged_q_truncation,
     pin_ragged_q_sdpa, pin_ragged_q_one_token_is_decode])
 def test_decode_pins(orc, pin):

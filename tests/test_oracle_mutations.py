@@ -4,6 +4,7 @@ pins worth trusting: each mistake below is the kind a careless restatement
 of the method would make."""
 import os
 
+import numpy as np
 import pytest
 
 import oracle
@@ -66,3 +67,27 @@ def test_planted_mistake_is_caught(tmp_path, name, old, new, pins):
     for pin in pins:
         with pytest.raises((AssertionError, ValueError)):
             pin(bad)
+
+
+@pytest.mark.parametrize("axis", ["slot", "page"])
+def test_head_scale_broadcast_mistake_is_caught(axis):
+    """The per-head oracle broadcasts [num_kv_heads] scales over
+    [num_pages, num_kv_heads, page_size]; a broadcast along the wrong axis
+    (the scales taken by slot or by page instead of by head) breaks the
+    per-head pin."""
+    orc = oracle._default()
+    args, kh, vh, *_ = T._head_scale_case()
+    qb, qc, kb, kc, indptr, ids, last, Hq, Hkv, D, P = args
+    num_pages = kb.size // (2 * P * Hkv * D)
+    shape = (num_pages, Hkv, P)
+    k_by = np.resize(kh, P if axis == "slot" else num_pages).astype(np.float32)
+    v_by = np.resize(vh, P if axis == "slot" else num_pages).astype(np.float32)
+    if axis == "slot":
+        ks = np.broadcast_to(k_by[None, None, :], shape)
+        vs = np.broadcast_to(v_by[None, None, :], shape)
+    else:
+        ks = np.broadcast_to(k_by[:, None, None], shape)
+        vs = np.broadcast_to(v_by[:, None, None], shape)
+    o, lse = orc.batch_decode_token_scales(*args, ks, vs)
+    with pytest.raises(AssertionError):
+        T.head_scales_match_per_tensor_per_head(orc, o, lse, args, kh, vh)
