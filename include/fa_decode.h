@@ -225,6 +225,25 @@ int fa_decode_run_token_scales(fa_decode_plan_t plan, const void* q,
                                const float* v_scales, void* o, float* lse,
                                void* cuda_stream);
 
+/* run with one FP8 scale per kv head: like fa_decode_run for a plan whose
+ * kv dtype is E4M3, but the K (V) elements of kv head h are dequantised with
+ * k_head_scales[h] (v_head_scales[h]) - scales finer than one per tensor,
+ * coarser than fa_decode_run_token_scales' per token ("FlashInfer vs
+ * FlashAttention-3", section "Production War Story: The FP8 Precision
+ * Underflow Failure").
+ *
+ *  k_head_scales, v_head_scales  [num_kv_heads] float32, device, 4-byte
+ *                      aligned, caller-owned: the K (V) element of kv head h
+ *                      has the value code * scales[h].
+ * Other arguments as fa_decode_run (sm_scale <= 0 selects 1/sqrt(head_dim)).
+ * Every plan kind (plain, multi-token, ragged query rows) and kernel takes
+ * it; plans whose kv dtype is not E4M3 return FA_ERR_UNSUPPORTED, NULL
+ * scales FA_ERR_INVALID_ARG. */
+int fa_decode_run_head_scales(fa_decode_plan_t plan, const void* q, const void* paged_kv,
+                              int64_t num_pages, float sm_scale, const float* k_head_scales,
+                              const float* v_head_scales, void* o, float* lse,
+                              void* cuda_stream);
+
 /* run with a unified max (page "FlashDecoding + FlashInfer", section
  * "FlashDecoding++", item 1 "Async-softmax with unified max"): instead of a
  * running maximum per query head, every weight is exp(s - max_bound) for a

@@ -41,6 +41,7 @@ EXPORTED_SYMBOLS = (
     "fa_cascade_check", "fa_decode_run_unified_max", "fa_decode_unified_max_fallbacks",
     "fa_cascade_set_timing_events", "fa_decode_static_check", "fa_library_get_stats",
     "fa_decode_plan_ragged_q", "fa_decode_workspace_size_ragged_q", "fa_cascade_run_scaled",
+    "fa_decode_run_head_scales",
 )
 
 FA_OK = 0
@@ -106,6 +107,8 @@ def _load() -> ctypes.CDLL:
     lib.fa_decode_run.restype = i32
     lib.fa_decode_run_token_scales.argtypes = [P, P, P, i64, f32, P, P, P, P, P]
     lib.fa_decode_run_token_scales.restype = i32
+    lib.fa_decode_run_head_scales.argtypes = [P, P, P, i64, f32, P, P, P, P, P]
+    lib.fa_decode_run_head_scales.restype = i32
     lib.fa_decode_run_unified_max.argtypes = [P, P, P, i64, f32, f32, f32, f32, P, P, P]
     lib.fa_decode_run_unified_max.restype = i32
     lib.fa_decode_unified_max_fallbacks.argtypes = [P, P, ctypes.POINTER(i32)]
@@ -310,6 +313,25 @@ class DecodePlan:
             0.0 if sm_scale is None else float(sm_scale), float(k_scale), float(v_scale),
             float(max_bound), out.data_ptr(), lse.data_ptr() if lse is not None else None,
             _stream_handle(stream)), "fa_decode_run_unified_max")
+        return out, lse
+
+    def run_head_scales(self, q: torch.Tensor, paged_kv: torch.Tensor, k_scales: torch.Tensor,
+                        v_scales: torch.Tensor, *, sm_scale: float | None = None,
+                        out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                        return_lse: bool = True, stream=None):
+        """Decode over an E4M3 cache with one scale per kv head: k_scales /
+        v_scales [num_kv_heads] float32 CUDA tensors; returns (o, lse)."""
+        for s in (k_scales, v_scales):
+            if (s.dtype != torch.float32 or tuple(s.shape) != (self.num_kv_heads,)
+                    or not s.is_contiguous() or not s.is_cuda):
+                raise ValueError(f"scales must be contiguous float32 CUDA tensors "
+                                 f"[{self.num_kv_heads}]")
+        out, lse = self._outputs(q, paged_kv, out, lse, return_lse)
+        _check(_L().fa_decode_run_head_scales(
+            self._h, q.data_ptr(), paged_kv.data_ptr(), paged_kv.shape[0],
+            0.0 if sm_scale is None else float(sm_scale), k_scales.data_ptr(),
+            v_scales.data_ptr(), out.data_ptr(), lse.data_ptr() if lse is not None else None,
+            _stream_handle(stream)), "fa_decode_run_head_scales")
         return out, lse
 
     def unified_max_fallbacks(self, stream=None) -> int:

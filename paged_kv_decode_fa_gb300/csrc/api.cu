@@ -292,7 +292,8 @@ struct LaunchView {
 int launch_decode(const LaunchView& lv, const void* q, const void* paged_kv, int64_t num_pages,
                   float sm_scale, float k_scale, float v_scale, const float* k_scales,
                   const float* v_scales, float max_bound, void* o, float* lse,
-                  void* cuda_stream);
+                  void* cuda_stream, const float* head_k_scales = nullptr,
+                  const float* head_v_scales = nullptr);
 
 }  // namespace
 
@@ -300,7 +301,9 @@ struct fa_decode_plan_s;
 static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
                     const void* paged_kv, int64_t num_pages, float sm_scale, float k_scale,
                     float v_scale, const float* k_scales, const float* v_scales,
-                    float max_bound, void* o, float* lse, void* cuda_stream);
+                    float max_bound, void* o, float* lse, void* cuda_stream,
+                    const float* head_k_scales = nullptr,
+                    const float* head_v_scales = nullptr);
 
 struct fa_decode_plan_s {
   int device = 0;
@@ -628,6 +631,20 @@ int fa_decode_run_token_scales(fa_decode_plan_t plan, const void* q, const void*
                   v_scales, 0.f, o, lse, cuda_stream);
 }
 
+int fa_decode_run_head_scales(fa_decode_plan_t plan, const void* q, const void* paged_kv,
+                              int64_t num_pages, float sm_scale, const float* k_head_scales,
+                              const float* v_head_scales, void* o, float* lse,
+                              void* cuda_stream) {
+  if (!plan) return FA_ERR_INVALID_ARG;
+  if (plan->kv_dtype != FA_DTYPE_E4M3) return FA_ERR_UNSUPPORTED;
+  if (plan->batch > 0 && (!k_head_scales || !v_head_scales)) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(k_head_scales) % 4 ||
+      reinterpret_cast<uintptr_t>(v_head_scales) % 4)
+    return FA_ERR_INVALID_ARG;
+  return run_impl(plan, kPlain, q, paged_kv, num_pages, sm_scale, 1.f, 1.f, nullptr, nullptr,
+                  0.f, o, lse, cuda_stream, k_head_scales, v_head_scales);
+}
+
 int fa_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
                     void* o_out, float* lse_out, int n, int num_heads, int head_dim,
                     fa_dtype dtype, void* cuda_stream) {
@@ -840,7 +857,8 @@ int static_decode(void* scratch, size_t scratch_bytes, const int32_t* indptr_hos
 static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
                     const void* paged_kv, int64_t num_pages, float sm_scale, float k_scale,
                     float v_scale, const float* k_scales, const float* v_scales,
-                    float max_bound, void* o, float* lse, void* cuda_stream) {
+                    float max_bound, void* o, float* lse, void* cuda_stream,
+                    const float* head_k_scales, const float* head_v_scales) {
   LaunchView lv;
   lv.batch = plan->batch;
   lv.hq = plan->hq;
@@ -864,7 +882,7 @@ static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
   lv.ev_before = plan->ev_before;
   lv.ev_after = plan->ev_after;
   return launch_decode(lv, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, k_scales,
-                       v_scales, max_bound, o, lse, cuda_stream);
+                       v_scales, max_bound, o, lse, cuda_stream, head_k_scales, head_v_scales);
 }
 
 namespace {
@@ -872,7 +890,8 @@ namespace {
 int launch_decode(const LaunchView& lv, const void* q, const void* paged_kv, int64_t num_pages,
                   float sm_scale, float k_scale, float v_scale, const float* k_scales,
                   const float* v_scales, float max_bound, void* o, float* lse,
-                  void* cuda_stream) {
+                  void* cuda_stream, const float* head_k_scales,
+                  const float* head_v_scales) {
   if (lv.batch == 0) return FA_OK;
   if (!q || !paged_kv || !o || num_pages <= 0) return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(paged_kv) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
@@ -904,6 +923,8 @@ int launch_decode(const LaunchView& lv, const void* q, const void* paged_kv, int
   prm.fused_merge = lv.fused_merge ? 1 : 0;
   prm.k_scales = k_scales;
   prm.v_scales = v_scales;
+  prm.head_k_scales = head_k_scales;
+  prm.head_v_scales = head_v_scales;
   prm.num_pages = num_pages;
   prm.num_qo_heads = lv.hq;
   prm.num_kv_heads = lv.hkv;

@@ -789,6 +789,9 @@ __device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const fl
   // a split piece stores every column of its slot; final rows only the
   // columns in use
   const int cols = out_slot < 0 ? qr.ncols : NC;
+  // the per-tensor V scale, times the kv head's own (per-head scales)
+  const float v_scale =
+      p.head_v_scales ? p.v_scale * __ldg(p.head_v_scales + kvh) : p.v_scale;
   for (int e = threadIdx.x; e < cols * D; e += CT) {
     const int h = e / D, dd = e % D;
     float M = -INFINITY;
@@ -803,7 +806,7 @@ __device__ __forceinline__ void combine_and_emit(const DecodeParams& p, const fl
         den = fmaf(md[w * NC + h], sw, den);
         num = fmaf(mo[(w * NC + h) * D + dd], sw, num);
       }
-      out = num / den * p.v_scale;
+      out = num / den * v_scale;
       lse2 = M + dev::fast_log2(den);
     }
     if (out_slot < 0) {
@@ -952,6 +955,8 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
     const int4 sb = *reinterpret_cast<const int4*>(p.segments + 8 * si + 4);
     const int req = sa.x, kvh = sa.y, npg = sa.w - sa.z;
     const int last_valid = sb.x, out_slot = sb.y;
+    const float q_scale =
+        p.head_k_scales ? p.q_scale * __ldg(p.head_k_scales + kvh) : p.q_scale;
 
     float qf[G][VEC];
     float acc[G][VEC];
@@ -961,7 +966,7 @@ __global__ void __launch_bounds__(DecodeCfg<QT, KVT, D, G, NW>::THREADS)
       dev::load_q<QT, VEC>(qp, qf[h]);
 #pragma unroll
       for (int v = 0; v < VEC; ++v) {
-        qf[h][v] *= p.q_scale;
+        qf[h][v] *= q_scale;
         acc[h][v] = 0.f;
       }
     }

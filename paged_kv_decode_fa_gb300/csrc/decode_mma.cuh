@@ -308,7 +308,10 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
     // granules 2t and 2t+1 of each 128-byte row segment (the same elements
     // the lane loads from K).
     uint32_t qb[KSTEPS][2];
-    float qscale = p.q_scale;
+    // per-kv-head scales (fa_decode_run_head_scales) join the per-tensor ones
+    const float seg_q_scale = p.head_k_scales ? p.q_scale * __ldg(p.head_k_scales + kvh)
+                                              : p.q_scale;
+    float qscale = seg_q_scale;
     {
       float qf[KSTEPS][4];
 #pragma unroll
@@ -356,7 +359,7 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
           shift = min(max(14 - ex, -120), 120);
         }
         const float up = ldexpf(1.f, shift);
-        qscale = p.q_scale * ldexpf(1.f, -shift);
+        qscale = seg_q_scale * ldexpf(1.f, -shift);
 #pragma unroll
         for (int j = 0; j < KSTEPS; ++j) {
           qb[j][0] = mma::pack2(qf[j][0] * up, qf[j][1] * up, false);

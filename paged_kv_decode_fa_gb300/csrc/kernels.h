@@ -27,6 +27,8 @@ struct DecodeParams {
   int fused_merge;             // 1: the last CTA of a split unit merges it
   const float* k_scales;       // [num_pages, Hkv, page_size] per-token scales, or nullptr
   const float* v_scales;       // same for V
+  const float* head_k_scales;  // [Hkv] one K scale per kv head (times q_scale), or nullptr
+  const float* head_v_scales;  // [Hkv] one V scale per kv head (times v_scale), or nullptr
   int64_t num_pages;
   int num_qo_heads;
   int num_kv_heads;

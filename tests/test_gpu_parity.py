@@ -502,6 +502,124 @@ def test_token_scales_unsupported(lib, cuda):
     assert rc == -2   # bf16 KV has no per-token scales
 
 
+# ------------------------------------------------------------------ per-head FP8 scales
+
+def quantise_per_head(b, spread, seed):
+    """Redraw b's E4M3 cache with K and V of kv head h at magnitude
+    2^(u_h * spread) and one scale per head and half (amax / 448), as a
+    cache quantised head by head would hold; returns the two scale tensors."""
+    gen = torch.Generator(device=b.paged_kv.device).manual_seed(seed)
+    pool, _, P, Hkv, D = b.paged_kv.shape
+    scales = []
+    for half in range(2):
+        mag = torch.exp2((torch.rand(Hkv, generator=gen, device=b.paged_kv.device) * 2 - 1)
+                         * spread)
+        x = torch.randn((pool, P, Hkv, D), generator=gen, device=b.paged_kv.device) * mag[:, None]
+        s = (x.abs().amax(dim=(0, 1, 3)) / 448.0).clamp_min(1e-12)
+        b.paged_kv[:, half] = (x / s[:, None]).to(torch.float8_e4m3fn)
+        scales.append(s.to(torch.float32).contiguous())
+    return scales
+
+
+def oracle_head_scales(b, ks, vs):
+    from tests.helpers import as_bits
+    q, qc = as_bits(b.q)
+    kv, kc = as_bits(b.paged_kv)
+    return oracle.batch_decode_head_scales(q, qc, kv, kc, b.indptr.numpy(),
+                                           b.indices.cpu().numpy(), b.last_page_len.numpy(),
+                                           b.num_qo_heads, b.num_kv_heads, b.head_dim,
+                                           b.page_size, ks.cpu().numpy(), vs.cpu().numpy())
+
+
+@pytest.mark.parametrize("q_dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+@pytest.mark.parametrize("hq,hkv,d", [(16, 8, 128), (32, 4, 128), (64, 8, 128), (8, 8, 128),
+                                      (16, 4, 64)],
+                         ids=["g2", "g8", "g8-fp8kv", "g1-cuda-cores", "d64-cuda-cores"])
+def test_head_scales_against_oracle(lib, cuda, q_dtype, hq, hkv, d):
+    """One scale per kv head (fa_decode_run_head_scales) on a cache whose
+    heads differ in magnitude by up to 2^2 either way: every row against the
+    per-head oracle, on the tensor-core and the CUDA-core consumers, with
+    split units.  |o| reaches about 16 on the largest heads, where the bf16
+    output's own rounding (half an ulp, 2^-9 relative) passes an absolute
+    3e-2, so the bound is abs 3e-2 + 2^-8 |oracle o|, as for the per-token
+    spread workload."""
+    b = W.make_batch(batch_lengths=[1, 16, 17, 300, 2900, 45], num_qo_heads=hq,
+                     num_kv_heads=hkv, head_dim=d, q_dtype=q_dtype,
+                     kv_dtype=torch.float8_e4m3fn, seed=hq + hkv + d, device=cuda)
+    ks, vs = quantise_per_head(b, 2.0, seed=7 + hq)
+    p = lib.plan(b.indptr, b.indices, b.last_page_len, hq, hkv, d, 16, q_data_type=q_dtype,
+                 kv_data_type=torch.float8_e4m3fn)
+    o, lse = p.run_head_scales(b.q, b.paged_kv, ks, vs)
+    torch.cuda.synchronize()
+    assert p.check() == 0 and p.info["num_merge_units"] > 0
+    ref_o, ref_lse = oracle_head_scales(b, ks, vs)
+    compare(o, lse, ref_o, ref_lse, TOL[torch.float8_e4m3fn], rel=2 ** -8)
+
+
+def test_head_scales_equal_heads_is_per_tensor(lib, cuda):
+    """Every head with the same two scales gives the per-tensor run (within
+    the fp32 rounding of where the scale is folded in)."""
+    b = W.make_batch(batch_lengths=[33, 700, 5000], num_qo_heads=32, num_kv_heads=8,
+                     head_dim=128, q_dtype=torch.bfloat16, kv_dtype=torch.float8_e4m3fn,
+                     seed=31, device=cuda)
+    p = lib.plan(b.indptr, b.indices, b.last_page_len, 32, 8, 128, 16,
+                 q_data_type=torch.bfloat16, kv_data_type=torch.float8_e4m3fn)
+    ref, ref_lse = p.run(b.q, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale)
+    ks = torch.full((8,), b.k_scale, dtype=torch.float32, device=cuda)
+    vs = torch.full((8,), b.v_scale, dtype=torch.float32, device=cuda)
+    o, lse = p.run_head_scales(b.q, b.paged_kv, ks, vs)
+    torch.cuda.synchronize()
+    assert (o.float() - ref.float()).abs().max().item() <= 2 ** -7
+    assert (lse - ref_lse).abs().max().item() <= 1e-4
+
+
+def test_head_scales_ragged_q(lib, cuda):
+    """Per-head scales on a ragged multi-token plan (group 8, 1..4 drafts:
+    the column split) against the ragged oracle run head by head."""
+    lengths = [20, 400, 3000, 64, 9]
+    counts = [1, 4, 2, 3, 4]
+    b = W.make_ragged_q_batch(batch_lengths=lengths, q_counts=counts, num_qo_heads=16,
+                              num_kv_heads=2, head_dim=128, q_dtype=torch.bfloat16,
+                              kv_dtype=torch.float8_e4m3fn, seed=41, device=cuda)
+    ks, vs = quantise_per_head(b, 1.0, seed=42)
+    p = lib.plan_ragged_q(b.indptr, b.indices, b.last_page_len, b.extra["qo_indptr"], 16, 2,
+                          128, 16, q_data_type=torch.bfloat16, kv_data_type=torch.float8_e4m3fn)
+    o, lse = p.run_head_scales(b.q, b.paged_kv, ks, vs)
+    torch.cuda.synchronize()
+    assert p.check() == 0
+    # the heads do not interact: kv head h's rows are the per-tensor oracle
+    # with head h's scales
+    import dataclasses
+    g = 8
+    for h in range(2):
+        bh = dataclasses.replace(b, k_scale=float(ks[h]), v_scale=float(vs[h]))
+        ref_o, ref_lse = oracle_decode(bh)
+        rows = slice(h * g, (h + 1) * g)
+        compare(o[:, rows], lse[:, rows], ref_o[:, rows], ref_lse[:, rows],
+                TOL[torch.float8_e4m3fn], rel=2 ** -8)
+
+
+def test_head_scales_rejects(lib, cuda):
+    idx = torch.zeros(1, dtype=torch.int32, device=cuda)
+    q = torch.zeros((1, 8, 128), dtype=torch.bfloat16, device=cuda)
+    sc = torch.ones(8, dtype=torch.float32, device=cuda)
+    kvb = torch.zeros((1, 2, 16, 8, 128), dtype=torch.bfloat16, device=cuda)
+    pb = lib.plan([0, 1], idx, [1], 8, 8, 128, 16, q_data_type=torch.bfloat16)
+    with pytest.raises(lib.FaError) as e:     # a 16-bit cache has no per-head scales
+        pb.run_head_scales(q, kvb, sc, sc)
+    assert e.value.status == -2
+    kv = torch.zeros((1, 2, 16, 8, 128), dtype=torch.float8_e4m3fn, device=cuda)
+    p = lib.plan([0, 1], idx, [1], 8, 8, 128, 16, q_data_type=torch.bfloat16,
+                 kv_data_type=torch.float8_e4m3fn)
+    rc = lib.library().fa_decode_run_head_scales(p._h, q.data_ptr(), kv.data_ptr(), 1, 0.0,
+                                                 None, sc.data_ptr(),
+                                                 torch.empty_like(q).data_ptr(), None,
+                                                 torch.cuda.current_stream().cuda_stream)
+    assert rc == -1
+    with pytest.raises(ValueError):
+        p.run_head_scales(q, kv, sc[:4], sc)
+
+
 # ------------------------------------------------------------------ multi-token decode
 
 def run_ragged(lib, b, workspace=None):
