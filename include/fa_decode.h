@@ -366,6 +366,24 @@ int fa_plan_work_host(const int32_t* indptr, const int32_t* last_page_len,
                       int32_t* segments, int32_t* merge, int* n_ctas,
                       int* n_segments, int* n_merge, int* n_slots);
 
+/* The plan fa_decode_plan makes by default, on the host: the grid in
+ * groups of num_kv_heads CTAs, group g taking the g-th equal share of the
+ * batch's page stream (request by request, a fixed cost of 2 pages before
+ * each non-empty request) for every kv head, CTA g * num_kv_heads + h the
+ * head-h part, so that a group's CTAs read the same pages' kv-head rows side
+ * by side.  A request a group boundary falls inside is split there for
+ * every head, and its pieces are merged as in fa_plan_work_host's plans.
+ * fa_plan_work_host gives the other plan, the stream of (request, kv head)
+ * units cut into equal quotas, which fa_decode_plan uses with a run-time
+ * pool or with FADECODE_PLAN=stream in the environment, and whenever the
+ * grid has fewer CTAs than kv heads.  Arguments, capacities and errors as
+ * fa_plan_work_host (no pool). */
+int fa_plan_work_host_heads(const int32_t* indptr, const int32_t* last_page_len, int batch,
+                            int num_kv_heads, int page_size, int max_ctas,
+                            int min_pages_per_cta, int32_t* cta_offsets, int32_t* segments,
+                            int32_t* merge, int* n_ctas, int* n_segments, int* n_merge,
+                            int* n_slots);
+
 /* Wait for cuda_stream, then read and clear the plan's device-check word.
  * Returns FA_OK, FA_ERR_DEVICE_CHECK with *flags set (bit 0: page id outside
  * [0, num_pages); bit 1: a pipeline wait timed out), or FA_ERR_CUDA.

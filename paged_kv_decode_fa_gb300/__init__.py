@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = (
     "fa_cascade_check", "fa_decode_run_unified_max", "fa_decode_unified_max_fallbacks",
     "fa_cascade_set_timing_events", "fa_decode_static_check", "fa_library_get_stats",
     "fa_decode_plan_ragged_q", "fa_decode_workspace_size_ragged_q", "fa_cascade_run_scaled",
-    "fa_decode_run_head_scales",
+    "fa_decode_run_head_scales", "fa_plan_work_host_heads",
 )
 
 FA_OK = 0
@@ -139,6 +139,8 @@ def _load() -> ctypes.CDLL:
                                       ctypes.POINTER(i32), ctypes.POINTER(i32),
                                       ctypes.POINTER(i32), ctypes.POINTER(i32)]
     lib.fa_plan_work_host.restype = i32
+    lib.fa_plan_work_host_heads.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
+    lib.fa_plan_work_host_heads.restype = i32
     lib.fa_decode_check.argtypes = [P, P, ctypes.POINTER(i32)]
     lib.fa_decode_check.restype = i32
     lib.fa_decode_set_timing_events.argtypes = [P, P, P]
@@ -547,9 +549,11 @@ def merge_states(o_a: torch.Tensor, lse_a: torch.Tensor, o_b: torch.Tensor, lse_
 
 
 def plan_work_host(indptr, last_page_len, num_kv_heads: int, page_size: int, max_ctas: int,
-                   min_pages_per_cta: int = 8, pool_fraction: float = 0.0):
+                   min_pages_per_cta: int = 8, pool_fraction: float = 0.0, heads: bool = False):
     """Host-only work-list builder (no GPU).  Returns (cta_offsets, segments [n,8],
-    merge [m,4], n_slots); segments cta_offsets[-1]: are the run-time pool."""
+    merge [m,4], n_slots); segments cta_offsets[-1]: are the run-time pool.
+    heads=True: the head-grouped plan fa_decode_plan makes by default
+    (fa_plan_work_host_heads; no pool)."""
     indptr_h, indptr_p, n_indptr = _host_i32_ptr(indptr)
     last_h, last_p, n_last = _host_i32_ptr(last_page_len)
     B = n_indptr - 1
@@ -560,11 +564,18 @@ def plan_work_host(indptr, last_page_len, num_kv_heads: int, page_size: int, max
     seg = np.zeros(((B * num_kv_heads + cuts) * SEGMENT_INTS,), np.int32)
     mer = np.zeros((cuts * MERGE_INTS,), np.int32)
     n_c, n_s, n_m, n_sl = (ctypes.c_int() for _ in range(4))
-    _check(_L().fa_plan_work_host(indptr_p, last_p if B else None, B,
-                                  num_kv_heads, page_size, max_ctas, min_pages_per_cta,
-                                  float(pool_fraction), cta.ctypes.data, seg.ctypes.data, mer.ctypes.data,
-                                  ctypes.byref(n_c), ctypes.byref(n_s), ctypes.byref(n_m),
-                                  ctypes.byref(n_sl)), "fa_plan_work_host")
+    if heads:
+        _check(_L().fa_plan_work_host_heads(
+            indptr_p, last_p if B else None, B, num_kv_heads, page_size, max_ctas,
+            min_pages_per_cta, cta.ctypes.data, seg.ctypes.data, mer.ctypes.data,
+            ctypes.byref(n_c), ctypes.byref(n_s), ctypes.byref(n_m), ctypes.byref(n_sl)),
+            "fa_plan_work_host_heads")
+    else:
+        _check(_L().fa_plan_work_host(indptr_p, last_p if B else None, B,
+                                      num_kv_heads, page_size, max_ctas, min_pages_per_cta,
+                                      float(pool_fraction), cta.ctypes.data, seg.ctypes.data,
+                                      mer.ctypes.data, ctypes.byref(n_c), ctypes.byref(n_s),
+                                      ctypes.byref(n_m), ctypes.byref(n_sl)), "fa_plan_work_host")
     return (cta[: n_c.value + 1].copy(), seg[: n_s.value * SEGMENT_INTS].reshape(-1, SEGMENT_INTS).copy(),
             mer[: n_m.value * MERGE_INTS].reshape(-1, MERGE_INTS).copy(), n_sl.value)
 

@@ -91,6 +91,15 @@ double pool_fraction() {
   return f >= 0.0 && f <= 0.5 ? f : kPoolFraction;
 }
 
+// Plans put the grid in groups of num_kv_heads CTAs that stream the same
+// pages, one kv head each (the planner's plan_heads); FADECODE_PLAN=stream
+// cuts the stream of (request, kv head) units instead (for comparisons, and
+// what a run-time pool uses).
+bool heads_plan() {
+  const char* v = std::getenv("FADECODE_PLAN");
+  return !(v && std::strcmp(v, "stream") == 0);
+}
+
 // FADECODE_KERNEL=simt keeps every plan on the CUDA-core consumer (for
 // comparisons); by default the tensor-core consumer is used where it applies.
 bool tensor_cores_allowed() {
@@ -358,6 +367,31 @@ size_t fa_decode_workspace_size(int batch, int num_qo_heads, int num_kv_heads, i
   return make_layout(max_ctas, segs, cuts, 2 * cuts, G, head_dim, (int64_t)batch + 1).total;
 }
 
+int fa_plan_work_host_heads(const int32_t* indptr, const int32_t* last_page_len, int batch,
+                            int num_kv_heads, int page_size, int max_ctas,
+                            int min_pages_per_cta, int32_t* cta_offsets, int32_t* segments,
+                            int32_t* merge, int* n_ctas, int* n_segments, int* n_merge,
+                            int* n_slots) {
+  if (!cta_offsets || !segments || !merge || !n_ctas || !n_segments || !n_merge || !n_slots)
+    return FA_ERR_INVALID_ARG;
+  WorkList wl;
+  try {
+    if (fadecode::build_work_list(indptr, last_page_len, batch, num_kv_heads, page_size,
+                                  max_ctas, min_pages_per_cta, 0.0, &wl, true) != 0)
+      return FA_ERR_INVALID_ARG;
+  } catch (const std::bad_alloc&) {
+    return FA_ERR_INVALID_ARG;
+  }
+  std::memcpy(cta_offsets, wl.cta_offsets.data(), sizeof(int32_t) * wl.cta_offsets.size());
+  std::memcpy(segments, wl.segments.data(), sizeof(fadecode::Segment) * wl.segments.size());
+  std::memcpy(merge, wl.merge.data(), sizeof(fadecode::MergeUnit) * wl.merge.size());
+  *n_ctas = wl.num_ctas;
+  *n_segments = (int)wl.segments.size();
+  *n_merge = (int)wl.merge.size();
+  *n_slots = wl.num_slots;
+  return FA_OK;
+}
+
 int fa_plan_work_host(const int32_t* indptr, const int32_t* last_page_len, int batch,
                       int num_kv_heads, int page_size, int max_ctas, int min_pages_per_cta,
                       double pool_fraction, int32_t* cta_offsets, int32_t* segments, int32_t* merge, int* n_ctas,
@@ -534,11 +568,13 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
   try {
     // with the run-time pool if its partial states fit the workspace, else
     // static quotas only
-    const double fractions[2] = {pool_fraction(), 0.0};
+    const bool heads = heads_plan() && pool_fraction() == 0.0;
+    const double fractions[2] = {heads ? 0.0 : pool_fraction(), 0.0};
     rc = FA_ERR_WORKSPACE_TOO_SMALL;
     for (double f : fractions) {
       if (fadecode::build_work_list(indptr_host, last_page_len_host, batch, num_kv_heads,
-                                    page_size, sms * occ, kMinPagesPerCta, f, &plan->wl) != 0) {
+                                    page_size, sms * occ, kMinPagesPerCta, f, &plan->wl,
+                                    heads) != 0) {
         rc = FA_ERR_INVALID_ARG;
         break;
       }
@@ -810,7 +846,7 @@ int static_decode(void* scratch, size_t scratch_bytes, const int32_t* indptr_hos
   fw.merge_capacity = kStaticMaxMerge;
   const int prc = build_work_list_fixed(indptr_host, last_page_len_host, batch, num_kv_heads,
                                         page_size, std::min(sms * occ, kStaticMaxCtas),
-                                        kMinPagesPerCta, &fw);
+                                        kMinPagesPerCta, &fw, heads_plan());
   if (prc == -2) return FA_ERR_WORKSPACE_TOO_SMALL;
   if (prc != 0) return FA_ERR_INVALID_ARG;
   const Layout L = make_layout(fw.num_ctas, fw.num_segments, fw.num_merge, fw.num_slots, G,

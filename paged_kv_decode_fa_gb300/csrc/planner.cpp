@@ -236,17 +236,153 @@ int plan_stream(const int32_t* indptr, const int32_t* last_page_len, int batch,
   return 0;
 }
 
+// The plan in groups of num_kv_heads CTAs.  The batch's pages form one
+// stream, request by request (each request preceded by the fixed cost c0);
+// equal quotas of it go to the groups, and within group g CTA g * H + h
+// takes the quota's pages for kv head h.  The group's CTAs therefore stream
+// the same pages at the same time, each its own kv head's rows of them:
+// neighbouring rows of the cache (the heads of one token are adjacent) are
+// read together, which the memory streams markedly faster than rows read
+// far apart in time (one kv head of an E4M3 page is 128-byte rows 1 KB
+// apart).  A request a quota boundary falls inside is cut there for every
+// head alike; its pieces are merged as in plan_stream.  Segments are
+// produced CTA by CTA (group by group, head by head), the merge table
+// first, so that both sinks receive them in order; nothing is allocated.
+template <typename Sink>
+int plan_heads(const int32_t* indptr, const int32_t* last_page_len, int batch,
+               int num_kv_heads, int page_size, int max_ctas, int min_pages_per_cta, Sink& sink,
+               Totals* tot) {
+  if (!indptr || batch < 0 || num_kv_heads <= 0 || page_size <= 0 || max_ctas < num_kv_heads)
+    return -1;
+  if (batch > 0 && !last_page_len) return -1;
+  if (indptr[0] != 0) return -1;
+  const int64_t H = num_kv_heads;
+  int64_t total_tokens = 0, busy = 0;
+  for (int i = 0; i < batch; ++i) {
+    const int64_t np = (int64_t)indptr[i + 1] - indptr[i];
+    if (np < 0) return -1;
+    if (np > 0) {
+      if (last_page_len[i] < 1 || last_page_len[i] > page_size) return -1;
+      total_tokens += (np - 1) * page_size + last_page_len[i];
+      ++busy;
+    }
+  }
+  const int64_t T = indptr[batch];  // pages of one kv head
+  if (min_pages_per_cta < 1) min_pages_per_cta = 1;
+  int64_t groups = max_ctas / H;
+  if (T > 0) groups = std::min<int64_t>(groups, (T + min_pages_per_cta - 1) / min_pages_per_cta);
+  groups = std::max<int64_t>(groups, 1);
+  int64_t c0 = kSegmentCostPages;
+  if ((T + c0 * busy + groups - 1) / groups <= 2 * c0) c0 = 0;
+  const int64_t C = T + c0 * busy;  // stream length in cost positions
+  const int64_t quota = C > 0 ? (C + groups - 1) / groups : 1;
+  if (T > 0) groups = (C - 1) / quota + 1;  // every group holds a page
+  const int64_t n = groups * H;
+  auto group_of = [&](int64_t x) { return std::min(x / quota, groups - 1); };
+  if (!sink.start((int)n, (size_t)batch * num_kv_heads, false)) return -2;
+
+  // merge table: split requests in order, all heads of one request together
+  int slots = 0;
+  {
+    int64_t pos = 0;
+    for (int i = 0; i < batch; ++i) {
+      const int64_t np = (int64_t)indptr[i + 1] - indptr[i];
+      if (np == 0) continue;
+      const int64_t start = pos + c0, end = start + np;
+      pos = end;
+      const int pieces = (int)(group_of(end - 1) - group_of(start) + 1);
+      if (pieces < 2) continue;
+      for (int h = 0; h < num_kv_heads; ++h) {
+        if (!sink.merge(MergeUnit{i, h, slots, pieces})) return -2;
+        slots += pieces;
+      }
+    }
+  }
+
+  // segments, CTA by CTA.  The cursor (i0, its stream position, the split
+  // requests and slots before it) is the first request that may reach into
+  // group g.
+  int i0 = 0;
+  int64_t pos0 = 0, units0 = 0, slots0 = 0;
+  for (int64_t g = 0; g < groups; ++g) {
+    for (int h = 0; h < num_kv_heads; ++h) {
+      int64_t pos = pos0, units = units0, sl = slots0;
+      for (int i = i0; i < batch; ++i) {
+        const int32_t pb = indptr[i];
+        const int64_t np = (int64_t)indptr[i + 1] - pb;
+        if (np == 0) {  // an empty request: one empty segment per head, where it sits
+          const int64_t ge = group_of(pos);
+          if (ge > g) break;
+          if (ge == g && !sink.segment(g * H + h, Segment{i, h, pb, pb, page_size, -1, -1, 0}))
+            return -2;
+          continue;
+        }
+        const int64_t start = pos + c0, end = start + np;
+        const int64_t gs = group_of(start), gz = group_of(end - 1);
+        if (gs > g) break;
+        const int pieces = (int)(gz - gs + 1);
+        if (gz >= g) {
+          const int64_t a = std::max(start, g * quota);
+          const int64_t b = g == groups - 1 ? end : std::min(end, (g + 1) * quota);
+          const int64_t len = (np - 1) * page_size + last_page_len[i];
+          const int k = (int)(g - gs);  // this piece's place among the request's
+          const int unit = pieces > 1 ? (int)(units * H + h) : -1;
+          const int slot = pieces > 1 ? (int)(sl + (int64_t)h * pieces + k) : -1;
+          const Segment sg{i, h, (int32_t)(pb + (a - start)), (int32_t)(pb + (b - start)),
+                           b == end ? last_page_len[i] : page_size, slot, unit,
+                           (int32_t)(len - (a - start) * page_size)};
+          if (!sink.segment(g * H + h, sg)) return -2;
+        }
+        if (pieces > 1) {
+          ++units;
+          sl += (int64_t)pieces * H;
+        }
+        pos = end;
+      }
+    }
+    // move the cursor past the requests that end inside group g
+    const int64_t next = (g + 1) * quota;
+    while (i0 < batch) {
+      const int64_t np = (int64_t)indptr[i0 + 1] - indptr[i0];
+      if (np == 0) {
+        if (group_of(pos0) > g) break;
+        ++i0;
+        continue;
+      }
+      const int64_t start = pos0 + c0, end = start + np;
+      if (end > next) break;
+      if (group_of(end - 1) > group_of(start)) {
+        ++units0;
+        slots0 += (group_of(end - 1) - group_of(start) + 1) * H;
+      }
+      pos0 = end;
+      ++i0;
+    }
+  }
+  sink.finish((int)n);
+  tot->num_ctas = (int)n;
+  tot->num_slots = slots;
+  tot->total_pages = T;
+  tot->total_tokens = total_tokens;
+  tot->pool_pages = 0;
+  return 0;
+}
+
 }  // namespace
 
 int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
                     int batch, int num_kv_heads, int page_size, int max_ctas,
-                    int min_pages_per_cta, double pool_fraction, WorkList* out) {
+                    int min_pages_per_cta, double pool_fraction, WorkList* out, bool heads) {
   if (!out) return -1;
   WorkList wl;
   VectorSink sink{&wl, {}};
   Totals tot;
-  const int rc = plan_stream(indptr, last_page_len, batch, num_kv_heads, page_size, max_ctas,
-                             min_pages_per_cta, pool_fraction, sink, &tot);
+  const int rc =
+      heads && pool_fraction == 0.0 && max_ctas >= num_kv_heads
+          ? plan_heads(indptr, last_page_len, batch, num_kv_heads, page_size, max_ctas,
+                       min_pages_per_cta, sink, &tot)
+          : plan_stream(indptr, last_page_len, batch, num_kv_heads, page_size, max_ctas,
+                        min_pages_per_cta, pool_fraction, sink, &tot);
   if (rc != 0) return -1;
   wl.num_ctas = tot.num_ctas;
   wl.num_slots = tot.num_slots;
@@ -259,12 +395,15 @@ int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
 
 int build_work_list_fixed(const int32_t* indptr, const int32_t* last_page_len, int batch,
                           int num_kv_heads, int page_size, int max_ctas, int min_pages_per_cta,
-                          FixedWorkList* out) {
+                          FixedWorkList* out, bool heads) {
   if (!out || !out->cta_offsets || !out->segments || !out->merge) return -1;
   FixedSink sink{out};
   Totals tot;
-  const int rc = plan_stream(indptr, last_page_len, batch, num_kv_heads, page_size, max_ctas,
-                             min_pages_per_cta, 0.0, sink, &tot);
+  const int rc = heads && max_ctas >= num_kv_heads
+                     ? plan_heads(indptr, last_page_len, batch, num_kv_heads, page_size,
+                                  max_ctas, min_pages_per_cta, sink, &tot)
+                     : plan_stream(indptr, last_page_len, batch, num_kv_heads, page_size,
+                                   max_ctas, min_pages_per_cta, 0.0, sink, &tot);
   if (rc != 0) return rc;
   out->num_ctas = tot.num_ctas;
   out->num_slots = tot.num_slots;

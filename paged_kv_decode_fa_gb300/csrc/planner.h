@@ -64,9 +64,14 @@ struct WorkList {
 
 // Returns 0 on success, -1 for malformed input (see fa_decode.h).
 // pool_fraction in [0, 1): share of the page stream left to the pool.
+// heads: plan the grid in groups of num_kv_heads CTAs that take the same
+// share of the page stream, one kv head each (plan_heads in planner.cpp),
+// instead of cutting the stream of (request, kv head) units; applies only
+// without a pool and with at least num_kv_heads CTAs.
 int build_work_list(const int32_t* indptr, const int32_t* last_page_len,
                     int batch, int num_kv_heads, int page_size, int max_ctas,
-                    int min_pages_per_cta, double pool_fraction, WorkList* out);
+                    int min_pages_per_cta, double pool_fraction, WorkList* out,
+                    bool heads = false);
 
 // The same plan without a pool, written into arrays the caller owns (no
 // allocation): cta_offsets[cta_capacity + 1], segments[segment_capacity],
@@ -83,6 +88,6 @@ struct FixedWorkList {
 // Returns 0, -1 for malformed input, -2 when a plan does not fit the arrays.
 int build_work_list_fixed(const int32_t* indptr, const int32_t* last_page_len, int batch,
                           int num_kv_heads, int page_size, int max_ctas, int min_pages_per_cta,
-                          FixedWorkList* out);
+                          FixedWorkList* out, bool heads = false);
 
 }  // namespace fadecode

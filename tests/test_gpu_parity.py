@@ -205,6 +205,49 @@ def test_run_time_pool(lib, cuda, monkeypatch, case):
             rel=TOKEN_SCALE_REL if path == "token_scales" else 0.0)
 
 
+@pytest.mark.parametrize("kind", ["bf16-g4", "e4m3-g8", "ragged-q", "mha"])
+def test_both_plan_kinds(lib, cuda, monkeypatch, kind):
+    """The head-grouped plan (default) and the stream plan
+    (FADECODE_PLAN=stream) over the same batch: both against the oracle,
+    both with exact coverage, and within the output dtype's rounding of
+    each other (their split pieces differ, so their sums run in other
+    orders)."""
+    lengths = [3000, 17, 0, 900, 1, 12000, 260, 48]
+    if kind == "ragged-q":
+        b = W.make_ragged_q_batch(batch_lengths=lengths, q_counts=[2, 1, 0, 4, 1, 3, 4, 2],
+                                  num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                                  q_dtype=torch.bfloat16, kv_dtype=torch.float8_e4m3fn,
+                                  seed=61, device=cuda)
+    else:
+        hq, hkv, kv_dt = {"bf16-g4": (32, 8, torch.bfloat16), "e4m3-g8": (64, 8,
+                          torch.float8_e4m3fn), "mha": (16, 16, torch.bfloat16)}[kind]
+        b = W.make_batch(batch_lengths=lengths, num_qo_heads=hq, num_kv_heads=hkv,
+                         head_dim=128, q_dtype=torch.bfloat16, kv_dtype=kv_dt, seed=62,
+                         device=cuda)
+    runner = run_ragged if kind == "ragged-q" else run_lib
+    outs = {}
+    for mode in ("heads", "stream"):
+        if mode == "stream":
+            monkeypatch.setenv("FADECODE_PLAN", "stream")
+        else:
+            monkeypatch.delenv("FADECODE_PLAN", raising=False)
+        p, o, lse = runner(lib, b)
+        assert p.check() == 0 and p.info["num_merge_units"] > 0
+        check_coverage(p, b)
+        outs[mode] = (o, lse)
+        if mode == "heads":
+            _, seg, _ = p.work()
+            cta = p.work()[0]
+            H = b.num_kv_heads
+            for c in range(len(cta) - 1):   # CTA c serves kv head c % num_kv_heads
+                assert np.all(seg[cta[c]:cta[c + 1], 1] == c % H)
+    ref_o, ref_lse = oracle_decode(b)
+    for o, lse in outs.values():
+        compare(o, lse, ref_o, ref_lse, tol_for(b))
+    diff = (outs["heads"][0].float() - outs["stream"][0].float()).abs().max().item()
+    assert diff <= 2 ** -6
+
+
 def _short_lengths(seed):
     rng = np.random.default_rng(seed)
     lengths = rng.integers(0, 49, size=2500)

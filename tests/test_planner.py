@@ -315,3 +315,103 @@ def test_token_coverage_catches_planted_mistakes(lib):
     bad = seg.copy(); bad[long_, 2] += 1                         # a page dropped
     with pytest.raises(AssertionError):
         assert_token_coverage(bad, indptr, last, 2)
+
+
+# ---------------------------------------------------------------- head-grouped plans
+
+def expected_group_pages(indptr, Hkv, max_ctas, min_pages):
+    """Pages each group of the head-grouped plan holds (for each kv head):
+    the batch's pages in request order, a fixed cost before every non-empty
+    request, cut into equal quotas of cost positions, one per group."""
+    np_req = np.diff(np.asarray(indptr, np.int64))
+    T = int(np_req.sum())
+    groups = max(1, min(max_ctas // Hkv, -(-T // min_pages) if T else max_ctas // Hkv))
+    busy = int((np_req > 0).sum())
+    c0 = SEG_COST
+    if -(-(T + c0 * busy) // groups) <= 2 * c0:
+        c0 = 0
+    C = T + c0 * busy
+    quota = -(-C // groups) if C else 1
+    if T:
+        groups = (C - 1) // quota + 1
+    length = np_req + c0 * (np_req > 0)
+    first = np.cumsum(length) - np_req
+    pos = np.repeat(first, np_req) + (np.arange(T) - np.repeat(np.cumsum(np_req) - np_req, np_req))
+    return np.bincount(np.minimum(pos // quota, groups - 1), minlength=groups), groups
+
+
+def check_heads_work(lib, indptr, last, Hkv, max_ctas, min_pages=8, P=16):
+    cta, seg, mer, n_slots = lib.plan_work_host(indptr, last, Hkv, P, max_ctas, min_pages,
+                                                heads=True)
+    if max_ctas < Hkv:   # not one group: the stream plan
+        ref = lib.plan_work_host(indptr, last, Hkv, P, max_ctas, min_pages)
+        for x, y in zip(ref[:3], (cta, seg, mer)):
+            np.testing.assert_array_equal(x, y)
+        return cta, seg, mer, n_slots
+    indptr = np.asarray(indptr, np.int64)
+    n = len(cta) - 1
+    # coverage, bit-exact, pages and tokens
+    np.testing.assert_array_equal(expand(seg), oracle.expected_coverage(indptr, Hkv))
+    assert_token_coverage(seg, indptr, last, Hkv, P)
+    assert cta[0] == 0 and cta[-1] == len(seg) and np.all(np.diff(cta) >= 0)
+    want, groups = expected_group_pages(indptr, Hkv, max_ctas, min_pages)
+    assert n == groups * Hkv <= max_ctas
+    for c in range(n):
+        s = seg[cta[c]:cta[c + 1]]
+        assert np.all(s[:, 1] == c % Hkv)                     # one kv head per CTA
+        assert (s[:, 3] - s[:, 2]).sum() == want[c // Hkv]    # its group's share of pages
+        if c % Hkv:                                           # the group's CTAs: same pieces
+            first = seg[cta[c - c % Hkv]:cta[c - c % Hkv + 1]]
+            np.testing.assert_array_equal(np.delete(s, [1, 5, 6], 1),
+                                          np.delete(first, [1, 5, 6], 1))
+    if int(indptr[-1]):
+        assert np.all(want > 0)                               # every group holds pages
+    # last_valid and to_end as the kernels read them
+    for s in seg:
+        r, pe = s[0], s[3]
+        if s[2] < pe:
+            assert s[4] == (last[r] if pe == indptr[r + 1] else P)
+            length = (indptr[r + 1] - indptr[r] - 1) * P + last[r]
+            assert s[7] == length - (s[2] - indptr[r]) * P
+    # split units: contiguous slots in page order, every slot used once
+    seen = []
+    for u, (r, h, s0, ns) in enumerate(mer):
+        pieces = seg[(seg[:, 0] == r) & (seg[:, 1] == h)]
+        pieces = pieces[np.argsort(pieces[:, 2])]
+        assert len(pieces) == ns >= 2
+        assert list(pieces[:, 5]) == list(range(s0, s0 + ns)) and np.all(pieces[:, 6] == u)
+        assert np.all(pieces[1:, 2] == pieces[:-1, 3])
+        seen += list(range(s0, s0 + ns))
+    assert sorted(seen) == list(range(n_slots))
+    for r, h in seg[seg[:, 5] < 0][:, :2]:
+        assert ((seg[:, 0] == r) & (seg[:, 1] == h)).sum() == 1
+    assert n_slots <= 2 * n
+    return cta, seg, mer, n_slots
+
+
+@pytest.mark.parametrize("name", list(W.CONFIGS))
+def test_heads_plan_named_workloads(lib, name):
+    cfg = W.CONFIGS[name]
+    indptr, last = _table(W.draw_lengths(cfg, torch.Generator().manual_seed(cfg.seed)))
+    for max_ctas in (152 * 4, 152 * 3, 9, cfg.num_kv_heads):
+        check_heads_work(lib, indptr, last, cfg.num_kv_heads, max_ctas)
+
+
+def test_heads_plan_random_batches(lib):
+    rng = np.random.default_rng(21)
+    for _ in range(60):
+        B = int(rng.integers(1, 40))
+        lengths = rng.integers(0, 900, size=B)
+        lengths[rng.random(B) < 0.15] = 0
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        indptr, last = _table(lengths)
+        check_heads_work(lib, indptr, last, Hkv, int(rng.integers(Hkv, 500)),
+                         int(rng.integers(1, 20)))
+
+
+def test_heads_plan_edge_batches(lib):
+    check_heads_work(lib, *_table([0, 0, 0]), 2, 100)
+    check_heads_work(lib, *_table([0, 5, 0, 0]), 4, 100)
+    check_heads_work(lib, *_table([1]), 1, 100)
+    check_heads_work(lib, *_table([65536]), 32, 456)      # one long request over 14 groups
+    check_heads_work(lib, *_table([100, 900]), 8, 4)       # fewer CTAs than kv heads
