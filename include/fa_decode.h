@@ -100,7 +100,11 @@ size_t fa_decode_workspace_size(int batch, int num_qo_heads, int num_kv_heads,
  *
  * Per request, len = (pages - 1) * page_size + last_page_len.  Every
  * (request, kv head, page) is assigned to exactly one chunk of the work list;
- * fa_decode_plan_get_work exposes that list for inspection.
+ * fa_decode_plan_get_work exposes that list for inspection.  The grid is
+ * planned in groups of num_kv_heads CTAs that take equal shares of the page
+ * stream, one kv head each (fa_plan_work_host_heads shows the same plan on
+ * the host); FADECODE_PLAN=stream in the environment selects the plan of
+ * fa_plan_work_host instead.
  * Errors: FA_ERR_INVALID_ARG for a malformed indptr or last_page_len, NULL
  * pointers or non-positive sizes; FA_ERR_UNSUPPORTED for shapes or types that
  * are not built; FA_ERR_WORKSPACE_TOO_SMALL; FA_ERR_CUDA. */
