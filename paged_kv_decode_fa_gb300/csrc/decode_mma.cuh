@@ -196,6 +196,9 @@ constexpr float kUmAboveF16 = 15.f, kUmBelowF16 = 8.f;
 // the largest weight of a column is at least 1, so the weights that the
 // f16 conversion flushes (below 2^-24) weigh nothing next to it.
 constexpr float kLazyAbove = 8.f;
+// E4M3 page split: load a page's V fragments into registers right after its
+// scores and release the stage then, instead of after P.V.
+constexpr bool kEarlyVRelease = true;
 
 template <typename QT, typename KVT, int D, int G, int NW, bool TS, int QL, bool UM,
           bool RQ = false>
@@ -400,7 +403,19 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
     // the copy engine, which refills it for a later page as soon as this
     // warp releases it.  Each fragment register holds two consecutive
     // tokens (low half 2t, high half 2t+1; +8 for the upper token block).
-    auto pv_step = [&](auto masked, uint32_t st, uint32_t pb0, uint32_t pb1, int valid) {
+    // E4M3 V fragments of one page, as loaded (four 8x8 matrices of byte
+    // pairs per 16 dims x 16 tokens, transposed by ldmatrix)
+    auto load_v_fp8 = [&](uint32_t st, uint32_t (&vf)[MTILES / 2][4]) {
+#pragma unroll
+      for (int c2 = 0; c2 < MTILES / 2; ++c2) {
+        const int mi = lane >> 3, r = lane & 7;
+        const int gran = 2 * c2 + (mi >> 1), tok = (mi & 1) * 8 + r;
+        mma::ldsm_x4_trans(st + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16), vf[c2][0],
+                           vf[c2][1], vf[c2][2], vf[c2][3]);
+      }
+    };
+    auto pv_step = [&](auto masked, uint32_t st, uint32_t pb0, uint32_t pb1, int valid,
+                       const uint32_t* vf_loaded = nullptr) {
       constexpr bool kMask = decltype(masked)::value;
       uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
       if constexpr (kMask) {
@@ -408,12 +423,18 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
         vmask_hi = (2 * t + 8 < valid ? 0x0000ffffu : 0u) | (2 * t + 9 < valid ? 0xffff0000u : 0u);
       }
       if constexpr (kFp8) {
+        uint32_t vf[MTILES / 2][4];
+        if (vf_loaded) {
+#pragma unroll
+          for (int c2 = 0; c2 < MTILES / 2; ++c2)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) vf[c2][e] = vf_loaded[4 * c2 + e];
+        } else {
+          load_v_fp8(st, vf);
+        }
 #pragma unroll
         for (int c2 = 0; c2 < MTILES / 2; ++c2) {
-          const int mi = lane >> 3, r = lane & 7;
-          const int gran = 2 * c2 + (mi >> 1), tok = (mi & 1) * 8 + r;
-          uint32_t d0, d1, d2, d3;
-          mma::ldsm_x4_trans(st + (P + tok) * 128 + ((gran ^ (tok & 7)) * 16), d0, d1, d2, d3);
+          uint32_t d0 = vf[c2][0], d1 = vf[c2][1], d2 = vf[c2][2], d3 = vf[c2][3];
           // matrices 0 and 2 hold tokens 2t, 2t+1; 1 and 3 tokens 2t+8, 2t+9
           if constexpr (kMask) {
             d0 &= vmask_lo;
@@ -541,6 +562,19 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
         }
       }
 
+      // E4M3 page split: V's fragments go to registers now and the stage goes
+      // back to the copy engine before the softmax, so the ring holds a page
+      // only while its bytes are read (16 registers a page)
+      constexpr bool kEarlyV = kFp8 && !CS && kEarlyVRelease;
+      uint32_t vfrag[kEarlyV ? NPP : 1][MTILES / 2][4];
+      if constexpr (kEarlyV) {
+#pragma unroll
+        for (int u = 0; u < NPP; ++u) {
+          load_v_fp8(st[u], vfrag[u]);
+          dev::release_stage(dev::smem_addr(&empty[stage[u]]), lane);
+        }
+      }
+
       // ---- softmax for heads 2t (s[.][0], s[.][2]) and 2t+1 (s[.][1], s[.][3])
       // The weights use a reference per column that moves only rarely, so a
       // step needs no column reduction - only a vote on whether some lane's
@@ -630,11 +664,12 @@ __global__ void __launch_bounds__(MmaCfg<QT, KVT, D, G, NW, TS, QL>::THREADS,
         const uint16_t* pu = pT + u * 8 * P;
         const uint32_t pb0 = *reinterpret_cast<const uint32_t*>(pu + g * P + 2 * t);
         const uint32_t pb1 = *reinterpret_cast<const uint32_t*>(pu + g * P + 2 * t + 8);
+        const uint32_t* vf = kEarlyV ? &vfrag[kEarlyV ? u : 0][0][0] : nullptr;
         if (valid[u] < P)
-          pv_step(std::true_type{}, st[u], pb0, pb1, valid[u]);
+          pv_step(std::true_type{}, st[u], pb0, pb1, valid[u], vf);
         else
-          pv_step(std::false_type{}, st[u], pb0, pb1, valid[u]);
-        dev::release_stage(dev::smem_addr(&empty[stage[u]]), lane);
+          pv_step(std::false_type{}, st[u], pb0, pb1, valid[u], vf);
+        if constexpr (!kEarlyV) dev::release_stage(dev::smem_addr(&empty[stage[u]]), lane);
       }
     };
 
