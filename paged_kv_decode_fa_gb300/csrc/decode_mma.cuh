@@ -20,14 +20,24 @@
 //    permuted so that these are exactly the lane's A-fragment elements, and
 //    q's B fragment (held in registers for the whole segment) uses the same
 //    permutation; E4M3 K is widened to f16 in registers;
-//  - softmax on the C fragment (tokens g, g+8 x heads 2t, 2t+1): column max
-//    over the 8 lanes of a column with three shuffles per page (none with the
-//    unified max, which only votes); each lane keeps its own share of the
-//    denominator, summed over the column once per segment;
+//  - softmax on the C fragment (tokens g, g+8 x heads 2t, 2t+1): weights
+//    against a per-column reference that moves only when a page's maximum
+//    passes it by more than 2^8 (or against a caller's static bound, the
+//    unified max), so a page costs one warp vote; the column reduction (three
+//    shuffles) and the exact rescale of the state run only when it moves;
+//    each lane keeps its own share of the denominator, summed over the column
+//    once per segment;
 //  - P.V: P is rounded to the MMA type, transposed through a 256-byte
 //    per-warp buffer into B fragments, V^T fragments come straight from the
 //    stage with ldmatrix.trans (for E4M3, pairs of bytes are transposed as
-//    16-bit elements and split with one byte permute).
+//    16-bit elements and split with one byte permute; the page split loads
+//    them right after the scores and hands the stage back before the
+//    softmax).
+//
+// Up to 8 columns (query heads x query tokens) the warps split the pages
+// (page k to warp k % NW).  With more, each warp owns 8 columns and takes
+// every page of the segment (the column split), several pages a step so that
+// their independent loads and MMA chains overlap.
 #pragma once
 #include <type_traits>
 
