@@ -97,8 +97,10 @@ NOT_DECODE_SOURCES = ("cascade.cu", "cascade_tc.cuh", "static_scratch.cu", "merg
 
 
 def kernel_source_hash(workload: str = "gqa_uniform") -> str:
-    """Hash of the sources a workload's kernels are built and launched from
-    (a profile summary is current while this hash matches)."""
+    """Hash of the code a workload's kernels are built and launched from,
+    comments and layout left out (a profile summary is current while this
+    hash matches: a changed comment changes no kernel)."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_fa_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
@@ -106,8 +108,12 @@ def kernel_source_hash(workload: str = "gqa_uniform") -> str:
             continue
         if workload != "cascade" and fn in NOT_DECODE_SOURCES:
             continue
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(fn.encode() + f.read())
+        with open(os.path.join(csrc, fn), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        text = " ".join(text.split())
+        h.update(fn.encode() + text.encode())
     return h.hexdigest()[:16]
 
 
