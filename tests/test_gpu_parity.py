@@ -205,6 +205,22 @@ def test_run_time_pool(lib, cuda, monkeypatch, case):
             rel=TOKEN_SCALE_REL if path == "token_scales" else 0.0)
 
 
+@pytest.mark.parametrize("hq,hkv,kv_dtype", [(12, 3, torch.bfloat16), (40, 5, torch.float8_e4m3fn),
+                                          (6, 3, torch.bfloat16)],
+                         ids=["3-kv-heads", "5-kv-heads-e4m3", "3-kv-heads-g2"])
+def test_head_groups_of_odd_size(lib, cuda, hq, hkv, kv_dtype):
+    """Head-grouped plans whose groups do not divide the grid evenly (3 or 5
+    kv heads): every row against the oracle, exact coverage."""
+    b = W.make_batch(batch_lengths=[5000, 33, 0, 1200, 16, 777, 2], num_qo_heads=hq,
+                     num_kv_heads=hkv, head_dim=128, q_dtype=torch.bfloat16, kv_dtype=kv_dtype,
+                     seed=hq + hkv, device=cuda)
+    p, o, lse = run_lib(lib, b)
+    assert p.check() == 0 and p.info["num_ctas"] % hkv == 0
+    check_coverage(p, b)
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, tol_for(b))
+
+
 @pytest.mark.parametrize("kind", ["bf16-g4", "e4m3-g8", "ragged-q", "mha"])
 def test_both_plan_kinds(lib, cuda, monkeypatch, kind):
     """The head-grouped plan (default) and the stream plan

@@ -403,7 +403,7 @@ def test_heads_plan_random_batches(lib):
         B = int(rng.integers(1, 40))
         lengths = rng.integers(0, 900, size=B)
         lengths[rng.random(B) < 0.15] = 0
-        Hkv = int(rng.choice([1, 2, 4, 8]))
+        Hkv = int(rng.choice([1, 2, 3, 4, 5, 8]))
         indptr, last = _table(lengths)
         check_heads_work(lib, indptr, last, Hkv, int(rng.integers(Hkv, 500)),
                          int(rng.integers(1, 20)))
