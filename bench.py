@@ -535,6 +535,20 @@ def plan_batch(fa, b: W.DecodeBatch, idx=None, ws=None):
                    kv_data_type=b.paged_kv.dtype, workspace=ws)
 
 
+def launches_per_run(p) -> int:
+    """Kernel launches one run of a plan makes: one decode launch, two for a
+    ragged plan in two buckets, and with the separate merge kernel one more
+    after each decode launch that has split requests to fold."""
+    info = p.info
+    nb = info.get("bucket_ctas", 0)
+    n = 2 if nb > 0 else 1
+    if info["num_merge_units"] > 0 and not info["fused_merge"]:
+        cta, seg, _ = p.work()
+        first_b = int(cta[info["num_ctas"] - nb]) if nb > 0 else len(seg)
+        n += int((seg[:first_b, 6] >= 0).any()) + int((seg[first_b:, 6] >= 0).any())
+    return n
+
+
 def workspace_bytes(fa, b: W.DecodeBatch) -> int:
     """Workspace bound of the batch's plan kind."""
     G = b.num_qo_heads // b.num_kv_heads
@@ -595,7 +609,7 @@ def measure_other(args, world, dev, name: str) -> dict:
     torch.cuda.synchronize(dev)
     if p.check() != 0:
         raise RuntimeError(f"device check flagged the {name} batch")
-    launches = 1 + (1 if info["num_merge_units"] > 0 and not info["fused_merge"] else 0)
+    launches = launches_per_run(p)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(dev.index).start()
     time.sleep(0.05)
@@ -626,7 +640,8 @@ def measure_other(args, world, dev, name: str) -> dict:
                                 else "fa_decode_split_kernel"),
                      "algorithmic_bytes_per_launch": alg, "duration_us": step_s * 1e6,
                      "duration_from": ("timed-region events / launches" if launches == 1 else
-                                       "timed-region events / steps (decode + merge kernel)")},
+                                       f"timed-region events / steps ({launches} launches a "
+                                       "step: decode buckets and merge kernels)")},
         "steps": steps, "warmup": warmup, "gpu_launches": steps * launches,
         "clocks": clocks.summary(t0, t1),
     }
@@ -687,11 +702,10 @@ def bench_ours(args, world, rank, local):
     if um_bound is not None:
         p.unified_max_fallbacks()  # clear the warm-up count
 
-    launches_per_step = 1 + (1 if info["num_merge_units"] > 0 and not info["fused_merge"] else 0)
+    launches_per_step = launches_per_run(p)
     # The timed region: the production step back to back, nothing recorded
     # between launches (an event pair around every launch adds its own
-    # records and keeps the next launch from being prepared while the
-    # kernel drains: about 4 us per step).
+    # records between the kernels).
     clocks = ClockSampler(local).start()
     time.sleep(0.3)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -163,8 +163,12 @@ int fa_decode_plan_multi_token(const int32_t* indptr_host,
  * (BF16, BF16) or (BF16, E4M3), groups 1, 2, 4, 8 with
  * group x max_i n_i <= 32 (group 8: up to 4 query tokens per request).
  * Up to 8 columns (group x n) the consumer warps split a segment's pages; with
- * more, each warp owns 8 columns and reads every page.  Errors as
- * fa_decode_plan; FA_ERR_UNSUPPORTED for shapes beyond those. */
+ * more, each warp owns 8 columns and reads every page.  A batch that mixes
+ * both kinds of request is planned in two buckets, launched one after the
+ * other by fa_decode_run: the requests of more than 8 columns on the
+ * column-split kernel, the others on the 8-column kernel (fa_plan_info
+ * bucket_ctas; FADECODE_BUCKETS=0 in the environment plans one launch).
+ * Errors as fa_decode_plan; FA_ERR_UNSUPPORTED for shapes beyond those. */
 int fa_decode_plan_ragged_q(const int32_t* indptr_host, const int32_t* indices_dev,
                             const int32_t* last_page_len_host,
                             const int32_t* qo_indptr_host, int batch,
@@ -325,6 +329,9 @@ typedef struct {
   int64_t pool_pages;         /* (page, kv head) pairs in those segments */
   int ragged_q;               /* 1: query rows per request from qo_indptr */
   int64_t total_q_rows;       /* query rows of q / o (batch * q_len unless ragged) */
+  int bucket_ctas;            /* ragged plans in two buckets: CTAs of the second launch,
+                                 the last bucket_ctas of num_ctas (0: one launch) */
+  int bucket_q_len;           /* query tokens per request its kernel holds (0: none) */
 } fa_plan_info;
 
 int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info);
@@ -396,8 +403,9 @@ int fa_decode_check(fa_decode_plan_t plan, void* cuda_stream, int* flags);
 
 /* Optional timing hook: when both events are non-NULL, later fa_decode_run
  * calls record ev_before on the stream just before the split-KV decode kernel
- * and ev_after just after it (events are cudaEvent_t passed as void*, created
- * by the caller).  Pass NULLs to turn the hook off. */
+ * and ev_after just after it (both launches of a ragged plan in two buckets
+ * lie between them; events are cudaEvent_t passed as void*, created by the
+ * caller).  Pass NULLs to turn the hook off. */
 int fa_decode_set_timing_events(fa_decode_plan_t plan, void* ev_before,
                                 void* ev_after);
 

@@ -66,7 +66,8 @@ class PlanInfo(ctypes.Structure):
         ("tensor_cores", ctypes.c_int), ("fused_merge", ctypes.c_int), ("q_len", ctypes.c_int),
         ("unified_max", ctypes.c_int), ("num_pool_segments", ctypes.c_int),
         ("pool_pages", ctypes.c_int64), ("ragged_q", ctypes.c_int),
-        ("total_q_rows", ctypes.c_int64)]
+        ("total_q_rows", ctypes.c_int64), ("bucket_ctas", ctypes.c_int),
+        ("bucket_q_len", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -405,7 +406,8 @@ class DecodePlan:
         return int(flags.value)
 
     def set_timing_events(self, before, after) -> None:
-        """Record torch.cuda.Events around the decode kernel of later runs (None = off).
+        """Record torch.cuda.Events around the decode kernel of later runs (both
+        launches of a ragged plan in two buckets; None = off).
 
         torch creates an event lazily at its first record, so record each
         event once from torch before handing it over."""

@@ -102,6 +102,13 @@ bool heads_plan() {
 
 // FADECODE_KERNEL=simt keeps every plan on the CUDA-core consumer (for
 // comparisons); by default the tensor-core consumer is used where it applies.
+// FADECODE_BUCKETS=0 plans a ragged batch on the one kernel its widest
+// request needs, instead of two buckets (for comparisons).
+bool buckets_enabled() {
+  const char* v = std::getenv("FADECODE_BUCKETS");
+  return !(v && std::strcmp(v, "0") == 0);
+}
+
 bool tensor_cores_allowed() {
   const char* v = std::getenv("FADECODE_KERNEL");
   return !(v && std::strcmp(v, "simt") == 0);
@@ -206,6 +213,43 @@ bool find_token_scale_kernel(fa_dtype q, fa_dtype kv, int D, int G, DecodeKernel
   return false;
 }
 
+// Whether a decode launch of `func` on `st` may be a programmatic dependent
+// of the stream's previous kernel, and record it as the stream's last decode
+// kernel.  The decode kernels let the next launch in at their start
+// (griddepcontrol.launch_dependents), so a dependent launch's CTAs are
+// placed on SMs that the previous launch's CTAs are still leaving.  Behind
+// the same kernel each takes the slot of one that left.  Behind a decode
+// kernel of another shape the launch ran up to half as long again (the
+// E4M3 column split: 365 us alone, about 540 us right behind an 8-column
+// launch), the mark of a persistent grid whose CTAs did not all fit at
+// once: placed among departing CTAs of another size, they leave some SMs
+// with fewer than the grid was sized for.  So only a launch of the same
+// kernel as the stream's last decode launch is a dependent one; a stream
+// not seen before (or dropped from the table) gets an ordinary launch.
+// Kernels that do not let the next launch in early leave every SM empty
+// before a dependent launch's CTAs are placed, whatever the table says.
+bool dependent_launch_ok(cudaStream_t st, const void* func) {
+  struct Entry {
+    cudaStream_t stream;
+    const void* func;
+  };
+  constexpr int kEntries = 64;  // streams remembered; the oldest entry is reused
+  static std::mutex mu;
+  static Entry table[kEntries];
+  static int used = 0, next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i) {
+    if (table[i].stream != st) continue;
+    const bool same = table[i].func == func;
+    table[i].func = func;
+    return same;
+  }
+  const int slot = used < kEntries ? used++ : next;
+  if (used == kEntries) next = (slot + 1) % kEntries;
+  table[slot] = Entry{st, func};
+  return false;
+}
+
 // Set a kernel's shared-memory limit and return how many of its CTAs fit on
 // one SM (0 on failure).  Cached per (kernel, device): a plan per decode
 // step should not pay for these queries every time.
@@ -293,6 +337,8 @@ struct LaunchView {
   uint8_t* ws = nullptr;
   Layout layout{};
   int num_ctas = 0, num_merge = 0, pool_begin = 0, pool_count = 0;
+  // this launch's first CTA entry and first merge unit in the plan's tables
+  int cta_first = 0, merge_first = 0;
   bool fused_merge = true;
   bool ragged_q = false;  // query rows per request from the plan's qo_indptr copy
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
@@ -335,6 +381,14 @@ struct fa_decode_plan_s {
   int64_t total_q = 0;    // query rows of the batch
   // cached TMA descriptors of the KV cache, one per kernel variant
   MapCache map[kNumVariants];
+  // A bucketed ragged plan: CTAs [0, ctas_a) run kern[kPlain] (the column
+  // split) over the requests with more rows than one 8-column tile holds,
+  // CTAs [ctas_a, wl.num_ctas) run kern_b (pages split over the warps) over
+  // the rest; merge units [0, merges_a) belong to the first launch.
+  bool bucketed = false;
+  DecodeKernel kern_b;
+  MapCache map_b;
+  int ctas_a = 0, merges_a = 0;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
 };
 
@@ -485,6 +539,106 @@ size_t fa_decode_workspace_size_ragged_q(int batch, int num_qo_heads, int num_kv
 
 }  // extern "C"
 
+namespace {
+
+// The requests of a ragged batch on one side of a query-row threshold, as a
+// batch of their own: indptr and last_page_len compacted, and each one's id
+// in the whole batch.
+struct SubBatch {
+  std::vector<int32_t> indptr{0}, last, ids;
+};
+
+void take_requests(const int32_t* indptr, const int32_t* last, const int32_t* qo, int batch,
+                   int max_rows, bool at_most, SubBatch* s) {
+  for (int i = 0; i < batch; ++i) {
+    if ((qo[i + 1] - qo[i] <= max_rows) != at_most) continue;
+    s->ids.push_back(i);
+    s->indptr.push_back(s->indptr.back() + (indptr[i + 1] - indptr[i]));
+    s->last.push_back(last[i]);
+  }
+}
+
+// Append the work list of a sub-batch to `out`: its CTAs after out's, its
+// requests and page positions mapped back to the whole batch, its merge
+// units numbered after out's, its partial slots from slot_base on.
+void append_work(const WorkList& w, const SubBatch& s, const int32_t* indptr, int64_t slot_base,
+                 WorkList* out) {
+  const int32_t seg0 = (int32_t)out->segments.size(), m0 = (int32_t)out->merge.size();
+  if (out->cta_offsets.empty()) out->cta_offsets.push_back(0);
+  for (int c = 1; c <= w.num_ctas; ++c) out->cta_offsets.push_back(seg0 + w.cta_offsets[c]);
+  for (fadecode::Segment sg : w.segments) {
+    const int32_t shift = indptr[s.ids[sg.request]] - s.indptr[sg.request];
+    sg.request = s.ids[sg.request];
+    sg.page_begin += shift;
+    sg.page_end += shift;
+    if (sg.merge_unit >= 0) sg.merge_unit += m0;
+    if (sg.out_slot >= 0) sg.out_slot += (int32_t)slot_base;
+    out->segments.push_back(sg);
+  }
+  for (fadecode::MergeUnit m : w.merge) {
+    m.request = s.ids[m.request];
+    m.first_slot += (int32_t)slot_base;
+    out->merge.push_back(m);
+  }
+  out->num_ctas += w.num_ctas;
+  out->total_pages += w.total_pages;
+  out->total_tokens += w.total_tokens;
+}
+
+// Two buckets for a ragged batch planned on a column-split kernel (more
+// than 8 columns): that kernel's warps each take every page of a request
+// for 8 columns of their own, so a request whose rows fit one 8-column
+// tile keeps three of its four warps idle while the CTA streams its pages.
+// Such requests go to the ragged kernel of at most 8 columns instead, whose
+// warps split the pages, in a launch of its own after the column split's.
+// Both grids take the whole GPU in turn.  The partial slots of the second
+// bucket follow the first's, in units of its smaller slot.  Returns false
+// (and leaves the plan alone) when the batch has a single bucket, no such
+// kernel is built or the plan does not fit the workspace.
+bool plan_buckets(fa_decode_plan_s* plan, const int32_t* indptr, const int32_t* last,
+                  const int32_t* qo, int batch, int sms, int occ, size_t workspace_bytes) {
+  const int G = plan->group;
+  const int ql_a = plan->kern[kPlain].q_len;
+  if (G * ql_a <= 8 || 8 % G != 0) return false;
+  const int small_rows = 8 / G;
+  DecodeKernel kb;
+  if (!find_ragged_q_kernel(plan->q_dtype, plan->kv_dtype, plan->d, G, small_rows, &kb) ||
+      G * kb.q_len > 8 || ql_a % kb.q_len != 0)
+    return false;
+  const int occ_b = std::min(kernel_occupancy(kb), kMaxCtasPerSmBound);
+  if (occ_b <= 0) return false;
+  SubBatch sa, sb;
+  take_requests(indptr, last, qo, batch, small_rows, false, &sa);
+  take_requests(indptr, last, qo, batch, small_rows, true, &sb);
+  if (sa.ids.empty() || sb.ids.empty()) return false;
+  const bool heads = heads_plan();
+  WorkList wa, wb;
+  if (fadecode::build_work_list(sa.indptr.data(), sa.last.data(), (int)sa.ids.size(),
+                                plan->hkv, plan->page_size, sms * occ, kMinPagesPerCta, 0.0,
+                                &wa, heads) != 0 ||
+      fadecode::build_work_list(sb.indptr.data(), sb.last.data(), (int)sb.ids.size(),
+                                plan->hkv, plan->page_size, sms * occ_b, kMinPagesPerCta, 0.0,
+                                &wb, heads) != 0)
+    return false;
+  const int ratio = ql_a / kb.q_len;  // slot size of the first bucket over the second's
+  WorkList w;
+  append_work(wa, sa, indptr, 0, &w);
+  append_work(wb, sb, indptr, (int64_t)ratio * wa.num_slots, &w);
+  w.num_slots = wa.num_slots + (wb.num_slots + ratio - 1) / ratio;
+  const Layout L = make_layout(w.num_ctas, (int64_t)w.segments.size(), (int64_t)w.merge.size(),
+                               w.num_slots, G * ql_a, plan->d, (int64_t)batch + 1);
+  if (L.total > workspace_bytes) return false;
+  plan->wl = std::move(w);
+  plan->layout = L;
+  plan->bucketed = true;
+  plan->kern_b = kb;
+  plan->ctas_a = wa.num_ctas;
+  plan->merges_a = (int)wa.merge.size();
+  return true;
+}
+
+}  // namespace
+
 static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
                      const int32_t* last_page_len_host, int batch, int q_len, int num_qo_heads,
                      int num_kv_heads, int head_dim, int page_size, fa_dtype q_dtype,
@@ -566,12 +720,16 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
 
   int rc = FA_OK;
   try {
+    const bool buckets = ragged && buckets_enabled() && pool_fraction() == 0.0 &&
+                         plan_buckets(plan, indptr_host, last_page_len_host, qo_indptr_host,
+                                      batch, sms, occ, workspace_bytes);
     // with the run-time pool if its partial states fit the workspace, else
     // static quotas only
     const bool heads = heads_plan() && pool_fraction() == 0.0;
     const double fractions[2] = {heads ? 0.0 : pool_fraction(), 0.0};
-    rc = FA_ERR_WORKSPACE_TOO_SMALL;
+    rc = buckets ? FA_OK : FA_ERR_WORKSPACE_TOO_SMALL;
     for (double f : fractions) {
+      if (buckets) break;
       if (fadecode::build_work_list(indptr_host, last_page_len_host, batch, num_kv_heads,
                                     page_size, sms * occ, kMinPagesPerCta, f, &plan->wl,
                                     heads) != 0) {
@@ -728,6 +886,8 @@ int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info) {
   i.unified_max = plan->has[kUnifiedMax] ? 1 : 0;
   i.num_pool_segments = plan->wl.pool_count();
   i.pool_pages = plan->wl.pool_pages;
+  i.bucket_ctas = plan->bucketed ? plan->wl.num_ctas - plan->ctas_a : 0;
+  i.bucket_q_len = plan->bucketed ? plan->kern_b.q_len : 0;
   *info = i;
   return FA_OK;
 }
@@ -917,8 +1077,37 @@ static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
   lv.ragged_q = plan->ragged_q;
   lv.ev_before = plan->ev_before;
   lv.ev_after = plan->ev_after;
-  return launch_decode(lv, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, k_scales,
-                       v_scales, max_bound, o, lse, cuda_stream, head_k_scales, head_v_scales);
+  if (!plan->bucketed)
+    return launch_decode(lv, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, k_scales,
+                         v_scales, max_bound, o, lse, cuda_stream, head_k_scales,
+                         head_v_scales);
+  // two launches, the column split's bucket first; the timing events (if
+  // set) bracket both
+  if (variant != kPlain) return FA_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const bool timed = plan->ev_before && plan->ev_after;
+  if (plan->batch > 0 && timed && cudaEventRecord(plan->ev_before, st) != cudaSuccess)
+    return FA_ERR_CUDA;
+  lv.ev_before = lv.ev_after = nullptr;
+  lv.num_ctas = plan->ctas_a;
+  lv.num_merge = plan->merges_a;
+  int rc = launch_decode(lv, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, k_scales,
+                         v_scales, max_bound, o, lse, cuda_stream, head_k_scales, head_v_scales);
+  if (rc != FA_OK) return rc;
+  LaunchView lb = lv;
+  lb.kern = &plan->kern_b;
+  lb.map = &plan->map_b;
+  lb.q_len = plan->kern_b.q_len;
+  lb.cta_first = plan->ctas_a;
+  lb.num_ctas = plan->wl.num_ctas - plan->ctas_a;
+  lb.merge_first = plan->merges_a;
+  lb.num_merge = (int)plan->wl.merge.size() - plan->merges_a;
+  rc = launch_decode(lb, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, k_scales, v_scales,
+                     max_bound, o, lse, cuda_stream, head_k_scales, head_v_scales);
+  if (rc != FA_OK) return rc;
+  if (plan->batch > 0 && timed && cudaEventRecord(plan->ev_after, st) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
 }
 
 namespace {
@@ -949,7 +1138,7 @@ int launch_decode(const LaunchView& lv, const void* q, const void* paged_kv, int
   prm.o = o;
   prm.lse = lse;
   prm.indices = lv.indices;
-  prm.cta_offsets = reinterpret_cast<const int32_t*>(ws + L.off_cta);
+  prm.cta_offsets = reinterpret_cast<const int32_t*>(ws + L.off_cta) + lv.cta_first;
   prm.segments = reinterpret_cast<const int32_t*>(ws + L.off_seg);
   prm.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
   prm.part_lse = reinterpret_cast<float*>(ws + L.off_part_lse);
@@ -981,9 +1170,11 @@ int launch_decode(const LaunchView& lv, const void* q, const void* paged_kv, int
   const bool timed = lv.ev_before && lv.ev_after;
   if (timed && cudaEventRecord(lv.ev_before, st) != cudaSuccess) return FA_ERR_CUDA;
   void* args[2] = {&mc.tmap, &prm};
-  // A programmatic dependent launch: the kernel's CTAs may be placed while
-  // the previous kernel in the stream drains; they read nothing global
-  // before it has completed (griddepcontrol.wait).
+  // A programmatic dependent launch where the stream's previous decode
+  // launch was this kernel: its CTAs may then be placed while that launch
+  // drains, each in a slot one of its CTAs left; they read nothing global
+  // before it has completed (griddepcontrol.wait).  After another decode
+  // kernel, an ordinary launch (see dependent_launch_ok).
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(lv.num_ctas);
   cfg.blockDim = dim3(kern.threads);
@@ -993,12 +1184,13 @@ int launch_decode(const LaunchView& lv, const void* q, const void* paged_kv, int
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = dependent_launch_ok(st, kern.func) ? 1 : 0;
   if (cudaLaunchKernelExC(&cfg, kern.func, args) != cudaSuccess) return FA_ERR_CUDA;
   if (timed && cudaEventRecord(lv.ev_after, st) != cudaSuccess) return FA_ERR_CUDA;
   if (!lv.fused_merge && lv.num_merge > 0) {
     MergeParams mp;
-    mp.merge = reinterpret_cast<const int32_t*>(ws + L.off_merge);
+    mp.merge = reinterpret_cast<const int32_t*>(ws + L.off_merge) +
+               (size_t)lv.merge_first * FA_MERGE_INTS;
     mp.qo_indptr = prm.qo_indptr;
     mp.part_o = prm.part_o;
     mp.part_lse = prm.part_lse;

@@ -386,12 +386,11 @@ def test_stream_handle_is_current_stream(lib, cuda):
 
 
 def test_dependent_launch_chain(lib, cuda):
-    """Decode launches are programmatic dependents of the kernel before them
-    in the stream.  Here each second launch decodes with q = the output of
-    the launch just before it (nothing in between, fresh q for the first
-    launch every round): it must read that q only once the first launch
-    has completed, so its result equals the oracle on the first launch's
-    actual output, round after round."""
+    """Back-to-back decode launches in one stream, each second one decoding
+    with q = the output of the launch just before it (nothing in between,
+    fresh q for the first launch every round): it must read that q only
+    once the first launch has completed, so its result equals the oracle on
+    the first launch's actual output, round after round."""
     import dataclasses
     b = W.make_batch(batch_lengths=[3000, 17, 900, 5000, 64, 2048], num_qo_heads=16,
                      num_kv_heads=4, head_dim=128, q_dtype=torch.bfloat16,
@@ -417,6 +416,42 @@ def test_dependent_launch_chain(lib, cuda):
         ref2 = oracle_decode(dataclasses.replace(b, q=o1s[k]))
         compare(o1s[k], l1s[k], ref1[0], ref1[1], TOL[torch.bfloat16])
         compare(o2s[k], l2s[k], ref2[0], ref2[1], TOL[torch.bfloat16])
+
+
+def test_alternating_kernels_in_one_stream(lib, cuda):
+    """Plans of different decode kernels launched in turn on one stream (a
+    16-bit and an E4M3 page split, a ragged plan in two buckets; the
+    library chains only launches of the same kernel as dependents): every
+    run bitwise equal to the same plan run on its own, and the second plan
+    reading q from the first's output sees it complete."""
+    import dataclasses
+    ba = W.make_batch(batch_lengths=[3000, 17, 900, 5000], num_qo_heads=16, num_kv_heads=2,
+                      head_dim=128, q_dtype=torch.bfloat16, kv_dtype=torch.bfloat16, seed=191,
+                      device=cuda)
+    bb = W.make_batch(batch_lengths=[700, 4000, 1, 2500], num_qo_heads=16, num_kv_heads=2,
+                      head_dim=128, q_dtype=torch.bfloat16, kv_dtype=torch.float8_e4m3fn,
+                      seed=192, device=cuda)
+    br = W.make_ragged_q_batch(batch_lengths=[3000, 40, 2500, 5000], q_counts=[1, 4, 2, 1],
+                               num_qo_heads=16, num_kv_heads=2, head_dim=128,
+                               q_dtype=torch.bfloat16, kv_dtype=torch.float8_e4m3fn, seed=193,
+                               device=cuda)
+    pa, oa, la = run_lib(lib, ba)
+    pb, ob, lb = run_lib(lib, bb)
+    pr, orr, lr = run_ragged(lib, br)
+    assert pr.info["bucket_ctas"] > 0
+    ob2 = torch.empty_like(ob)
+    lb2 = torch.empty_like(lb)
+    for _ in range(3):
+        xa, ya = pa.run(ba.q, ba.paged_kv)
+        xb, yb = pb.run(oa, bb.paged_kv, k_scale=bb.k_scale, v_scale=bb.v_scale, out=ob2,
+                        lse=lb2)
+        xr, yr = pr.run(br.q, br.paged_kv, k_scale=br.k_scale, v_scale=br.v_scale)
+        torch.cuda.synchronize()
+        assert torch.equal(xa, oa) and torch.equal(ya, la)
+        assert torch.equal(xr, orr) and torch.equal(yr, lr)
+    ref = oracle_decode(dataclasses.replace(bb, q=oa))
+    compare(ob2, lb2, ref[0], ref[1], tol_for(bb))
+    assert pa.check() == 0 and pb.check() == 0 and pr.check() == 0
 
 
 @pytest.mark.parametrize("merge", ["fused", "kernel"])
@@ -721,6 +756,66 @@ def test_ragged_q_small(lib, cuda, kv_dtype, group, max_q):
     o2, lse2 = p.run(b.q, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale)
     torch.cuda.synchronize()
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+@pytest.mark.parametrize("merge", ["fused", "kernel"])
+@pytest.mark.parametrize("kv_dtype", [torch.bfloat16, torch.float8_e4m3fn], ids=["bf16", "e4m3"])
+@pytest.mark.parametrize("group,max_q", [(8, 4), (4, 5), (2, 12), (1, 20)])
+def test_ragged_q_buckets(lib, cuda, monkeypatch, kv_dtype, group, max_q, merge):
+    """A batch that mixes requests of at most 8 columns (group x query
+    rows) with wider ones is planned in two buckets: the wide requests on
+    the column-split kernel, the others, in a second launch, on the
+    8-column kernel.  Both buckets hold split requests, whose partial states
+    share the workspace.  Every row against the oracle; the work list covers
+    every page once; each bucket holds only its own requests; the buckets'
+    partial states do not overlap; a one-launch plan (FADECODE_BUCKETS=0)
+    gives the same rows within the bound; a rerun is bitwise the same; the
+    plan's timing events bracket both launches."""
+    if merge == "kernel":
+        monkeypatch.setenv("FADECODE_MERGE", "kernel")
+    else:
+        monkeypatch.delenv("FADECODE_MERGE", raising=False)
+    monkeypatch.delenv("FADECODE_BUCKETS", raising=False)
+    small = 8 // group
+    lengths = [3000, 40, 2500, 17, 1000, 611, 5000, 9, 250, 4100]
+    counts = [small, max_q, max(1, small // 2), 0, small + 1, max_q, small, 1, max_q, small]
+    b = W.make_ragged_q_batch(batch_lengths=lengths, q_counts=counts, num_qo_heads=2 * group,
+                              num_kv_heads=2, head_dim=128, q_dtype=torch.bfloat16,
+                              kv_dtype=kv_dtype, seed=300 + group + max_q, device=cuda)
+    p, o, lse = run_ragged(lib, b)
+    info = p.info
+    assert info["bucket_ctas"] > 0 and group * info["bucket_q_len"] <= 8 < group * info["q_len"]
+    assert p.check() == 0
+    check_coverage(p, b)
+    cta, seg, _ = p.work()
+    first_b = int(cta[info["num_ctas"] - info["bucket_ctas"]])
+    rows = np.diff(np.asarray(b.extra["qo_indptr"]))
+    assert np.all(rows[seg[:first_b, 0]] * group > 8)
+    assert np.all(rows[seg[first_b:, 0]] * group <= 8)
+    assert (seg[:first_b, 6] >= 0).any() and (seg[first_b:, 6] >= 0).any()
+    # partial states in floats per row: slot x columns of the bucket's kernel
+    cols = [group * info["q_len"] if k < first_b else group * info["bucket_q_len"]
+            for k in range(len(seg))]
+    spans = sorted((int(s[5]) * c, (int(s[5]) + 1) * c) for s, c in zip(seg, cols) if s[5] >= 0)
+    assert all(a[1] <= z[0] for a, z in zip(spans, spans[1:]))
+    assert spans[-1][1] <= info["num_partial_slots"] * group * info["q_len"]
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, tol_for(b))
+    o2, lse2 = p.run(b.q, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    ev1.record()
+    p.set_timing_events(ev0, ev1)
+    p.run(b.q, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale, out=o2, lse=lse2)
+    p.set_timing_events(None, None)
+    torch.cuda.synchronize()
+    assert ev0.elapsed_time(ev1) > 0 and torch.equal(o, o2)
+    monkeypatch.setenv("FADECODE_BUCKETS", "0")
+    p1, o1, lse1 = run_ragged(lib, b)
+    assert p1.info["bucket_ctas"] == 0 and p1.check() == 0
+    compare(o1, lse1, ref_o, ref_lse, tol_for(b))
 
 
 def test_ragged_q_one_token_each_is_decode(lib, cuda):
