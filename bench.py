@@ -536,16 +536,18 @@ def plan_batch(fa, b: W.DecodeBatch, idx=None, ws=None):
 
 
 def launches_per_run(p) -> int:
-    """Kernel launches one run of a plan makes: one decode launch, two for a
-    ragged plan in two buckets, and with the separate merge kernel one more
-    after each decode launch that has split requests to fold."""
+    """Kernel launches one run of a plan makes: one decode launch per bucket
+    (one, or up to four for a ragged plan), and with the separate merge
+    kernel one more after each decode launch that has split requests to
+    fold."""
     info = p.info
-    nb = info.get("bucket_ctas", 0)
-    n = 2 if nb > 0 else 1
+    nb = info.get("num_buckets", 1)
+    n = nb
     if info["num_merge_units"] > 0 and not info["fused_merge"]:
         cta, seg, _ = p.work()
-        first_b = int(cta[info["num_ctas"] - nb]) if nb > 0 else len(seg)
-        n += int((seg[:first_b, 6] >= 0).any()) + int((seg[first_b:, 6] >= 0).any())
+        first = list(info["bucket_first_cta"][:nb]) + [info["num_ctas"]]
+        for b in range(nb):
+            n += int((seg[cta[first[b]]:cta[first[b + 1]], 6] >= 0).any())
     return n
 
 

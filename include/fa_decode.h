@@ -163,11 +163,14 @@ int fa_decode_plan_multi_token(const int32_t* indptr_host,
  * (BF16, BF16) or (BF16, E4M3), groups 1, 2, 4, 8 with
  * group x max_i n_i <= 32 (group 8: up to 4 query tokens per request).
  * Up to 8 columns (group x n) the consumer warps split a segment's pages; with
- * more, each warp owns 8 columns and reads every page.  A batch that mixes
- * both kinds of request is planned in two buckets, launched one after the
- * other by fa_decode_run: the requests of more than 8 columns on the
- * column-split kernel, the others on the 8-column kernel (fa_plan_info
- * bucket_ctas; FADECODE_BUCKETS=0 in the environment plans one launch).
+ * more, each warp owns 8 columns and reads every page, on a kernel of as
+ * many warps as the batch's widest request has 8-column tiles
+ * (t = ceil(group x n_i / 8): 2, 3 or 4).  With E4M3 KV the requests of one
+ * tile take a launch of their own on the 8-column kernel when they hold
+ * enough work; fa_decode_run then makes both launches, one after the other
+ * (fa_plan_info num_buckets, bucket_first_cta, bucket_q_len; in the
+ * environment FADECODE_BUCKETS=0 plans one launch of the max_q kernel,
+ * FADECODE_BUCKETS=all a launch for every tile count present).
  * Errors as fa_decode_plan; FA_ERR_UNSUPPORTED for shapes beyond those. */
 int fa_decode_plan_ragged_q(const int32_t* indptr_host, const int32_t* indices_dev,
                             const int32_t* last_page_len_host,
@@ -329,9 +332,12 @@ typedef struct {
   int64_t pool_pages;         /* (page, kv head) pairs in those segments */
   int ragged_q;               /* 1: query rows per request from qo_indptr */
   int64_t total_q_rows;       /* query rows of q / o (batch * q_len unless ragged) */
-  int bucket_ctas;            /* ragged plans in two buckets: CTAs of the second launch,
-                                 the last bucket_ctas of num_ctas (0: one launch) */
-  int bucket_q_len;           /* query tokens per request its kernel holds (0: none) */
+  int num_buckets;            /* decode launches per run: 1, or more for a ragged plan in
+                                 buckets by 8-column tiles (fa_decode_plan_ragged_q) */
+  int bucket_first_cta[4];    /* launch b runs CTAs bucket_first_cta[b] up to the next
+                                 launch's first (num_ctas for the last); -1 unused */
+  int bucket_q_len[4];        /* query tokens per request launch b's kernel holds
+                                 (group x bucket_q_len[b] columns); 0 unused */
 } fa_plan_info;
 
 int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info);

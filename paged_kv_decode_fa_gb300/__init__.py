@@ -66,11 +66,15 @@ class PlanInfo(ctypes.Structure):
         ("tensor_cores", ctypes.c_int), ("fused_merge", ctypes.c_int), ("q_len", ctypes.c_int),
         ("unified_max", ctypes.c_int), ("num_pool_segments", ctypes.c_int),
         ("pool_pages", ctypes.c_int64), ("ragged_q", ctypes.c_int),
-        ("total_q_rows", ctypes.c_int64), ("bucket_ctas", ctypes.c_int),
-        ("bucket_q_len", ctypes.c_int)]
+        ("total_q_rows", ctypes.c_int64), ("num_buckets", ctypes.c_int),
+        ("bucket_first_cta", ctypes.c_int * 4), ("bucket_q_len", ctypes.c_int * 4)]
 
     def as_dict(self) -> dict:
-        return {n: getattr(self, n) for n, _ in self._fields_}
+        out = {}
+        for n, _ in self._fields_:
+            v = getattr(self, n)
+            out[n] = list(v) if isinstance(v, ctypes.Array) else v
+        return out
 
 
 class LibraryStats(ctypes.Structure):

@@ -26,6 +26,12 @@ namespace {
 
 constexpr int kMinPagesPerCta = 8;     // smallest chunk worth a CTA of its own
 constexpr int kMaxCtasPerSmBound = 4;  // grid bound (every kernel fits 3 or 4 CTAs per SM)
+// Ragged plans in buckets (plan_buckets): at most one launch per number of
+// 8-column tiles (1-4) a request needs; the one-tile requests of an E4M3
+// batch take a launch of their own from kMinBucketUnitsPerSm (page, kv head)
+// pairs per SM on (below that a launch's fixed time outweighs the gain).
+constexpr int kMaxBuckets = 4;
+constexpr int kMinBucketUnitsPerSm = 64;
 // Share of the page stream balanced at run time.  Off: on a GB300 the
 // static quotas already finish within a few percent of each other in
 // back-to-back launches, and the pool's extra pieces cost more than it saves
@@ -102,11 +108,16 @@ bool heads_plan() {
 
 // FADECODE_KERNEL=simt keeps every plan on the CUDA-core consumer (for
 // comparisons); by default the tensor-core consumer is used where it applies.
-// FADECODE_BUCKETS=0 plans a ragged batch on the one kernel its widest
-// request needs, instead of two buckets (for comparisons).
-bool buckets_enabled() {
+// Ragged plans in buckets by 8-column tiles (plan_buckets): FADECODE_BUCKETS=0
+// plans a ragged batch on the one kernel its max_q needs (for comparisons);
+// FADECODE_BUCKETS=all gives every tile count present a launch of its own,
+// however little work it holds (for tests of every bucket kernel).
+enum class BucketMode { kOff, kDefault, kAll };
+BucketMode bucket_mode() {
   const char* v = std::getenv("FADECODE_BUCKETS");
-  return !(v && std::strcmp(v, "0") == 0);
+  if (v && std::strcmp(v, "0") == 0) return BucketMode::kOff;
+  if (v && std::strcmp(v, "all") == 0) return BucketMode::kAll;
+  return BucketMode::kDefault;
 }
 
 bool tensor_cores_allowed() {
@@ -192,6 +203,19 @@ bool find_ragged_q_kernel(fa_dtype q, fa_dtype kv, int D, int G, int max_q, Deco
   if (!tensor_cores_allowed() || q != FA_DTYPE_BF16) return false;
   if (kv == FA_DTYPE_BF16) return fadecode::find_ragged_q_kernel_bf16(D, G, max_q, k);
   if (kv == FA_DTYPE_E4M3) return fadecode::find_ragged_q_kernel_bf16_e4m3(D, G, max_q, k);
+  return false;
+}
+
+// The ragged kernel for requests of `tiles` 8-column tiles (1-4): the
+// 8-column kernel (pages split over its warps) for one, a column split of
+// `tiles` warps otherwise.
+bool find_ragged_tiles_kernel(fa_dtype q, fa_dtype kv, int D, int G, int tiles, DecodeKernel* k) {
+  if (G < 1 || 8 % G != 0 || tiles < 1 || tiles > 4) return false;
+  if (tiles == 1 || tiles == 4)
+    return find_ragged_q_kernel(q, kv, D, G, 8 * tiles / G, k) && k->q_len * G == 8 * tiles;
+  if (!tensor_cores_allowed() || q != FA_DTYPE_BF16) return false;
+  if (kv == FA_DTYPE_BF16) return fadecode::find_ragged_q_tiles_kernel_bf16(D, G, tiles, k);
+  if (kv == FA_DTYPE_E4M3) return fadecode::find_ragged_q_tiles_kernel_bf16_e4m3(D, G, tiles, k);
   return false;
 }
 
@@ -381,14 +405,17 @@ struct fa_decode_plan_s {
   int64_t total_q = 0;    // query rows of the batch
   // cached TMA descriptors of the KV cache, one per kernel variant
   MapCache map[kNumVariants];
-  // A bucketed ragged plan: CTAs [0, ctas_a) run kern[kPlain] (the column
-  // split) over the requests with more rows than one 8-column tile holds,
-  // CTAs [ctas_a, wl.num_ctas) run kern_b (pages split over the warps) over
-  // the rest; merge units [0, merges_a) belong to the first launch.
-  bool bucketed = false;
-  DecodeKernel kern_b;
-  MapCache map_b;
-  int ctas_a = 0, merges_a = 0;
+  // A ragged plan in buckets (plan_buckets): launch b runs bucket[b].kern
+  // over CTAs [cta_first, cta_first + num_ctas) of the work list and owns
+  // merge units [merge_first, merge_first + num_merge).  0: one launch of
+  // kern[variant] over the whole work list.
+  struct Bucket {
+    DecodeKernel kern;
+    MapCache map;
+    int tiles = 0, cta_first = 0, num_ctas = 0, merge_first = 0, num_merge = 0;
+  };
+  int num_buckets = 0;
+  Bucket bucket[kMaxBuckets];
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
 };
 
@@ -541,22 +568,16 @@ size_t fa_decode_workspace_size_ragged_q(int batch, int num_qo_heads, int num_kv
 
 namespace {
 
-// The requests of a ragged batch on one side of a query-row threshold, as a
-// batch of their own: indptr and last_page_len compacted, and each one's id
-// in the whole batch.
+// Requests of a ragged batch as a batch of their own: indptr and
+// last_page_len compacted, and each one's id in the whole batch.
 struct SubBatch {
   std::vector<int32_t> indptr{0}, last, ids;
-};
-
-void take_requests(const int32_t* indptr, const int32_t* last, const int32_t* qo, int batch,
-                   int max_rows, bool at_most, SubBatch* s) {
-  for (int i = 0; i < batch; ++i) {
-    if ((qo[i + 1] - qo[i] <= max_rows) != at_most) continue;
-    s->ids.push_back(i);
-    s->indptr.push_back(s->indptr.back() + (indptr[i + 1] - indptr[i]));
-    s->last.push_back(last[i]);
+  void add(const int32_t* indptr_all, const int32_t* last_all, int i) {
+    ids.push_back(i);
+    indptr.push_back(indptr.back() + (indptr_all[i + 1] - indptr_all[i]));
+    last.push_back(last_all[i]);
   }
-}
+};
 
 // Append the work list of a sub-batch to `out`: its CTAs after out's, its
 // requests and page positions mapped back to the whole batch, its merge
@@ -585,55 +606,102 @@ void append_work(const WorkList& w, const SubBatch& s, const int32_t* indptr, in
   out->total_tokens += w.total_tokens;
 }
 
-// Two buckets for a ragged batch planned on a column-split kernel (more
-// than 8 columns): that kernel's warps each take every page of a request
-// for 8 columns of their own, so a request whose rows fit one 8-column
-// tile keeps three of its four warps idle while the CTA streams its pages.
-// Such requests go to the ragged kernel of at most 8 columns instead, whose
-// warps split the pages, in a launch of its own after the column split's.
-// Both grids take the whole GPU in turn.  The partial slots of the second
-// bucket follow the first's, in units of its smaller slot.  Returns false
-// (and leaves the plan alone) when the batch has a single bucket, no such
-// kernel is built or the plan does not fit the workspace.
+// Buckets for a ragged batch whose widest request takes the column split
+// (more than 8 columns).  Request i needs t_i = ceil(G x n_i / 8) 8-column
+// tiles (1 for n_i = 0).  A column split's warps each take every page of a
+// request for 8 columns of their own, so the batch runs on the column split
+// of as many warps as its widest request has tiles - two or three warps a
+// CTA leave room for five or four CTAs per SM (a batch of 2 or 3 tiles a
+// request: -15 % on an E4M3 cache, -2 to -6 % on a 16-bit one, against
+// four warps).  With E4M3 KV the column split is bound by its arithmetic,
+// and a CTA streams pages at the same rate however many of its warps have
+// columns, so the requests of one tile take a launch of their own on the
+// 8-column kernel (pages split over its warps) when they hold enough work
+// to outweigh a launch's fixed time (spec_decode_ragged: 449 -> 413 us).
+// A 16-bit column split streams near the copy rate already, and the
+// 8-column kernel is no faster on those requests.  Buckets run one after
+// the other, widest first, each grid over the whole GPU.  Partial states:
+// each bucket's slots follow the previous bucket's columns, in units of its
+// own slot (G x its q_len columns).  Returns false (and leaves the plan
+// alone) when one launch of the plan's own kernel is what remains, a kernel
+// is not built or the plan does not fit the workspace.
 bool plan_buckets(fa_decode_plan_s* plan, const int32_t* indptr, const int32_t* last,
-                  const int32_t* qo, int batch, int sms, int occ, size_t workspace_bytes) {
+                  const int32_t* qo, int batch, int sms, size_t workspace_bytes,
+                  BucketMode mode) {
   const int G = plan->group;
-  const int ql_a = plan->kern[kPlain].q_len;
-  if (G * ql_a <= 8 || 8 % G != 0) return false;
-  const int small_rows = 8 / G;
-  DecodeKernel kb;
-  if (!find_ragged_q_kernel(plan->q_dtype, plan->kv_dtype, plan->d, G, small_rows, &kb) ||
-      G * kb.q_len > 8 || ql_a % kb.q_len != 0)
-    return false;
-  const int occ_b = std::min(kernel_occupancy(kb), kMaxCtasPerSmBound);
-  if (occ_b <= 0) return false;
-  SubBatch sa, sb;
-  take_requests(indptr, last, qo, batch, small_rows, false, &sa);
-  take_requests(indptr, last, qo, batch, small_rows, true, &sb);
-  if (sa.ids.empty() || sb.ids.empty()) return false;
+  const int nc_max = G * plan->kern[kPlain].q_len;
+  if (nc_max <= 8 || nc_max % 8 != 0 || nc_max / 8 > kMaxBuckets) return false;
+  const int widest = nc_max / 8;
+  auto tiles_of = [&](int i) { return std::max(1, (G * (qo[i + 1] - qo[i]) + 7) / 8); };
+  int64_t units[kMaxBuckets + 1] = {0};
+  int count[kMaxBuckets + 1] = {0};
+  for (int i = 0; i < batch; ++i) {
+    const int t = tiles_of(i);
+    if (t > widest) return false;
+    units[t] += (int64_t)(indptr[i + 1] - indptr[i]) * plan->hkv;
+    ++count[t];
+  }
+  int top = 0;  // the widest tile count present
+  for (int t = 1; t <= widest; ++t)
+    if (count[t] > 0) top = t;
+  // where each tile count goes: its own launch, or the widest one's
+  int dest[kMaxBuckets + 1];
+  for (int t = 1; t <= widest; ++t) {
+    const bool own = mode == BucketMode::kAll ||
+                     (t == 1 && plan->kv_dtype == FA_DTYPE_E4M3 &&
+                      units[1] >= (int64_t)kMinBucketUnitsPerSm * sms);
+    dest[t] = own ? t : top;
+  }
+  int order[kMaxBuckets], nb = 0;
+  for (int t = widest; t >= 1; --t) {
+    bool used = false;
+    for (int u = 1; u <= widest; ++u) used = used || (count[u] > 0 && dest[u] == t);
+    if (used) order[nb++] = t;
+  }
+  if (nb == 0 || (nb == 1 && order[0] == widest)) return false;
+
+  fa_decode_plan_s::Bucket bk[kMaxBuckets];
+  SubBatch sub[kMaxBuckets];
+  for (int b = 0; b < nb; ++b) {
+    bk[b].tiles = order[b];
+    if (!find_ragged_tiles_kernel(plan->q_dtype, plan->kv_dtype, plan->d, G, order[b],
+                                  &bk[b].kern))
+      return false;
+  }
+  for (int i = 0; i < batch; ++i) {
+    const int t = dest[tiles_of(i)];
+    for (int b = 0; b < nb; ++b)
+      if (order[b] == t) sub[b].add(indptr, last, i);
+  }
   const bool heads = heads_plan();
-  WorkList wa, wb;
-  if (fadecode::build_work_list(sa.indptr.data(), sa.last.data(), (int)sa.ids.size(),
-                                plan->hkv, plan->page_size, sms * occ, kMinPagesPerCta, 0.0,
-                                &wa, heads) != 0 ||
-      fadecode::build_work_list(sb.indptr.data(), sb.last.data(), (int)sb.ids.size(),
-                                plan->hkv, plan->page_size, sms * occ_b, kMinPagesPerCta, 0.0,
-                                &wb, heads) != 0)
-    return false;
-  const int ratio = ql_a / kb.q_len;  // slot size of the first bucket over the second's
   WorkList w;
-  append_work(wa, sa, indptr, 0, &w);
-  append_work(wb, sb, indptr, (int64_t)ratio * wa.num_slots, &w);
-  w.num_slots = wa.num_slots + (wb.num_slots + ratio - 1) / ratio;
+  int64_t cols = 0;  // partial-state columns taken by the buckets so far
+  for (int b = 0; b < nb; ++b) {
+    const int occ = std::min(kernel_occupancy(bk[b].kern), 8);
+    if (occ <= 0) return false;
+    WorkList wb;
+    if (fadecode::build_work_list(sub[b].indptr.data(), sub[b].last.data(),
+                                  (int)sub[b].ids.size(), plan->hkv, plan->page_size, sms * occ,
+                                  kMinPagesPerCta, 0.0, &wb, heads) != 0)
+      return false;
+    const int nc = G * bk[b].kern.q_len;
+    const int64_t slot_base = (cols + nc - 1) / nc;
+    bk[b].cta_first = w.num_ctas;
+    bk[b].num_ctas = wb.num_ctas;
+    bk[b].merge_first = (int)w.merge.size();
+    bk[b].num_merge = (int)wb.merge.size();
+    append_work(wb, sub[b], indptr, slot_base, &w);
+    cols = (slot_base + wb.num_slots) * nc;
+  }
+  if (cols > INT32_MAX) return false;
+  w.num_slots = (int)((cols + nc_max - 1) / nc_max);
   const Layout L = make_layout(w.num_ctas, (int64_t)w.segments.size(), (int64_t)w.merge.size(),
-                               w.num_slots, G * ql_a, plan->d, (int64_t)batch + 1);
+                               w.num_slots, nc_max, plan->d, (int64_t)batch + 1);
   if (L.total > workspace_bytes) return false;
   plan->wl = std::move(w);
   plan->layout = L;
-  plan->bucketed = true;
-  plan->kern_b = kb;
-  plan->ctas_a = wa.num_ctas;
-  plan->merges_a = (int)wa.merge.size();
+  plan->num_buckets = nb;
+  for (int b = 0; b < nb; ++b) plan->bucket[b] = bk[b];
   return true;
 }
 
@@ -720,9 +788,10 @@ static int plan_impl(const int32_t* indptr_host, const int32_t* indices_dev,
 
   int rc = FA_OK;
   try {
-    const bool buckets = ragged && buckets_enabled() && pool_fraction() == 0.0 &&
+    const BucketMode bm = bucket_mode();
+    const bool buckets = ragged && bm != BucketMode::kOff && pool_fraction() == 0.0 &&
                          plan_buckets(plan, indptr_host, last_page_len_host, qo_indptr_host,
-                                      batch, sms, occ, workspace_bytes);
+                                      batch, sms, workspace_bytes, bm);
     // with the run-time pool if its partial states fit the workspace, else
     // static quotas only
     const bool heads = heads_plan() && pool_fraction() == 0.0;
@@ -886,8 +955,12 @@ int fa_decode_plan_get_info(fa_decode_plan_t plan, fa_plan_info* info) {
   i.unified_max = plan->has[kUnifiedMax] ? 1 : 0;
   i.num_pool_segments = plan->wl.pool_count();
   i.pool_pages = plan->wl.pool_pages;
-  i.bucket_ctas = plan->bucketed ? plan->wl.num_ctas - plan->ctas_a : 0;
-  i.bucket_q_len = plan->bucketed ? plan->kern_b.q_len : 0;
+  i.num_buckets = plan->num_buckets > 0 ? plan->num_buckets : 1;
+  for (int b = 0; b < kMaxBuckets; ++b) {
+    i.bucket_first_cta[b] = b < plan->num_buckets ? plan->bucket[b].cta_first : (b ? -1 : 0);
+    i.bucket_q_len[b] = b < plan->num_buckets ? plan->bucket[b].kern.q_len
+                                              : (b ? 0 : plan->q_len);
+  }
   *info = i;
   return FA_OK;
 }
@@ -1077,36 +1150,31 @@ static int run_impl(fa_decode_plan_s* plan, Variant variant, const void* q,
   lv.ragged_q = plan->ragged_q;
   lv.ev_before = plan->ev_before;
   lv.ev_after = plan->ev_after;
-  if (!plan->bucketed)
+  if (plan->num_buckets == 0)
     return launch_decode(lv, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, k_scales,
                          v_scales, max_bound, o, lse, cuda_stream, head_k_scales,
                          head_v_scales);
-  // two launches, the column split's bucket first; the timing events (if
-  // set) bracket both
+  // one launch per bucket, in order; the timing events (if set) bracket all
   if (variant != kPlain) return FA_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  const bool timed = plan->ev_before && plan->ev_after;
-  if (plan->batch > 0 && timed && cudaEventRecord(plan->ev_before, st) != cudaSuccess)
-    return FA_ERR_CUDA;
+  const bool timed = plan->batch > 0 && plan->ev_before && plan->ev_after;
+  if (timed && cudaEventRecord(plan->ev_before, st) != cudaSuccess) return FA_ERR_CUDA;
   lv.ev_before = lv.ev_after = nullptr;
-  lv.num_ctas = plan->ctas_a;
-  lv.num_merge = plan->merges_a;
-  int rc = launch_decode(lv, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, k_scales,
-                         v_scales, max_bound, o, lse, cuda_stream, head_k_scales, head_v_scales);
-  if (rc != FA_OK) return rc;
-  LaunchView lb = lv;
-  lb.kern = &plan->kern_b;
-  lb.map = &plan->map_b;
-  lb.q_len = plan->kern_b.q_len;
-  lb.cta_first = plan->ctas_a;
-  lb.num_ctas = plan->wl.num_ctas - plan->ctas_a;
-  lb.merge_first = plan->merges_a;
-  lb.num_merge = (int)plan->wl.merge.size() - plan->merges_a;
-  rc = launch_decode(lb, q, paged_kv, num_pages, sm_scale, k_scale, v_scale, k_scales, v_scales,
-                     max_bound, o, lse, cuda_stream, head_k_scales, head_v_scales);
-  if (rc != FA_OK) return rc;
-  if (plan->batch > 0 && timed && cudaEventRecord(plan->ev_after, st) != cudaSuccess)
-    return FA_ERR_CUDA;
+  for (int b = 0; b < plan->num_buckets; ++b) {
+    fa_decode_plan_s::Bucket& bk = plan->bucket[b];
+    lv.kern = &bk.kern;
+    lv.map = &bk.map;
+    lv.q_len = bk.kern.q_len;
+    lv.cta_first = bk.cta_first;
+    lv.num_ctas = bk.num_ctas;
+    lv.merge_first = bk.merge_first;
+    lv.num_merge = bk.num_merge;
+    const int rc = launch_decode(lv, q, paged_kv, num_pages, sm_scale, k_scale, v_scale,
+                                 k_scales, v_scales, max_bound, o, lse, cuda_stream,
+                                 head_k_scales, head_v_scales);
+    if (rc != FA_OK) return rc;
+  }
+  if (timed && cudaEventRecord(plan->ev_after, st) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
 

@@ -160,15 +160,20 @@ struct MmaCfg {
   // two CTAs per SM), three CTAs per SM.  E4M3 KV: 32 KB (two 4 KB pages per
   // warp) so that four CTAs fit per SM - its denser per-byte arithmetic needs
   // the extra warps to hide each page's dependent chain; the E4M3 column
-  // split (two pages a warp step) 48 KB at three CTAs per SM.
-  static constexpr int RING_BYTES = KV_ES == 1 ? (CS ? 49152 : 32768) : (NC >= 8 ? 49152 : 65536);
+  // split (three pages a warp step) 48 KB at three CTAs per SM.  A column
+  // split of two or three warps (16 or 24 columns) takes 32 KB, so that five
+  // or four CTAs fit per SM.
+  static constexpr int RING_BYTES =
+      CS && NW < 4 ? 32768
+                   : (KV_ES == 1 ? (CS ? 49152 : 32768) : (NC >= 8 ? 49152 : 65536));
   static constexpr int SPW0 = RING_BYTES / STAGE_BYTES / NW;
   static constexpr int SPW = SPW0 < 1 ? 1 : (SPW0 > 4 ? 4 : SPW0);
   // column split: every warp reads every stage, any number of stages works
   static constexpr int S = CS ? RING_BYTES / STAGE_BYTES : SPW * NW;
   static constexpr int THREADS = (NW + 1) * 32;
-  // CTAs per SM the ring size is chosen for; the register budget must allow it
-  static constexpr int MIN_CTAS = KV_ES == 1 && !CS ? 4 : 3;
+  // CTAs per SM the ring size is chosen for; the register budget must allow
+  // it (column split: 480 or 512 threads per SM at two or three warps)
+  static constexpr int MIN_CTAS = CS ? (NW <= 2 ? 5 : NW == 3 ? 4 : 3) : (KV_ES == 1 ? 4 : 3);
   static constexpr int OFF_FULL = S * STAGE_BYTES;
   static constexpr int OFF_EMPTY = OFF_FULL + 8 * S;
   static constexpr int OFF_PT = OFF_EMPTY + 8 * S;  // [NW][NPP][8 heads][16 tokens] 16-bit
@@ -817,6 +822,22 @@ inline bool find_ragged_q_kernel_for(int head_dim, int group, int max_q, DecodeK
   FA_RQ_CASE(1, 8) FA_RQ_CASE(1, 32) FA_RQ_CASE(2, 4) FA_RQ_CASE(2, 16)
   FA_RQ_CASE(4, 2) FA_RQ_CASE(4, 8) FA_RQ_CASE(8, 1) FA_RQ_CASE(8, 4)
 #undef FA_RQ_CASE
+  return false;
+}
+
+// Ragged query rows on the kernel of a request's 8-column tiles: a column
+// split of `tiles` warps (8 x tiles columns: 2 or 3), each warp one tile.
+template <typename QT, typename KVT>
+inline bool find_ragged_q_tiles_kernel_for(int head_dim, int group, int tiles, DecodeKernel* k) {
+  if (head_dim != 128) return false;
+#define FA_RT_CASE(GG, TT)                                                           \
+  if (group == GG && tiles == TT) {                                                  \
+    fill_mma_kernel<QT, KVT, 128, GG, TT, false, 8 * TT / GG, false, true>(k);       \
+    return true;                                                                     \
+  }
+  FA_RT_CASE(1, 2) FA_RT_CASE(1, 3) FA_RT_CASE(2, 2) FA_RT_CASE(2, 3)
+  FA_RT_CASE(4, 2) FA_RT_CASE(4, 3) FA_RT_CASE(8, 2) FA_RT_CASE(8, 3)
+#undef FA_RT_CASE
   return false;
 }
 

@@ -97,6 +97,10 @@ bool find_multi_token_kernel_bf16_e4m3(int head_dim, int group, int q_len, Decod
 // query tokens (head_dim 128; group x max_q <= 32).
 bool find_ragged_q_kernel_bf16(int head_dim, int group, int max_q, DecodeKernel* k);
 bool find_ragged_q_kernel_bf16_e4m3(int head_dim, int group, int max_q, DecodeKernel* k);
+// The same for requests of `tiles` (2 or 3) 8-column tiles: a column split
+// of that many consumer warps, with more CTAs per SM than four warps allow.
+bool find_ragged_q_tiles_kernel_bf16(int head_dim, int group, int tiles, DecodeKernel* k);
+bool find_ragged_q_tiles_kernel_bf16_e4m3(int head_dim, int group, int tiles, DecodeKernel* k);
 // Unified-max softmax (groups 2, 4, 8; bf16 q and KV at head_dim 64 or 128).
 bool find_unified_max_kernel_bf16(int head_dim, int group, DecodeKernel* k);
 // The same with f16 weights: f16 q and KV, or E4M3 KV (head_dim 128 for E4M3).

@@ -437,8 +437,13 @@ def test_alternating_kernels_in_one_stream(lib, cuda):
                                device=cuda)
     pa, oa, la = run_lib(lib, ba)
     pb, ob, lb = run_lib(lib, bb)
-    pr, orr, lr = run_ragged(lib, br)
-    assert pr.info["bucket_ctas"] > 0
+    import os
+    os.environ["FADECODE_BUCKETS"] = "all"
+    try:
+        pr, orr, lr = run_ragged(lib, br)
+    finally:
+        del os.environ["FADECODE_BUCKETS"]
+    assert pr.info["num_buckets"] == 3
     ob2 = torch.empty_like(ob)
     lb2 = torch.empty_like(lb)
     for _ in range(3):
@@ -758,44 +763,57 @@ def test_ragged_q_small(lib, cuda, kv_dtype, group, max_q):
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
 
 
+def bucket_of_segments(info, cta, seg):
+    """Bucket index of every segment of a plan's work list."""
+    nb = info["num_buckets"]
+    first = list(info["bucket_first_cta"][:nb]) + [info["num_ctas"]]
+    out = np.zeros(len(seg), np.int64)
+    for b in range(nb):
+        out[cta[first[b]]:cta[first[b + 1]]] = b
+    return out
+
+
+# (group, query rows per request): requests of 1 to 4 (or 3) 8-column tiles
+BUCKET_CASES = [(8, [1, 4, 2, 0, 3, 4, 1, 1, 2, 3]), (4, [2, 8, 1, 0, 3, 6, 2, 1, 5, 4]),
+                (2, [4, 12, 2, 0, 5, 16, 4, 1, 9, 8]), (1, [8, 20, 4, 0, 9, 32, 8, 1, 17, 24])]
+
+
 @pytest.mark.parametrize("merge", ["fused", "kernel"])
 @pytest.mark.parametrize("kv_dtype", [torch.bfloat16, torch.float8_e4m3fn], ids=["bf16", "e4m3"])
-@pytest.mark.parametrize("group,max_q", [(8, 4), (4, 5), (2, 12), (1, 20)])
-def test_ragged_q_buckets(lib, cuda, monkeypatch, kv_dtype, group, max_q, merge):
-    """A batch that mixes requests of at most 8 columns (group x query
-    rows) with wider ones is planned in two buckets: the wide requests on
-    the column-split kernel, the others, in a second launch, on the
-    8-column kernel.  Both buckets hold split requests, whose partial states
-    share the workspace.  Every row against the oracle; the work list covers
-    every page once; each bucket holds only its own requests; the buckets'
-    partial states do not overlap; a one-launch plan (FADECODE_BUCKETS=0)
-    gives the same rows within the bound; a rerun is bitwise the same; the
-    plan's timing events bracket both launches."""
+@pytest.mark.parametrize("group,counts", BUCKET_CASES, ids=[f"g{g}" for g, _ in BUCKET_CASES])
+def test_ragged_q_buckets(lib, cuda, monkeypatch, kv_dtype, group, counts, merge):
+    """A ragged batch planned in buckets by the 8-column tiles its requests
+    need (FADECODE_BUCKETS=all: a launch for every tile count present,
+    however small): one launch each on the 8-column kernel, the two- and
+    three-warp column splits and the four-warp one, their partial states
+    sharing the workspace.  Every row against the oracle; the work list
+    covers every page once; each bucket holds exactly the requests of its
+    tile count; the buckets' partial states do not overlap; a one-launch
+    plan (FADECODE_BUCKETS=0) gives the same rows within the bound; a rerun
+    is bitwise the same; the plan's timing events bracket every launch."""
     if merge == "kernel":
         monkeypatch.setenv("FADECODE_MERGE", "kernel")
     else:
         monkeypatch.delenv("FADECODE_MERGE", raising=False)
-    monkeypatch.delenv("FADECODE_BUCKETS", raising=False)
-    small = 8 // group
+    monkeypatch.setenv("FADECODE_BUCKETS", "all")
     lengths = [3000, 40, 2500, 17, 1000, 611, 5000, 9, 250, 4100]
-    counts = [small, max_q, max(1, small // 2), 0, small + 1, max_q, small, 1, max_q, small]
     b = W.make_ragged_q_batch(batch_lengths=lengths, q_counts=counts, num_qo_heads=2 * group,
                               num_kv_heads=2, head_dim=128, q_dtype=torch.bfloat16,
-                              kv_dtype=kv_dtype, seed=300 + group + max_q, device=cuda)
+                              kv_dtype=kv_dtype, seed=300 + group, device=cuda)
     p, o, lse = run_ragged(lib, b)
     info = p.info
-    assert info["bucket_ctas"] > 0 and group * info["bucket_q_len"] <= 8 < group * info["q_len"]
-    assert p.check() == 0
+    tiles = np.maximum(1, (group * np.asarray(counts) + 7) // 8)
+    nb = info["num_buckets"]
+    assert nb == len(set(tiles.tolist())) and p.check() == 0
+    bq = np.asarray(info["bucket_q_len"][:nb])
+    assert list(group * bq // 8) == sorted(set(tiles.tolist()), reverse=True)
     check_coverage(p, b)
     cta, seg, _ = p.work()
-    first_b = int(cta[info["num_ctas"] - info["bucket_ctas"]])
-    rows = np.diff(np.asarray(b.extra["qo_indptr"]))
-    assert np.all(rows[seg[:first_b, 0]] * group > 8)
-    assert np.all(rows[seg[first_b:, 0]] * group <= 8)
-    assert (seg[:first_b, 6] >= 0).any() and (seg[first_b:, 6] >= 0).any()
+    bucket = bucket_of_segments(info, cta, seg)
+    assert np.array_equal(tiles[seg[:, 0]], group * bq[bucket] // 8)
+    assert (seg[:, 6] >= 0).any()
     # partial states in floats per row: slot x columns of the bucket's kernel
-    cols = [group * info["q_len"] if k < first_b else group * info["bucket_q_len"]
-            for k in range(len(seg))]
+    cols = group * bq[bucket]
     spans = sorted((int(s[5]) * c, (int(s[5]) + 1) * c) for s, c in zip(seg, cols) if s[5] >= 0)
     assert all(a[1] <= z[0] for a, z in zip(spans, spans[1:]))
     assert spans[-1][1] <= info["num_partial_slots"] * group * info["q_len"]
@@ -814,8 +832,42 @@ def test_ragged_q_buckets(lib, cuda, monkeypatch, kv_dtype, group, max_q, merge)
     assert ev0.elapsed_time(ev1) > 0 and torch.equal(o, o2)
     monkeypatch.setenv("FADECODE_BUCKETS", "0")
     p1, o1, lse1 = run_ragged(lib, b)
-    assert p1.info["bucket_ctas"] == 0 and p1.check() == 0
+    assert p1.info["num_buckets"] == 1 and p1.check() == 0
     compare(o1, lse1, ref_o, ref_lse, tol_for(b))
+    monkeypatch.delenv("FADECODE_BUCKETS")
+    pd, od, lsed = run_ragged(lib, b)   # default: small buckets join wider ones
+    assert pd.check() == 0 and pd.info["num_buckets"] <= nb
+    compare(od, lsed, ref_o, ref_lse, tol_for(b))
+
+
+@pytest.mark.parametrize("case", ["e4m3", "e4m3_little", "bf16"])
+def test_ragged_q_bucket_policy(lib, cuda, monkeypatch, case):
+    """The default plan of a ragged batch at group 8 whose widest request has
+    3 tiles: one launch on the three-warp column split, plus, with E4M3 KV
+    and enough work in the one-tile requests (here 1,252 pages x 8 kv heads,
+    above 64 per SM), a second launch of those on the 8-column kernel.
+    Every row against the oracle."""
+    monkeypatch.delenv("FADECODE_BUCKETS", raising=False)
+    kv = torch.bfloat16 if case == "bf16" else torch.float8_e4m3fn
+    one = [40] * 4 if case == "e4m3_little" else [5000] * 4
+    lengths = one + [3000, 2000, 700]
+    counts = [1, 1, 1, 1, 3, 2, 3]
+    b = W.make_ragged_q_batch(batch_lengths=lengths, q_counts=counts, num_qo_heads=64,
+                              num_kv_heads=8, head_dim=128, q_dtype=torch.bfloat16, kv_dtype=kv,
+                              seed=331, device=cuda)
+    p, o, lse = run_ragged(lib, b)
+    info = p.info
+    assert p.check() == 0
+    if case == "e4m3":
+        assert info["num_buckets"] == 2 and info["bucket_q_len"][:2] == [3, 1]
+        cta, seg, _ = p.work()
+        bucket = bucket_of_segments(info, cta, seg)
+        assert set(seg[bucket == 1, 0].tolist()) == {0, 1, 2, 3}
+    else:
+        assert info["num_buckets"] == 1 and info["bucket_q_len"][0] == 3
+    check_coverage(p, b)
+    ref_o, ref_lse = oracle_decode(b)
+    compare(o, lse, ref_o, ref_lse, tol_for(b))
 
 
 def test_ragged_q_one_token_each_is_decode(lib, cuda):
@@ -835,16 +887,21 @@ def test_ragged_q_one_token_each_is_decode(lib, cuda):
 
 
 @pytest.mark.parametrize("kv_dtype", [torch.bfloat16, torch.float8_e4m3fn], ids=["bf16", "e4m3"])
-@pytest.mark.parametrize("group,q_len", [(8, 2), (8, 4), (4, 4), (2, 8), (1, 16)])
+@pytest.mark.parametrize("group,q_len", [(8, 2), (8, 3), (8, 4), (4, 4), (4, 6), (2, 8),
+                                         (2, 12), (1, 16), (1, 24)])
 def test_multi_token_wide(lib, cuda, kv_dtype, group, q_len):
     """Uniform multi-token plans with more than 8 columns (group x q_len, up
-    to 32): the group-8 shape verifying 2 or 4 draft tokens."""
+    to 32): the group-8 shape verifying 2, 3 or 4 draft tokens; 16 and 24
+    columns run on the column split of two and three warps (one bucket)."""
     lengths = [max(n, q_len) for n in (8, 9, 16, 17, 250, 1000, 33, 611, 2500)]
     b = W.make_batch(batch_lengths=lengths, num_qo_heads=2 * group, num_kv_heads=2,
                      head_dim=128, q_dtype=torch.bfloat16, kv_dtype=kv_dtype,
                      seed=80 + group + q_len, device=cuda, q_len=q_len)
     p, o, lse = run_multi(lib, b)
     assert p.info["q_len"] >= q_len and p.check() == 0
+    tiles = group * q_len // 8
+    assert p.info["num_buckets"] == 1
+    assert group * p.info["bucket_q_len"][0] == 8 * tiles or tiles == 4
     check_coverage(p, b)
     ref_o, ref_lse = oracle_decode(b)
     compare(o, lse, ref_o, ref_lse, tol_for(b))
