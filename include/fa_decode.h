@@ -383,6 +383,40 @@ int fa_plan_work_host(const int32_t* indptr, const int32_t* last_page_len,
                       int32_t* segments, int32_t* merge, int* n_ctas,
                       int* n_segments, int* n_merge, int* n_slots);
 
+/* The buckets fa_decode_plan_ragged_q makes of a batch whose widest
+ * request takes the column split, on the host (no CUDA call).  Request i
+ * of group G with n_i = qo_indptr[i+1] - qo_indptr[i] query rows needs
+ * t_i = max(1, ceil(G x n_i / 8)) 8-column tiles, at most widest_tiles (the
+ * tiles of the batch's one-launch kernel, 2..4).  Every request goes to the
+ * bucket of the widest tile count present, except the one-tile requests
+ * when flags bit 0 is set (E4M3 KV) and they hold at least min_own_units
+ * (page, kv head) pairs, or every tile count when flags bit 1 is set.  One
+ * head-grouped work list per bucket (as fa_plan_work_host_heads, with
+ * max_ctas_by_tiles[t-1] CTAs at most for the kernel of t tiles),
+ * concatenated widest bucket first: a later bucket's CTAs, segments and
+ * merge units follow the earlier ones' (request ids and page positions are
+ * the batch's); its partial slots start after the columns the earlier
+ * buckets' slots take, in units of its own slot of 8t columns
+ * (*slot_columns: the total).
+ *  qo_indptr        [batch + 1] int32, host, 0 first, non-decreasing.
+ *  max_ctas_by_tiles[4]: grid bound of the kernel of 1..4 tiles.
+ *  Outputs as fa_plan_work_host, with capacities for the sum of the grids
+ *  (C = sum over t of max_ctas_by_tiles[t-1] * 7 + 1), plus *n_buckets (0:
+ *  the batch stays one launch of the widest kernel, nothing else written
+ *  but zero counts), bucket_tiles[4] and bucket_first_cta[4] (0 / -1 past
+ *  *n_buckets).
+ * Errors: FA_ERR_INVALID_ARG (malformed input, a tile count above
+ * widest_tiles, a bucket whose grid bound is 0). */
+int fa_plan_work_host_buckets(const int32_t* indptr, const int32_t* last_page_len,
+                              const int32_t* qo_indptr, int batch, int group,
+                              int num_kv_heads, int page_size, int widest_tiles,
+                              const int* max_ctas_by_tiles, int flags,
+                              int64_t min_own_units, int32_t* cta_offsets,
+                              int32_t* segments, int32_t* merge, int* n_ctas,
+                              int* n_segments, int* n_merge, int* n_buckets,
+                              int* bucket_tiles, int* bucket_first_cta,
+                              int64_t* slot_columns);
+
 /* The plan fa_decode_plan makes by default, on the host: the grid in
  * groups of num_kv_heads CTAs, group g taking the g-th equal share of the
  * batch's page stream (request by request, a fixed cost of 2 pages before

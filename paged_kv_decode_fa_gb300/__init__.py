@@ -23,7 +23,8 @@ __all__ = [
     "FA_OK", "FaError", "DecodePlan", "plan", "plan_multi_token", "plan_ragged_q", "run",
     "merge_states",
     "CascadePlan", "cascade_plan",
-    "workspace_size", "plan_work_host", "BatchDecodeWithPagedKVCacheWrapper",
+    "workspace_size", "plan_work_host", "plan_work_host_buckets",
+    "BatchDecodeWithPagedKVCacheWrapper",
     "LIB_PATH", "EXPORTED_SYMBOLS", "library", "library_stats",
 ]
 
@@ -41,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "fa_cascade_check", "fa_decode_run_unified_max", "fa_decode_unified_max_fallbacks",
     "fa_cascade_set_timing_events", "fa_decode_static_check", "fa_library_get_stats",
     "fa_decode_plan_ragged_q", "fa_decode_workspace_size_ragged_q", "fa_cascade_run_scaled",
+    "fa_plan_work_host_buckets",
     "fa_decode_run_head_scales", "fa_plan_work_host_heads",
 )
 
@@ -146,6 +148,9 @@ def _load() -> ctypes.CDLL:
     lib.fa_plan_work_host.restype = i32
     lib.fa_plan_work_host_heads.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
     lib.fa_plan_work_host_heads.restype = i32
+    lib.fa_plan_work_host_buckets.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, i32,
+                                              ctypes.c_int64, P, P, P, P, P, P, P, P, P, P]
+    lib.fa_plan_work_host_buckets.restype = i32
     lib.fa_decode_check.argtypes = [P, P, ctypes.POINTER(i32)]
     lib.fa_decode_check.restype = i32
     lib.fa_decode_set_timing_events.argtypes = [P, P, P]
@@ -584,6 +589,47 @@ def plan_work_host(indptr, last_page_len, num_kv_heads: int, page_size: int, max
                                       ctypes.byref(n_m), ctypes.byref(n_sl)), "fa_plan_work_host")
     return (cta[: n_c.value + 1].copy(), seg[: n_s.value * SEGMENT_INTS].reshape(-1, SEGMENT_INTS).copy(),
             mer[: n_m.value * MERGE_INTS].reshape(-1, MERGE_INTS).copy(), n_sl.value)
+
+
+def plan_work_host_buckets(indptr, last_page_len, qo_indptr, group: int, num_kv_heads: int,
+                           page_size: int, widest_tiles: int, max_ctas_by_tiles,
+                           one_tile_own: bool = False, min_own_units: int = 0,
+                           all_buckets: bool = False):
+    """Host-only buckets of a ragged plan (fa_plan_work_host_buckets, no GPU).
+    Returns None when the batch stays one launch of the widest kernel, else
+    (cta_offsets, segments [n,8], merge [m,4], bucket_tiles, bucket_first_cta,
+    slot_columns) for the buckets' concatenated work list."""
+    indptr_h, indptr_p, n_indptr = _host_i32_ptr(indptr)
+    last_h, last_p, n_last = _host_i32_ptr(last_page_len)
+    qo_h, qo_p, n_qo = _host_i32_ptr(qo_indptr)
+    B = n_indptr - 1
+    if n_last < B or n_qo < B + 1:
+        raise ValueError("last_page_len / qo_indptr shorter than the batch")
+    mc = np.zeros(4, np.int32)
+    mc[:len(max_ctas_by_tiles)] = max_ctas_by_tiles
+    total = int(mc.sum())
+    cuts = sum(int(m) * 7 + 1 for m in mc)
+    cta = np.zeros(total + 1, np.int32)
+    seg = np.zeros(((B * num_kv_heads + cuts) * SEGMENT_INTS,), np.int32)
+    mer = np.zeros((cuts * MERGE_INTS,), np.int32)
+    tiles = np.zeros(4, np.int32)
+    first = np.zeros(4, np.int32)
+    n_c, n_s, n_m, n_b = (ctypes.c_int() for _ in range(4))
+    cols = ctypes.c_int64()
+    flags = (1 if one_tile_own else 0) | (2 if all_buckets else 0)
+    _check(_L().fa_plan_work_host_buckets(
+        indptr_p, last_p if B else None, qo_p, B, group, num_kv_heads, page_size, widest_tiles,
+        mc.ctypes.data, flags, int(min_own_units), cta.ctypes.data, seg.ctypes.data,
+        mer.ctypes.data, ctypes.byref(n_c), ctypes.byref(n_s), ctypes.byref(n_m),
+        ctypes.byref(n_b), tiles.ctypes.data, first.ctypes.data, ctypes.byref(cols)),
+        "fa_plan_work_host_buckets")
+    if n_b.value == 0:
+        return None
+    nb = n_b.value
+    return (cta[: n_c.value + 1].copy(),
+            seg[: n_s.value * SEGMENT_INTS].reshape(-1, SEGMENT_INTS).copy(),
+            mer[: n_m.value * MERGE_INTS].reshape(-1, MERGE_INTS).copy(),
+            tiles[:nb].copy(), first[:nb].copy(), cols.value)
 
 
 class CascadePlan:

@@ -473,6 +473,51 @@ int fa_plan_work_host_heads(const int32_t* indptr, const int32_t* last_page_len,
   return FA_OK;
 }
 
+int fa_plan_work_host_buckets(const int32_t* indptr, const int32_t* last_page_len,
+                              const int32_t* qo_indptr, int batch, int group, int num_kv_heads,
+                              int page_size, int widest_tiles, const int* max_ctas_by_tiles,
+                              int flags, int64_t min_own_units, int32_t* cta_offsets,
+                              int32_t* segments, int32_t* merge, int* n_ctas, int* n_segments,
+                              int* n_merge, int* n_buckets, int* bucket_tiles,
+                              int* bucket_first_cta, int64_t* slot_columns) {
+  if (!max_ctas_by_tiles || !cta_offsets || !segments || !merge || !n_ctas || !n_segments ||
+      !n_merge || !n_buckets || !bucket_tiles || !bucket_first_cta || !slot_columns ||
+      widest_tiles < 1 || widest_tiles > fadecode::kMaxTileBuckets)
+    return FA_ERR_INVALID_ARG;
+  fadecode::BucketPolicy pol;
+  pol.group = group;
+  pol.widest = widest_tiles;
+  for (int t = 1; t <= widest_tiles; ++t) pol.max_ctas[t] = max_ctas_by_tiles[t - 1];
+  pol.one_tile_own = (flags & 1) != 0;
+  pol.all = (flags & 2) != 0;
+  pol.min_own_units = min_own_units;
+  pol.min_pages_per_cta = kMinPagesPerCta;
+  pol.heads = true;
+  WorkList wl;
+  fadecode::BucketList bl;
+  try {
+    if (fadecode::build_bucket_work_list(indptr, last_page_len, qo_indptr, batch, num_kv_heads,
+                                         page_size, pol, &wl, &bl) != 0)
+      return FA_ERR_INVALID_ARG;
+  } catch (const std::bad_alloc&) {
+    return FA_ERR_INVALID_ARG;
+  }
+  *n_buckets = bl.num;
+  *slot_columns = bl.slot_columns;
+  for (int b = 0; b < fadecode::kMaxTileBuckets; ++b) {
+    bucket_tiles[b] = b < bl.num ? bl.tiles[b] : 0;
+    bucket_first_cta[b] = b < bl.num ? bl.cta_first[b] : -1;
+  }
+  *n_ctas = wl.num_ctas;
+  *n_segments = (int)wl.segments.size();
+  *n_merge = (int)wl.merge.size();
+  if (bl.num == 0) return FA_OK;
+  std::memcpy(cta_offsets, wl.cta_offsets.data(), sizeof(int32_t) * wl.cta_offsets.size());
+  std::memcpy(segments, wl.segments.data(), sizeof(fadecode::Segment) * wl.segments.size());
+  std::memcpy(merge, wl.merge.data(), sizeof(fadecode::MergeUnit) * wl.merge.size());
+  return FA_OK;
+}
+
 int fa_plan_work_host(const int32_t* indptr, const int32_t* last_page_len, int batch,
                       int num_kv_heads, int page_size, int max_ctas, int min_pages_per_cta,
                       double pool_fraction, int32_t* cta_offsets, int32_t* segments, int32_t* merge, int* n_ctas,
@@ -568,44 +613,6 @@ size_t fa_decode_workspace_size_ragged_q(int batch, int num_qo_heads, int num_kv
 
 namespace {
 
-// Requests of a ragged batch as a batch of their own: indptr and
-// last_page_len compacted, and each one's id in the whole batch.
-struct SubBatch {
-  std::vector<int32_t> indptr{0}, last, ids;
-  void add(const int32_t* indptr_all, const int32_t* last_all, int i) {
-    ids.push_back(i);
-    indptr.push_back(indptr.back() + (indptr_all[i + 1] - indptr_all[i]));
-    last.push_back(last_all[i]);
-  }
-};
-
-// Append the work list of a sub-batch to `out`: its CTAs after out's, its
-// requests and page positions mapped back to the whole batch, its merge
-// units numbered after out's, its partial slots from slot_base on.
-void append_work(const WorkList& w, const SubBatch& s, const int32_t* indptr, int64_t slot_base,
-                 WorkList* out) {
-  const int32_t seg0 = (int32_t)out->segments.size(), m0 = (int32_t)out->merge.size();
-  if (out->cta_offsets.empty()) out->cta_offsets.push_back(0);
-  for (int c = 1; c <= w.num_ctas; ++c) out->cta_offsets.push_back(seg0 + w.cta_offsets[c]);
-  for (fadecode::Segment sg : w.segments) {
-    const int32_t shift = indptr[s.ids[sg.request]] - s.indptr[sg.request];
-    sg.request = s.ids[sg.request];
-    sg.page_begin += shift;
-    sg.page_end += shift;
-    if (sg.merge_unit >= 0) sg.merge_unit += m0;
-    if (sg.out_slot >= 0) sg.out_slot += (int32_t)slot_base;
-    out->segments.push_back(sg);
-  }
-  for (fadecode::MergeUnit m : w.merge) {
-    m.request = s.ids[m.request];
-    m.first_slot += (int32_t)slot_base;
-    out->merge.push_back(m);
-  }
-  out->num_ctas += w.num_ctas;
-  out->total_pages += w.total_pages;
-  out->total_tokens += w.total_tokens;
-}
-
 // Buckets for a ragged batch whose widest request takes the column split
 // (more than 8 columns).  Request i needs t_i = ceil(G x n_i / 8) 8-column
 // tiles (1 for n_i = 0).  A column split's warps each take every page of a
@@ -619,89 +626,55 @@ void append_work(const WorkList& w, const SubBatch& s, const int32_t* indptr, in
 // 8-column kernel (pages split over its warps) when they hold enough work
 // to outweigh a launch's fixed time (spec_decode_ragged: 449 -> 413 us).
 // A 16-bit column split streams near the copy rate already, and the
-// 8-column kernel is no faster on those requests.  Buckets run one after
-// the other, widest first, each grid over the whole GPU.  Partial states:
-// each bucket's slots follow the previous bucket's columns, in units of its
-// own slot (G x its q_len columns).  Returns false (and leaves the plan
-// alone) when one launch of the plan's own kernel is what remains, a kernel
-// is not built or the plan does not fit the workspace.
+// 8-column kernel is no faster on those requests.  The work lists are
+// built by fadecode::build_bucket_work_list; buckets run one after the
+// other, widest first, each grid over the whole GPU.  Returns false (and
+// leaves the plan alone) when one launch of the plan's own kernel is what
+// remains, a kernel is not built or the plan does not fit the workspace.
 bool plan_buckets(fa_decode_plan_s* plan, const int32_t* indptr, const int32_t* last,
                   const int32_t* qo, int batch, int sms, size_t workspace_bytes,
                   BucketMode mode) {
   const int G = plan->group;
   const int nc_max = G * plan->kern[kPlain].q_len;
-  if (nc_max <= 8 || nc_max % 8 != 0 || nc_max / 8 > kMaxBuckets) return false;
-  const int widest = nc_max / 8;
-  auto tiles_of = [&](int i) { return std::max(1, (G * (qo[i + 1] - qo[i]) + 7) / 8); };
-  int64_t units[kMaxBuckets + 1] = {0};
-  int count[kMaxBuckets + 1] = {0};
-  for (int i = 0; i < batch; ++i) {
-    const int t = tiles_of(i);
-    if (t > widest) return false;
-    units[t] += (int64_t)(indptr[i + 1] - indptr[i]) * plan->hkv;
-    ++count[t];
-  }
-  int top = 0;  // the widest tile count present
-  for (int t = 1; t <= widest; ++t)
-    if (count[t] > 0) top = t;
-  // where each tile count goes: its own launch, or the widest one's
-  int dest[kMaxBuckets + 1];
-  for (int t = 1; t <= widest; ++t) {
-    const bool own = mode == BucketMode::kAll ||
-                     (t == 1 && plan->kv_dtype == FA_DTYPE_E4M3 &&
-                      units[1] >= (int64_t)kMinBucketUnitsPerSm * sms);
-    dest[t] = own ? t : top;
-  }
-  int order[kMaxBuckets], nb = 0;
-  for (int t = widest; t >= 1; --t) {
-    bool used = false;
-    for (int u = 1; u <= widest; ++u) used = used || (count[u] > 0 && dest[u] == t);
-    if (used) order[nb++] = t;
-  }
-  if (nb == 0 || (nb == 1 && order[0] == widest)) return false;
-
-  fa_decode_plan_s::Bucket bk[kMaxBuckets];
-  SubBatch sub[kMaxBuckets];
-  for (int b = 0; b < nb; ++b) {
-    bk[b].tiles = order[b];
-    if (!find_ragged_tiles_kernel(plan->q_dtype, plan->kv_dtype, plan->d, G, order[b],
-                                  &bk[b].kern))
+  if (nc_max <= 8 || nc_max % 8 != 0 || nc_max / 8 > kMaxBuckets || 8 % G != 0) return false;
+  fadecode::BucketPolicy pol;
+  pol.group = G;
+  pol.widest = nc_max / 8;
+  DecodeKernel kern[kMaxBuckets + 1];
+  for (int t = 1; t <= pol.widest; ++t) {
+    if (!find_ragged_tiles_kernel(plan->q_dtype, plan->kv_dtype, plan->d, G, t, &kern[t]))
       return false;
-  }
-  for (int i = 0; i < batch; ++i) {
-    const int t = dest[tiles_of(i)];
-    for (int b = 0; b < nb; ++b)
-      if (order[b] == t) sub[b].add(indptr, last, i);
-  }
-  const bool heads = heads_plan();
-  WorkList w;
-  int64_t cols = 0;  // partial-state columns taken by the buckets so far
-  for (int b = 0; b < nb; ++b) {
-    const int occ = std::min(kernel_occupancy(bk[b].kern), 8);
+    const int occ = std::min(kernel_occupancy(kern[t]), 8);
     if (occ <= 0) return false;
-    WorkList wb;
-    if (fadecode::build_work_list(sub[b].indptr.data(), sub[b].last.data(),
-                                  (int)sub[b].ids.size(), plan->hkv, plan->page_size, sms * occ,
-                                  kMinPagesPerCta, 0.0, &wb, heads) != 0)
-      return false;
-    const int nc = G * bk[b].kern.q_len;
-    const int64_t slot_base = (cols + nc - 1) / nc;
-    bk[b].cta_first = w.num_ctas;
-    bk[b].num_ctas = wb.num_ctas;
-    bk[b].merge_first = (int)w.merge.size();
-    bk[b].num_merge = (int)wb.merge.size();
-    append_work(wb, sub[b], indptr, slot_base, &w);
-    cols = (slot_base + wb.num_slots) * nc;
+    pol.max_ctas[t] = sms * occ;
   }
-  if (cols > INT32_MAX) return false;
-  w.num_slots = (int)((cols + nc_max - 1) / nc_max);
+  pol.one_tile_own = plan->kv_dtype == FA_DTYPE_E4M3;
+  pol.min_own_units = (int64_t)kMinBucketUnitsPerSm * sms;
+  pol.all = mode == BucketMode::kAll;
+  pol.min_pages_per_cta = kMinPagesPerCta;
+  pol.heads = heads_plan();
+  WorkList w;
+  fadecode::BucketList bl;
+  if (fadecode::build_bucket_work_list(indptr, last, qo, batch, plan->hkv, plan->page_size, pol,
+                                       &w, &bl) != 0 ||
+      bl.num == 0)
+    return false;
+  w.num_slots = (int)((bl.slot_columns + nc_max - 1) / nc_max);
   const Layout L = make_layout(w.num_ctas, (int64_t)w.segments.size(), (int64_t)w.merge.size(),
                                w.num_slots, nc_max, plan->d, (int64_t)batch + 1);
   if (L.total > workspace_bytes) return false;
   plan->wl = std::move(w);
   plan->layout = L;
-  plan->num_buckets = nb;
-  for (int b = 0; b < nb; ++b) plan->bucket[b] = bk[b];
+  plan->num_buckets = bl.num;
+  for (int b = 0; b < bl.num; ++b) {
+    fa_decode_plan_s::Bucket& bk = plan->bucket[b];
+    bk.kern = kern[bl.tiles[b]];
+    bk.tiles = bl.tiles[b];
+    bk.cta_first = bl.cta_first[b];
+    bk.num_ctas = bl.num_ctas[b];
+    bk.merge_first = bl.merge_first[b];
+    bk.num_merge = bl.num_merge[b];
+  }
   return true;
 }
 

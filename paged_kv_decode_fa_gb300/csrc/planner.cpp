@@ -33,6 +33,7 @@
 #include "planner.h"
 
 #include <algorithm>
+#include <climits>
 
 namespace fadecode {
 namespace {
@@ -409,6 +410,117 @@ int build_work_list_fixed(const int32_t* indptr, const int32_t* last_page_len, i
   out->num_slots = tot.num_slots;
   out->total_pages = tot.total_pages;
   out->total_tokens = tot.total_tokens;
+  return 0;
+}
+
+namespace {
+
+// Requests of a batch as a batch of their own: indptr and last_page_len
+// compacted, and each one's id in the whole batch.
+struct SubBatch {
+  std::vector<int32_t> indptr{0}, last, ids;
+  void add(const int32_t* indptr_all, const int32_t* last_all, int i) {
+    ids.push_back(i);
+    indptr.push_back(indptr.back() + (indptr_all[i + 1] - indptr_all[i]));
+    last.push_back(last_all[i]);
+  }
+};
+
+// Append the work list of a sub-batch to `out` (see build_bucket_work_list).
+void append_work(const WorkList& w, const SubBatch& s, const int32_t* indptr, int64_t slot_base,
+                 WorkList* out) {
+  const int32_t seg0 = (int32_t)out->segments.size(), m0 = (int32_t)out->merge.size();
+  if (out->cta_offsets.empty()) out->cta_offsets.push_back(0);
+  for (int c = 1; c <= w.num_ctas; ++c) out->cta_offsets.push_back(seg0 + w.cta_offsets[c]);
+  for (Segment sg : w.segments) {
+    const int32_t shift = indptr[s.ids[sg.request]] - s.indptr[sg.request];
+    sg.request = s.ids[sg.request];
+    sg.page_begin += shift;
+    sg.page_end += shift;
+    if (sg.merge_unit >= 0) sg.merge_unit += m0;
+    if (sg.out_slot >= 0) sg.out_slot += (int32_t)slot_base;
+    out->segments.push_back(sg);
+  }
+  for (MergeUnit m : w.merge) {
+    m.request = s.ids[m.request];
+    m.first_slot += (int32_t)slot_base;
+    out->merge.push_back(m);
+  }
+  out->num_ctas += w.num_ctas;
+  out->total_pages += w.total_pages;
+  out->total_tokens += w.total_tokens;
+}
+
+}  // namespace
+
+int build_bucket_work_list(const int32_t* indptr, const int32_t* last_page_len,
+                           const int32_t* qo_indptr, int batch, int num_kv_heads, int page_size,
+                           const BucketPolicy& pol, WorkList* out, BucketList* buckets) {
+  if (!indptr || !qo_indptr || !out || !buckets || batch < 0 || num_kv_heads <= 0 ||
+      page_size <= 0 || pol.group < 1 || 8 % pol.group != 0 || pol.widest < 1 ||
+      pol.widest > kMaxTileBuckets)
+    return -1;
+  if (batch > 0 && !last_page_len) return -1;
+  if (indptr[0] != 0 || qo_indptr[0] != 0) return -1;
+  const int G = pol.group;
+  int64_t units[kMaxTileBuckets + 1] = {0};
+  int count[kMaxTileBuckets + 1] = {0};
+  for (int i = 0; i < batch; ++i) {
+    const int64_t np = (int64_t)indptr[i + 1] - indptr[i];
+    const int64_t nq = (int64_t)qo_indptr[i + 1] - qo_indptr[i];
+    if (np < 0 || nq < 0) return -1;
+    const int64_t t = std::max<int64_t>(1, (G * nq + 7) / 8);
+    if (t > pol.widest) return -1;
+    units[t] += np * num_kv_heads;
+    ++count[t];
+  }
+  int top = 0;  // the widest tile count present
+  for (int t = 1; t <= pol.widest; ++t)
+    if (count[t] > 0) top = t;
+  int dest[kMaxTileBuckets + 1] = {0};
+  for (int t = 1; t <= pol.widest; ++t) {
+    const bool own = pol.all || (t == 1 && pol.one_tile_own && units[1] >= pol.min_own_units);
+    dest[t] = own ? t : top;
+  }
+  BucketList bl;
+  for (int t = pol.widest; t >= 1; --t) {
+    bool used = false;
+    for (int u = 1; u <= pol.widest; ++u) used = used || (count[u] > 0 && dest[u] == t);
+    if (used) bl.tiles[bl.num++] = t;
+  }
+  *buckets = BucketList{};
+  if (bl.num == 0 || (bl.num == 1 && bl.tiles[0] == pol.widest)) return 0;
+  for (int b = 0; b < bl.num; ++b)
+    if (pol.max_ctas[bl.tiles[b]] < 1) return -1;
+
+  SubBatch sub[kMaxTileBuckets];
+  for (int i = 0; i < batch; ++i) {
+    const int nq = qo_indptr[i + 1] - qo_indptr[i];
+    const int t = dest[std::max(1, (G * nq + 7) / 8)];
+    for (int b = 0; b < bl.num; ++b)
+      if (bl.tiles[b] == t) sub[b].add(indptr, last_page_len, i);
+  }
+  WorkList w;
+  int64_t cols = 0;  // partial-state columns taken by the buckets so far
+  for (int b = 0; b < bl.num; ++b) {
+    WorkList wb;
+    if (build_work_list(sub[b].indptr.data(), sub[b].last.data(), (int)sub[b].ids.size(),
+                        num_kv_heads, page_size, pol.max_ctas[bl.tiles[b]],
+                        pol.min_pages_per_cta, 0.0, &wb, pol.heads) != 0)
+      return -1;
+    const int nc = 8 * bl.tiles[b];
+    const int64_t slot_base = (cols + nc - 1) / nc;
+    if (slot_base + wb.num_slots > INT32_MAX) return -1;
+    bl.cta_first[b] = w.num_ctas;
+    bl.num_ctas[b] = wb.num_ctas;
+    bl.merge_first[b] = (int)w.merge.size();
+    bl.num_merge[b] = (int)wb.merge.size();
+    append_work(wb, sub[b], indptr, slot_base, &w);
+    cols = (slot_base + wb.num_slots) * nc;
+  }
+  bl.slot_columns = cols;
+  *out = std::move(w);
+  *buckets = bl;
   return 0;
 }
 

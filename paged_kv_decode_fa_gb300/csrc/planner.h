@@ -90,4 +90,44 @@ int build_work_list_fixed(const int32_t* indptr, const int32_t* last_page_len, i
                           int num_kv_heads, int page_size, int max_ctas, int min_pages_per_cta,
                           FixedWorkList* out, bool heads = false);
 
+// Buckets of a ragged plan by 8-column tiles.  Request i of a batch with
+// group G has n_i query rows and needs t_i = max(1, ceil(G n_i / 8)) tiles;
+// the kernel of t tiles holds 8t / G rows a request.  policy: which tile
+// counts take a launch of their own (see build_bucket_work_list).
+constexpr int kMaxTileBuckets = 4;
+
+struct BucketPolicy {
+  int group = 1;                               // query heads per kv head (1, 2, 4, 8)
+  int widest = kMaxTileBuckets;                // tiles the batch's one-launch kernel holds
+  int max_ctas[kMaxTileBuckets + 1] = {0};     // grid bound of the kernel of t tiles [t]
+  bool one_tile_own = false;                   // one-tile requests may take their own launch
+  int64_t min_own_units = 0;                   // ... from this many (page, kv head) pairs
+  bool all = false;                            // a launch for every tile count present
+  int min_pages_per_cta = 8;
+  bool heads = true;                           // head-grouped plan per bucket
+};
+
+struct BucketList {
+  int num = 0;  // launches; 0: the batch stays one launch of the widest kernel
+  int tiles[kMaxTileBuckets] = {0};
+  int cta_first[kMaxTileBuckets] = {0}, num_ctas[kMaxTileBuckets] = {0};
+  int merge_first[kMaxTileBuckets] = {0}, num_merge[kMaxTileBuckets] = {0};
+  int64_t slot_columns = 0;  // partial-state columns (x head_dim floats) the buckets take
+};
+
+// Plan a ragged batch in buckets: every request goes to the kernel of the
+// widest tile count present (top), except, when one_tile_own and the
+// one-tile requests hold at least min_own_units (page, kv head) pairs, or
+// when all, those of a tile count with a launch of its own.  One work list
+// per bucket (build_work_list on the bucket's requests, its kernel's grid
+// bound), concatenated widest first: a later bucket's CTAs, segments and
+// merge units follow the earlier ones', its requests and page positions
+// mapped back to the batch, its partial slots after the columns the
+// earlier buckets' slots take, in units of its own slot (8t columns).
+// Returns 0 (out and buckets filled; buckets->num = 0 and out untouched
+// when one launch of the widest kernel remains) or -1 for malformed input.
+int build_bucket_work_list(const int32_t* indptr, const int32_t* last_page_len,
+                           const int32_t* qo_indptr, int batch, int num_kv_heads, int page_size,
+                           const BucketPolicy& policy, WorkList* out, BucketList* buckets);
+
 }  // namespace fadecode

@@ -415,3 +415,146 @@ def test_heads_plan_edge_batches(lib):
     check_heads_work(lib, *_table([1]), 1, 100)
     check_heads_work(lib, *_table([65536]), 32, 456)      # one long request over 14 groups
     check_heads_work(lib, *_table([100, 900]), 8, 4)       # fewer CTAs than kv heads
+
+
+# ------------------------------------------------------------------ buckets by 8-column tiles
+
+def tiles_of(qo, G):
+    """8-column tiles each request of a ragged batch needs (1 for no rows)."""
+    return np.maximum(1, (G * np.diff(np.asarray(qo, np.int64)) + 7) // 8)
+
+
+def expected_buckets(indptr, qo, G, Hkv, widest, one_tile_own, min_units, all_b):
+    """The documented policy: every request to the widest tile count
+    present, except the one-tile requests when they may and do hold enough
+    (page, kv head) pairs, or every tile count with all_b.  Returns the
+    buckets' tile counts (widest first; [] for one launch of the widest
+    kernel) and each request's bucket tile count."""
+    t = tiles_of(qo, G)
+    if len(t) == 0:
+        return [], t
+    top = int(t.max())
+    pages = np.diff(np.asarray(indptr, np.int64))
+    one_units = Hkv * int(pages[t == 1].sum())
+    own = {u: all_b or (u == 1 and one_tile_own and one_units >= min_units)
+           for u in range(1, widest + 1)}
+    dest = np.array([u if own[int(u)] else top for u in t])
+    tiles = sorted(set(dest.tolist()), reverse=True)
+    return ([] if tiles == [widest] else tiles), dest
+
+
+def check_buckets(lib, indptr, last, qo, G, Hkv, widest, max_ctas, one_tile_own=False,
+                  min_units=0, all_b=False, P=16):
+    """The buckets' concatenated work list against its definition, rebuilt
+    from independent pieces: per bucket, the head-grouped plan of its
+    requests as a batch of their own (fa_plan_work_host_heads) with request
+    ids, page positions, merge units and partial slots moved as documented;
+    then coverage of the whole batch bit for bit, and partial slots of
+    different buckets disjoint in columns."""
+    res = lib.plan_work_host_buckets(indptr, last, qo, G, Hkv, P, widest, max_ctas,
+                                     one_tile_own, min_units, all_b)
+    tiles, dest = expected_buckets(indptr, qo, G, Hkv, widest, one_tile_own, min_units, all_b)
+    if not tiles:
+        assert res is None
+        return None
+    cta, seg, mer, btiles, first, cols = res
+    assert list(btiles) == tiles
+    indptr = np.asarray(indptr, np.int64)
+    last = np.asarray(last, np.int64)
+    np.testing.assert_array_equal(expand(seg), oracle.expected_coverage(indptr, Hkv))
+    assert_token_coverage(seg, indptr, last, Hkv, P)
+    bounds = list(first) + [len(cta) - 1]
+    col_end, m0 = 0, 0
+    spans = []
+    for b, tb in enumerate(tiles):
+        reqs = np.nonzero(dest == tb)[0]
+        sub_ip = np.concatenate([[0], np.cumsum(np.diff(indptr)[reqs])]).astype(np.int32)
+        ref_cta, ref_seg, ref_mer, ref_slots = lib.plan_work_host(
+            sub_ip, last[reqs].astype(np.int32), Hkv, P, int(max_ctas[tb - 1]), 8, heads=True)
+        c0, c1 = bounds[b], bounds[b + 1]
+        assert c1 - c0 == len(ref_cta) - 1 <= max_ctas[tb - 1]
+        np.testing.assert_array_equal(cta[c0:c1 + 1] - cta[c0], ref_cta)
+        nc = 8 * tb
+        slot_base = -(-col_end // nc)
+        exp = ref_seg.astype(np.int64)
+        exp[:, 2:4] += (indptr[reqs] - sub_ip[:-1])[exp[:, 0]][:, None]
+        exp[:, 0] = reqs[exp[:, 0]]
+        exp[:, 5] = np.where(exp[:, 5] >= 0, exp[:, 5] + slot_base, -1)
+        exp[:, 6] = np.where(exp[:, 6] >= 0, exp[:, 6] + m0, -1)
+        got = seg[cta[c0]:cta[c1]]
+        np.testing.assert_array_equal(got, exp)
+        expm = ref_mer.astype(np.int64)
+        if len(expm):
+            expm[:, 0] = reqs[expm[:, 0]]
+            expm[:, 2] += slot_base
+        np.testing.assert_array_equal(mer[m0:m0 + len(ref_mer)], expm)
+        spans += [(int(s) * nc, (int(s) + 1) * nc) for s in got[:, 5] if s >= 0]
+        m0 += len(ref_mer)
+        col_end = (slot_base + ref_slots) * nc
+    assert m0 == len(mer) and cols == col_end
+    spans.sort()
+    assert all(a[1] <= z[0] for a, z in zip(spans, spans[1:]))
+    return res
+
+
+def _ragged_rows(rng, lengths, G, widest):
+    """Query rows per request for a random tile count 1..widest each (0
+    rows for a request without tokens)."""
+    rows = []
+    for n in lengths:
+        t = int(rng.integers(1, widest + 1))
+        lo, hi = (8 * (t - 1)) // G + 1, (8 * t) // G
+        rows.append(0 if n == 0 else min(int(n), int(rng.integers(lo, hi + 1))))
+    return np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+
+
+def test_buckets_random_batches(lib):
+    rng = np.random.default_rng(41)
+    for _ in range(80):
+        G = int(rng.choice([1, 2, 4, 8]))
+        widest = int(rng.integers(2, 5))
+        B = int(rng.integers(1, 40))
+        lengths = rng.integers(0, 900, size=B)
+        lengths[rng.random(B) < 0.15] = 0
+        Hkv = int(rng.choice([1, 2, 3, 8]))
+        indptr, last = _table(lengths)
+        qo = _ragged_rows(rng, lengths, G, widest)
+        max_ctas = [int(x) for x in rng.integers(1, 200, size=4)]
+        units = int(rng.integers(0, 2000))
+        for own, all_b in ((False, False), (True, False), (False, True)):
+            check_buckets(lib, indptr, last, qo, G, Hkv, widest, max_ctas, own, units, all_b)
+
+
+def test_buckets_policy(lib):
+    """Which launches the policy makes (group 8: tiles = query rows)."""
+    indptr, last = _table([5000, 5000, 300, 900, 40])
+    mc = [608, 760, 608, 456]
+    qo = np.array([0, 1, 2, 5, 7, 11], np.int32)           # 1, 1, 3, 2, 4 rows
+    one_units = 8 * 2 * 313                                  # the one-row requests' pairs
+    r = check_buckets(lib, indptr, last, qo, 8, 8, 4, mc)    # 16-bit KV: one launch, widest
+    assert r is None
+    r = check_buckets(lib, indptr, last, qo, 8, 8, 4, mc, True, one_units)   # E4M3, enough
+    assert list(r[3]) == [4, 1]
+    r = check_buckets(lib, indptr, last, qo, 8, 8, 4, mc, True, one_units + 1)   # too little
+    assert r is None
+    r = check_buckets(lib, indptr, last, qo, 8, 8, 4, mc, all_b=True)
+    assert list(r[3]) == [4, 3, 2, 1]
+    qo3 = np.array([0, 1, 2, 5, 7, 10], np.int32)          # widest request: 3 rows
+    r = check_buckets(lib, indptr, last, qo3, 8, 8, 4, mc)   # one launch on three warps
+    assert list(r[3]) == [3] and r[4][0] == 0
+    r = check_buckets(lib, indptr, last, qo3, 8, 8, 4, mc, True, one_units)
+    assert list(r[3]) == [3, 1]
+    qo2 = np.array([0, 2, 4, 6, 8, 10], np.int32)          # uniform 2 rows
+    r = check_buckets(lib, indptr, last, qo2, 8, 8, 4, mc, True, 0)
+    assert list(r[3]) == [2]
+
+
+def test_buckets_rejects(lib):
+    indptr, last = _table([100, 200])
+    with pytest.raises(lib.FaError):                        # 5 rows at group 8 > 4 tiles
+        lib.plan_work_host_buckets(indptr, last, [0, 5, 6], 8, 2, 16, 4, [8, 8, 8, 8])
+    with pytest.raises(lib.FaError):                        # qo_indptr must start at 0
+        lib.plan_work_host_buckets(indptr, last, [1, 2, 3], 8, 2, 16, 4, [8, 8, 8, 8])
+    with pytest.raises(lib.FaError):                        # no grid for a used bucket
+        lib.plan_work_host_buckets(indptr, last, [0, 1, 3], 8, 2, 16, 4, [8, 0, 8, 8],
+                                   all_buckets=True)
