@@ -372,6 +372,57 @@ def test_cuda_graph_capture(lib, cuda):
     assert p.check() == 0
 
 
+def test_cuda_graph_capture_buckets(lib, cuda, monkeypatch):
+    """A ragged plan in four buckets (four launches a run) captured into a
+    CUDA graph: every replay equals the eager run bit for bit."""
+    monkeypatch.setenv("FADECODE_BUCKETS", "all")
+    b = W.make_ragged_q_batch(batch_lengths=[3000, 40, 2500, 17, 5000], q_counts=[1, 4, 2, 0, 3],
+                              num_qo_heads=16, num_kv_heads=2, head_dim=128,
+                              q_dtype=torch.bfloat16, kv_dtype=torch.float8_e4m3fn, seed=137,
+                              device=cuda)
+    p, ref_o, ref_lse = run_ragged(lib, b)
+    assert p.info["num_buckets"] == 4 and p.info["num_merge_units"] > 0
+    o, lse = torch.empty_like(ref_o), torch.empty_like(ref_lse)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        p.run(b.q, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale, out=o, lse=lse)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        p.run(b.q, b.paged_kv, k_scale=b.k_scale, v_scale=b.v_scale, out=o, lse=lse)
+    for _ in range(3):
+        o.zero_()
+        lse.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+    assert p.check() == 0
+
+
+def test_ragged_q_buckets_fall_back_to_one_launch(lib, cuda, monkeypatch):
+    """A workspace that holds the one-launch plan but not the plan in
+    buckets: the plan falls back to one launch, with the same rows."""
+    b = W.make_ragged_q_batch(batch_lengths=[3000, 40, 2500, 17, 5000], q_counts=[1, 4, 2, 0, 3],
+                              num_qo_heads=16, num_kv_heads=2, head_dim=128,
+                              q_dtype=torch.bfloat16, kv_dtype=torch.float8_e4m3fn, seed=139,
+                              device=cuda)
+    monkeypatch.setenv("FADECODE_BUCKETS", "0")
+    p1, o1, lse1 = run_ragged(lib, b)
+    one = p1.info["workspace_bytes_used"]
+    monkeypatch.setenv("FADECODE_BUCKETS", "all")
+    p4, o4, lse4 = run_ragged(lib, b)
+    four = p4.info["workspace_bytes_used"]
+    assert p4.info["num_buckets"] == 4
+    ws = torch.empty(one, dtype=torch.uint8, device=cuda)
+    p, o, lse = run_ragged(lib, b, workspace=ws)
+    assert p.check() == 0
+    assert p.info["num_buckets"] == (1 if four > one else 4)
+    ref_o, ref_lse = oracle_decode(b)
+    for x, y in ((o, lse), (o1, lse1), (o4, lse4)):
+        compare(x, y, ref_o, ref_lse, tol_for(b))
+
+
 def test_stream_handle_is_current_stream(lib, cuda):
     """Without an explicit stream, calls go to torch's current stream of the
     current device, inside a stream context too; an explicit stream or raw
@@ -672,9 +723,15 @@ def test_head_scales_equal_heads_is_per_tensor(lib, cuda):
     assert (lse - ref_lse).abs().max().item() <= 1e-4
 
 
-def test_head_scales_ragged_q(lib, cuda):
+@pytest.mark.parametrize("buckets", ["default", "all"])
+def test_head_scales_ragged_q(lib, cuda, monkeypatch, buckets):
     """Per-head scales on a ragged multi-token plan (group 8, 1..4 drafts:
-    the column split) against the ragged oracle run head by head."""
+    the column split; with FADECODE_BUCKETS=all one launch per tile count,
+    every bucket kernel) against the ragged oracle run head by head."""
+    if buckets == "all":
+        monkeypatch.setenv("FADECODE_BUCKETS", "all")
+    else:
+        monkeypatch.delenv("FADECODE_BUCKETS", raising=False)
     lengths = [20, 400, 3000, 64, 9]
     counts = [1, 4, 2, 3, 4]
     b = W.make_ragged_q_batch(batch_lengths=lengths, q_counts=counts, num_qo_heads=16,
@@ -686,6 +743,7 @@ def test_head_scales_ragged_q(lib, cuda):
     o, lse = p.run_head_scales(b.q, b.paged_kv, ks, vs)
     torch.cuda.synchronize()
     assert p.check() == 0
+    assert p.info["num_buckets"] == (4 if buckets == "all" else 1)
     # the heads do not interact: kv head h's rows are the per-tensor oracle
     # with head h's scales
     import dataclasses
