@@ -106,8 +106,6 @@ bool heads_plan() {
   return !(v && std::strcmp(v, "stream") == 0);
 }
 
-// FADECODE_KERNEL=simt keeps every plan on the CUDA-core consumer (for
-// comparisons); by default the tensor-core consumer is used where it applies.
 // Ragged plans in buckets by 8-column tiles (plan_buckets): FADECODE_BUCKETS=0
 // plans a ragged batch on the one kernel its max_q needs (for comparisons);
 // FADECODE_BUCKETS=all gives every tile count present a launch of its own,
@@ -120,6 +118,8 @@ BucketMode bucket_mode() {
   return BucketMode::kDefault;
 }
 
+// FADECODE_KERNEL=simt keeps every plan on the CUDA-core consumer (for
+// comparisons); by default the tensor-core consumer is used where it applies.
 bool tensor_cores_allowed() {
   const char* v = std::getenv("FADECODE_KERNEL");
   return !(v && std::strcmp(v, "simt") == 0);
